@@ -1,0 +1,340 @@
+/*
+ * AirCache oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded fp64 CPU restatement of AirCache's one-shot
+ * post-prefill visual KV-cache compression.  Only the test-suite, the smoke
+ * check and the CPU-baseline leg of the benchmark may load this library; the
+ * product (the CUDA library under lvlm_kv_cache_gb300/) never does, and the two
+ * share no code, header, table or helper.
+ *
+ * Source of every formula: the paper-notes page "AirCache: Activating
+ * Inter-Modal Relevancy KV Cache Compression for Efficient Large
+ * Vision-Language Model Inference" (ICCV 2025), section "Method details":
+ *   - "Key design 1: Elite Observation Window": the prompt layout
+ *     X = Concat(X_v, X_t), the text self-attention Att, the elite set k,
+ *     the cross-modal attention A_vtk and the visual importance I_v;
+ *   - "Key design 2: Layer-wise KV Cache Budget Allocation": strength s_t,
+ *     skewness s_k and the layer budget r_hat = 1/2 (s'_t + s'_k) r;
+ *   - "Loss / training strategy": the one-shot schedule (save every layer,
+ *     then budget all layers, then compress).
+ *
+ * Readings of points the page leaves open (each is listed in the design notes):
+ *   R1  scores are computed per query head and averaged over all H_q heads;
+ *       the elite set is taken on the head-mean softmax row P; query head h
+ *       reads KV head floor(h / (H_q/H_kv)); one visual index set per layer.
+ *   R2  D under the square root is the head dimension.
+ *   R3  A_vtk carries no causal mask.
+ *   R5  sigma in s_k is the sample standard deviation (n-1); sigma == 0
+ *       gives s_k = 0.
+ *   R6  s'_t = s_t / mean_l s_t and s'_k = (s_k - min_l s_k + 1e-6) /
+ *       mean_l(s_k - min_l s_k + 1e-6), per request over its own layers;
+ *       if mean_l s_t == 0 every s'_t is 1.
+ *   R7  keep_l = clamp(floor(r_l * N_v + 1/2), 1, N_v).
+ *   R8  top-k by I_v, ties to the lower index, output in ascending order.
+ *   R9  the elite threshold is inclusive (>=).
+ *   R10 every text token is kept in every layer, after the kept visual rows.
+ *
+ * Element access: tensors are token-major [tokens][heads][D] with explicit
+ * element strides for the token and head axes and D contiguous; the element
+ * type is fp32 or bf16 (decoded here, exactly, by a 16-bit shift).
+ */
+#include "aircache_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------- access */
+
+static double elem(const oracle_view* t, int64_t tok, int64_t head, int64_t i) {
+    int64_t off = tok * t->stride_tok + head * t->stride_head + i;
+    if (t->dtype == ORACLE_F32) {
+        return (double)((const float*)t->base)[off];
+    }
+    uint16_t bits = ((const uint16_t*)t->base)[off];
+    uint32_t word = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &word, sizeof f);
+    return (double)f;
+}
+
+/* q_row . k_row / sqrt(D), both rows read in fp64 (R2: D = head dimension). */
+static double scaled_dot(const oracle_view* q, int64_t q_tok, int64_t q_head,
+                         const oracle_view* k, int64_t k_tok, int64_t k_head, int d) {
+    double s = 0.0;
+    for (int i = 0; i < d; ++i) {
+        s += elem(q, q_tok, q_head, i) * elem(k, k_tok, k_head, i);
+    }
+    return s / sqrt((double)d);
+}
+
+/* ------------------------------------------------------- elite window */
+
+/*
+ * "Key design 1", Att equation and elite set k.
+ * Att = Softmax(Q_t K_t^T / sqrt(D)); only its last row (the last text query
+ * against every text key) is needed.  Per R1 the row is formed per query head
+ * and averaged over heads: P[j] = (1/H_q) sum_h softmax_j(q_h[N_t-1] . k[N_v+j]).
+ * The elite set is {j : P[j] >= alpha * max P} in ascending order (R9).
+ *
+ * q      : text queries of this request, row t = text token t (0..N_t-1).
+ * k      : keys of this request, row c = prompt position c (visual 0..N_v-1,
+ *          then text N_v..N_v+N_t-1) -- the layout X = Concat(X_v, X_t).
+ * p_out  : [n_t] the head-mean row P (may be NULL).
+ * elite  : [n_t] receives the elite positions (text-relative, ascending).
+ * returns N_tk, or -1 on bad arguments.
+ */
+int oracle_elite(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, int d,
+                 int n_v, int n_t, double alpha, double* p_out, int32_t* elite) {
+    if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || n_t <= 0 || d <= 0) return -1;
+    const int g = h_q / h_kv;
+    double* logit = (double*)malloc(sizeof(double) * (size_t)n_t);
+    double* P = (double*)calloc((size_t)n_t, sizeof(double));
+    if (!logit || !P) { free(logit); free(P); return -1; }
+
+    for (int h = 0; h < h_q; ++h) {
+        const int kvh = h / g;
+        double m = -INFINITY;
+        for (int j = 0; j < n_t; ++j) {
+            logit[j] = scaled_dot(q, n_t - 1, h, k, (int64_t)n_v + j, kvh, d);
+            if (logit[j] > m) m = logit[j];
+        }
+        double z = 0.0;
+        for (int j = 0; j < n_t; ++j) z += exp(logit[j] - m);
+        for (int j = 0; j < n_t; ++j) P[j] += exp(logit[j] - m) / z;
+    }
+    double mx = -INFINITY;
+    for (int j = 0; j < n_t; ++j) {
+        P[j] /= (double)h_q;
+        if (P[j] > mx) mx = P[j];
+    }
+    int n_tk = 0;
+    for (int j = 0; j < n_t; ++j) {
+        if (P[j] >= alpha * mx) elite[n_tk++] = j;
+    }
+    if (p_out) memcpy(p_out, P, sizeof(double) * (size_t)n_t);
+    free(logit);
+    free(P);
+    return n_tk;
+}
+
+/* ------------------------------------------------- cross-modal scoring */
+
+/*
+ * "Key design 1", A_vtk and I_v equations.
+ * For each query head h and each elite text row e, a softmax over the keys
+ * {visual 0..N_v-1} U {text N_v+e' : e' in elite} (no mask, R3); then
+ * I_v[i] = 1/(H_q N_tk) sum_h sum_e A_vtk[h, e, i] for i < N_v (R1).
+ *
+ * iv          : [n_v] output.
+ * elite_mass  : [h_q * n_tk] optional output, the softmax mass each row puts on
+ *               the elite text keys (index h * n_tk + e).
+ * returns 0, or -1 on bad arguments.
+ */
+int oracle_score(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, int d,
+                 int n_v, int n_t, const int32_t* elite, int n_tk,
+                 double* iv, double* elite_mass) {
+    if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || n_v <= 0 || n_tk <= 0) return -1;
+    for (int e = 0; e < n_tk; ++e) {
+        if (elite[e] < 0 || elite[e] >= n_t) return -1;
+    }
+    const int g = h_q / h_kv;
+    const int n_keys = n_v + n_tk;
+    double* logit = (double*)malloc(sizeof(double) * (size_t)n_keys);
+    if (!logit) return -1;
+    for (int i = 0; i < n_v; ++i) iv[i] = 0.0;
+
+    for (int h = 0; h < h_q; ++h) {
+        const int kvh = h / g;
+        for (int e = 0; e < n_tk; ++e) {
+            const int64_t q_tok = elite[e];
+            double m = -INFINITY;
+            for (int c = 0; c < n_v; ++c) {
+                logit[c] = scaled_dot(q, q_tok, h, k, c, kvh, d);
+                if (logit[c] > m) m = logit[c];
+            }
+            for (int e2 = 0; e2 < n_tk; ++e2) {
+                logit[n_v + e2] = scaled_dot(q, q_tok, h, k, (int64_t)n_v + elite[e2], kvh, d);
+                if (logit[n_v + e2] > m) m = logit[n_v + e2];
+            }
+            double z = 0.0;
+            for (int c = 0; c < n_keys; ++c) z += exp(logit[c] - m);
+            for (int c = 0; c < n_v; ++c) iv[c] += exp(logit[c] - m) / z;
+            if (elite_mass) {
+                double mass = 0.0;
+                for (int e2 = 0; e2 < n_tk; ++e2) mass += exp(logit[n_v + e2] - m) / z;
+                elite_mass[(int64_t)h * n_tk + e] = mass;
+            }
+        }
+    }
+    const double norm = (double)h_q * (double)n_tk;
+    for (int i = 0; i < n_v; ++i) iv[i] /= norm;
+    free(logit);
+    return 0;
+}
+
+/* ------------------------------------------------ strength and skewness */
+
+/*
+ * "Key design 2", strength s_t = sum_i I_v[i] and skewness
+ * s_k = N_v / ((N_v-1)(N_v-2)) sum_i ((I_v[i] - mu) / sigma)^3, with sigma the
+ * sample standard deviation (R5).  Needs N_v >= 3.
+ * out[0] = s_t, out[1] = s_k, out[2] = mu, out[3] = sigma.
+ */
+int oracle_stats(const double* iv, int n_v, double* out) {
+    if (n_v < 3) return -1;
+    double s_t = 0.0;
+    for (int i = 0; i < n_v; ++i) s_t += iv[i];
+    const double mu = s_t / n_v;
+    double ss = 0.0;
+    for (int i = 0; i < n_v; ++i) ss += (iv[i] - mu) * (iv[i] - mu);
+    const double sigma = sqrt(ss / (n_v - 1));
+    double s_k = 0.0;
+    if (sigma > 0.0) {
+        double cube = 0.0;
+        for (int i = 0; i < n_v; ++i) {
+            const double z = (iv[i] - mu) / sigma;
+            cube += z * z * z;
+        }
+        s_k = (double)n_v / ((double)(n_v - 1) * (double)(n_v - 2)) * cube;
+    }
+    out[0] = s_t;
+    out[1] = s_k;
+    out[2] = mu;
+    out[3] = sigma;
+    return 0;
+}
+
+/* ------------------------------------------------------- layer budget */
+
+/*
+ * "Key design 2", budget r_hat = 1/2 (s'_t + s'_k) r with the cross-layer
+ * normalisation of R6, over the n_layers layers of one request, then the keep
+ * count of R7.
+ * s_t, s_k : [n_layers]; r_l : [n_layers] output (may be NULL);
+ * keep : [n_layers] output.
+ */
+int oracle_budget(const double* s_t, const double* s_k, int n_layers, int n_v, double r,
+                  double* r_l, int32_t* keep) {
+    if (n_layers <= 0 || n_v <= 0) return -1;
+    double mean_st = 0.0, min_sk = INFINITY;
+    for (int l = 0; l < n_layers; ++l) {
+        mean_st += s_t[l];
+        if (s_k[l] < min_sk) min_sk = s_k[l];
+    }
+    mean_st /= n_layers;
+    double mean_u = 0.0;
+    for (int l = 0; l < n_layers; ++l) mean_u += s_k[l] - min_sk + 1e-6;
+    mean_u /= n_layers;
+    for (int l = 0; l < n_layers; ++l) {
+        const double st_n = (mean_st != 0.0) ? s_t[l] / mean_st : 1.0;
+        const double sk_n = (s_k[l] - min_sk + 1e-6) / mean_u;
+        const double rl = 0.5 * (st_n + sk_n) * r;
+        double kf = floor(rl * (double)n_v + 0.5);
+        if (kf < 1.0) kf = 1.0;
+        if (kf > (double)n_v) kf = (double)n_v;
+        keep[l] = (int32_t)kf;
+        if (r_l) r_l[l] = rl;
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------- selection */
+
+/* Sort key for the selection: larger I_v first, then lower index (R8). */
+typedef struct { double v; int32_t i; } scored_index;
+
+static int by_score_then_index(const void* a, const void* b) {
+    const scored_index* x = (const scored_index*)a;
+    const scored_index* y = (const scored_index*)b;
+    if (x->v > y->v) return -1;
+    if (x->v < y->v) return 1;
+    return (x->i > y->i) - (x->i < y->i);
+}
+
+static int ascending_int(const void* a, const void* b) {
+    const int32_t x = *(const int32_t*)a, y = *(const int32_t*)b;
+    return (x > y) - (x < y);
+}
+
+/*
+ * Keep the `keep` visual positions with the largest I_v (R8): order all
+ * positions by (I_v descending, index ascending), take the first `keep`,
+ * return them sorted ascending in idx[0..keep).
+ */
+int oracle_select(const double* iv, int n_v, int keep, int32_t* idx) {
+    if (n_v <= 0 || keep < 0 || keep > n_v) return -1;
+    scored_index* s = (scored_index*)malloc(sizeof(scored_index) * (size_t)n_v);
+    if (!s) return -1;
+    for (int i = 0; i < n_v; ++i) { s[i].v = iv[i]; s[i].i = i; }
+    qsort(s, (size_t)n_v, sizeof(scored_index), by_score_then_index);
+    for (int j = 0; j < keep; ++j) idx[j] = s[j].i;
+    qsort(idx, (size_t)keep, sizeof(int32_t), ascending_int);
+    free(s);
+    return 0;
+}
+
+/* -------------------------------------------------------- compaction */
+
+/*
+ * "Loss / training strategy" step 3 (the compressed cache feeds decoding) and
+ * R10: the compacted rows of one (request, layer) are [K_v[idx]; K_t], i.e. the
+ * kept visual positions in ascending order followed by every text position.
+ * Rows are copied element by element (bit-exact, in the source type) into a
+ * dense [rows][h_kv][d] destination.  Returns the number of rows written.
+ */
+int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t,
+                       const int32_t* idx, int keep, void* dst) {
+    const size_t esize = (src->dtype == ORACLE_F32) ? 4 : 2;
+    unsigned char* out = (unsigned char*)dst;
+    int64_t row = 0;
+    for (int j = 0; j < keep + n_t; ++j) {
+        const int64_t tok = (j < keep) ? idx[j] : (int64_t)n_v + (j - keep);
+        for (int h = 0; h < h_kv; ++h) {
+            const unsigned char* from = (const unsigned char*)src->base +
+                (size_t)(tok * src->stride_tok + h * src->stride_head) * esize;
+            memcpy(out + ((size_t)row * h_kv + h) * d * esize, from, (size_t)d * esize);
+        }
+        ++row;
+    }
+    return row;
+}
+
+/* ------------------------------------------------------ one request */
+
+/*
+ * The one-shot schedule of "Loss / training strategy" for one request over
+ * all of its layers: elite + score + stats for every layer, then one budget
+ * over the layers, then selection per layer.  Compaction is left to
+ * oracle_compact so that callers choose where rows go.
+ *
+ * q[l], k[l] : views of layer l restricted to this request.
+ * iv         : [n_layers * n_v] output; elite: [n_layers * n_t]; n_tk: [n_layers];
+ * stats      : [n_layers * 4]; keep: [n_layers]; idx: [n_layers * n_v].
+ */
+int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int h_q, int h_kv,
+                   int d, int n_v, int n_t, double alpha, double r,
+                   double* iv, int32_t* elite, int32_t* n_tk, double* stats,
+                   int32_t* keep, int32_t* idx) {
+    double* s_t = (double*)malloc(sizeof(double) * (size_t)n_layers);
+    double* s_k = (double*)malloc(sizeof(double) * (size_t)n_layers);
+    if (!s_t || !s_k) { free(s_t); free(s_k); return -1; }
+    int rc = 0;
+    for (int l = 0; l < n_layers && rc == 0; ++l) {
+        int32_t* el = elite + (int64_t)l * n_t;
+        const int ntk = oracle_elite(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, alpha, NULL, el);
+        if (ntk <= 0) { rc = -1; break; }
+        n_tk[l] = ntk;
+        double* ivl = iv + (int64_t)l * n_v;
+        rc = oracle_score(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, el, ntk, ivl, NULL);
+        if (rc == 0) rc = oracle_stats(ivl, n_v, stats + (int64_t)l * 4);
+        if (rc == 0) { s_t[l] = stats[l * 4 + 0]; s_k[l] = stats[l * 4 + 1]; }
+    }
+    if (rc == 0) rc = oracle_budget(s_t, s_k, n_layers, n_v, r, NULL, keep);
+    for (int l = 0; l < n_layers && rc == 0; ++l) {
+        rc = oracle_select(iv + (int64_t)l * n_v, n_v, keep[l], idx + (int64_t)l * n_v);
+    }
+    free(s_t);
+    free(s_k);
+    return rc;
+}

@@ -1,0 +1,45 @@
+/*
+ * AirCache oracle -- TEST INFRASTRUCTURE ONLY (see aircache_oracle.c).
+ * This header belongs to the oracle alone; the CUDA library does not include it.
+ */
+#ifndef AIRCACHE_ORACLE_H
+#define AIRCACHE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+/* A token-major tensor [tokens][heads][D]; strides in elements, D contiguous. */
+typedef struct {
+    const void* base;
+    int32_t dtype;
+    int32_t pad_;
+    int64_t stride_tok;
+    int64_t stride_head;
+} oracle_view;
+
+int oracle_elite(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, int d,
+                 int n_v, int n_t, double alpha, double* p_out, int32_t* elite);
+int oracle_score(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, int d,
+                 int n_v, int n_t, const int32_t* elite, int n_tk,
+                 double* iv, double* elite_mass);
+int oracle_stats(const double* iv, int n_v, double* out);
+int oracle_budget(const double* s_t, const double* s_k, int n_layers, int n_v, double r,
+                  double* r_l, int32_t* keep);
+int oracle_select(const double* iv, int n_v, int keep, int32_t* idx);
+int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t,
+                       const int32_t* idx, int keep, void* dst);
+int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int h_q, int h_kv,
+                   int d, int n_v, int n_t, double alpha, double r,
+                   double* iv, int32_t* elite, int32_t* n_tk, double* stats,
+                   int32_t* keep, int32_t* idx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

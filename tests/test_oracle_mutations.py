@@ -1,0 +1,55 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of the oracle's C source (on the CPU,
+in a temporary directory), builds it, and runs the pin suite against that build
+in a subprocess: the suite has to fail.  The committed oracle is untouched."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "aircache_oracle.c")
+
+MUTATIONS = {
+    "elite reads the wrong query row": ("scaled_dot(q, n_t - 1, h,", "scaled_dot(q, n_t - 2, h,"),
+    "elite averages logits, not softmax rows": ("P[j] += exp(logit[j] - m) / z;", "P[j] += logit[j];"),
+    "elite threshold exclusive": ("if (P[j] >= alpha * mx)", "if (P[j] > alpha * mx)"),
+    "head map h mod h_kv": ("const int kvh = h / g;\n        double m = -INFINITY;",
+                            "const int kvh = h % h_kv;\n        double m = -INFINITY;"),
+    "scale by D instead of sqrt(D)": ("return s / sqrt((double)d);", "return s / (double)d;"),
+    "softmax drops the elite text keys": ("for (int c = 0; c < n_keys; ++c) z +=",
+                                          "for (int c = 0; c < n_v; ++c) z +="),
+    "elite text key index not mapped": ("(int64_t)n_v + elite[e2], kvh, d);", "(int64_t)n_v + e2, kvh, d);"),
+    "score query row not mapped": ("const int64_t q_tok = elite[e];", "const int64_t q_tok = e;"),
+    "I_v not averaged over heads": ("const double norm = (double)h_q * (double)n_tk;",
+                                    "const double norm = (double)n_tk;"),
+    "population sigma": ("sqrt(ss / (n_v - 1))", "sqrt(ss / n_v)"),
+    "skewness prefactor dropped": ("s_k = (double)n_v / ((double)(n_v - 1) * (double)(n_v - 2)) * cube;",
+                                   "s_k = cube;"),
+    "budget skips the min shift": ("mean_u += s_k[l] - min_sk + 1e-6;", "mean_u += s_k[l] + 1e-6;"),
+    "budget uses banker's rounding": ("floor(rl * (double)n_v + 0.5)", "nearbyint(rl * (double)n_v)"),
+    "budget drops the 1/2": ("const double rl = 0.5 * (st_n + sk_n) * r;", "const double rl = (st_n + sk_n) * r;"),
+    "ties go to the higher index": ("return (x->i > y->i) - (x->i < y->i);", "return (x->i < y->i) - (x->i > y->i);"),
+    "selection left in score order": ("    qsort(idx, (size_t)keep, sizeof(int32_t), ascending_int);\n", ""),
+    "text rows shifted by one": ("(int64_t)n_v + (j - keep);", "(int64_t)n_v + (j - keep) - (j > keep);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(name, tmp_path):
+    before, after = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(before) == 1, f"mutation anchor not unique/found: {name}"
+    mutated = tmp_path / "aircache_oracle.c"
+    mutated.write_text(src.replace(before, after))
+    (tmp_path / "aircache_oracle.h").write_text(open(os.path.join(ROOT, "oracle", "aircache_oracle.h")).read())
+    so = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                           "-o", str(so), str(mutated), "-lm"])
+    env = dict(os.environ, AIRCACHE_ORACLE_LIB=str(so))
+    res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                          os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                         cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert res.returncode != 0, f"pins did not catch: {name}\n{res.stdout[-2000:]}"
