@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Benchmark of the fused AirCache compression (one-shot visual KV compression
+after prefill) on GB300.
+
+One step = one aircache_compress call over the whole workload (elite window,
+cross-modal scores, layer budgets, top-k, gather-compact), inputs resident in
+HBM.  Default workload: the 7B LVLM-shaped batch (1 request, 28 layers,
+H_q=28, H_kv=4, D=128, N_v=7290, N_t=128, bf16, alpha=0.9, r=0.10).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank compresses its own
+copy of the workload (requests are independent: weak scaling, no collective on
+the data path); the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "visual KV tokens compressed/sec on 1 GB300; fused-compress HBM GB/s vs 8 TB/s"
+UNIT = "visual KV tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+DESCRIPTIONS = {
+    "7b": "7B LVLM-shaped (Qwen2-7B-like GQA): 1 request, L=28, H_q=28, H_kv=4, D=128, "
+          "N_v=7290 visual + N_t=128 text, bf16, 10% heavy visual keys, alpha=0.9, r=0.10",
+    "tiny": "tiny: 1 request, L=2, H_q=H_kv=4, D=64, N_v=64, N_t=16, fp32, alpha=0.9, r=0.25",
+    "llama_mha": "Llama-7B MHA-shaped batch: 8 requests, L=32, H=32, D=128, N_v=2880, N_t=512, bf16, r=0.10",
+    "video_r01": "video-shaped: 4 requests, L=28, H_q=28, H_kv=4, D=128, N_v=12544, N_t=256, bf16, r=0.01",
+    "video_r10": "video-shaped: 4 requests, L=28, H_q=28, H_kv=4, D=128, N_v=12544, N_t=256, bf16, r=0.10",
+    "ragged": "ragged serving batch: 32 requests, L=28, H_q=28, H_kv=4, D=128, N_v~U[576,9000], "
+              "N_t~U[32,1024], bf16, r=0.05",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="7b")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=1.5, help="untimed back-to-back load before timing")
+    ap.add_argument("--cpu-sample-s", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "lvlm_kv_cache_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config, kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(config, {}).get(kernel)
+    if not e or e.get("sources") != kernel_sources_hash():
+        return None
+    return float(e["dram_bytes_per_launch_full"])
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    if int(parts[0]) != self.gpu_index and self.gpu_index is not None:
+                        continue
+                    rows.append(parts)
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        mx = max(float(r[2]) for r in rows)
+        loaded = [s for s in sm if s > 0.5 * mx] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows)}
+
+
+def unit_lengths(spec):
+    return [(spec.n_visual[b], spec.n_text[b]) for b in range(spec.B)]
+
+
+def algorithmic_bytes(spec, n_tk, keep, esize):
+    """Per-kernel algorithmic bytes of one compression (each input read once,
+    each output written once) and the whole-path total of the per-(request,
+    layer) formula 2*H_kv*D*(N_v+N_t) + 2*H_q*D*(1+N_tk) + 8*H_kv*D*(keep+N_t)
+    (bf16; esize-scaled) + the I_v workspace."""
+    row = spec.H_kv * spec.D * esize
+    qrow = spec.H_q * spec.D * esize
+    k = {"elite_window": 0, "score_pass1": 0, "score_pass2": 0, "stats_budget": 0, "select_topk": 0,
+         "gather_compact": 0}
+    path = 0
+    for l in range(spec.L):
+        for b, (nv, nt) in enumerate(unit_lengths(spec)):
+            u = l * spec.B + b
+            t, kp = int(n_tk[u]), int(keep[u])
+            k["elite_window"] += nt * row + qrow + 4 * t
+            k["score_pass1"] += (nv + t) * row + t * qrow
+            k["score_pass2"] += nv * row + t * qrow + 4 * nv
+            k["stats_budget"] += 4 * nv + 4
+            k["select_topk"] += 4 * nv + 4 * kp
+            k["gather_compact"] += 2 * 2 * (kp + nt) * row + 4 * kp
+            path += (nv + nt) * row + (1 + t) * qrow + 2 * 2 * (kp + nt) * row + 4 * nv * 3 + 8 * kp
+    return k, path
+
+
+def oracle_sample(wl, budget_s, device_for_copy=None):
+    """Time the oracle (single thread) on whole requests of the workload until
+    budget_s is spent (at least one request).  Returns (tokens, seconds, requests)."""
+    from lvlm_kv_cache_gb300 import workloads as W
+    from oracle import oracle as O
+
+    spec = wl.spec
+    cu_s, cu_v, cu_t = W.offsets(spec)
+    tokens, elapsed, done = 0, 0.0, 0
+    for b in range(spec.B):
+        s0, s1 = cu_s[b], cu_s[b + 1]
+        t0, t1 = cu_t[b], cu_t[b + 1]
+        nv, nt = spec.n_visual[b], spec.n_text[b]
+        q = W.host_bits(wl.q[:, t0:t1])
+        k = W.host_bits(wl.k[:, s0:s1])
+        v = W.host_bits(wl.v[:, s0:s1])
+        t = time.perf_counter()
+        res = O.request([q[l] for l in range(spec.L)], [k[l] for l in range(spec.L)], nv, spec.alpha, spec.r)
+        for l in range(spec.L):
+            O.compact(k[l], nv, nt, res["idx"][l])
+            O.compact(v[l], nv, nt, res["idx"][l])
+        elapsed += time.perf_counter() - t
+        tokens += nv * spec.L
+        done += 1
+        if elapsed >= budget_s:
+            break
+    return tokens, elapsed, done
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, rank, world):
+    """The oracle, as it stands, on the host cores: each step is a bounded
+    sample (whole requests) of the same workload."""
+    if rank != 0:
+        return
+    from lvlm_kv_cache_gb300 import workloads as W
+
+    spec = W.spec(args.config)
+    wl = W.generate(spec, seed=0, device="cpu")
+    for _ in range(args.warmup):
+        oracle_sample(wl, 0.0)
+    tok, secs = 0, 0.0
+    for _ in range(args.steps):
+        t, s, _ = oracle_sample(wl, 0.0)
+        tok += t
+        secs += s
+    value = tok / secs
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS.get(args.config, args.config), "name": args.config,
+                   "sample": "one request (all layers) per step"},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "request 0 of the workload, all layers, per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+
+    from lvlm_kv_cache_gb300 import aircache as A
+    from lvlm_kv_cache_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = W.make(args.config, seed=rank, device=dev)
+    spec = wl.spec
+    esize = 2 if spec.dtype == torch.bfloat16 else 4
+    prob = A.Problem(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.cu_visual, max(spec.n_visual), max(spec.n_text),
+                     spec.alpha, spec.r, total_tokens=wl.total_tokens, total_visual=wl.total_visual)
+    ws = prob.new_workspace()
+    out = A.alloc_outputs(prob)
+    L, B, TV = prob.L, prob.B, prob.total_visual
+    # elite sizes (for the byte accounting) from the staged scorer, outside timing
+    iv_s = torch.empty((L, TV), dtype=torch.float32, device=dev)
+    el_s = torch.empty((L * B, prob.max_text), dtype=torch.int32, device=dev)
+    ntk_s = torch.empty(L * B, dtype=torch.int32, device=dev)
+    A.aircache_score(prob, ws, iv_s, el_s, ntk_s)
+    assert A.aircache_get_error(ws) == 0
+
+    def step():
+        A.aircache_compress(prob, ws, out["out_k"], out["out_v"], out["out_offsets"], out["keep"],
+                            out["idx"], out["iv"])
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    st = A.aircache_get_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error {st}: {A.status_string(st)}")
+    n_tk = ntk_s.cpu().numpy()
+    keep = out["keep"].cpu().numpy()
+    kbytes, path_bytes = algorithmic_bytes(spec, n_tk, keep, esize)
+
+    vis_idx = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    try:
+        gpu_index = int(vis_idx[local]) if vis_idx != [""] else local
+    except ValueError:
+        gpu_index = None
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak_s:
+        for _ in range(20):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+
+    # ---- timed region: K steps, L2 flushed before each (outside the events)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record()
+        step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    st = A.aircache_get_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error {st}: {A.status_string(st)}")
+
+    units = spec.L * sum(spec.n_visual)  # visual KV rows (token x layer) per step per rank
+    ms_per_step = total_ms / args.steps
+    value = world * units * args.steps / (total_ms / 1e3)
+
+    # ---- per-kernel durations on the launching stream
+    nk = prob.launches()
+    names = A.kernel_names(nk)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    for row in ev:  # torch creates the CUDA event on first record
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        A.aircache_compress_profile(prob, ws, out["out_k"], out["out_v"], out["out_offsets"], out["keep"],
+                                    ev[i], out["idx"], out["iv"])
+    torch.cuda.synchronize()
+    per_kernel = {n: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+                  for j, n in enumerate(names)}
+    peak, peak_kind = load_peaks()
+    kernels = []
+    for n in names:
+        ms = per_kernel[n]
+        gbs = kbytes[n] / (ms * 1e-3) / 1e9 if ms > 0 else None
+        kernels.append({"name": n, "ms": ms, "algorithmic_bytes": kbytes[n], "gbs": gbs,
+                        "frac": gbs / peak if gbs else None})
+    dom = max(kernels, key=lambda k: k["ms"])
+    roof = {"bound": "hbm", "kernel": dom["name"], "achieved": dom["gbs"], "peak": peak, "unit": "GB/s",
+            "frac": dom["frac"], "peak_kind": peak_kind,
+            "traffic": recorded_traffic(args.config, dom["name"])}
+    path_gbs = path_bytes / (ms_per_step * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if esize == 2 else "f32",
+        "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS.get(args.config, args.config), "name": args.config,
+                   "requests_per_rank": spec.B, "layers": spec.L, "seed": "rank",
+                   "l2": "flushed before every timed step (256 MB write outside the events)"},
+        "requests_per_s": world * spec.B * args.steps / (total_ms / 1e3),
+        "visual_tokens_per_s": world * sum(spec.n_visual) * args.steps / (total_ms / 1e3),
+        "fused_compress": {"algorithmic_bytes": path_bytes, "gbs": path_gbs,
+                           "frac_of_8tbs": path_gbs / 8000.0, "frac_of_measured": path_gbs / peak},
+        "roofline": roof,
+        "kernels": kernels,
+        "gpu_launches": nk * args.steps,
+        "clocks": clocks,
+    }
+
+    # ---- end to end through the public API, host buffers, copies timed
+    if not args.no_e2e:
+        hq = wl.q.cpu().pin_memory()
+        hk = wl.k.cpu().pin_memory()
+        hv = wl.v.cpu().pin_memory()
+        hcs = wl.cu_seqlens.cpu().pin_memory()
+        hcv = wl.cu_visual.cpu().pin_memory()
+        ok_h = torch.empty(out["out_k"].shape, dtype=out["out_k"].dtype).pin_memory()
+        ov_h = torch.empty_like(ok_h).pin_memory()
+        of_h = torch.empty(out["out_offsets"].shape, dtype=torch.int64).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hcs, hcv))
+        d2h = sum(t.numel() * t.element_size() for t in (ok_h, ov_h, of_h))
+
+        def e2e_step():
+            wl.q.copy_(hq, non_blocking=True)
+            wl.k.copy_(hk, non_blocking=True)
+            wl.v.copy_(hv, non_blocking=True)
+            wl.cu_seqlens.copy_(hcs, non_blocking=True)
+            wl.cu_visual.copy_(hcv, non_blocking=True)
+            step()
+            ok_h.copy_(out["out_k"], non_blocking=True)
+            ov_h.copy_(out["out_v"], non_blocking=True)
+            of_h.copy_(out["out_offsets"], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 20))
+        s_ev = torch.cuda.Event(enable_timing=True)
+        e_ev = torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        s_ev.record()
+        for _ in range(n_e2e):
+            e2e_step()
+        e_ev.record()
+        torch.cuda.synchronize()
+        e2e_ms = s_ev.elapsed_time(e_ev)
+        if dist:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        assert int(of_h[-1]) == int(out["out_offsets"][-1])
+        line["e2e"] = {"value": world * units * n_e2e / (e2e_ms / 1e3), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+                       "ms_per_step": e2e_ms / n_e2e}
+
+    # ---- CPU baseline: the oracle on the host cores, rank 0 at N=1 only
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok, secs, nreq = oracle_sample(wl, args.cpu_sample_s)
+        line["cpu_baseline"] = {"value": tok / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{nreq} whole request(s) x {spec.L} layers "
+                                          f"({tok} visual KV rows) in {secs:.2f} s, single thread"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * aircache.h -- C ABI of the GB300 (sm_103a) AirCache compressor.
+ *
+ * AirCache compresses the visual part of a vision-language decoder's KV cache
+ * once, right after prefill (paper notes "AirCache: Activating Inter-Modal
+ * Relevancy KV Cache Compression for Efficient Large Vision-Language Model
+ * Inference", ICCV 2025; section "Method details").  For every layer:
+ *   1. elite observation window ("Key design 1", equations Att and k): the
+ *      softmax row of the last text query over the text keys, averaged over
+ *      the query heads, keeps the text positions j with P[j] >= alpha * max P;
+ *   2. cross-modal scoring ("Key design 1", equations A_vtk and I_v): the elite
+ *      text queries attend over [visual keys; elite text keys]; the visual
+ *      columns are averaged over the elite rows and the query heads into I_v;
+ *   3. layer budget ("Key design 2"): strength s_t = sum I_v and sample
+ *      skewness s_k of I_v, normalised across the request's layers, give
+ *      r_l = 1/2 (s'_t + s'_k) r and keep_l = clamp(floor(r_l N_v + 1/2), 1, N_v);
+ *   4. selection and compaction ("Loss / training strategy", one-shot steps):
+ *      the keep_l visual positions with the largest I_v (ties to the lower
+ *      position), then every text position, gathered into a dense cache.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every data pointer is caller-owned DEVICE memory unless stated otherwise;
+ *   the library allocates nothing, frees nothing and never synchronises, except
+ *   aircache_get_error.  `stream` is a cudaStream_t (NULL = legacy default).
+ * - Argument errors are detected on the host and returned before anything is
+ *   enqueued.  Launch failures return AIRCACHE_ERR_CUDA.  Errors that only the
+ *   GPU can see (inconsistent cu_seqlens/cu_visual contents, an elite set larger
+ *   than max_elite, an output arena that is too small, a bounded wait that
+ *   expired) are written to an error word in the workspace; read it with
+ *   aircache_get_error.  Each entry point clears that word when it starts, so
+ *   it reports the most recent call on that workspace.
+ * - Calls are stateless.  Two calls may run concurrently only with distinct
+ *   workspaces and outputs.
+ * - Layout (varlen, token-major, like FlashAttention's varlen convention):
+ *   request b owns prompt positions cu_seqlens[b] .. cu_seqlens[b+1]-1 of every
+ *   layer's K and V; its first N_v[b] = cu_visual[b+1]-cu_visual[b] positions
+ *   are visual, the remaining N_t[b] are text (visual first, X = Concat(X_v, X_t)).
+ *   Its text queries are rows cu_seqlens[b]-cu_visual[b] .. +N_t[b]-1 of the
+ *   layer's Q_text.  K/V rows are [h_kv][head_dim], Q rows [h_q][head_dim], with
+ *   element strides per token and per head; head_dim is contiguous.
+ * - Inputs are post-RoPE.  Compaction keeps the values bit-exact; a decoder
+ *   continuing from the compressed cache keeps the original positions
+ *   (N_v + N_t onwards), not the compacted length.
+ * - The per-layer visual index set is shared by all KV heads of the layer.
+ */
+#ifndef AIRCACHE_H
+#define AIRCACHE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define AIRCACHE_API __attribute__((visibility("default")))
+#else
+#define AIRCACHE_API
+#endif
+
+#define AIRCACHE_MAX_LAYERS 256
+#define AIRCACHE_MAX_TEXT 8192
+
+typedef enum {
+    AIRCACHE_OK = 0,
+    AIRCACHE_ERR_INVALID_ARG = -1,   /* host: a bad pointer, size, stride or parameter */
+    AIRCACHE_ERR_UNSUPPORTED = -2,   /* host: a valid problem this build does not handle */
+    AIRCACHE_ERR_WORKSPACE = -3,     /* host: ws_bytes < aircache_workspace_size() */
+    AIRCACHE_ERR_CUDA = -4,          /* a CUDA launch or memset failed */
+    AIRCACHE_ERR_DEVICE_TIMEOUT = -5,  /* device: a bounded wait gave up */
+    AIRCACHE_ERR_DEVICE_BOUNDS = -6,   /* device: cu_seqlens / cu_visual contents inconsistent */
+    AIRCACHE_ERR_ELITE_OVERFLOW = -7,  /* device: an elite set larger than max_elite */
+    AIRCACHE_ERR_CAPACITY = -8         /* device: output arena smaller than the compacted rows */
+} aircache_status;
+
+typedef enum { AIRCACHE_F32 = 0, AIRCACHE_BF16 = 1 } aircache_dtype;
+
+/*
+ * One compression problem: B requests, L layers.  All fields are read on the
+ * host; the pointer fields marked "device" are read only by the GPU.
+ */
+typedef struct aircache_problem {
+    int32_t num_layers;    /* L, 1..AIRCACHE_MAX_LAYERS */
+    int32_t num_requests;  /* B >= 1 */
+    int32_t h_q;           /* query heads; h_q % h_kv == 0 (query head h reads KV head h / (h_q/h_kv)) */
+    int32_t h_kv;          /* key/value heads */
+    int32_t head_dim;      /* D: 64 or 128 */
+    int32_t dtype;         /* aircache_dtype of q_text, k and v */
+    int32_t max_visual;    /* >= every N_v[b]; every N_v[b] must be >= 3 (skewness) */
+    int32_t max_text;      /* >= every N_t[b], 1..AIRCACHE_MAX_TEXT; every N_t[b] >= 1 */
+    int32_t max_elite;     /* cap on N_tk that the workspace is sized for; 0 means max_text */
+    int32_t reserved0;     /* must be 0 */
+    int64_t total_tokens;  /* == cu_seqlens[B] */
+    int64_t total_visual;  /* == cu_visual[B] */
+    const int32_t* cu_seqlens;  /* device [B+1], non-decreasing, cu_seqlens[0] == 0 */
+    const int32_t* cu_visual;   /* device [B+1], non-decreasing, cu_visual[0] == 0 */
+    const void* const* q_text;  /* HOST array [L] of device pointers: [total_tokens - total_visual] text rows */
+    const void* const* k;       /* HOST array [L] of device pointers: [total_tokens] rows */
+    const void* const* v;       /* HOST array [L] of device pointers: [total_tokens] rows */
+    int64_t q_stride_tok;   /* elements between consecutive Q_text rows */
+    int64_t q_stride_head;  /* elements between consecutive query heads */
+    int64_t kv_stride_tok;  /* elements between consecutive K/V rows (same for K and V) */
+    int64_t kv_stride_head; /* elements between consecutive KV heads */
+    double alpha;           /* elite threshold, [0, 1] (the notes use 0.9) */
+    double r;               /* mean visual retention ratio, (0, 1] */
+} aircache_problem;
+
+/*
+ * Bytes of device workspace a call on `p` needs (every entry point takes the
+ * same workspace).  Returns 0 if `p` is invalid.  Host only; no CUDA call.
+ * The workspace must be 256-byte aligned.
+ */
+AIRCACHE_API size_t aircache_workspace_size(const aircache_problem* p);
+
+/*
+ * Upper bound on the rows the compacted cache of `p` can hold, summed over all
+ * layers and requests:  L * total_text + ceil(r * L * total_visual) + B * (2L + 1),
+ * capped at L * total_tokens.  It holds because the budgets of a request
+ * average to r over its layers and rounding/clamping add at most 3/2 per layer.
+ * Returns -1 if `p` is invalid.  Host only; no CUDA call.
+ */
+AIRCACHE_API int64_t aircache_compress_bound(const aircache_problem* p);
+
+/*
+ * Steps 1-2: elite window and cross-modal scores of every (request, layer).
+ *   iv    [L][total_visual] fp32: I_v of request b, layer l at
+ *         iv[l * total_visual + cu_visual[b] + i], i < N_v[b].
+ *   elite [L][B][max_text] int32: the first n_tk[l*B+b] entries of row (l, b)
+ *         are that request's elite text positions (text-relative, ascending).
+ *   n_tk  [L][B] int32: elite-set sizes N_tk (>= 1).
+ */
+AIRCACHE_API int aircache_score(const aircache_problem* p, void* ws, size_t ws_bytes,
+                   float* iv, int32_t* elite, int32_t* n_tk, void* stream);
+
+/*
+ * Step 3: strength, skewness and keep counts from I_v (as written by
+ * aircache_score).
+ *   stats [L][B][2] fp64: (s_t, s_k) per (layer, request); may be NULL.
+ *   keep  [L][B] int32: kept visual positions per (layer, request).
+ */
+AIRCACHE_API int aircache_budget(const aircache_problem* p, const float* iv, void* ws, size_t ws_bytes,
+                    double* stats, int32_t* keep, void* stream);
+
+/*
+ * Step 4a: top-keep selection.  For each (l, b) writes the keep[l*B+b] visual
+ * positions (request-relative, ascending) with the largest I_v, ties to the
+ * lower position, to idx[l * total_visual + cu_visual[b] + j].  Entries past
+ * the keep count are left untouched.
+ *   idx [L][total_visual] int32.
+ */
+AIRCACHE_API int aircache_select(const aircache_problem* p, const float* iv, const int32_t* keep,
+                    void* ws, size_t ws_bytes, int32_t* idx, void* stream);
+
+/*
+ * Step 4b: compaction.  Writes, for each layer l and request b in that order,
+ * the rows [K_v[idx]; K_t] (keep + N_t rows) of that (l, b), and the same for V,
+ * into the dense arenas out_k / out_v ([rows][h_kv][head_dim], same dtype as
+ * the input), bit-exact.  out_offsets [L*B + 1] int64 receives the first row of
+ * each (l, b): rows of (l, b) are out_offsets[l*B+b] .. out_offsets[l*B+b+1]-1.
+ * out_rows_capacity is the number of rows out_k and out_v can hold
+ * (aircache_compress_bound rows always suffice).
+ */
+AIRCACHE_API int aircache_compact(const aircache_problem* p, const int32_t* idx, const int32_t* keep,
+                     void* ws, size_t ws_bytes, void* out_k, void* out_v,
+                     int64_t* out_offsets, int64_t out_rows_capacity, void* stream);
+
+/*
+ * Steps 1-4 in one call on one stream (the one-shot schedule: every layer is
+ * scored, then every budget is set, then every layer is compacted).
+ * keep [L][B] is required; iv [L][total_visual] and idx [L][total_visual] are
+ * optional (NULL keeps them inside the workspace).  Outputs as above.
+ */
+AIRCACHE_API int aircache_compress(const aircache_problem* p, void* ws, size_t ws_bytes,
+                      void* out_k, void* out_v, int64_t* out_offsets, int64_t out_rows_capacity,
+                      int32_t* keep, int32_t* idx, float* iv, void* stream);
+
+/*
+ * Waits for `stream`, then reads the device error word of `ws` into *status
+ * (AIRCACHE_OK or a device error code).  The only entry point that blocks.
+ */
+AIRCACHE_API int aircache_get_error(const void* ws, void* stream, int32_t* status);
+
+/* Static description of a status code. */
+AIRCACHE_API const char* aircache_status_string(int status);
+
+/* Number of kernels one aircache_compress call launches (for launch accounting). */
+AIRCACHE_API int aircache_compress_launches(const aircache_problem* p);
+
+/*
+ * aircache_compress with timing marks, for measurement: `events` is a host
+ * array of n_events == aircache_compress_launches(p) + 1 cudaEvent_t handles
+ * created by the caller; events[0] is recorded on `stream` before the first
+ * kernel and events[i] right after kernel i, so the elapsed time between
+ * consecutive events is that kernel's duration on the launching stream.
+ * Results are identical to aircache_compress.
+ */
+AIRCACHE_API int aircache_compress_profile(const aircache_problem* p, void* ws, size_t ws_bytes,
+                                           void* out_k, void* out_v, int64_t* out_offsets,
+                                           int64_t out_rows_capacity, int32_t* keep, int32_t* idx,
+                                           float* iv, void* const* events, int n_events, void* stream);
+
+/* Name of kernel i (0-based, launch order) of aircache_compress, or NULL. */
+AIRCACHE_API const char* aircache_kernel_name(int i);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AIRCACHE_H */

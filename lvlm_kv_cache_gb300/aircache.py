@@ -1,0 +1,322 @@
+"""Thin ctypes binding of the AirCache C ABI (include/aircache.h).
+
+Argument marshalling only: every step of the compression runs in the CUDA
+library ``libaircache.so`` built from ``csrc/``.  If that library is missing the
+binding raises; there is no fallback path.
+
+Tensors are torch CUDA tensors; the functions take the same arguments as the C
+entry points (device buffers are tensors, the stream is a torch stream or None
+for the current one) and raise ``AirCacheError`` on a non-zero status.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libaircache.so")
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_WORKSPACE = -3
+ERR_CUDA = -4
+ERR_DEVICE_TIMEOUT = -5
+ERR_DEVICE_BOUNDS = -6
+ERR_ELITE_OVERFLOW = -7
+ERR_CAPACITY = -8
+
+F32, BF16 = 0, 1
+MAX_LAYERS = 256
+
+
+class AirCacheError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({status_string(status)})")
+
+
+class ProblemStruct(ctypes.Structure):
+    _fields_ = [
+        ("num_layers", ctypes.c_int32),
+        ("num_requests", ctypes.c_int32),
+        ("h_q", ctypes.c_int32),
+        ("h_kv", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("dtype", ctypes.c_int32),
+        ("max_visual", ctypes.c_int32),
+        ("max_text", ctypes.c_int32),
+        ("max_elite", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("total_tokens", ctypes.c_int64),
+        ("total_visual", ctypes.c_int64),
+        ("cu_seqlens", ctypes.c_void_p),
+        ("cu_visual", ctypes.c_void_p),
+        ("q_text", ctypes.POINTER(ctypes.c_void_p)),
+        ("k", ctypes.POINTER(ctypes.c_void_p)),
+        ("v", ctypes.POINTER(ctypes.c_void_p)),
+        ("q_stride_tok", ctypes.c_int64),
+        ("q_stride_head", ctypes.c_int64),
+        ("kv_stride_tok", ctypes.c_int64),
+        ("kv_stride_head", ctypes.c_int64),
+        ("alpha", ctypes.c_double),
+        ("r", ctypes.c_double),
+    ]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded CUDA library (raises if it was not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing; build it with `python -m lvlm_kv_cache_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER(ProblemStruct)
+        vp, sz, i64, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64, ctypes.c_int
+        L.aircache_workspace_size.argtypes = [P]
+        L.aircache_workspace_size.restype = sz
+        L.aircache_compress_bound.argtypes = [P]
+        L.aircache_compress_bound.restype = i64
+        L.aircache_score.argtypes = [P, vp, sz, vp, vp, vp, vp]
+        L.aircache_score.restype = i32
+        L.aircache_budget.argtypes = [P, vp, vp, sz, vp, vp, vp]
+        L.aircache_budget.restype = i32
+        L.aircache_select.argtypes = [P, vp, vp, vp, sz, vp, vp]
+        L.aircache_select.restype = i32
+        L.aircache_compact.argtypes = [P, vp, vp, vp, sz, vp, vp, vp, i64, vp]
+        L.aircache_compact.restype = i32
+        L.aircache_compress.argtypes = [P, vp, sz, vp, vp, vp, i64, vp, vp, vp, vp]
+        L.aircache_compress.restype = i32
+        L.aircache_get_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
+        L.aircache_get_error.restype = i32
+        L.aircache_status_string.argtypes = [i32]
+        L.aircache_status_string.restype = ctypes.c_char_p
+        L.aircache_compress_launches.argtypes = [P]
+        L.aircache_compress_launches.restype = i32
+        L.aircache_compress_profile.argtypes = [P, vp, sz, vp, vp, vp, i64, vp, vp, vp,
+                                                ctypes.POINTER(ctypes.c_void_p), i32, vp]
+        L.aircache_compress_profile.restype = i32
+        L.aircache_kernel_name.argtypes = [i32]
+        L.aircache_kernel_name.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().aircache_status_string(int(status)).decode()
+    except ImportError:
+        return "library not loaded"
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise AirCacheError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Problem:
+    """A compression problem over torch tensors (kept alive by this object).
+
+    q, k, v: either stacked tensors [L, T, H, D] or lists of per-layer [T, H, D]
+    tensors (same strides for every layer); q holds the text rows only.
+    cu_seqlens, cu_visual: int32 device tensors [B+1].
+    max_visual, max_text: host maxima over the requests.
+    """
+
+    def __init__(self, q, k, v, cu_seqlens, cu_visual, max_visual, max_text, alpha=0.9, r=0.1,
+                 max_elite=0, total_tokens=None, total_visual=None):
+        qs = list(q.unbind(0)) if torch.is_tensor(q) else list(q)
+        ks = list(k.unbind(0)) if torch.is_tensor(k) else list(k)
+        vs = list(v.unbind(0)) if torch.is_tensor(v) else list(v)
+        L = len(qs)
+        if not (len(ks) == len(vs) == L) or L < 1 or L > MAX_LAYERS:
+            raise ValueError("q, k, v must have the same number of layers (1..256)")
+        dt = qs[0].dtype
+        if dt not in (torch.float32, torch.bfloat16) or any(t.dtype != dt for t in qs + ks + vs):
+            raise TypeError("q, k, v must all be float32 or all bfloat16")
+        self.dtype = dt
+        self.layers = (qs, ks, vs)  # keep alive
+        B = cu_seqlens.numel() - 1
+        T = int(total_tokens) if total_tokens is not None else int(ks[0].shape[0])
+        TV = int(total_visual) if total_visual is not None else None
+        if TV is None:
+            TV = int(cu_visual[-1].item())
+        self.B, self.L = B, L
+        self.h_q, self.h_kv, self.d = int(qs[0].shape[1]), int(ks[0].shape[1]), int(ks[0].shape[2])
+        self.total_tokens, self.total_visual = T, TV
+        self.cu_seqlens, self.cu_visual = cu_seqlens, cu_visual
+        arr = ctypes.c_void_p * L
+        self._q = arr(*[t.data_ptr() for t in qs])
+        self._k = arr(*[t.data_ptr() for t in ks])
+        self._v = arr(*[t.data_ptr() for t in vs])
+        self.c = ProblemStruct(
+            num_layers=L, num_requests=B, h_q=self.h_q, h_kv=self.h_kv, head_dim=self.d,
+            dtype=BF16 if dt == torch.bfloat16 else F32,
+            max_visual=int(max_visual), max_text=int(max_text), max_elite=int(max_elite), reserved0=0,
+            total_tokens=T, total_visual=TV,
+            cu_seqlens=cu_seqlens.data_ptr(), cu_visual=cu_visual.data_ptr(),
+            q_text=ctypes.cast(self._q, ctypes.POINTER(ctypes.c_void_p)),
+            k=ctypes.cast(self._k, ctypes.POINTER(ctypes.c_void_p)),
+            v=ctypes.cast(self._v, ctypes.POINTER(ctypes.c_void_p)),
+            q_stride_tok=qs[0].stride(0), q_stride_head=qs[0].stride(1),
+            kv_stride_tok=ks[0].stride(0), kv_stride_head=ks[0].stride(1),
+            alpha=float(alpha), r=float(r),
+        )
+        for t in ks + vs + qs:
+            if t.stride(2) != 1:
+                raise ValueError("head_dim must be contiguous")
+        if any(t.stride() != ks[0].stride() for t in ks + vs) or any(t.stride() != qs[0].stride() for t in qs):
+            raise ValueError("every layer must share the same strides")
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+    def workspace_size(self) -> int:
+        n = lib().aircache_workspace_size(self.ref)
+        if n == 0:
+            raise AirCacheError(ERR_INVALID_ARG, "aircache_workspace_size")
+        return int(n)
+
+    def compress_bound(self) -> int:
+        n = lib().aircache_compress_bound(self.ref)
+        if n < 0:
+            raise AirCacheError(ERR_INVALID_ARG, "aircache_compress_bound")
+        return int(n)
+
+    def launches(self) -> int:
+        return int(lib().aircache_compress_launches(self.ref))
+
+    @property
+    def max_text(self):
+        return self.c.max_text
+
+    def new_workspace(self, device=None) -> torch.Tensor:
+        """A 256-byte-aligned device workspace (torch allocations are 512-B aligned)."""
+        dev = device or self.layers[1][0].device
+        return torch.empty(self.workspace_size(), dtype=torch.uint8, device=dev)
+
+
+# ------------------------------------------------------------------ entry points
+
+def aircache_score(prob: Problem, ws, iv, elite, n_tk, stream=None):
+    _check(lib().aircache_score(prob.ref, _ptr(ws), ws.numel(), _ptr(iv), _ptr(elite), _ptr(n_tk),
+                                _stream(stream)), "aircache_score")
+
+
+def aircache_budget(prob: Problem, iv, ws, stats, keep, stream=None):
+    _check(lib().aircache_budget(prob.ref, _ptr(iv), _ptr(ws), ws.numel(), _ptr(stats), _ptr(keep),
+                                 _stream(stream)), "aircache_budget")
+
+
+def aircache_select(prob: Problem, iv, keep, ws, idx, stream=None):
+    _check(lib().aircache_select(prob.ref, _ptr(iv), _ptr(keep), _ptr(ws), ws.numel(), _ptr(idx),
+                                 _stream(stream)), "aircache_select")
+
+
+def aircache_compact(prob: Problem, idx, keep, ws, out_k, out_v, out_offsets, stream=None):
+    cap = out_k.shape[0]
+    _check(lib().aircache_compact(prob.ref, _ptr(idx), _ptr(keep), _ptr(ws), ws.numel(), _ptr(out_k),
+                                  _ptr(out_v), _ptr(out_offsets), cap, _stream(stream)),
+           "aircache_compact")
+
+
+def aircache_compress(prob: Problem, ws, out_k, out_v, out_offsets, keep, idx=None, iv=None, stream=None):
+    cap = out_k.shape[0]
+    _check(lib().aircache_compress(prob.ref, _ptr(ws), ws.numel(), _ptr(out_k), _ptr(out_v),
+                                   _ptr(out_offsets), cap, _ptr(keep), _ptr(idx), _ptr(iv),
+                                   _stream(stream)), "aircache_compress")
+
+
+def aircache_compress_profile(prob: Problem, ws, out_k, out_v, out_offsets, keep, events, idx=None,
+                              iv=None, stream=None):
+    """aircache_compress recording torch.cuda.Event objects around each kernel
+    (len(events) == prob.launches() + 1)."""
+    cap = out_k.shape[0]
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(lib().aircache_compress_profile(prob.ref, _ptr(ws), ws.numel(), _ptr(out_k), _ptr(out_v),
+                                           _ptr(out_offsets), cap, _ptr(keep), _ptr(idx), _ptr(iv),
+                                           arr, len(events), _stream(stream)),
+           "aircache_compress_profile")
+
+
+def kernel_names(n: int):
+    return [lib().aircache_kernel_name(i).decode() for i in range(n)]
+
+
+def aircache_get_error(ws, stream=None) -> int:
+    st = ctypes.c_int32(0)
+    _check(lib().aircache_get_error(_ptr(ws), _stream(stream), ctypes.byref(st)), "aircache_get_error")
+    return int(st.value)
+
+
+# ------------------------------------------------------------------ conveniences
+
+def alloc_outputs(prob: Problem, device=None):
+    """Device buffers for aircache_compress: out_k, out_v ([bound, H_kv, D]),
+    out_offsets [L*B+1], keep [L*B], idx and iv [L, total_visual]."""
+    dev = device or prob.layers[1][0].device
+    rows = prob.compress_bound()
+    L, B = prob.L, prob.B
+    return {
+        "out_k": torch.empty((rows, prob.h_kv, prob.d), dtype=prob.dtype, device=dev),
+        "out_v": torch.empty((rows, prob.h_kv, prob.d), dtype=prob.dtype, device=dev),
+        "out_offsets": torch.empty(L * B + 1, dtype=torch.int64, device=dev),
+        "keep": torch.empty(L * B, dtype=torch.int32, device=dev),
+        "idx": torch.empty((L, prob.total_visual), dtype=torch.int32, device=dev),
+        "iv": torch.empty((L, prob.total_visual), dtype=torch.float32, device=dev),
+    }
+
+
+def compress(prob: Problem, ws=None, out=None, stream=None, check=True):
+    """One fused compression; returns the output dict (see alloc_outputs).
+    With check=True the device error word is read (this synchronises)."""
+    ws = prob.new_workspace() if ws is None else ws
+    out = alloc_outputs(prob) if out is None else out
+    aircache_compress(prob, ws, out["out_k"], out["out_v"], out["out_offsets"], out["keep"],
+                      out["idx"], out["iv"], stream)
+    if check:
+        st = aircache_get_error(ws, stream)
+        if st != OK:
+            raise AirCacheError(st, "aircache_compress (device)")
+    return out
+
+
+def compress_host(q, k, v, cu_seqlens, cu_visual, max_visual, max_text, alpha=0.9, r=0.1,
+                  device="cuda", stream=None):
+    """End-to-end from HOST tensors: copies q/k/v and the offsets to the device,
+    compresses, and copies the compacted cache and its offsets back.
+    Returns (out_k, out_v, out_offsets) as host tensors trimmed to the rows used."""
+    dq = q.to(device, non_blocking=True)
+    dk = k.to(device, non_blocking=True)
+    dv = v.to(device, non_blocking=True)
+    dcs = cu_seqlens.to(device, non_blocking=True)
+    dcv = cu_visual.to(device, non_blocking=True)
+    prob = Problem(dq, dk, dv, dcs, dcv, max_visual, max_text, alpha, r,
+                   total_tokens=k.shape[1], total_visual=int(cu_visual[-1]))
+    out = compress(prob, stream=stream)
+    offs = out["out_offsets"].cpu()
+    rows = int(offs[-1])
+    return out["out_k"][:rows].cpu(), out["out_v"][:rows].cpu(), offs
+
+
+def math_bound(L, B, total_text, total_visual, r):
+    """The compress_bound formula, for host-side sizing without the library."""
+    return L * total_text + math.ceil(r * L * total_visual) + B * (2 * L + 1)

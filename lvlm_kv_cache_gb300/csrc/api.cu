@@ -1,0 +1,347 @@
+// Host runtime of the AirCache library: argument validation, workspace
+// carve-up, and the C ABI entry points declared in include/aircache.h.  Every
+// entry point validates on the host, then enqueues its kernels on the caller's
+// stream; nothing here allocates, frees or synchronises except
+// aircache_get_error.
+#include <cmath>
+#include <cstring>
+
+#include "internal.cuh"
+
+using namespace aircache;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kCompressKernels = 6;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+int esize_of(int dtype) { return dtype == AIRCACHE_BF16 ? 2 : 4; }
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+int validate(const aircache_problem* p) {
+  if (!p) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->num_layers < 1 || p->num_layers > AIRCACHE_MAX_LAYERS) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->num_requests < 1) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->num_requests > 65535) return AIRCACHE_ERR_UNSUPPORTED;  // grid dimension
+  if (p->h_q < 1 || p->h_kv < 1 || p->h_q % p->h_kv != 0) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->head_dim < 1) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->head_dim != 64 && p->head_dim != 128) return AIRCACHE_ERR_UNSUPPORTED;
+  if (p->dtype != AIRCACHE_F32 && p->dtype != AIRCACHE_BF16) return AIRCACHE_ERR_UNSUPPORTED;
+  if (p->max_visual < 3 || p->max_text < 1) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->max_text > AIRCACHE_MAX_TEXT) return AIRCACHE_ERR_UNSUPPORTED;
+  if (p->max_elite < 0 || p->max_elite > p->max_text) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->reserved0 != 0) return AIRCACHE_ERR_INVALID_ARG;
+  const int64_t B = p->num_requests;
+  const int64_t total_text = p->total_tokens - p->total_visual;
+  if (p->total_visual < 3 * B || total_text < B) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->total_visual > B * p->max_visual || total_text > B * p->max_text) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->total_tokens > INT32_MAX) return AIRCACHE_ERR_UNSUPPORTED;
+  if (!p->cu_seqlens || !p->cu_visual || !p->q_text || !p->k || !p->v) return AIRCACHE_ERR_INVALID_ARG;
+  const int es = esize_of(p->dtype);
+  for (int l = 0; l < p->num_layers; ++l) {
+    if (!p->q_text[l] || !p->k[l] || !p->v[l]) return AIRCACHE_ERR_INVALID_ARG;
+    if (!aligned16(p->q_text[l]) || !aligned16(p->k[l]) || !aligned16(p->v[l])) return AIRCACHE_ERR_INVALID_ARG;
+  }
+  const int64_t strides[4] = {p->q_stride_tok, p->q_stride_head, p->kv_stride_tok, p->kv_stride_head};
+  for (int64_t st : strides) {
+    if (st <= 0 || (st * es) % 16 != 0) return AIRCACHE_ERR_INVALID_ARG;
+  }
+  if (p->q_stride_head < p->head_dim && p->h_q > 1) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->kv_stride_head < p->head_dim && p->h_kv > 1) return AIRCACHE_ERR_INVALID_ARG;
+  if (!(p->alpha >= 0.0 && p->alpha <= 1.0)) return AIRCACHE_ERR_INVALID_ARG;
+  if (!(p->r > 0.0 && p->r <= 1.0)) return AIRCACHE_ERR_INVALID_ARG;
+  // elite-window kernel holds one query row and P in shared memory
+  const size_t elite_fixed = sizeof(float) * ((size_t)p->h_q * p->head_dim + 3 * (size_t)p->max_text + 2);
+  if (elite_fixed > 200 * 1024) return AIRCACHE_ERR_UNSUPPORTED;
+  const int64_t max_elite = p->max_elite ? p->max_elite : p->max_text;
+  if ((int64_t)p->h_q * max_elite > (1 << 30)) return AIRCACHE_ERR_UNSUPPORTED;
+  return AIRCACHE_OK;
+}
+
+// Device description of a validated problem.
+Dev make_dev(const aircache_problem* p) {
+  Dev d;
+  std::memset(&d, 0, sizeof d);
+  d.L = p->num_layers;
+  d.B = p->num_requests;
+  d.h_q = p->h_q;
+  d.h_kv = p->h_kv;
+  d.d = p->head_dim;
+  d.g = p->h_q / p->h_kv;
+  d.dtype = p->dtype;
+  d.max_visual = p->max_visual;
+  d.max_text = p->max_text;
+  d.max_elite = p->max_elite ? p->max_elite : p->max_text;
+  d.rows_max = d.h_q * d.max_elite;
+  const long long units = (long long)d.L * d.B;
+  const long long tiles_max = (d.max_visual + d.max_elite + kTileKeys - 1) / kTileKeys;
+  long long C = (kTargetCtas + units - 1) / units;
+  const long long c_min = (tiles_max + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
+  if (C < c_min) C = c_min;
+  if (C > tiles_max) C = tiles_max;
+  if (C < 1) C = 1;
+  d.chunks = (int)C;
+  d.tiles_per_cta = (int)((tiles_max + C - 1) / C);
+  d.total_tokens = p->total_tokens;
+  d.total_visual = p->total_visual;
+  d.total_text = p->total_tokens - p->total_visual;
+  d.cu_seqlens = p->cu_seqlens;
+  d.cu_visual = p->cu_visual;
+  d.q_stride_tok = p->q_stride_tok;
+  d.q_stride_head = p->q_stride_head;
+  d.kv_stride_tok = p->kv_stride_tok;
+  d.kv_stride_head = p->kv_stride_head;
+  d.alpha = p->alpha;
+  d.r = p->r;
+  d.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->head_dim));
+  return d;
+}
+
+LayerPtrs make_ptrs(const aircache_problem* p) {
+  LayerPtrs lp;
+  std::memset(&lp, 0, sizeof lp);
+  for (int l = 0; l < p->num_layers; ++l) {
+    lp.q[l] = p->q_text[l];
+    lp.k[l] = p->k[l];
+    lp.v[l] = p->v[l];
+  }
+  return lp;
+}
+
+// Carve the workspace; with base == nullptr only the size is computed.
+size_t carve(const Dev& d, char* base, Ws* w) {
+  const size_t LB = (size_t)d.L * d.B;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* ptr = base ? base + off : nullptr;
+    off = align_up(off + bytes);
+    return ptr;
+  };
+  Ws t;
+  std::memset(&t, 0, sizeof t);
+  // zeroed block: error, cnt_all, cnt_req[B], cnt_unit[L*B]
+  char* zero = take(sizeof(int32_t) * (2 + d.B + LB));
+  t.error = reinterpret_cast<int32_t*>(zero);
+  t.cnt_all = reinterpret_cast<uint32_t*>(zero ? zero + 4 : nullptr);
+  t.cnt_req = reinterpret_cast<uint32_t*>(zero ? zero + 8 : nullptr);
+  t.cnt_unit = reinterpret_cast<uint32_t*>(zero ? zero + 8 + 4 * d.B : nullptr);
+  t.zero_bytes = sizeof(int32_t) * (2 + d.B + LB);
+  t.elite = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB * d.max_text));
+  t.n_tk = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
+  t.part = reinterpret_cast<float2*>(take(sizeof(float2) * LB * d.chunks * d.rows_max));
+  t.lse = reinterpret_cast<float*>(take(sizeof(float) * LB * d.rows_max));
+  t.iv = reinterpret_cast<float*>(take(sizeof(float) * (size_t)d.L * d.total_visual));
+  t.stats = reinterpret_cast<double*>(take(sizeof(double) * 2 * LB));
+  t.keep = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
+  t.idx = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (size_t)d.L * d.total_visual));
+  t.out_offsets = reinterpret_cast<int64_t*>(take(sizeof(int64_t) * (LB + 1)));
+  if (w) *w = t;
+  return off;
+}
+
+int check_ws(const aircache_problem* p, void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return AIRCACHE_ERR_INVALID_ARG;
+  if (ws_bytes < aircache_workspace_size(p)) return AIRCACHE_ERR_WORKSPACE;
+  return AIRCACHE_OK;
+}
+
+#define AC_TRY(expr)                                 \
+  do {                                               \
+    if ((expr) != cudaSuccess) return AIRCACHE_ERR_CUDA; \
+  } while (0)
+
+int begin(const Ws& w, cudaStream_t s) {
+  return cudaMemsetAsync(w.error, 0, w.zero_bytes, s) == cudaSuccess ? AIRCACHE_OK : AIRCACHE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t aircache_workspace_size(const aircache_problem* p) {
+  if (validate(p) != AIRCACHE_OK) return 0;
+  return carve(make_dev(p), nullptr, nullptr);
+}
+
+int64_t aircache_compress_bound(const aircache_problem* p) {
+  if (validate(p) != AIRCACHE_OK) return -1;
+  const int64_t L = p->num_layers, B = p->num_requests;
+  const int64_t text = p->total_tokens - p->total_visual;
+  const double vis = std::ceil(p->r * (double)L * (double)p->total_visual);
+  int64_t bound = L * text + (int64_t)vis + B * (2 * L + 1);
+  const int64_t cap = L * p->total_tokens;
+  return bound < cap ? bound : cap;
+}
+
+int aircache_score(const aircache_problem* p, void* ws, size_t ws_bytes, float* iv, int32_t* elite,
+                   int32_t* n_tk, void* stream) {
+  int rc = validate(p);
+  if (rc != AIRCACHE_OK) return rc;
+  if ((rc = check_ws(p, ws, ws_bytes)) != AIRCACHE_OK) return rc;
+  if (!iv || !elite || !n_tk) return AIRCACHE_ERR_INVALID_ARG;
+  const Dev d = make_dev(p);
+  const LayerPtrs lp = make_ptrs(p);
+  Ws w;
+  carve(d, static_cast<char*>(ws), &w);
+  w.iv = iv;
+  w.elite = elite;
+  w.n_tk = n_tk;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
+  AC_TRY(launch_elite(d, lp, w, s));
+  AC_TRY(launch_score_pass1(d, lp, w, s));
+  AC_TRY(launch_score_pass2(d, lp, w, s));
+  return AIRCACHE_OK;
+}
+
+int aircache_budget(const aircache_problem* p, const float* iv, void* ws, size_t ws_bytes, double* stats,
+                    int32_t* keep, void* stream) {
+  int rc = validate(p);
+  if (rc != AIRCACHE_OK) return rc;
+  if ((rc = check_ws(p, ws, ws_bytes)) != AIRCACHE_OK) return rc;
+  if (!iv || !keep) return AIRCACHE_ERR_INVALID_ARG;
+  const Dev d = make_dev(p);
+  Ws w;
+  carve(d, static_cast<char*>(ws), &w);
+  w.iv = const_cast<float*>(iv);
+  w.keep = keep;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
+  AC_TRY(launch_stats_budget(d, w, stats, 0, false, s));
+  return AIRCACHE_OK;
+}
+
+int aircache_select(const aircache_problem* p, const float* iv, const int32_t* keep, void* ws,
+                    size_t ws_bytes, int32_t* idx, void* stream) {
+  int rc = validate(p);
+  if (rc != AIRCACHE_OK) return rc;
+  if ((rc = check_ws(p, ws, ws_bytes)) != AIRCACHE_OK) return rc;
+  if (!iv || !keep || !idx) return AIRCACHE_ERR_INVALID_ARG;
+  const Dev d = make_dev(p);
+  Ws w;
+  carve(d, static_cast<char*>(ws), &w);
+  w.iv = const_cast<float*>(iv);
+  w.keep = const_cast<int32_t*>(keep);
+  w.idx = idx;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
+  AC_TRY(launch_select(d, w, s));
+  return AIRCACHE_OK;
+}
+
+int aircache_compact(const aircache_problem* p, const int32_t* idx, const int32_t* keep, void* ws,
+                     size_t ws_bytes, void* out_k, void* out_v, int64_t* out_offsets,
+                     int64_t out_rows_capacity, void* stream) {
+  int rc = validate(p);
+  if (rc != AIRCACHE_OK) return rc;
+  if ((rc = check_ws(p, ws, ws_bytes)) != AIRCACHE_OK) return rc;
+  if (!idx || !keep || !out_k || !out_v || !out_offsets || out_rows_capacity < 0) return AIRCACHE_ERR_INVALID_ARG;
+  if (!aligned16(out_k) || !aligned16(out_v)) return AIRCACHE_ERR_INVALID_ARG;
+  const Dev d = make_dev(p);
+  const LayerPtrs lp = make_ptrs(p);
+  Ws w;
+  carve(d, static_cast<char*>(ws), &w);
+  w.idx = const_cast<int32_t*>(idx);
+  w.keep = const_cast<int32_t*>(keep);
+  w.out_offsets = out_offsets;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
+  AC_TRY(launch_offsets(d, w, out_rows_capacity, s));
+  AC_TRY(launch_compact(d, lp, w, out_k, out_v, out_rows_capacity, s));
+  return AIRCACHE_OK;
+}
+
+static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, void* out_k, void* out_v,
+                         int64_t* out_offsets, int64_t out_rows_capacity, int32_t* keep, int32_t* idx,
+                         float* iv, void* const* events, int n_events, void* stream) {
+  int rc = validate(p);
+  if (rc != AIRCACHE_OK) return rc;
+  if ((rc = check_ws(p, ws, ws_bytes)) != AIRCACHE_OK) return rc;
+  if (!out_k || !out_v || !out_offsets || !keep || out_rows_capacity < 0) return AIRCACHE_ERR_INVALID_ARG;
+  if (!aligned16(out_k) || !aligned16(out_v)) return AIRCACHE_ERR_INVALID_ARG;
+  if (events && n_events != kCompressKernels + 1) return AIRCACHE_ERR_INVALID_ARG;
+  const Dev d = make_dev(p);
+  const LayerPtrs lp = make_ptrs(p);
+  Ws w;
+  carve(d, static_cast<char*>(ws), &w);
+  w.keep = keep;
+  w.out_offsets = out_offsets;
+  if (idx) w.idx = idx;
+  if (iv) w.iv = iv;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto mark = [&](int i) {
+    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
+  };
+  if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
+  AC_TRY(mark(0));
+  AC_TRY(launch_elite(d, lp, w, s));
+  AC_TRY(mark(1));
+  AC_TRY(launch_score_pass1(d, lp, w, s));
+  AC_TRY(mark(2));
+  AC_TRY(launch_score_pass2(d, lp, w, s));
+  AC_TRY(mark(3));
+  AC_TRY(launch_stats_budget(d, w, nullptr, out_rows_capacity, true, s));
+  AC_TRY(mark(4));
+  AC_TRY(launch_select(d, w, s));
+  AC_TRY(mark(5));
+  AC_TRY(launch_compact(d, lp, w, out_k, out_v, out_rows_capacity, s));
+  AC_TRY(mark(6));
+  return AIRCACHE_OK;
+}
+
+int aircache_compress(const aircache_problem* p, void* ws, size_t ws_bytes, void* out_k, void* out_v,
+                      int64_t* out_offsets, int64_t out_rows_capacity, int32_t* keep, int32_t* idx,
+                      float* iv, void* stream) {
+  return compress_impl(p, ws, ws_bytes, out_k, out_v, out_offsets, out_rows_capacity, keep, idx, iv,
+                       nullptr, 0, stream);
+}
+
+int aircache_compress_profile(const aircache_problem* p, void* ws, size_t ws_bytes, void* out_k,
+                              void* out_v, int64_t* out_offsets, int64_t out_rows_capacity,
+                              int32_t* keep, int32_t* idx, float* iv, void* const* events,
+                              int n_events, void* stream) {
+  if (!events) return AIRCACHE_ERR_INVALID_ARG;
+  return compress_impl(p, ws, ws_bytes, out_k, out_v, out_offsets, out_rows_capacity, keep, idx, iv,
+                       events, n_events, stream);
+}
+
+const char* aircache_kernel_name(int i) {
+  static const char* names[kCompressKernels] = {"elite_window", "score_pass1", "score_pass2",
+                                                "stats_budget", "select_topk", "gather_compact"};
+  return (i >= 0 && i < kCompressKernels) ? names[i] : nullptr;
+}
+
+int aircache_compress_launches(const aircache_problem* p) {
+  if (validate(p) != AIRCACHE_OK) return -1;
+  return kCompressKernels;
+}
+
+int aircache_get_error(const void* ws, void* stream, int32_t* status) {
+  if (!ws || !status) return AIRCACHE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return AIRCACHE_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return AIRCACHE_ERR_CUDA;
+  *status = v;
+  return AIRCACHE_OK;
+}
+
+const char* aircache_status_string(int status) {
+  switch (status) {
+    case AIRCACHE_OK: return "ok";
+    case AIRCACHE_ERR_INVALID_ARG: return "invalid argument";
+    case AIRCACHE_ERR_UNSUPPORTED: return "unsupported problem";
+    case AIRCACHE_ERR_WORKSPACE: return "workspace too small";
+    case AIRCACHE_ERR_CUDA: return "CUDA launch or memset failed";
+    case AIRCACHE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case AIRCACHE_ERR_DEVICE_BOUNDS: return "inconsistent request layout seen on the device";
+    case AIRCACHE_ERR_ELITE_OVERFLOW: return "elite set larger than max_elite";
+    case AIRCACHE_ERR_CAPACITY: return "output arena too small";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,125 @@
+// Compaction of the kept rows into the decode cache (AirCache notes, "Loss /
+// training strategy": the compressed cache is what decoding reads; every text
+// position is kept after the selected visual positions).
+//
+// The output arena holds, for each layer l and request b in that order, the
+// rows [K_v[idx]; K_t] (and the same rows of V) as dense [h_kv][head_dim] rows.
+// A persistent grid of warps walks the output rows; each warp finds its row's
+// (l, b) by binary search over the row offsets (staged in shared memory),
+// resolves the source position and copies the K and V rows with 16-byte loads
+// and stores.  Bit-exact: no arithmetic touches the data.
+#include "internal.cuh"
+
+namespace aircache {
+namespace {
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyWarps = kCopyThreads / 32;
+constexpr int kMaxSmemOffsets = 4096;
+
+struct CompactArgs {
+  Dev p;
+  LayerPtrs lp;
+  Ws w;
+  void* out_k;
+  void* out_v;
+  int64_t capacity;  // rows out_k / out_v hold
+};
+
+__global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_constant__ CompactArgs a) {
+  const Dev& p = a.p;
+  const Ws& w = a.w;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ long long offs[kMaxSmemOffsets + 1];
+  if (*(volatile int32_t*)w.error != 0) return;
+  const int units = p.L * p.B;
+  const bool in_smem = units <= kMaxSmemOffsets;
+  if (in_smem) {
+    for (int i = tid; i <= units; i += kCopyThreads) offs[i] = w.out_offsets[i];
+  }
+  __syncthreads();
+  const long long* off = in_smem ? offs : reinterpret_cast<const long long*>(w.out_offsets);
+  const long long total = off[units];
+  if (total > a.capacity || total < 0) {
+    if (tid == 0) set_error(w.error, AIRCACHE_ERR_CAPACITY);
+    return;
+  }
+
+  const int esize = (p.dtype == AIRCACHE_BF16) ? 2 : 4;
+  const int vec_per_head = p.d * esize / 16;
+  const int vec_per_row = p.h_kv * vec_per_head;
+  const int64_t elems_per_vec = 16 / esize;
+  uint4* outk = reinterpret_cast<uint4*>(a.out_k);
+  uint4* outv = reinterpret_cast<uint4*>(a.out_v);
+
+  const long long warps = (long long)gridDim.x * kCopyWarps;
+  for (long long row = (long long)blockIdx.x * kCopyWarps + warp; row < total; row += warps) {
+    // unit u with off[u] <= row < off[u+1]
+    int lo = 0, hi = units - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (off[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    const int u = lo, l = u / p.B, b = u % p.B;
+    const long long j = row - off[u];
+    Req R;
+    const bool ok = load_req(p, b, R);
+    const int kp = w.keep[u];
+    int64_t pos;
+    if (j < kp) {
+      pos = w.idx[(size_t)l * p.total_visual + R.vis0 + j];
+      if (pos < 0 || pos >= R.n_v) pos = -1;
+    } else {
+      pos = (int64_t)R.n_v + (j - kp);
+      if (pos >= (int64_t)R.n_v + R.n_t) pos = -1;
+    }
+    if (!ok || pos < 0) {
+      if (lane == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    const char* kb = reinterpret_cast<const char*>(a.lp.k[l]);
+    const char* vb = reinterpret_cast<const char*>(a.lp.v[l]);
+    const int64_t tok = R.seq0 + pos;
+    uint4 kbuf[4], vbuf[4];
+    for (int v0 = 0; v0 < vec_per_row; v0 += 4 * 32) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int vec = v0 + i * 32 + lane;
+        if (vec < vec_per_row) {
+          const int head = vec / vec_per_head, part = vec % vec_per_head;
+          const int64_t eo = tok * p.kv_stride_tok + head * p.kv_stride_head + part * elems_per_vec;
+          kbuf[i] = __ldg(reinterpret_cast<const uint4*>(kb + eo * esize));
+          vbuf[i] = __ldg(reinterpret_cast<const uint4*>(vb + eo * esize));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int vec = v0 + i * 32 + lane;
+        if (vec < vec_per_row) {
+          outk[row * vec_per_row + vec] = kbuf[i];
+          outv[row * vec_per_row + vec] = vbuf[i];
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_compact(const Dev& p, const LayerPtrs& lp, const Ws& w, void* out_k, void* out_v,
+                           int64_t capacity, cudaStream_t s) {
+  CompactArgs a;
+  a.p = p;
+  a.lp = lp;
+  a.w = w;
+  a.out_k = out_k;
+  a.out_v = out_v;
+  a.capacity = capacity;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  compact_kernel<<<sms * 4, kCopyThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace aircache

@@ -1,0 +1,101 @@
+// Internal interfaces of the AirCache CUDA library: the device-side problem
+// description, the workspace carve-up and the kernel launchers.  Not installed;
+// the public ABI is include/aircache.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/aircache.h"
+
+namespace aircache {
+
+constexpr int kTileKeys = 64;        // keys per score tile (4 warps x 16 keys)
+constexpr int kRowChunk = 32;        // query rows per score chunk (4 n8 MMA tiles)
+constexpr int kScoreThreads = 128;
+constexpr int kMaxTilesPerCta = 128; // bound on the pass-2 accumulator (128 x 64 fp32)
+constexpr int kTargetCtas = 1184;    // score grid target (8 x 148 SMs)
+constexpr long long kSpinLimit = 1LL << 26;  // bounded waits (iterations)
+
+// Device-visible description of one problem (host checks done).
+struct Dev {
+  int L, B, h_q, h_kv, d, g, dtype;
+  int max_visual, max_text, max_elite;
+  int rows_max;          // h_q * max_elite: query rows per (layer, request)
+  int chunks;            // C: score CTAs per (layer, request)
+  int tiles_per_cta;     // ceil(tiles_max / C)
+  int64_t total_tokens, total_visual, total_text;
+  const int32_t* cu_seqlens;
+  const int32_t* cu_visual;
+  int64_t q_stride_tok, q_stride_head, kv_stride_tok, kv_stride_head;
+  double alpha, r;
+  float scale_log2;      // log2(e) / sqrt(D): logits are kept in base 2
+};
+
+struct LayerPtrs {
+  const void* q[AIRCACHE_MAX_LAYERS];
+  const void* k[AIRCACHE_MAX_LAYERS];
+  const void* v[AIRCACHE_MAX_LAYERS];
+};
+
+// Workspace carve-up.  The first block (error word and counters) is zeroed by
+// every entry point.
+struct Ws {
+  int32_t* error;        // [1]
+  uint32_t* cnt_all;     // [1]   requests whose budget is done
+  uint32_t* cnt_req;     // [B]   layers of a request whose stats are done
+  uint32_t* cnt_unit;    // [L*B] pass-1 CTAs done per (layer, request)
+  int32_t* elite;        // [L*B*max_text]
+  int32_t* n_tk;         // [L*B]
+  float2* part;          // [L*B*C*rows_max] pass-1 row partials (max, sum), base 2
+  float* lse;            // [L*B*rows_max]   row log-sum-exp, base 2
+  float* iv;             // [L*total_visual]
+  double* stats;         // [L*B*2]
+  int32_t* keep;         // [L*B]
+  int32_t* idx;          // [L*total_visual]
+  int64_t* out_offsets;  // [L*B+1]
+  size_t zero_bytes;     // bytes of the zeroed block
+};
+
+// One request's slice of the packed layout, validated on the device.
+struct Req {
+  int64_t seq0;   // first prompt position in K/V
+  int64_t vis0;   // first I_v slot
+  int64_t txt0;   // first Q_text row
+  int n_v, n_t;
+};
+
+__device__ __forceinline__ void set_error(int32_t* err, int code) {
+  atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ bool load_req(const Dev& p, int b, Req& r) {
+  const int64_t s0 = p.cu_seqlens[b], s1 = p.cu_seqlens[b + 1];
+  const int64_t v0 = p.cu_visual[b], v1 = p.cu_visual[b + 1];
+  const int64_t n_v = v1 - v0, n_t = (s1 - s0) - n_v;
+  bool ok = s0 >= 0 && s1 <= p.total_tokens && v0 >= 0 && v1 <= p.total_visual &&
+            n_v >= 3 && n_v <= p.max_visual && n_t >= 1 && n_t <= p.max_text &&
+            (s0 - v0) >= 0 && (s0 - v0) + n_t <= p.total_text;
+  if (b == 0) ok = ok && s0 == 0 && v0 == 0;
+  if (b == p.B - 1) ok = ok && s1 == p.total_tokens && v1 == p.total_visual;
+  r.seq0 = s0;
+  r.vis0 = v0;
+  r.txt0 = s0 - v0;
+  r.n_v = (int)n_v;
+  r.n_t = (int)n_t;
+  return ok;
+}
+
+// Launchers (each returns cudaGetLastError() of its launches).
+cudaError_t launch_elite(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_t s);
+cudaError_t launch_score_pass1(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_t s);
+cudaError_t launch_score_pass2(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_t s);
+cudaError_t launch_stats_budget(const Dev& p, const Ws& w, double* stats_out,
+                                int64_t out_capacity, bool offsets, cudaStream_t s);
+cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s);
+cudaError_t launch_offsets(const Dev& p, const Ws& w, int64_t out_capacity, cudaStream_t s);
+cudaError_t launch_compact(const Dev& p, const LayerPtrs& lp, const Ws& w, void* out_k,
+                           void* out_v, int64_t capacity, cudaStream_t s);
+
+}  // namespace aircache
