@@ -143,6 +143,22 @@ class ClockSampler:
                 "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows)}
 
 
+def max_over_ranks(x, dist, device):
+    """The max of a per-rank float over all ranks (the bench's only collective)."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, units_per_rank, steps, total_ms):
+    """Units processed by all ranks per second, timed by the slowest rank."""
+    return world * units_per_rank * steps / (total_ms / 1e3)
+
+
 def unit_lengths(spec):
     return [(spec.n_visual[b], spec.n_text[b]) for b in range(spec.B)]
 
@@ -315,18 +331,14 @@ def main():
         dist.barrier()
     clocks = sampler.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     st = A.aircache_get_error(ws)
     if st != 0:
         raise RuntimeError(f"device error {st}: {A.status_string(st)}")
 
     units = spec.L * sum(spec.n_visual)  # visual KV rows (token x layer) per step per rank
     ms_per_step = total_ms / args.steps
-    value = world * units * args.steps / (total_ms / 1e3)
+    value = whole_job_rate(world, units, args.steps, total_ms)
 
     # ---- per-kernel durations on the launching stream
     nk = prob.launches()
@@ -412,13 +424,9 @@ def main():
             e2e_step()
         e_ev.record()
         torch.cuda.synchronize()
-        e2e_ms = s_ev.elapsed_time(e_ev)
-        if dist:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(s_ev.elapsed_time(e_ev), dist, dev)
         assert int(of_h[-1]) == int(out["out_offsets"][-1])
-        line["e2e"] = {"value": world * units * n_e2e / (e2e_ms / 1e3), "unit": UNIT,
+        line["e2e"] = {"value": whole_job_rate(world, units, n_e2e, e2e_ms), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                        "ms_per_step": e2e_ms / n_e2e}
 
