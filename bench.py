@@ -170,17 +170,15 @@ def algorithmic_bytes(spec, n_tk, keep, esize):
     (bf16; esize-scaled) + the I_v workspace."""
     row = spec.H_kv * spec.D * esize
     qrow = spec.H_q * spec.D * esize
-    k = {"elite_window": 0, "score_pass1": 0, "score_pass2": 0, "stats_budget": 0, "select_topk": 0,
-         "gather_compact": 0}
+    k = {"elite_window": 0, "score_budget": 0, "select_topk": 0, "gather_compact": 0}
     path = 0
     for l in range(spec.L):
         for b, (nv, nt) in enumerate(unit_lengths(spec)):
             u = l * spec.B + b
             t, kp = int(n_tk[u]), int(keep[u])
             k["elite_window"] += nt * row + qrow + 4 * t
-            k["score_pass1"] += (nv + t) * row + t * qrow
-            k["score_pass2"] += nv * row + t * qrow + 4 * nv
-            k["stats_budget"] += 4 * nv + 4
+            # K read once (the second pass is meant to hit L2), elite Q rows, I_v written
+            k["score_budget"] += (nv + t) * row + t * qrow + 4 * nv
             k["select_topk"] += 4 * nv + 4 * kp
             k["gather_compact"] += 2 * 2 * (kp + nt) * row + 4 * kp
             path += (nv + nt) * row + (1 + t) * qrow + 2 * 2 * (kp + nt) * row + 4 * nv * 3 + 8 * kp

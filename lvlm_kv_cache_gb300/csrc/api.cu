@@ -13,7 +13,7 @@ using namespace aircache;
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kCompressKernels = 6;
+constexpr int kCompressKernels = 4;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -76,15 +76,8 @@ Dev make_dev(const aircache_problem* p) {
   d.max_text = p->max_text;
   d.max_elite = p->max_elite ? p->max_elite : p->max_text;
   d.rows_max = d.h_q * d.max_elite;
-  const long long units = (long long)d.L * d.B;
-  const long long tiles_max = (d.max_visual + d.max_elite + kTileKeys - 1) / kTileKeys;
-  long long C = (kTargetCtas + units - 1) / units;
-  const long long c_min = (tiles_max + kMaxTilesPerCta - 1) / kMaxTilesPerCta;
-  if (C < c_min) C = c_min;
-  if (C > tiles_max) C = tiles_max;
-  if (C < 1) C = 1;
-  d.chunks = (int)C;
-  d.tiles_per_cta = (int)((tiles_max + C - 1) / C);
+  d.rc_max = (d.g * d.max_elite + 31) / 32;
+  d.lse_stride = d.h_kv * d.rc_max * 32;
   d.total_tokens = p->total_tokens;
   d.total_visual = p->total_visual;
   d.total_text = p->total_tokens - p->total_visual;
@@ -122,17 +115,29 @@ size_t carve(const Dev& d, char* base, Ws* w) {
   };
   Ws t;
   std::memset(&t, 0, sizeof t);
-  // zeroed block: error, cnt_all, cnt_req[B], cnt_unit[L*B]
-  char* zero = take(sizeof(int32_t) * (2 + d.B + LB));
+  // zeroed block: error, cnt_all, ticket, cnt_req[B], cnt_p1/cnt_p2/lse_ready/p2claim[L*B]
+  const size_t zbytes = 16 + sizeof(uint32_t) * (d.B + 4 * LB);
+  char* zero = take(zbytes);
   t.error = reinterpret_cast<int32_t*>(zero);
   t.cnt_all = reinterpret_cast<uint32_t*>(zero ? zero + 4 : nullptr);
-  t.cnt_req = reinterpret_cast<uint32_t*>(zero ? zero + 8 : nullptr);
-  t.cnt_unit = reinterpret_cast<uint32_t*>(zero ? zero + 8 + 4 * d.B : nullptr);
-  t.zero_bytes = sizeof(int32_t) * (2 + d.B + LB);
+  t.ticket = reinterpret_cast<unsigned long long*>(zero ? zero + 8 : nullptr);
+  t.cnt_req = reinterpret_cast<uint32_t*>(zero ? zero + 16 : nullptr);
+  t.cnt_p1 = t.cnt_req ? t.cnt_req + d.B : nullptr;
+  t.cnt_p2 = t.cnt_p1 ? t.cnt_p1 + LB : nullptr;
+  t.lse_ready = t.cnt_p2 ? t.cnt_p2 + LB : nullptr;
+  t.p2claim = t.lse_ready ? t.lse_ready + LB : nullptr;
+  t.zero_bytes = zbytes;
+  const size_t T1 = (size_t)(d.max_visual + 127) / 128 + (size_t)(d.max_elite + 127) / 128;  // score tile slots
+  const size_t G = (size_t)(d.h_kv + 3) / 4;
   t.elite = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB * d.max_text));
   t.n_tk = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
-  t.part = reinterpret_cast<float2*>(take(sizeof(float2) * LB * d.chunks * d.rows_max));
-  t.lse = reinterpret_cast<float*>(take(sizeof(float) * LB * d.rows_max));
+  t.uinfo = reinterpret_cast<int4*>(take(sizeof(int4) * 2 * LB));
+  const size_t esz = d.dtype == AIRCACHE_BF16 ? 2 : 4;
+  t.qel = take(esz * LB * d.rows_max * d.d);
+  t.kel = take(esz * LB * d.h_kv * d.max_elite * d.d);
+  t.part = reinterpret_cast<float2*>(take(sizeof(float2) * LB * T1 * d.rows_max));
+  t.lse = reinterpret_cast<float*>(take(sizeof(float) * LB * d.lse_stride));
+  t.ivp = G > 1 ? reinterpret_cast<float*>(take(sizeof(float) * G * (size_t)d.L * d.total_visual)) : nullptr;
   t.iv = reinterpret_cast<float*>(take(sizeof(float) * (size_t)d.L * d.total_visual));
   t.stats = reinterpret_cast<double*>(take(sizeof(double) * 2 * LB));
   t.keep = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
@@ -152,6 +157,14 @@ int check_ws(const aircache_problem* p, void* ws, size_t ws_bytes) {
   do {                                               \
     if ((expr) != cudaSuccess) return AIRCACHE_ERR_CUDA; \
   } while (0)
+
+// SMs of the current device (the persistent scoring grid is one CTA per SM).
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) return 148;
+  return sms;
+}
 
 int begin(const Ws& w, cudaStream_t s) {
   return cudaMemsetAsync(w.error, 0, w.zero_bytes, s) == cudaSuccess ? AIRCACHE_OK : AIRCACHE_ERR_CUDA;
@@ -192,8 +205,7 @@ int aircache_score(const aircache_problem* p, void* ws, size_t ws_bytes, float* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
   AC_TRY(launch_elite(d, lp, w, s));
-  AC_TRY(launch_score_pass1(d, lp, w, s));
-  AC_TRY(launch_score_pass2(d, lp, w, s));
+  AC_TRY(launch_score(d, lp, w, plan_score(d, sm_count(), false, 0), s));
   return AIRCACHE_OK;
 }
 
@@ -279,16 +291,12 @@ static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, v
   AC_TRY(mark(0));
   AC_TRY(launch_elite(d, lp, w, s));
   AC_TRY(mark(1));
-  AC_TRY(launch_score_pass1(d, lp, w, s));
+  AC_TRY(launch_score(d, lp, w, plan_score(d, sm_count(), true, out_rows_capacity), s));
   AC_TRY(mark(2));
-  AC_TRY(launch_score_pass2(d, lp, w, s));
-  AC_TRY(mark(3));
-  AC_TRY(launch_stats_budget(d, w, nullptr, out_rows_capacity, true, s));
-  AC_TRY(mark(4));
   AC_TRY(launch_select(d, w, s));
-  AC_TRY(mark(5));
+  AC_TRY(mark(3));
   AC_TRY(launch_compact(d, lp, w, out_k, out_v, out_rows_capacity, s));
-  AC_TRY(mark(6));
+  AC_TRY(mark(4));
   return AIRCACHE_OK;
 }
 
@@ -309,8 +317,8 @@ int aircache_compress_profile(const aircache_problem* p, void* ws, size_t ws_byt
 }
 
 const char* aircache_kernel_name(int i) {
-  static const char* names[kCompressKernels] = {"elite_window", "score_pass1", "score_pass2",
-                                                "stats_budget", "select_topk", "gather_compact"};
+  static const char* names[kCompressKernels] = {"elite_window", "score_budget", "select_topk",
+                                                "gather_compact"};
   return (i >= 0 && i < kCompressKernels) ? names[i] : nullptr;
 }
 

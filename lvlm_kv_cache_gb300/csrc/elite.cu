@@ -1,116 +1,139 @@
 // Elite observation window (AirCache notes, "Key design 1": equations Att and k).
 //
-// One CTA per (request, layer).  For every query head h the last text query is
-// dotted with the N_t text keys of KV head h/g; each head's row is softmaxed in
-// fp32 (base-2 logits, max-subtracted) and the rows are summed over heads into
-// P (the head mean up to the common factor 1/H_q, which the threshold test does
-// not see).  The elite set is {j : P[j] >= alpha * max P}, written in ascending
-// order.  Heads are processed in chunks whose logits fit in shared memory.
+// One CTA per (request, layer).  The last text query of every head is dotted
+// with the N_t text keys of its KV head: the text keys stream through a ring of
+// shared-memory stages (128 keys of one KV head per stage, cp.async), and the
+// logit tile is the same MMA tile as the scoring kernel's (query rows = the g
+// heads of that KV head).  Base-2 logits are kept in shared memory, each head's
+// row is softmaxed in fp32 (max-subtracted), and the rows are summed over heads
+// into P (the head mean up to the common factor 1/H_q, which the threshold test
+// does not see).  The elite set is {j : P[j] >= alpha * max P}, written in
+// ascending order.  When the logits of every head do not fit in shared memory,
+// KV heads are processed in chunks and P accumulates across chunks.
 #include "internal.cuh"
+#include "ptx.cuh"
+#include "tile.cuh"
 
 namespace aircache {
 namespace {
 
 constexpr int kEliteThreads = 256;
+constexpr int kEliteWarps = kEliteThreads / 32;
+constexpr int kSmemBudget = 220 * 1024;
 
 struct EliteArgs {
   Dev p;
   LayerPtrs lp;
   Ws w;
-  int head_chunk;  // heads whose logits are held at once
+  int kv_chunk;  // KV heads whose logits are held at once
 };
 
-template <typename T>
-__device__ __forceinline__ float dot_row(const float* __restrict__ qs, const T* __restrict__ krow,
-                                         int d);
-
-template <>
-__device__ __forceinline__ float dot_row<float>(const float* __restrict__ qs,
-                                                const float* __restrict__ krow, int d) {
-  float acc = 0.f;
-  const float4* k4 = reinterpret_cast<const float4*>(krow);
-  for (int i = 0; i < d / 4; ++i) {
-    const float4 kv = __ldg(k4 + i);
-    acc = fmaf(qs[4 * i + 0], kv.x, acc);
-    acc = fmaf(qs[4 * i + 1], kv.y, acc);
-    acc = fmaf(qs[4 * i + 2], kv.z, acc);
-    acc = fmaf(qs[4 * i + 3], kv.w, acc);
-  }
-  return acc;
-}
-
-template <>
-__device__ __forceinline__ float dot_row<__nv_bfloat16>(const float* __restrict__ qs,
-                                                        const __nv_bfloat16* __restrict__ krow,
-                                                        int d) {
-  float acc = 0.f;
-  const uint4* k4 = reinterpret_cast<const uint4*>(krow);
-  for (int i = 0; i < d / 8; ++i) {
-    const uint4 raw = __ldg(k4 + i);
-    const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 kv = __bfloat1622float2(pr[j]);
-      acc = fmaf(qs[8 * i + 2 * j], kv.x, acc);
-      acc = fmaf(qs[8 * i + 2 * j + 1], kv.y, acc);
+// Issue the cp.async copies of item i of a KV-head chunk: items run over
+// (kv head, query-row chunk, key tile).  Keys >= N_t and rows >= g are zero.
+template <typename T, int D>
+__device__ __forceinline__ void load_item(const Dev& p, const Req& R, const char* kbase, const char* qbase,
+                                          int kv0, int n_rc, int n_kt, int i, unsigned char* stage) {
+  using G = TileGeom<T, D>;
+  const int per_kv = n_rc * n_kt;
+  const int kvh = kv0 + i / per_kv, rc = (i % per_kv) / n_kt, t = i % n_kt;
+  constexpr int kVec = G::kRowBytes / 16;
+  for (int c = threadIdx.x; c < kTK * kVec; c += kEliteThreads) {
+    const int row = c / kVec, v = c % kVec;
+    const int key = t * kTK + row;
+    const char* src = kbase;
+    int bytes = 0;
+    if (key < R.n_t) {
+      src = kbase + ((R.seq0 + R.n_v + key) * p.kv_stride_tok + (int64_t)kvh * p.kv_stride_head) * sizeof(T) + 16 * v;
+      bytes = 16;
     }
+    cp_async16(stage + row * G::kRowPitch + 16 * v, src, bytes);
   }
-  return acc;
+  for (int c = threadIdx.x; c < kRC * kVec; c += kEliteThreads) {
+    const int n = c / kVec, v = c % kVec;
+    const int hh = rc * kRC + n;
+    const char* src = qbase;
+    int bytes = 0;
+    if (hh < p.g) {
+      const int h = kvh * p.g + hh;
+      src = qbase + ((R.txt0 + R.n_t - 1) * p.q_stride_tok + (int64_t)h * p.q_stride_head) * sizeof(T) + 16 * v;
+      bytes = 16;
+    }
+    cp_async16(stage + G::kKBytes + n * G::kRowPitch + 16 * v, src, bytes);
+  }
 }
 
-template <typename T>
-__device__ __forceinline__ float to_float(T x);
-template <>
-__device__ __forceinline__ float to_float<float>(float x) { return x; }
-template <>
-__device__ __forceinline__ float to_float<__nv_bfloat16>(__nv_bfloat16 x) {
-  return __bfloat162float(x);
-}
-
-template <typename T>
+template <typename T, int D, int NS>
 __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_constant__ EliteArgs a) {
+  using G = TileGeom<T, D>;
   const Dev& p = a.p;
-  const int b = blockIdx.x, l = blockIdx.y;
-  const int u = l * p.B + b;
+  const int b = blockIdx.x, l = blockIdx.y, u = l * p.B + b;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  constexpr int kWarps = kEliteThreads / 32;
+  const int g4 = lane >> 2, c4 = lane & 3;
 
   Req R;
   if (!load_req(p, b, R)) {
     if (tid == 0) set_error(a.w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
     return;
   }
-  const int n_t = R.n_t, d = p.d, HC = a.head_chunk;
+  const int n_t = R.n_t;
+  const int hc = a.kv_chunk * p.g;  // heads per chunk
 
-  extern __shared__ float smem[];
-  float* qs = smem;                              // [h_q][d] last text query, fp32
-  float* P = qs + p.h_q * d;                     // [max_text] sum over heads of softmax rows
-  float* lg = P + p.max_text;                    // [HC][max_text] base-2 logits
-  float* hmax = lg + (size_t)HC * p.max_text;    // [HC]
-  float* hinv = hmax + HC;                       // [HC]
-  __shared__ float red[kWarps];
-  __shared__ int wcount[kWarps];
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* stages = smem;
+  float* lg = reinterpret_cast<float*>(smem + NS * G::kStageBytes);  // [hc][max_text]
+  float* P = lg + (size_t)hc * p.max_text;                          // [max_text]
+  float* hmax = P + p.max_text;                                      // [hc]
+  float* hinv = hmax + hc;                                           // [hc]
+  __shared__ float red[kEliteWarps];
+  __shared__ int wcount[kEliteWarps];
 
-  const T* qbase = reinterpret_cast<const T*>(a.lp.q[l]);
-  const T* qlast = qbase + (R.txt0 + n_t - 1) * p.q_stride_tok;
-  for (int i = tid; i < p.h_q * d; i += kEliteThreads) {
-    const int h = i / d, c = i % d;
-    qs[i] = to_float<T>(qlast[h * p.q_stride_head + c]);
-  }
+  const char* kbase = reinterpret_cast<const char*>(a.lp.k[l]);
+  const char* qbase = reinterpret_cast<const char*>(a.lp.q[l]);
   for (int j = tid; j < n_t; j += kEliteThreads) P[j] = 0.f;
-  __syncthreads();
 
-  const T* kbase = reinterpret_cast<const T*>(a.lp.k[l]);
-  for (int h0 = 0; h0 < p.h_q; h0 += HC) {
-    const int hc = min(HC, p.h_q - h0);
-    for (int i = tid; i < hc * n_t; i += kEliteThreads) {
-      const int hh = i / n_t, j = i % n_t;
-      const int h = h0 + hh;
-      const T* krow = kbase + (R.seq0 + R.n_v + j) * p.kv_stride_tok + (h / p.g) * p.kv_stride_head;
-      lg[(size_t)hh * p.max_text + j] = dot_row<T>(qs + h * d, krow, d) * p.scale_log2;
-    }
+  const int n_kt = (n_t + kTK - 1) / kTK;
+  const int n_rc = (p.g + kRC - 1) / kRC;
+  for (int kv0 = 0; kv0 < p.h_kv; kv0 += a.kv_chunk) {
+    const int kv1 = min(p.h_kv, kv0 + a.kv_chunk);
+    const int items = (kv1 - kv0) * n_rc * n_kt;
     __syncthreads();
-    for (int hh = warp; hh < hc; hh += kWarps) {
+#pragma unroll
+    for (int i = 0; i < NS - 1; ++i) {
+      if (i < items) load_item<T, D>(p, R, kbase, qbase, kv0, n_rc, n_kt, i, stages + i * G::kStageBytes);
+      cp_async_commit();
+    }
+    for (int i = 0; i < items; ++i) {
+      const int pre = i + NS - 1;
+      if (pre < items) load_item<T, D>(p, R, kbase, qbase, kv0, n_rc, n_kt, pre, stages + (pre % NS) * G::kStageBytes);
+      cp_async_commit();
+      cp_async_wait<NS - 1>();
+      __syncthreads();
+      const int per_kv = n_rc * n_kt;
+      const int kvh = kv0 + i / per_kv, rc = (i % per_kv) / n_kt, t = i % n_kt;
+      const int rows = min(kRC, p.g - rc * kRC);
+      const unsigned char* st = stages + (i % NS) * G::kStageBytes;
+      float acc[4][4];
+      TileLogits<T, D>::run(reinterpret_cast<const T*>(st), reinterpret_cast<const T*>(st + G::kKBytes), rows,
+                            p.scale_log2, warp, lane, acc);
+      const int kA = t * kTK + warp * 16 + g4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int row = 8 * j + 2 * c4 + e;
+          if (row < rows) {
+            const int hrow = (kvh - kv0) * p.g + rc * kRC + row;  // head within the chunk
+            float* lr = lg + (size_t)hrow * p.max_text;
+            if (kA < n_t) lr[kA] = acc[j][e];
+            if (kA + 8 < n_t) lr[kA + 8] = acc[j][2 + e];
+          }
+        }
+      __syncthreads();
+    }
+    cp_async_wait<0>();
+    // per-head softmax statistics
+    const int hcur = (kv1 - kv0) * p.g;
+    for (int hh = warp; hh < hcur; hh += kEliteWarps) {
       const float* row = lg + (size_t)hh * p.max_text;
       float m = -INFINITY;
       for (int j = lane; j < n_t; j += 32) m = fmaxf(m, row[j]);
@@ -127,12 +150,12 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
     }
     __syncthreads();
     for (int j = tid; j < n_t; j += kEliteThreads) {
-      float acc = P[j];
-      for (int hh = 0; hh < hc; ++hh) acc += exp2f(lg[(size_t)hh * p.max_text + j] - hmax[hh]) * hinv[hh];
-      P[j] = acc;
+      float accp = P[j];
+      for (int hh = 0; hh < hcur; ++hh) accp += exp2f(lg[(size_t)hh * p.max_text + j] - hmax[hh]) * hinv[hh];
+      P[j] = accp;
     }
-    __syncthreads();
   }
+  __syncthreads();
 
   // max P
   float m = -INFINITY;
@@ -143,7 +166,7 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
   __syncthreads();
   m = red[0];
 #pragma unroll
-  for (int i = 1; i < kWarps; ++i) m = fmaxf(m, red[i]);
+  for (int i = 1; i < kEliteWarps; ++i) m = fmaxf(m, red[i]);
   const float thr = (float)p.alpha * m;
 
   // ordered compaction of {j : P[j] >= thr}
@@ -159,7 +182,7 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
     __syncthreads();
     int wbase = 0, total = 0;
 #pragma unroll
-    for (int i = 0; i < kWarps; ++i) {
+    for (int i = 0; i < kEliteWarps; ++i) {
       wbase += (i < warp) ? wcount[i] : 0;
       total += wcount[i];
     }
@@ -167,35 +190,78 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
     if (take && pos < p.max_elite) out[pos] = j;
     base += total;
   }
+  // Gather the unit's elite query rows (row kvh*g*N_tk + hh*N_tk + e) and elite
+  // text keys into dense buffers: the scoring kernel then addresses them by
+  // arithmetic alone.
+  if (base <= p.max_elite) {
+    __syncthreads();  // the elite list written above is visible to the whole CTA
+    constexpr int kVec = TileGeom<T, D>::kRowBytes / 16;
+    const int n_tk = base;
+    const int rows_g = p.g * n_tk;
+    uint4* qdst = reinterpret_cast<uint4*>(a.w.qel) + (size_t)u * p.rows_max * kVec;
+    for (int i = tid; i < p.h_q * n_tk * kVec; i += kEliteThreads) {
+      const int r = i / kVec, v = i % kVec;
+      const int kvh = r / rows_g, rr = r % rows_g, hh = rr / n_tk, e = rr % n_tk;
+      const int pos = min(max(out[e], 0), n_t - 1);
+      const uint4* src = reinterpret_cast<const uint4*>(
+          qbase + ((R.txt0 + pos) * p.q_stride_tok + (int64_t)(kvh * p.g + hh) * p.q_stride_head) * sizeof(T));
+      qdst[(size_t)r * kVec + v] = __ldg(src + v);
+    }
+    uint4* kdst = reinterpret_cast<uint4*>(a.w.kel) + (size_t)u * p.h_kv * p.max_elite * kVec;
+    for (int i = tid; i < p.h_kv * n_tk * kVec; i += kEliteThreads) {
+      const int r = i / kVec, v = i % kVec;
+      const int kvh = r / n_tk, e = r % n_tk;
+      const int pos = min(max(out[e], 0), n_t - 1);
+      const uint4* src = reinterpret_cast<const uint4*>(
+          kbase + ((R.seq0 + R.n_v + pos) * p.kv_stride_tok + (int64_t)kvh * p.kv_stride_head) * sizeof(T));
+      kdst[((size_t)kvh * p.max_elite + e) * kVec + v] = __ldg(src + v);
+    }
+  }
   if (tid == 0) {
     a.w.n_tk[u] = base;
+    // the unit's layout, so that the scoring kernel resolves a work item with one load
+    a.w.uinfo[2 * u] = make_int4((int)R.seq0, (int)R.vis0, (int)R.txt0, R.n_v);
+    a.w.uinfo[2 * u + 1] = make_int4(R.n_t, base, 1, 0);
     if (base > p.max_elite) set_error(a.w.error, AIRCACHE_ERR_ELITE_OVERFLOW);
   }
+}
+
+template <typename T, int D>
+cudaError_t launch_t(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_t s) {
+  using G = TileGeom<T, D>;
+  EliteArgs a;
+  a.p = p;
+  a.lp = lp;
+  a.w = w;
+  // logits of kv_chunk KV heads + P + per-head stats next to NS stages
+  auto bytes = [&](int ns, int kvc) {
+    const size_t hc = (size_t)kvc * p.g;
+    return (size_t)ns * G::kStageBytes + sizeof(float) * (hc * p.max_text + p.max_text + 2 * hc);
+  };
+  int ns = 4;
+  if (bytes(4, p.h_kv) > (size_t)kSmemBudget) ns = 2;
+  int kvc = p.h_kv;
+  while (kvc > 1 && bytes(ns, kvc) > (size_t)kSmemBudget) --kvc;
+  a.kv_chunk = kvc;
+  const size_t smem = bytes(ns, kvc);
+  dim3 grid(p.B, p.L);
+  if (ns == 4) {
+    cudaFuncSetAttribute(elite_kernel<T, D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    elite_kernel<T, D, 4><<<grid, kEliteThreads, smem, s>>>(a);
+  } else {
+    cudaFuncSetAttribute(elite_kernel<T, D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    elite_kernel<T, D, 2><<<grid, kEliteThreads, smem, s>>>(a);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_elite(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_t s) {
-  EliteArgs a;
-  a.p = p;
-  a.lp = lp;
-  a.w = w;
-  const size_t budget = 96 * 1024;
-  const size_t fixed = sizeof(float) * ((size_t)p.h_q * p.d + p.max_text);
-  long long hc = (long long)((budget > fixed ? budget - fixed : 0) / sizeof(float)) / (p.max_text + 2);
-  if (hc < 1) hc = 1;
-  if (hc > p.h_q) hc = p.h_q;
-  a.head_chunk = (int)hc;
-  const size_t smem = fixed + sizeof(float) * (size_t)hc * (p.max_text + 2);
-  dim3 grid(p.B, p.L);
   if (p.dtype == AIRCACHE_BF16) {
-    cudaFuncSetAttribute(elite_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    elite_kernel<__nv_bfloat16><<<grid, kEliteThreads, smem, s>>>(a);
-  } else {
-    cudaFuncSetAttribute(elite_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    elite_kernel<float><<<grid, kEliteThreads, smem, s>>>(a);
+    return p.d == 128 ? launch_t<__nv_bfloat16, 128>(p, lp, w, s) : launch_t<__nv_bfloat16, 64>(p, lp, w, s);
   }
-  return cudaGetLastError();
+  return p.d == 128 ? launch_t<float, 128>(p, lp, w, s) : launch_t<float, 64>(p, lp, w, s);
 }
 
 }  // namespace aircache

@@ -11,20 +11,13 @@
 
 namespace aircache {
 
-constexpr int kTileKeys = 64;        // keys per score tile (4 warps x 16 keys)
-constexpr int kRowChunk = 32;        // query rows per score chunk (4 n8 MMA tiles)
-constexpr int kScoreThreads = 128;
-constexpr int kMaxTilesPerCta = 128; // bound on the pass-2 accumulator (128 x 64 fp32)
-constexpr int kTargetCtas = 1184;    // score grid target (8 x 148 SMs)
-constexpr long long kSpinLimit = 1LL << 26;  // bounded waits (iterations)
-
 // Device-visible description of one problem (host checks done).
 struct Dev {
   int L, B, h_q, h_kv, d, g, dtype;
   int max_visual, max_text, max_elite;
   int rows_max;          // h_q * max_elite: query rows per (layer, request)
-  int chunks;            // C: score CTAs per (layer, request)
-  int tiles_per_cta;     // ceil(tiles_max / C)
+  int rc_max;            // ceil(g * max_elite / 32): 32-row chunks per KV head
+  int lse_stride;        // h_kv * rc_max * 32: floats of row LSEs per (layer, request)
   int64_t total_tokens, total_visual, total_text;
   const int32_t* cu_seqlens;
   const int32_t* cu_visual;
@@ -44,12 +37,20 @@ struct LayerPtrs {
 struct Ws {
   int32_t* error;        // [1]
   uint32_t* cnt_all;     // [1]   requests whose budget is done
+  unsigned long long* ticket;  // [1] next pass-1 work item of the scoring kernel
   uint32_t* cnt_req;     // [B]   layers of a request whose stats are done
-  uint32_t* cnt_unit;    // [L*B] pass-1 CTAs done per (layer, request)
+  uint32_t* p2claim;     // [L*B] claimed pass-2 work items per (layer, request)
+  uint32_t* cnt_p1;      // [L*B] finished pass-1 items per (layer, request)
+  uint32_t* cnt_p2;      // [L*B] finished pass-2 items per (layer, request)
+  uint32_t* lse_ready;   // [L*B] row log-sum-exps published
   int32_t* elite;        // [L*B*max_text]
   int32_t* n_tk;         // [L*B]
-  float2* part;          // [L*B*C*rows_max] pass-1 row partials (max, sum), base 2
-  float* lse;            // [L*B*rows_max]   row log-sum-exp, base 2
+  int4* uinfo;           // [L*B][2] {seq0, vis0, txt0, N_v}, {N_t, N_tk, 1, 0} per (layer, request)
+  void* qel;             // [L*B][rows_max][D] elite query rows, row kvh*g*N_tk + hh*N_tk + e
+  void* kel;             // [L*B][h_kv][max_elite][D] elite text keys
+  float2* part;          // [L*B][TV+TT][rows_max] pass-1 (max, sum of exp2) per (tile, row)
+  float* lse;            // [L*B][h_kv][rc_max][32] row log-sum-exp, base 2
+  float* ivp;            // [G][L*total_visual] per-KV-group I_v partials (G > 1 only)
   float* iv;             // [L*total_visual]
   double* stats;         // [L*B*2]
   int32_t* keep;         // [L*B]
@@ -87,10 +88,23 @@ __device__ __forceinline__ bool load_req(const Dev& p, int b, Req& r) {
   return ok;
 }
 
+// Launch plan of the persistent scoring kernel.
+struct ScoreLaunch {
+  int TV, TT;      // visual / elite-text tile slots per unit
+  int G;           // KV-head groups per tile
+  int lag;         // units between a unit's two passes in the ticket order
+  int tail;        // 1: also stats, budgets and offsets
+  int grid;        // CTAs
+  int allow_tma;   // 1: use TMA tensor copies when the layout allows
+  long long tickets;
+  int64_t out_capacity;
+};
+ScoreLaunch plan_score(const Dev& p, int sms, bool tail, int64_t out_capacity);
+
 // Launchers (each returns cudaGetLastError() of its launches).
 cudaError_t launch_elite(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_t s);
-cudaError_t launch_score_pass1(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_t s);
-cudaError_t launch_score_pass2(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_t s);
+cudaError_t launch_score(const Dev& p, const LayerPtrs& lp, const Ws& w, const ScoreLaunch& L,
+                         cudaStream_t s);
 cudaError_t launch_stats_budget(const Dev& p, const Ws& w, double* stats_out,
                                 int64_t out_capacity, bool offsets, cudaStream_t s);
 cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s);

@@ -218,6 +218,45 @@ def test_strided_fused_kv_layout(A, oracle):
     full_check(A, oracle, wl)
 
 
+def _uneven_layers(t):
+    """Copies of the layers of a stacked [L, ...] tensor placed at unevenly spaced
+    offsets of one buffer (so no single layer stride describes them)."""
+    L, n = t.shape[0], t[0].numel()
+    offs = [l * n + 64 * l * l for l in range(L)]  # 64 elements: keeps 16-byte alignment
+    buf = torch.empty(offs[-1] + n, dtype=t.dtype, device=t.device)
+    return [buf[o:o + n].view(t.shape[1:]).copy_(t[l]) for l, o in enumerate(offs)]
+
+
+def test_unevenly_placed_layers(A, oracle):
+    """Per-layer K/V/Q at uneven addresses: the scoring kernel cannot use one
+    tensor map over the layers and copies its stages with cp.async instead."""
+    wl = custom_workload([700, 129], [25, 40], L=3, H_q=28, H_kv=4)
+    wl.q, wl.k, wl.v = _uneven_layers(wl.q), _uneven_layers(wl.k), _uneven_layers(wl.v)
+    full_check_lists(A, oracle, wl)
+
+
+def full_check_lists(A, oracle, wl):
+    """full_check for per-layer lists (the generator's stacked tensors replaced)."""
+    s = wl.spec
+    prob = A.Problem(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.cu_visual, max(s.n_visual), max(s.n_text),
+                     alpha=s.alpha, r=s.r, total_tokens=wl.k[0].shape[0], total_visual=sum(s.n_visual))
+    staged = run_staged(A, prob)
+    fused = run_fused(A, prob)
+    assert_same(staged, fused, prob)
+    stacked = W.Workload(s, torch.stack(wl.q), torch.stack(wl.k), torch.stack(wl.v), wl.cu_seqlens, wl.cu_visual)
+    cu_s, cu_v, _ = W.offsets(s)
+    report = {}
+    oiv = {}
+    for l in range(s.L):
+        for b in range(s.B):
+            oiv[(l, b)] = PU.check_unit(oracle, stacked, l, b, cu_s, cu_v, staged, report)
+    for b in range(s.B):
+        PU.check_request(oracle, stacked, b, cu_s, cu_v, staged, report, {l: oiv[(l, b)] for l in range(s.L)})
+        for l in range(s.L):
+            PU.check_compaction(oracle, stacked, l, b, cu_s, cu_v, staged)
+    return staged, report
+
+
 def test_device_errors_reported(A):
     wl = custom_workload([100, 50], [10, 8])
     s = wl.spec
