@@ -62,6 +62,7 @@ extern "C" {
 
 #define AIRCACHE_MAX_LAYERS 256
 #define AIRCACHE_MAX_TEXT 8192
+#define AIRCACHE_NOALLOC_MAX_UNITS 2048  /* L * B limit of aircache_budget_noalloc */
 
 typedef enum {
     AIRCACHE_OK = 0,
@@ -142,6 +143,39 @@ AIRCACHE_API int aircache_score(const aircache_problem* p, void* ws, size_t ws_b
  */
 AIRCACHE_API int aircache_budget(const aircache_problem* p, const float* iv, void* ws, size_t ws_bytes,
                     double* stats, int32_t* keep, void* stream);
+
+/*
+ * Step 3 without a workspace: the same strength, skewness and keep counts as
+ * aircache_budget, for callers that cannot hand the library device memory --
+ * for instance a serving engine that has given its whole memory pool to the
+ * KV cache and must not call the allocator between requests, so it has no
+ * aircache_workspace_size() bytes to pass.  The AirCache notes have no
+ * counterpart of this call; it only changes where the scratch lives.
+ *
+ * Scratch: a fixed 41,216-byte array in the library's own device memory (one
+ * per device, part of the loaded module): the error word, one arrival counter
+ * per request and the (s_t, s_k) of each (layer, request).  Nothing is
+ * allocated or freed.  The error word and the B counters must be zero when the
+ * kernel starts; the call zeroes them itself with an asynchronous memset on
+ * `stream` before its kernel.
+ * Limit: num_layers * num_requests <= AIRCACHE_NOALLOC_MAX_UNITS (2048); a
+ * larger problem returns AIRCACHE_ERR_UNSUPPORTED before anything is enqueued
+ * (use aircache_budget with a workspace instead).
+ * First call on a device: looks up the scratch address (cudaGetSymbolAddress,
+ * which may load the module) with that device current and caches it; make
+ * that first call before capturing any stream.  Later calls reuse the address.
+ * Concurrency: the scratch is shared by every call on the device in the
+ * process, so calls whose executions overlap (other streams, other host
+ * threads) race on it and give wrong results; order them on one stream or
+ * synchronise between them.
+ *   iv, stats, keep: as in aircache_budget (stats may be NULL).
+ *   device_status: NULL, or a device int32 that receives the device-side
+ *     status (AIRCACHE_OK or an AIRCACHE_ERR_DEVICE_* code) by a 4-byte
+ *     device-to-device copy enqueued after the kernel.
+ * Host-detected errors are returned as by aircache_budget.
+ */
+AIRCACHE_API int aircache_budget_noalloc(const aircache_problem* p, const float* iv, double* stats,
+                                         int32_t* keep, int32_t* device_status, void* stream);
 
 /*
  * Step 4a: top-keep selection.  For each (l, b) writes the keep[l*B+b] visual

@@ -88,6 +88,8 @@ def lib():
         L.aircache_score.restype = i32
         L.aircache_budget.argtypes = [P, vp, vp, sz, vp, vp, vp]
         L.aircache_budget.restype = i32
+        L.aircache_budget_noalloc.argtypes = [P, vp, vp, vp, vp, vp]
+        L.aircache_budget_noalloc.restype = i32
         L.aircache_select.argtypes = [P, vp, vp, vp, sz, vp, vp]
         L.aircache_select.restype = i32
         L.aircache_compact.argtypes = [P, vp, vp, vp, sz, vp, vp, vp, i64, vp]
@@ -224,6 +226,14 @@ def aircache_score(prob: Problem, ws, iv, elite, n_tk, stream=None):
 def aircache_budget(prob: Problem, iv, ws, stats, keep, stream=None):
     _check(lib().aircache_budget(prob.ref, _ptr(iv), _ptr(ws), ws.numel(), _ptr(stats), _ptr(keep),
                                  _stream(stream)), "aircache_budget")
+
+
+def aircache_budget_noalloc(prob: Problem, iv, stats, keep, device_status=None, stream=None):
+    """aircache_budget with the library's fixed device scratch instead of a
+    workspace (for callers that cannot allocate; at most
+    AIRCACHE_NOALLOC_MAX_UNITS layer-request pairs; calls must not overlap)."""
+    _check(lib().aircache_budget_noalloc(prob.ref, _ptr(iv), _ptr(stats), _ptr(keep), _ptr(device_status),
+                                         _stream(stream)), "aircache_budget_noalloc")
 
 
 def aircache_select(prob: Problem, iv, keep, ws, idx, stream=None):

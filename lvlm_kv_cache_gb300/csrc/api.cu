@@ -226,6 +226,15 @@ int aircache_budget(const aircache_problem* p, const float* iv, void* ws, size_t
   return AIRCACHE_OK;
 }
 
+int aircache_budget_noalloc(const aircache_problem* p, const float* iv, double* stats, int32_t* keep,
+                            int32_t* device_status, void* stream) {
+  int rc = validate(p);
+  if (rc != AIRCACHE_OK) return rc;
+  if (!iv || !keep) return AIRCACHE_ERR_INVALID_ARG;
+  if ((int64_t)p->num_layers * p->num_requests > AIRCACHE_NOALLOC_MAX_UNITS) return AIRCACHE_ERR_UNSUPPORTED;
+  return budget_noalloc(make_dev(p), iv, stats, keep, device_status, static_cast<cudaStream_t>(stream));
+}
+
 int aircache_select(const aircache_problem* p, const float* iv, const int32_t* keep, void* ws,
                     size_t ws_bytes, int32_t* idx, void* stream) {
   int rc = validate(p);

@@ -7,6 +7,9 @@
 // computes the same quantities at the tail of the scoring kernel with the same
 // device functions.  A separate one-CTA kernel writes the compacted-cache row
 // offsets for the staged compaction.
+#include <cstring>
+#include <mutex>
+
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "reduce.cuh"
@@ -78,7 +81,67 @@ __global__ void __launch_bounds__(kStatsThreads) offsets_kernel(const __grid_con
                                kBarAll);
 }
 
+// ---------------------------------------------------------------- fixed scratch
+// Scratch of aircache_budget_noalloc, part of the module's device memory: the
+// error word, one arrival counter per request and the (s_t, s_k) of every
+// (layer, request), for at most AIRCACHE_NOALLOC_MAX_UNITS layer-request pairs.
+// The error word and the counters must be 0 when the kernel starts; every call
+// clears them on its stream first.  One copy per device, shared by every call
+// in the process.
+constexpr size_t kNaCntOff = 256;
+constexpr size_t kNaStatsOff = kNaCntOff + sizeof(uint32_t) * AIRCACHE_NOALLOC_MAX_UNITS;
+constexpr size_t kNaBytes = kNaStatsOff + 2 * sizeof(double) * AIRCACHE_NOALLOC_MAX_UNITS;
+static_assert(kNaStatsOff % 256 == 0, "stats block alignment");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaBytes];
+
+constexpr int kNaMaxDevices = 64;
+std::mutex g_na_mutex;
+char* g_na_addr[kNaMaxDevices] = {};
+
+// Device address of the scratch on the current device; looked up once per
+// device (the lookup may load the module), then cached.
+int noalloc_scratch(char** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AIRCACHE_ERR_CUDA;
+  if (dev < 0 || dev >= kNaMaxDevices) return AIRCACHE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_na_mutex);
+  if (!g_na_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return AIRCACHE_ERR_CUDA;
+    g_na_addr[dev] = static_cast<char*>(ptr);
+  }
+  *out = g_na_addr[dev];
+  return AIRCACHE_OK;
+}
+
 }  // namespace
+
+int budget_noalloc(const Dev& p, const float* iv, double* stats_out, int32_t* keep, int32_t* device_status,
+                   cudaStream_t s) {
+  if ((long long)p.L * p.B > AIRCACHE_NOALLOC_MAX_UNITS) return AIRCACHE_ERR_UNSUPPORTED;
+  char* base = nullptr;
+  int rc = noalloc_scratch(&base);
+  if (rc != AIRCACHE_OK) return rc;
+  if (cudaMemsetAsync(base, 0, kNaCntOff + sizeof(uint32_t) * p.B, s) != cudaSuccess) return AIRCACHE_ERR_CUDA;
+  StatsArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.p = p;
+  a.w.error = reinterpret_cast<int32_t*>(base);
+  a.w.cnt_req = reinterpret_cast<uint32_t*>(base + kNaCntOff);
+  a.w.stats = reinterpret_cast<double*>(base + kNaStatsOff);
+  a.w.iv = const_cast<float*>(iv);
+  a.w.keep = keep;
+  a.stats_out = stats_out;
+  a.out_capacity = 0;
+  stats_budget_kernel<<<dim3(p.B, p.L), kStatsThreads, 0, s>>>(a);
+  if (cudaGetLastError() != cudaSuccess) return AIRCACHE_ERR_CUDA;
+  if (device_status &&
+      cudaMemcpyAsync(device_status, base, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess) {
+    return AIRCACHE_ERR_CUDA;
+  }
+  return AIRCACHE_OK;
+}
 
 cudaError_t launch_stats_budget(const Dev& p, const Ws& w, double* stats_out, int64_t out_capacity,
                                 bool offsets, cudaStream_t s) {

@@ -109,6 +109,10 @@ cudaError_t launch_stats_budget(const Dev& p, const Ws& w, double* stats_out,
                                 int64_t out_capacity, bool offsets, cudaStream_t s);
 cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s);
 cudaError_t launch_offsets(const Dev& p, const Ws& w, int64_t out_capacity, cudaStream_t s);
+// aircache_budget_noalloc after host validation: stats, budgets and the
+// optional device status copy, with the module's fixed scratch.
+int budget_noalloc(const Dev& p, const float* iv, double* stats_out, int32_t* keep, int32_t* device_status,
+                   cudaStream_t s);
 cudaError_t launch_compact(const Dev& p, const LayerPtrs& lp, const Ws& w, void* out_k,
                            void* out_v, int64_t capacity, cudaStream_t s);
 
