@@ -165,20 +165,28 @@ def unit_lengths(spec):
 
 def algorithmic_bytes(spec, n_tk, keep, esize):
     """Per-kernel algorithmic bytes of one compression (each input read once,
-    each output written once) and the whole-path total of the per-(request,
+    each output written once; intermediates such as stored logits and
+    partials are not counted) and the whole-path total of the per-(request,
     layer) formula 2*H_kv*D*(N_v+N_t) + 2*H_q*D*(1+N_tk) + 8*H_kv*D*(keep+N_t)
-    (bf16; esize-scaled) + the I_v workspace."""
+    (bf16; esize-scaled) + the I_v workspace.  bf16 units take the streaming
+    path (pass 1 reads the unit's keys and elite query rows; pass 2, or pass 2k
+    when g * N_tk > 32, writes I_v); other units the wide kernel."""
     row = spec.H_kv * spec.D * esize
     qrow = spec.H_q * spec.D * esize
-    k = {"elite_window": 0, "score_budget": 0, "select_topk": 0, "gather_compact": 0}
+    g = spec.H_q // spec.H_kv
+    k = {"elite_window": 0, "score_pass1": 0, "score_pass2": 0, "score_pass2k": 0, "score_wide": 0,
+         "select_topk": 0, "gather_compact": 0}
     path = 0
     for l in range(spec.L):
         for b, (nv, nt) in enumerate(unit_lengths(spec)):
             u = l * spec.B + b
             t, kp = int(n_tk[u]), int(keep[u])
             k["elite_window"] += nt * row + qrow + 4 * t
-            # K read once (the second pass is meant to hit L2), elite Q rows, I_v written
-            k["score_budget"] += (nv + t) * row + t * qrow + 4 * nv
+            if esize == 2:
+                k["score_pass1"] += (nv + t) * row + t * qrow
+                k["score_pass2" if g * t <= 32 else "score_pass2k"] += 4 * nv  # I_v written
+            else:
+                k["score_wide"] += (nv + t) * row + t * qrow + 4 * nv
             k["select_topk"] += 4 * nv + 4 * kp
             k["gather_compact"] += 2 * 2 * (kp + nt) * row + 4 * kp
             path += (nv + nt) * row + (1 + t) * qrow + 2 * 2 * (kp + nt) * row + 4 * nv * 3 + 8 * kp
@@ -340,7 +348,7 @@ def main():
 
     # ---- per-kernel durations on the launching stream
     nk = prob.launches()
-    names = A.kernel_names(nk)
+    names = A.kernel_names(prob)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     for row in ev:  # torch creates the CUDA event on first record
         for e in row:

@@ -219,7 +219,12 @@ AIRCACHE_API int aircache_get_error(const void* ws, void* stream, int32_t* statu
 /* Static description of a status code. */
 AIRCACHE_API const char* aircache_status_string(int status);
 
-/* Number of kernels one aircache_compress call launches (for launch accounting). */
+/*
+ * Number of kernels one aircache_compress call on `p` launches (for launch
+ * accounting), or -1 if `p` is invalid.  It depends on the scoring path, which
+ * the problem alone decides: bf16 inputs whose per-layer key pointers are
+ * evenly strided take the streaming path (6 kernels), others the wide path (4).
+ */
 AIRCACHE_API int aircache_compress_launches(const aircache_problem* p);
 
 /*
@@ -235,8 +240,8 @@ AIRCACHE_API int aircache_compress_profile(const aircache_problem* p, void* ws, 
                                            int64_t out_rows_capacity, int32_t* keep, int32_t* idx,
                                            float* iv, void* const* events, int n_events, void* stream);
 
-/* Name of kernel i (0-based, launch order) of aircache_compress, or NULL. */
-AIRCACHE_API const char* aircache_kernel_name(int i);
+/* Name of kernel i (0-based, launch order) of aircache_compress on `p`, or NULL. */
+AIRCACHE_API const char* aircache_kernel_name(const aircache_problem* p, int i);
 
 #ifdef __cplusplus
 }

@@ -105,7 +105,7 @@ def lib():
         L.aircache_compress_profile.argtypes = [P, vp, sz, vp, vp, vp, i64, vp, vp, vp,
                                                 ctypes.POINTER(ctypes.c_void_p), i32, vp]
         L.aircache_compress_profile.restype = i32
-        L.aircache_kernel_name.argtypes = [i32]
+        L.aircache_kernel_name.argtypes = [P, i32]
         L.aircache_kernel_name.restype = ctypes.c_char_p
         _lib = L
     return _lib
@@ -267,8 +267,10 @@ def aircache_compress_profile(prob: Problem, ws, out_k, out_v, out_offsets, keep
            "aircache_compress_profile")
 
 
-def kernel_names(n: int):
-    return [lib().aircache_kernel_name(i).decode() for i in range(n)]
+def kernel_names(prob: "Problem"):
+    """Names of the kernels one aircache_compress call on `prob` launches, in order."""
+    n = prob.launches()
+    return [lib().aircache_kernel_name(prob.ref, i).decode() for i in range(n)]
 
 
 def aircache_get_error(ws, stream=None) -> int:

@@ -5,15 +5,44 @@
 // aircache_get_error.
 #include <cmath>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "internal.cuh"
+
+namespace aircache {
+
+cudaError_t allow_smem(const void* func, int bytes) {
+  struct Entry {
+    const void* func;
+    int dev, bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& x : done) {
+    if (x.func == func && x.dev == dev && x.bytes >= bytes) return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.push_back(Entry{func, dev, bytes});
+  return e;
+}
+
+}  // namespace aircache
 
 using namespace aircache;
 
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kCompressKernels = 4;
+// Kernels of one aircache_compress call, by scoring path.
+const char* const kStreamKernels[] = {"elite_window", "score_pass1", "score_pass2", "score_pass2k",
+                                      "select_topk",  "gather_compact"};
+const char* const kWideKernels[] = {"elite_window", "score_wide", "select_topk", "gather_compact"};
+constexpr int kStreamCount = 6, kWideCount = 4;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -90,6 +119,9 @@ Dev make_dev(const aircache_problem* p) {
   d.alpha = p->alpha;
   d.r = p->r;
   d.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->head_dim));
+  const int tv = (d.max_visual + 127) / 128;
+  d.chn = (tv + kStreamTiles - 1) / kStreamTiles + 1;
+  d.stream_ok = 0;  // set per call from stream_eligible()
   return d;
 }
 
@@ -115,13 +147,16 @@ size_t carve(const Dev& d, char* base, Ws* w) {
   };
   Ws t;
   std::memset(&t, 0, sizeof t);
-  // zeroed block: error, cnt_all, ticket, cnt_req[B], cnt_p1/cnt_p2/lse_ready/p2claim[L*B]
-  const size_t zbytes = 16 + sizeof(uint32_t) * (d.B + 4 * LB);
+  // zeroed block: error, cnt_all, ticket, ticket_n, list_n[3], cnt_req[B],
+  // cnt_p1/cnt_p2/lse_ready/p2claim[L*B]
+  const size_t zbytes = 40 + sizeof(uint32_t) * (d.B + 4 * LB);
   char* zero = take(zbytes);
   t.error = reinterpret_cast<int32_t*>(zero);
   t.cnt_all = reinterpret_cast<uint32_t*>(zero ? zero + 4 : nullptr);
   t.ticket = reinterpret_cast<unsigned long long*>(zero ? zero + 8 : nullptr);
-  t.cnt_req = reinterpret_cast<uint32_t*>(zero ? zero + 16 : nullptr);
+  t.ticket_n = reinterpret_cast<unsigned long long*>(zero ? zero + 16 : nullptr);
+  t.list_n = reinterpret_cast<int32_t*>(zero ? zero + 24 : nullptr);
+  t.cnt_req = reinterpret_cast<uint32_t*>(zero ? zero + 40 : nullptr);
   t.cnt_p1 = t.cnt_req ? t.cnt_req + d.B : nullptr;
   t.cnt_p2 = t.cnt_p1 ? t.cnt_p1 + LB : nullptr;
   t.lse_ready = t.cnt_p2 ? t.cnt_p2 + LB : nullptr;
@@ -131,6 +166,14 @@ size_t carve(const Dev& d, char* base, Ws* w) {
   const size_t G = (size_t)(d.h_kv + 3) / 4;
   t.elite = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB * d.max_text));
   t.n_tk = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
+  t.stream_list = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
+  t.wide_list = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
+  t.multi_list = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
+  if (d.dtype == AIRCACHE_BF16) {  // the streaming path exists for bf16 only
+    const size_t kvrows = (size_t)d.L * d.h_kv;
+    t.lg = reinterpret_cast<float*>(take(sizeof(float) * kvrows * kRowChunk * d.total_visual));
+    t.part_s = reinterpret_cast<float2*>(take(sizeof(float2) * LB * d.h_kv * d.rc_max * kRowChunk * d.chn));
+  }
   t.uinfo = reinterpret_cast<int4*>(take(sizeof(int4) * 2 * LB));
   const size_t esz = d.dtype == AIRCACHE_BF16 ? 2 : 4;
   t.qel = take(esz * LB * d.rows_max * d.d);
@@ -165,6 +208,9 @@ int sm_count() {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) return 148;
   return sms;
 }
+
+// The scoring path of a validated problem (known on the host: see stream_eligible).
+bool stream_path(const aircache_problem* p) { return stream_eligible(make_dev(p), make_ptrs(p)); }
 
 int begin(const Ws& w, cudaStream_t s) {
   return cudaMemsetAsync(w.error, 0, w.zero_bytes, s) == cudaSuccess ? AIRCACHE_OK : AIRCACHE_ERR_CUDA;
@@ -203,9 +249,20 @@ int aircache_score(const aircache_problem* p, void* ws, size_t ws_bytes, float* 
   w.elite = elite;
   w.n_tk = n_tk;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int sms = sm_count();
+  Dev dn = d;
+  StreamMaps maps;
+  dn.stream_ok = stream_eligible(d, lp) ? 1 : 0;
+  if (dn.stream_ok && !encode_stream_maps(dn, lp, w, &maps)) return AIRCACHE_ERR_CUDA;
   if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
-  AC_TRY(launch_elite(d, lp, w, s));
-  AC_TRY(launch_score(d, lp, w, plan_score(d, sm_count(), false, 0), s));
+  AC_TRY(launch_elite(dn, lp, w, s));
+  if (dn.stream_ok) {
+    AC_TRY(launch_stream_p1(dn, maps, w, sms, s));
+    AC_TRY(launch_stream_p2(dn, w, false, 0, s));
+    AC_TRY(launch_stream_p2k(dn, maps, w, sms, false, 0, s));
+  } else {
+    AC_TRY(launch_score(dn, lp, w, plan_score(dn, sms, false, 0), s));
+  }
   return AIRCACHE_OK;
 }
 
@@ -283,9 +340,11 @@ static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, v
   if ((rc = check_ws(p, ws, ws_bytes)) != AIRCACHE_OK) return rc;
   if (!out_k || !out_v || !out_offsets || !keep || out_rows_capacity < 0) return AIRCACHE_ERR_INVALID_ARG;
   if (!aligned16(out_k) || !aligned16(out_v)) return AIRCACHE_ERR_INVALID_ARG;
-  if (events && n_events != kCompressKernels + 1) return AIRCACHE_ERR_INVALID_ARG;
   const Dev d = make_dev(p);
   const LayerPtrs lp = make_ptrs(p);
+  Dev dn = d;
+  dn.stream_ok = stream_eligible(d, lp) ? 1 : 0;
+  if (events && n_events != (dn.stream_ok ? kStreamCount : kWideCount) + 1) return AIRCACHE_ERR_INVALID_ARG;
   Ws w;
   carve(d, static_cast<char*>(ws), &w);
   w.keep = keep;
@@ -296,16 +355,29 @@ static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, v
   auto mark = [&](int i) {
     return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
   };
+  const int sms = sm_count();
+  StreamMaps maps;
+  if (dn.stream_ok && !encode_stream_maps(dn, lp, w, &maps)) return AIRCACHE_ERR_CUDA;
   if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
-  AC_TRY(mark(0));
-  AC_TRY(launch_elite(d, lp, w, s));
-  AC_TRY(mark(1));
-  AC_TRY(launch_score(d, lp, w, plan_score(d, sm_count(), true, out_rows_capacity), s));
-  AC_TRY(mark(2));
-  AC_TRY(launch_select(d, w, s));
-  AC_TRY(mark(3));
-  AC_TRY(launch_compact(d, lp, w, out_k, out_v, out_rows_capacity, s));
-  AC_TRY(mark(4));
+  int k = 0;
+  AC_TRY(mark(k++));
+  AC_TRY(launch_elite(dn, lp, w, s));
+  AC_TRY(mark(k++));
+  if (dn.stream_ok) {
+    AC_TRY(launch_stream_p1(dn, maps, w, sms, s));
+    AC_TRY(mark(k++));
+    AC_TRY(launch_stream_p2(dn, w, true, out_rows_capacity, s));
+    AC_TRY(mark(k++));
+    AC_TRY(launch_stream_p2k(dn, maps, w, sms, true, out_rows_capacity, s));
+    AC_TRY(mark(k++));
+  } else {
+    AC_TRY(launch_score(dn, lp, w, plan_score(dn, sms, true, out_rows_capacity), s));
+    AC_TRY(mark(k++));
+  }
+  AC_TRY(launch_select(dn, w, s));
+  AC_TRY(mark(k++));
+  AC_TRY(launch_compact(dn, lp, w, out_k, out_v, out_rows_capacity, s));
+  AC_TRY(mark(k++));
   return AIRCACHE_OK;
 }
 
@@ -325,15 +397,15 @@ int aircache_compress_profile(const aircache_problem* p, void* ws, size_t ws_byt
                        events, n_events, stream);
 }
 
-const char* aircache_kernel_name(int i) {
-  static const char* names[kCompressKernels] = {"elite_window", "score_budget", "select_topk",
-                                                "gather_compact"};
-  return (i >= 0 && i < kCompressKernels) ? names[i] : nullptr;
+const char* aircache_kernel_name(const aircache_problem* p, int i) {
+  if (validate(p) != AIRCACHE_OK) return nullptr;
+  if (stream_path(p)) return (i >= 0 && i < kStreamCount) ? kStreamKernels[i] : nullptr;
+  return (i >= 0 && i < kWideCount) ? kWideKernels[i] : nullptr;
 }
 
 int aircache_compress_launches(const aircache_problem* p) {
   if (validate(p) != AIRCACHE_OK) return -1;
-  return kCompressKernels;
+  return stream_path(p) ? kStreamCount : kWideCount;
 }
 
 int aircache_get_error(const void* ws, void* stream, int32_t* status) {

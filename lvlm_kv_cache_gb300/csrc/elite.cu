@@ -222,7 +222,17 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
     // the unit's layout, so that the scoring kernel resolves a work item with one load
     a.w.uinfo[2 * u] = make_int4((int)R.seq0, (int)R.vis0, (int)R.txt0, R.n_v);
     a.w.uinfo[2 * u + 1] = make_int4(R.n_t, base, 1, 0);
-    if (base > p.max_elite) set_error(a.w.error, AIRCACHE_ERR_ELITE_OVERFLOW);
+    if (base > p.max_elite) {
+      set_error(a.w.error, AIRCACHE_ERR_ELITE_OVERFLOW);
+    } else {
+      // route the unit to its scoring path
+      if (p.stream_ok) {
+        a.w.stream_list[atomicAdd(&a.w.list_n[0], 1)] = u;
+        if (p.g * base > kRowChunk) a.w.multi_list[atomicAdd(&a.w.list_n[2], 1)] = u;
+      } else {
+        a.w.wide_list[atomicAdd(&a.w.list_n[1], 1)] = u;
+      }
+    }
   }
 }
 
@@ -246,10 +256,12 @@ cudaError_t launch_t(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_
   const size_t smem = bytes(ns, kvc);
   dim3 grid(p.B, p.L);
   if (ns == 4) {
-    cudaFuncSetAttribute(elite_kernel<T, D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(elite_kernel<T, D, 4>), (int)smem);
+    if (e != cudaSuccess) return e;
     elite_kernel<T, D, 4><<<grid, kEliteThreads, smem, s>>>(a);
   } else {
-    cudaFuncSetAttribute(elite_kernel<T, D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(elite_kernel<T, D, 2>), (int)smem);
+    if (e != cudaSuccess) return e;
     elite_kernel<T, D, 2><<<grid, kEliteThreads, smem, s>>>(a);
   }
   return cudaGetLastError();

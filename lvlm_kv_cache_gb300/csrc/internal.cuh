@@ -3,6 +3,7 @@
 // the public ABI is include/aircache.h.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -24,7 +25,15 @@ struct Dev {
   int64_t q_stride_tok, q_stride_head, kv_stride_tok, kv_stride_head;
   double alpha, r;
   float scale_log2;      // log2(e) / sqrt(D): logits are kept in base 2
+  int stream_ok;         // 1: every unit takes the streaming scoring path (stream.cu)
+  int chn;               // streaming pass-1 chunks per (unit, KV head): visual chunks + 1 text chunk
 };
+
+// Streaming scoring path: query rows are taken in chunks of this many (a unit
+// with at most one chunk per KV head stores its logits), and a pass-1 work item
+// covers this many 128-key visual tiles.
+constexpr int kRowChunk = 32;
+constexpr int kStreamTiles = 4;
 
 struct LayerPtrs {
   const void* q[AIRCACHE_MAX_LAYERS];
@@ -37,7 +46,10 @@ struct LayerPtrs {
 struct Ws {
   int32_t* error;        // [1]
   uint32_t* cnt_all;     // [1]   requests whose budget is done
-  unsigned long long* ticket;  // [1] next pass-1 work item of the scoring kernel
+  unsigned long long* ticket;  // [1] next pass-1 work item of the wide scoring kernel
+  unsigned long long* ticket_n;  // [1] next pass-1 work item of the streaming path
+  int32_t* list_n;       // [3]   units on the streaming path / the wide path / the streaming
+                         //       path with more than one row chunk per KV head
   uint32_t* cnt_req;     // [B]   layers of a request whose stats are done
   uint32_t* p2claim;     // [L*B] claimed pass-2 work items per (layer, request)
   uint32_t* cnt_p1;      // [L*B] finished pass-1 items per (layer, request)
@@ -45,6 +57,11 @@ struct Ws {
   uint32_t* lse_ready;   // [L*B] row log-sum-exps published
   int32_t* elite;        // [L*B*max_text]
   int32_t* n_tk;         // [L*B]
+  int32_t* stream_list;  // [L*B] units u = l*B + b on the streaming path (list_n[0] of them, any order)
+  int32_t* wide_list;    // [L*B] units on the wide path (list_n[1] of them, any order)
+  int32_t* multi_list;   // [L*B] streaming units with g * N_tk > 32 (list_n[2] of them)
+  float* lg;             // [L][h_kv][32][total_visual] streaming path: logits of row r of KV head h
+  float2* part_s;        // [L*B][h_kv][rc_max*32][chn] streaming pass 1: (max, sum of exp2) per (row, chunk)
   int4* uinfo;           // [L*B][2] {seq0, vis0, txt0, N_v}, {N_t, N_tk, 1, 0} per (layer, request)
   void* qel;             // [L*B][rows_max][D] elite query rows, row kvh*g*N_tk + hh*N_tk + e
   void* kel;             // [L*B][h_kv][max_elite][D] elite text keys
@@ -108,6 +125,27 @@ cudaError_t launch_score(const Dev& p, const LayerPtrs& lp, const Ws& w, const S
 cudaError_t launch_stats_budget(const Dev& p, const Ws& w, double* stats_out,
                                 int64_t out_capacity, bool offsets, cudaStream_t s);
 cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s);
+// Streaming scoring path (stream.cu).  stream_eligible: the problem's dtype,
+// sizes and key layout allow it (bf16, per-layer key pointers evenly strided);
+// it depends on the problem alone, so the kernel sequence of a call is known on
+// the host.  Pass 1 streams the keys and produces row partials (and, for units
+// with one row chunk per KV head, their logits); pass 2 turns stored logits
+// into I_v and merges the other units' row LSEs; pass 2k recomputes those
+// units' logits from the keys.  With `tail`, the CTA completing a unit also
+// computes stats, budgets and offsets.
+struct StreamMaps {
+  CUtensorMap kmap, qmap, kelmap;
+};
+bool stream_eligible(const Dev& p, const LayerPtrs& lp);
+bool encode_stream_maps(const Dev& p, const LayerPtrs& lp, const Ws& w, StreamMaps* m);
+cudaError_t launch_stream_p1(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s);
+cudaError_t launch_stream_p2(const Dev& p, const Ws& w, bool tail, int64_t out_capacity, cudaStream_t s);
+cudaError_t launch_stream_p2k(const Dev& p, const StreamMaps& m, const Ws& w, int sms, bool tail,
+                              int64_t out_capacity, cudaStream_t s);
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for `func` on the current
+// device, skipped when an earlier call already allowed at least `bytes`.
+cudaError_t allow_smem(const void* func, int bytes);
 cudaError_t launch_offsets(const Dev& p, const Ws& w, int64_t out_capacity, cudaStream_t s);
 // aircache_budget_noalloc after host validation: stats, budgets and the
 // optional device status copy, with the module's fixed scratch.

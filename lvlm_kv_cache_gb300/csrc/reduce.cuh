@@ -78,17 +78,18 @@ __device__ __forceinline__ ff block_sum_ff(ff v, ff* red, int tix, int bar_id) {
 }
 
 // (s_t, s_k) of x[0..n) (n >= 3), computed by NT threads whose index within the
-// group is tix.  Returns the pair in every thread.
+// group is tix.  Returns the pair in every thread.  Each thread loads eight
+// values before it adds any, so a pass costs n / (8 NT) memory round trips.
 template <int NT>
 __device__ __forceinline__ double2 unit_moments(const float* x, int n, int tix, ff* red, int bar_id) {
-  // four independent accumulators per thread keep the float-float chains short
+  constexpr int V = 8;
   ff s4[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-  for (int i0 = tix; i0 < n; i0 += 4 * NT) {
+  for (int i0 = tix; i0 < n; i0 += V * NT) {
+    float v[V];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int i = i0 + q * NT;
-      if (i < n) s4[q] = ff_add(s4[q], ff{__ldcg(x + i), 0.f});
-    }
+    for (int q = 0; q < V; ++q) v[q] = (i0 + q * NT < n) ? __ldcg(x + i0 + q * NT) : 0.f;
+#pragma unroll
+    for (int q = 0; q < V; ++q) s4[q & 3] = ff_add(s4[q & 3], ff{v[q], 0.f});
   }
   ff s = ff_add(ff_add(s4[0], s4[1]), ff_add(s4[2], s4[3]));
   s = block_sum_ff<NT>(s, red, tix, bar_id);
@@ -96,16 +97,18 @@ __device__ __forceinline__ double2 unit_moments(const float* x, int n, int tix, 
   const ff mu = ff_from_double(s_t / n);
   ff m2q[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
   ff m3q[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-  for (int i0 = tix; i0 < n; i0 += 4 * NT) {
+  for (int i0 = tix; i0 < n; i0 += V * NT) {
+    float v[V];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int i = i0 + q * NT;
-      if (i < n) {
-        ff d = ff_two_sum(__ldcg(x + i), -mu.hi);
+    for (int q = 0; q < V; ++q) v[q] = (i0 + q * NT < n) ? __ldcg(x + i0 + q * NT) : 0.f;
+#pragma unroll
+    for (int q = 0; q < V; ++q) {
+      if (i0 + q * NT < n) {
+        ff d = ff_two_sum(v[q], -mu.hi);
         d = ff_two_sum(d.hi, __fsub_rn(d.lo, mu.lo));
         const ff d2 = ff_mul(d, d);
-        m2q[q] = ff_add(m2q[q], d2);
-        m3q[q] = ff_add(m3q[q], ff_mul(d2, d));
+        m2q[q & 3] = ff_add(m2q[q & 3], d2);
+        m3q[q & 3] = ff_add(m3q[q & 3], ff_mul(d2, d));
       }
     }
   }
@@ -130,17 +133,33 @@ template <int NT>
 __device__ __forceinline__ void request_budget(const Dev& p, int b, int n_v, const double* stats,
                                                int32_t* keep, double* sh, int tix, int bar_id) {
   if (tix == 0) {
-    double mean_st = 0.0, min_sk = INFINITY;
-    for (int l = 0; l < p.L; ++l) {
-      const int u = l * p.B + b;
-      mean_st = __dadd_rn(mean_st, __ldcg(&stats[2 * u]));
-      min_sk = fmin(min_sk, __ldcg(&stats[2 * u + 1]));
+    // loads are issued eight layers at a time; the sums still run in layer order
+    double mean_st = 0.0, min_sk = INFINITY, mean_u = 0.0;
+    for (int l0 = 0; l0 < p.L; l0 += 8) {
+      double st[8], sk[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int u = (l0 + q) * p.B + b;
+        st[q] = (l0 + q < p.L) ? __ldcg(&stats[2 * u]) : 0.0;
+        sk[q] = (l0 + q < p.L) ? __ldcg(&stats[2 * u + 1]) : INFINITY;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (l0 + q < p.L) {
+          mean_st = __dadd_rn(mean_st, st[q]);
+          min_sk = fmin(min_sk, sk[q]);
+        }
+      }
     }
     mean_st = __ddiv_rn(mean_st, (double)p.L);
-    double mean_u = 0.0;
-    for (int l = 0; l < p.L; ++l) {
-      const double sk = __ldcg(&stats[2 * (l * p.B + b) + 1]);
-      mean_u = __dadd_rn(mean_u, __dadd_rn(__dsub_rn(sk, min_sk), 1e-6));
+    for (int l0 = 0; l0 < p.L; l0 += 8) {
+      double sk[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sk[q] = (l0 + q < p.L) ? __ldcg(&stats[2 * ((l0 + q) * p.B + b) + 1]) : 0.0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (l0 + q < p.L) mean_u = __dadd_rn(mean_u, __dadd_rn(__dsub_rn(sk[q], min_sk), 1e-6));
+      }
     }
     sh[0] = mean_st;
     sh[1] = min_sk;

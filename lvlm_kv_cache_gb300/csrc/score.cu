@@ -53,6 +53,7 @@
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "reduce.cuh"
+#include "tmap.cuh"
 
 namespace aircache {
 namespace {
@@ -161,33 +162,6 @@ __device__ __forceinline__ bool wait_eq(const int* p, int v, long long limit) {
   return true;
 }
 
-__device__ __forceinline__ uint32_t swz(uint32_t slab, int row, int chunk) {
-  return slab + (uint32_t)(row * 128) + (uint32_t)((chunk ^ (row & 7)) << 4);
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-      "[%4];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
-      "%5}], [%6];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t r[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
 // ------------------------------------------------------------------ logits
 
 // acc[mt][nt][0..1]: query row 16mt + lane/4, keys 16*warp + 8nt + 2(lane%4) + {0,1};
@@ -275,8 +249,8 @@ struct Logits<float, D> {
 
 // ------------------------------------------------------------------ scheduler
 
-// Unit order index k (requests outermost) -> unit u = l*B + b.
-__device__ __forceinline__ int unit_of(const Dev& p, int k) { return (k % p.L) * p.B + k / p.L; }
+// Unit of position k of the wide-path list.
+__device__ __forceinline__ int unit_of(const Ws& w, int k) { return __ldcg(&w.wide_list[k]); }
 
 __device__ __forceinline__ bool unit_valid(const Dev& p, const int4& i0, const int4& i1) {
   const long long seq0 = i0.x, vis0 = i0.y, txt0 = i0.z;
@@ -291,7 +265,11 @@ __device__ __forceinline__ bool p1_item(const PArgs& a, long long t1, Item& it, 
   const Dev& p = a.p;
   const long long S1 = (long long)(a.TV + a.TT) * a.G;
   const int k = (int)(t1 / S1), slot = (int)(t1 % S1);
-  const int u = unit_of(p, k);
+  const int u = unit_of(a.w, k);
+  if (u < 0 || u >= p.L * p.B) {
+    bad = true;
+    return false;
+  }
   const int4 i0 = __ldcg(&a.w.uinfo[2 * u]);
   const int4 i1 = __ldcg(&a.w.uinfo[2 * u + 1]);
   if (!unit_valid(p, i0, i1)) {
@@ -305,8 +283,8 @@ __device__ __forceinline__ bool p1_item(const PArgs& a, long long t1, Item& it, 
   if (klim <= 0) return false;
   it.kind = kP1;
   it.u = u;
-  it.b = k / p.L;
-  it.l = k % p.L;
+  it.b = u % p.B;
+  it.l = u / p.B;
   it.tile = tile;
   it.grp = slot % a.G;
   it.text = text ? 1 : 0;
@@ -326,9 +304,10 @@ __device__ __forceinline__ bool p1_item(const PArgs& a, long long t1, Item& it, 
 // together so that their latencies overlap.
 __device__ void scheduler(const PArgs& a, Ctl* c) {
   const Dev& p = a.p;
-  const int U = p.L * p.B;
+  const int U = __ldcg(&a.w.list_n[1]);  // units on this path
+  const long long n_p1 = (long long)U * (a.TV + a.TT) * a.G;
   bool p1_done = false, stop = false;
-  int scan_k = 0, scan_u = unit_of(p, 0), scan_items = -1;
+  int scan_k = 0, scan_u = 0, scan_items = -1;
   int4 s0 = make_int4(0, 0, 0, 0), s1 = make_int4(0, 0, 0, 0);
   int qi = 0;
   long long wait0 = 0;
@@ -348,7 +327,11 @@ __device__ void scheduler(const PArgs& a, Ctl* c) {
   while (!stop) {
     if (*(volatile int32_t*)a.w.error != 0) break;
     if (scan_k < U && scan_items < 0) {
-      scan_u = unit_of(p, scan_k);
+      scan_u = unit_of(a.w, scan_k);
+      if (scan_u < 0 || scan_u >= p.L * p.B) {
+        set_error(a.w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+        break;
+      }
       s0 = __ldcg(&a.w.uinfo[2 * scan_u]);
       s1 = __ldcg(&a.w.uinfo[2 * scan_u + 1]);
       if (!unit_valid(p, s0, s1)) {
@@ -368,8 +351,8 @@ __device__ void scheduler(const PArgs& a, Ctl* c) {
         Item it{};
         it.kind = kP2;
         it.u = scan_u;
-        it.b = scan_k / p.L;
-        it.l = scan_k % p.L;
+        it.b = scan_u % p.B;
+        it.l = scan_u / p.B;
         it.tile = ci / a.G;
         it.grp = ci % a.G;
         it.text = 0;
@@ -388,7 +371,7 @@ __device__ void scheduler(const PArgs& a, Ctl* c) {
     }
     if (!p1_done) {
       for (int q = 0; q < 2; ++q) {
-        if (t1 + q >= a.n_p1) {
+        if (t1 + q >= n_p1) {
           p1_done = true;
           break;
         }
@@ -890,62 +873,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(const __grid_constan
 
 // ------------------------------------------------------------------ host
 
-PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess) {
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
-  }
-  return fn;
-}
-
-template <typename T>
-CUtensorMapDataType tma_type() {
-  return sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-}
-
-// A 2-D map over dense rows of D elements, box = (128 bytes, rows_box).
-template <typename T>
-bool encode_rows(CUtensorMap* m, const void* base, int d, long long rows, int rows_box) {
-  auto enc = encoder();
-  if (!enc || rows < 1) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)d * sizeof(T)};
-  cuuint32_t box[2] = {(cuuint32_t)(128 / sizeof(T)), (cuuint32_t)rows_box};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, tma_type<T>(), 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// The 4-D map over every layer's keys, if the per-layer pointers are evenly strided.
-template <typename T>
-bool encode_keys(CUtensorMap* m, const Dev& p, const LayerPtrs& lp) {
-  auto enc = encoder();
-  if (!enc) return false;
-  const char* k0 = reinterpret_cast<const char*>(lp.k[0]);
-  const long long lstride = (p.L > 1) ? (reinterpret_cast<const char*>(lp.k[1]) - k0) : 16;
-  if (lstride <= 0 || lstride % 16 != 0) return false;
-  for (int l = 2; l < p.L; ++l) {
-    if (reinterpret_cast<const char*>(lp.k[l]) - k0 != (long long)l * lstride) return false;
-  }
-  cuuint64_t dims[4] = {(cuuint64_t)p.d, (cuuint64_t)p.h_kv, (cuuint64_t)p.total_tokens, (cuuint64_t)p.L};
-  cuuint64_t strides[3] = {(cuuint64_t)p.kv_stride_head * sizeof(T), (cuuint64_t)p.kv_stride_tok * sizeof(T),
-                           (cuuint64_t)lstride};
-  cuuint32_t box[4] = {(cuuint32_t)(128 / sizeof(T)), 1, (cuuint32_t)kTK, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return enc(m, tma_type<T>(), 4, const_cast<char*>(k0), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename T, int D>
 cudaError_t launch_t(const Dev& p, const LayerPtrs& lp, const Ws& w, const ScoreLaunch& L, cudaStream_t s) {
   using Gm = Geo<T, D>;
@@ -961,13 +888,14 @@ cudaError_t launch_t(const Dev& p, const LayerPtrs& lp, const Ws& w, const Score
   a.n_p1 = L.tickets;
   a.out_capacity = L.out_capacity;
   const long long U = (long long)p.L * p.B;
-  a.tma = (L.allow_tma && encode_keys<T>(&a.kmap, p, lp) &&
+  a.tma = (L.allow_tma && encode_keys<T>(&a.kmap, p, lp, kTK) &&
            encode_rows<T>(&a.qmap, w.qel, p.d, U * p.rows_max, kRC) &&
            encode_rows<T>(&a.kelmap, w.kel, p.d, U * p.h_kv * p.max_elite, kTK))
               ? 1
               : 0;
   const int smem = Gm::kStages * Gm::kRing + kCtlBytes + 1024;
-  cudaFuncSetAttribute(score_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(score_kernel<T, D>), smem);
+  if (e != cudaSuccess) return e;
   score_kernel<T, D><<<L.grid, kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }

@@ -1,0 +1,774 @@
+// Cross-modal scores (AirCache notes, "Key design 1": equations A_vtk and I_v)
+// on the streaming path: bf16 inputs whose keys a TMA tensor map can address.
+//
+// Problem.  For one (layer l, request b) -- a "unit" -- the query rows are the
+// pairs (query head, elite text position): g * N_tk rows read each KV head
+// (g = H_q/H_kv).  Each row is a softmax over the N_v visual keys and the N_tk
+// elite text keys; I_v[i] is the mean over all H_q N_tk rows of the
+// probability of visual key i.  With an elite threshold near the notes'
+// alpha = 0.9 the window holds a few text tokens, so a unit has few rows and
+// many keys, and scoring is a stream over the keys.  Rows are taken in chunks
+// of 32 (one mma.sync M extent of two 16-row tiles).
+//
+// Pass 1 (score_pass1, persistent, one CTA per SM).  A work item is (unit, KV
+// head, chunk of four 128-key visual tiles) or (unit, KV head, the elite text
+// keys); it runs once per row chunk of the unit.  A producer thread claims
+// items from an atomic counter and moves each key tile into a shared-memory
+// ring with one TMA tensor copy per 128-byte column slab; the row chunk's
+// queries come with its first tile.  Eight consumer warps (16 keys each) hold
+// the chunk's queries in registers as mma.sync A fragments, compute the 32 x 128
+// logit tile (bf16 x bf16 -> fp32, base-2 logits), and keep a running (max, sum
+// of exp2) per row and thread; at the item's end the pairs are merged across
+// lanes and warps in a fixed order into one partial per (row, item).  A unit
+// with a single row chunk per KV head also writes its visual logits to a
+// row-major buffer (4 bytes per row and key: cheaper than reading the keys
+// again while rows <= 32; its keys are read once, with an L2 evict-first
+// policy).
+//
+// Pass 2 (score_pass2, one CTA per (unit, 256 keys)).  Single-chunk units:
+// each CTA merges the unit's row partials (chunk order) into row
+// log-sum-exps, then sums exp2(logit - lse) over every row of every KV head
+// for each of its keys.  Multi-chunk units: the first CTA of the unit merges
+// the row LSEs into the workspace for pass 2k.
+//
+// Pass 2k (score_pass2k, persistent).  Multi-chunk units: a work item is (unit,
+// key tile); for each KV head the tile is loaded once and its B fragments stay
+// in registers while that head's row chunks (queries + LSEs) stream through a
+// small TMA ring; per-key sums of exp2(logit - lse) over every row give the
+// tile's I_v directly.
+//
+// With `tail`, the CTA completing a unit also computes its (s_t, s_k) ("Key
+// design 2"), the one completing a request's last unit its keep counts, and
+// the last request the compacted-cache row offsets.
+#include <cstring>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "reduce.cuh"
+#include "tmap.cuh"
+
+namespace aircache {
+namespace {
+
+constexpr int kTK = 128;                  // keys per tile
+constexpr int kRC = kRowChunk;            // query rows per chunk
+constexpr int kCK = kStreamTiles;         // visual tiles per pass-1 item
+constexpr int kCW = 8;                    // consumer warps
+constexpr int kCT = kCW * 32;             // consumer threads
+constexpr int kThreads1 = kCT + 32;       // + the producer warp
+constexpr int kBarC = 1;                  // named barrier of the consumer threads
+constexpr int kT2 = 256;                  // pass-2 / pass-2k threads
+constexpr int kBarT = 1;                  // named barrier over all kT2 threads
+constexpr int kMaxStages = 12;
+constexpr int kNQ = 4;                    // pass-2k query-chunk ring
+
+enum : int { kEnd = 0, kVis = 1, kTxt = 2 };
+
+template <int D>
+struct SGeo {
+  static constexpr int kKS = D / 16;       // mma k-steps
+  static constexpr int kNH = D * 2 / 128;  // 128-byte slabs per bf16 row
+  static constexpr int kKSlab = kTK * 128;
+  static constexpr int kKBytes = kNH * kKSlab;
+  static constexpr int kQSlab = kRC * 128;
+  static constexpr int kQBytes = kNH * kQSlab;
+  // pass 1: key-tile ring, two query buffers, control
+  static constexpr int kStages = D == 128 ? 6 : 11;
+  static constexpr int kQOff = kStages * kKBytes;
+  static constexpr int kCtlOff = kQOff + 2 * kQBytes;
+  static_assert(kStages <= kMaxStages, "ring depth");
+  // pass 2k: one key tile, kNQ query chunks (+ their LSEs), control
+  static constexpr int kQ2 = (kQBytes + kRC * 4 + 1023) / 1024 * 1024;
+  static constexpr int kCtl2Off = kKBytes + kNQ * kQ2;
+};
+
+struct Hdr {
+  int kind, u, l, kvh, tile, klim, rows, r0, first, last, chunk, qbuf, store, pad;
+  long long vis0;
+};
+
+struct Ctl1 {
+  uint64_t full[kMaxStages], empty[kMaxStages], qempty[2];
+  Hdr hdr[kMaxStages];
+  float2 red[2][kCW][kRC];
+};
+
+struct SArgs {
+  CUtensorMap kmap;    // keys of every layer: (D, H_kv, tokens, layers), box 128 tokens
+  CUtensorMap qmap;    // gathered elite query rows (D, rows), box 32 rows
+  CUtensorMap kelmap;  // gathered elite text keys (D, rows), box 128 rows
+  Dev p;
+  Ws w;
+  int tail;
+  int64_t out_capacity;
+};
+
+__device__ __forceinline__ float2 merge_ms(float2 a, float2 b) {
+  const float m = fmaxf(a.x, b.x);
+  if (m == -INFINITY) return make_float2(-INFINITY, 0.f);
+  return make_float2(m, a.y * exp2f(a.x - m) + b.y * exp2f(b.x - m));
+}
+
+__device__ __forceinline__ bool stream_unit(const Dev& p, int u, const int4& i0, const int4& i1) {
+  const int n_v = i0.w, n_t = i1.x, n_tk = i1.y;
+  return u >= 0 && u < p.L * p.B && i1.z == 1 && n_tk >= 1 && n_tk <= n_t && n_tk <= p.max_elite &&
+         n_v >= 3 && n_v <= p.max_visual && i0.x >= 0 && (long long)i0.x + n_v + n_t <= p.total_tokens &&
+         i0.y >= 0 && (long long)i0.y + n_v <= p.total_visual;
+}
+
+__device__ __forceinline__ int rows_per_kv(const Dev& p) { return p.rc_max * kRC; }
+
+// Row partial (row, chunk) of KV head kvh of unit u.
+__device__ __forceinline__ size_t part_index(const Dev& p, int u, int kvh, int row, int chunk) {
+  return (((size_t)u * p.h_kv + kvh) * rows_per_kv(p) + row) * p.chn + chunk;
+}
+
+// Merge row `row`'s partials in chunk order (visual chunks, then the text chunk)
+// into its base-2 log-sum-exp.
+// (Loads are issued eight chunks at a time.)
+__device__ __forceinline__ float row_lse(const Dev& p, const Ws& w, int u, int kvh, int row, int chv) {
+  const float2* pr = w.part_s + part_index(p, u, kvh, row, 0);
+  float2 ms = make_float2(-INFINITY, 0.f);
+  for (int c0 = 0; c0 < chv; c0 += 8) {
+    float2 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = (c0 + q < chv) ? __ldcg(pr + c0 + q) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) ms = merge_ms(ms, v[q]);
+  }
+  ms = merge_ms(ms, __ldcg(pr + p.chn - 1));
+  return ms.x + log2f(ms.y);
+}
+
+// The end of a unit's scoring, run by every thread of a kT2-thread CTA once
+// the unit's I_v (at iv) is complete and visible: (s_t, s_k), then the
+// request's keep counts if this was its last unit, then the row offsets if
+// this was the last request.
+struct TailSmem {
+  ff redff[kT2 / 32];
+  double sh[4];
+  long long seg[kT2];
+  int flag;
+};
+
+__device__ void unit_tail(const SArgs& a, TailSmem& t, int u, int n_v, const float* iv) {
+  const Dev& p = a.p;
+  const Ws& w = a.w;
+  const int tid = threadIdx.x, b = u % p.B;
+  const double2 mo = unit_moments<kT2>(iv, n_v, tid, t.redff, kBarT);
+  if (tid == 0) {
+    w.stats[2 * u] = mo.x;
+    w.stats[2 * u + 1] = mo.y;
+    __threadfence();
+    t.flag = (atomicAdd(&w.cnt_req[b], 1u) == (unsigned)(p.L - 1)) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!t.flag) return;
+  __threadfence();
+  request_budget<kT2>(p, b, n_v, w.stats, w.keep, t.sh, tid, kBarT);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) t.flag = (atomicAdd(w.cnt_all, 1u) == (unsigned)(p.B - 1)) ? 1 : 0;
+  __syncthreads();
+  if (!t.flag) return;
+  __threadfence();
+  write_offsets<kT2>(p, w.keep, w.out_offsets, w.error, a.out_capacity, t.seg, tid, kBarT);
+}
+
+// ------------------------------------------------------------------ pass 1
+
+template <int D>
+__device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
+  using Gm = SGeo<D>;
+  constexpr int NS = Gm::kStages;
+  const Dev& p = a.p;
+  const Ws& w = a.w;
+  const uint32_t sbase = smem_u32(sm);
+  const long long per_unit = (long long)p.h_kv * p.chn;
+  const long long total = (long long)__ldcg(&w.list_n[0]) * per_unit;
+  const uint64_t evict_first = l2_evict_first_policy();
+  long long st = 0;  // stages issued
+  int sub = 0;       // row-chunk items issued (selects the query buffer)
+  bool ok = true;
+  long long claim = (long long)atomicAdd(w.ticket_n, 1ULL);
+  while (ok && claim < total) {
+    const long long next = (long long)atomicAdd(w.ticket_n, 1ULL);  // used at the loop's end
+    const int li = (int)(claim / per_unit);
+    const int rem = (int)(claim % per_unit);
+    const int kvh = rem / p.chn, ch = rem % p.chn;
+    const int u = __ldcg(&w.stream_list[li]);
+    const int4 i0 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u]) : make_int4(0, 0, 0, 0);
+    const int4 i1 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u + 1]) : make_int4(0, 0, 0, 0);
+    if (!stream_unit(p, u, i0, i1)) {
+      set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+      break;
+    }
+    const int n_v = i0.w, n_tk = i1.y, rows = p.g * n_tk;
+    const int n_rc = (rows + kRC - 1) / kRC;
+    const int tv = (n_v + kTK - 1) / kTK;
+    const int chv = (tv + kCK - 1) / kCK;
+    int kind, t0, nt;
+    if (ch < p.chn - 1) {
+      if (ch >= chv) {  // a chunk past this unit's keys
+        claim = next;
+        continue;
+      }
+      kind = kVis;
+      t0 = ch * kCK;
+      nt = min(kCK, tv - t0);
+    } else {
+      kind = kTxt;  // elite text keys: at most max_elite <= 8192, in tiles of 128
+      t0 = 0;
+      nt = (n_tk + kTK - 1) / kTK;
+    }
+    const int l = u / p.B;
+    for (int rc = 0; ok && rc < n_rc; ++rc, ++sub) {
+      const int qb = sub & 1;
+      // the query buffer is free once every consumer warp has loaded the chunk that used it before
+      if (!mbar_wait(&c->qempty[qb], (uint32_t)(((sub >> 1) & 1) ^ 1))) {
+        ok = false;
+        break;
+      }
+      for (int j = 0; j < nt; ++j, ++st) {
+        const int s = (int)(st % NS);
+        if (!mbar_wait(&c->empty[s], (uint32_t)(((st / NS) & 1) ^ 1))) {
+          ok = false;
+          break;
+        }
+        Hdr& h = c->hdr[s];
+        h.kind = kind;
+        h.u = u;
+        h.l = l;
+        h.kvh = kvh;
+        h.tile = t0 + j;
+        h.klim = kind == kVis ? min(kTK, n_v - (t0 + j) * kTK) : min(kTK, n_tk - (t0 + j) * kTK);
+        h.rows = min(kRC, rows - rc * kRC);
+        h.r0 = rc * kRC;
+        h.first = (j == 0);
+        h.last = (j == nt - 1);
+        h.chunk = ch;
+        h.qbuf = qb;
+        h.store = (kind == kVis && n_rc == 1) ? 1 : 0;
+        h.vis0 = i0.y;
+        mbar_arrive_expect_tx(&c->full[s], (uint32_t)(Gm::kKBytes + (j == 0 ? Gm::kQBytes : 0)));
+        const uint32_t kdst = sbase + (uint32_t)(s * Gm::kKBytes);
+#pragma unroll
+        for (int sl = 0; sl < Gm::kNH; ++sl) {
+          if (kind == kVis) {
+            if (n_rc == 1) {  // read once
+              tma_load_4d_hint(kdst + sl * Gm::kKSlab, &a.kmap, sl * 64, kvh, i0.x + (t0 + j) * kTK, l,
+                               &c->full[s], evict_first);
+            } else {  // read again by the next row chunk
+              tma_load_4d(kdst + sl * Gm::kKSlab, &a.kmap, sl * 64, kvh, i0.x + (t0 + j) * kTK, l, &c->full[s]);
+            }
+          } else {
+            tma_load_2d(kdst + sl * Gm::kKSlab, &a.kelmap, sl * 64,
+                        (u * p.h_kv + kvh) * p.max_elite + (t0 + j) * kTK, &c->full[s]);
+          }
+        }
+        if (j == 0) {
+          const uint32_t qdst = sbase + (uint32_t)(Gm::kQOff + qb * Gm::kQBytes);
+#pragma unroll
+          for (int sl = 0; sl < Gm::kNH; ++sl) {
+            tma_load_2d(qdst + sl * Gm::kQSlab, &a.qmap, sl * 64, u * p.rows_max + kvh * rows + rc * kRC,
+                        &c->full[s]);
+          }
+        }
+      }
+    }
+    claim = next;
+  }
+  if (!ok) {
+    set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+    return;  // consumers give up on their own (longer) wait
+  }
+  const int s = (int)(st % NS);
+  if (!mbar_wait(&c->empty[s], (uint32_t)(((st / NS) & 1) ^ 1))) {
+    set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+    return;
+  }
+  c->hdr[s].kind = kEnd;
+  mbar_arrive(&c->full[s]);
+}
+
+template <int D>
+__device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
+  using Gm = SGeo<D>;
+  constexpr int NS = Gm::kStages;
+  constexpr int KS = Gm::kKS;
+  const Dev& p = a.p;
+  const Ws& w = a.w;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g4 = lane >> 2, c4 = lane & 3;
+  const uint32_t sbase = smem_u32(sm);
+  // ldmatrix lane roles: key rows as the B operand, query rows as the A operand
+  const int kr = 16 * warp + (lane & 7) + 8 * (lane >> 4);
+  const int kc = (lane >> 3) & 1;
+  const int qr = lane & 15, qc = lane >> 4;
+  const float scale = p.scale_log2;
+  const long long TV = p.total_visual;
+  uint32_t qf[2][KS][4];
+  float m_run[2][2], s_run[2][2];
+  int mts = 1, par = 0;
+  for (long long it = 0;; ++it) {
+    const int s = (int)(it % NS);
+    if (!mbar_wait(&c->full[s], (uint32_t)((it / NS) & 1), 8 * kWaitCycles)) {
+      if (lane == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    const Hdr h = c->hdr[s];
+    if (h.kind == kEnd) return;
+    if (h.first) {
+      mts = h.rows > 16 ? 2 : 1;
+      const uint32_t qs = sbase + (uint32_t)(Gm::kQOff + h.qbuf * Gm::kQBytes);
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const int slab = kk >> 2, c0 = (kk & 3) * 2;
+        ldsm_x4(qf[0][kk], swz(qs + slab * Gm::kQSlab, qr, c0 + qc));
+        if (mts > 1) ldsm_x4(qf[1][kk], swz(qs + slab * Gm::kQSlab, 16 + qr, c0 + qc));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c->qempty[h.qbuf]);
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          m_run[mt][hh] = -INFINITY;
+          s_run[mt][hh] = 0.f;
+        }
+    }
+    float acc[2][2][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
+    const uint32_t ks = sbase + (uint32_t)(s * Gm::kKBytes);
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      const int slab = kk >> 2, c0 = (kk & 3) * 2;
+      uint32_t b[4];
+      ldsm_x4(b, swz(ks + slab * Gm::kKSlab, kr, c0 + kc));
+      mma_bf16_16816(acc[0][0], qf[0][kk], b[0], b[1]);
+      mma_bf16_16816(acc[0][1], qf[0][kk], b[2], b[3]);
+      if (mts > 1) {
+        mma_bf16_16816(acc[1][0], qf[1][kk], b[0], b[1]);
+        mma_bf16_16816(acc[1][1], qf[1][kk], b[2], b[3]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c->empty[s]);  // the tile is read: the producer may refill it
+
+    // epilogue: store logits (single-chunk units), update the running pairs
+    float* lbase = nullptr;
+    if (h.store) lbase = w.lg + ((size_t)h.l * p.h_kv + h.kvh) * kRC * TV + h.vis0 + (long long)h.tile * kTK;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      if (mt < mts) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int row = 16 * mt + g4 + 8 * hh;
+          if (row < h.rows) {
+            float v[4];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int key = 16 * warp + 8 * nt + 2 * c4 + e;
+                const float x = acc[mt][nt][2 * hh + e] * scale;
+                v[2 * nt + e] = key < h.klim ? x : -INFINITY;
+                mx = fmaxf(mx, v[2 * nt + e]);
+                if (lbase && key < h.klim) lbase[(size_t)row * TV + key] = x;
+              }
+            const float mn = fmaxf(m_run[mt][hh], mx);
+            if (mn != -INFINITY) {
+              float sum = s_run[mt][hh] * exp2f(m_run[mt][hh] - mn);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) sum += exp2f(v[q] - mn);
+              s_run[mt][hh] = sum;
+              m_run[mt][hh] = mn;
+            }
+          }
+        }
+      }
+    }
+    if (h.last) {
+      // merge the item's running pairs: the four lanes of a row, then the warps in order
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float2 ms = make_float2(m_run[mt][hh], s_run[mt][hh]);
+#pragma unroll
+          for (int o = 1; o <= 2; o <<= 1) {
+            const float2 other =
+                make_float2(__shfl_xor_sync(0xffffffffu, ms.x, o), __shfl_xor_sync(0xffffffffu, ms.y, o));
+            ms = merge_ms(ms, other);
+          }
+          if (c4 == 0) c->red[par][warp][16 * mt + g4 + 8 * hh] = ms;
+        }
+      named_bar_sync(kBarC, kCT);
+      if (warp == 0 && lane < h.rows) {
+        float2 ms = c->red[par][0][lane];
+#pragma unroll
+        for (int ww = 1; ww < kCW; ++ww) ms = merge_ms(ms, c->red[par][ww][lane]);
+        w.part_s[part_index(p, h.u, h.kvh, h.r0 + lane, h.chunk)] = ms;
+      }
+      par ^= 1;
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads1, 1) stream_p1_kernel(const __grid_constant__ SArgs a) {
+  using Gm = SGeo<D>;
+  extern __shared__ unsigned char smem_raw[];
+  // tiles need 1024-byte alignment (the 128-byte swizzle repeats every 8 rows)
+  unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  Ctl1* c = reinterpret_cast<Ctl1*>(sm + Gm::kCtlOff);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Gm::kStages; ++s) {
+      mbar_init(&c->full[s], 1);
+      mbar_init(&c->empty[s], kCW);
+    }
+    mbar_init(&c->qempty[0], kCW);
+    mbar_init(&c->qempty[1], kCW);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (*(volatile int32_t*)a.w.error != 0) return;  // an earlier kernel reported an error
+  if (threadIdx.x < kCT) {
+    p1_consumers<D>(a, c, sm);
+  } else if (threadIdx.x == kCT) {
+    p1_producer<D>(a, c, sm);
+  }
+}
+
+// ------------------------------------------------------------------ pass 2
+
+__global__ void __launch_bounds__(kT2) stream_p2_kernel(const __grid_constant__ SArgs a) {
+  const Dev& p = a.p;
+  const Ws& w = a.w;
+  extern __shared__ float lse_s[];  // [h_kv][32]
+  __shared__ TailSmem t;
+  const int tid = threadIdx.x;
+  if (*(volatile int32_t*)w.error != 0) return;
+  const int li = blockIdx.x;
+  if (li >= __ldcg(&w.list_n[0])) return;
+  const int u = __ldcg(&w.stream_list[li]);
+  const int4 i0 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u]) : make_int4(0, 0, 0, 0);
+  const int4 i1 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u + 1]) : make_int4(0, 0, 0, 0);
+  if (!stream_unit(p, u, i0, i1)) {
+    if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int n_v = i0.w, n_tk = i1.y, rows = p.g * n_tk;
+  const int tv = (n_v + kTK - 1) / kTK;
+  const int chv = (tv + kCK - 1) / kCK;
+  if (rows > kRC) {
+    // several row chunks: publish the row LSEs for pass 2k (first CTA of the unit)
+    if (blockIdx.y != 0) return;
+    float* lse_u = w.lse + (size_t)u * p.lse_stride;
+    for (int q = tid; q < p.h_kv * rows; q += kT2) {
+      const int kvh = q / rows, r = q % rows;
+      lse_u[kvh * rows_per_kv(p) + r] = row_lse(p, w, u, kvh, r, chv);
+    }
+    return;
+  }
+  const int k0 = blockIdx.y * kT2;
+  if (k0 >= n_v) return;
+  const int l = u / p.B;
+  for (int q = tid; q < p.h_kv * rows; q += kT2) {
+    const int kvh = q / rows, r = q % rows;
+    lse_s[kvh * kRC + r] = row_lse(p, w, u, kvh, r, chv);
+  }
+  __syncthreads();
+  const long long TV = p.total_visual;
+  const int key = k0 + tid;
+  float* iv = w.iv + (size_t)l * TV + i0.y;
+  if (key < n_v) {
+    const float* col = w.lg + (size_t)l * p.h_kv * kRC * TV + i0.y + key;
+    float acc = 0.f;
+    for (int kvh = 0; kvh < p.h_kv; ++kvh) {
+      const float* ch = col + (size_t)kvh * kRC * TV;
+      const float* ls = lse_s + kvh * kRC;
+      int r = 0;
+      for (; r + 8 <= rows; r += 8) {
+        float x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) x[q] = __ldcg(ch + (size_t)(r + q) * TV);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc += exp2f(x[q] - ls[r + q]);
+      }
+      for (; r < rows; ++r) acc += exp2f(__ldcg(ch + (size_t)r * TV) - ls[r]);
+    }
+    iv[key] = acc / (float)(p.h_q * n_tk);
+    __threadfence();
+  }
+  if (!a.tail) return;
+  // the CTA completing the unit finishes it
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned blocks = (unsigned)((n_v + kT2 - 1) / kT2);
+    t.flag = (atomicAdd(&w.cnt_p2[u], 1u) == blocks - 1u) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!t.flag) return;
+  __threadfence();
+  unit_tail(a, t, u, n_v, iv);
+}
+
+// ------------------------------------------------------------------ pass 2k
+
+struct Ctl2 {
+  uint64_t kfull, qfull[kNQ];
+  int flag;
+};
+
+// Multi-chunk units.  Item = (unit, key tile): for each KV head in turn the
+// key tile's B fragments are loaded into registers (the buffer is refilled
+// with the next head's tile at once), and the head's row chunks stream through
+// a ring of query chunks with their LSEs.  Each thread sums exp2(logit - lse)
+// for its four keys over every row it sees; a reduction over the lanes that
+// share those keys gives the tile's final I_v.
+template <int D>
+__global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constant__ SArgs a) {
+  using Gm = SGeo<D>;
+  constexpr int KS = Gm::kKS;
+  const Dev& p = a.p;
+  const Ws& w = a.w;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  Ctl2* c = reinterpret_cast<Ctl2*>(sm + Gm::kCtl2Off);
+  __shared__ TailSmem t;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g4 = lane >> 2, c4 = lane & 3;
+  const uint32_t sbase = smem_u32(sm);
+  if (tid == 0) {
+    mbar_init(&c->kfull, 1);
+    for (int i = 0; i < kNQ; ++i) mbar_init(&c->qfull[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (*(volatile int32_t*)w.error != 0) return;
+  const int TVmax = (p.max_visual + kTK - 1) / kTK;
+  const long long total = (long long)__ldcg(&w.list_n[2]) * TVmax;
+  const int kr = 16 * warp + (lane & 7) + 8 * (lane >> 4);
+  const int kc = (lane >> 3) & 1;
+  const int qr = lane & 15, qc = lane >> 4;
+  const float scale = p.scale_log2;
+  const long long TV = p.total_visual;
+  uint32_t kph = 0;  // key-tile barrier phase
+  long long qn = 0;  // query chunks consumed (ring position)
+  if (tid == 0) fence_proxy_async_global();  // LSEs were written by the previous kernel's generic stores
+  for (long long item = blockIdx.x; item < total; item += gridDim.x) {
+    const int li = (int)(item / TVmax), tile = (int)(item % TVmax);
+    const int u = __ldcg(&w.multi_list[li]);
+    const int4 i0 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u]) : make_int4(0, 0, 0, 0);
+    const int4 i1 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u + 1]) : make_int4(0, 0, 0, 0);
+    if (!stream_unit(p, u, i0, i1)) {
+      if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+      return;
+    }
+    const int n_v = i0.w, n_tk = i1.y, rows = p.g * n_tk;
+    const int tv = (n_v + kTK - 1) / kTK;
+    if (tile >= tv) continue;  // a tile past this unit's keys (same verdict in every thread)
+    const int n_rc = (rows + kRC - 1) / kRC;
+    const int steps = p.h_kv * n_rc;  // (KV head, row chunk) pairs, head-major
+    const int l = u / p.B;
+    const int klim = min(kTK, n_v - tile * kTK);
+    auto issue_k = [&](int kvh) {
+      mbar_arrive_expect_tx(&c->kfull, (uint32_t)Gm::kKBytes);
+#pragma unroll
+      for (int sl = 0; sl < Gm::kNH; ++sl) {
+        tma_load_4d(sbase + sl * Gm::kKSlab, &a.kmap, sl * 64, kvh, i0.x + tile * kTK, l, &c->kfull);
+      }
+    };
+    auto issue_q = [&](int step, long long pos) {
+      const int kvh = step / n_rc, rc = step % n_rc;
+      const int slot = (int)(pos % kNQ);
+      const uint32_t qdst = sbase + (uint32_t)(Gm::kKBytes + slot * Gm::kQ2);
+      mbar_arrive_expect_tx(&c->qfull[slot], (uint32_t)(Gm::kQBytes + kRC * 4));
+#pragma unroll
+      for (int sl = 0; sl < Gm::kNH; ++sl) {
+        tma_load_2d(qdst + sl * Gm::kQSlab, &a.qmap, sl * 64, u * p.rows_max + kvh * rows + rc * kRC,
+                    &c->qfull[slot]);
+      }
+      const float* lse = w.lse + (size_t)u * p.lse_stride + (size_t)kvh * rows_per_kv(p) + rc * kRC;
+      bulk_g2s(sm + Gm::kKBytes + slot * Gm::kQ2 + Gm::kQBytes, lse, kRC * 4, &c->qfull[slot]);
+    };
+    if (tid == 0) {
+      issue_k(0);
+      for (int st = 0; st < min(steps, kNQ); ++st) issue_q(st, qn + st);
+    }
+    float accK[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    int step = 0;
+    for (int kvh = 0; kvh < p.h_kv; ++kvh) {
+      if (!mbar_wait(&c->kfull, kph, 4 * kWaitCycles)) {
+        if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+        return;
+      }
+      kph ^= 1;
+      uint32_t kf[KS][4];
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const int slab = kk >> 2, c0 = (kk & 3) * 2;
+        ldsm_x4(kf[kk], swz(sbase + slab * Gm::kKSlab, kr, c0 + kc));
+      }
+      __syncthreads();  // the key buffer is free again
+      if (tid == 0 && kvh + 1 < p.h_kv) issue_k(kvh + 1);
+      for (int rc = 0; rc < n_rc; ++rc, ++qn, ++step) {
+        const int slot = (int)(qn % kNQ);
+        if (!mbar_wait(&c->qfull[slot], (uint32_t)((qn / kNQ) & 1), 4 * kWaitCycles)) {
+          if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+          return;
+        }
+        const int rows_c = min(kRC, rows - rc * kRC);
+        const uint32_t qs = sbase + (uint32_t)(Gm::kKBytes + slot * Gm::kQ2);
+        const float* ls = reinterpret_cast<const float*>(sm + Gm::kKBytes + slot * Gm::kQ2 + Gm::kQBytes);
+        float acc[2][2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
+        const int mts = rows_c > 16 ? 2 : 1;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const int slab = kk >> 2, c0 = (kk & 3) * 2;
+          uint32_t qa[4];
+          ldsm_x4(qa, swz(qs + slab * Gm::kQSlab, qr, c0 + qc));
+          mma_bf16_16816(acc[0][0], qa, kf[kk][0], kf[kk][1]);
+          mma_bf16_16816(acc[0][1], qa, kf[kk][2], kf[kk][3]);
+          if (mts > 1) {
+            ldsm_x4(qa, swz(qs + slab * Gm::kQSlab, 16 + qr, c0 + qc));
+            mma_bf16_16816(acc[1][0], qa, kf[kk][0], kf[kk][1]);
+            mma_bf16_16816(acc[1][1], qa, kf[kk][2], kf[kk][3]);
+          }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int row = 16 * mt + g4 + 8 * hh;
+            if (mt < mts && row < rows_c) {
+              const float lse = ls[row];
+#pragma unroll
+              for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) accK[nt][e] += exp2f(acc[mt][nt][2 * hh + e] * scale - lse);
+            }
+          }
+        __syncthreads();  // every thread is done with the slot
+        if (tid == 0 && step + kNQ < steps) issue_q(step + kNQ, qn + kNQ);
+      }
+    }
+    // per key: the sum over every row (lanes with the same c4 hold the same keys)
+    float* iv = w.iv + (size_t)l * TV + i0.y;
+    const float denom = (float)(p.h_q * n_tk);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float v = accK[nt][e];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        const int key = 16 * warp + 8 * nt + 2 * c4 + e;
+        if (g4 == 0 && key < klim) iv[(long long)tile * kTK + key] = v / denom;
+      }
+    if (!a.tail) continue;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) c->flag = (atomicAdd(&w.cnt_p2[u], 1u) == (unsigned)(tv - 1)) ? 1 : 0;
+    __syncthreads();
+    if (c->flag) {
+      __threadfence();
+      unit_tail(a, t, u, n_v, iv);  // this CTA completed the unit
+    }
+    __syncthreads();
+  }
+}
+
+template <int D>
+cudaError_t launch_p1_t(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s) {
+  using Gm = SGeo<D>;
+  SArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.kmap = m.kmap;
+  a.qmap = m.qmap;
+  a.kelmap = m.kelmap;
+  a.p = p;
+  a.w = w;
+  const int smem = Gm::kCtlOff + (int)sizeof(Ctl1) + 1024;
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(stream_p1_kernel<D>), smem);
+  if (e != cudaSuccess) return e;
+  stream_p1_kernel<D><<<sms, kThreads1, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_p2k_t(const Dev& p, const StreamMaps& m, const Ws& w, int sms, bool tail,
+                         int64_t out_capacity, cudaStream_t s) {
+  using Gm = SGeo<D>;
+  SArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.kmap = m.kmap;
+  a.qmap = m.qmap;
+  a.p = p;
+  a.w = w;
+  a.tail = tail ? 1 : 0;
+  a.out_capacity = out_capacity;
+  const int smem = Gm::kCtl2Off + (int)sizeof(Ctl2) + 1024;
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(stream_p2k_kernel<D>), smem);
+  if (e != cudaSuccess) return e;
+  stream_p2k_kernel<D><<<2 * sms, kT2, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool stream_eligible(const Dev& p, const LayerPtrs& lp) {
+  if (p.dtype != AIRCACHE_BF16 || (p.d != 64 && p.d != 128)) return false;
+  if ((p.max_visual + kT2 - 1) / kT2 > 65535 || p.h_kv * kRC * (int)sizeof(float) > 48 * 1024) return false;
+  const long long U = (long long)p.L * p.B;
+  if (U * p.rows_max + kRC > INT32_MAX || U * p.h_kv * p.max_elite + kTK > INT32_MAX) {
+    return false;  // TMA row coordinates are 32-bit
+  }
+  CUtensorMap m;
+  return encode_keys<__nv_bfloat16>(&m, p, lp, kTK);
+}
+
+bool encode_stream_maps(const Dev& p, const LayerPtrs& lp, const Ws& w, StreamMaps* m) {
+  const long long U = (long long)p.L * p.B;
+  return w.lg && w.part_s && encode_keys<__nv_bfloat16>(&m->kmap, p, lp, kTK) &&
+         encode_rows<__nv_bfloat16>(&m->qmap, w.qel, p.d, U * p.rows_max, kRC) &&
+         encode_rows<__nv_bfloat16>(&m->kelmap, w.kel, p.d, U * p.h_kv * p.max_elite, kTK);
+}
+
+cudaError_t launch_stream_p1(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s) {
+  return p.d == 128 ? launch_p1_t<128>(p, m, w, sms, s) : launch_p1_t<64>(p, m, w, sms, s);
+}
+
+cudaError_t launch_stream_p2(const Dev& p, const Ws& w, bool tail, int64_t out_capacity, cudaStream_t s) {
+  SArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.p = p;
+  a.w = w;
+  a.tail = tail ? 1 : 0;
+  a.out_capacity = out_capacity;
+  const dim3 grid((unsigned)(p.L * p.B), (unsigned)((p.max_visual + kT2 - 1) / kT2));
+  stream_p2_kernel<<<grid, kT2, sizeof(float) * p.h_kv * kRC, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stream_p2k(const Dev& p, const StreamMaps& m, const Ws& w, int sms, bool tail,
+                              int64_t out_capacity, cudaStream_t s) {
+  return p.d == 128 ? launch_p2k_t<128>(p, m, w, sms, tail, out_capacity, s)
+                    : launch_p2k_t<64>(p, m, w, sms, tail, out_capacity, s);
+}
+
+}  // namespace aircache

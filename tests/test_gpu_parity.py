@@ -166,6 +166,32 @@ def test_alpha_zero_many_row_chunks(A, oracle):
     assert staged["n_tk"].tolist() == [40, 17] * 2
 
 
+def test_mixed_narrow_and_wide_units(A, oracle):
+    """alpha = 0 with one short and one long text: request 0's units have
+    g * N_tk = 21 query rows per KV head (narrow scoring path), request 1's
+    have 7 * 17 = 119 (wide path), in every layer; budgets and offsets span
+    both paths."""
+    wl = custom_workload([700, 390], [3, 17], L=3, H_q=28, H_kv=4, alpha=0.0)
+    staged, _ = full_check(A, oracle, wl)
+    assert staged["n_tk"].tolist() == [3, 17] * 3
+
+
+def test_narrow_two_row_tiles(A, oracle):
+    """MHA-style g = 1 with 20 elite rows per KV head: the narrow path's
+    second 16-row m-tile and a ragged last key tile."""
+    wl = custom_workload([1000, 333], [20, 25], L=2, H_q=4, H_kv=4, alpha=0.0)
+    staged, _ = full_check(A, oracle, wl)
+    assert staged["n_tk"].tolist() == [20, 25] * 2
+
+
+def test_many_elite_text_tiles(A, oracle):
+    """alpha = 0 with 200 text tokens: the elite text keys span two 128-key
+    tiles and the rows of one KV head span 25 row chunks."""
+    wl = custom_workload([300], [200], L=2, H_q=8, H_kv=2, alpha=0.0)
+    staged, _ = full_check(A, oracle, wl)
+    assert staged["n_tk"].tolist() == [200, 200]
+
+
 def test_alpha_one(A, oracle):
     wl = custom_workload([257, 64], [33, 5], alpha=1.0)
     full_check(A, oracle, wl)
