@@ -175,7 +175,7 @@ def algorithmic_bytes(spec, n_tk, keep, esize):
     qrow = spec.H_q * spec.D * esize
     g = spec.H_q // spec.H_kv
     k = {"elite_window": 0, "score_pass1": 0, "score_pass2": 0, "score_pass2k": 0, "score_wide": 0,
-         "select_topk": 0, "gather_compact": 0}
+         "stats_budget": 0, "select_topk": 0, "gather_compact": 0}
     path = 0
     for l in range(spec.L):
         for b, (nv, nt) in enumerate(unit_lengths(spec)):
@@ -185,6 +185,7 @@ def algorithmic_bytes(spec, n_tk, keep, esize):
             if esize == 2:
                 k["score_pass1"] += (nv + t) * row + t * qrow
                 k["score_pass2" if g * t <= 32 else "score_pass2k"] += 4 * nv  # I_v written
+                k["stats_budget"] += 4 * nv  # I_v read once more for the moments
             else:
                 k["score_wide"] += (nv + t) * row + t * qrow + 4 * nv
             k["select_topk"] += 4 * nv + 4 * kp

@@ -223,7 +223,7 @@ AIRCACHE_API const char* aircache_status_string(int status);
  * Number of kernels one aircache_compress call on `p` launches (for launch
  * accounting), or -1 if `p` is invalid.  It depends on the scoring path, which
  * the problem alone decides: bf16 inputs whose per-layer key pointers are
- * evenly strided take the streaming path (6 kernels), others the wide path (4).
+ * evenly strided take the streaming path (7 kernels), others the wide path (4).
  */
 AIRCACHE_API int aircache_compress_launches(const aircache_problem* p);
 

@@ -39,10 +39,10 @@ namespace {
 
 constexpr size_t kAlign = 256;
 // Kernels of one aircache_compress call, by scoring path.
-const char* const kStreamKernels[] = {"elite_window", "score_pass1", "score_pass2", "score_pass2k",
-                                      "select_topk",  "gather_compact"};
+const char* const kStreamKernels[] = {"elite_window", "score_pass1", "score_pass2",   "score_pass2k",
+                                      "stats_budget", "select_topk", "gather_compact"};
 const char* const kWideKernels[] = {"elite_window", "score_wide", "select_topk", "gather_compact"};
-constexpr int kStreamCount = 6, kWideCount = 4;
+constexpr int kStreamCount = 7, kWideCount = 4;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -258,8 +258,8 @@ int aircache_score(const aircache_problem* p, void* ws, size_t ws_bytes, float* 
   AC_TRY(launch_elite(dn, lp, w, s));
   if (dn.stream_ok) {
     AC_TRY(launch_stream_p1(dn, maps, w, sms, s));
-    AC_TRY(launch_stream_p2(dn, w, false, 0, s));
-    AC_TRY(launch_stream_p2k(dn, maps, w, sms, false, 0, s));
+    AC_TRY(launch_stream_p2(dn, w, s));
+    AC_TRY(launch_stream_p2k(dn, maps, w, sms, s));
   } else {
     AC_TRY(launch_score(dn, lp, w, plan_score(dn, sms, false, 0), s));
   }
@@ -366,9 +366,11 @@ static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, v
   if (dn.stream_ok) {
     AC_TRY(launch_stream_p1(dn, maps, w, sms, s));
     AC_TRY(mark(k++));
-    AC_TRY(launch_stream_p2(dn, w, true, out_rows_capacity, s));
+    AC_TRY(launch_stream_p2(dn, w, s));
     AC_TRY(mark(k++));
-    AC_TRY(launch_stream_p2k(dn, maps, w, sms, true, out_rows_capacity, s));
+    AC_TRY(launch_stream_p2k(dn, maps, w, sms, s));
+    AC_TRY(mark(k++));
+    AC_TRY(launch_stats_budget(dn, w, nullptr, out_rows_capacity, true, s));
     AC_TRY(mark(k++));
   } else {
     AC_TRY(launch_score(dn, lp, w, plan_score(dn, sms, true, out_rows_capacity), s));

@@ -3,9 +3,10 @@
 //
 // One CTA per (request, layer) computes that layer's (s_t, s_k) (float-float
 // moments, see reduce.cuh); the CTA finishing a request's last layer (atomic
-// arrival count) computes the request's keep counts.  The fused compression
-// computes the same quantities at the tail of the scoring kernel with the same
-// device functions.  A separate one-CTA kernel writes the compacted-cache row
+// arrival count) computes the request's keep counts, and in the fused
+// compression the CTA finishing the last request writes the compacted-cache
+// row offsets.  The wide scoring kernel computes the same quantities at its
+// tail with the same device functions.  A separate one-CTA kernel writes the
 // offsets for the staged compaction.
 #include <cstring>
 #include <mutex>
@@ -17,7 +18,8 @@
 namespace aircache {
 namespace {
 
-constexpr int kStatsThreads = 256;
+constexpr int kStatsThreads = 256;   // stand-alone offsets kernel, allocation-free budget
+constexpr int kTailThreads = 1024;   // one (layer, request) per CTA: one load round per moment pass
 constexpr int kBarAll = 1;
 
 struct StatsArgs {
@@ -27,14 +29,21 @@ struct StatsArgs {
   int64_t out_capacity;   // rows of the output arena (offsets kernel only)
 };
 
-__global__ void __launch_bounds__(kStatsThreads) stats_budget_kernel(const __grid_constant__ StatsArgs a) {
+// (s_t, s_k) of one (layer, request) per CTA; the CTA finishing a request's
+// last layer computes its keep counts; with OFFSETS, the CTA finishing the
+// last request writes the compacted-cache row offsets.
+template <int NT, bool OFFSETS>
+__global__ void __launch_bounds__(NT) stats_budget_kernel(const __grid_constant__ StatsArgs a) {
   const Dev& p = a.p;
   const Ws& w = a.w;
   const int b = blockIdx.x, l = blockIdx.y, u = l * p.B + b;
   const int tid = threadIdx.x;
-  __shared__ ff redff[kStatsThreads / 32];
-  __shared__ double sh[4];
+  __shared__ ff redff[2 * (NT / 32) + 1];
+  __shared__ double sh[2 * (NT / 32) + 4];
+  __shared__ long long seg[NT / 32 + 1];
   __shared__ int flag;
+  pdl_trigger();
+  pdl_wait();  // I_v
   if (*(volatile int32_t*)w.error != 0) return;
   Req R;
   if (!load_req(p, b, R)) {
@@ -42,7 +51,7 @@ __global__ void __launch_bounds__(kStatsThreads) stats_budget_kernel(const __gri
     return;
   }
   const float* x = w.iv + (size_t)l * p.total_visual + R.vis0;
-  const double2 m = unit_moments<kStatsThreads>(x, R.n_v, tid, redff, kBarAll);
+  const double2 m = unit_moments<NT>(x, R.n_v, tid, redff, kBarAll);
   if (tid == 0) {
     w.stats[2 * u] = m.x;
     w.stats[2 * u + 1] = m.y;
@@ -56,12 +65,23 @@ __global__ void __launch_bounds__(kStatsThreads) stats_budget_kernel(const __gri
   __syncthreads();
   if (!flag) return;
   __threadfence();
-  request_budget<kStatsThreads>(p, b, R.n_v, w.stats, w.keep, sh, tid, kBarAll);
+  request_budget<NT>(p, b, R.n_v, w.stats, w.keep, sh, tid, kBarAll);
+  if constexpr (OFFSETS) {
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) flag = (atomicAdd(w.cnt_all, 1u) == (unsigned)(p.B - 1)) ? 1 : 0;
+    __syncthreads();
+    if (!flag) return;
+    __threadfence();
+    write_offsets<NT>(p, w.keep, w.out_offsets, w.error, a.out_capacity, seg, tid, kBarAll);
+  }
 }
 
 // Stand-alone offsets (staged compaction): one CTA.
 __global__ void __launch_bounds__(kStatsThreads) offsets_kernel(const __grid_constant__ StatsArgs a) {
   __shared__ long long seg[kStatsThreads];
+  pdl_trigger();
+  pdl_wait();
   if (*(volatile int32_t*)a.w.error != 0) return;
   const Dev& p = a.p;
   // every request's lengths and keep counts must be consistent before they size the arena
@@ -134,7 +154,7 @@ int budget_noalloc(const Dev& p, const float* iv, double* stats_out, int32_t* ke
   a.w.keep = keep;
   a.stats_out = stats_out;
   a.out_capacity = 0;
-  stats_budget_kernel<<<dim3(p.B, p.L), kStatsThreads, 0, s>>>(a);
+  stats_budget_kernel<kStatsThreads, false><<<dim3(p.B, p.L), kStatsThreads, 0, s>>>(a);
   if (cudaGetLastError() != cudaSuccess) return AIRCACHE_ERR_CUDA;
   if (device_status &&
       cudaMemcpyAsync(device_status, base, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess) {
@@ -145,15 +165,13 @@ int budget_noalloc(const Dev& p, const float* iv, double* stats_out, int32_t* ke
 
 cudaError_t launch_stats_budget(const Dev& p, const Ws& w, double* stats_out, int64_t out_capacity,
                                 bool offsets, cudaStream_t s) {
-  (void)offsets;
-  (void)out_capacity;
   StatsArgs a;
   a.p = p;
   a.w = w;
   a.stats_out = stats_out;
-  a.out_capacity = 0;
-  stats_budget_kernel<<<dim3(p.B, p.L), kStatsThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  a.out_capacity = out_capacity;
+  return offsets ? launch_pdl(stats_budget_kernel<kTailThreads, true>, dim3(p.B, p.L), dim3(kTailThreads), 0, s, a)
+                 : launch_pdl(stats_budget_kernel<kTailThreads, false>, dim3(p.B, p.L), dim3(kTailThreads), 0, s, a);
 }
 
 cudaError_t launch_offsets(const Dev& p, const Ws& w, int64_t out_capacity, cudaStream_t s) {
@@ -162,8 +180,7 @@ cudaError_t launch_offsets(const Dev& p, const Ws& w, int64_t out_capacity, cuda
   a.w = w;
   a.stats_out = nullptr;
   a.out_capacity = out_capacity;
-  offsets_kernel<<<1, kStatsThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(offsets_kernel, dim3(1), dim3(kStatsThreads), 0, s, a);
 }
 
 }  // namespace aircache

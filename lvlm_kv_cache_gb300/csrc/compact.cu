@@ -9,6 +9,7 @@
 // resolves the source position and copies the K and V rows with 16-byte loads
 // and stores.  Bit-exact: no arithmetic touches the data.
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace aircache {
 namespace {
@@ -31,6 +32,8 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_cons
   const Ws& w = a.w;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ long long offs[kMaxSmemOffsets + 1];
+  pdl_trigger();
+  pdl_wait();  // selections, keep counts and row offsets
   if (*(volatile int32_t*)w.error != 0) return;
   const int units = p.L * p.B;
   const bool in_smem = units <= kMaxSmemOffsets;
@@ -118,8 +121,7 @@ cudaError_t launch_compact(const Dev& p, const LayerPtrs& lp, const Ws& w, void*
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  compact_kernel<<<sms * 4, kCopyThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(compact_kernel, dim3(sms * 4), dim3(kCopyThreads), 0, s, a);
 }
 
 }  // namespace aircache

@@ -64,6 +64,7 @@ __device__ __forceinline__ void load_item(const Dev& p, const Req& R, const char
 
 template <typename T, int D, int NS>
 __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_constant__ EliteArgs a) {
+  pdl_trigger();  // the next kernel may set up while this one runs
   using G = TileGeom<T, D>;
   const Dev& p = a.p;
   const int b = blockIdx.x, l = blockIdx.y, u = l * p.B + b;

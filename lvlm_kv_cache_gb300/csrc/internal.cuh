@@ -122,6 +122,8 @@ ScoreLaunch plan_score(const Dev& p, int sms, bool tail, int64_t out_capacity);
 cudaError_t launch_elite(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_t s);
 cudaError_t launch_score(const Dev& p, const LayerPtrs& lp, const Ws& w, const ScoreLaunch& L,
                          cudaStream_t s);
+// Stats and keep counts from I_v, one CTA per (layer, request); with
+// `offsets` also the compacted-cache row offsets (checked against out_capacity).
 cudaError_t launch_stats_budget(const Dev& p, const Ws& w, double* stats_out,
                                 int64_t out_capacity, bool offsets, cudaStream_t s);
 cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s);
@@ -131,17 +133,33 @@ cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s);
 // the host.  Pass 1 streams the keys and produces row partials (and, for units
 // with one row chunk per KV head, their logits); pass 2 turns stored logits
 // into I_v and merges the other units' row LSEs; pass 2k recomputes those
-// units' logits from the keys.  With `tail`, the CTA completing a unit also
-// computes stats, budgets and offsets.
+// units' logits from the keys.
 struct StreamMaps {
   CUtensorMap kmap, qmap, kelmap;
 };
 bool stream_eligible(const Dev& p, const LayerPtrs& lp);
 bool encode_stream_maps(const Dev& p, const LayerPtrs& lp, const Ws& w, StreamMaps* m);
 cudaError_t launch_stream_p1(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s);
-cudaError_t launch_stream_p2(const Dev& p, const Ws& w, bool tail, int64_t out_capacity, cudaStream_t s);
-cudaError_t launch_stream_p2k(const Dev& p, const StreamMaps& m, const Ws& w, int sms, bool tail,
-                              int64_t out_capacity, cudaStream_t s);
+cudaError_t launch_stream_p2(const Dev& p, const Ws& w, cudaStream_t s);
+cudaError_t launch_stream_p2k(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s);
+
+// Launch `kernel` on `s` with programmatic stream serialization, so that its
+// CTAs may start (and run up to pdl_wait()) while the previous kernel on the
+// stream finishes.
+template <typename Arg>
+cudaError_t launch_pdl(void (*kernel)(Arg), dim3 grid, dim3 block, size_t smem, cudaStream_t s, const Arg& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
 
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) for `func` on the current
 // device, skipped when an earlier call already allowed at least `bytes`.

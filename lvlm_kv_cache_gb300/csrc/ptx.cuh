@@ -104,6 +104,17 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag) {
   return true;
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may start before the previous kernel on the
+// stream has finished; pdl_wait() blocks until that kernel has completed and
+// its memory operations are visible (a no-op without the attribute).
+// pdl_trigger() lets the next kernel start launching once every CTA of this
+// grid has called it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 // ---------------------------------------------------------------- cp.async
 
 // 16-byte async copy global -> shared; src_bytes = 0 zero-fills the destination.

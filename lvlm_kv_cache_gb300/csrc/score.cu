@@ -124,8 +124,8 @@ struct Ctl {
   int svc_flag[4];
   SvcJob svc_job;
   float2 red[2 * kCW * kRC];
-  ff svc_red[kSvcT / 32];
-  double svc_sh[4];
+  ff svc_red[2 * (kSvcT / 32) + 1];
+  double svc_sh[2 * (kSvcT / 32) + 4];
   long long svc_seg[kSvcT];
 };
 

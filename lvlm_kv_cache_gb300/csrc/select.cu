@@ -2,23 +2,29 @@
 // the AirCache budget feeds: the keep_l highest-scoring visual tokens of layer l
 // stay in the cache, ties to the lower position, emitted in ascending order).
 //
-// One CTA per (request, layer).  I_v is mapped to order-preserving 32-bit keys;
-// a 4-digit (8-bit) MSB-first radix select finds the exact keep-th largest key
-// T and how many keys equal to T are still wanted; a final ordered sweep emits
-// every key > T plus the lowest-position keys == T, in ascending position, via
-// block-wide ballot scans.  Integer work only: the result is exact and
-// deterministic.
+// One CTA of 1024 threads per (request, layer).  I_v is mapped to
+// order-preserving 32-bit keys, held in shared memory when the unit fits
+// (otherwise re-read from global memory each pass).  A 4-digit (8-bit)
+// MSB-first radix select finds the exact keep-th largest key T and how many
+// keys equal to T are still wanted; histogram increments are aggregated over
+// the lanes of a warp that share a digit.  A final sweep in which each thread
+// owns a contiguous run of positions emits every key > T plus the
+// lowest-position keys == T, in ascending position, with two block-wide
+// exclusive scans.  Integer work only: the result is exact and deterministic.
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace aircache {
 namespace {
 
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSmemKeys = 40 * 1024;  // units up to this many keys are staged in shared memory
 
 struct SelectArgs {
   Dev p;
   Ws w;
+  int smem_keys;  // capacity of the dynamic shared-memory key buffer
 };
 
 // Larger float <=> larger key (handles -0.0 and negatives, which I_v never has).
@@ -27,33 +33,47 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Exclusive block prefix of a per-thread flag; returns this thread's prefix,
-// *total receives the block total.
-__device__ __forceinline__ int block_scan_flag(bool f, int* wsum, int* total) {
+// Exclusive prefix over the CTA of one int per thread; *total receives the sum.
+// `wsum` is shared scratch of kSelWarps + 1 ints.
+__device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned bal = __ballot_sync(0xffffffffu, f);
-  const int before = __popc(bal & ((1u << lane) - 1u));
-  __syncthreads();
-  if (lane == 0) wsum[warp] = __popc(bal);
-  __syncthreads();
-  int base = 0, tot = 0;
+  int incl = v;
 #pragma unroll
-  for (int i = 0; i < kSelWarps; ++i) {
-    base += (i < warp) ? wsum[i] : 0;
-    tot += wsum[i];
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
   }
-  *total = tot;
-  return base + before;
+  __syncthreads();  // earlier readers of wsum are done
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int t = wsum[lane];  // kSelWarps == 32
+    int ti = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, ti, o);
+      if (lane >= o) ti += x;
+    }
+    wsum[lane] = ti - t;
+    if (lane == 31) wsum[kSelWarps] = ti;
+  }
+  __syncthreads();
+  *total = wsum[kSelWarps];
+  return wsum[warp] + incl - v;
 }
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_constant__ SelectArgs a) {
+  static_assert(kSelWarps == 32, "the warp-total scan assumes 32 warps");
   const Dev& p = a.p;
   const Ws& w = a.w;
   const int b = blockIdx.x, l = blockIdx.y, u = l * p.B + b;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  extern __shared__ uint32_t keys_s[];
   __shared__ unsigned hist[256];
-  __shared__ int wsum[kSelWarps];
+  __shared__ int wsum[kSelWarps + 1];
   __shared__ unsigned sel_digit, sel_above;
+  pdl_trigger();
+  pdl_wait();  // I_v and the keep counts
   if (*(volatile int32_t*)w.error != 0) return;
   Req R;
   if (!load_req(p, b, R)) {
@@ -73,15 +93,33 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
     return;
   }
   if (k == 0) return;
+  const bool staged = n <= a.smem_keys;
+  if (staged) {
+    for (int i0 = tid; i0 < n; i0 += 8 * kSelThreads) {
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = (i0 + q * kSelThreads < n) ? __ldcg(x + i0 + q * kSelThreads) : 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (i0 + q * kSelThreads < n) keys_s[i0 + q * kSelThreads] = order_key(v[q]);
+      }
+    }
+  }
+  auto key_at = [&](int i) -> uint32_t { return staged ? keys_s[i] : order_key(__ldcg(x + i)); };
 
   uint32_t prefix = 0, mask = 0;
   unsigned want = (unsigned)k;  // keys >= the answer still to account for
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
     __syncthreads();
-    for (int i = tid; i < n; i += kSelThreads) {
-      const uint32_t key = order_key(__ldcg(x + i));
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    for (int i0 = 0; i0 < n; i0 += kSelThreads) {
+      const int i = i0 + tid;
+      const uint32_t key = i < n ? key_at(i) : 0u;
+      const bool in = i < n && (key & mask) == prefix;
+      const unsigned digit = in ? ((key >> shift) & 255u) : 256u;
+      // one increment per distinct digit of the warp
+      const unsigned peers = __match_any_sync(0xffffffffu, digit);
+      if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (unsigned)__popc(peers));
     }
     __syncthreads();
     if (warp == 0) {
@@ -116,26 +154,40 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
     want -= sel_above;
     prefix |= sel_digit << shift;
     mask |= 255u << shift;
-    __syncthreads();
   }
-  // prefix = exact key of the keep-th largest; take all keys > prefix and the
-  // first `want` keys == prefix in position order.
-  int base = 0, eq_base = 0;
-  for (int i0 = 0; i0 < n; i0 += kSelThreads) {
-    const int i = i0 + tid;
-    const uint32_t key = (i < n) ? order_key(__ldcg(x + i)) : 0u;
-    const bool eq = i < n && key == prefix;
-    const bool gt = i < n && key > prefix;
-    int eq_total;
-    const int eq_rank = eq_base + block_scan_flag(eq, wsum, &eq_total);
-    const bool take = gt || (eq && eq_rank < (int)want);
-    int tk_total;
-    const int pos = base + block_scan_flag(take, wsum, &tk_total);
-    if (take) out[pos] = i;
-    base += tk_total;
-    eq_base += eq_total;
+  // prefix = exact key of the keep-th largest: take every key > prefix and the
+  // first `want` keys == prefix in position order.  Thread tid owns positions
+  // [tid * per, tid * per + per).
+  const int per = (n + kSelThreads - 1) / kSelThreads;
+  const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+  int n_eq = 0;
+  for (int i = i0; i < i1; ++i) n_eq += key_at(i) == prefix ? 1 : 0;
+  int eq_total;
+  int eq_rank = block_excl_scan(n_eq, wsum, &eq_total);
+  int n_take = 0;
+  {
+    int r = eq_rank;
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t key = key_at(i);
+      if (key > prefix) {
+        ++n_take;
+      } else if (key == prefix) {
+        if (r < (int)want) ++n_take;
+        ++r;
+      }
+    }
   }
-  (void)lane;
+  int take_total;
+  int pos = block_excl_scan(n_take, wsum, &take_total);
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = key_at(i);
+    if (key > prefix) {
+      out[pos++] = i;
+    } else if (key == prefix) {
+      if (eq_rank < (int)want) out[pos++] = i;
+      ++eq_rank;
+    }
+  }
 }
 
 }  // namespace
@@ -144,8 +196,11 @@ cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s) {
   SelectArgs a;
   a.p = p;
   a.w = w;
-  select_kernel<<<dim3(p.B, p.L), kSelThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  a.smem_keys = p.max_visual < kSmemKeys ? p.max_visual : kSmemKeys;
+  const int smem = (int)sizeof(uint32_t) * a.smem_keys;
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(select_kernel), smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(select_kernel, dim3(p.B, p.L), dim3(kSelThreads), smem, s, a);
 }
 
 }  // namespace aircache

@@ -37,9 +37,8 @@
 // small TMA ring; per-key sums of exp2(logit - lse) over every row give the
 // tile's I_v directly.
 //
-// With `tail`, the CTA completing a unit also computes its (s_t, s_k) ("Key
-// design 2"), the one completing a request's last unit its keep counts, and
-// the last request the compacted-cache row offsets.
+// The per-layer statistics, budgets and offsets follow in a kernel of their own
+// (budget.cu), one CTA per unit.
 #include <cstring>
 
 #include "internal.cuh"
@@ -58,7 +57,6 @@ constexpr int kCT = kCW * 32;             // consumer threads
 constexpr int kThreads1 = kCT + 32;       // + the producer warp
 constexpr int kBarC = 1;                  // named barrier of the consumer threads
 constexpr int kT2 = 256;                  // pass-2 / pass-2k threads
-constexpr int kBarT = 1;                  // named barrier over all kT2 threads
 constexpr int kMaxStages = 12;
 constexpr int kNQ = 4;                    // pass-2k query-chunk ring
 
@@ -99,8 +97,6 @@ struct SArgs {
   CUtensorMap kelmap;  // gathered elite text keys (D, rows), box 128 rows
   Dev p;
   Ws w;
-  int tail;
-  int64_t out_capacity;
 };
 
 __device__ __forceinline__ float2 merge_ms(float2 a, float2 b) {
@@ -138,41 +134,6 @@ __device__ __forceinline__ float row_lse(const Dev& p, const Ws& w, int u, int k
   }
   ms = merge_ms(ms, __ldcg(pr + p.chn - 1));
   return ms.x + log2f(ms.y);
-}
-
-// The end of a unit's scoring, run by every thread of a kT2-thread CTA once
-// the unit's I_v (at iv) is complete and visible: (s_t, s_k), then the
-// request's keep counts if this was its last unit, then the row offsets if
-// this was the last request.
-struct TailSmem {
-  ff redff[kT2 / 32];
-  double sh[4];
-  long long seg[kT2];
-  int flag;
-};
-
-__device__ void unit_tail(const SArgs& a, TailSmem& t, int u, int n_v, const float* iv) {
-  const Dev& p = a.p;
-  const Ws& w = a.w;
-  const int tid = threadIdx.x, b = u % p.B;
-  const double2 mo = unit_moments<kT2>(iv, n_v, tid, t.redff, kBarT);
-  if (tid == 0) {
-    w.stats[2 * u] = mo.x;
-    w.stats[2 * u + 1] = mo.y;
-    __threadfence();
-    t.flag = (atomicAdd(&w.cnt_req[b], 1u) == (unsigned)(p.L - 1)) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!t.flag) return;
-  __threadfence();
-  request_budget<kT2>(p, b, n_v, w.stats, w.keep, t.sh, tid, kBarT);
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) t.flag = (atomicAdd(w.cnt_all, 1u) == (unsigned)(p.B - 1)) ? 1 : 0;
-  __syncthreads();
-  if (!t.flag) return;
-  __threadfence();
-  write_offsets<kT2>(p, w.keep, w.out_offsets, w.error, a.out_capacity, t.seg, tid, kBarT);
 }
 
 // ------------------------------------------------------------------ pass 1
@@ -438,6 +399,8 @@ __global__ void __launch_bounds__(kThreads1, 1) stream_p1_kernel(const __grid_co
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_trigger();
+  pdl_wait();  // the elite kernel's lists, query rows and elite keys
   if (*(volatile int32_t*)a.w.error != 0) return;  // an earlier kernel reported an error
   if (threadIdx.x < kCT) {
     p1_consumers<D>(a, c, sm);
@@ -452,8 +415,9 @@ __global__ void __launch_bounds__(kT2) stream_p2_kernel(const __grid_constant__ 
   const Dev& p = a.p;
   const Ws& w = a.w;
   extern __shared__ float lse_s[];  // [h_kv][32]
-  __shared__ TailSmem t;
   const int tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();  // pass 1's partials and logits
   if (*(volatile int32_t*)w.error != 0) return;
   const int li = blockIdx.x;
   if (li >= __ldcg(&w.list_n[0])) return;
@@ -505,26 +469,13 @@ __global__ void __launch_bounds__(kT2) stream_p2_kernel(const __grid_constant__ 
       for (; r < rows; ++r) acc += exp2f(__ldcg(ch + (size_t)r * TV) - ls[r]);
     }
     iv[key] = acc / (float)(p.h_q * n_tk);
-    __threadfence();
   }
-  if (!a.tail) return;
-  // the CTA completing the unit finishes it
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned blocks = (unsigned)((n_v + kT2 - 1) / kT2);
-    t.flag = (atomicAdd(&w.cnt_p2[u], 1u) == blocks - 1u) ? 1 : 0;
-  }
-  __syncthreads();
-  if (!t.flag) return;
-  __threadfence();
-  unit_tail(a, t, u, n_v, iv);
 }
 
 // ------------------------------------------------------------------ pass 2k
 
 struct Ctl2 {
   uint64_t kfull, qfull[kNQ];
-  int flag;
 };
 
 // Multi-chunk units.  Item = (unit, key tile): for each KV head in turn the
@@ -542,7 +493,6 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   Ctl2* c = reinterpret_cast<Ctl2*>(sm + Gm::kCtl2Off);
-  __shared__ TailSmem t;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g4 = lane >> 2, c4 = lane & 3;
   const uint32_t sbase = smem_u32(sm);
@@ -552,6 +502,8 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_trigger();
+  pdl_wait();  // pass 2's row LSEs
   if (*(volatile int32_t*)w.error != 0) return;
   const int TVmax = (p.max_visual + kTK - 1) / kTK;
   const long long total = (long long)__ldcg(&w.list_n[2]) * TVmax;
@@ -680,16 +632,6 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
         const int key = 16 * warp + 8 * nt + 2 * c4 + e;
         if (g4 == 0 && key < klim) iv[(long long)tile * kTK + key] = v / denom;
       }
-    if (!a.tail) continue;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) c->flag = (atomicAdd(&w.cnt_p2[u], 1u) == (unsigned)(tv - 1)) ? 1 : 0;
-    __syncthreads();
-    if (c->flag) {
-      __threadfence();
-      unit_tail(a, t, u, n_v, iv);  // this CTA completed the unit
-    }
-    __syncthreads();
   }
 }
 
@@ -706,13 +648,11 @@ cudaError_t launch_p1_t(const Dev& p, const StreamMaps& m, const Ws& w, int sms,
   const int smem = Gm::kCtlOff + (int)sizeof(Ctl1) + 1024;
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(stream_p1_kernel<D>), smem);
   if (e != cudaSuccess) return e;
-  stream_p1_kernel<D><<<sms, kThreads1, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(stream_p1_kernel<D>, dim3(sms), dim3(kThreads1), smem, s, a);
 }
 
 template <int D>
-cudaError_t launch_p2k_t(const Dev& p, const StreamMaps& m, const Ws& w, int sms, bool tail,
-                         int64_t out_capacity, cudaStream_t s) {
+cudaError_t launch_p2k_t(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s) {
   using Gm = SGeo<D>;
   SArgs a;
   std::memset(&a, 0, sizeof a);
@@ -720,13 +660,10 @@ cudaError_t launch_p2k_t(const Dev& p, const StreamMaps& m, const Ws& w, int sms
   a.qmap = m.qmap;
   a.p = p;
   a.w = w;
-  a.tail = tail ? 1 : 0;
-  a.out_capacity = out_capacity;
   const int smem = Gm::kCtl2Off + (int)sizeof(Ctl2) + 1024;
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(stream_p2k_kernel<D>), smem);
   if (e != cudaSuccess) return e;
-  stream_p2k_kernel<D><<<2 * sms, kT2, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(stream_p2k_kernel<D>, dim3(2 * sms), dim3(kT2), smem, s, a);
 }
 
 }  // namespace
@@ -753,22 +690,17 @@ cudaError_t launch_stream_p1(const Dev& p, const StreamMaps& m, const Ws& w, int
   return p.d == 128 ? launch_p1_t<128>(p, m, w, sms, s) : launch_p1_t<64>(p, m, w, sms, s);
 }
 
-cudaError_t launch_stream_p2(const Dev& p, const Ws& w, bool tail, int64_t out_capacity, cudaStream_t s) {
+cudaError_t launch_stream_p2(const Dev& p, const Ws& w, cudaStream_t s) {
   SArgs a;
   std::memset(&a, 0, sizeof a);
   a.p = p;
   a.w = w;
-  a.tail = tail ? 1 : 0;
-  a.out_capacity = out_capacity;
   const dim3 grid((unsigned)(p.L * p.B), (unsigned)((p.max_visual + kT2 - 1) / kT2));
-  stream_p2_kernel<<<grid, kT2, sizeof(float) * p.h_kv * kRC, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(stream_p2_kernel, grid, dim3(kT2), sizeof(float) * p.h_kv * kRC, s, a);
 }
 
-cudaError_t launch_stream_p2k(const Dev& p, const StreamMaps& m, const Ws& w, int sms, bool tail,
-                              int64_t out_capacity, cudaStream_t s) {
-  return p.d == 128 ? launch_p2k_t<128>(p, m, w, sms, tail, out_capacity, s)
-                    : launch_p2k_t<64>(p, m, w, sms, tail, out_capacity, s);
+cudaError_t launch_stream_p2k(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s) {
+  return p.d == 128 ? launch_p2k_t<128>(p, m, w, sms, s) : launch_p2k_t<64>(p, m, w, sms, s);
 }
 
 }  // namespace aircache
