@@ -171,7 +171,10 @@ size_t carve(const Dev& d, char* base, Ws* w) {
   t.multi_list = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
   if (d.dtype == AIRCACHE_BF16) {  // the streaming path exists for bf16 only
     const size_t kvrows = (size_t)d.L * d.h_kv;
-    t.lg = reinterpret_cast<float*>(take(sizeof(float) * kvrows * kRowChunk * d.total_visual));
+    // rows of the streaming path's logit buffer: every request's keys, each
+    // request starting at a multiple of 4 columns (4 columns of padding per request)
+    const size_t stride = (size_t)(d.total_visual + 4 * (int64_t)d.B + 7) / 4 * 4;
+    t.lg = reinterpret_cast<float*>(take(sizeof(float) * kvrows * kRowChunk * stride));
     t.part_s = reinterpret_cast<float2*>(take(sizeof(float2) * LB * d.h_kv * d.rc_max * kRowChunk * d.chn));
   }
   t.uinfo = reinterpret_cast<int4*>(take(sizeof(int4) * 2 * LB));

@@ -60,7 +60,7 @@ struct Ws {
   int32_t* stream_list;  // [L*B] units u = l*B + b on the streaming path (list_n[0] of them, any order)
   int32_t* wide_list;    // [L*B] units on the wide path (list_n[1] of them, any order)
   int32_t* multi_list;   // [L*B] streaming units with g * N_tk > 32 (list_n[2] of them)
-  float* lg;             // [L][h_kv][32][total_visual] streaming path: logits of row r of KV head h
+  float* lg;             // [L][h_kv][32][lg stride] streaming path: logits of row r of KV head h
   float2* part_s;        // [L*B][h_kv][rc_max*32][chn] streaming pass 1: (max, sum of exp2) per (row, chunk)
   int4* uinfo;           // [L*B][2] {seq0, vis0, txt0, N_v}, {N_t, N_tk, 1, 0} per (layer, request)
   void* qel;             // [L*B][rows_max][D] elite query rows, row kvh*g*N_tk + hh*N_tk + e
@@ -135,7 +135,7 @@ cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s);
 // into I_v and merges the other units' row LSEs; pass 2k recomputes those
 // units' logits from the keys.
 struct StreamMaps {
-  CUtensorMap kmap, qmap, kelmap;
+  CUtensorMap kmap, kmap2, qmap, kelmap;  // keys (boxes of 128 / 256 rows), elite queries, elite keys
 };
 bool stream_eligible(const Dev& p, const LayerPtrs& lp);
 bool encode_stream_maps(const Dev& p, const LayerPtrs& lp, const Ws& w, StreamMaps* m);

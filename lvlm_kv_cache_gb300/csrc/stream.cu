@@ -70,9 +70,12 @@ struct SGeo {
   static constexpr int kKBytes = kNH * kKSlab;
   static constexpr int kQSlab = kRC * 128;
   static constexpr int kQBytes = kNH * kQSlab;
-  // pass 1: key-tile ring, two query buffers, control
-  static constexpr int kStages = D == 128 ? 6 : 11;
-  static constexpr int kQOff = kStages * kKBytes;
+  // pass 1: ring of 256-key stages, two query buffers, control
+  static constexpr int kSK = 2 * kTK;       // keys per pass-1 stage
+  static constexpr int kSSlab = kSK * 128;  // one 128-byte column slab of a stage
+  static constexpr int kSBytes = kNH * kSSlab;
+  static constexpr int kStages = D == 128 ? 3 : 6;
+  static constexpr int kQOff = kStages * kSBytes;
   static constexpr int kCtlOff = kQOff + 2 * kQBytes;
   static_assert(kStages <= kMaxStages, "ring depth");
   // pass 2k: one key tile, kNQ query chunks (+ their LSEs), control
@@ -80,24 +83,21 @@ struct SGeo {
   static constexpr int kCtl2Off = kKBytes + kNQ * kQ2;
 };
 
-struct Hdr {
-  int kind, u, l, kvh, tile, klim, rows, r0, first, last, chunk, qbuf, store, pad;
-  long long vis0;
-};
-
-struct Ctl1 {
-  uint64_t full[kMaxStages], empty[kMaxStages], qempty[2];
-  Hdr hdr[kMaxStages];
-  float2 red[2][kCW][kRC];
-};
-
 struct SArgs {
-  CUtensorMap kmap;    // keys of every layer: (D, H_kv, tokens, layers), box 128 tokens
+  CUtensorMap kmap;    // keys of every layer: (D, H_kv, tokens, layers), box 128 tokens (pass 2k)
+  CUtensorMap kmap2;   // the same keys, box 256 tokens (pass 1)
   CUtensorMap qmap;    // gathered elite query rows (D, rows), box 32 rows
   CUtensorMap kelmap;  // gathered elite text keys (D, rows), box 128 rows
   Dev p;
   Ws w;
 };
+
+// Logit buffer: row r of KV head h of layer l holds the logits of every
+// request's visual keys; request b's keys start at column lg_col0(vis0, b),
+// a multiple of 4 (so that pairs of keys are 8-byte aligned), and rows are
+// lg_stride(p) floats apart.
+__device__ __forceinline__ long long lg_col0(long long vis0, int b) { return (vis0 + 3) / 4 * 4 + 4LL * b; }
+__device__ __forceinline__ long long lg_stride(const Dev& p) { return (p.total_visual + 4LL * p.B + 7) / 4 * 4; }
 
 __device__ __forceinline__ float2 merge_ms(float2 a, float2 b) {
   const float m = fmaxf(a.x, b.x);
@@ -120,7 +120,7 @@ __device__ __forceinline__ size_t part_index(const Dev& p, int u, int kvh, int r
 }
 
 // Merge row `row`'s partials in chunk order (visual chunks, then the text chunk)
-// into its base-2 log-sum-exp.
+// into its base-2 log-sum-exp (one thread).
 // (Loads are issued eight chunks at a time.)
 __device__ __forceinline__ float row_lse(const Dev& p, const Ws& w, int u, int kvh, int row, int chv) {
   const float2* pr = w.part_s + part_index(p, u, kvh, row, 0);
@@ -136,8 +136,44 @@ __device__ __forceinline__ float row_lse(const Dev& p, const Ws& w, int u, int k
   return ms.x + log2f(ms.y);
 }
 
+// The same merge by the four lanes q = lane & 3 of a quad (all four call it):
+// lane q merges chunks q, q+4, ... in order, then the quad combines its four
+// partials (0+1, 2+3, then the two) and the text chunk.  Fixed order: the
+// result is the same run to run (it may differ from row_lse in the last bits).
+__device__ __forceinline__ float row_lse4(const Dev& p, const Ws& w, int u, int kvh, int row, int chv, int q) {
+  const float2* pr = w.part_s + part_index(p, u, kvh, row, 0);
+  float2 v[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c = q + 4 * j;
+    v[j] = c < chv ? __ldcg(pr + c) : make_float2(-INFINITY, 0.f);
+  }
+  const float2 txt = __ldcg(pr + p.chn - 1);
+  float2 ms = merge_ms(merge_ms(v[0], v[1]), merge_ms(v[2], v[3]));
+  for (int c = q + 16; c < chv; c += 4) ms = merge_ms(ms, __ldcg(pr + c));
+  float2 o = make_float2(__shfl_xor_sync(0xffffffffu, ms.x, 1), __shfl_xor_sync(0xffffffffu, ms.y, 1));
+  ms = (q & 1) ? merge_ms(o, ms) : merge_ms(ms, o);
+  o = make_float2(__shfl_xor_sync(0xffffffffu, ms.x, 2), __shfl_xor_sync(0xffffffffu, ms.y, 2));
+  ms = (q & 2) ? merge_ms(o, ms) : merge_ms(ms, o);
+  ms = merge_ms(ms, txt);
+  return ms.x + log2f(ms.y);
+}
+
 // ------------------------------------------------------------------ pass 1
 
+struct Hdr {
+  int kind, u, l, kvh, key0, klim, rows, r0, first, last, chunk, qbuf, store, b;
+  long long vis0;
+};
+
+struct Ctl1 {
+  uint64_t full[kMaxStages], empty[kMaxStages], qempty[2];
+  Hdr hdr[kMaxStages];
+  float2 red[2][kCW][kRC];
+};
+
+// One thread.  Stages: a visual stage is 256 keys (one TMA box of 256 rows per
+// column slab), a text stage up to 128 elite keys.
 template <int D>
 __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
   using Gm = SGeo<D>;
@@ -168,20 +204,24 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
     const int n_rc = (rows + kRC - 1) / kRC;
     const int tv = (n_v + kTK - 1) / kTK;
     const int chv = (tv + kCK - 1) / kCK;
-    int kind, t0, nt;
+    int kind, key0, nkeys, stage_keys;
     if (ch < p.chn - 1) {
       if (ch >= chv) {  // a chunk past this unit's keys
         claim = next;
         continue;
       }
       kind = kVis;
-      t0 = ch * kCK;
-      nt = min(kCK, tv - t0);
+      key0 = ch * kCK * kTK;
+      nkeys = min(kCK * kTK, n_v - key0);
+      stage_keys = Gm::kSK;
     } else {
-      kind = kTxt;  // elite text keys: at most max_elite <= 8192, in tiles of 128
-      t0 = 0;
-      nt = (n_tk + kTK - 1) / kTK;
+      kind = kTxt;  // elite text keys: at most max_elite <= 8192, 128 per stage
+      key0 = 0;
+      nkeys = n_tk;
+      stage_keys = kTK;
     }
+    const int nst = (nkeys + stage_keys - 1) / stage_keys;
+    const uint32_t kbytes = kind == kVis ? (uint32_t)Gm::kSBytes : (uint32_t)(Gm::kNH * kTK * 128);
     const int l = u / p.B;
     for (int rc = 0; ok && rc < n_rc; ++rc, ++sub) {
       const int qb = sub & 1;
@@ -190,41 +230,43 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
         ok = false;
         break;
       }
-      for (int j = 0; j < nt; ++j, ++st) {
+      for (int j = 0; j < nst; ++j, ++st) {
         const int s = (int)(st % NS);
         if (!mbar_wait(&c->empty[s], (uint32_t)(((st / NS) & 1) ^ 1))) {
           ok = false;
           break;
         }
+        const int k0 = key0 + j * stage_keys;
         Hdr& h = c->hdr[s];
         h.kind = kind;
         h.u = u;
         h.l = l;
         h.kvh = kvh;
-        h.tile = t0 + j;
-        h.klim = kind == kVis ? min(kTK, n_v - (t0 + j) * kTK) : min(kTK, n_tk - (t0 + j) * kTK);
+        h.key0 = k0;
+        h.klim = min(stage_keys, (kind == kVis ? n_v : n_tk) - k0);
         h.rows = min(kRC, rows - rc * kRC);
         h.r0 = rc * kRC;
         h.first = (j == 0);
-        h.last = (j == nt - 1);
+        h.last = (j == nst - 1);
         h.chunk = ch;
         h.qbuf = qb;
         h.store = (kind == kVis && n_rc == 1) ? 1 : 0;
+        h.b = u % p.B;
         h.vis0 = i0.y;
-        mbar_arrive_expect_tx(&c->full[s], (uint32_t)(Gm::kKBytes + (j == 0 ? Gm::kQBytes : 0)));
-        const uint32_t kdst = sbase + (uint32_t)(s * Gm::kKBytes);
+        mbar_arrive_expect_tx(&c->full[s], kbytes + (j == 0 ? (uint32_t)Gm::kQBytes : 0u));
+        const uint32_t kdst = sbase + (uint32_t)(s * Gm::kSBytes);
 #pragma unroll
         for (int sl = 0; sl < Gm::kNH; ++sl) {
           if (kind == kVis) {
             if (n_rc == 1) {  // read once
-              tma_load_4d_hint(kdst + sl * Gm::kKSlab, &a.kmap, sl * 64, kvh, i0.x + (t0 + j) * kTK, l,
-                               &c->full[s], evict_first);
+              tma_load_4d_hint(kdst + sl * Gm::kSSlab, &a.kmap2, sl * 64, kvh, i0.x + k0, l, &c->full[s],
+                               evict_first);
             } else {  // read again by the next row chunk
-              tma_load_4d(kdst + sl * Gm::kKSlab, &a.kmap, sl * 64, kvh, i0.x + (t0 + j) * kTK, l, &c->full[s]);
+              tma_load_4d(kdst + sl * Gm::kSSlab, &a.kmap2, sl * 64, kvh, i0.x + k0, l, &c->full[s]);
             }
           } else {
-            tma_load_2d(kdst + sl * Gm::kKSlab, &a.kelmap, sl * 64,
-                        (u * p.h_kv + kvh) * p.max_elite + (t0 + j) * kTK, &c->full[s]);
+            tma_load_2d(kdst + sl * Gm::kSSlab, &a.kelmap, sl * 64, (u * p.h_kv + kvh) * p.max_elite + k0,
+                        &c->full[s]);
           }
         }
         if (j == 0) {
@@ -252,6 +294,9 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
   mbar_arrive(&c->full[s]);
 }
 
+// Eight warps; warp w owns keys 32w .. 32w+31 of a stage (four 8-key mma N
+// tiles).  Thread (g4 = lane/4, c4 = lane%4) holds, for query rows g4 and g4+8
+// of each 16-row M tile, keys 32w + 8nt + 2c4 + {0, 1}, nt = 0..3.
 template <int D>
 __device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
   using Gm = SGeo<D>;
@@ -263,11 +308,11 @@ __device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
   const int g4 = lane >> 2, c4 = lane & 3;
   const uint32_t sbase = smem_u32(sm);
   // ldmatrix lane roles: key rows as the B operand, query rows as the A operand
-  const int kr = 16 * warp + (lane & 7) + 8 * (lane >> 4);
+  const int kr = 32 * warp + (lane & 7) + 8 * (lane >> 4);
   const int kc = (lane >> 3) & 1;
   const int qr = lane & 15, qc = lane >> 4;
   const float scale = p.scale_log2;
-  const long long TV = p.total_visual;
+  const long long LS = lg_stride(p);
   uint32_t qf[2][KS][4];
   float m_run[2][2], s_run[2][2];
   int mts = 1, par = 0;
@@ -298,58 +343,86 @@ __device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
           s_run[mt][hh] = 0.f;
         }
     }
-    float acc[2][2][4];
+    float acc[2][4][4];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
-    const uint32_t ks = sbase + (uint32_t)(s * Gm::kKBytes);
+    const bool busy = 32 * warp < h.klim;  // a warp whose keys are all masked skips the tile
+    if (busy) {
+      const uint32_t ks = sbase + (uint32_t)(s * Gm::kSBytes);
 #pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-      const int slab = kk >> 2, c0 = (kk & 3) * 2;
-      uint32_t b[4];
-      ldsm_x4(b, swz(ks + slab * Gm::kKSlab, kr, c0 + kc));
-      mma_bf16_16816(acc[0][0], qf[0][kk], b[0], b[1]);
-      mma_bf16_16816(acc[0][1], qf[0][kk], b[2], b[3]);
-      if (mts > 1) {
-        mma_bf16_16816(acc[1][0], qf[1][kk], b[0], b[1]);
-        mma_bf16_16816(acc[1][1], qf[1][kk], b[2], b[3]);
+      for (int kk = 0; kk < KS; ++kk) {
+        const int slab = kk >> 2, c0 = (kk & 3) * 2;
+        uint32_t b0[4], b1[4];
+        ldsm_x4(b0, swz(ks + slab * Gm::kSSlab, kr, c0 + kc));
+        ldsm_x4(b1, swz(ks + slab * Gm::kSSlab, kr + 16, c0 + kc));
+        mma_bf16_16816(acc[0][0], qf[0][kk], b0[0], b0[1]);
+        mma_bf16_16816(acc[0][1], qf[0][kk], b0[2], b0[3]);
+        mma_bf16_16816(acc[0][2], qf[0][kk], b1[0], b1[1]);
+        mma_bf16_16816(acc[0][3], qf[0][kk], b1[2], b1[3]);
+        if (mts > 1) {
+          mma_bf16_16816(acc[1][0], qf[1][kk], b0[0], b0[1]);
+          mma_bf16_16816(acc[1][1], qf[1][kk], b0[2], b0[3]);
+          mma_bf16_16816(acc[1][2], qf[1][kk], b1[0], b1[1]);
+          mma_bf16_16816(acc[1][3], qf[1][kk], b1[2], b1[3]);
+        }
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&c->empty[s]);  // the tile is read: the producer may refill it
+    if (lane == 0) mbar_arrive(&c->empty[s]);  // the stage is read: the producer may refill it
 
-    // epilogue: store logits (single-chunk units), update the running pairs
-    float* lbase = nullptr;
-    if (h.store) lbase = w.lg + ((size_t)h.l * p.h_kv + h.kvh) * kRC * TV + h.vis0 + (long long)h.tile * kTK;
+    if (busy) {
+      // epilogue: store logits (single-chunk units), update the running pairs
+      float* lbase = nullptr;
+      if (h.store) {
+        lbase = w.lg + ((size_t)h.l * p.h_kv + h.kvh) * kRC * LS + lg_col0(h.vis0, h.b) + h.key0;
+      }
+      const bool full = h.klim >= Gm::kSK;
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      if (mt < mts) {
+      for (int mt = 0; mt < 2; ++mt) {
+        if (mt < mts) {
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int row = 16 * mt + g4 + 8 * hh;
-          if (row < h.rows) {
-            float v[4];
-            float mx = -INFINITY;
+          for (int hh = 0; hh < 2; ++hh) {
+            const int row = 16 * mt + g4 + 8 * hh;
+            if (row < h.rows) {
+              float v[8];
+              float mx = -INFINITY;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int key = 16 * warp + 8 * nt + 2 * c4 + e;
-                const float x = acc[mt][nt][2 * hh + e] * scale;
-                v[2 * nt + e] = key < h.klim ? x : -INFINITY;
-                mx = fmaxf(mx, v[2 * nt + e]);
-                if (lbase && key < h.klim) lbase[(size_t)row * TV + key] = x;
+              for (int nt = 0; nt < 4; ++nt) {
+                const int key = 32 * warp + 8 * nt + 2 * c4;
+                const float x0 = acc[mt][nt][2 * hh] * scale, x1 = acc[mt][nt][2 * hh + 1] * scale;
+                if (full) {
+                  v[2 * nt] = x0;
+                  v[2 * nt + 1] = x1;
+                  if (lbase) *reinterpret_cast<float2*>(lbase + (size_t)row * LS + key) = make_float2(x0, x1);
+                } else {
+                  v[2 * nt] = key < h.klim ? x0 : -INFINITY;
+                  v[2 * nt + 1] = key + 1 < h.klim ? x1 : -INFINITY;
+                  if (lbase) {
+                    float* dst = lbase + (size_t)row * LS + key;
+                    if (key + 1 < h.klim) {
+                      *reinterpret_cast<float2*>(dst) = make_float2(x0, x1);
+                    } else if (key < h.klim) {
+                      *dst = x0;
+                    }
+                  }
+                }
+                mx = fmaxf(mx, fmaxf(v[2 * nt], v[2 * nt + 1]));
               }
-            const float mn = fmaxf(m_run[mt][hh], mx);
-            if (mn != -INFINITY) {
-              float sum = s_run[mt][hh] * exp2f(m_run[mt][hh] - mn);
+              // running (max, sum of exp2): rescale only when the maximum grows
+              if (mx > m_run[mt][hh]) {
+                s_run[mt][hh] *= exp2f(m_run[mt][hh] - mx);
+                m_run[mt][hh] = mx;
+              }
+              if (m_run[mt][hh] != -INFINITY) {
+                float sum = 0.f;
 #pragma unroll
-              for (int q = 0; q < 4; ++q) sum += exp2f(v[q] - mn);
-              s_run[mt][hh] = sum;
-              m_run[mt][hh] = mn;
+                for (int q = 0; q < 8; ++q) sum += exp2f(v[q] - m_run[mt][hh]);
+                s_run[mt][hh] += sum;
+              }
             }
           }
         }
@@ -411,6 +484,12 @@ __global__ void __launch_bounds__(kThreads1, 1) stream_p1_kernel(const __grid_co
 
 // ------------------------------------------------------------------ pass 2
 
+constexpr int kKeysP2 = kT2;  // keys per pass-2 CTA (one per thread)
+
+// One CTA per (unit, 256 keys).  Single-chunk units: the quads of the CTA
+// merge the row LSEs, then each thread sums exp2(logit - lse) over the rows of
+// every KV head for its key (eight rows' loads in flight).  Multi-chunk units:
+// the first CTA of the unit writes its row LSEs for pass 2k.
 __global__ void __launch_bounds__(kT2) stream_p2_kernel(const __grid_constant__ SArgs a) {
   const Dev& p = a.p;
   const Ws& w = a.w;
@@ -441,34 +520,36 @@ __global__ void __launch_bounds__(kT2) stream_p2_kernel(const __grid_constant__ 
     }
     return;
   }
-  const int k0 = blockIdx.y * kT2;
+  const int k0 = blockIdx.y * kKeysP2;
   if (k0 >= n_v) return;
-  const int l = u / p.B;
-  for (int q = tid; q < p.h_kv * rows; q += kT2) {
-    const int kvh = q / rows, r = q % rows;
-    lse_s[kvh * kRC + r] = row_lse(p, w, u, kvh, r, chv);
+  const int l = u / p.B, b = u % p.B;
+  // row LSEs, four lanes per row (whole quads iterate together)
+  for (int q4 = tid >> 2; q4 < (p.h_kv * rows + kT2 / 4 - 1) / (kT2 / 4) * (kT2 / 4); q4 += kT2 / 4) {
+    const int qq = min(q4, p.h_kv * rows - 1);
+    const int kvh = qq / rows, r = qq % rows;
+    const float lse = row_lse4(p, w, u, kvh, r, chv, tid & 3);
+    if (q4 < p.h_kv * rows && (tid & 3) == 0) lse_s[kvh * kRC + r] = lse;
   }
   __syncthreads();
-  const long long TV = p.total_visual;
+  const long long LS = lg_stride(p);
   const int key = k0 + tid;
-  float* iv = w.iv + (size_t)l * TV + i0.y;
   if (key < n_v) {
-    const float* col = w.lg + (size_t)l * p.h_kv * kRC * TV + i0.y + key;
+    const float* col = w.lg + (size_t)l * p.h_kv * kRC * LS + lg_col0(i0.y, b) + key;
     float acc = 0.f;
     for (int kvh = 0; kvh < p.h_kv; ++kvh) {
-      const float* ch = col + (size_t)kvh * kRC * TV;
+      const float* ch = col + (size_t)kvh * kRC * LS;
       const float* ls = lse_s + kvh * kRC;
       int r = 0;
       for (; r + 8 <= rows; r += 8) {
         float x[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = __ldcg(ch + (size_t)(r + q) * TV);
+        for (int q = 0; q < 8; ++q) x[q] = __ldcg(ch + (size_t)(r + q) * LS);
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc += exp2f(x[q] - ls[r + q]);
       }
-      for (; r < rows; ++r) acc += exp2f(__ldcg(ch + (size_t)r * TV) - ls[r]);
+      for (; r < rows; ++r) acc += exp2f(__ldcg(ch + (size_t)r * LS) - ls[r]);
     }
-    iv[key] = acc / (float)(p.h_q * n_tk);
+    w.iv[(size_t)l * p.total_visual + i0.y + key] = acc / (float)(p.h_q * n_tk);
   }
 }
 
@@ -640,7 +721,7 @@ cudaError_t launch_p1_t(const Dev& p, const StreamMaps& m, const Ws& w, int sms,
   using Gm = SGeo<D>;
   SArgs a;
   std::memset(&a, 0, sizeof a);
-  a.kmap = m.kmap;
+  a.kmap2 = m.kmap2;
   a.qmap = m.qmap;
   a.kelmap = m.kelmap;
   a.p = p;
@@ -670,7 +751,7 @@ cudaError_t launch_p2k_t(const Dev& p, const StreamMaps& m, const Ws& w, int sms
 
 bool stream_eligible(const Dev& p, const LayerPtrs& lp) {
   if (p.dtype != AIRCACHE_BF16 || (p.d != 64 && p.d != 128)) return false;
-  if ((p.max_visual + kT2 - 1) / kT2 > 65535 || p.h_kv * kRC * (int)sizeof(float) > 48 * 1024) return false;
+  if ((p.max_visual + kKeysP2 - 1) / kKeysP2 > 65535 || p.h_kv * kRC * (int)sizeof(float) > 48 * 1024) return false;
   const long long U = (long long)p.L * p.B;
   if (U * p.rows_max + kRC > INT32_MAX || U * p.h_kv * p.max_elite + kTK > INT32_MAX) {
     return false;  // TMA row coordinates are 32-bit
@@ -682,6 +763,7 @@ bool stream_eligible(const Dev& p, const LayerPtrs& lp) {
 bool encode_stream_maps(const Dev& p, const LayerPtrs& lp, const Ws& w, StreamMaps* m) {
   const long long U = (long long)p.L * p.B;
   return w.lg && w.part_s && encode_keys<__nv_bfloat16>(&m->kmap, p, lp, kTK) &&
+         encode_keys<__nv_bfloat16>(&m->kmap2, p, lp, 2 * kTK) &&
          encode_rows<__nv_bfloat16>(&m->qmap, w.qel, p.d, U * p.rows_max, kRC) &&
          encode_rows<__nv_bfloat16>(&m->kelmap, w.kel, p.d, U * p.h_kv * p.max_elite, kTK);
 }
@@ -695,8 +777,11 @@ cudaError_t launch_stream_p2(const Dev& p, const Ws& w, cudaStream_t s) {
   std::memset(&a, 0, sizeof a);
   a.p = p;
   a.w = w;
-  const dim3 grid((unsigned)(p.L * p.B), (unsigned)((p.max_visual + kT2 - 1) / kT2));
-  return launch_pdl(stream_p2_kernel, grid, dim3(kT2), sizeof(float) * p.h_kv * kRC, s, a);
+  const dim3 grid((unsigned)(p.L * p.B), (unsigned)((p.max_visual + kKeysP2 - 1) / kKeysP2));
+  const int smem = (int)sizeof(float) * p.h_kv * kRC;
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(stream_p2_kernel), smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(stream_p2_kernel, grid, dim3(kT2), smem, s, a);
 }
 
 cudaError_t launch_stream_p2k(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s) {
