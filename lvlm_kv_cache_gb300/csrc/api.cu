@@ -147,7 +147,7 @@ size_t carve(const Dev& d, char* base, Ws* w) {
   };
   Ws t;
   std::memset(&t, 0, sizeof t);
-  // zeroed block: error, cnt_all, ticket, ticket_n, list_n[3], cnt_req[B],
+  // zeroed block: error, cnt_all, ticket, ticket_n, list_n[4], cnt_req[B],
   // cnt_p1/cnt_p2/lse_ready/p2claim[L*B]
   const size_t zbytes = 40 + sizeof(uint32_t) * (d.B + 4 * LB);
   char* zero = take(zbytes);
@@ -167,8 +167,8 @@ size_t carve(const Dev& d, char* base, Ws* w) {
   t.elite = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB * d.max_text));
   t.n_tk = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
   t.stream_list = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
+  t.stream_info = reinterpret_cast<int4*>(take(sizeof(int4) * 2 * LB));
   t.wide_list = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
-  t.multi_list = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
   if (d.dtype == AIRCACHE_BF16) {  // the streaming path exists for bf16 only
     const size_t kvrows = (size_t)d.L * d.h_kv;
     // rows of the streaming path's logit buffer: every request's keys, each

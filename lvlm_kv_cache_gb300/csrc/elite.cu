@@ -228,8 +228,14 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
     } else {
       // route the unit to its scoring path
       if (p.stream_ok) {
-        a.w.stream_list[atomicAdd(&a.w.list_n[0], 1)] = u;
-        if (p.g * base > kRowChunk) a.w.multi_list[atomicAdd(&a.w.list_n[2], 1)] = u;
+        // units with several row chunks (the heavier work) fill the list from the
+        // front, the others from the back: the streaming pass claims the heavy ones first
+        atomicAdd(&a.w.list_n[0], 1);
+        const int slot = p.g * base > kRowChunk ? atomicAdd(&a.w.list_n[2], 1)
+                                                : p.L * p.B - 1 - atomicAdd(&a.w.list_n[3], 1);
+        a.w.stream_list[slot] = u;
+        a.w.stream_info[2 * slot] = make_int4((int)R.seq0, (int)R.vis0, (int)R.txt0, R.n_v);
+        a.w.stream_info[2 * slot + 1] = make_int4(R.n_t, base, 1, u);
       } else {
         a.w.wide_list[atomicAdd(&a.w.list_n[1], 1)] = u;
       }

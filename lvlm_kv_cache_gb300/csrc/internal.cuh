@@ -48,8 +48,8 @@ struct Ws {
   uint32_t* cnt_all;     // [1]   requests whose budget is done
   unsigned long long* ticket;  // [1] next pass-1 work item of the wide scoring kernel
   unsigned long long* ticket_n;  // [1] next pass-1 work item of the streaming path
-  int32_t* list_n;       // [3]   units on the streaming path / the wide path / the streaming
-                         //       path with more than one row chunk per KV head
+  int32_t* list_n;       // [4]   units on the streaming path, on the wide path, streaming units
+                         //       with more than one row chunk per KV head, the other streaming units
   uint32_t* cnt_req;     // [B]   layers of a request whose stats are done
   uint32_t* p2claim;     // [L*B] claimed pass-2 work items per (layer, request)
   uint32_t* cnt_p1;      // [L*B] finished pass-1 items per (layer, request)
@@ -57,9 +57,10 @@ struct Ws {
   uint32_t* lse_ready;   // [L*B] row log-sum-exps published
   int32_t* elite;        // [L*B*max_text]
   int32_t* n_tk;         // [L*B]
-  int32_t* stream_list;  // [L*B] units u = l*B + b on the streaming path (list_n[0] of them, any order)
+  int32_t* stream_list;  // [L*B] streaming units: multi-chunk ones in slots [0, list_n[2]), the
+                         //       others in [L*B - list_n[3], L*B) (any order within each)
+  int4* stream_info;     // [L*B][2] the layout record of stream_list[i] (as uinfo, with .w of the second = u)
   int32_t* wide_list;    // [L*B] units on the wide path (list_n[1] of them, any order)
-  int32_t* multi_list;   // [L*B] streaming units with g * N_tk > 32 (list_n[2] of them)
   float* lg;             // [L][h_kv][32][lg stride] streaming path: logits of row r of KV head h
   float2* part_s;        // [L*B][h_kv][rc_max*32][chn] streaming pass 1: (max, sum of exp2) per (row, chunk)
   int4* uinfo;           // [L*B][2] {seq0, vis0, txt0, N_v}, {N_t, N_tk, 1, 0} per (layer, request)

@@ -135,6 +135,17 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
+// ---------------------------------------------------------------- math
+
+// 2^x with the SFU's base-2 exponential (PTX ex2.approx.ftz: relative error
+// about 2^-22; 2^-inf = 0; results below 2^-126 flush to 0, which only drops
+// terms far below the last bit of the sums they join).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ---------------------------------------------------------------- MMA
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t r[4], const void* ptr) {

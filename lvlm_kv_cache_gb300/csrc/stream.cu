@@ -102,7 +102,7 @@ __device__ __forceinline__ long long lg_stride(const Dev& p) { return (p.total_v
 __device__ __forceinline__ float2 merge_ms(float2 a, float2 b) {
   const float m = fmaxf(a.x, b.x);
   if (m == -INFINITY) return make_float2(-INFINITY, 0.f);
-  return make_float2(m, a.y * exp2f(a.x - m) + b.y * exp2f(b.x - m));
+  return make_float2(m, a.y * fast_exp2(a.x - m) + b.y * fast_exp2(b.x - m));
 }
 
 __device__ __forceinline__ bool stream_unit(const Dev& p, int u, const int4& i0, const int4& i1) {
@@ -113,6 +113,12 @@ __device__ __forceinline__ bool stream_unit(const Dev& p, int u, const int4& i0,
 }
 
 __device__ __forceinline__ int rows_per_kv(const Dev& p) { return p.rc_max * kRC; }
+
+// Slot in stream_list / stream_info of position li of the streaming units in
+// claim order (multi-chunk units first; n_multi of n_total).
+__device__ __forceinline__ int stream_slot(const Dev& p, int li, int n_multi, int n_total) {
+  return li < n_multi ? li : p.L * p.B - (n_total - li);
+}
 
 // Row partial (row, chunk) of KV head kvh of unit u.
 __device__ __forceinline__ size_t part_index(const Dev& p, int u, int kvh, int row, int chunk) {
@@ -172,8 +178,12 @@ struct Ctl1 {
   float2 red[2][kCW][kRC];
 };
 
-// One thread.  Stages: a visual stage is 256 keys (one TMA box of 256 rows per
-// column slab), a text stage up to 128 elite keys.
+// One thread.  Items (unit, KV head, chunk of four visual tiles or the elite
+// text keys) are claimed from an atomic counter; the claim after the current
+// one and its unit's layout record (stored beside the list slot by the elite
+// kernel) are fetched while the current item's stages are issued, so no
+// dependent load stalls the ring between items.  A visual stage is 256 keys
+// (one TMA box of 256 rows per column slab), a text stage up to 128 elite keys.
 template <int D>
 __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
   using Gm = SGeo<D>;
@@ -182,20 +192,30 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
   const Ws& w = a.w;
   const uint32_t sbase = smem_u32(sm);
   const long long per_unit = (long long)p.h_kv * p.chn;
-  const long long total = (long long)__ldcg(&w.list_n[0]) * per_unit;
+  const int n_total = __ldcg(&w.list_n[0]), n_multi = __ldcg(&w.list_n[2]);
+  const long long total = (long long)n_total * per_unit;
   const uint64_t evict_first = l2_evict_first_policy();
+  auto record = [&](long long claim, int4& r0, int4& r1) {
+    if (claim < total) {
+      const int slot = stream_slot(p, (int)(claim / per_unit), n_multi, n_total);
+      r0 = __ldcg(&w.stream_info[2 * slot]);
+      r1 = __ldcg(&w.stream_info[2 * slot + 1]);
+    }
+  };
   long long st = 0;  // stages issued
-  int sub = 0;       // row-chunk items issued (selects the query buffer)
+  int sub = 0;       // row-chunk passes issued (selects the query buffer)
   bool ok = true;
   long long claim = (long long)atomicAdd(w.ticket_n, 1ULL);
+  long long next = (long long)atomicAdd(w.ticket_n, 1ULL);
+  int4 i0 = make_int4(0, 0, 0, 0), i1 = make_int4(0, 0, 0, 0);
+  record(claim, i0, i1);
   while (ok && claim < total) {
-    const long long next = (long long)atomicAdd(w.ticket_n, 1ULL);  // used at the loop's end
-    const int li = (int)(claim / per_unit);
+    int4 n0 = make_int4(0, 0, 0, 0), n1 = make_int4(0, 0, 0, 0);
+    record(next, n0, n1);                                               // used by the next item
+    const long long next2 = (long long)atomicAdd(w.ticket_n, 1ULL);  // the claim after that
     const int rem = (int)(claim % per_unit);
     const int kvh = rem / p.chn, ch = rem % p.chn;
-    const int u = __ldcg(&w.stream_list[li]);
-    const int4 i0 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u]) : make_int4(0, 0, 0, 0);
-    const int4 i1 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u + 1]) : make_int4(0, 0, 0, 0);
+    const int u = i1.w;
     if (!stream_unit(p, u, i0, i1)) {
       set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
       break;
@@ -204,82 +224,84 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
     const int n_rc = (rows + kRC - 1) / kRC;
     const int tv = (n_v + kTK - 1) / kTK;
     const int chv = (tv + kCK - 1) / kCK;
-    int kind, key0, nkeys, stage_keys;
-    if (ch < p.chn - 1) {
-      if (ch >= chv) {  // a chunk past this unit's keys
-        claim = next;
-        continue;
+    const bool skip = ch < p.chn - 1 && ch >= chv;  // a chunk past this unit's keys
+    if (!skip) {
+      int kind, key0, nkeys, stage_keys;
+      if (ch < p.chn - 1) {
+        kind = kVis;
+        key0 = ch * kCK * kTK;
+        nkeys = min(kCK * kTK, n_v - key0);
+        stage_keys = Gm::kSK;
+      } else {
+        kind = kTxt;  // elite text keys: at most max_elite <= 8192, 128 per stage
+        key0 = 0;
+        nkeys = n_tk;
+        stage_keys = kTK;
       }
-      kind = kVis;
-      key0 = ch * kCK * kTK;
-      nkeys = min(kCK * kTK, n_v - key0);
-      stage_keys = Gm::kSK;
-    } else {
-      kind = kTxt;  // elite text keys: at most max_elite <= 8192, 128 per stage
-      key0 = 0;
-      nkeys = n_tk;
-      stage_keys = kTK;
-    }
-    const int nst = (nkeys + stage_keys - 1) / stage_keys;
-    const uint32_t kbytes = kind == kVis ? (uint32_t)Gm::kSBytes : (uint32_t)(Gm::kNH * kTK * 128);
-    const int l = u / p.B;
-    for (int rc = 0; ok && rc < n_rc; ++rc, ++sub) {
-      const int qb = sub & 1;
-      // the query buffer is free once every consumer warp has loaded the chunk that used it before
-      if (!mbar_wait(&c->qempty[qb], (uint32_t)(((sub >> 1) & 1) ^ 1))) {
-        ok = false;
-        break;
-      }
-      for (int j = 0; j < nst; ++j, ++st) {
-        const int s = (int)(st % NS);
-        if (!mbar_wait(&c->empty[s], (uint32_t)(((st / NS) & 1) ^ 1))) {
+      const int nst = (nkeys + stage_keys - 1) / stage_keys;
+      const uint32_t kbytes = kind == kVis ? (uint32_t)Gm::kSBytes : (uint32_t)(Gm::kNH * kTK * 128);
+      const int l = u / p.B;
+      for (int rc = 0; ok && rc < n_rc; ++rc, ++sub) {
+        const int qb = sub & 1;
+        // the query buffer is free once every consumer warp has loaded the pass that used it before
+        if (!mbar_wait(&c->qempty[qb], (uint32_t)(((sub >> 1) & 1) ^ 1))) {
           ok = false;
           break;
         }
-        const int k0 = key0 + j * stage_keys;
-        Hdr& h = c->hdr[s];
-        h.kind = kind;
-        h.u = u;
-        h.l = l;
-        h.kvh = kvh;
-        h.key0 = k0;
-        h.klim = min(stage_keys, (kind == kVis ? n_v : n_tk) - k0);
-        h.rows = min(kRC, rows - rc * kRC);
-        h.r0 = rc * kRC;
-        h.first = (j == 0);
-        h.last = (j == nst - 1);
-        h.chunk = ch;
-        h.qbuf = qb;
-        h.store = (kind == kVis && n_rc == 1) ? 1 : 0;
-        h.b = u % p.B;
-        h.vis0 = i0.y;
-        mbar_arrive_expect_tx(&c->full[s], kbytes + (j == 0 ? (uint32_t)Gm::kQBytes : 0u));
-        const uint32_t kdst = sbase + (uint32_t)(s * Gm::kSBytes);
-#pragma unroll
-        for (int sl = 0; sl < Gm::kNH; ++sl) {
-          if (kind == kVis) {
-            if (n_rc == 1) {  // read once
-              tma_load_4d_hint(kdst + sl * Gm::kSSlab, &a.kmap2, sl * 64, kvh, i0.x + k0, l, &c->full[s],
-                               evict_first);
-            } else {  // read again by the next row chunk
-              tma_load_4d(kdst + sl * Gm::kSSlab, &a.kmap2, sl * 64, kvh, i0.x + k0, l, &c->full[s]);
-            }
-          } else {
-            tma_load_2d(kdst + sl * Gm::kSSlab, &a.kelmap, sl * 64, (u * p.h_kv + kvh) * p.max_elite + k0,
-                        &c->full[s]);
+        for (int j = 0; j < nst; ++j, ++st) {
+          const int s = (int)(st % NS);
+          if (!mbar_wait(&c->empty[s], (uint32_t)(((st / NS) & 1) ^ 1))) {
+            ok = false;
+            break;
           }
-        }
-        if (j == 0) {
-          const uint32_t qdst = sbase + (uint32_t)(Gm::kQOff + qb * Gm::kQBytes);
+          const int k0 = key0 + j * stage_keys;
+          Hdr& h = c->hdr[s];
+          h.kind = kind;
+          h.u = u;
+          h.l = l;
+          h.kvh = kvh;
+          h.key0 = k0;
+          h.klim = min(stage_keys, (kind == kVis ? n_v : n_tk) - k0);
+          h.rows = min(kRC, rows - rc * kRC);
+          h.r0 = rc * kRC;
+          h.first = (j == 0);
+          h.last = (j == nst - 1);
+          h.chunk = ch;
+          h.qbuf = qb;
+          h.store = (kind == kVis && n_rc == 1) ? 1 : 0;
+          h.b = u % p.B;
+          h.vis0 = i0.y;
+          mbar_arrive_expect_tx(&c->full[s], kbytes + (j == 0 ? (uint32_t)Gm::kQBytes : 0u));
+          const uint32_t kdst = sbase + (uint32_t)(s * Gm::kSBytes);
 #pragma unroll
           for (int sl = 0; sl < Gm::kNH; ++sl) {
-            tma_load_2d(qdst + sl * Gm::kQSlab, &a.qmap, sl * 64, u * p.rows_max + kvh * rows + rc * kRC,
-                        &c->full[s]);
+            if (kind == kVis) {
+              if (n_rc == 1) {  // read once
+                tma_load_4d_hint(kdst + sl * Gm::kSSlab, &a.kmap2, sl * 64, kvh, i0.x + k0, l, &c->full[s],
+                                 evict_first);
+              } else {  // read again by the next row chunk
+                tma_load_4d(kdst + sl * Gm::kSSlab, &a.kmap2, sl * 64, kvh, i0.x + k0, l, &c->full[s]);
+              }
+            } else {
+              tma_load_2d(kdst + sl * Gm::kSSlab, &a.kelmap, sl * 64, (u * p.h_kv + kvh) * p.max_elite + k0,
+                          &c->full[s]);
+            }
+          }
+          if (j == 0) {
+            const uint32_t qdst = sbase + (uint32_t)(Gm::kQOff + qb * Gm::kQBytes);
+#pragma unroll
+            for (int sl = 0; sl < Gm::kNH; ++sl) {
+              tma_load_2d(qdst + sl * Gm::kQSlab, &a.qmap, sl * 64, u * p.rows_max + kvh * rows + rc * kRC,
+                          &c->full[s]);
+            }
           }
         }
       }
     }
     claim = next;
+    next = next2;
+    i0 = n0;
+    i1 = n1;
   }
   if (!ok) {
     set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
@@ -375,10 +397,12 @@ __device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
     if (lane == 0) mbar_arrive(&c->empty[s]);  // the stage is read: the producer may refill it
 
     if (busy) {
-      // epilogue: store logits (single-chunk units), update the running pairs
+      // epilogue: store the raw logits (single-chunk units; the scale is applied
+      // where they are read), update the running pairs in base-2 units
       float* lbase = nullptr;
       if (h.store) {
-        lbase = w.lg + ((size_t)h.l * p.h_kv + h.kvh) * kRC * LS + lg_col0(h.vis0, h.b) + h.key0;
+        lbase = w.lg + ((size_t)h.l * p.h_kv + h.kvh) * kRC * LS + lg_col0(h.vis0, h.b) + h.key0 +
+                32 * warp + 2 * c4;
       }
       const bool full = h.klim >= Gm::kSK;
 #pragma unroll
@@ -390,37 +414,39 @@ __device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
             if (row < h.rows) {
               float v[8];
               float mx = -INFINITY;
+              float* dst = lbase ? lbase + (size_t)row * LS : nullptr;
 #pragma unroll
               for (int nt = 0; nt < 4; ++nt) {
                 const int key = 32 * warp + 8 * nt + 2 * c4;
-                const float x0 = acc[mt][nt][2 * hh] * scale, x1 = acc[mt][nt][2 * hh + 1] * scale;
+                const float x0 = acc[mt][nt][2 * hh], x1 = acc[mt][nt][2 * hh + 1];
                 if (full) {
                   v[2 * nt] = x0;
                   v[2 * nt + 1] = x1;
-                  if (lbase) *reinterpret_cast<float2*>(lbase + (size_t)row * LS + key) = make_float2(x0, x1);
+                  if (dst) *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(x0, x1);
                 } else {
                   v[2 * nt] = key < h.klim ? x0 : -INFINITY;
                   v[2 * nt + 1] = key + 1 < h.klim ? x1 : -INFINITY;
-                  if (lbase) {
-                    float* dst = lbase + (size_t)row * LS + key;
+                  if (dst) {
                     if (key + 1 < h.klim) {
-                      *reinterpret_cast<float2*>(dst) = make_float2(x0, x1);
+                      *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(x0, x1);
                     } else if (key < h.klim) {
-                      *dst = x0;
+                      dst[8 * nt] = x0;
                     }
                   }
                 }
                 mx = fmaxf(mx, fmaxf(v[2 * nt], v[2 * nt + 1]));
               }
-              // running (max, sum of exp2): rescale only when the maximum grows
-              if (mx > m_run[mt][hh]) {
-                s_run[mt][hh] *= exp2f(m_run[mt][hh] - mx);
-                m_run[mt][hh] = mx;
-              }
-              if (m_run[mt][hh] != -INFINITY) {
+              // running (max, sum of exp2) of the scaled logits: rescale only when the maximum grows
+              if (mx != -INFINITY) {
+                const float ms = mx * scale;
+                if (ms > m_run[mt][hh]) {
+                  s_run[mt][hh] *= fast_exp2(m_run[mt][hh] - ms);
+                  m_run[mt][hh] = ms;
+                }
+                const float neg = -m_run[mt][hh];
                 float sum = 0.f;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) sum += exp2f(v[q] - m_run[mt][hh]);
+                for (int q = 0; q < 8; ++q) sum += fast_exp2(fmaf(v[q], scale, neg));
                 s_run[mt][hh] += sum;
               }
             }
@@ -499,8 +525,9 @@ __global__ void __launch_bounds__(kT2) stream_p2_kernel(const __grid_constant__ 
   pdl_wait();  // pass 1's partials and logits
   if (*(volatile int32_t*)w.error != 0) return;
   const int li = blockIdx.x;
-  if (li >= __ldcg(&w.list_n[0])) return;
-  const int u = __ldcg(&w.stream_list[li]);
+  const int n_total = __ldcg(&w.list_n[0]);
+  if (li >= n_total) return;
+  const int u = __ldcg(&w.stream_list[stream_slot(p, li, __ldcg(&w.list_n[2]), n_total)]);
   const int4 i0 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u]) : make_int4(0, 0, 0, 0);
   const int4 i1 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u + 1]) : make_int4(0, 0, 0, 0);
   if (!stream_unit(p, u, i0, i1)) {
@@ -532,6 +559,7 @@ __global__ void __launch_bounds__(kT2) stream_p2_kernel(const __grid_constant__ 
   }
   __syncthreads();
   const long long LS = lg_stride(p);
+  const float scale = p.scale_log2;  // stored logits are raw q.k
   const int key = k0 + tid;
   if (key < n_v) {
     const float* col = w.lg + (size_t)l * p.h_kv * kRC * LS + lg_col0(i0.y, b) + key;
@@ -545,9 +573,9 @@ __global__ void __launch_bounds__(kT2) stream_p2_kernel(const __grid_constant__ 
 #pragma unroll
         for (int q = 0; q < 8; ++q) x[q] = __ldcg(ch + (size_t)(r + q) * LS);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc += exp2f(x[q] - ls[r + q]);
+        for (int q = 0; q < 8; ++q) acc += fast_exp2(fmaf(x[q], scale, -ls[r + q]));
       }
-      for (; r < rows; ++r) acc += exp2f(__ldcg(ch + (size_t)r * LS) - ls[r]);
+      for (; r < rows; ++r) acc += fast_exp2(fmaf(__ldcg(ch + (size_t)r * LS), scale, -ls[r]));
     }
     w.iv[(size_t)l * p.total_visual + i0.y + key] = acc / (float)(p.h_q * n_tk);
   }
@@ -598,7 +626,7 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
   if (tid == 0) fence_proxy_async_global();  // LSEs were written by the previous kernel's generic stores
   for (long long item = blockIdx.x; item < total; item += gridDim.x) {
     const int li = (int)(item / TVmax), tile = (int)(item % TVmax);
-    const int u = __ldcg(&w.multi_list[li]);
+    const int u = __ldcg(&w.stream_list[li]);  // slots [0, list_n[2]): the multi-chunk units
     const int4 i0 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u]) : make_int4(0, 0, 0, 0);
     const int4 i1 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u + 1]) : make_int4(0, 0, 0, 0);
     if (!stream_unit(p, u, i0, i1)) {
@@ -692,7 +720,7 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
 #pragma unroll
               for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) accK[nt][e] += exp2f(acc[mt][nt][2 * hh + e] * scale - lse);
+                for (int e = 0; e < 2; ++e) accK[nt][e] += fast_exp2(fmaf(acc[mt][nt][2 * hh + e], scale, -lse));
             }
           }
         __syncthreads();  // every thread is done with the slot
