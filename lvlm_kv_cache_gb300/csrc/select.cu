@@ -7,10 +7,12 @@
 // (otherwise re-read from global memory each pass).  A 4-digit (8-bit)
 // MSB-first radix select finds the exact keep-th largest key T and how many
 // keys equal to T are still wanted; histogram increments are aggregated over
-// the lanes of a warp that share a digit.  A final sweep in which each thread
-// owns a contiguous run of positions emits every key > T plus the
-// lowest-position keys == T, in ascending position, with two block-wide
-// exclusive scans.  Integer work only: the result is exact and deterministic.
+// the lanes of a warp that share a digit, and after the first digit the keys
+// that can still be T are compacted so the later passes touch only them.  A
+// final sweep in which each thread owns a contiguous run of positions emits
+// every key > T plus the lowest-position keys == T, in ascending position,
+// with block-wide exclusive scans (one when every key == T is taken).
+// Integer work only: the result is exact and deterministic.
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -19,7 +21,7 @@ namespace {
 
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSmemKeys = 40 * 1024;  // units up to this many keys are staged in shared memory
+constexpr int kSmemKeys = 24 * 1024;  // units up to this many keys are staged in shared memory
 
 struct SelectArgs {
   Dev p;
@@ -68,10 +70,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   const Ws& w = a.w;
   const int b = blockIdx.x, l = blockIdx.y, u = l * p.B + b;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  extern __shared__ uint32_t keys_s[];
+  extern __shared__ uint32_t keys_s[];  // [smem_keys] keys, then [smem_keys] candidates
   __shared__ unsigned hist[256];
   __shared__ int wsum[kSelWarps + 1];
-  __shared__ unsigned sel_digit, sel_above;
+  __shared__ unsigned sel_digit, sel_above, sel_count;
   pdl_trigger();
   pdl_wait();  // I_v and the keep counts
   if (*(volatile int32_t*)w.error != 0) return;
@@ -107,15 +109,19 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   }
   auto key_at = [&](int i) -> uint32_t { return staged ? keys_s[i] : order_key(__ldcg(x + i)); };
 
+  uint32_t* cand = keys_s + a.smem_keys;  // keys still able to be the answer (staged units)
+  int n_cand = n;                         // after the first digit: their number
   uint32_t prefix = 0, mask = 0;
   unsigned want = (unsigned)k;  // keys >= the answer still to account for
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
     __syncthreads();
-    for (int i0 = 0; i0 < n; i0 += kSelThreads) {
+    const bool from_cand = staged && shift < 24;
+    const int m = from_cand ? n_cand : n;
+    for (int i0 = 0; i0 < m; i0 += kSelThreads) {
       const int i = i0 + tid;
-      const uint32_t key = i < n ? key_at(i) : 0u;
-      const bool in = i < n && (key & mask) == prefix;
+      const uint32_t key = i < m ? (from_cand ? cand[i] : key_at(i)) : 0u;
+      const bool in = i < m && (key & mask) == prefix;
       const unsigned digit = in ? ((key >> shift) & 255u) : 256u;
       // one increment per distinct digit of the warp
       const unsigned peers = __match_any_sync(0xffffffffu, digit);
@@ -145,6 +151,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
           if (run < want && want <= run + cnt[i]) {
             sel_digit = 8 * (31 - lane) + (7 - i);
             sel_above = run;
+            sel_count = cnt[i];
           }
           run += cnt[i];
         }
@@ -154,12 +161,42 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
     want -= sel_above;
     prefix |= sel_digit << shift;
     mask |= 255u << shift;
+    if (staged && shift == 24) {
+      // compact the keys whose top digit is the selected one (order is irrelevant
+      // here: one shared counter, one atomic per warp and pass over the keys)
+      if (tid == 0) sel_above = 0;
+      __syncthreads();
+      for (int i0 = 0; i0 < n; i0 += kSelThreads) {
+        const int i = i0 + tid;
+        const bool c = i < n && (keys_s[i] & mask) == prefix;
+        const unsigned bal = __ballot_sync(0xffffffffu, c);
+        int base = 0;
+        if (lane == 0 && bal) base = (int)atomicAdd(&sel_above, (unsigned)__popc(bal));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (c) cand[base + __popc(bal & ((1u << lane) - 1u))] = keys_s[i];
+      }
+      __syncthreads();
+      n_cand = (int)sel_above;
+      __syncthreads();
+    }
   }
+  const unsigned eq_all = sel_count;  // keys equal to the answer
   // prefix = exact key of the keep-th largest: take every key > prefix and the
   // first `want` keys == prefix in position order.  Thread tid owns positions
   // [tid * per, tid * per + per).
   const int per = (n + kSelThreads - 1) / kSelThreads;
   const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
+  if (want == eq_all) {
+    // every key equal to the answer is taken: keys >= prefix, one scan
+    int n_take = 0;
+    for (int i = i0; i < i1; ++i) n_take += key_at(i) >= prefix ? 1 : 0;
+    int take_total;
+    int pos = block_excl_scan(n_take, wsum, &take_total);
+    for (int i = i0; i < i1; ++i) {
+      if (key_at(i) >= prefix) out[pos++] = i;
+    }
+    return;
+  }
   int n_eq = 0;
   for (int i = i0; i < i1; ++i) n_eq += key_at(i) == prefix ? 1 : 0;
   int eq_total;
@@ -188,6 +225,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
       ++eq_rank;
     }
   }
+  (void)lane;
 }
 
 }  // namespace
@@ -197,7 +235,7 @@ cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s) {
   a.p = p;
   a.w = w;
   a.smem_keys = p.max_visual < kSmemKeys ? p.max_visual : kSmemKeys;
-  const int smem = (int)sizeof(uint32_t) * a.smem_keys;
+  const int smem = 2 * (int)sizeof(uint32_t) * a.smem_keys;  // keys + candidates
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(select_kernel), smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(select_kernel, dim3(p.B, p.L), dim3(kSelThreads), smem, s, a);
