@@ -184,13 +184,19 @@ def algorithmic_bytes(spec, n_tk, keep, esize):
             k["elite_window"] += nt * row + qrow + 4 * t
             if esize == 2:
                 k["score_pass1"] += (nv + t) * row + t * qrow
-                k["score_pass2" if g * t <= 32 else "score_pass2k"] += 4 * nv  # I_v written
-                k["stats_budget"] += 4 * nv  # I_v read once more for the moments
+                # I_v written, plus one 48-byte moment record per key block
+                # (256 keys in pass 2, 128 in pass 2k), read back by the stats kernel
+                recs = -(-nv // (256 if g * t <= 32 else 128))
+                k["score_pass2" if g * t <= 32 else "score_pass2k"] += 4 * nv + 48 * recs
+                k["stats_budget"] += 48 * recs
+                iv_passes = 2  # written, read by the selection
             else:
                 k["score_wide"] += (nv + t) * row + t * qrow + 4 * nv
+                recs, iv_passes = 0, 3  # written, read for the moments and by the selection
             k["select_topk"] += 4 * nv + 4 * kp
             k["gather_compact"] += 2 * 2 * (kp + nt) * row + 4 * kp
-            path += (nv + nt) * row + (1 + t) * qrow + 2 * 2 * (kp + nt) * row + 4 * nv * 3 + 8 * kp
+            path += ((nv + nt) * row + (1 + t) * qrow + 2 * 2 * (kp + nt) * row + 4 * nv * iv_passes
+                     + 96 * recs + 8 * kp)
     return k, path
 
 

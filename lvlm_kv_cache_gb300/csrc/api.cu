@@ -122,6 +122,7 @@ Dev make_dev(const aircache_problem* p) {
   const int tv = (d.max_visual + 127) / 128;
   d.chn = (tv + kStreamTiles - 1) / kStreamTiles + 1;
   d.stream_ok = 0;  // set per call from stream_eligible()
+  d.mom_slots = (d.max_visual + 127) / 128;
   return d;
 }
 
@@ -175,6 +176,7 @@ size_t carve(const Dev& d, char* base, Ws* w) {
     // request starting at a multiple of 4 columns (4 columns of padding per request)
     const size_t stride = (size_t)(d.total_visual + 4 * (int64_t)d.B + 7) / 4 * 4;
     t.lg = reinterpret_cast<float*>(take(sizeof(float) * kvrows * kRowChunk * stride));
+    t.mom = reinterpret_cast<float4*>(take(sizeof(float4) * 3 * LB * (size_t)d.mom_slots));
     t.part_s = reinterpret_cast<float2*>(take(sizeof(float2) * LB * d.h_kv * d.rc_max * kRowChunk * d.chn));
   }
   t.uinfo = reinterpret_cast<int4*>(take(sizeof(int4) * 2 * LB));
@@ -373,7 +375,7 @@ static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, v
     AC_TRY(mark(k++));
     AC_TRY(launch_stream_p2k(dn, maps, w, sms, s));
     AC_TRY(mark(k++));
-    AC_TRY(launch_stats_budget(dn, w, nullptr, out_rows_capacity, true, s));
+    AC_TRY(launch_stats_budget(dn, w, nullptr, out_rows_capacity, true, s, true));
     AC_TRY(mark(k++));
   } else {
     AC_TRY(launch_score(dn, lp, w, plan_score(dn, sms, true, out_rows_capacity), s));

@@ -1,15 +1,19 @@
 // Elite observation window (AirCache notes, "Key design 1": equations Att and k).
 //
-// One CTA per (request, layer).  The last text query of every head is dotted
-// with the N_t text keys of its KV head: the text keys stream through a ring of
-// shared-memory stages (128 keys of one KV head per stage, cp.async), and the
-// logit tile is the same MMA tile as the scoring kernel's (query rows = the g
-// heads of that KV head).  Base-2 logits are kept in shared memory, each head's
-// row is softmaxed in fp32 (max-subtracted), and the rows are summed over heads
-// into P (the head mean up to the common factor 1/H_q, which the threshold test
-// does not see).  The elite set is {j : P[j] >= alpha * max P}, written in
-// ascending order.  When the logits of every head do not fit in shared memory,
-// KV heads are processed in chunks and P accumulates across chunks.
+// One thread-block cluster per (request, layer), one CTA per group of KV heads
+// (a single KV head when H_kv <= 8).  The last text query of every head is
+// dotted with the N_t text keys of its KV head: the text keys stream through a
+// ring of shared-memory stages (128 keys of one KV head per stage, cp.async),
+// and the logit tile is the same MMA tile as the scoring kernel's (query rows =
+// the g heads of that KV head).  Base-2 logits are kept in shared memory, each
+// head's row is softmaxed in fp32 (max-subtracted), and the CTA sums its heads'
+// rows into a partial P.  The partials are added across the cluster through
+// distributed shared memory in CTA order, so every CTA holds the same P (the
+// head mean up to the common factor 1/H_q, which the threshold test does not
+// see).  The elite set is {j : P[j] >= alpha * max P}, in ascending order;
+// each CTA then gathers the elite query rows and text keys of its own KV heads.
+// When the logits of a CTA's heads do not fit in shared memory, its KV heads
+// are processed in chunks and the partial P accumulates across chunks.
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "tile.cuh"
@@ -20,12 +24,15 @@ namespace {
 constexpr int kEliteThreads = 256;
 constexpr int kEliteWarps = kEliteThreads / 32;
 constexpr int kSmemBudget = 220 * 1024;
+constexpr int kMaxCluster = 8;  // portable cluster size
+constexpr int kGatherBatch = 8; // 16-byte loads in flight per thread in the gathers
 
 struct EliteArgs {
   Dev p;
   LayerPtrs lp;
   Ws w;
-  int kv_chunk;  // KV heads whose logits are held at once
+  int kv_chunk;    // KV heads whose logits are held at once
+  int kv_per_cta;  // KV heads of one CTA of the cluster
 };
 
 // Issue the cp.async copies of item i of a KV-head chunk: items run over
@@ -66,25 +73,31 @@ template <typename T, int D, int NS>
 __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_constant__ EliteArgs a) {
   pdl_trigger();  // the next kernel may set up while this one runs
   using G = TileGeom<T, D>;
+  constexpr int kVec = G::kRowBytes / 16;
   const Dev& p = a.p;
-  const int b = blockIdx.x, l = blockIdx.y, u = l * p.B + b;
+  // grid (C, B, L), cluster (C, 1, 1): blockIdx.x is the rank within the cluster
+  const int rank = blockIdx.x, C = gridDim.x;
+  const int b = blockIdx.y, l = blockIdx.z, u = l * p.B + b;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g4 = lane >> 2, c4 = lane & 3;
 
   Req R;
-  if (!load_req(p, b, R)) {
-    if (tid == 0) set_error(a.w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+  if (!load_req(p, b, R)) {  // the same verdict in every CTA of the cluster
+    if (rank == 0 && tid == 0) set_error(a.w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
     return;
   }
   const int n_t = R.n_t;
   const int hc = a.kv_chunk * p.g;  // heads per chunk
+  const int kvb = min(p.h_kv, rank * a.kv_per_cta), kve = min(p.h_kv, kvb + a.kv_per_cta);
 
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* stages = smem;
   float* lg = reinterpret_cast<float*>(smem + NS * G::kStageBytes);  // [hc][max_text]
-  float* P = lg + (size_t)hc * p.max_text;                          // [max_text]
-  float* hmax = P + p.max_text;                                      // [hc]
+  float* P = lg + (size_t)hc * p.max_text;                          // [max_text] this CTA's heads
+  float* Pt = P + p.max_text;                                        // [max_text] every head
+  float* hmax = Pt + p.max_text;                                     // [hc]
   float* hinv = hmax + hc;                                           // [hc]
+  int32_t* pos_s = reinterpret_cast<int32_t*>(hinv + hc);            // [max_elite]
   __shared__ float red[kEliteWarps];
   __shared__ int wcount[kEliteWarps];
 
@@ -94,8 +107,8 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
 
   const int n_kt = (n_t + kTK - 1) / kTK;
   const int n_rc = (p.g + kRC - 1) / kRC;
-  for (int kv0 = 0; kv0 < p.h_kv; kv0 += a.kv_chunk) {
-    const int kv1 = min(p.h_kv, kv0 + a.kv_chunk);
+  for (int kv0 = kvb; kv0 < kve; kv0 += a.kv_chunk) {
+    const int kv1 = min(kve, kv0 + a.kv_chunk);
     const int items = (kv1 - kv0) * n_rc * n_kt;
     __syncthreads();
 #pragma unroll
@@ -156,11 +169,21 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
       P[j] = accp;
     }
   }
+  // P over every head: the CTAs' partials added in rank order (the same sum,
+  // bit for bit, in every CTA of the cluster)
   __syncthreads();
+  cluster_sync_all();  // every CTA's partial P is complete
+  for (int j = tid; j < n_t; j += kEliteThreads) {
+    const uint32_t pj = smem_u32(P + j);
+    float s = 0.f;
+    for (int c = 0; c < C; ++c) s += ld_cluster_f32(cluster_map(pj, (uint32_t)c));
+    Pt[j] = s;
+  }
+  cluster_sync_all();  // no CTA reads another's partial after this point
 
   // max P
   float m = -INFINITY;
-  for (int j = tid; j < n_t; j += kEliteThreads) m = fmaxf(m, P[j]);
+  for (int j = tid; j < n_t; j += kEliteThreads) m = fmaxf(m, Pt[j]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   if (lane == 0) red[warp] = m;
@@ -175,7 +198,7 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
   int base = 0;
   for (int j0 = 0; j0 < n_t; j0 += kEliteThreads) {
     const int j = j0 + tid;
-    const bool take = j < n_t && P[j] >= thr;
+    const bool take = j < n_t && Pt[j] >= thr;
     const unsigned bal = __ballot_sync(0xffffffffu, take);
     const int before = __popc(bal & ((1u << lane) - 1u));
     __syncthreads();
@@ -188,37 +211,71 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
       total += wcount[i];
     }
     const int pos = base + wbase + before;
-    if (take && pos < p.max_elite) out[pos] = j;
+    if (take && pos < p.max_elite) {
+      pos_s[pos] = j;
+      if (rank == 0) out[pos] = j;
+    }
     base += total;
   }
-  // Gather the unit's elite query rows (row kvh*g*N_tk + hh*N_tk + e) and elite
+  // Gather this CTA's elite query rows (row kvh*g*N_tk + hh*N_tk + e) and elite
   // text keys into dense buffers: the scoring kernel then addresses them by
-  // arithmetic alone.
+  // arithmetic alone.  Each thread keeps kGatherBatch loads in flight.
   if (base <= p.max_elite) {
-    __syncthreads();  // the elite list written above is visible to the whole CTA
-    constexpr int kVec = TileGeom<T, D>::kRowBytes / 16;
+    __syncthreads();  // the elite positions are in shared memory
     const int n_tk = base;
     const int rows_g = p.g * n_tk;
-    uint4* qdst = reinterpret_cast<uint4*>(a.w.qel) + (size_t)u * p.rows_max * kVec;
-    for (int i = tid; i < p.h_q * n_tk * kVec; i += kEliteThreads) {
-      const int r = i / kVec, v = i % kVec;
-      const int kvh = r / rows_g, rr = r % rows_g, hh = rr / n_tk, e = rr % n_tk;
-      const int pos = min(max(out[e], 0), n_t - 1);
-      const uint4* src = reinterpret_cast<const uint4*>(
-          qbase + ((R.txt0 + pos) * p.q_stride_tok + (int64_t)(kvh * p.g + hh) * p.q_stride_head) * sizeof(T));
-      qdst[(size_t)r * kVec + v] = __ldg(src + v);
+    const int q_r0 = kvb * rows_g, q_n = (kve - kvb) * rows_g * kVec;
+    uint4* qdst = reinterpret_cast<uint4*>(a.w.qel) + ((size_t)u * p.rows_max + q_r0) * kVec;
+    for (int i0 = tid; i0 < q_n; i0 += kGatherBatch * kEliteThreads) {
+      uint4 v[kGatherBatch];
+#pragma unroll
+      for (int q = 0; q < kGatherBatch; ++q) {
+        const int i = i0 + q * kEliteThreads;
+        if (i < q_n) {
+          const int r = q_r0 + i / kVec, c = i % kVec;
+          const int kvh = r / rows_g, rr = r % rows_g, hh = rr / n_tk, e = rr % n_tk;
+          const int pos = min(max(pos_s[e], 0), n_t - 1);
+          v[q] = __ldg(reinterpret_cast<const uint4*>(
+                           qbase + ((R.txt0 + pos) * p.q_stride_tok + (int64_t)(kvh * p.g + hh) * p.q_stride_head) *
+                                       sizeof(T)) +
+                       c);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kGatherBatch; ++q) {
+        const int i = i0 + q * kEliteThreads;
+        if (i < q_n) qdst[i] = v[q];
+      }
     }
-    uint4* kdst = reinterpret_cast<uint4*>(a.w.kel) + (size_t)u * p.h_kv * p.max_elite * kVec;
-    for (int i = tid; i < p.h_kv * n_tk * kVec; i += kEliteThreads) {
-      const int r = i / kVec, v = i % kVec;
-      const int kvh = r / n_tk, e = r % n_tk;
-      const int pos = min(max(out[e], 0), n_t - 1);
-      const uint4* src = reinterpret_cast<const uint4*>(
-          kbase + ((R.seq0 + R.n_v + pos) * p.kv_stride_tok + (int64_t)kvh * p.kv_stride_head) * sizeof(T));
-      kdst[((size_t)kvh * p.max_elite + e) * kVec + v] = __ldg(src + v);
+    const int k_n = (kve - kvb) * n_tk * kVec;
+    for (int i0 = tid; i0 < k_n; i0 += kGatherBatch * kEliteThreads) {
+      uint4 v[kGatherBatch];
+#pragma unroll
+      for (int q = 0; q < kGatherBatch; ++q) {
+        const int i = i0 + q * kEliteThreads;
+        if (i < k_n) {
+          const int r = i / kVec, c = i % kVec;
+          const int kvh = kvb + r / n_tk, e = r % n_tk;
+          const int pos = min(max(pos_s[e], 0), n_t - 1);
+          v[q] = __ldg(reinterpret_cast<const uint4*>(
+                           kbase + ((R.seq0 + R.n_v + pos) * p.kv_stride_tok + (int64_t)kvh * p.kv_stride_head) *
+                                       sizeof(T)) +
+                       c);
+        }
+      }
+      uint4* kdst = reinterpret_cast<uint4*>(a.w.kel) + (size_t)u * p.h_kv * p.max_elite * kVec;
+#pragma unroll
+      for (int q = 0; q < kGatherBatch; ++q) {
+        const int i = i0 + q * kEliteThreads;
+        if (i < k_n) {
+          const int r = i / kVec, c = i % kVec;
+          const int kvh = kvb + r / n_tk, e = r % n_tk;
+          kdst[((size_t)kvh * p.max_elite + e) * kVec + c] = v[q];
+        }
+      }
     }
   }
-  if (tid == 0) {
+  if (rank == 0 && tid == 0) {
     a.w.n_tk[u] = base;
     // the unit's layout, so that the scoring kernel resolves a work item with one load
     a.w.uinfo[2 * u] = make_int4((int)R.seq0, (int)R.vis0, (int)R.txt0, R.n_v);
@@ -243,6 +300,25 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
   }
 }
 
+template <typename T, int D, int NS>
+cudaError_t launch_ns(const EliteArgs& a, int C, size_t smem, cudaStream_t s) {
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(elite_kernel<T, D, NS>), (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, a.p.B, a.p.L);
+  cfg.blockDim = dim3(kEliteThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, elite_kernel<T, D, NS>, a);
+}
+
 template <typename T, int D>
 cudaError_t launch_t(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_t s) {
   using G = TileGeom<T, D>;
@@ -250,28 +326,22 @@ cudaError_t launch_t(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_
   a.p = p;
   a.lp = lp;
   a.w = w;
-  // logits of kv_chunk KV heads + P + per-head stats next to NS stages
+  // KV heads split over a cluster of at most kMaxCluster CTAs
+  a.kv_per_cta = (p.h_kv + kMaxCluster - 1) / kMaxCluster;
+  const int C = (p.h_kv + a.kv_per_cta - 1) / a.kv_per_cta;
+  // NS stages, logits of kv_chunk KV heads, two P rows, per-head stats, elite positions
   auto bytes = [&](int ns, int kvc) {
     const size_t hc = (size_t)kvc * p.g;
-    return (size_t)ns * G::kStageBytes + sizeof(float) * (hc * p.max_text + p.max_text + 2 * hc);
+    return (size_t)ns * G::kStageBytes + sizeof(float) * (hc * p.max_text + 2 * (size_t)p.max_text + 2 * hc) +
+           sizeof(int32_t) * (size_t)p.max_elite;
   };
   int ns = 4;
-  if (bytes(4, p.h_kv) > (size_t)kSmemBudget) ns = 2;
-  int kvc = p.h_kv;
+  if (bytes(4, a.kv_per_cta) > (size_t)kSmemBudget) ns = 2;
+  int kvc = a.kv_per_cta;
   while (kvc > 1 && bytes(ns, kvc) > (size_t)kSmemBudget) --kvc;
   a.kv_chunk = kvc;
   const size_t smem = bytes(ns, kvc);
-  dim3 grid(p.B, p.L);
-  if (ns == 4) {
-    cudaError_t e = allow_smem(reinterpret_cast<const void*>(elite_kernel<T, D, 4>), (int)smem);
-    if (e != cudaSuccess) return e;
-    elite_kernel<T, D, 4><<<grid, kEliteThreads, smem, s>>>(a);
-  } else {
-    cudaError_t e = allow_smem(reinterpret_cast<const void*>(elite_kernel<T, D, 2>), (int)smem);
-    if (e != cudaSuccess) return e;
-    elite_kernel<T, D, 2><<<grid, kEliteThreads, smem, s>>>(a);
-  }
-  return cudaGetLastError();
+  return ns == 4 ? launch_ns<T, D, 4>(a, C, smem, s) : launch_ns<T, D, 2>(a, C, smem, s);
 }
 
 }  // namespace

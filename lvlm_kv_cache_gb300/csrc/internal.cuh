@@ -26,6 +26,7 @@ struct Dev {
   double alpha, r;
   float scale_log2;      // log2(e) / sqrt(D): logits are kept in base 2
   int stream_ok;         // 1: every unit takes the streaming scoring path (stream.cu)
+  int mom_slots;         // ceil(max_visual / 128): moment records per unit
   int chn;               // streaming pass-1 chunks per (unit, KV head): visual chunks + 1 text chunk
 };
 
@@ -62,6 +63,7 @@ struct Ws {
   int4* stream_info;     // [L*B][2] the layout record of stream_list[i] (as uinfo, with .w of the second = u)
   int32_t* wide_list;    // [L*B] units on the wide path (list_n[1] of them, any order)
   float* lg;             // [L][h_kv][32][lg stride] streaming path: logits of row r of KV head h
+  float4* mom;           // [L*B][mom_slots][3] streaming path: moments of each key block / tile of I_v
   float2* part_s;        // [L*B][h_kv][rc_max*32][chn] streaming pass 1: (max, sum of exp2) per (row, chunk)
   int4* uinfo;           // [L*B][2] {seq0, vis0, txt0, N_v}, {N_t, N_tk, 1, 0} per (layer, request)
   void* qel;             // [L*B][rows_max][D] elite query rows, row kvh*g*N_tk + hh*N_tk + e
@@ -125,8 +127,10 @@ cudaError_t launch_score(const Dev& p, const LayerPtrs& lp, const Ws& w, const S
                          cudaStream_t s);
 // Stats and keep counts from I_v, one CTA per (layer, request); with
 // `offsets` also the compacted-cache row offsets (checked against out_capacity).
+// With `parts` (streaming path), the statistics come from the per-block moment
+// records that passes 2 and 2k wrote instead of a pass over I_v.
 cudaError_t launch_stats_budget(const Dev& p, const Ws& w, double* stats_out,
-                                int64_t out_capacity, bool offsets, cudaStream_t s);
+                                int64_t out_capacity, bool offsets, cudaStream_t s, bool parts = false);
 cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s);
 // Streaming scoring path (stream.cu).  stream_eligible: the problem's dtype,
 // sizes and key layout allow it (bf16, per-layer key pointers evenly strided);

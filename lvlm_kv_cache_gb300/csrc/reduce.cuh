@@ -61,6 +61,69 @@ __device__ __forceinline__ ff ff_shfl_xor(ff a, int o) {
   return {__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
 }
 
+__device__ __forceinline__ ff ff_neg(ff a) { return {-a.hi, -a.lo}; }
+
+// a / b for a float b: the rounded quotient of the leading part plus one
+// correction from the exact remainder.
+__device__ __forceinline__ ff ff_div_f(ff a, float b) {
+  const float q1 = __fdiv_rn(a.hi, b);
+  const ff r = ff_add(a, ff_neg(ff_mul(ff{q1, 0.f}, ff{b, 0.f})));
+  return ff_fast_two_sum(q1, __fdiv_rn(r.hi, b));
+}
+
+// a / b: the quotient of the leading parts, then one correction from the
+// remainder a - q b (formed exactly) — about 44 significant bits.
+__device__ __forceinline__ ff ff_div(ff a, ff b) {
+  const float q1 = __fdividef(a.hi, b.hi);
+  const ff r = ff_add(a, ff_neg(ff_mul(b, ff{q1, 0.f})));
+  return ff_two_sum(q1, __fdividef(r.hi, b.hi));
+}
+
+// sqrt(a) for a >= 0: the float root s, then one Newton step s + (a - s^2) / 2s
+// with the residual formed exactly.
+__device__ __forceinline__ ff ff_sqrt(ff a) {
+  if (!(a.hi > 0.f)) return {0.f, 0.f};
+  const float s = sqrtf(a.hi);
+  const ff r = ff_add(a, ff_neg(ff_mul(ff{s, 0.f}, ff{s, 0.f})));
+  return ff_fast_two_sum(s, __fdividef(r.hi, 2.f * s));
+}
+
+// a < b for normalised values (|lo| at most half an ulp of hi).
+__device__ __forceinline__ bool ff_lt(ff a, ff b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+
+// floor(a) as a float (exact for |a| < 2^24): the floor of hi, one less when hi
+// is an integer and lo is negative.
+__device__ __forceinline__ float ff_floor(ff a) {
+  const float f = floorf(a.hi);
+  return (f == a.hi && a.lo < 0.f) ? f - 1.f : f;
+}
+
+// Sum over the 32 lanes of a warp (butterfly: every lane gets the same value,
+// since ff_add is symmetric in its operands).
+__device__ __forceinline__ ff warp_sum_ff(ff v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff_shfl_xor(v, o));
+  return v;
+}
+
+// The moments of a block of values, as one record: count n, the float-float
+// sum and mean, the sums of squared and cubed deviations from the block mean
+// (float-float), and the smallest and largest value (so that an all-equal set
+// is recognised exactly).
+struct Mom {
+  float n;
+  ff s, mean, m2, m3;
+  float mn, mx;
+};
+
+// A record in global memory: three 16-byte words.
+__device__ __forceinline__ void mom_store(float4* dst, const Mom& m) {
+  dst[0] = make_float4(m.n, m.s.hi, m.s.lo, m.mn);
+  dst[1] = make_float4(m.m2.hi, m.m2.lo, m.m3.hi, m.m3.lo);
+  dst[2] = make_float4(m.mx, m.mean.hi, m.mean.lo, 0.f);
+}
+constexpr int kMomWords = 3;  // float4 words per record
+
 // Sum over NT threads (all of them call it, tix = index within the group);
 // every thread gets the result.  Each warp reduces with shuffles, then warp 0
 // reduces the warp totals the same way: a fixed order, so the result is the
@@ -179,77 +242,185 @@ __device__ __forceinline__ double2 unit_moments(const float* x, int n, int tix, 
   return make_double2(s_t, s_k);
 }
 
-// Keep counts of request b from the (s_t, s_k) of its L layers (stats[2u],
-// stats[2u+1], u = l*B + b):  s'_t = s_t/mean s_t (1 if the mean is 0),
-// s'_k = (s_k - min s_k + 1e-6)/mean(.), r_l = 1/2 (s'_t + s'_k) r,
-// keep = clamp(floor(r_l N_v + 1/2), 1, N_v).  NT threads; thread tix owns
-// layers tix, tix+NT, ...  The two sums over layers run as fixed-order
-// float-float reductions (about 48 significant bits: a different summation
-// order than a sequential fp64 loop changes r_l N_v by ~1e-13 at most, which
-// matters only within that distance of a half-integer); the per-layer steps
-// run in fp64, one layer per thread.  `sh` is shared scratch of
-// 2 * NT/32 + 4 doubles.
-template <int NT>
-__device__ __forceinline__ void request_budget(const Dev& p, int b, int n_v, const double* stats,
-                                               int32_t* keep, double* sh, int tix, int bar_id) {
+// Moments of the values held by NT threads (each thread up to V values, valid
+// where ok[i]; n = the number of valid values, n >= 1), two-pass within the
+// group: the mean from a float-float block sum, then the centred sums.  The
+// result is valid in thread tix == 0.  `red` is shared scratch of
+// 2 * NT/32 + 1 ff, `redf` of 2 * NT/32 floats.
+template <int NT, int V>
+__device__ __forceinline__ Mom block_moments(const float (&x)[V], const bool (&ok)[V], float n, ff* red,
+                                             float* redf, int tix, int bar_id) {
   constexpr int NW = NT / 32;
-  constexpr int kMaxOwn = (AIRCACHE_MAX_LAYERS + NT - 1) / NT;
-  static_assert(sizeof(ff) <= sizeof(double), "ff scratch overlays the double scratch");
   const int lane = tix & 31, warp = tix >> 5;
-  ff* red = reinterpret_cast<ff*>(sh);
-  double st[kMaxOwn], sk[kMaxOwn];
-  ff st_sum{0.f, 0.f};
-  double sk_min = INFINITY;
+  ff s{0.f, 0.f};
+  float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < kMaxOwn; ++j) {
-    const int l = tix + j * NT;
-    st[j] = l < p.L ? __ldcg(&stats[2 * (l * p.B + b)]) : 0.0;
-    sk[j] = l < p.L ? __ldcg(&stats[2 * (l * p.B + b) + 1]) : INFINITY;
+  for (int i = 0; i < V; ++i) {
+    if (ok[i]) {
+      s = ff_add(s, ff{x[i], 0.f});
+      mn = fminf(mn, x[i]);
+      mx = fmaxf(mx, x[i]);
+    }
   }
+  s = block_sum_ff<NT>(s, red, tix, bar_id);
+  const ff mean = ff_div_f(s, n);
+  ff m2{0.f, 0.f}, m3{0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < kMaxOwn; ++j) {
-    st_sum = ff_add(st_sum, ff_from_double(st[j]));
-    sk_min = fmin(sk_min, sk[j]);
+  for (int i = 0; i < V; ++i) {
+    if (ok[i]) {
+      const ff d = ff_add(ff{x[i], 0.f}, ff_neg(mean));
+      const ff d2 = ff_mul(d, d);
+      m2 = ff_add(m2, d2);
+      m3 = ff_add(m3, ff_mul(d2, d));
+    }
   }
-  // minimum of s_k: exact (a min is order-free); shuffled as two 32-bit halves
+  block_sum_ff2<NT>(m2, m3, red, tix, bar_id);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sk_min = fmin(sk_min, __shfl_xor_sync(0xffffffffu, sk_min, o));
-  st_sum = block_sum_ff<NT>(st_sum, red, tix, bar_id);
-  named_bar_sync(bar_id, NT);  // everyone has read red[0]
-  if (lane == 0) sh[NW + warp] = sk_min;
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  if (lane == 0) {
+    redf[warp] = mn;
+    redf[NW + warp] = mx;
+  }
   named_bar_sync(bar_id, NT);
-  if (warp == 0) {
-    double m = lane < NW ? sh[NW + lane] : INFINITY;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmin(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) sh[2 * NW + 1] = m;
+  Mom r;
+  r.n = n;
+  r.s = s;
+  r.mean = mean;
+  r.m2 = m2;
+  r.m3 = m3;
+  r.mn = redf[0];
+  r.mx = redf[NW];
+  for (int i = 1; i < NW; ++i) {
+    r.mn = fminf(r.mn, redf[i]);
+    r.mx = fmaxf(r.mx, redf[NW + i]);
   }
-  named_bar_sync(bar_id, NT);
-  const double min_sk = sh[2 * NW + 1];
+  return r;
+}
+
+// Sample skewness n / ((n-1)(n-2)) M3 / sigma^3, sigma^2 = M2 / (n-1), in
+// float-float (n < 2^24, so n-1, n-2 and their product are exact); 0 for an
+// all-equal set or sigma = 0.
+__device__ __forceinline__ ff skew_ff(float n, ff m2, ff m3, bool all_equal) {
+  if (all_equal) return {0.f, 0.f};
+  const ff var = ff_div_f(m2, n - 1.f);
+  if (!(var.hi > 0.f)) return {0.f, 0.f};
+  const ff s3 = ff_mul(var, ff_sqrt(var));
+  const ff den = ff_mul(s3, ff_mul(ff{n - 1.f, 0.f}, ff{n - 2.f, 0.f}));
+  return ff_div(ff_mul(m3, ff{n, 0.f}), den);
+}
+
+// (s_t, s_k) of one (layer, request) from its block records rec[0..nslots),
+// by one warp (every lane gets the result).  The union's moments about the
+// overall mean mu: with delta_j = mean_j - mu,
+//   M2 = sum_j M2_j + n_j delta_j^2,
+//   M3 = sum_j M3_j + 3 delta_j M2_j + n_j delta_j^3
+// (the block's own deviations sum to zero).  Lane j takes records j, j+32, ...;
+// the lane totals are summed in a fixed butterfly order.
+__device__ __forceinline__ void layer_stats_warp(const float4* rec, int nslots, int lane, ff& s_t, ff& s_k) {
+  float n = 0.f, mn = INFINITY, mx = -INFINITY;
+  ff s{0.f, 0.f};
+  for (int j = lane; j < nslots; j += 32) {
+    const float4 w0 = __ldcg(rec + (size_t)j * kMomWords), w2 = __ldcg(rec + (size_t)j * kMomWords + 2);
+    n += w0.x;  // integers below 2^24: exact
+    s = ff_add(s, ff{w0.y, w0.z});
+    mn = fminf(mn, w0.w);
+    mx = fmaxf(mx, w2.x);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    n += __shfl_xor_sync(0xffffffffu, n, o);
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  s = warp_sum_ff(s);
+  const ff mu = ff_div_f(s, n);
+  ff m2{0.f, 0.f}, m3{0.f, 0.f};
+  for (int j = lane; j < nslots; j += 32) {
+    const float4 w0 = __ldcg(rec + (size_t)j * kMomWords), w1 = __ldcg(rec + (size_t)j * kMomWords + 1),
+                 w2 = __ldcg(rec + (size_t)j * kMomWords + 2);
+    const ff nj{w0.x, 0.f}, m2j{w1.x, w1.y}, m3j{w1.z, w1.w};
+    const ff d = ff_add(ff{w2.y, w2.z}, ff_neg(mu));
+    const ff nd2 = ff_mul(nj, ff_mul(d, d));
+    m2 = ff_add(m2, ff_add(m2j, nd2));
+    m3 = ff_add(m3, ff_add(m3j, ff_add(ff_mul(ff_mul(ff{3.f, 0.f}, d), m2j), ff_mul(nd2, d))));
+  }
+  m2 = warp_sum_ff(m2);
+  m3 = warp_sum_ff(m3);
+  s_t = s;
+  s_k = skew_ff(n, m2, m3, !(mx > mn));
+}
+
+// Keep counts of request b from the (s_t, s_k) of its L layers, by one warp
+// (lane j owns layers j, j+32, ...):  s'_t = s_t/mean s_t (1 if the mean is 0),
+// s'_k = (s_k - min s_k + 1e-6)/mean(.), r_l = 1/2 (s'_t + s'_k) r,
+// keep = clamp(floor(r_l N_v + 1/2), 1, N_v).  `get(l, st, sk)` yields layer
+// l's pair.  Float-float throughout (about 44 significant bits per division:
+// against an fp64 evaluation r_l N_v moves by ~1e-10 at most, which matters only
+// within that distance of a half-integer); the layer sums are fixed-order
+// butterflies, so the result is the same run to run.
+template <typename Get>
+__device__ __forceinline__ void request_budget_warp(const Dev& p, int b, int n_v, Get get, int32_t* keep,
+                                                    int lane) {
+  constexpr int kOwn = (AIRCACHE_MAX_LAYERS + 31) / 32;
+  ff st[kOwn], sk[kOwn];
+  ff st_sum{0.f, 0.f}, sk_min{INFINITY, 0.f};
+#pragma unroll
+  for (int j = 0; j < kOwn; ++j) {
+    const int l = lane + 32 * j;
+    if (l < p.L) {
+      get(l, st[j], sk[j]);
+      st_sum = ff_add(st_sum, st[j]);
+      if (ff_lt(sk[j], sk_min)) sk_min = sk[j];
+    }
+  }
+  st_sum = warp_sum_ff(st_sum);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const ff t{__shfl_xor_sync(0xffffffffu, sk_min.hi, o), __shfl_xor_sync(0xffffffffu, sk_min.lo, o)};
+    if (ff_lt(t, sk_min)) sk_min = t;
+  }
+  constexpr float kEpsHi = (float)1e-6;
+  constexpr float kEpsLo = (float)(1e-6 - (double)kEpsHi);
   ff u_sum{0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < kMaxOwn; ++j) {
-    if (tix + j * NT < p.L) u_sum = ff_add(u_sum, ff_from_double(__dadd_rn(__dsub_rn(sk[j], min_sk), 1e-6)));
+  for (int j = 0; j < kOwn; ++j) {
+    if (lane + 32 * j < p.L) {
+      sk[j] = ff_add(ff_add(sk[j], ff_neg(sk_min)), ff{kEpsHi, kEpsLo});  // now u_l
+      u_sum = ff_add(u_sum, sk[j]);
+    }
   }
-  u_sum = block_sum_ff<NT>(u_sum, red, tix, bar_id);
-  if (tix == 0) {
-    sh[2 * NW + 2] = __ddiv_rn(ff_to_double(st_sum), (double)p.L);
-    sh[2 * NW + 3] = __ddiv_rn(ff_to_double(u_sum), (double)p.L);
-  }
-  named_bar_sync(bar_id, NT);
-  const double mean_st = sh[2 * NW + 2], mean_u = sh[2 * NW + 3];
+  u_sum = warp_sum_ff(u_sum);
+  const ff mean_st = ff_div_f(st_sum, (float)p.L), mean_u = ff_div_f(u_sum, (float)p.L);
+  const float r_hi = (float)p.r;
+  const ff r{r_hi, (float)(p.r - (double)r_hi)};
 #pragma unroll
-  for (int j = 0; j < kMaxOwn; ++j) {
-    const int l = tix + j * NT;
+  for (int j = 0; j < kOwn; ++j) {
+    const int l = lane + 32 * j;
     if (l < p.L) {
-      const double st_n = (mean_st != 0.0) ? __ddiv_rn(st[j], mean_st) : 1.0;
-      const double sk_n = __ddiv_rn(__dadd_rn(__dsub_rn(sk[j], min_sk), 1e-6), mean_u);
-      const double rl = __dmul_rn(__dmul_rn(0.5, __dadd_rn(st_n, sk_n)), p.r);
-      double kf = floor(__dadd_rn(__dmul_rn(rl, (double)n_v), 0.5));
-      kf = fmin(fmax(kf, 1.0), (double)n_v);
+      const ff st_n = (mean_st.hi != 0.f) ? ff_div(st[j], mean_st) : ff{1.f, 0.f};
+      const ff sk_n = ff_div(sk[j], mean_u);
+      const ff rl = ff_mul(ff_mul(ff{0.5f, 0.f}, ff_add(st_n, sk_n)), r);
+      float kf = ff_floor(ff_add(ff_mul(rl, ff{(float)n_v, 0.f}), ff{0.5f, 0.f}));
+      kf = fminf(fmaxf(kf, 1.f), (float)n_v);
       keep[l * p.B + b] = (int32_t)kf;
     }
   }
+}
+
+// request_budget_warp over (s_t, s_k) pairs stored as doubles (stats[2u],
+// stats[2u+1], u = l*B + b).
+__device__ __forceinline__ void request_budget(const Dev& p, int b, int n_v, const double* stats,
+                                               int32_t* keep, int lane) {
+  request_budget_warp(
+      p, b, n_v,
+      [&](int l, ff& st, ff& sk) {
+        st = ff_from_double(__ldcg(&stats[2 * (l * p.B + b)]));
+        sk = ff_from_double(__ldcg(&stats[2 * (l * p.B + b) + 1]));
+      },
+      keep, lane);
 }
 
 // out_offsets[u] (u = l*B + b): exclusive prefix over u of keep[u] + N_t[b];

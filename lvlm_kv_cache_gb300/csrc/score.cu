@@ -125,7 +125,6 @@ struct Ctl {
   SvcJob svc_job;
   float2 red[2 * kCW * kRC];
   ff svc_red[2 * (kSvcT / 32) + 1];
-  double svc_sh[2 * (kSvcT / 32) + 4];
   long long svc_seg[kSvcT];
 };
 
@@ -659,7 +658,7 @@ __device__ void service(const PArgs& a, Ctl* c) {
     named_bar_sync(kBarSvc, kSvcT);
     if (!c->svc_flag[0]) continue;
     __threadfence();
-    request_budget<kSvcT>(p, job.b, job.n_v, w.stats, w.keep, c->svc_sh, tix, kBarSvc);
+    if (tix < 32) request_budget(p, job.b, job.n_v, w.stats, w.keep, tix);
     __threadfence();
     named_bar_sync(kBarSvc, kSvcT);
     if (tix == 0) c->svc_flag[1] = (atomicAdd(w.cnt_all, 1u) == (unsigned)(p.B - 1)) ? 1 : 0;

@@ -57,6 +57,7 @@ constexpr int kCT = kCW * 32;             // consumer threads
 constexpr int kThreads1 = kCT + 32;       // + the producer warp
 constexpr int kBarC = 1;                  // named barrier of the consumer threads
 constexpr int kT2 = 256;                  // pass-2 / pass-2k threads
+constexpr int kBarT2 = 1;                 // named barrier over all kT2 threads
 constexpr int kMaxStages = 12;
 constexpr int kNQ = 4;                    // pass-2k query-chunk ring
 
@@ -561,6 +562,8 @@ __global__ void __launch_bounds__(kT2) stream_p2_kernel(const __grid_constant__ 
   const long long LS = lg_stride(p);
   const float scale = p.scale_log2;  // stored logits are raw q.k
   const int key = k0 + tid;
+  float xv[1] = {0.f};
+  bool okv[1] = {key < n_v};
   if (key < n_v) {
     const float* col = w.lg + (size_t)l * p.h_kv * kRC * LS + lg_col0(i0.y, b) + key;
     float acc = 0.f;
@@ -577,8 +580,14 @@ __global__ void __launch_bounds__(kT2) stream_p2_kernel(const __grid_constant__ 
       }
       for (; r < rows; ++r) acc += fast_exp2(fmaf(__ldcg(ch + (size_t)r * LS), scale, -ls[r]));
     }
-    w.iv[(size_t)l * p.total_visual + i0.y + key] = acc / (float)(p.h_q * n_tk);
+    xv[0] = acc / (float)(p.h_q * n_tk);
+    w.iv[(size_t)l * p.total_visual + i0.y + key] = xv[0];
   }
+  // this block's moments, for the statistics kernel
+  __shared__ ff red[2 * (kT2 / 32) + 1];
+  __shared__ float redf[2 * (kT2 / 32)];
+  const Mom mb = block_moments<kT2, 1>(xv, okv, (float)min(kKeysP2, n_v - k0), red, redf, tid, kBarT2);
+  if (tid == 0) mom_store(w.mom + ((size_t)u * p.mom_slots + blockIdx.y) * kMomWords, mb);
 }
 
 // ------------------------------------------------------------------ pass 2k
@@ -602,6 +611,8 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   Ctl2* c = reinterpret_cast<Ctl2*>(sm + Gm::kCtl2Off);
+  __shared__ ff red[2 * (kT2 / 32) + 1];
+  __shared__ float redf[2 * (kT2 / 32)];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g4 = lane >> 2, c4 = lane & 3;
   const uint32_t sbase = smem_u32(sm);
@@ -730,6 +741,8 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
     // per key: the sum over every row (lanes with the same c4 hold the same keys)
     float* iv = w.iv + (size_t)l * TV + i0.y;
     const float denom = (float)(p.h_q * n_tk);
+    float xv[4];
+    bool okv[4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -739,8 +752,13 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
         v += __shfl_xor_sync(0xffffffffu, v, 8);
         v += __shfl_xor_sync(0xffffffffu, v, 16);
         const int key = 16 * warp + 8 * nt + 2 * c4 + e;
-        if (g4 == 0 && key < klim) iv[(long long)tile * kTK + key] = v / denom;
+        xv[2 * nt + e] = v / denom;
+        okv[2 * nt + e] = g4 == 0 && key < klim;
+        if (okv[2 * nt + e]) iv[(long long)tile * kTK + key] = xv[2 * nt + e];
       }
+    // this tile's moments, for the statistics kernel
+    const Mom mb = block_moments<kT2, 4>(xv, okv, (float)klim, red, redf, tid, kBarT2);
+    if (tid == 0) mom_store(w.mom + ((size_t)u * p.mom_slots + tile) * kMomWords, mb);
   }
 }
 
