@@ -263,7 +263,7 @@ int aircache_score(const aircache_problem* p, void* ws, size_t ws_bytes, float* 
   AC_TRY(launch_elite(dn, lp, w, s));
   if (dn.stream_ok) {
     AC_TRY(launch_stream_p1(dn, maps, w, sms, s));
-    AC_TRY(launch_stream_p2(dn, w, s));
+    AC_TRY(launch_stream_p2(dn, maps, w, sms, s));
     AC_TRY(launch_stream_p2k(dn, maps, w, sms, s));
   } else {
     AC_TRY(launch_score(dn, lp, w, plan_score(dn, sms, false, 0), s));
@@ -371,7 +371,7 @@ static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, v
   if (dn.stream_ok) {
     AC_TRY(launch_stream_p1(dn, maps, w, sms, s));
     AC_TRY(mark(k++));
-    AC_TRY(launch_stream_p2(dn, w, s));
+    AC_TRY(launch_stream_p2(dn, maps, w, sms, s));
     AC_TRY(mark(k++));
     AC_TRY(launch_stream_p2k(dn, maps, w, sms, s));
     AC_TRY(mark(k++));

@@ -141,11 +141,12 @@ cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s);
 // units' logits from the keys.
 struct StreamMaps {
   CUtensorMap kmap, kmap2, qmap, kelmap;  // keys (boxes of 128 / 256 rows), elite queries, elite keys
+  CUtensorMap lgmap;                      // stored logits of the streaming path
 };
 bool stream_eligible(const Dev& p, const LayerPtrs& lp);
 bool encode_stream_maps(const Dev& p, const LayerPtrs& lp, const Ws& w, StreamMaps* m);
 cudaError_t launch_stream_p1(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s);
-cudaError_t launch_stream_p2(const Dev& p, const Ws& w, cudaStream_t s);
+cudaError_t launch_stream_p2(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s);
 cudaError_t launch_stream_p2k(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s);
 
 // Launch `kernel` on `s` with programmatic stream serialization, so that its

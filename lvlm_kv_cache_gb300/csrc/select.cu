@@ -4,14 +4,16 @@
 //
 // One CTA of 1024 threads per (request, layer).  I_v is mapped to
 // order-preserving 32-bit keys, held in shared memory when the unit fits
-// (otherwise re-read from global memory each pass).  A 4-digit (8-bit)
-// MSB-first radix select finds the exact keep-th largest key T and how many
-// keys equal to T are still wanted; histogram increments are aggregated over
-// the lanes of a warp that share a digit, and after the first digit the keys
-// that can still be T are compacted so the later passes touch only them.  A
-// final sweep in which each thread owns a contiguous run of positions emits
-// every key > T plus the lowest-position keys == T, in ascending position,
-// with block-wide exclusive scans (one when every key == T is taken).
+// (otherwise re-read from global memory each pass).  An MSB-first radix select
+// with digits of 11, 11 and 10 bits finds the exact keep-th largest key T and
+// how many keys equal to T are still wanted (it stops early once every key of
+// the selected bucket is taken).  Wide digits matter here: the I_v of a layer
+// spans a few octaves, so an 8-bit top digit would put nearly every key in one
+// bucket.  After the first digit the keys that can still be T are compacted, so
+// the later passes touch only them.  The emission splits the positions into 32
+// contiguous segments, one per warp, and takes every key > T plus the
+// lowest-position keys == T with ballots and one scan of the warp totals, so
+// the output is in ascending position order.
 // Integer work only: the result is exact and deterministic.
 #include "internal.cuh"
 #include "ptx.cuh"
@@ -22,6 +24,7 @@ namespace {
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSmemKeys = 24 * 1024;  // units up to this many keys are staged in shared memory
+constexpr int kMaxBins = 2048;        // widest digit: 11 bits
 
 struct SelectArgs {
   Dev p;
@@ -65,15 +68,16 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
 }
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_constant__ SelectArgs a) {
-  static_assert(kSelWarps == 32, "the warp-total scan assumes 32 warps");
+  static_assert(kSelWarps == 32, "the warp-total scans assume 32 warps");
   const Dev& p = a.p;
   const Ws& w = a.w;
   const int b = blockIdx.x, l = blockIdx.y, u = l * p.B + b;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   extern __shared__ uint32_t keys_s[];  // [smem_keys] keys, then [smem_keys] candidates
-  __shared__ unsigned hist[256];
+  __shared__ unsigned hist[kMaxBins];
   __shared__ int wsum[kSelWarps + 1];
-  __shared__ unsigned sel_digit, sel_above, sel_count;
+  __shared__ int wgt[kSelWarps + 1], weq[kSelWarps + 1];
+  __shared__ unsigned sel_digit, sel_above, sel_count, n_cand_s;
   pdl_trigger();
   pdl_wait();  // I_v and the keep counts
   if (*(volatile int32_t*)w.error != 0) return;
@@ -109,123 +113,117 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   }
   auto key_at = [&](int i) -> uint32_t { return staged ? keys_s[i] : order_key(__ldcg(x + i)); };
 
-  uint32_t* cand = keys_s + a.smem_keys;  // keys still able to be the answer (staged units)
-  int n_cand = n;                         // after the first digit: their number
+  uint32_t* cand = keys_s + a.smem_keys;  // keys still able to be T (staged units, after the first digit)
+  int n_cand = n;
   uint32_t prefix = 0, mask = 0;
-  unsigned want = (unsigned)k;  // keys >= the answer still to account for
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
-    __syncthreads();
-    const bool from_cand = staged && shift < 24;
+  unsigned want = (unsigned)k;  // keys >= T still to account for
+  bool all_taken = false;       // every key of the selected bucket is taken: T = prefix, no ties to break
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int bits = pass == 2 ? 10 : 11;
+    const int nb = 1 << bits;
+    const uint32_t dmask = (uint32_t)nb - 1u;
+    for (int i = tid; i < nb; i += kSelThreads) hist[i] = 0;
+    __syncthreads();  // also: the staged keys are in shared memory
+    const bool from_cand = staged && pass > 0;
     const int m = from_cand ? n_cand : n;
-    for (int i0 = 0; i0 < m; i0 += kSelThreads) {
-      const int i = i0 + tid;
-      const uint32_t key = i < m ? (from_cand ? cand[i] : key_at(i)) : 0u;
-      const bool in = i < m && (key & mask) == prefix;
-      const unsigned digit = in ? ((key >> shift) & 255u) : 256u;
-      // one increment per distinct digit of the warp
-      const unsigned peers = __match_any_sync(0xffffffffu, digit);
-      if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (unsigned)__popc(peers));
+    for (int i = tid; i < m; i += kSelThreads) {
+      const uint32_t key = from_cand ? cand[i] : key_at(i);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
     }
     __syncthreads();
-    if (warp == 0) {
-      // lane owns digits [8*(31-lane), 8*(31-lane)+8): lane 0 the highest
-      unsigned cnt[8];
-      unsigned lsum = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        cnt[i] = hist[8 * (31 - lane) + (7 - i)];  // descending digits
-        lsum += cnt[i];
-      }
-      unsigned incl = lsum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const unsigned excl = incl - lsum;  // count of digits above this lane's range
-      if (excl < want && want <= incl) {
-        unsigned run = excl;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (run < want && want <= run + cnt[i]) {
-            sel_digit = 8 * (31 - lane) + (7 - i);
-            sel_above = run;
-            sel_count = cnt[i];
-          }
-          run += cnt[i];
-        }
-      }
+    // bins in descending digit order: thread t owns positions t*bpt .. t*bpt+bpt-1
+    const int bpt = nb / kSelThreads;  // 2 or 1
+    unsigned c0 = hist[nb - 1 - tid * bpt], c1 = bpt > 1 ? hist[nb - 2 - tid * bpt] : 0u;
+    int total;
+    const unsigned excl = (unsigned)block_excl_scan((int)(c0 + c1), wsum, &total);
+    if (excl < want && want <= excl + c0) {
+      sel_digit = (unsigned)(nb - 1 - tid * bpt);
+      sel_above = excl;
+      sel_count = c0;
+    } else if (bpt > 1 && excl + c0 < want && want <= excl + c0 + c1) {
+      sel_digit = (unsigned)(nb - 2 - tid * bpt);
+      sel_above = excl + c0;
+      sel_count = c1;
     }
     __syncthreads();
     want -= sel_above;
     prefix |= sel_digit << shift;
-    mask |= 255u << shift;
-    if (staged && shift == 24) {
-      // compact the keys whose top digit is the selected one (order is irrelevant
-      // here: one shared counter, one atomic per warp and pass over the keys)
-      if (tid == 0) sel_above = 0;
+    mask |= dmask << shift;
+    if (want == sel_count) {
+      all_taken = true;  // keys >= prefix are exactly the keep largest
+      break;
+    }
+    if (staged && pass == 0) {
+      // compact the keys of the selected bucket (order is irrelevant here: one
+      // shared counter, one atomic per warp and pass over the keys)
+      if (tid == 0) n_cand_s = 0;
       __syncthreads();
       for (int i0 = 0; i0 < n; i0 += kSelThreads) {
         const int i = i0 + tid;
         const bool c = i < n && (keys_s[i] & mask) == prefix;
         const unsigned bal = __ballot_sync(0xffffffffu, c);
         int base = 0;
-        if (lane == 0 && bal) base = (int)atomicAdd(&sel_above, (unsigned)__popc(bal));
+        if (lane == 0 && bal) base = (int)atomicAdd(&n_cand_s, (unsigned)__popc(bal));
         base = __shfl_sync(0xffffffffu, base, 0);
         if (c) cand[base + __popc(bal & ((1u << lane) - 1u))] = keys_s[i];
       }
       __syncthreads();
-      n_cand = (int)sel_above;
-      __syncthreads();
+      n_cand = (int)n_cand_s;
     }
   }
-  const unsigned eq_all = sel_count;  // keys equal to the answer
-  // prefix = exact key of the keep-th largest: take every key > prefix and the
-  // first `want` keys == prefix in position order.  Thread tid owns positions
-  // [tid * per, tid * per + per).
-  const int per = (n + kSelThreads - 1) / kSelThreads;
-  const int i0 = min(n, tid * per), i1 = min(n, i0 + per);
-  if (want == eq_all) {
-    // every key equal to the answer is taken: keys >= prefix, one scan
-    int n_take = 0;
-    for (int i = i0; i < i1; ++i) n_take += key_at(i) >= prefix ? 1 : 0;
-    int take_total;
-    int pos = block_excl_scan(n_take, wsum, &take_total);
-    for (int i = i0; i < i1; ++i) {
-      if (key_at(i) >= prefix) out[pos++] = i;
-    }
-    return;
+  // prefix = T (exact unless all_taken, when every key >= prefix is taken).
+  // Take every key > T and the first `want` keys == T in position order.
+  // Warp w scans the positions [w*seg, (w+1)*seg) in steps of 32.
+  const unsigned keep_eq = all_taken ? 0u : want;
+  const uint32_t thr = prefix;
+  const int seg = ((n + kSelWarps - 1) / kSelWarps + 31) / 32 * 32;
+  const int s0 = warp * seg, s1 = min(n, s0 + seg);
+  const unsigned lt = (1u << lane) - 1u;
+  int gt = 0, eq = 0;
+  for (int i0 = s0; i0 < s1; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t key = i < s1 ? key_at(i) : 0u;
+    const bool g = i < s1 && (all_taken ? key >= thr : key > thr);
+    const bool e = i < s1 && !all_taken && key == thr;
+    gt += __popc(__ballot_sync(0xffffffffu, g));
+    eq += __popc(__ballot_sync(0xffffffffu, e));
   }
-  int n_eq = 0;
-  for (int i = i0; i < i1; ++i) n_eq += key_at(i) == prefix ? 1 : 0;
-  int eq_total;
-  int eq_rank = block_excl_scan(n_eq, wsum, &eq_total);
-  int n_take = 0;
-  {
-    int r = eq_rank;
-    for (int i = i0; i < i1; ++i) {
-      const uint32_t key = key_at(i);
-      if (key > prefix) {
-        ++n_take;
-      } else if (key == prefix) {
-        if (r < (int)want) ++n_take;
-        ++r;
+  if (lane == 0) {
+    wgt[warp] = gt;
+    weq[warp] = eq;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive prefixes of the warp totals
+    int tg = wgt[lane], te = weq[lane];
+    int ig = tg, ie = te;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yg = __shfl_up_sync(0xffffffffu, ig, o), ye = __shfl_up_sync(0xffffffffu, ie, o);
+      if (lane >= o) {
+        ig += yg;
+        ie += ye;
       }
     }
+    wgt[lane] = ig - tg;
+    weq[lane] = ie - te;
   }
-  int take_total;
-  int pos = block_excl_scan(n_take, wsum, &take_total);
-  for (int i = i0; i < i1; ++i) {
-    const uint32_t key = key_at(i);
-    if (key > prefix) {
-      out[pos++] = i;
-    } else if (key == prefix) {
-      if (eq_rank < (int)want) out[pos++] = i;
-      ++eq_rank;
-    }
+  __syncthreads();
+  int gt_run = wgt[warp], eq_run = weq[warp];
+  for (int i0 = s0; i0 < s1; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t key = i < s1 ? key_at(i) : 0u;
+    const bool g = i < s1 && (all_taken ? key >= thr : key > thr);
+    const bool e = i < s1 && !all_taken && key == thr;
+    const unsigned bg = __ballot_sync(0xffffffffu, g), be = __ballot_sync(0xffffffffu, e);
+    const int eq_before = eq_run + __popc(be & lt);
+    // output slot = keys taken before position i = (keys > T before i) + min(keys == T before i, keep_eq)
+    const int pos = gt_run + __popc(bg & lt) + min(eq_before, (int)keep_eq);
+    if (g || (e && eq_before < (int)keep_eq)) out[pos] = i;
+    gt_run += __popc(bg);
+    eq_run += __popc(be);
   }
-  (void)lane;
 }
 
 }  // namespace

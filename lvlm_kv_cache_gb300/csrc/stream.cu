@@ -89,6 +89,7 @@ struct SArgs {
   CUtensorMap kmap2;   // the same keys, box 256 tokens (pass 1)
   CUtensorMap qmap;    // gathered elite query rows (D, rows), box 32 rows
   CUtensorMap kelmap;  // gathered elite text keys (D, rows), box 128 rows
+  CUtensorMap lgmap;   // stored logits (columns, rows), box 256 columns x 8 rows
   Dev p;
   Ws w;
 };
@@ -511,83 +512,262 @@ __global__ void __launch_bounds__(kThreads1, 1) stream_p1_kernel(const __grid_co
 
 // ------------------------------------------------------------------ pass 2
 
-constexpr int kKeysP2 = kT2;  // keys per pass-2 CTA (one per thread)
+constexpr int kKeysP2 = kT2;                  // keys per pass-2 item (one per thread)
+constexpr int kP2Box = 8;                     // logit rows per TMA box
+constexpr int kP2Slice = kRC * kKeysP2 * 4;   // one KV head's logits of an item (32 KB)
+constexpr int kP2Stages = 6;                  // slices in flight
+constexpr int kT2p = 2 * kT2;                 // pass-2 threads: streamers, then moment warps
+constexpr int kBarP2S = 1;                    // named barrier of the streamers
+constexpr int kBarP2M = 2;                    // named barrier of the moment warps
+constexpr int kP2CtlOff = kP2Stages * kP2Slice;
 
-// One CTA per (unit, 256 keys).  Single-chunk units: the quads of the CTA
-// merge the row LSEs, then each thread sums exp2(logit - lse) over the rows of
-// every KV head for its key (eight rows' loads in flight).  Multi-chunk units:
-// the first CTA of the unit writes its row LSEs for pass 2k.
-__global__ void __launch_bounds__(kT2) stream_p2_kernel(const __grid_constant__ SArgs a) {
+// What a pass-2 stage holds: the logits of KV head kvh for item (unit u, key
+// block kb), or the end of the CTA's walk (state 1), or a unit record that
+// failed validation (state 2).
+struct P2Rec {
+  int state, u, l, b, kb, n_v, n_tk, rows, kvh;
+  long long vis0;
+};
+
+// Hand-off of one item's I_v from the streaming warps to the moment warps.
+struct P2Hand {
+  int u, kb, n, end;
+};
+
+struct Ctl2p {
+  uint64_t full[kP2Stages];
+  uint64_t hfull[2], hempty[2];  // hand-off buffers: filled by the streamers, released by the moment warps
+  P2Rec rec[kP2Stages];
+  P2Hand hand[2];
+  float hx[2][kKeysP2];
+};
+
+// The unit record (seq0, vis0, txt0, n_v), (n_t, n_tk, 1, u) of single unit
+// si, loaded once per unit.
+struct P2Unit {
+  int si = -1;
+  int4 r0, r1;
+};
+
+// The first item at or after `item` (< end) whose key block lies inside its
+// unit; items run over (single unit si, key block kb), si-major, KB blocks per
+// unit.  Returns 0 past the end, 1 with the item in `r`, 2 for a unit record
+// that fails validation.
+__device__ __forceinline__ int p2_item(const Dev& p, const Ws& w, long long& item, long long end, int KB, int slot0,
+                                       P2Unit& cu, P2Rec& r) {
+  for (; item < end; ++item) {
+    const int si = (int)(item / KB), kb = (int)(item % KB);
+    if (si != cu.si) {
+      cu.si = si;
+      cu.r0 = __ldcg(&w.stream_info[2 * (slot0 + si)]);
+      cu.r1 = __ldcg(&w.stream_info[2 * (slot0 + si) + 1]);
+    }
+    const int4 r0 = cu.r0, r1 = cu.r1;
+    if (!stream_unit(p, r1.w, r0, r1) || p.g * r1.y > kRC) return 2;
+    if (kb * kKeysP2 < r0.w) {
+      r.state = 0;
+      r.u = r1.w;
+      r.l = r1.w / p.B;
+      r.b = r1.w % p.B;
+      r.kb = kb;
+      r.n_v = r0.w;
+      r.n_tk = r1.y;
+      r.rows = p.g * r1.y;
+      r.kvh = 0;
+      r.vis0 = r0.y;
+      return 1;
+    }
+  }
+  return 0;
+}
+
+// Pass 2 for one-chunk units (g * N_tk <= 32), persistent: CTA c takes a
+// contiguous range of the items.  Streaming warps: thread 0 walks the range
+// ahead of the others and loads, for each item and KV head, that head's logits
+// (rows < 32, 256 keys) by TMA into a ring of 32 KB shared-memory stages, with
+// a record of what the stage holds; streaming thread t owns key k0 + t and sums
+// exp2(logit - lse) over the rows of every KV head, writes I_v and hands the
+// item's 256 values to the moment warps (double-buffered), which reduce them to
+// the item's moment record while the streamers go on with the next item.  The
+// row LSEs of a unit are merged from pass 1's partials (quads of lanes) when the
+// walk enters the unit, while later slices are in flight.  Multi-chunk units:
+// every thread first helps publish their row LSEs for pass 2k.
+__global__ void __launch_bounds__(kT2p, 1) stream_p2_kernel(const __grid_constant__ SArgs a) {
   const Dev& p = a.p;
   const Ws& w = a.w;
-  extern __shared__ float lse_s[];  // [h_kv][32]
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
+  const float* slices = reinterpret_cast<const float*>(sm);  // [kP2Stages][32][256]
+  Ctl2p* c = reinterpret_cast<Ctl2p*>(sm + kP2CtlOff);
+  float* lse_s = reinterpret_cast<float*>(sm + kP2CtlOff + sizeof(Ctl2p));  // [h_kv][32]
+  __shared__ ff red[2 * (kT2 / 32) + 1];
+  __shared__ float redf[2 * (kT2 / 32)];
   const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int i = 0; i < kP2Stages; ++i) mbar_init(&c->full[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c->hfull[i], kT2);
+      mbar_init(&c->hempty[i], kT2);
+    }
+    fence_mbar_init();
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&a.lgmap)) : "memory");
+  }
+  __syncthreads();
   pdl_trigger();
   pdl_wait();  // pass 1's partials and logits
   if (*(volatile int32_t*)w.error != 0) return;
-  const int li = blockIdx.x;
-  const int n_total = __ldcg(&w.list_n[0]);
-  if (li >= n_total) return;
-  const int u = __ldcg(&w.stream_list[stream_slot(p, li, __ldcg(&w.list_n[2]), n_total)]);
-  const int4 i0 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u]) : make_int4(0, 0, 0, 0);
-  const int4 i1 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u + 1]) : make_int4(0, 0, 0, 0);
-  if (!stream_unit(p, u, i0, i1)) {
+  const int n_total = __ldcg(&w.list_n[0]), n_multi = __ldcg(&w.list_n[2]);
+  const int LB = p.L * p.B;
+  if (n_total < 0 || n_total > LB || n_multi < 0 || n_multi > n_total) {
     if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
     return;
   }
-  const int n_v = i0.w, n_tk = i1.y, rows = p.g * n_tk;
-  const int tv = (n_v + kTK - 1) / kTK;
-  const int chv = (tv + kCK - 1) / kCK;
-  if (rows > kRC) {
-    // several row chunks: publish the row LSEs for pass 2k (first CTA of the unit)
-    if (blockIdx.y != 0) return;
+  // multi-chunk units: row LSEs for pass 2k
+  for (int m = blockIdx.x; m < n_multi; m += gridDim.x) {
+    const int u = __ldcg(&w.stream_list[m]);
+    const int4 i0 = (u >= 0 && u < LB) ? __ldcg(&w.uinfo[2 * u]) : make_int4(0, 0, 0, 0);
+    const int4 i1 = (u >= 0 && u < LB) ? __ldcg(&w.uinfo[2 * u + 1]) : make_int4(0, 0, 0, 0);
+    if (!stream_unit(p, u, i0, i1)) {
+      if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+      return;
+    }
+    const int rows = p.g * i1.y;
+    const int chv = ((i0.w + kTK - 1) / kTK + kCK - 1) / kCK;
     float* lse_u = w.lse + (size_t)u * p.lse_stride;
-    for (int q = tid; q < p.h_kv * rows; q += kT2) {
+    for (int q = tid; q < p.h_kv * rows; q += kT2p) {
       const int kvh = q / rows, r = q % rows;
       lse_u[kvh * rows_per_kv(p) + r] = row_lse(p, w, u, kvh, r, chv);
     }
+  }
+
+  if (tid >= kT2) {
+    // moment warps: one record per handed-off item
+    const int mt = tid - kT2;
+    for (int n = 0;; ++n) {
+      const int hb = n & 1;
+      if (!mbar_wait(&c->hfull[hb], (uint32_t)((n >> 1) & 1), 4 * kWaitCycles)) {
+        if (mt == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+        return;
+      }
+      const P2Hand h = c->hand[hb];
+      float xv[1] = {c->hx[hb][mt]};
+      mbar_arrive(&c->hempty[hb]);
+      if (h.end) break;
+      bool okv[1] = {mt < h.n};
+      const Mom mb = block_moments<kT2, 1>(xv, okv, (float)h.n, red, redf, mt, kBarP2M);
+      if (mt == 0) mom_store(w.mom + ((size_t)h.u * p.mom_slots + h.kb) * kMomWords, mb);
+    }
     return;
   }
-  const int k0 = blockIdx.y * kKeysP2;
-  if (k0 >= n_v) return;
-  const int l = u / p.B, b = u % p.B;
-  // row LSEs, four lanes per row (whole quads iterate together)
-  for (int q4 = tid >> 2; q4 < (p.h_kv * rows + kT2 / 4 - 1) / (kT2 / 4) * (kT2 / 4); q4 += kT2 / 4) {
-    const int qq = min(q4, p.h_kv * rows - 1);
-    const int kvh = qq / rows, r = qq % rows;
-    const float lse = row_lse4(p, w, u, kvh, r, chv, tid & 3);
-    if (q4 < p.h_kv * rows && (tid & 3) == 0) lse_s[kvh * kRC + r] = lse;
-  }
-  __syncthreads();
-  const long long LS = lg_stride(p);
-  const float scale = p.scale_log2;  // stored logits are raw q.k
-  const int key = k0 + tid;
-  float xv[1] = {0.f};
-  bool okv[1] = {key < n_v};
-  if (key < n_v) {
-    const float* col = w.lg + (size_t)l * p.h_kv * kRC * LS + lg_col0(i0.y, b) + key;
-    float acc = 0.f;
-    for (int kvh = 0; kvh < p.h_kv; ++kvh) {
-      const float* ch = col + (size_t)kvh * kRC * LS;
-      const float* ls = lse_s + kvh * kRC;
-      int r = 0;
-      for (; r + 8 <= rows; r += 8) {
-        float x[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = __ldcg(ch + (size_t)(r + q) * LS);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc += fast_exp2(fmaf(x[q], scale, -ls[r + q]));
-      }
-      for (; r < rows; ++r) acc += fast_exp2(fmaf(__ldcg(ch + (size_t)r * LS), scale, -ls[r]));
+
+  // streaming warps
+  const int n_single = n_total - n_multi;
+  const int slot0 = LB - n_single;
+  const int KB = (p.max_visual + kKeysP2 - 1) / kKeysP2;
+  const long long n_items = (long long)n_single * KB;
+  const long long i_beg = n_items * blockIdx.x / gridDim.x, i_end = n_items * (blockIdx.x + 1) / gridDim.x;
+  // producer state (thread 0): the next stage to fill
+  long long pi = i_beg;
+  P2Rec pr = {};
+  P2Unit pu;
+  int pstate = 0;      // 1: pr holds the next slice; 0 / 2: end / bad record next
+  bool ended = false;  // the end record has been sent
+  auto issue = [&](int slot) {
+    if (ended) return;
+    if (pstate != 1) {
+      c->rec[slot].state = pstate == 0 ? 1 : 2;
+      mbar_arrive(&c->full[slot]);
+      ended = true;
+      return;
     }
-    xv[0] = acc / (float)(p.h_q * n_tk);
-    w.iv[(size_t)l * p.total_visual + i0.y + key] = xv[0];
+    c->rec[slot] = pr;
+    const int nb = (pr.rows + kP2Box - 1) / kP2Box;
+    mbar_arrive_expect_tx(&c->full[slot], (uint32_t)(nb * kP2Box * kKeysP2 * 4));
+    const int x = (int)(lg_col0(pr.vis0, pr.b) + (long long)pr.kb * kKeysP2);
+    const int y = (pr.l * p.h_kv + pr.kvh) * kRC;
+    for (int j = 0; j < nb; ++j) {
+      tma_load_2d(smem_u32(sm + slot * kP2Slice + j * kP2Box * kKeysP2 * 4), &a.lgmap, x, y + j * kP2Box,
+                  &c->full[slot]);
+    }
+    if (++pr.kvh == p.h_kv) {
+      ++pi;
+      pstate = p2_item(p, w, pi, i_end, KB, slot0, pu, pr);
+    }
+  };
+  if (tid == 0) {
+    fence_proxy_async_global();  // the logits were written by the previous kernel's generic stores
+    pstate = p2_item(p, w, pi, i_end, KB, slot0, pu, pr);
+    for (int st = 0; st < kP2Stages; ++st) issue(st);
   }
-  // this block's moments, for the statistics kernel
-  __shared__ ff red[2 * (kT2 / 32) + 1];
-  __shared__ float redf[2 * (kT2 / 32)];
-  const Mom mb = block_moments<kT2, 1>(xv, okv, (float)min(kKeysP2, n_v - k0), red, redf, tid, kBarT2);
-  if (tid == 0) mom_store(w.mom + ((size_t)u * p.mom_slots + blockIdx.y) * kMomWords, mb);
+  const float scale = p.scale_log2;  // stored logits are raw q.k
+  int cur_u = -1, n_hand = 0;
+  float acc = 0.f;
+  // hand an item (or the end) to the moment warps
+  auto hand_off = [&](const P2Hand& h, float x) -> bool {
+    const int hb = n_hand & 1;
+    if (!mbar_wait(&c->hempty[hb], (uint32_t)(((n_hand >> 1) & 1) ^ 1), 4 * kWaitCycles)) return false;
+    c->hx[hb][tid] = x;
+    if (tid == 0) c->hand[hb] = h;
+    mbar_arrive(&c->hfull[hb]);
+    ++n_hand;
+    return true;
+  };
+  for (long long stage = 0;; ++stage) {
+    const int slot = (int)(stage % kP2Stages);
+    if (!mbar_wait(&c->full[slot], (uint32_t)((stage / kP2Stages) & 1), 4 * kWaitCycles)) {
+      if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+      break;
+    }
+    const P2Rec it = c->rec[slot];
+    if (it.state != 0) {
+      if (it.state == 2 && tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+      break;
+    }
+    if (it.kvh == 0) {
+      if (it.u != cur_u) {
+        // the unit's row LSEs, four lanes per row (whole quads iterate together)
+        const int chv = ((it.n_v + kTK - 1) / kTK + kCK - 1) / kCK;
+        const int nr = p.h_kv * it.rows;
+        for (int q4 = tid >> 2; q4 < (nr + kT2 / 4 - 1) / (kT2 / 4) * (kT2 / 4); q4 += kT2 / 4) {
+          const int qq = min(q4, nr - 1);
+          const int kvh = qq / it.rows, r = qq % it.rows;
+          const float lse = row_lse4(p, w, it.u, kvh, r, chv, tid & 3);
+          if (q4 < nr && (tid & 3) == 0) lse_s[kvh * kRC + r] = lse;
+        }
+        named_bar_sync(kBarP2S, kT2);
+        cur_u = it.u;
+      }
+      acc = 0.f;
+    }
+    const float* x = slices + (size_t)slot * (kRC * kKeysP2) + tid;
+    const float* ls = lse_s + it.kvh * kRC;
+    int r = 0;
+    for (; r + 8 <= it.rows; r += 8) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc += fast_exp2(fmaf(x[(r + q) * kKeysP2], scale, -ls[r + q]));
+    }
+    for (; r < it.rows; ++r) acc += fast_exp2(fmaf(x[r * kKeysP2], scale, -ls[r]));
+    named_bar_sync(kBarP2S, kT2);  // every streamer is done with the slot and its record
+    if (tid == 0) issue(slot);
+    if (it.kvh == p.h_kv - 1) {
+      const int key = it.kb * kKeysP2 + tid;
+      const float v = acc / (float)(p.h_q * it.n_tk);
+      if (key < it.n_v) w.iv[(size_t)it.l * p.total_visual + it.vis0 + key] = v;
+      P2Hand h;
+      h.u = it.u;
+      h.kb = it.kb;
+      h.n = min(kKeysP2, it.n_v - it.kb * kKeysP2);
+      h.end = 0;
+      if (!hand_off(h, v)) {
+        if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+        return;
+      }
+    }
+  }
+  P2Hand h;
+  h.u = h.kb = h.n = 0;
+  h.end = 1;
+  if (!hand_off(h, 0.f) && tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
 }
 
 // ------------------------------------------------------------------ pass 2k
@@ -797,7 +977,7 @@ cudaError_t launch_p2k_t(const Dev& p, const StreamMaps& m, const Ws& w, int sms
 
 bool stream_eligible(const Dev& p, const LayerPtrs& lp) {
   if (p.dtype != AIRCACHE_BF16 || (p.d != 64 && p.d != 128)) return false;
-  if ((p.max_visual + kKeysP2 - 1) / kKeysP2 > 65535 || p.h_kv * kRC * (int)sizeof(float) > 48 * 1024) return false;
+  if ((p.max_visual + kKeysP2 - 1) / kKeysP2 > 65535 || p.h_kv * kRC * (int)sizeof(float) > 16 * 1024) return false;
   const long long U = (long long)p.L * p.B;
   if (U * p.rows_max + kRC > INT32_MAX || U * p.h_kv * p.max_elite + kTK > INT32_MAX) {
     return false;  // TMA row coordinates are 32-bit
@@ -811,23 +991,25 @@ bool encode_stream_maps(const Dev& p, const LayerPtrs& lp, const Ws& w, StreamMa
   return w.lg && w.part_s && encode_keys<__nv_bfloat16>(&m->kmap, p, lp, kTK) &&
          encode_keys<__nv_bfloat16>(&m->kmap2, p, lp, 2 * kTK) &&
          encode_rows<__nv_bfloat16>(&m->qmap, w.qel, p.d, U * p.rows_max, kRC) &&
-         encode_rows<__nv_bfloat16>(&m->kelmap, w.kel, p.d, U * p.h_kv * p.max_elite, kTK);
+         encode_rows<__nv_bfloat16>(&m->kelmap, w.kel, p.d, U * p.h_kv * p.max_elite, kTK) &&
+         encode_logits(&m->lgmap, w.lg, (p.total_visual + 4LL * p.B + 7) / 4 * 4, (long long)p.L * p.h_kv * kRC,
+                       kKeysP2, kP2Box);
 }
 
 cudaError_t launch_stream_p1(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s) {
   return p.d == 128 ? launch_p1_t<128>(p, m, w, sms, s) : launch_p1_t<64>(p, m, w, sms, s);
 }
 
-cudaError_t launch_stream_p2(const Dev& p, const Ws& w, cudaStream_t s) {
+cudaError_t launch_stream_p2(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s) {
   SArgs a;
   std::memset(&a, 0, sizeof a);
+  a.lgmap = m.lgmap;
   a.p = p;
   a.w = w;
-  const dim3 grid((unsigned)(p.L * p.B), (unsigned)((p.max_visual + kKeysP2 - 1) / kKeysP2));
-  const int smem = (int)sizeof(float) * p.h_kv * kRC;
+  const int smem = kP2CtlOff + (int)sizeof(Ctl2p) + (int)sizeof(float) * p.h_kv * kRC + 128;
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(stream_p2_kernel), smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(stream_p2_kernel, grid, dim3(kT2), smem, s, a);
+  return launch_pdl(stream_p2_kernel, dim3(sms), dim3(kT2p), smem, s, a);
 }
 
 cudaError_t launch_stream_p2k(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s) {

@@ -118,4 +118,20 @@ bool encode_keys(CUtensorMap* m, const Dev& p, const LayerPtrs& lp, int rows_box
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A 2-D map over an fp32 matrix of `rows` rows of `cols` elements (cols a
+// multiple of 4, so rows are 16-byte aligned), box (box_cols, box_rows), no
+// swizzle: a copied box lands row-major, box_cols floats per row.
+inline bool encode_logits(CUtensorMap* m, const float* base, long long cols, long long rows, int box_cols,
+                          int box_rows) {
+  auto enc = tma_encoder();
+  if (!enc || rows < 1 || cols < 1 || cols % 4 != 0 || !base) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * sizeof(float)};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace aircache
