@@ -5,12 +5,13 @@
 // One CTA of 1024 threads per (request, layer).  I_v is mapped to
 // order-preserving 32-bit keys, held in shared memory when the unit fits
 // (otherwise re-read from global memory each pass).  An MSB-first radix select
-// with digits of 11, 11 and 10 bits finds the exact keep-th largest key T and
-// how many keys equal to T are still wanted (it stops early once every key of
-// the selected bucket is taken).  Wide digits matter here: the I_v of a layer
-// spans a few octaves, so an 8-bit top digit would put nearly every key in one
-// bucket.  After the first digit the keys that can still be T are compacted, so
-// the later passes touch only them.  The emission splits the positions into 32
+// finds the exact keep-th largest key T and how many keys equal to T are still
+// wanted (it stops early once every key of the selected bucket is taken).  The
+// digits are 11 bits wide and start below the highest bit in which the unit's
+// smallest and largest keys differ: the I_v of a layer spans a few octaves, so
+// digits taken from the top of the word would put nearly every key in one
+// bucket (and its shared-memory counter).  After the first digit the keys that
+// can still be T are compacted, so the later passes touch only them.  The emission splits the positions into 32
 // contiguous segments, one per warp, and takes every key > T plus the
 // lowest-position keys == T with ballots and one scan of the warp totals, so
 // the output is in ascending position order.
@@ -78,6 +79,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   __shared__ int wsum[kSelWarps + 1];
   __shared__ int wgt[kSelWarps + 1], weq[kSelWarps + 1];
   __shared__ unsigned sel_digit, sel_above, sel_count, n_cand_s;
+  __shared__ uint32_t wmin[kSelWarps], wmax[kSelWarps];
   pdl_trigger();
   pdl_wait();  // I_v and the keep counts
   if (*(volatile int32_t*)w.error != 0) return;
@@ -100,27 +102,47 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   }
   if (k == 0) return;
   const bool staged = n <= a.smem_keys;
-  if (staged) {
-    for (int i0 = tid; i0 < n; i0 += 8 * kSelThreads) {
-      float v[8];
+  // stage the keys (when they fit) and find the smallest and largest
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+  for (int i0 = tid; i0 < n; i0 += 8 * kSelThreads) {
+    float v[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) v[q] = (i0 + q * kSelThreads < n) ? __ldcg(x + i0 + q * kSelThreads) : 0.f;
+    for (int q = 0; q < 8; ++q) v[q] = (i0 + q * kSelThreads < n) ? __ldcg(x + i0 + q * kSelThreads) : 0.f;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (i0 + q * kSelThreads < n) keys_s[i0 + q * kSelThreads] = order_key(v[q]);
+    for (int q = 0; q < 8; ++q) {
+      if (i0 + q * kSelThreads < n) {
+        const uint32_t key = order_key(v[q]);
+        if (staged) keys_s[i0 + q * kSelThreads] = key;
+        kmin = min(kmin, key);
+        kmax = max(kmax, key);
       }
     }
   }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) {
+    wmin[warp] = kmin;
+    wmax[warp] = kmax;
+  }
+  __syncthreads();
+  kmin = __reduce_min_sync(0xffffffffu, wmin[lane]);
+  kmax = __reduce_max_sync(0xffffffffu, wmax[lane]);
   auto key_at = [&](int i) -> uint32_t { return staged ? keys_s[i] : order_key(__ldcg(x + i)); };
 
   uint32_t* cand = keys_s + a.smem_keys;  // keys still able to be T (staged units, after the first digit)
   int n_cand = n;
-  uint32_t prefix = 0, mask = 0;
+  // every key shares the bits above the highest bit in which kmin and kmax differ
+  int top = kmin == kmax ? -1 : 31 - __clz((int)(kmin ^ kmax));
+  uint32_t mask = top >= 31 ? 0u : ~((2u << top) - 1u);
+  if (top < 0) mask = 0xffffffffu;
+  uint32_t prefix = kmin & mask;
   unsigned want = (unsigned)k;  // keys >= T still to account for
   bool all_taken = false;       // every key of the selected bucket is taken: T = prefix, no ties to break
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const int bits = pass == 2 ? 10 : 11;
+  if (tid == 0) sel_count = (unsigned)n;  // all keys equal: every one is == T
+  for (int pass = 0; top >= 0; ++pass) {
+    const int bits = min(11, top + 1);
+    const int shift = top - bits + 1;
+    top = shift - 1;
     const int nb = 1 << bits;
     const uint32_t dmask = (uint32_t)nb - 1u;
     for (int i = tid; i < nb; i += kSelThreads) hist[i] = 0;
@@ -133,11 +155,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
     }
     __syncthreads();
     // bins in descending digit order: thread t owns positions t*bpt .. t*bpt+bpt-1
-    const int bpt = nb / kSelThreads;  // 2 or 1
-    unsigned c0 = hist[nb - 1 - tid * bpt], c1 = bpt > 1 ? hist[nb - 2 - tid * bpt] : 0u;
+    const int bpt = nb > kSelThreads ? nb / kSelThreads : 1;  // 2 or 1
+    const unsigned c0 = tid * bpt < nb ? hist[nb - 1 - tid * bpt] : 0u;
+    const unsigned c1 = bpt > 1 ? hist[nb - 2 - tid * bpt] : 0u;
     int total;
     const unsigned excl = (unsigned)block_excl_scan((int)(c0 + c1), wsum, &total);
-    if (excl < want && want <= excl + c0) {
+    if (tid * bpt < nb && excl < want && want <= excl + c0) {
       sel_digit = (unsigned)(nb - 1 - tid * bpt);
       sel_above = excl;
       sel_count = c0;
@@ -180,14 +203,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   const int seg = ((n + kSelWarps - 1) / kSelWarps + 31) / 32 * 32;
   const int s0 = warp * seg, s1 = min(n, s0 + seg);
   const unsigned lt = (1u << lane) - 1u;
+  __syncthreads();  // sel_count of the last pass is read above by every thread
   int gt = 0, eq = 0;
-  for (int i0 = s0; i0 < s1; i0 += 32) {
-    const int i = i0 + lane;
-    const uint32_t key = i < s1 ? key_at(i) : 0u;
-    const bool g = i < s1 && (all_taken ? key >= thr : key > thr);
-    const bool e = i < s1 && !all_taken && key == thr;
-    gt += __popc(__ballot_sync(0xffffffffu, g));
-    eq += __popc(__ballot_sync(0xffffffffu, e));
+  for (int i0 = s0; i0 < s1; i0 += 8 * 32) {
+    uint32_t kk[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = i0 + 32 * q + lane;
+      kk[q] = i < s1 ? key_at(i) : 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = i0 + 32 * q + lane;
+      const bool g = i < s1 && (all_taken ? kk[q] >= thr : kk[q] > thr);
+      const bool e = i < s1 && !all_taken && kk[q] == thr;
+      gt += __popc(__ballot_sync(0xffffffffu, g));
+      eq += __popc(__ballot_sync(0xffffffffu, e));
+    }
   }
   if (lane == 0) {
     wgt[warp] = gt;
@@ -211,18 +243,26 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   }
   __syncthreads();
   int gt_run = wgt[warp], eq_run = weq[warp];
-  for (int i0 = s0; i0 < s1; i0 += 32) {
-    const int i = i0 + lane;
-    const uint32_t key = i < s1 ? key_at(i) : 0u;
-    const bool g = i < s1 && (all_taken ? key >= thr : key > thr);
-    const bool e = i < s1 && !all_taken && key == thr;
-    const unsigned bg = __ballot_sync(0xffffffffu, g), be = __ballot_sync(0xffffffffu, e);
-    const int eq_before = eq_run + __popc(be & lt);
-    // output slot = keys taken before position i = (keys > T before i) + min(keys == T before i, keep_eq)
-    const int pos = gt_run + __popc(bg & lt) + min(eq_before, (int)keep_eq);
-    if (g || (e && eq_before < (int)keep_eq)) out[pos] = i;
-    gt_run += __popc(bg);
-    eq_run += __popc(be);
+  for (int i0 = s0; i0 < s1; i0 += 8 * 32) {
+    uint32_t kk[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = i0 + 32 * q + lane;
+      kk[q] = i < s1 ? key_at(i) : 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int i = i0 + 32 * q + lane;
+      const bool g = i < s1 && (all_taken ? kk[q] >= thr : kk[q] > thr);
+      const bool e = i < s1 && !all_taken && kk[q] == thr;
+      const unsigned bg = __ballot_sync(0xffffffffu, g), be = __ballot_sync(0xffffffffu, e);
+      const int eq_before = eq_run + __popc(be & lt);
+      // output slot = keys taken before position i = (keys > T before i) + min(keys == T before i, keep_eq)
+      const int pos = gt_run + __popc(bg & lt) + min(eq_before, (int)keep_eq);
+      if (g || (e && eq_before < (int)keep_eq)) out[pos] = i;
+      gt_run += __popc(bg);
+      eq_run += __popc(be);
+    }
   }
 }
 

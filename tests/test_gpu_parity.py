@@ -210,6 +210,24 @@ def test_keep_everything_and_keep_one(A, oracle):
     assert staged2["keep"].max() <= 2
 
 
+def test_long_visual_span_unstaged_select(A, oracle):
+    """30,000 visual positions: more keys than the selection stages in shared
+    memory, so its radix passes and emission read I_v from global memory."""
+    wl = custom_workload([30000, 500], [16, 8], L=2, H_q=4, H_kv=2)
+    full_check(A, oracle, wl)
+
+
+def test_long_visual_span_ties(A, oracle):
+    """Zero queries over 30,000 visual positions: every I_v of a unit is equal,
+    so the unstaged selection keeps the lowest positions."""
+    wl = custom_workload([30000], [6], L=2, H_q=4, H_kv=2)
+    wl.q.zero_()
+    staged, _ = full_check(A, oracle, wl)
+    for l in range(2):
+        kp = int(staged["keep"][l])
+        assert staged["idx"][l, :kp].tolist() == list(range(kp))
+
+
 def test_zero_queries_give_ties(A, oracle):
     wl = custom_workload([150], [10], L=2)
     wl.q.zero_()
