@@ -242,39 +242,75 @@ __device__ __forceinline__ double2 unit_moments(const float* x, int n, int tix, 
   return make_double2(s_t, s_k);
 }
 
+// Sums of three float-float values over NT threads, fixed order (each warp by
+// shuffles, then warp 0 over the warp totals); every thread gets the result.
+// `red` is shared scratch of 3 * NT/32 entries.
+template <int NT>
+__device__ __forceinline__ void block_sum_ff3(ff& a, ff& b, ff& c, ff* red, int tix, int bar_id) {
+  constexpr int NW = NT / 32;
+  const int lane = tix & 31, warp = tix >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = ff_add(a, ff_shfl_xor(a, o));
+    b = ff_add(b, ff_shfl_xor(b, o));
+    c = ff_add(c, ff_shfl_xor(c, o));
+  }
+  named_bar_sync(bar_id, NT);  // earlier readers of red are done
+  if (lane == 0) {
+    red[warp] = a;
+    red[NW + warp] = b;
+    red[2 * NW + warp] = c;
+  }
+  named_bar_sync(bar_id, NT);
+  if (warp == 0) {
+    ff ta = lane < NW ? red[lane] : ff{0.f, 0.f};
+    ff tb = lane < NW ? red[NW + lane] : ff{0.f, 0.f};
+    ff tc = lane < NW ? red[2 * NW + lane] : ff{0.f, 0.f};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ta = ff_add(ta, ff_shfl_xor(ta, o));
+      tb = ff_add(tb, ff_shfl_xor(tb, o));
+      tc = ff_add(tc, ff_shfl_xor(tc, o));
+    }
+    if (lane == 0) {
+      red[0] = ta;
+      red[1] = tb;
+      red[2] = tc;
+    }
+  }
+  named_bar_sync(bar_id, NT);
+  a = red[0];
+  b = red[1];
+  c = red[2];
+}
+
 // Moments of the values held by NT threads (each thread up to V values, valid
-// where ok[i]; n = the number of valid values, n >= 1), two-pass within the
-// group: the mean from a float-float block sum, then the centred sums.  The
-// result is valid in thread tix == 0.  `red` is shared scratch of
-// 2 * NT/32 + 1 ff, `redf` of 2 * NT/32 floats.
+// where ok[i]; n = the number of valid values, n >= 1) in one pass: with a
+// shift c near the values (any float; the same in every thread) the sums
+// T_k = sum (x - c)^k, k = 1..3, are formed in float-float (x - c exactly),
+// reduced once over the group, and turned into the central moments about the
+// mean (q = T_1 / n):  M2 = T_2 - q T_1,  M3 = T_3 - 3 q T_2 + 2 q^2 T_1.
+// The result is valid in thread tix == 0.  `red` is shared scratch of
+// 3 * NT/32 ff, `redf` of 2 * NT/32 floats.
 template <int NT, int V>
-__device__ __forceinline__ Mom block_moments(const float (&x)[V], const bool (&ok)[V], float n, ff* red,
+__device__ __forceinline__ Mom block_moments(const float (&x)[V], const bool (&ok)[V], float n, float c, ff* red,
                                              float* redf, int tix, int bar_id) {
   constexpr int NW = NT / 32;
   const int lane = tix & 31, warp = tix >> 5;
-  ff s{0.f, 0.f};
+  ff t1{0.f, 0.f}, t2{0.f, 0.f}, t3{0.f, 0.f};
   float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     if (ok[i]) {
-      s = ff_add(s, ff{x[i], 0.f});
+      const ff d = ff_two_sum(x[i], -c);  // exact
+      const ff d2 = ff_mul(d, d);
+      t1 = ff_add(t1, d);
+      t2 = ff_add(t2, d2);
+      t3 = ff_add(t3, ff_mul(d2, d));
       mn = fminf(mn, x[i]);
       mx = fmaxf(mx, x[i]);
     }
   }
-  s = block_sum_ff<NT>(s, red, tix, bar_id);
-  const ff mean = ff_div_f(s, n);
-  ff m2{0.f, 0.f}, m3{0.f, 0.f};
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    if (ok[i]) {
-      const ff d = ff_add(ff{x[i], 0.f}, ff_neg(mean));
-      const ff d2 = ff_mul(d, d);
-      m2 = ff_add(m2, d2);
-      m3 = ff_add(m3, ff_mul(d2, d));
-    }
-  }
-  block_sum_ff2<NT>(m2, m3, red, tix, bar_id);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
@@ -284,18 +320,21 @@ __device__ __forceinline__ Mom block_moments(const float (&x)[V], const bool (&o
     redf[warp] = mn;
     redf[NW + warp] = mx;
   }
-  named_bar_sync(bar_id, NT);
+  block_sum_ff3<NT>(t1, t2, t3, red, tix, bar_id);  // its barriers also publish redf
   Mom r;
   r.n = n;
-  r.s = s;
-  r.mean = mean;
-  r.m2 = m2;
-  r.m3 = m3;
-  r.mn = redf[0];
-  r.mx = redf[NW];
-  for (int i = 1; i < NW; ++i) {
-    r.mn = fminf(r.mn, redf[i]);
-    r.mx = fmaxf(r.mx, redf[NW + i]);
+  if (tix == 0) {
+    const ff q = ff_div_f(t1, n);
+    r.s = ff_add(ff_mul(ff{n, 0.f}, ff{c, 0.f}), t1);
+    r.mean = ff_add(ff{c, 0.f}, q);
+    r.m2 = ff_add(t2, ff_neg(ff_mul(q, t1)));
+    r.m3 = ff_add(ff_add(t3, ff_neg(ff_mul(ff_mul(ff{3.f, 0.f}, q), t2))), ff_mul(ff_mul(ff{2.f, 0.f}, ff_mul(q, q)), t1));
+    r.mn = redf[0];
+    r.mx = redf[NW];
+    for (int i = 1; i < NW; ++i) {
+      r.mn = fminf(r.mn, redf[i]);
+      r.mx = fmaxf(r.mx, redf[NW + i]);
+    }
   }
   return r;
 }

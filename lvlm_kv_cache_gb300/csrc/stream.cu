@@ -516,7 +516,9 @@ constexpr int kKeysP2 = kT2;                  // keys per pass-2 item (one per t
 constexpr int kP2Box = 8;                     // logit rows per TMA box
 constexpr int kP2Slice = kRC * kKeysP2 * 4;   // one KV head's logits of an item (32 KB)
 constexpr int kP2Stages = 6;                  // slices in flight
-constexpr int kT2p = 2 * kT2;                 // pass-2 threads: streamers, then moment warps
+constexpr int kMomT = 128;                    // pass-2 moment threads (two values each)
+constexpr int kT2p = kT2 + 32 + kMomT;        // pass-2 threads: streamers, the producer warp, moment warps
+constexpr int kP2Prod = kT2 / 32;             // the producer warp
 constexpr int kBarP2S = 1;                    // named barrier of the streamers
 constexpr int kBarP2M = 2;                    // named barrier of the moment warps
 constexpr int kP2CtlOff = kP2Stages * kP2Slice;
@@ -535,7 +537,7 @@ struct P2Hand {
 };
 
 struct Ctl2p {
-  uint64_t full[kP2Stages];
+  uint64_t full[kP2Stages], empty[kP2Stages];
   uint64_t hfull[2], hempty[2];  // hand-off buffers: filled by the streamers, released by the moment warps
   P2Rec rec[kP2Stages];
   P2Hand hand[2];
@@ -544,32 +546,35 @@ struct Ctl2p {
 
 // The unit record (seq0, vis0, txt0, n_v), (n_t, n_tk, 1, u) of single unit
 // si, loaded once per unit.
-struct P2Unit {
-  int si = -1;
+// The walk of a CTA's items: item index, its (single unit si, key block kb),
+// and the record (seq0, vis0, txt0, n_v), (n_t, n_tk, 1, u) of unit si, loaded
+// once per unit.
+struct P2Cursor {
+  long long item, end;
+  int si, kb, KB, slot0;
+  int loaded = -1;
   int4 r0, r1;
 };
 
-// The first item at or after `item` (< end) whose key block lies inside its
-// unit; items run over (single unit si, key block kb), si-major, KB blocks per
-// unit.  Returns 0 past the end, 1 with the item in `r`, 2 for a unit record
-// that fails validation.
-__device__ __forceinline__ int p2_item(const Dev& p, const Ws& w, long long& item, long long end, int KB, int slot0,
-                                       P2Unit& cu, P2Rec& r) {
-  for (; item < end; ++item) {
-    const int si = (int)(item / KB), kb = (int)(item % KB);
-    if (si != cu.si) {
-      cu.si = si;
-      cu.r0 = __ldcg(&w.stream_info[2 * (slot0 + si)]);
-      cu.r1 = __ldcg(&w.stream_info[2 * (slot0 + si) + 1]);
+// Advance the cursor to the first item at or after its position whose key
+// block lies inside its unit; items run over (si, kb), si-major, KB blocks per
+// unit.  Returns 0 past the end, 1 with the item in `r` (the cursor stays on
+// it), 2 for a unit record that fails validation.
+__device__ __forceinline__ int p2_item(const Dev& p, const Ws& w, P2Cursor& cu, P2Rec& r) {
+  for (; cu.item < cu.end; ++cu.item) {
+    if (cu.si != cu.loaded) {
+      cu.loaded = cu.si;
+      cu.r0 = __ldcg(&w.stream_info[2 * (cu.slot0 + cu.si)]);
+      cu.r1 = __ldcg(&w.stream_info[2 * (cu.slot0 + cu.si) + 1]);
     }
     const int4 r0 = cu.r0, r1 = cu.r1;
     if (!stream_unit(p, r1.w, r0, r1) || p.g * r1.y > kRC) return 2;
-    if (kb * kKeysP2 < r0.w) {
+    if (cu.kb * kKeysP2 < r0.w) {
       r.state = 0;
       r.u = r1.w;
       r.l = r1.w / p.B;
       r.b = r1.w % p.B;
-      r.kb = kb;
+      r.kb = cu.kb;
       r.n_v = r0.w;
       r.n_tk = r1.y;
       r.rows = p.g * r1.y;
@@ -577,40 +582,221 @@ __device__ __forceinline__ int p2_item(const Dev& p, const Ws& w, long long& ite
       r.vis0 = r0.y;
       return 1;
     }
+    if (++cu.kb == cu.KB) {
+      cu.kb = 0;
+      ++cu.si;
+    }
   }
   return 0;
 }
 
+// Step past the current item.
+__device__ __forceinline__ void p2_next(P2Cursor& cu) {
+  ++cu.item;
+  if (++cu.kb == cu.KB) {
+    cu.kb = 0;
+    ++cu.si;
+  }
+}
+
 // Pass 2 for one-chunk units (g * N_tk <= 32), persistent: CTA c takes a
-// contiguous range of the items.  Streaming warps: thread 0 walks the range
-// ahead of the others and loads, for each item and KV head, that head's logits
-// (rows < 32, 256 keys) by TMA into a ring of 32 KB shared-memory stages, with
-// a record of what the stage holds; streaming thread t owns key k0 + t and sums
+// contiguous range of the (unit, 256-key block) items.  A producer warp walks
+// the range and loads, for each item and KV head, that head's logits (rows <
+// 32, 256 keys) by TMA into a ring of 32 KB shared-memory stages, with a record
+// of what the stage holds.  Streaming thread t owns key k0 + t and sums
 // exp2(logit - lse) over the rows of every KV head, writes I_v and hands the
-// item's 256 values to the moment warps (double-buffered), which reduce them to
-// the item's moment record while the streamers go on with the next item.  The
-// row LSEs of a unit are merged from pass 1's partials (quads of lanes) when the
-// walk enters the unit, while later slices are in flight.  Multi-chunk units:
-// every thread first helps publish their row LSEs for pass 2k.
+// item's values to the moment warps (double-buffered), which reduce them to the
+// item's moment record while the streamers go on.  The row LSEs of a unit are
+// merged from pass 1's partials (quads of lanes) when the walk enters the unit.
+// Multi-chunk units: every thread first helps publish their row LSEs for pass
+// 2k.
+
+// Shared state of a pass-2 CTA.
+struct P2Smem {
+  unsigned char* sm;  // stage area
+  Ctl2p* c;           // ring and the moment hand-off
+  float* lse_s;       // [h_kv][32] row LSEs of the current unit
+  ff* red;
+  float* redf;
+};
+
+// Hand an item (or the end) from the 256 streamers to the moment warps.  The
+// caller's values go to hx[hb][key] where `ok`; every streamer arrives.
+__device__ __forceinline__ bool p2_hand_off(Ctl2p* c, int& n_hand, const P2Hand& h, int nval, const float* x,
+                                            const int* key, const bool* ok) {
+  const int hb = n_hand & 1;
+  if (!mbar_wait(&c->hempty[hb], (uint32_t)(((n_hand >> 1) & 1) ^ 1), 4 * kWaitCycles)) return false;
+  for (int i = 0; i < nval; ++i) {
+    if (ok[i]) c->hx[hb][key[i]] = x[i];
+  }
+  if (threadIdx.x == 0) c->hand[hb] = h;
+  mbar_arrive(&c->hfull[hb]);
+  ++n_hand;
+  return true;
+}
+
+// Moment warps: one record per handed-off item, until the end record.
+__device__ __forceinline__ void p2_moments(const Dev& p, const Ws& w, const P2Smem& S, int mt) {
+  Ctl2p* c = S.c;
+  for (int n = 0;; ++n) {
+    const int hb = n & 1;
+    if (!mbar_wait(&c->hfull[hb], (uint32_t)((n >> 1) & 1), 4 * kWaitCycles)) {
+      if (mt == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    const P2Hand h = c->hand[hb];
+    const float* hx = c->hx[hb];
+    float xv[2] = {(!h.end && mt < h.n) ? hx[mt] : 0.f, (!h.end && mt + kMomT < h.n) ? hx[mt + kMomT] : 0.f};
+    // shift: the mean of four of the item's values (the same in every thread)
+    const float sh = h.end ? 0.f
+                           : 0.25f * ((hx[0] + hx[min(64, h.n - 1)]) + (hx[min(128, h.n - 1)] + hx[min(192, h.n - 1)]));
+    mbar_arrive(&c->hempty[hb]);
+    if (h.end) return;
+    bool okv[2] = {mt < h.n, mt + kMomT < h.n};
+    const Mom mb = block_moments<kMomT, 2>(xv, okv, (float)h.n, sh, S.red, S.redf, mt, kBarP2M);
+    if (mt == 0) mom_store(w.mom + ((size_t)h.u * p.mom_slots + h.kb) * kMomWords, mb);
+  }
+}
+
+// One-chunk role: the producer warp (warp kP2Prod, lane 0) and the 256
+// streamers over items [i_beg, i_end) of the one-chunk units.
+__device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, long long i_beg, long long i_end, int KB,
+                                          int slot0) {
+  const Dev& p = a.p;
+  const Ws& w = a.w;
+  Ctl2p* c = S.c;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float* slices = reinterpret_cast<const float*>(S.sm);  // [kP2Stages][32][256]
+  if (warp == kP2Prod) {
+    // producer: one thread fills the ring, then sends the end record
+    if (lane != 0) return;
+    fence_proxy_async_global();  // the logits were written by the previous kernel's generic stores
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&a.lgmap)) : "memory");
+    P2Cursor cu;
+    cu.item = i_beg;
+    cu.end = i_end;
+    cu.KB = KB;
+    cu.slot0 = slot0;
+    cu.si = (int)(i_beg / KB);
+    cu.kb = (int)(i_beg % KB);
+    P2Rec pr = {};
+    int pstate = p2_item(p, w, cu, pr);
+    for (long long st = 0;; ++st) {
+      const int slot = (int)(st % kP2Stages);
+      if (!mbar_wait(&c->empty[slot], (uint32_t)(((st / kP2Stages) & 1) ^ 1), 4 * kWaitCycles)) {
+        set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+        return;
+      }
+      if (pstate != 1) {
+        c->rec[slot].state = pstate == 0 ? 1 : 2;
+        mbar_arrive(&c->full[slot]);
+        return;
+      }
+      c->rec[slot] = pr;
+      const int nb = (pr.rows + kP2Box - 1) / kP2Box;
+      mbar_arrive_expect_tx(&c->full[slot], (uint32_t)(nb * kP2Box * kKeysP2 * 4));
+      const int x = (int)(lg_col0(pr.vis0, pr.b) + (long long)pr.kb * kKeysP2);
+      const int y = (pr.l * p.h_kv + pr.kvh) * kRC;
+      for (int j = 0; j < nb; ++j) {
+        tma_load_2d(smem_u32(S.sm + slot * kP2Slice + j * kP2Box * kKeysP2 * 4), &a.lgmap, x, y + j * kP2Box,
+                    &c->full[slot]);
+      }
+      if (++pr.kvh == p.h_kv) {
+        p2_next(cu);
+        pstate = p2_item(p, w, cu, pr);
+      }
+    }
+  }
+  if (warp > kP2Prod) return;
+  // streamers
+  const float scale = p.scale_log2;  // stored logits are raw q.k
+  int cur_u = -1, n_hand = 0;
+  float acc = 0.f;
+  for (long long stage = 0;; ++stage) {
+    const int slot = (int)(stage % kP2Stages);
+    if (!mbar_wait(&c->full[slot], (uint32_t)((stage / kP2Stages) & 1), 4 * kWaitCycles)) {
+      if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+      break;
+    }
+    const P2Rec it = c->rec[slot];
+    if (it.state != 0) {
+      if (it.state == 2 && tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+      break;
+    }
+    if (it.kvh == 0) {
+      if (it.u != cur_u) {
+        // the unit's row LSEs, four lanes per row (whole quads iterate together)
+        named_bar_sync(kBarP2S, kT2);  // every streamer is done with the previous unit's LSEs
+        const int chv = ((it.n_v + kTK - 1) / kTK + kCK - 1) / kCK;
+        const int nr = p.h_kv * it.rows;
+        for (int q4 = tid >> 2; q4 < (nr + kT2 / 4 - 1) / (kT2 / 4) * (kT2 / 4); q4 += kT2 / 4) {
+          const int qq = min(q4, nr - 1);
+          const int kvh = qq / it.rows, r = qq % it.rows;
+          const float lse = row_lse4(p, w, it.u, kvh, r, chv, tid & 3);
+          if (q4 < nr && (tid & 3) == 0) S.lse_s[kvh * kRC + r] = lse;
+        }
+        named_bar_sync(kBarP2S, kT2);
+        cur_u = it.u;
+      }
+      acc = 0.f;
+    }
+    const float* x = slices + (size_t)slot * (kRC * kKeysP2) + tid;
+    const float* ls = S.lse_s + it.kvh * kRC;
+    int r = 0;
+    for (; r + 8 <= it.rows; r += 8) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc += fast_exp2(fmaf(x[(r + q) * kKeysP2], scale, -ls[r + q]));
+    }
+    for (; r < it.rows; ++r) acc += fast_exp2(fmaf(x[r * kKeysP2], scale, -ls[r]));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&c->empty[slot]);  // this warp is done with the slot and its record
+    if (it.kvh == p.h_kv - 1) {
+      const int key = it.kb * kKeysP2 + tid;
+      const float v = acc / (float)(p.h_q * it.n_tk);
+      const bool ok = key < it.n_v;
+      if (ok) w.iv[(size_t)it.l * p.total_visual + it.vis0 + key] = v;
+      P2Hand h;
+      h.u = it.u;
+      h.kb = it.kb;
+      h.n = min(kKeysP2, it.n_v - it.kb * kKeysP2);
+      h.end = 0;
+      if (!p2_hand_off(c, n_hand, h, 1, &v, &tid, &ok)) {
+        if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+        return;
+      }
+    }
+  }
+  P2Hand h;
+  h.u = h.kb = h.n = 0;
+  h.end = 1;
+  const bool no = false;
+  const float zero = 0.f;
+  if (!p2_hand_off(c, n_hand, h, 1, &zero, &tid, &no) && tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+}
+
 __global__ void __launch_bounds__(kT2p, 1) stream_p2_kernel(const __grid_constant__ SArgs a) {
   const Dev& p = a.p;
   const Ws& w = a.w;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
-  const float* slices = reinterpret_cast<const float*>(sm);  // [kP2Stages][32][256]
-  Ctl2p* c = reinterpret_cast<Ctl2p*>(sm + kP2CtlOff);
-  float* lse_s = reinterpret_cast<float*>(sm + kP2CtlOff + sizeof(Ctl2p));  // [h_kv][32]
-  __shared__ ff red[2 * (kT2 / 32) + 1];
-  __shared__ float redf[2 * (kT2 / 32)];
-  const int tid = threadIdx.x;
+  __shared__ ff red[3 * (kMomT / 32)];
+  __shared__ float redf[2 * (kMomT / 32)];
+  P2Smem S;
+  S.sm = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
+  S.c = reinterpret_cast<Ctl2p*>(S.sm + kP2CtlOff);
+  S.lse_s = reinterpret_cast<float*>(S.sm + kP2CtlOff + sizeof(Ctl2p));
+  S.red = red;
+  S.redf = redf;
+  const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
-    for (int i = 0; i < kP2Stages; ++i) mbar_init(&c->full[i], 1);
+    for (int i = 0; i < kP2Stages; ++i) {
+      mbar_init(&S.c->full[i], 1);
+      mbar_init(&S.c->empty[i], kT2 / 32);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&c->hfull[i], kT2);
-      mbar_init(&c->hempty[i], kT2);
+      mbar_init(&S.c->hfull[i], kT2);
+      mbar_init(&S.c->hempty[i], kMomT);
     }
     fence_mbar_init();
-    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&a.lgmap)) : "memory");
   }
   __syncthreads();
   pdl_trigger();
@@ -639,135 +825,15 @@ __global__ void __launch_bounds__(kT2p, 1) stream_p2_kernel(const __grid_constan
       lse_u[kvh * rows_per_kv(p) + r] = row_lse(p, w, u, kvh, r, chv);
     }
   }
-
-  if (tid >= kT2) {
-    // moment warps: one record per handed-off item
-    const int mt = tid - kT2;
-    for (int n = 0;; ++n) {
-      const int hb = n & 1;
-      if (!mbar_wait(&c->hfull[hb], (uint32_t)((n >> 1) & 1), 4 * kWaitCycles)) {
-        if (mt == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
-        return;
-      }
-      const P2Hand h = c->hand[hb];
-      float xv[1] = {c->hx[hb][mt]};
-      mbar_arrive(&c->hempty[hb]);
-      if (h.end) break;
-      bool okv[1] = {mt < h.n};
-      const Mom mb = block_moments<kT2, 1>(xv, okv, (float)h.n, red, redf, mt, kBarP2M);
-      if (mt == 0) mom_store(w.mom + ((size_t)h.u * p.mom_slots + h.kb) * kMomWords, mb);
-    }
+  if (warp > kP2Prod) {
+    p2_moments(p, w, S, tid - kT2 - 32);
     return;
   }
-
-  // streaming warps
   const int n_single = n_total - n_multi;
-  const int slot0 = LB - n_single;
   const int KB = (p.max_visual + kKeysP2 - 1) / kKeysP2;
-  const long long n_items = (long long)n_single * KB;
-  const long long i_beg = n_items * blockIdx.x / gridDim.x, i_end = n_items * (blockIdx.x + 1) / gridDim.x;
-  // producer state (thread 0): the next stage to fill
-  long long pi = i_beg;
-  P2Rec pr = {};
-  P2Unit pu;
-  int pstate = 0;      // 1: pr holds the next slice; 0 / 2: end / bad record next
-  bool ended = false;  // the end record has been sent
-  auto issue = [&](int slot) {
-    if (ended) return;
-    if (pstate != 1) {
-      c->rec[slot].state = pstate == 0 ? 1 : 2;
-      mbar_arrive(&c->full[slot]);
-      ended = true;
-      return;
-    }
-    c->rec[slot] = pr;
-    const int nb = (pr.rows + kP2Box - 1) / kP2Box;
-    mbar_arrive_expect_tx(&c->full[slot], (uint32_t)(nb * kP2Box * kKeysP2 * 4));
-    const int x = (int)(lg_col0(pr.vis0, pr.b) + (long long)pr.kb * kKeysP2);
-    const int y = (pr.l * p.h_kv + pr.kvh) * kRC;
-    for (int j = 0; j < nb; ++j) {
-      tma_load_2d(smem_u32(sm + slot * kP2Slice + j * kP2Box * kKeysP2 * 4), &a.lgmap, x, y + j * kP2Box,
-                  &c->full[slot]);
-    }
-    if (++pr.kvh == p.h_kv) {
-      ++pi;
-      pstate = p2_item(p, w, pi, i_end, KB, slot0, pu, pr);
-    }
-  };
-  if (tid == 0) {
-    fence_proxy_async_global();  // the logits were written by the previous kernel's generic stores
-    pstate = p2_item(p, w, pi, i_end, KB, slot0, pu, pr);
-    for (int st = 0; st < kP2Stages; ++st) issue(st);
-  }
-  const float scale = p.scale_log2;  // stored logits are raw q.k
-  int cur_u = -1, n_hand = 0;
-  float acc = 0.f;
-  // hand an item (or the end) to the moment warps
-  auto hand_off = [&](const P2Hand& h, float x) -> bool {
-    const int hb = n_hand & 1;
-    if (!mbar_wait(&c->hempty[hb], (uint32_t)(((n_hand >> 1) & 1) ^ 1), 4 * kWaitCycles)) return false;
-    c->hx[hb][tid] = x;
-    if (tid == 0) c->hand[hb] = h;
-    mbar_arrive(&c->hfull[hb]);
-    ++n_hand;
-    return true;
-  };
-  for (long long stage = 0;; ++stage) {
-    const int slot = (int)(stage % kP2Stages);
-    if (!mbar_wait(&c->full[slot], (uint32_t)((stage / kP2Stages) & 1), 4 * kWaitCycles)) {
-      if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
-      break;
-    }
-    const P2Rec it = c->rec[slot];
-    if (it.state != 0) {
-      if (it.state == 2 && tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
-      break;
-    }
-    if (it.kvh == 0) {
-      if (it.u != cur_u) {
-        // the unit's row LSEs, four lanes per row (whole quads iterate together)
-        const int chv = ((it.n_v + kTK - 1) / kTK + kCK - 1) / kCK;
-        const int nr = p.h_kv * it.rows;
-        for (int q4 = tid >> 2; q4 < (nr + kT2 / 4 - 1) / (kT2 / 4) * (kT2 / 4); q4 += kT2 / 4) {
-          const int qq = min(q4, nr - 1);
-          const int kvh = qq / it.rows, r = qq % it.rows;
-          const float lse = row_lse4(p, w, it.u, kvh, r, chv, tid & 3);
-          if (q4 < nr && (tid & 3) == 0) lse_s[kvh * kRC + r] = lse;
-        }
-        named_bar_sync(kBarP2S, kT2);
-        cur_u = it.u;
-      }
-      acc = 0.f;
-    }
-    const float* x = slices + (size_t)slot * (kRC * kKeysP2) + tid;
-    const float* ls = lse_s + it.kvh * kRC;
-    int r = 0;
-    for (; r + 8 <= it.rows; r += 8) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc += fast_exp2(fmaf(x[(r + q) * kKeysP2], scale, -ls[r + q]));
-    }
-    for (; r < it.rows; ++r) acc += fast_exp2(fmaf(x[r * kKeysP2], scale, -ls[r]));
-    named_bar_sync(kBarP2S, kT2);  // every streamer is done with the slot and its record
-    if (tid == 0) issue(slot);
-    if (it.kvh == p.h_kv - 1) {
-      const int key = it.kb * kKeysP2 + tid;
-      const float v = acc / (float)(p.h_q * it.n_tk);
-      if (key < it.n_v) w.iv[(size_t)it.l * p.total_visual + it.vis0 + key] = v;
-      P2Hand h;
-      h.u = it.u;
-      h.kb = it.kb;
-      h.n = min(kKeysP2, it.n_v - it.kb * kKeysP2);
-      h.end = 0;
-      if (!hand_off(h, v)) {
-        if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
-        return;
-      }
-    }
-  }
-  P2Hand h;
-  h.u = h.kb = h.n = 0;
-  h.end = 1;
-  if (!hand_off(h, 0.f) && tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+  const long long N_s = (long long)n_single * KB;
+  const long long i_beg = N_s * blockIdx.x / gridDim.x, i_end = N_s * (blockIdx.x + 1) / gridDim.x;
+  p2_single(a, S, i_beg, i_end, KB, LB - n_single);
 }
 
 // ------------------------------------------------------------------ pass 2k
@@ -791,8 +857,9 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   Ctl2* c = reinterpret_cast<Ctl2*>(sm + Gm::kCtl2Off);
-  __shared__ ff red[2 * (kT2 / 32) + 1];
+  __shared__ ff red[3 * (kT2 / 32)];
   __shared__ float redf[2 * (kT2 / 32)];
+  __shared__ float shs[4];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g4 = lane >> 2, c4 = lane & 3;
   const uint32_t sbase = smem_u32(sm);
@@ -936,8 +1003,15 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
         okv[2 * nt + e] = g4 == 0 && key < klim;
         if (okv[2 * nt + e]) iv[(long long)tile * kTK + key] = xv[2 * nt + e];
       }
-    // this tile's moments, for the statistics kernel
-    const Mom mb = block_moments<kT2, 4>(xv, okv, (float)klim, red, redf, tid, kBarT2);
+    // this tile's moments, for the statistics kernel; shift: the mean of the
+    // tile's values at keys 0, 32, 64, 96 that exist (warps 0, 2, 4, 6, lane 0)
+    if ((warp & 1) == 0 && lane == 0) shs[warp >> 1] = okv[0] ? xv[0] : 0.f;
+    named_bar_sync(kBarT2, kT2);
+    const int nsh = min(4, (klim + 31) / 32);
+    float sh = shs[0];
+    for (int i = 1; i < nsh; ++i) sh += shs[i];
+    sh /= (float)nsh;
+    const Mom mb = block_moments<kT2, 4>(xv, okv, (float)klim, sh, red, redf, tid, kBarT2);
     if (tid == 0) mom_store(w.mom + ((size_t)u * p.mom_slots + tile) * kMomWords, mb);
   }
 }
