@@ -403,17 +403,16 @@ __device__ __forceinline__ void layer_stats_warp(const float4* rec, int nslots, 
 template <typename Get>
 __device__ __forceinline__ void request_budget_warp(const Dev& p, int b, int n_v, Get get, int32_t* keep,
                                                     int lane) {
-  constexpr int kOwn = (AIRCACHE_MAX_LAYERS + 31) / 32;
-  ff st[kOwn], sk[kOwn];
+  // The loops over a lane's layers stay rolled (re-reading the pairs through
+  // `get`): this runs once per request, so its code is usually cold in the
+  // instruction cache and its size, not its arithmetic, sets the time.
   ff st_sum{0.f, 0.f}, sk_min{INFINITY, 0.f};
-#pragma unroll
-  for (int j = 0; j < kOwn; ++j) {
-    const int l = lane + 32 * j;
-    if (l < p.L) {
-      get(l, st[j], sk[j]);
-      st_sum = ff_add(st_sum, st[j]);
-      if (ff_lt(sk[j], sk_min)) sk_min = sk[j];
-    }
+#pragma unroll 1
+  for (int l = lane; l < p.L; l += 32) {
+    ff st, sk;
+    get(l, st, sk);
+    st_sum = ff_add(st_sum, st);
+    if (ff_lt(sk, sk_min)) sk_min = sk;
   }
   st_sum = warp_sum_ff(st_sum);
 #pragma unroll
@@ -423,29 +422,29 @@ __device__ __forceinline__ void request_budget_warp(const Dev& p, int b, int n_v
   }
   constexpr float kEpsHi = (float)1e-6;
   constexpr float kEpsLo = (float)(1e-6 - (double)kEpsHi);
+  const ff eps{kEpsHi, kEpsLo};
   ff u_sum{0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < kOwn; ++j) {
-    if (lane + 32 * j < p.L) {
-      sk[j] = ff_add(ff_add(sk[j], ff_neg(sk_min)), ff{kEpsHi, kEpsLo});  // now u_l
-      u_sum = ff_add(u_sum, sk[j]);
-    }
+#pragma unroll 1
+  for (int l = lane; l < p.L; l += 32) {
+    ff st, sk;
+    get(l, st, sk);
+    u_sum = ff_add(u_sum, ff_add(ff_add(sk, ff_neg(sk_min)), eps));  // u_l
   }
   u_sum = warp_sum_ff(u_sum);
   const ff mean_st = ff_div_f(st_sum, (float)p.L), mean_u = ff_div_f(u_sum, (float)p.L);
   const float r_hi = (float)p.r;
   const ff r{r_hi, (float)(p.r - (double)r_hi)};
-#pragma unroll
-  for (int j = 0; j < kOwn; ++j) {
-    const int l = lane + 32 * j;
-    if (l < p.L) {
-      const ff st_n = (mean_st.hi != 0.f) ? ff_div(st[j], mean_st) : ff{1.f, 0.f};
-      const ff sk_n = ff_div(sk[j], mean_u);
-      const ff rl = ff_mul(ff_mul(ff{0.5f, 0.f}, ff_add(st_n, sk_n)), r);
-      float kf = ff_floor(ff_add(ff_mul(rl, ff{(float)n_v, 0.f}), ff{0.5f, 0.f}));
-      kf = fminf(fmaxf(kf, 1.f), (float)n_v);
-      keep[l * p.B + b] = (int32_t)kf;
-    }
+#pragma unroll 1
+  for (int l = lane; l < p.L; l += 32) {
+    ff st, sk;
+    get(l, st, sk);
+    const ff u_l = ff_add(ff_add(sk, ff_neg(sk_min)), eps);
+    const ff st_n = (mean_st.hi != 0.f) ? ff_div(st, mean_st) : ff{1.f, 0.f};
+    const ff sk_n = ff_div(u_l, mean_u);
+    const ff rl = ff_mul(ff_mul(ff{0.5f, 0.f}, ff_add(st_n, sk_n)), r);
+    float kf = ff_floor(ff_add(ff_mul(rl, ff{(float)n_v, 0.f}), ff{0.5f, 0.f}));
+    kf = fminf(fmaxf(kf, 1.f), (float)n_v);
+    keep[l * p.B + b] = (int32_t)kf;
   }
 }
 
