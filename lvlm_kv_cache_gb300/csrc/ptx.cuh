@@ -169,10 +169,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // ---------------------------------------------------------------- MMA
 
+// The "memory" clobber keeps the compiler from moving the shared-memory read
+// above the barrier wait that guards the data (the operand is only an address).
 __device__ __forceinline__ void ldmatrix_x4(uint32_t r[4], const void* ptr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(ptr)));
+               : "r"(smem_u32(ptr))
+               : "memory");
 }
 
 // D(16x8, fp32) += A(16x16, bf16, row) * B(16x8, bf16, col)

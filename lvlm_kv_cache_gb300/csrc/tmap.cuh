@@ -52,10 +52,13 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// The "memory" clobber keeps the compiler from moving the shared-memory read
+// above the barrier wait that guards the data (the operand is only an address).
 __device__ __forceinline__ void ldsm_x4(uint32_t r[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
+               : "r"(addr)
+               : "memory");
 }
 
 // ------------------------------------------------------------------ host
