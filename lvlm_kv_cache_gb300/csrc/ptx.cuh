@@ -71,8 +71,10 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 
 // ---------------------------------------------------------------- sync
 
+// Named barrier over `nthreads` threads (a multiple of 32).  The non-aligned
+// form: a warp may arrive with its lanes diverged (after per-lane loops).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+  asm volatile("barrier.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // Thread-block clusters: every thread of every CTA of the cluster arrives

@@ -185,6 +185,7 @@ struct Logits<__nv_bfloat16, D> {
     const int qr = lane & 15;
     const int qc = lane >> 4;
     if (rows > 16) {
+      __syncwarp();  // ldmatrix / mma are warp-collective: the whole warp, converged
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const int slab = kk >> 2, c0 = (kk & 3) * 2;
@@ -198,6 +199,7 @@ struct Logits<__nv_bfloat16, D> {
         mma_bf16_16816(acc[1][1], a1, b[2], b[3]);
       }
     } else {
+      __syncwarp();  // ldmatrix / mma are warp-collective: the whole warp, converged
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const int slab = kk >> 2, c0 = (kk & 3) * 2;

@@ -351,6 +351,7 @@ __device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
     if (h.first) {
       mts = h.rows > 16 ? 2 : 1;
       const uint32_t qs = sbase + (uint32_t)(Gm::kQOff + h.qbuf * Gm::kQBytes);
+      __syncwarp();  // ldmatrix / mma are warp-collective: the whole warp, converged
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
         const int slab = kk >> 2, c0 = (kk & 3) * 2;
@@ -377,6 +378,7 @@ __device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
     const bool busy = 32 * warp < h.klim;  // a warp whose keys are all masked skips the tile
     if (busy) {
       const uint32_t ks = sbase + (uint32_t)(s * Gm::kSBytes);
+      __syncwarp();  // ldmatrix / mma are warp-collective: the whole warp, converged
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
         const int slab = kk >> 2, c0 = (kk & 3) * 2;
@@ -931,6 +933,7 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
       }
       kph ^= 1;
       uint32_t kf[KS][4];
+      __syncwarp();  // ldmatrix / mma are warp-collective: the whole warp, converged
 #pragma unroll
       for (int kk = 0; kk < KS; ++kk) {
         const int slab = kk >> 2, c0 = (kk & 3) * 2;
@@ -955,6 +958,7 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
         const int mts = rows_c > 16 ? 2 : 1;
+        __syncwarp();  // ldmatrix / mma are warp-collective: the whole warp, converged
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           const int slab = kk >> 2, c0 = (kk & 3) * 2;

@@ -42,6 +42,7 @@ struct TileLogits<__nv_bfloat16, D> {
     const __nv_bfloat16* a_base = Ks + (warp * 16 + (lane & 15)) * C::kStride + 8 * (lane >> 4);
     const __nv_bfloat16* b_base = Qs + ((lane & 7) + 8 * (lane >> 4)) * C::kStride + 8 * ((lane >> 3) & 1);
     if (rows > 16) {
+      __syncwarp();  // ldmatrix / mma are warp-collective: the whole warp, converged
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         uint32_t a[4], b0[4], b1[4];
@@ -54,6 +55,7 @@ struct TileLogits<__nv_bfloat16, D> {
         mma_bf16_16816(acc[3], a, b1[2], b1[3]);
       }
     } else {
+      __syncwarp();  // ldmatrix / mma are warp-collective: the whole warp, converged
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         uint32_t a[4], b0[4];
