@@ -69,6 +69,13 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;\n" ::: "memory");
 }
 
+// Order this thread's view of shared memory (including other threads' reads and
+// writes it has synchronised with) before its later async-proxy (TMA) accesses
+// of it: issued before a bulk copy overwrites a buffer that generic loads read.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
 // ---------------------------------------------------------------- sync
 
 // Named barrier over `nthreads` threads (a multiple of 32).  The non-aligned

@@ -488,6 +488,7 @@ __device__ void issuer(const PArgs& a, Ctl* c, unsigned char* stages) {
       if (a.tma) {
         if (lane == 0) {
           const uint32_t kb = smem_u32(base), qb = kb + Gm::kKBytes;
+          fence_proxy_async_smem();  // the stage was last read by generic loads
           mbar_arrive_expect_tx(&c->full[s], (uint32_t)(Gm::kKBytes + Gm::kQBytes + (it.kind == kP2 ? kRC * 4 : 0)));
 #pragma unroll
           for (int sl = 0; sl < Gm::kNH; ++sl) {

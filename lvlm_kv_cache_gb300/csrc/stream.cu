@@ -273,6 +273,7 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
           h.store = (kind == kVis && n_rc == 1) ? 1 : 0;
           h.b = u % p.B;
           h.vis0 = i0.y;
+          fence_proxy_async_smem();  // the stage (and query buffer) were last read by generic loads
           mbar_arrive_expect_tx(&c->full[s], kbytes + (j == 0 ? (uint32_t)Gm::kQBytes : 0u));
           const uint32_t kdst = sbase + (uint32_t)(s * Gm::kSBytes);
 #pragma unroll
@@ -696,6 +697,7 @@ __device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, long 
       }
       c->rec[slot] = pr;
       const int nb = (pr.rows + kP2Box - 1) / kP2Box;
+      fence_proxy_async_smem();  // the slot was last read by generic loads
       mbar_arrive_expect_tx(&c->full[slot], (uint32_t)(nb * kP2Box * kKeysP2 * 4));
       const int x = (int)(lg_col0(pr.vis0, pr.b) + (long long)pr.kb * kKeysP2);
       const int y = (pr.l * p.h_kv + pr.kvh) * kRC;
@@ -901,6 +903,7 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
     const int l = u / p.B;
     const int klim = min(kTK, n_v - tile * kTK);
     auto issue_k = [&](int kvh) {
+      fence_proxy_async_smem();  // the buffer's previous contents were read by ldmatrix
       mbar_arrive_expect_tx(&c->kfull, (uint32_t)Gm::kKBytes);
 #pragma unroll
       for (int sl = 0; sl < Gm::kNH; ++sl) {
@@ -911,6 +914,7 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
       const int kvh = step / n_rc, rc = step % n_rc;
       const int slot = (int)(pos % kNQ);
       const uint32_t qdst = sbase + (uint32_t)(Gm::kKBytes + slot * Gm::kQ2);
+      fence_proxy_async_smem();  // the slot's previous contents were read by ldmatrix and loads
       mbar_arrive_expect_tx(&c->qfull[slot], (uint32_t)(Gm::kQBytes + kRC * 4));
 #pragma unroll
       for (int sl = 0; sl < Gm::kNH; ++sl) {
