@@ -320,8 +320,10 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
 }
 
 // Eight warps; warp w owns keys 32w .. 32w+31 of a stage (four 8-key mma N
-// tiles).  Thread (g4 = lane/4, c4 = lane%4) holds, for query rows g4 and g4+8
-// of each 16-row M tile, keys 32w + 8nt + 2c4 + {0, 1}, nt = 0..3.
+// tiles).  The key rows are fed to the B fragments permuted, so that thread
+// (g4 = lane/4, c4 = lane%4) holds, for query rows g4 and g4+8 of each 16-row M
+// tile, the four contiguous keys 32w + 16j + 4c4 + {0..3} in N tiles 2j and
+// 2j+1 (j = 0, 1): its logits of a row leave as two 16-byte stores.
 template <int D>
 __device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
   using Gm = SGeo<D>;
@@ -333,7 +335,9 @@ __device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
   const int g4 = lane >> 2, c4 = lane & 3;
   const uint32_t sbase = smem_u32(sm);
   // ldmatrix lane roles: key rows as the B operand, query rows as the A operand
-  const int kr = 32 * warp + (lane & 7) + 8 * (lane >> 4);
+  // row j of N tile t (lanes 8m..8m+7 address matrix m: t = m >> 1, k half m & 1)
+  // is key 4(j >> 1) + (j & 1) + 2t of the 16-key group
+  const int kr = 32 * warp + 4 * ((lane & 7) >> 1) + (lane & 1) + 2 * (lane >> 4);
   const int kc = (lane >> 3) & 1;
   const int qr = lane & 15, qc = lane >> 4;
   const float scale = p.scale_log2;
@@ -407,7 +411,7 @@ __device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
       float* lbase = nullptr;
       if (h.store) {
         lbase = w.lg + ((size_t)h.l * p.h_kv + h.kvh) * kRC * LS + lg_col0(h.vis0, h.b) + h.key0 +
-                32 * warp + 2 * c4;
+                32 * warp + 4 * c4;
       }
       const bool full = h.klim >= Gm::kSK;
 #pragma unroll
@@ -421,25 +425,33 @@ __device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
               float mx = -INFINITY;
               float* dst = lbase ? lbase + (size_t)row * LS : nullptr;
 #pragma unroll
-              for (int nt = 0; nt < 4; ++nt) {
-                const int key = 32 * warp + 8 * nt + 2 * c4;
-                const float x0 = acc[mt][nt][2 * hh], x1 = acc[mt][nt][2 * hh + 1];
+              for (int j = 0; j < 2; ++j) {
+                // keys 32w + 16j + 4c4 + {0..3}: N tiles 2j, 2j+1
+                const int key = 32 * warp + 16 * j + 4 * c4;
+                const float4 x = make_float4(acc[mt][2 * j][2 * hh], acc[mt][2 * j][2 * hh + 1],
+                                             acc[mt][2 * j + 1][2 * hh], acc[mt][2 * j + 1][2 * hh + 1]);
                 if (full) {
-                  v[2 * nt] = x0;
-                  v[2 * nt + 1] = x1;
-                  if (dst) *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(x0, x1);
+                  v[4 * j] = x.x;
+                  v[4 * j + 1] = x.y;
+                  v[4 * j + 2] = x.z;
+                  v[4 * j + 3] = x.w;
+                  if (dst) *reinterpret_cast<float4*>(dst + 16 * j) = x;
                 } else {
-                  v[2 * nt] = key < h.klim ? x0 : -INFINITY;
-                  v[2 * nt + 1] = key + 1 < h.klim ? x1 : -INFINITY;
+                  v[4 * j] = key < h.klim ? x.x : -INFINITY;
+                  v[4 * j + 1] = key + 1 < h.klim ? x.y : -INFINITY;
+                  v[4 * j + 2] = key + 2 < h.klim ? x.z : -INFINITY;
+                  v[4 * j + 3] = key + 3 < h.klim ? x.w : -INFINITY;
                   if (dst) {
-                    if (key + 1 < h.klim) {
-                      *reinterpret_cast<float2*>(dst + 8 * nt) = make_float2(x0, x1);
-                    } else if (key < h.klim) {
-                      dst[8 * nt] = x0;
+                    if (key + 3 < h.klim) {
+                      *reinterpret_cast<float4*>(dst + 16 * j) = x;
+                    } else {
+                      if (key < h.klim) dst[16 * j] = x.x;
+                      if (key + 1 < h.klim) dst[16 * j + 1] = x.y;
+                      if (key + 2 < h.klim) dst[16 * j + 2] = x.z;
                     }
                   }
                 }
-                mx = fmaxf(mx, fmaxf(v[2 * nt], v[2 * nt + 1]));
+                mx = fmaxf(mx, fmaxf(fmaxf(v[4 * j], v[4 * j + 1]), fmaxf(v[4 * j + 2], v[4 * j + 3])));
               }
               // running (max, sum of exp2) of the scaled logits: rescale only when the maximum grows
               if (mx != -INFINITY) {
