@@ -123,14 +123,6 @@ Dev make_dev(const aircache_problem* p) {
   d.chn = (tv + kStreamTiles - 1) / kStreamTiles + 1;
   d.stream_ok = 0;  // set per call from stream_eligible()
   d.mom_slots = (d.max_visual + 127) / 128;
-  {
-    // the elite kernel prefetches the visual keys of the first layers into L2
-    // (about half of it) while the key stream waits for the elite rows
-    const double layer_bytes =
-        (double)d.total_visual * (double)d.kv_stride_tok * (d.dtype == AIRCACHE_BF16 ? 2.0 : 4.0);
-    const double budget = 56.0 * 1024 * 1024;
-    d.prefetch_layers = layer_bytes > 0 ? (int)std::min<double>(d.L, std::floor(budget / layer_bytes)) : 0;
-  }
   return d;
 }
 

@@ -88,20 +88,6 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
   }
   const int n_t = R.n_t;
   const int hc = a.kv_chunk * p.g;  // heads per chunk
-  if (p.stream_ok && l < p.prefetch_layers && rank == 0 && tid < 32) {
-    // the key stream of the scoring pass waits for this kernel: start bringing the
-    // unit's visual keys (rows of kv_stride_tok elements) into L2 meanwhile
-    const int esz = (int)sizeof(T);
-    const long long row = p.kv_stride_tok * esz;
-    if (row % 16 == 0 && (reinterpret_cast<uintptr_t>(a.lp.k[l]) & 15) == 0) {
-      const char* k0 = reinterpret_cast<const char*>(a.lp.k[l]) + R.seq0 * row;
-      const long long bytes = (long long)R.n_v * row;
-      constexpr long long kPiece = 1LL << 20;
-      for (long long o = (long long)tid * kPiece; o < bytes; o += 32 * kPiece) {
-        prefetch_l2(k0 + o, (uint32_t)min(kPiece, bytes - o));
-      }
-    }
-  }
   const int kvb = min(p.h_kv, rank * a.kv_per_cta), kve = min(p.h_kv, kvb + a.kv_per_cta);
 
   extern __shared__ __align__(128) unsigned char smem[];

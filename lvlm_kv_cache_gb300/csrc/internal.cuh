@@ -27,7 +27,6 @@ struct Dev {
   float scale_log2;      // log2(e) / sqrt(D): logits are kept in base 2
   int stream_ok;         // 1: every unit takes the streaming scoring path (stream.cu)
   int mom_slots;         // ceil(max_visual / 128): moment records per unit
-  int prefetch_layers;   // streaming path: layers whose visual keys the elite kernel prefetches into L2
   int chn;               // streaming pass-1 chunks per (unit, KV head): visual chunks + 1 text chunk
 };
 

@@ -76,12 +76,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
-// Hint: bring `bytes` (a multiple of 16, 16-byte aligned) of global memory into
-// L2 without waiting for it.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // ---------------------------------------------------------------- sync
 
 // Named barrier over `nthreads` threads (a multiple of 32).  The non-aligned
