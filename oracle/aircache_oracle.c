@@ -33,6 +33,17 @@
  *   R8  top-k by I_v, ties to the lower index, output in ascending order.
  *   R9  the elite threshold is inclusive (>=).
  *   R10 every text token is kept in every layer, after the kept visual rows.
+ *   R14 the ablation windows of the same page (section "Ablation studies",
+ *       observation-window table): a continuous window of w = 16 or 32 is the
+ *       last w text tokens, "all text tokens" is every text token; either set
+ *       takes the elite set's place (its queries score, its keys join the
+ *       softmax).  The visual window needs visual-token queries and is not
+ *       restated.
+ *   R15 the ablation budgets (same section, layer-budget table): uniform
+ *       r_l = r; PyramidKV-style, linear in depth from (2 - 1/beta) r at layer
+ *       0 to r / beta at the last layer (mean r; beta = 20, PyramidKV's
+ *       default, the page gives none); strength only r_l = s'_t r; skewness
+ *       only r_l = s'_k r; keep_l as in R7.
  *
  * Element access: tensors are token-major [tokens][heads][D] with explicit
  * element strides for the token and head axes and D contiguous; the element
@@ -239,6 +250,68 @@ int oracle_budget(const double* s_t, const double* s_k, int n_layers, int n_v, d
     return 0;
 }
 
+/* ----------------------------------------------------- ablation variants */
+
+/*
+ * "Ablation studies", observation-window table (R14): the window that replaces
+ * the elite set.  mode 1: last 16 text tokens; 2: last 32; 3: every text token.
+ * positions : [n_t] receives the window (text-relative, ascending).
+ * returns its size, or -1 for an unknown mode or n_t < 1.
+ */
+int oracle_window(int n_t, int mode, int32_t* positions) {
+    if (n_t < 1) return -1;
+    int w;
+    if (mode == 1) w = 16;
+    else if (mode == 2) w = 32;
+    else if (mode == 3) w = n_t;
+    else return -1;
+    if (w > n_t) w = n_t;
+    for (int e = 0; e < w; ++e) positions[e] = n_t - w + e;
+    return w;
+}
+
+/*
+ * "Ablation studies", layer-budget table (R15): budget mode 0 is the method's
+ * own (oracle_budget); 1 uniform; 2 PyramidKV-style (beta = 20); 3 strength
+ * only; 4 skewness only.  Arguments as oracle_budget.
+ */
+int oracle_budget_variant(const double* s_t, const double* s_k, int n_layers, int n_v, double r,
+                          int mode, double* r_l, int32_t* keep) {
+    if (n_layers <= 0 || n_v <= 0 || mode < 0 || mode > 4) return -1;
+    if (mode == 0) return oracle_budget(s_t, s_k, n_layers, n_v, r, r_l, keep);
+    const double beta = 20.0;
+    double mean_st = 0.0, min_sk = INFINITY;
+    for (int l = 0; l < n_layers; ++l) {
+        mean_st += s_t[l];
+        if (s_k[l] < min_sk) min_sk = s_k[l];
+    }
+    mean_st /= n_layers;
+    double mean_u = 0.0;
+    for (int l = 0; l < n_layers; ++l) mean_u += s_k[l] - min_sk + 1e-6;
+    mean_u /= n_layers;
+    const double r_top = r / beta;
+    const double r_bottom = 2.0 * r - r_top;
+    for (int l = 0; l < n_layers; ++l) {
+        double rl;
+        if (mode == 1) {
+            rl = r;
+        } else if (mode == 2) {
+            const double t = n_layers > 1 ? (double)l / (double)(n_layers - 1) : 0.5;
+            rl = r_bottom + (r_top - r_bottom) * t;
+        } else if (mode == 3) {
+            rl = ((mean_st != 0.0) ? s_t[l] / mean_st : 1.0) * r;
+        } else {
+            rl = ((s_k[l] - min_sk + 1e-6) / mean_u) * r;
+        }
+        double kf = floor(rl * (double)n_v + 0.5);
+        if (kf < 1.0) kf = 1.0;
+        if (kf > (double)n_v) kf = (double)n_v;
+        keep[l] = (int32_t)kf;
+        if (r_l) r_l[l] = rl;
+    }
+    return 0;
+}
+
 /* ---------------------------------------------------------- selection */
 
 /* Sort key for the selection: larger I_v first, then lower index (R8). */
@@ -312,17 +385,18 @@ int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t
  * iv         : [n_layers * n_v] output; elite: [n_layers * n_t]; n_tk: [n_layers];
  * stats      : [n_layers * 4]; keep: [n_layers]; idx: [n_layers * n_v].
  */
-int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int h_q, int h_kv,
-                   int d, int n_v, int n_t, double alpha, double r,
-                   double* iv, int32_t* elite, int32_t* n_tk, double* stats,
-                   int32_t* keep, int32_t* idx) {
+int oracle_request_variant(const oracle_view* q, const oracle_view* k, int n_layers, int h_q,
+                           int h_kv, int d, int n_v, int n_t, double alpha, double r, int window_mode,
+                           int budget_mode, double* iv, int32_t* elite, int32_t* n_tk, double* stats,
+                           int32_t* keep, int32_t* idx) {
     double* s_t = (double*)malloc(sizeof(double) * (size_t)n_layers);
     double* s_k = (double*)malloc(sizeof(double) * (size_t)n_layers);
     if (!s_t || !s_k) { free(s_t); free(s_k); return -1; }
     int rc = 0;
     for (int l = 0; l < n_layers && rc == 0; ++l) {
         int32_t* el = elite + (int64_t)l * n_t;
-        const int ntk = oracle_elite(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, alpha, NULL, el);
+        const int ntk = window_mode == 0 ? oracle_elite(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, alpha, NULL, el)
+                                         : oracle_window(n_t, window_mode, el);
         if (ntk <= 0) { rc = -1; break; }
         n_tk[l] = ntk;
         double* ivl = iv + (int64_t)l * n_v;
@@ -330,11 +404,20 @@ int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int
         if (rc == 0) rc = oracle_stats(ivl, n_v, stats + (int64_t)l * 4);
         if (rc == 0) { s_t[l] = stats[l * 4 + 0]; s_k[l] = stats[l * 4 + 1]; }
     }
-    if (rc == 0) rc = oracle_budget(s_t, s_k, n_layers, n_v, r, NULL, keep);
+    if (rc == 0) rc = oracle_budget_variant(s_t, s_k, n_layers, n_v, r, budget_mode, NULL, keep);
     for (int l = 0; l < n_layers && rc == 0; ++l) {
         rc = oracle_select(iv + (int64_t)l * n_v, n_v, keep[l], idx + (int64_t)l * n_v);
     }
     free(s_t);
     free(s_k);
     return rc;
+}
+
+/* The method itself: the elite window and the strength + skewness budget. */
+int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int h_q, int h_kv,
+                   int d, int n_v, int n_t, double alpha, double r,
+                   double* iv, int32_t* elite, int32_t* n_tk, double* stats,
+                   int32_t* keep, int32_t* idx) {
+    return oracle_request_variant(q, k, n_layers, h_q, h_kv, d, n_v, n_t, alpha, r, 0, 0, iv, elite,
+                                  n_tk, stats, keep, idx);
 }

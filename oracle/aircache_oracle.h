@@ -33,6 +33,13 @@ int oracle_budget(const double* s_t, const double* s_k, int n_layers, int n_v, d
 int oracle_select(const double* iv, int n_v, int keep, int32_t* idx);
 int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t,
                        const int32_t* idx, int keep, void* dst);
+int oracle_window(int n_t, int mode, int32_t* positions);
+int oracle_budget_variant(const double* s_t, const double* s_k, int n_layers, int n_v, double r,
+                          int mode, double* r_l, int32_t* keep);
+int oracle_request_variant(const oracle_view* q, const oracle_view* k, int n_layers, int h_q,
+                           int h_kv, int d, int n_v, int n_t, double alpha, double r, int window_mode,
+                           int budget_mode, double* iv, int32_t* elite, int32_t* n_tk, double* stats,
+                           int32_t* keep, int32_t* idx);
 int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int h_q, int h_kv,
                    int d, int n_v, int n_t, double alpha, double r,
                    double* iv, int32_t* elite, int32_t* n_tk, double* stats,

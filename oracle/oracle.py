@@ -76,6 +76,13 @@ def lib():
         L.oracle_request.argtypes = [V, V, i32, i32, i32, i32, i32, i32, f64, f64,
                                      vp, vp, vp, vp, vp, vp]
         L.oracle_request.restype = i32
+        L.oracle_window.argtypes = [i32, i32, vp]
+        L.oracle_window.restype = i32
+        L.oracle_budget_variant.argtypes = [vp, vp, i32, i32, f64, i32, vp, vp]
+        L.oracle_budget_variant.restype = i32
+        L.oracle_request_variant.argtypes = [V, V, i32, i32, i32, i32, i32, i32, f64, f64, i32, i32,
+                                             vp, vp, vp, vp, vp, vp]
+        L.oracle_request_variant.restype = i32
         _lib = L
     return _lib
 
@@ -150,6 +157,30 @@ def budget(s_t, s_k, n_v: int, r: float):
     return rl, keep
 
 
+def window(n_t: int, mode: int) -> np.ndarray:
+    """Observation window of an ablation variant (1: last 16 text tokens,
+    2: last 32, 3: every text token), text-relative, ascending."""
+    pos = np.zeros(max(int(n_t), 1), np.int32)
+    n = lib().oracle_window(int(n_t), int(mode), _ptr(pos))
+    if n < 0:
+        raise ValueError("oracle_window rejected its arguments")
+    return pos[:n].copy()
+
+
+def budget_variant(s_t, s_k, n_v: int, r: float, mode: int):
+    """Per-layer (r_l, keep) under a budget variant (0: the method's own,
+    1: uniform, 2: PyramidKV-style, 3: strength only, 4: skewness only)."""
+    st = np.ascontiguousarray(s_t, dtype=np.float64)
+    sk = np.ascontiguousarray(s_k, dtype=np.float64)
+    L = len(st)
+    rl = np.zeros(L, np.float64)
+    keep = np.zeros(L, np.int32)
+    if lib().oracle_budget_variant(_ptr(st), _ptr(sk), L, n_v, float(r), int(mode), _ptr(rl),
+                                   _ptr(keep)) != 0:
+        raise ValueError("oracle_budget_variant rejected its arguments")
+    return rl, keep
+
+
 def select(iv: np.ndarray, keep: int) -> np.ndarray:
     """Ascending positions of the `keep` largest I_v (ties to the lower index)."""
     v = np.ascontiguousarray(iv, dtype=np.float64)
@@ -171,8 +202,10 @@ def compact(src: np.ndarray, n_v: int, n_t: int, idx: np.ndarray) -> np.ndarray:
     return out
 
 
-def request(q_layers, k_layers, n_v: int, alpha: float, r: float):
-    """The whole one-shot pass for one request over its layers.
+def request(q_layers, k_layers, n_v: int, alpha: float, r: float, window_mode: int = 0,
+            budget_mode: int = 0):
+    """The whole one-shot pass for one request over its layers (optionally
+    with an ablation window / budget variant).
 
     q_layers[l]: [N_t, H_q, D]; k_layers[l]: [N_v+N_t, H_kv, D].
     Returns a dict with per-layer iv, elite, n_tk, stats, keep, idx."""
@@ -187,8 +220,9 @@ def request(q_layers, k_layers, n_v: int, alpha: float, r: float):
     st = np.zeros((L, 4), np.float64)
     keep = np.zeros(L, np.int32)
     idx = np.zeros((L, n_v), np.int32)
-    rc = lib().oracle_request(qv, kv, L, h_q, h_kv, d, n_v, n_t, float(alpha), float(r),
-                              _ptr(iv), _ptr(el), _ptr(ntk), _ptr(st), _ptr(keep), _ptr(idx))
+    rc = lib().oracle_request_variant(qv, kv, L, h_q, h_kv, d, n_v, n_t, float(alpha), float(r),
+                                      int(window_mode), int(budget_mode), _ptr(iv), _ptr(el),
+                                      _ptr(ntk), _ptr(st), _ptr(keep), _ptr(idx))
     if rc != 0:
         raise ValueError("oracle_request rejected its arguments")
     return {
