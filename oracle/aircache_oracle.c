@@ -219,15 +219,11 @@ int oracle_stats(const double* iv, int n_v, double* out) {
 /* ------------------------------------------------------- layer budget */
 
 /*
- * "Key design 2", budget r_hat = 1/2 (s'_t + s'_k) r with the cross-layer
- * normalisation of R6, over the n_layers layers of one request, then the keep
- * count of R7.
- * s_t, s_k : [n_layers]; r_l : [n_layers] output (may be NULL);
- * keep : [n_layers] output.
+ * R6: s'_t[l] = s_t[l] / mean s_t (1 if the mean is 0) and
+ * s'_k[l] = (s_k[l] - min s_k + 1e-6) / mean(s_k - min s_k + 1e-6).
  */
-int oracle_budget(const double* s_t, const double* s_k, int n_layers, int n_v, double r,
-                  double* r_l, int32_t* keep) {
-    if (n_layers <= 0 || n_v <= 0) return -1;
+static void normalised_layers(const double* s_t, const double* s_k, int n_layers, double* st_n,
+                              double* sk_n) {
     double mean_st = 0.0, min_sk = INFINITY;
     for (int l = 0; l < n_layers; ++l) {
         mean_st += s_t[l];
@@ -238,15 +234,40 @@ int oracle_budget(const double* s_t, const double* s_k, int n_layers, int n_v, d
     for (int l = 0; l < n_layers; ++l) mean_u += s_k[l] - min_sk + 1e-6;
     mean_u /= n_layers;
     for (int l = 0; l < n_layers; ++l) {
-        const double st_n = (mean_st != 0.0) ? s_t[l] / mean_st : 1.0;
-        const double sk_n = (s_k[l] - min_sk + 1e-6) / mean_u;
-        const double rl = 0.5 * (st_n + sk_n) * r;
-        double kf = floor(rl * (double)n_v + 0.5);
-        if (kf < 1.0) kf = 1.0;
-        if (kf > (double)n_v) kf = (double)n_v;
-        keep[l] = (int32_t)kf;
+        st_n[l] = (mean_st != 0.0) ? s_t[l] / mean_st : 1.0;
+        sk_n[l] = (s_k[l] - min_sk + 1e-6) / mean_u;
+    }
+}
+
+/* R7: keep = clamp(floor(r_l N_v + 1/2), 1, N_v). */
+static int32_t keep_of(double rl, int n_v) {
+    double kf = floor(rl * (double)n_v + 0.5);
+    if (kf < 1.0) kf = 1.0;
+    if (kf > (double)n_v) kf = (double)n_v;
+    return (int32_t)kf;
+}
+
+/*
+ * "Key design 2", budget r_hat = 1/2 (s'_t + s'_k) r with the cross-layer
+ * normalisation of R6, over the n_layers layers of one request, then the keep
+ * count of R7.
+ * s_t, s_k : [n_layers]; r_l : [n_layers] output (may be NULL);
+ * keep : [n_layers] output.
+ */
+int oracle_budget(const double* s_t, const double* s_k, int n_layers, int n_v, double r,
+                  double* r_l, int32_t* keep) {
+    if (n_layers <= 0 || n_v <= 0) return -1;
+    double* st_n = (double*)malloc(sizeof(double) * (size_t)n_layers);
+    double* sk_n = (double*)malloc(sizeof(double) * (size_t)n_layers);
+    if (!st_n || !sk_n) { free(st_n); free(sk_n); return -1; }
+    normalised_layers(s_t, s_k, n_layers, st_n, sk_n);
+    for (int l = 0; l < n_layers; ++l) {
+        const double rl = 0.5 * (st_n[l] + sk_n[l]) * r;
+        keep[l] = keep_of(rl, n_v);
         if (r_l) r_l[l] = rl;
     }
+    free(st_n);
+    free(sk_n);
     return 0;
 }
 
@@ -279,16 +300,11 @@ int oracle_budget_variant(const double* s_t, const double* s_k, int n_layers, in
                           int mode, double* r_l, int32_t* keep) {
     if (n_layers <= 0 || n_v <= 0 || mode < 0 || mode > 4) return -1;
     if (mode == 0) return oracle_budget(s_t, s_k, n_layers, n_v, r, r_l, keep);
+    double* st_n = (double*)malloc(sizeof(double) * (size_t)n_layers);
+    double* sk_n = (double*)malloc(sizeof(double) * (size_t)n_layers);
+    if (!st_n || !sk_n) { free(st_n); free(sk_n); return -1; }
+    normalised_layers(s_t, s_k, n_layers, st_n, sk_n);
     const double beta = 20.0;
-    double mean_st = 0.0, min_sk = INFINITY;
-    for (int l = 0; l < n_layers; ++l) {
-        mean_st += s_t[l];
-        if (s_k[l] < min_sk) min_sk = s_k[l];
-    }
-    mean_st /= n_layers;
-    double mean_u = 0.0;
-    for (int l = 0; l < n_layers; ++l) mean_u += s_k[l] - min_sk + 1e-6;
-    mean_u /= n_layers;
     const double r_top = r / beta;
     const double r_bottom = 2.0 * r - r_top;
     for (int l = 0; l < n_layers; ++l) {
@@ -299,16 +315,15 @@ int oracle_budget_variant(const double* s_t, const double* s_k, int n_layers, in
             const double t = n_layers > 1 ? (double)l / (double)(n_layers - 1) : 0.5;
             rl = r_bottom + (r_top - r_bottom) * t;
         } else if (mode == 3) {
-            rl = ((mean_st != 0.0) ? s_t[l] / mean_st : 1.0) * r;
+            rl = st_n[l] * r;
         } else {
-            rl = ((s_k[l] - min_sk + 1e-6) / mean_u) * r;
+            rl = sk_n[l] * r;
         }
-        double kf = floor(rl * (double)n_v + 0.5);
-        if (kf < 1.0) kf = 1.0;
-        if (kf > (double)n_v) kf = (double)n_v;
-        keep[l] = (int32_t)kf;
+        keep[l] = keep_of(rl, n_v);
         if (r_l) r_l[l] = rl;
     }
+    free(st_n);
+    free(sk_n);
     return 0;
 }
 

@@ -30,7 +30,7 @@ MUTATIONS = {
                                    "s_k = cube;"),
     "budget skips the min shift": ("mean_u += s_k[l] - min_sk + 1e-6;", "mean_u += s_k[l] + 1e-6;"),
     "budget uses banker's rounding": ("floor(rl * (double)n_v + 0.5)", "nearbyint(rl * (double)n_v)"),
-    "budget drops the 1/2": ("const double rl = 0.5 * (st_n + sk_n) * r;", "const double rl = (st_n + sk_n) * r;"),
+    "budget drops the 1/2": ("const double rl = 0.5 * (st_n[l] + sk_n[l]) * r;", "const double rl = (st_n[l] + sk_n[l]) * r;"),
     "ties go to the higher index": ("return (x->i > y->i) - (x->i < y->i);", "return (x->i < y->i) - (x->i > y->i);"),
     "selection left in score order": ("    qsort(idx, (size_t)keep, sizeof(int32_t), ascending_int);\n", ""),
     "text rows shifted by one": ("(int64_t)n_v + (j - keep);", "(int64_t)n_v + (j - keep) - (j > keep);"),
