@@ -92,7 +92,14 @@ typedef struct aircache_problem {
     int32_t max_visual;    /* >= every N_v[b]; every N_v[b] must be >= 3 (skewness) */
     int32_t max_text;      /* >= every N_t[b], 1..AIRCACHE_MAX_TEXT; every N_t[b] >= 1 */
     int32_t max_elite;     /* cap on N_tk that the workspace is sized for; 0 means max_text */
-    int32_t reserved0;     /* must be 0 */
+    int32_t variant;       /* 0: the method.  Ablation variants (AirCache notes, "Ablation
+                            * studies"): bits 0-7 the observation window -- 0 the elite
+                            * window, 1 the last 16 text tokens, 2 the last 32, 3 every
+                            * text token (a fixed window takes the elite set's place);
+                            * bits 8-15 the layer budget -- 0 strength + skewness, 1
+                            * uniform (r_l = r), 2 PyramidKV-style (linear in depth from
+                            * (2 - 1/20) r to r/20), 3 strength only (s'_t r), 4
+                            * skewness only (s'_k r); other bits 0. */
     int64_t total_tokens;  /* == cu_seqlens[B] */
     int64_t total_visual;  /* == cu_visual[B] */
     const int32_t* cu_seqlens;  /* device [B+1], non-decreasing, cu_seqlens[0] == 0 */

@@ -50,7 +50,7 @@ class ProblemStruct(ctypes.Structure):
         ("max_visual", ctypes.c_int32),
         ("max_text", ctypes.c_int32),
         ("max_elite", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("variant", ctypes.c_int32),
         ("total_tokens", ctypes.c_int64),
         ("total_visual", ctypes.c_int64),
         ("cu_seqlens", ctypes.c_void_p),
@@ -143,7 +143,7 @@ class Problem:
     """
 
     def __init__(self, q, k, v, cu_seqlens, cu_visual, max_visual, max_text, alpha=0.9, r=0.1,
-                 max_elite=0, total_tokens=None, total_visual=None):
+                 max_elite=0, total_tokens=None, total_visual=None, window_mode=0, budget_mode=0):
         qs = list(q.unbind(0)) if torch.is_tensor(q) else list(q)
         ks = list(k.unbind(0)) if torch.is_tensor(k) else list(k)
         vs = list(v.unbind(0)) if torch.is_tensor(v) else list(v)
@@ -171,7 +171,8 @@ class Problem:
         self.c = ProblemStruct(
             num_layers=L, num_requests=B, h_q=self.h_q, h_kv=self.h_kv, head_dim=self.d,
             dtype=BF16 if dt == torch.bfloat16 else F32,
-            max_visual=int(max_visual), max_text=int(max_text), max_elite=int(max_elite), reserved0=0,
+            max_visual=int(max_visual), max_text=int(max_text), max_elite=int(max_elite),
+            variant=int(window_mode) | (int(budget_mode) << 8),
             total_tokens=T, total_visual=TV,
             cu_seqlens=cu_seqlens.data_ptr(), cu_visual=cu_visual.data_ptr(),
             q_text=ctypes.cast(self._q, ctypes.POINTER(ctypes.c_void_p)),

@@ -62,7 +62,9 @@ int validate(const aircache_problem* p) {
   if (p->max_visual < 3 || p->max_text < 1) return AIRCACHE_ERR_INVALID_ARG;
   if (p->max_text > AIRCACHE_MAX_TEXT) return AIRCACHE_ERR_UNSUPPORTED;
   if (p->max_elite < 0 || p->max_elite > p->max_text) return AIRCACHE_ERR_INVALID_ARG;
-  if (p->reserved0 != 0) return AIRCACHE_ERR_INVALID_ARG;
+  if ((p->variant & ~0xffff) != 0 || (p->variant & 0xff) > 3 || ((p->variant >> 8) & 0xff) > 4) {
+    return AIRCACHE_ERR_INVALID_ARG;
+  }
   const int64_t B = p->num_requests;
   const int64_t total_text = p->total_tokens - p->total_visual;
   if (p->total_visual < 3 * B || total_text < B) return AIRCACHE_ERR_INVALID_ARG;
@@ -118,6 +120,8 @@ Dev make_dev(const aircache_problem* p) {
   d.kv_stride_head = p->kv_stride_head;
   d.alpha = p->alpha;
   d.r = p->r;
+  d.window_mode = p->variant & 0xff;
+  d.budget_mode = (p->variant >> 8) & 0xff;
   d.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->head_dim));
   const int tv = (d.max_visual + 127) / 128;
   d.chn = (tv + kStreamTiles - 1) / kStreamTiles + 1;

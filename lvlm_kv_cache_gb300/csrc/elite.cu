@@ -103,119 +103,132 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
 
   const char* kbase = reinterpret_cast<const char*>(a.lp.k[l]);
   const char* qbase = reinterpret_cast<const char*>(a.lp.q[l]);
-  for (int j = tid; j < n_t; j += kEliteThreads) P[j] = 0.f;
-
-  const int n_kt = (n_t + kTK - 1) / kTK;
-  const int n_rc = (p.g + kRC - 1) / kRC;
-  for (int kv0 = kvb; kv0 < kve; kv0 += a.kv_chunk) {
-    const int kv1 = min(kve, kv0 + a.kv_chunk);
-    const int items = (kv1 - kv0) * n_rc * n_kt;
-    __syncthreads();
-#pragma unroll
-    for (int i = 0; i < NS - 1; ++i) {
-      if (i < items) load_item<T, D>(p, R, kbase, qbase, kv0, n_rc, n_kt, i, stages + i * G::kStageBytes);
-      cp_async_commit();
-    }
-    for (int i = 0; i < items; ++i) {
-      const int pre = i + NS - 1;
-      if (pre < items) load_item<T, D>(p, R, kbase, qbase, kv0, n_rc, n_kt, pre, stages + (pre % NS) * G::kStageBytes);
-      cp_async_commit();
-      cp_async_wait<NS - 1>();
-      __syncthreads();
-      const int per_kv = n_rc * n_kt;
-      const int kvh = kv0 + i / per_kv, rc = (i % per_kv) / n_kt, t = i % n_kt;
-      const int rows = min(kRC, p.g - rc * kRC);
-      const unsigned char* st = stages + (i % NS) * G::kStageBytes;
-      float acc[4][4];
-      TileLogits<T, D>::run(reinterpret_cast<const T*>(st), reinterpret_cast<const T*>(st + G::kKBytes), rows,
-                            p.scale_log2, warp, lane, acc);
-      const int kA = t * kTK + warp * 16 + g4;
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int row = 8 * j + 2 * c4 + e;
-          if (row < rows) {
-            const int hrow = (kvh - kv0) * p.g + rc * kRC + row;  // head within the chunk
-            float* lr = lg + (size_t)hrow * p.max_text;
-            if (kA < n_t) lr[kA] = acc[j][e];
-            if (kA + 8 < n_t) lr[kA + 8] = acc[j][2 + e];
-          }
-        }
-      __syncthreads();
-    }
-    cp_async_wait<0>();
-    // per-head softmax statistics
-    const int hcur = (kv1 - kv0) * p.g;
-    for (int hh = warp; hh < hcur; hh += kEliteWarps) {
-      const float* row = lg + (size_t)hh * p.max_text;
-      float m = -INFINITY;
-      for (int j = lane; j < n_t; j += 32) m = fmaxf(m, row[j]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float s = 0.f;
-      for (int j = lane; j < n_t; j += 32) s += exp2f(row[j] - m);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) {
-        hmax[hh] = m;
-        hinv[hh] = 1.f / s;
+  int base = 0;
+  int32_t* out = a.w.elite + (size_t)u * p.max_text;
+  if (p.window_mode != 0) {
+    // an ablation window takes the elite set's place: the last 16 / 32 text
+    // tokens or every one (the same in every CTA of the cluster)
+    const int wsz = p.window_mode == 1 ? 16 : (p.window_mode == 2 ? 32 : n_t);
+    base = min(wsz, n_t);
+    for (int e = tid; e < base; e += kEliteThreads) {
+      if (e < p.max_elite) {
+        pos_s[e] = n_t - base + e;
+        if (rank == 0) out[e] = n_t - base + e;
       }
     }
+  } else {
+    for (int j = tid; j < n_t; j += kEliteThreads) P[j] = 0.f;
+
+    const int n_kt = (n_t + kTK - 1) / kTK;
+    const int n_rc = (p.g + kRC - 1) / kRC;
+    for (int kv0 = kvb; kv0 < kve; kv0 += a.kv_chunk) {
+      const int kv1 = min(kve, kv0 + a.kv_chunk);
+      const int items = (kv1 - kv0) * n_rc * n_kt;
+      __syncthreads();
+  #pragma unroll
+      for (int i = 0; i < NS - 1; ++i) {
+        if (i < items) load_item<T, D>(p, R, kbase, qbase, kv0, n_rc, n_kt, i, stages + i * G::kStageBytes);
+        cp_async_commit();
+      }
+      for (int i = 0; i < items; ++i) {
+        const int pre = i + NS - 1;
+        if (pre < items) load_item<T, D>(p, R, kbase, qbase, kv0, n_rc, n_kt, pre, stages + (pre % NS) * G::kStageBytes);
+        cp_async_commit();
+        cp_async_wait<NS - 1>();
+        __syncthreads();
+        const int per_kv = n_rc * n_kt;
+        const int kvh = kv0 + i / per_kv, rc = (i % per_kv) / n_kt, t = i % n_kt;
+        const int rows = min(kRC, p.g - rc * kRC);
+        const unsigned char* st = stages + (i % NS) * G::kStageBytes;
+        float acc[4][4];
+        TileLogits<T, D>::run(reinterpret_cast<const T*>(st), reinterpret_cast<const T*>(st + G::kKBytes), rows,
+                              p.scale_log2, warp, lane, acc);
+        const int kA = t * kTK + warp * 16 + g4;
+  #pragma unroll
+        for (int j = 0; j < 4; ++j)
+  #pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int row = 8 * j + 2 * c4 + e;
+            if (row < rows) {
+              const int hrow = (kvh - kv0) * p.g + rc * kRC + row;  // head within the chunk
+              float* lr = lg + (size_t)hrow * p.max_text;
+              if (kA < n_t) lr[kA] = acc[j][e];
+              if (kA + 8 < n_t) lr[kA + 8] = acc[j][2 + e];
+            }
+          }
+        __syncthreads();
+      }
+      cp_async_wait<0>();
+      // per-head softmax statistics
+      const int hcur = (kv1 - kv0) * p.g;
+      for (int hh = warp; hh < hcur; hh += kEliteWarps) {
+        const float* row = lg + (size_t)hh * p.max_text;
+        float m = -INFINITY;
+        for (int j = lane; j < n_t; j += 32) m = fmaxf(m, row[j]);
+  #pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float s = 0.f;
+        for (int j = lane; j < n_t; j += 32) s += exp2f(row[j] - m);
+  #pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) {
+          hmax[hh] = m;
+          hinv[hh] = 1.f / s;
+        }
+      }
+      __syncthreads();
+      for (int j = tid; j < n_t; j += kEliteThreads) {
+        float accp = P[j];
+        for (int hh = 0; hh < hcur; ++hh) accp += exp2f(lg[(size_t)hh * p.max_text + j] - hmax[hh]) * hinv[hh];
+        P[j] = accp;
+      }
+    }
+    // P over every head: the CTAs' partials added in rank order (the same sum,
+    // bit for bit, in every CTA of the cluster)
     __syncthreads();
+    cluster_sync_all();  // every CTA's partial P is complete
     for (int j = tid; j < n_t; j += kEliteThreads) {
-      float accp = P[j];
-      for (int hh = 0; hh < hcur; ++hh) accp += exp2f(lg[(size_t)hh * p.max_text + j] - hmax[hh]) * hinv[hh];
-      P[j] = accp;
+      const uint32_t pj = smem_u32(P + j);
+      float s = 0.f;
+      for (int c = 0; c < C; ++c) s += ld_cluster_f32(cluster_map(pj, (uint32_t)c));
+      Pt[j] = s;
     }
-  }
-  // P over every head: the CTAs' partials added in rank order (the same sum,
-  // bit for bit, in every CTA of the cluster)
-  __syncthreads();
-  cluster_sync_all();  // every CTA's partial P is complete
-  for (int j = tid; j < n_t; j += kEliteThreads) {
-    const uint32_t pj = smem_u32(P + j);
-    float s = 0.f;
-    for (int c = 0; c < C; ++c) s += ld_cluster_f32(cluster_map(pj, (uint32_t)c));
-    Pt[j] = s;
-  }
-  cluster_sync_all();  // no CTA reads another's partial after this point
+    cluster_sync_all();  // no CTA reads another's partial after this point
 
-  // max P
-  float m = -INFINITY;
-  for (int j = tid; j < n_t; j += kEliteThreads) m = fmaxf(m, Pt[j]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  m = red[0];
-#pragma unroll
-  for (int i = 1; i < kEliteWarps; ++i) m = fmaxf(m, red[i]);
-  const float thr = (float)p.alpha * m;
+    // max P
+    float m = -INFINITY;
+    for (int j = tid; j < n_t; j += kEliteThreads) m = fmaxf(m, Pt[j]);
+  #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    m = red[0];
+  #pragma unroll
+    for (int i = 1; i < kEliteWarps; ++i) m = fmaxf(m, red[i]);
+    const float thr = (float)p.alpha * m;
 
-  // ordered compaction of {j : P[j] >= thr}
-  int32_t* out = a.w.elite + (size_t)u * p.max_text;
-  int base = 0;
-  for (int j0 = 0; j0 < n_t; j0 += kEliteThreads) {
-    const int j = j0 + tid;
-    const bool take = j < n_t && Pt[j] >= thr;
-    const unsigned bal = __ballot_sync(0xffffffffu, take);
-    const int before = __popc(bal & ((1u << lane) - 1u));
-    __syncthreads();
-    if (lane == 0) wcount[warp] = __popc(bal);
-    __syncthreads();
-    int wbase = 0, total = 0;
-#pragma unroll
-    for (int i = 0; i < kEliteWarps; ++i) {
-      wbase += (i < warp) ? wcount[i] : 0;
-      total += wcount[i];
+    // ordered compaction of {j : P[j] >= thr}
+    for (int j0 = 0; j0 < n_t; j0 += kEliteThreads) {
+      const int j = j0 + tid;
+      const bool take = j < n_t && Pt[j] >= thr;
+      const unsigned bal = __ballot_sync(0xffffffffu, take);
+      const int before = __popc(bal & ((1u << lane) - 1u));
+      __syncthreads();
+      if (lane == 0) wcount[warp] = __popc(bal);
+      __syncthreads();
+      int wbase = 0, total = 0;
+  #pragma unroll
+      for (int i = 0; i < kEliteWarps; ++i) {
+        wbase += (i < warp) ? wcount[i] : 0;
+        total += wcount[i];
+      }
+      const int pos = base + wbase + before;
+      if (take && pos < p.max_elite) {
+        pos_s[pos] = j;
+        if (rank == 0) out[pos] = j;
+      }
+      base += total;
     }
-    const int pos = base + wbase + before;
-    if (take && pos < p.max_elite) {
-      pos_s[pos] = j;
-      if (rank == 0) out[pos] = j;
-    }
-    base += total;
   }
   // Gather this CTA's elite query rows (row kvh*g*N_tk + hh*N_tk + e) and elite
   // text keys into dense buffers: the scoring kernel then addresses them by

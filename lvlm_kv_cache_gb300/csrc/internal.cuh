@@ -27,6 +27,8 @@ struct Dev {
   float scale_log2;      // log2(e) / sqrt(D): logits are kept in base 2
   int stream_ok;         // 1: every unit takes the streaming scoring path (stream.cu)
   int mom_slots;         // ceil(max_visual / 128): moment records per unit
+  int window_mode;       // 0 elite window; 1 / 2 / 3: last 16 / last 32 / every text token
+  int budget_mode;       // 0 strength + skewness; 1 uniform; 2 PyramidKV-style; 3 strength; 4 skewness
   int chn;               // streaming pass-1 chunks per (unit, KV head): visual chunks + 1 text chunk
 };
 

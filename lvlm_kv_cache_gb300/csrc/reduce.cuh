@@ -439,10 +439,30 @@ __device__ __forceinline__ void request_budget_warp(const Dev& p, int b, int n_v
     ff st, sk;
     get(l, st, sk);
     const ff u_l = ff_add(ff_add(sk, ff_neg(sk_min)), eps);
-    const ff st_n = (mean_st.hi != 0.f) ? ff_div(st, mean_st) : ff{1.f, 0.f};
-    const ff sk_n = ff_div(u_l, mean_u);
-    const ff rl = ff_mul(ff_mul(ff{0.5f, 0.f}, ff_add(st_n, sk_n)), r);
-    float kf = ff_floor(ff_add(ff_mul(rl, ff{(float)n_v, 0.f}), ff{0.5f, 0.f}));
+    float kf;
+    if (p.budget_mode == 1 || p.budget_mode == 2) {
+      // ablation budgets that do not look at the statistics (uniform; PyramidKV-
+      // style, linear in depth from (2 - 1/20) r to r/20): fp64, in the oracle's
+      // order of operations, so that structured values such as r N_v = x.5 round
+      // the same way
+      double rl = p.r;
+      if (p.budget_mode == 2) {
+        const double r_top = __ddiv_rn(p.r, 20.0);
+        const double r_bottom = __dsub_rn(__dmul_rn(2.0, p.r), r_top);
+        const double t = p.L > 1 ? __ddiv_rn((double)l, (double)(p.L - 1)) : 0.5;
+        rl = __dadd_rn(r_bottom, __dmul_rn(__dsub_rn(r_top, r_bottom), t));
+      }
+      kf = (float)floor(__dadd_rn(__dmul_rn(rl, (double)n_v), 0.5));
+    } else {
+      const ff st_n = (mean_st.hi != 0.f) ? ff_div(st, mean_st) : ff{1.f, 0.f};
+      const ff sk_n = ff_div(u_l, mean_u);
+      // the method: 1/2 (s'_t + s'_k) r; ablations: s'_t r (3), s'_k r (4)
+      const ff mix = p.budget_mode == 3 ? st_n
+                     : p.budget_mode == 4 ? sk_n
+                                          : ff_mul(ff{0.5f, 0.f}, ff_add(st_n, sk_n));
+      const ff rl = ff_mul(mix, r);
+      kf = ff_floor(ff_add(ff_mul(rl, ff{(float)n_v, 0.f}), ff{0.5f, 0.f}));
+    }
     kf = fminf(fmaxf(kf, 1.f), (float)n_v);
     keep[l * p.B + b] = (int32_t)kf;
   }

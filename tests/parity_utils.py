@@ -70,17 +70,21 @@ def near_half(x, band=1e-3):
     return abs(f - 0.5) < band
 
 
-def check_unit(oracle, wl, l, b, cu_s, cu_v, gpu, report):
-    """Full per-(layer, request) check of elite, I_v (stats/keep/select are
-    checked per request by check_request)."""
+def check_unit(oracle, wl, l, b, cu_s, cu_v, gpu, report, window_mode=0):
+    """Full per-(layer, request) check of elite (or the ablation window), I_v
+    (stats/keep/select are checked per request by check_request)."""
     spec = wl.spec
     n_v = cu_v[b + 1] - cu_v[b]
     q, k, _ = unit_views(wl, l, b, cu_s, cu_v)
     u = l * spec.B + b
     ntk = int(gpu["n_tk"][u])
     g_el = gpu["elite"][u, :ntk]
-    el, flips = check_elite(oracle, q, k, n_v, spec.alpha, g_el)
-    report["elite_flips"] = report.get("elite_flips", 0) + flips
+    if window_mode:
+        el = oracle.window(q.shape[0], window_mode)
+        assert np.array_equal(g_el, el), f"window differs at (l={l}, b={b})"
+    else:
+        el, flips = check_elite(oracle, q, k, n_v, spec.alpha, g_el)
+        report["elite_flips"] = report.get("elite_flips", 0) + flips
     iv_o, _ = oracle.score(q, k, n_v, el)
     iv_g = gpu["iv"][l, cu_v[b]:cu_v[b + 1]]
     check_iv(iv_o, iv_g, f"(l={l}, b={b})")
@@ -89,7 +93,7 @@ def check_unit(oracle, wl, l, b, cu_s, cu_v, gpu, report):
     return iv_o
 
 
-def check_request(oracle, wl, b, cu_s, cu_v, gpu, report, oracle_iv_by_layer=None):
+def check_request(oracle, wl, b, cu_s, cu_v, gpu, report, oracle_iv_by_layer=None, budget_mode=0):
     """Budget and selection of one request over all its layers, on the GPU's I_v."""
     spec = wl.spec
     n_v = cu_v[b + 1] - cu_v[b]
@@ -102,7 +106,7 @@ def check_request(oracle, wl, b, cu_s, cu_v, gpu, report, oracle_iv_by_layer=Non
         if gpu.get("stats") is not None:
             u = l * spec.B + b
             np.testing.assert_allclose(gpu["stats"][u], [s_t, s_k], rtol=1e-9, atol=1e-12)
-    rl, keep_o = oracle.budget(st, sk, n_v, spec.r)
+    rl, keep_o = oracle.budget_variant(st, sk, n_v, spec.r, budget_mode)
     keep_g = np.array([gpu["keep"][l * spec.B + b] for l in range(spec.L)])
     boundary = [l for l in range(spec.L) if near_half(rl[l] * n_v, 1e-9)]
     mism = [l for l in range(spec.L) if keep_g[l] != keep_o[l] and l not in boundary]
@@ -117,7 +121,7 @@ def check_request(oracle, wl, b, cu_s, cu_v, gpu, report, oracle_iv_by_layer=Non
                 oracle_iv_by_layer[l], sel_g, int(keep_g[l]))
     if oracle_iv_by_layer is not None and len(oracle_iv_by_layer) == spec.L:
         st_o, sk_o = zip(*[oracle.stats(oracle_iv_by_layer[l])[:2] for l in range(spec.L)])
-        rl_o, keep_oo = oracle.budget(st_o, sk_o, n_v, spec.r)
+        rl_o, keep_oo = oracle.budget_variant(st_o, sk_o, n_v, spec.r, budget_mode)
         for l in range(spec.L):
             if keep_oo[l] != keep_g[l]:
                 assert abs(int(keep_oo[l]) - int(keep_g[l])) <= 1 and near_half(rl_o[l] * n_v), \

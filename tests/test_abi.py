@@ -49,7 +49,7 @@ def fake_problem(A, **over):
     arr = (ctypes.c_void_p * L)(*[0x100000 + 0x10000 * i for i in range(L)])
     p = A.ProblemStruct(
         num_layers=L, num_requests=2, h_q=8, h_kv=2, head_dim=128, dtype=A.BF16,
-        max_visual=1000, max_text=64, max_elite=0, reserved0=0,
+        max_visual=1000, max_text=64, max_elite=0, variant=0,
         total_tokens=1000 + 900 + 64 + 50, total_visual=1900,
         cu_seqlens=0x200000, cu_visual=0x300000,
         q_text=ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)),
@@ -76,7 +76,7 @@ def test_sizes_of_a_valid_problem(A):
     ("num_layers", 0, -1), ("num_layers", 257, -1), ("num_requests", 0, -1),
     ("h_q", 7, -1), ("h_kv", 0, -1), ("head_dim", 96, -2), ("head_dim", 0, -1),
     ("dtype", 7, -2), ("max_visual", 2, -1), ("max_text", 0, -1), ("max_text", 9000, -2),
-    ("max_elite", 65, -1), ("max_elite", -1, -1), ("reserved0", 1, -1),
+    ("max_elite", 65, -1), ("max_elite", -1, -1), ("variant", 1 << 16, -1), ("variant", 4, -1), ("variant", 5 << 8, -1),
     ("total_visual", 5, -1), ("total_tokens", 1901, -1), ("total_visual", 2001, -1),
     ("cu_seqlens", None, -1), ("cu_visual", None, -1),
     ("kv_stride_tok", 0, -1), ("kv_stride_tok", 3, -1), ("q_stride_head", 4, -1),

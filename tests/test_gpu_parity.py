@@ -81,6 +81,7 @@ def assert_same(staged, fused, prob):
 
 
 def full_check(A, oracle, wl, units="all", compact_units="all", score_requests=None, **kw):
+    window_mode, budget_mode = kw.get("window_mode", 0), kw.get("budget_mode", 0)
     prob = make_problem(A, wl, **kw)
     staged = run_staged(A, prob)
     fused = run_fused(A, prob)
@@ -93,11 +94,11 @@ def full_check(A, oracle, wl, units="all", compact_units="all", score_requests=N
     report = {}
     oracle_iv = {}
     for (l, b) in chk:
-        oracle_iv[(l, b)] = PU.check_unit(oracle, wl, l, b, cu_s, cu_v, staged, report)
+        oracle_iv[(l, b)] = PU.check_unit(oracle, wl, l, b, cu_s, cu_v, staged, report, window_mode)
     reqs = range(spec.B) if score_requests is None else score_requests
     for b in reqs:
         by_layer = {l: oracle_iv[(l, b)] for l in range(spec.L) if (l, b) in oracle_iv}
-        PU.check_request(oracle, wl, b, cu_s, cu_v, staged, report, by_layer)
+        PU.check_request(oracle, wl, b, cu_s, cu_v, staged, report, by_layer, budget_mode)
     cu = all_units if compact_units == "all" else compact_units
     for (l, b) in cu:
         PU.check_compaction(oracle, wl, l, b, cu_s, cu_v, staged)
@@ -329,3 +330,33 @@ def test_device_errors_reported(A):
     A.aircache_compress(prob, ws, out["out_k"], out["out_v"], out["out_offsets"], out["keep"])
     assert A.aircache_get_error(ws) == 0
     del s
+
+
+# ------------------------------------------------------- ablation variants
+
+@pytest.mark.parametrize("window_mode", [1, 2, 3])
+def test_ablation_windows(A, oracle, window_mode):
+    """AirCache notes, "Ablation studies", observation windows: the last 16 /
+    32 text tokens or every text token take the elite set's place (texts of
+    40 and 9 tokens: a window longer and shorter than the text)."""
+    wl = custom_workload([500, 257], [40, 9], L=3, H_q=8, H_kv=2)
+    staged, rep = full_check(A, oracle, wl, window_mode=window_mode)
+    assert staged["n_tk"].tolist() == [min(w, n) for w in [{1: 16, 2: 32, 3: 10**9}[window_mode]]
+                                       for n in (40, 9)] * 3
+
+
+@pytest.mark.parametrize("budget_mode", [1, 2, 3, 4])
+def test_ablation_budgets(A, oracle, budget_mode):
+    """AirCache notes, "Ablation studies", layer budgets: uniform, PyramidKV-
+    style, strength only, skewness only (bf16 and fp32 paths)."""
+    wl = custom_workload([600, 333], [12, 20], L=5, H_q=8, H_kv=2)
+    full_check(A, oracle, wl, budget_mode=budget_mode)
+    wl32 = custom_workload([200], [7], L=4, H_q=4, H_kv=4, D=64, dtype=torch.float32)
+    full_check(A, oracle, wl32, budget_mode=budget_mode)
+
+
+def test_ablation_window_and_budget_on_7b_layers(A, oracle):
+    """A window and a budget variant together on the 7B-shaped workload
+    (4 layers), both scoring paths' unit kinds included."""
+    wl = W.make("7b", device="cuda", layers=4)
+    full_check(A, oracle, wl, window_mode=2, budget_mode=2)

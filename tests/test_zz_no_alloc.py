@@ -81,7 +81,7 @@ def host_only_problem(A, L, B):
     n_v, n_t = 100, 8
     return A.ProblemStruct(
         num_layers=L, num_requests=B, h_q=8, h_kv=2, head_dim=128, dtype=A.BF16,
-        max_visual=n_v, max_text=n_t, max_elite=0, reserved0=0,
+        max_visual=n_v, max_text=n_t, max_elite=0, variant=0,
         total_tokens=B * (n_v + n_t), total_visual=B * n_v,
         cu_seqlens=0x200000, cu_visual=0x300000,
         q_text=ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)),
