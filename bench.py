@@ -50,6 +50,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="7b")
+    ap.add_argument("--window-mode", type=int, default=0,
+                    help="ablation observation window: 0 elite (the method), 1 last 16, 2 last 32, 3 all text")
+    ap.add_argument("--budget-mode", type=int, default=0,
+                    help="ablation budget: 0 strength + skewness (the method), 1 uniform, 2 PyramidKV-style, "
+                         "3 strength only, 4 skewness only")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.5, help="untimed back-to-back load before timing")
@@ -200,7 +205,7 @@ def algorithmic_bytes(spec, n_tk, keep, esize):
     return k, path
 
 
-def oracle_sample(wl, budget_s, device_for_copy=None):
+def oracle_sample(wl, budget_s, device_for_copy=None, window_mode=0, budget_mode=0):
     """Time the oracle (single thread) on whole requests of the workload until
     budget_s is spent (at least one request).  Returns (tokens, seconds, requests)."""
     from lvlm_kv_cache_gb300 import workloads as W
@@ -217,7 +222,8 @@ def oracle_sample(wl, budget_s, device_for_copy=None):
         k = W.host_bits(wl.k[:, s0:s1])
         v = W.host_bits(wl.v[:, s0:s1])
         t = time.perf_counter()
-        res = O.request([q[l] for l in range(spec.L)], [k[l] for l in range(spec.L)], nv, spec.alpha, spec.r)
+        res = O.request([q[l] for l in range(spec.L)], [k[l] for l in range(spec.L)], nv, spec.alpha, spec.r,
+                        window_mode, budget_mode)
         for l in range(spec.L):
             O.compact(k[l], nv, nt, res["idx"][l])
             O.compact(v[l], nv, nt, res["idx"][l])
@@ -241,10 +247,10 @@ def run_reference(args, rank, world):
     spec = W.spec(args.config)
     wl = W.generate(spec, seed=0, device="cpu")
     for _ in range(args.warmup):
-        oracle_sample(wl, 0.0)
+        oracle_sample(wl, 0.0, window_mode=args.window_mode, budget_mode=args.budget_mode)
     tok, secs = 0, 0.0
     for _ in range(args.steps):
-        t, s, _ = oracle_sample(wl, 0.0)
+        t, s, _ = oracle_sample(wl, 0.0, window_mode=args.window_mode, budget_mode=args.budget_mode)
         tok += t
         secs += s
     value = tok / secs
@@ -253,7 +259,8 @@ def run_reference(args, rank, world):
         "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": DESCRIPTIONS.get(args.config, args.config), "name": args.config,
-                   "sample": "one request (all layers) per step"},
+                   "sample": "one request (all layers) per step",
+                   "variant": {"window_mode": args.window_mode, "budget_mode": args.budget_mode}},
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "request 0 of the workload, all layers, per step"},
@@ -289,7 +296,8 @@ def main():
     spec = wl.spec
     esize = 2 if spec.dtype == torch.bfloat16 else 4
     prob = A.Problem(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.cu_visual, max(spec.n_visual), max(spec.n_text),
-                     spec.alpha, spec.r, total_tokens=wl.total_tokens, total_visual=wl.total_visual)
+                     spec.alpha, spec.r, total_tokens=wl.total_tokens, total_visual=wl.total_visual,
+                     window_mode=args.window_mode, budget_mode=args.budget_mode)
     ws = prob.new_workspace()
     out = A.alloc_outputs(prob)
     L, B, TV = prob.L, prob.B, prob.total_visual
@@ -397,6 +405,7 @@ def main():
         "data": "synthetic",
         "config": {"workload": DESCRIPTIONS.get(args.config, args.config), "name": args.config,
                    "requests_per_rank": spec.B, "layers": spec.L, "seed": "rank",
+                   "variant": {"window_mode": args.window_mode, "budget_mode": args.budget_mode},
                    "l2": "flushed before every timed step outside the events: 256 MB written, then read back "
                          "(so the flush's own dirty lines are not written back inside the step)"},
         "requests_per_s": world * spec.B * args.steps / (total_ms / 1e3),
@@ -455,7 +464,8 @@ def main():
 
     # ---- CPU baseline: the oracle on the host cores, rank 0 at N=1 only
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tok, secs, nreq = oracle_sample(wl, args.cpu_sample_s)
+        tok, secs, nreq = oracle_sample(wl, args.cpu_sample_s, window_mode=args.window_mode,
+                                        budget_mode=args.budget_mode)
         line["cpu_baseline"] = {"value": tok / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"{nreq} whole request(s) x {spec.L} layers "
                                           f"({tok} visual KV rows) in {secs:.2f} s, single thread"}
