@@ -44,6 +44,9 @@
  *       0 to r / beta at the last layer (mean r; beta = 20, PyramidKV's
  *       default, the page gives none); strength only r_l = s'_t r; skewness
  *       only r_l = s'_k r; keep_l as in R7.
+ *   R16 a decode step (the consumer of the compacted cache) is plain softmax
+ *       attention of the step's query over every cached row, per query head,
+ *       with the head map of R1 and no mask.
  *
  * Element access: tensors are token-major [tokens][heads][D] with explicit
  * element strides for the token and head axes and D contiguous; the element
@@ -435,4 +438,51 @@ int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int
                    int32_t* keep, int32_t* idx) {
     return oracle_request_variant(q, k, n_layers, h_q, h_kv, d, n_v, n_t, alpha, r, 0, 0, iv, elite,
                                   n_tk, stats, keep, idx);
+}
+
+/* ------------------------------------------------------- decode consumer */
+
+/*
+ * One decode step over a KV cache (the KV-cache tutorial page, section
+ * "Prefill and Decode": each step brings one new query, which reads every
+ * cached key and value; the edge-device compression page, head-wise top-k
+ * scheme: once the cache is compacted, decoding is plain dense attention over
+ * the compacted rows).  R16: for query head h, reading KV head h / (H_q/H_kv)
+ * as in R1,
+ *   o_h = sum_j softmax_j(q_h . k_j / sqrt(D)) v_j
+ * over every row j of the cache, with no mask (every cached row precedes the
+ * query).
+ *
+ * q    : a view whose token 0 is the query, [H_q][D];
+ * k, v : views whose tokens 0..n_rows-1 are the cached rows, [H_kv][D] each;
+ * out  : [H_q * D] fp64, row h = o_h.
+ * returns 0, or -1 on bad arguments (n_rows < 1 among them).
+ */
+int oracle_decode(const oracle_view* q, const oracle_view* k, const oracle_view* v, int h_q, int h_kv,
+                  int d, int64_t n_rows, double* out) {
+    if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || d <= 0 || n_rows < 1) return -1;
+    const int group = h_q / h_kv;
+    double* w = (double*)malloc(sizeof(double) * (size_t)n_rows);
+    if (!w) return -1;
+    for (int h = 0; h < h_q; ++h) {
+        const int kv_head = h / group;
+        /* softmax weights of this head over the rows, max-subtracted */
+        double top = -INFINITY;
+        for (int64_t j = 0; j < n_rows; ++j) {
+            w[j] = scaled_dot(q, 0, h, k, j, kv_head, d);
+            top = fmax(top, w[j]);
+        }
+        double total = 0.0;
+        for (int64_t j = 0; j < n_rows; ++j) {
+            w[j] = exp(w[j] - top);
+            total += w[j];
+        }
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < n_rows; ++j) acc += w[j] / total * elem(v, j, kv_head, i);
+            out[(int64_t)h * d + i] = acc;
+        }
+    }
+    free(w);
+    return 0;
 }

@@ -33,6 +33,8 @@ int oracle_budget(const double* s_t, const double* s_k, int n_layers, int n_v, d
 int oracle_select(const double* iv, int n_v, int keep, int32_t* idx);
 int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t,
                        const int32_t* idx, int keep, void* dst);
+int oracle_decode(const oracle_view* q, const oracle_view* k, const oracle_view* v, int h_q, int h_kv,
+                  int d, int64_t n_rows, double* out);
 int oracle_window(int n_t, int mode, int32_t* positions);
 int oracle_budget_variant(const double* s_t, const double* s_k, int n_layers, int n_v, double r,
                           int mode, double* r_l, int32_t* keep);

@@ -76,6 +76,8 @@ def lib():
         L.oracle_request.argtypes = [V, V, i32, i32, i32, i32, i32, i32, f64, f64,
                                      vp, vp, vp, vp, vp, vp]
         L.oracle_request.restype = i32
+        L.oracle_decode.argtypes = [V, V, V, i32, i32, i32, i64, vp]
+        L.oracle_decode.restype = i32
         L.oracle_window.argtypes = [i32, i32, vp]
         L.oracle_window.restype = i32
         L.oracle_budget_variant.argtypes = [vp, vp, i32, i32, f64, i32, vp, vp]
@@ -155,6 +157,20 @@ def budget(s_t, s_k, n_v: int, r: float):
     if lib().oracle_budget(_ptr(st), _ptr(sk), L, n_v, float(r), _ptr(rl), _ptr(keep)) != 0:
         raise ValueError("oracle_budget rejected its arguments")
     return rl, keep
+
+
+def decode(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
+    """One decode step of attention: q [H_q, D] (one query row), k, v
+    [rows, H_kv, D] (the cached rows).  Returns o [H_q, D] in fp64."""
+    h_q, d = q.shape
+    h_kv = k.shape[1]
+    qv = _view(np.ascontiguousarray(q).reshape(1, h_q, d))
+    out = np.zeros((h_q, d), np.float64)
+    rc = lib().oracle_decode(ctypes.byref(qv), ctypes.byref(_view(k)), ctypes.byref(_view(v)), h_q, h_kv, d,
+                             int(k.shape[0]), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_decode rejected its arguments")
+    return out
 
 
 def window(n_t: int, mode: int) -> np.ndarray:

@@ -34,7 +34,17 @@ MUTATIONS = {
     "ties go to the higher index": ("return (x->i > y->i) - (x->i < y->i);", "return (x->i < y->i) - (x->i > y->i);"),
     "selection left in score order": ("    qsort(idx, (size_t)keep, sizeof(int32_t), ascending_int);\n", ""),
     "text rows shifted by one": ("(int64_t)n_v + (j - keep);", "(int64_t)n_v + (j - keep) - (j > keep);"),
+    "decode head map h mod h_kv": ("const int kv_head = h / group;", "const int kv_head = h % h_kv;"),
+    "decode weights not normalised": ("acc += w[j] / total * elem(v, j, kv_head, i);",
+                                      "acc += w[j] * elem(v, j, kv_head, i);"),
+    "decode reads keys as values": ("acc += w[j] / total * elem(v, j, kv_head, i);",
+                                    "acc += w[j] / total * elem(k, j, kv_head, i);"),
+    "decode drops the last row": ("for (int64_t j = 0; j < n_rows; ++j) acc +=",
+                                  "for (int64_t j = 0; j + 1 < n_rows; ++j) acc +="),
+    "decode logits unscaled": ("w[j] = scaled_dot(q, 0, h, k, j, kv_head, d);",
+                               "w[j] = scaled_dot(q, 0, h, k, j, kv_head, d) * sqrt((double)d);"),
 }
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_variants.py", "test_oracle_decode.py"]
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
@@ -50,6 +60,6 @@ def test_pins_catch_mutation(name, tmp_path):
                            "-o", str(so), str(mutated), "-lm"])
     env = dict(os.environ, AIRCACHE_ORACLE_LIB=str(so))
     res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                          os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                          *[os.path.join(ROOT, "tests", f) for f in PIN_FILES]],
                          cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert res.returncode != 0, f"pins did not catch: {name}\n{res.stdout[-2000:]}"
