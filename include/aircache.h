@@ -250,6 +250,86 @@ AIRCACHE_API int aircache_compress_profile(const aircache_problem* p, void* ws, 
 /* Name of kernel i (0-based, launch order) of aircache_compress on `p`, or NULL. */
 AIRCACHE_API const char* aircache_kernel_name(const aircache_problem* p, int i);
 
+/* ------------------------------------------------------------------ decode */
+
+/*
+ * One decode step of attention over cached K/V rows: the consumer of the
+ * compressed cache.  A decode step brings one new query per sequence, which
+ * reads every cached key and value (KV-cache tutorial page, section "Prefill
+ * and Decode"; the append K_{1:t} = [K_{1:t-1}; k_t]); once the cache is
+ * compacted, decoding is plain dense attention over the compacted rows (the
+ * edge-device compression page, head-wise top-k scheme).  For sequence s and
+ * query head h (KV head h / (h_q / h_kv)):
+ *   out[s][h] = sum_j softmax_j(q[s][h] . k_j / sqrt(head_dim)) v_j
+ * over the rows j = row_begin[s] .. row_end[s]-1 of the k / v arenas, plus the
+ * row (k_new[s], v_new[s]) when k_new is given.  No mask: every cached row
+ * precedes the query.  An empty sequence (no rows, no new row) gets out = 0.
+ *
+ * The arenas of aircache_compress plug in directly: for layer l of a batch of
+ * B requests, row_begin = out_offsets + l*B and row_end = out_offsets + l*B + 1
+ * (num_seqs = B); all layers at once use out_offsets and out_offsets + 1 with
+ * num_seqs = L*B.  A full cache [rows][h_kv][head_dim] uses its own ranges.
+ * Positions are the caller's: q and k_new are post-RoPE at the original
+ * position (N_v + N_t + step), not the compacted length.
+ *
+ * Layout (element strides; head_dim contiguous):
+ *   q      [num_seqs][h_q][head_dim]    q_stride_seq, q_stride_head
+ *   k, v   [kv_rows][h_kv][head_dim]    kv_stride_row, kv_stride_head
+ *   k_new, v_new [num_seqs][h_kv][head_dim]  new_stride_seq, new_stride_head
+ *   out    [num_seqs][h_q][head_dim]    fp32, dense
+ *   row_begin, row_end: device int64 [num_seqs].
+ * Requirements (else AIRCACHE_ERR_INVALID_ARG, or AIRCACHE_ERR_UNSUPPORTED
+ * for the dtype / group limits): dtype AIRCACHE_BF16; head_dim 64 or 128;
+ * h_q % h_kv == 0 and h_q / h_kv <= 16; k and v 16-byte aligned with
+ * kv_stride_row and kv_stride_head multiples of 8 elements (tensor-map rules);
+ * 1 <= kv_rows <= 2^31 - 2^16; num_seqs <= 65535; q 16-byte aligned with
+ * q_stride_seq and q_stride_head multiples of 8; max_rows >= 0; reserved0 == 0.
+ * max_rows is a hint, not a limit: the expected longest range, which sizes the
+ * split of each sequence across CTAs (and the workspace).  Device-side, a
+ * range with row_begin < 0, row_end < row_begin or row_end > kv_rows sets
+ * AIRCACHE_ERR_DEVICE_BOUNDS in the workspace error word and that sequence's
+ * output is left as zeros.
+ */
+typedef struct aircache_decode_problem {
+    int32_t num_seqs;
+    int32_t h_q;
+    int32_t h_kv;
+    int32_t head_dim;
+    int32_t dtype;
+    int32_t reserved0;
+    int64_t kv_rows;
+    int64_t max_rows;
+    const void* q;
+    const void* k;
+    const void* v;
+    const int64_t* row_begin;
+    const int64_t* row_end;
+    const void* k_new;  /* optional (NULL: no new row); v_new must then be NULL too */
+    const void* v_new;
+    int64_t q_stride_seq;
+    int64_t q_stride_head;
+    int64_t kv_stride_row;
+    int64_t kv_stride_head;
+    int64_t new_stride_seq;
+    int64_t new_stride_head;
+    float* out;
+} aircache_decode_problem;
+
+/* Workspace bytes aircache_decode needs for `p` on the current device, or 0 if
+ * `p` is invalid.  Depends on num_seqs, h_q, h_kv, head_dim, max_rows and the
+ * device's SM count. */
+AIRCACHE_API size_t aircache_decode_workspace_size(const aircache_decode_problem* p);
+
+/* Enqueue the decode step on `stream` (one memset of the workspace's first
+ * block, then one kernel).  ws is caller-owned device memory of at least
+ * aircache_decode_workspace_size(p) bytes (256-byte aligned); its error word is
+ * read by aircache_get_error. */
+AIRCACHE_API int aircache_decode(const aircache_decode_problem* p, void* ws, size_t ws_bytes, void* stream);
+
+/* Number of CTAs the decode kernel splits each (sequence, KV head) into for `p`
+ * on the current device, or -1 if `p` is invalid (for measurement). */
+AIRCACHE_API int aircache_decode_splits(const aircache_decode_problem* p);
+
 #ifdef __cplusplus
 }
 #endif

@@ -70,6 +70,21 @@ class ProblemStruct(ctypes.Structure):
 _lib = None
 
 
+class DecodeProblemStruct(ctypes.Structure):
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32), ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("kv_rows", ctypes.c_int64), ("max_rows", ctypes.c_int64),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("row_begin", ctypes.c_void_p), ("row_end", ctypes.c_void_p),
+        ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+        ("q_stride_seq", ctypes.c_int64), ("q_stride_head", ctypes.c_int64),
+        ("kv_stride_row", ctypes.c_int64), ("kv_stride_head", ctypes.c_int64),
+        ("new_stride_seq", ctypes.c_int64), ("new_stride_head", ctypes.c_int64),
+        ("out", ctypes.c_void_p),
+    ]
+
+
 def lib():
     """The loaded CUDA library (raises if it was not built)."""
     global _lib
@@ -107,6 +122,13 @@ def lib():
         L.aircache_compress_profile.restype = i32
         L.aircache_kernel_name.argtypes = [P, i32]
         L.aircache_kernel_name.restype = ctypes.c_char_p
+        DP = ctypes.POINTER(DecodeProblemStruct)
+        L.aircache_decode_workspace_size.argtypes = [DP]
+        L.aircache_decode_workspace_size.restype = sz
+        L.aircache_decode_splits.argtypes = [DP]
+        L.aircache_decode_splits.restype = i32
+        L.aircache_decode.argtypes = [DP, vp, sz, vp]
+        L.aircache_decode.restype = i32
         _lib = L
     return _lib
 
@@ -333,3 +355,80 @@ def compress_host(q, k, v, cu_seqlens, cu_visual, max_visual, max_text, alpha=0.
 def math_bound(L, B, total_text, total_visual, r):
     """The compress_bound formula, for host-side sizing without the library."""
     return L * total_text + math.ceil(r * L * total_visual) + B * (2 * L + 1)
+
+
+# ------------------------------------------------------------------ decode
+
+class DecodeProblem:
+    """One decode step over cached rows (see aircache_decode in the header).
+
+    q: [S, H_q, D] bf16 (one query row per sequence); k, v: arenas
+    [rows, H_kv, D] bf16; row_begin, row_end: int64 device tensors [S] (or one
+    offsets tensor [S+1] via ``offsets=``); k_new, v_new: optional [S, H_kv, D];
+    out: fp32 [S, H_q, D] (allocated when None).  max_rows: the expected
+    longest range (sizes the split; not a limit)."""
+
+    def __init__(self, q, k, v, row_begin=None, row_end=None, max_rows=0, k_new=None, v_new=None,
+                 out=None, offsets=None):
+        if offsets is not None:
+            row_begin, row_end = offsets[:-1], offsets[1:]
+        S, h_q, d = (int(x) for x in q.shape)
+        h_kv = int(k.shape[1])
+        if out is None:
+            out = torch.empty((S, h_q, d), dtype=torch.float32, device=q.device)
+        for t in (q, k, v) + ((k_new, v_new) if k_new is not None else ()):
+            if t.stride(-1) != 1:
+                raise ValueError("head_dim must be contiguous")
+        if k.stride() != v.stride() or (k_new is not None and k_new.stride() != v_new.stride()):
+            raise ValueError("k and v (and k_new and v_new) must share strides")
+        if row_begin.dtype != torch.int64 or row_end.dtype != torch.int64:
+            raise TypeError("row ranges are int64")
+        if not out.is_contiguous() or tuple(out.shape) != (S, h_q, d) or out.dtype != torch.float32:
+            raise ValueError("out must be a dense fp32 [S, H_q, D] tensor")
+        self.keep = (q, k, v, row_begin, row_end, k_new, v_new, out)
+        self.out = out
+        self.c = DecodeProblemStruct(
+            num_seqs=S, h_q=h_q, h_kv=h_kv, head_dim=d,
+            dtype=BF16 if q.dtype == torch.bfloat16 else F32, reserved0=0,
+            kv_rows=int(k.shape[0]), max_rows=int(max_rows),
+            q=q.data_ptr(), k=k.data_ptr(), v=v.data_ptr(),
+            row_begin=row_begin.data_ptr(), row_end=row_end.data_ptr(),
+            k_new=k_new.data_ptr() if k_new is not None else None,
+            v_new=v_new.data_ptr() if v_new is not None else None,
+            q_stride_seq=q.stride(0), q_stride_head=q.stride(1),
+            kv_stride_row=k.stride(0), kv_stride_head=k.stride(1),
+            new_stride_seq=k_new.stride(0) if k_new is not None else 0,
+            new_stride_head=k_new.stride(1) if k_new is not None else 0,
+            out=out.data_ptr(),
+        )
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+    def workspace_size(self) -> int:
+        n = lib().aircache_decode_workspace_size(self.ref)
+        if n == 0:
+            raise AirCacheError(ERR_INVALID_ARG, "aircache_decode_workspace_size")
+        return int(n)
+
+    def splits(self) -> int:
+        return int(lib().aircache_decode_splits(self.ref))
+
+    def new_workspace(self, device=None) -> torch.Tensor:
+        return torch.empty(self.workspace_size(), dtype=torch.uint8, device=device or self.out.device)
+
+
+def aircache_decode(prob: DecodeProblem, ws, stream=None):
+    _check(lib().aircache_decode(prob.ref, _ptr(ws), ws.numel(), _stream(stream)), "aircache_decode")
+
+
+def decode(prob: DecodeProblem, ws=None, stream=None, check=True):
+    """One decode step; returns prob.out.  check=True reads the device error word (synchronises)."""
+    ws = prob.new_workspace() if ws is None else ws
+    aircache_decode(prob, ws, stream)
+    if check:
+        st = aircache_get_error(ws, stream)
+        if st != OK:
+            raise AirCacheError(st, "aircache_decode (device)")
+    return prob.out

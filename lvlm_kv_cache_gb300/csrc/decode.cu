@@ -1,0 +1,506 @@
+// One decode step of attention over cached K/V rows: the consumer of the
+// compacted cache (KV-cache tutorial page, section "Prefill and Decode": each
+// step's single query reads every cached key and value; edge-device
+// compression page, head-wise top-k scheme: after compaction, decoding is
+// dense attention over the kept rows).
+//
+// Split-K over the rows.  CTA (x, h, s) takes the x-th slice of sequence s's
+// row range for KV head h and every query head of h's group (g <= 16, padded
+// to the 16 rows of an mma.sync A operand).  A producer warp streams 64-row
+// K and V tiles of that head with TMA (128-byte swizzle) through a ring of
+// stages; four consumer warps each take 16 rows of a tile:
+//   S = Q K^T      A = Q (16 heads x 16 d, in registers), B = K (ldmatrix),
+//   online softmax in base 2 per head, P rounded to bf16 (the normaliser sums
+//                  the rounded weights, so the output is an exact convex
+//                  combination with relatively perturbed weights),
+//   O += P V       A = P (the S accumulators repacked), B = V (ldmatrix.trans).
+// The warps' (max, sum, O) merge in shared memory into the slice's partial;
+// the last CTA of a (sequence, KV head) to finish (an atomic count, no
+// waiting) merges the slices, adds the step's own (k_new, v_new) row when
+// given, and writes out = O / sum in fp32.
+//
+// Traffic per launch: every cached row's K and V of each KV head once
+// (2 * head_dim * 2 bytes per row and head), the queries, and the fp32 output.
+#include <cuda_bf16.h>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "tmap.cuh"
+
+namespace aircache {
+namespace {
+
+constexpr int kDecRows = 64;          // rows per K/V tile
+constexpr int kDecWarps = 4;          // consumer warps, 16 rows each
+constexpr int kDecThreads = (kDecWarps + 1) * 32;
+constexpr int kDecMaxGroup = 16;      // query heads per KV head
+constexpr int kDecMaxSplit = 64;
+constexpr int kDecZeroBlock = 256;    // error word, then the per-(s, h) counters
+
+template <int D>
+struct DecCfg {
+  static constexpr int kSlabs = D / 64;                       // 128-byte column slabs per row
+  static constexpr int kTileBytes = kDecRows * D * 2;         // one K (or V) tile
+  static constexpr int kStages = D == 128 ? 3 : 5;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kQPitch = D + 8;                       // bf16 elements per staged query row
+  static constexpr int kRing = kStages * kStageBytes;
+  static constexpr int kMerge = kDecWarps * (kDecMaxGroup * D + 2 * kDecMaxGroup) * 4;
+  static constexpr int kMain = kRing > kMerge ? kRing : kMerge;
+  static constexpr int kQBytes = kDecMaxGroup * kQPitch * 2;
+  // 1024-byte alignment slack for the swizzled ring
+  static constexpr int kSmem = 1024 + kMain + kQBytes + 2 * kStages * 8 + 64 + kDecMaxGroup * kDecMaxSplit * 4 +
+                               2 * kDecMaxGroup * 4;
+};
+
+struct DecArgs {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  const int64_t* row_begin;
+  const int64_t* row_end;
+  float* out;
+  int32_t* error;
+  uint32_t* count;   // [S * h_kv]
+  float2* part_ml;   // [S * h_q * n_split] (max, sum) of each slice, base 2
+  float* part_o;     // [S * h_q * n_split * D]
+  int64_t kv_rows;
+  int64_t q_stride_seq, q_stride_head, new_stride_seq, new_stride_head;
+  int h_q, h_kv, group, n_split;
+  float scale_log2;  // log2(e) / sqrt(D)
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& lo_r, float& hi_r) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+  lo_r = __low2float(t);
+  hi_r = __high2float(t);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t r[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_constant__ CUtensorMap kmap,
+                                                             const __grid_constant__ CUtensorMap vmap,
+                                                             const __grid_constant__ DecArgs a) {
+  using C = DecCfg<D>;
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = dsm;                                                   // [stages][K tile, V tile]
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(dsm + C::kMain);  // [16][kQPitch]
+  uint64_t* full = reinterpret_cast<uint64_t*>(dsm + C::kMain + C::kQBytes);
+  uint64_t* empty = full + C::kStages;
+  int* ctl = reinterpret_cast<int*>(empty + C::kStages);                 // [16]
+  float* coef = reinterpret_cast<float*>(ctl + 16);                      // [16][kDecMaxSplit]
+  float* xnew = coef + kDecMaxGroup * kDecMaxSplit;                      // [16]
+  float* rnorm = xnew + kDecMaxGroup;                                    // [16]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int split = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int g = a.group;
+
+  // ---- this CTA's slice of the sequence's rows
+  if (tid == 0) {
+    const int64_t b = a.row_begin[s], e = a.row_end[s];
+    const bool ok = b >= 0 && e >= b && e <= a.kv_rows;
+    if (!ok && split == 0 && h == 0) set_error(a.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+    const int64_t n = ok ? e - b : 0;
+    int64_t per = (n + a.n_split - 1) / a.n_split;
+    per = (n >= (int64_t)kDecRows * a.n_split) ? (per + kDecRows - 1) / kDecRows * kDecRows : (per + 15) / 16 * 16;
+    const int64_t lo = b + (int64_t)split * per;
+    const int64_t hi = lo + per < e ? lo + per : e;
+    ctl[0] = (int)(lo & 0x7fffffff);
+    ctl[1] = ok && hi > lo ? (int)(hi - lo) : 0;
+    ctl[2] = ok ? 1 : 0;
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kDecWarps);
+    }
+    fence_mbar_init();
+  }
+  // ---- query rows of the group, zero-padded to 16 heads
+  for (int c = tid; c < kDecMaxGroup * (D / 8); c += kDecThreads) {
+    const int hh = c / (D / 8), ch = c % (D / 8);
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (hh < g) {
+      val = *reinterpret_cast<const uint4*>(a.q + (int64_t)s * a.q_stride_seq +
+                                            (int64_t)(h * g + hh) * a.q_stride_head + ch * 8);
+    }
+    *reinterpret_cast<uint4*>(qs + hh * C::kQPitch + ch * 8) = val;
+  }
+  __syncthreads();
+  const int row0 = ctl[0], nrows = ctl[1];
+  const int ntiles = (nrows + kDecRows - 1) / kDecRows;
+
+  if (warp == kDecWarps) {
+    // ---- producer: one elected lane streams the K/V tiles
+    if (lane == 0) {
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % C::kStages;
+        if (i >= C::kStages && !mbar_wait(&empty[st], ((i / C::kStages) - 1) & 1)) {
+          set_error(a.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+          break;
+        }
+        fence_proxy_async_smem();  // the consumers' generic reads of this stage come first
+        const uint32_t kb = smem_u32(ring + st * C::kStageBytes);
+        const uint32_t vb = kb + C::kTileBytes;
+        mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+        const int r = row0 + i * kDecRows;
+#pragma unroll
+        for (int sl = 0; sl < C::kSlabs; ++sl) {
+          tma_load_3d(kb + sl * kDecRows * 128, &kmap, sl * 64, h, r, &full[st]);
+          tma_load_3d(vb + sl * kDecRows * 128, &vmap, sl * 64, h, r, &full[st]);
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- consumers
+  const int hA = lane >> 2;  // heads of this thread's accumulator rows: hA and hA + 8
+  const int cq = lane & 3;
+  uint32_t qa[D / 16][4];
+  {
+    const int mi = lane >> 3, ri = lane & 7;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      ldmatrix_x4(qa[kk], qs + (ri + 8 * (mi & 1)) * C::kQPitch + 16 * kk + 8 * (mi >> 1));
+    }
+  }
+  float o[D / 8][4];
+#pragma unroll
+  for (int t = 0; t < D / 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+  const int r0 = 16 * warp;
+  bool alive = true;
+
+  for (int i = 0; i < ntiles && alive; ++i) {
+    const int st = i % C::kStages;
+    if (!mbar_wait(&full[st], (i / C::kStages) & 1)) {
+      if (lane == 0) set_error(a.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+      alive = false;
+      break;
+    }
+    const int valid = nrows - i * kDecRows - r0;  // rows of this warp's 16 that belong to the slice
+    if (valid > 0) {
+      const uint32_t kb = smem_u32(ring + st * C::kStageBytes);
+      const uint32_t vb = kb + C::kTileBytes;
+      if (valid < 16) {
+        // rows past the slice end may hold anything (another sequence, unused
+        // arena rows): zero their V so that 0-weight rows add exactly 0
+        uint8_t* vrow = ring + st * C::kStageBytes + C::kTileBytes;
+        for (int c = lane; c < 16 * C::kSlabs * 8; c += 32) {
+          const int rr = c / (C::kSlabs * 8), rest = c % (C::kSlabs * 8);
+          if (rr >= valid) {
+            *reinterpret_cast<uint4*>(vrow + (rest >> 3) * kDecRows * 128 + (r0 + rr) * 128 + (rest & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      __syncwarp();
+      // S = Q K^T for 16 rows: two n-tiles of 8 rows
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      {
+        const int mi = lane >> 3, ri = lane & 7;
+        const int row = r0 + ri + 8 * (mi >> 1);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          uint32_t kf[4];
+          ldsm_x4(kf, swz(kb + (kk >> 2) * kDecRows * 128, row, 2 * (kk & 3) + (mi & 1)));
+          mma_bf16_16816(sc[0], qa[kk], kf[0], kf[1]);
+          mma_bf16_16816(sc[1], qa[kk], kf[2], kf[3]);
+        }
+      }
+      // online softmax, base 2; rows at or past `valid` get weight 0
+      float tA = -INFINITY, tB = -INFINITY;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const bool ok = 8 * t + 2 * cq + e < valid;
+          sc[t][e] = ok ? sc[t][e] * a.scale_log2 : -INFINITY;
+          sc[t][2 + e] = ok ? sc[t][2 + e] * a.scale_log2 : -INFINITY;
+          tA = fmaxf(tA, sc[t][e]);
+          tB = fmaxf(tB, sc[t][2 + e]);
+        }
+      }
+      tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 1));
+      tA = fmaxf(tA, __shfl_xor_sync(0xffffffffu, tA, 2));
+      tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 1));
+      tB = fmaxf(tB, __shfl_xor_sync(0xffffffffu, tB, 2));
+      const float nA = fmaxf(mA, tA), nB = fmaxf(mB, tB);  // finite: row 0 of the slab is valid
+      const float fA = fast_exp2(mA - nA), fB = fast_exp2(mB - nB);
+      mA = nA;
+      mB = nB;
+      uint32_t pa[4];
+      float sA = 0.f, sB = 0.f;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        float x0, x1;
+        pa[2 * t] = pack_bf16(fast_exp2(sc[t][0] - nA), fast_exp2(sc[t][1] - nA), x0, x1);
+        sA += x0 + x1;
+        pa[2 * t + 1] = pack_bf16(fast_exp2(sc[t][2] - nB), fast_exp2(sc[t][3] - nB), x0, x1);
+        sB += x0 + x1;
+      }
+      lA = lA * fA + sA;
+      lB = lB * fB + sB;
+#pragma unroll
+      for (int t = 0; t < D / 8; ++t) {
+        o[t][0] *= fA;
+        o[t][1] *= fA;
+        o[t][2] *= fB;
+        o[t][3] *= fB;
+      }
+      // O += P V: B = V rows via the transposing ldmatrix, two n-tiles of 8 d per load
+      {
+        const int mi = lane >> 3, ri = lane & 7;
+        const int row = r0 + ri + 8 * (mi & 1);
+#pragma unroll
+        for (int np = 0; np < D / 16; ++np) {
+          uint32_t vf[4];
+          ldsm_x4_trans(vf, swz(vb + (np >> 2) * kDecRows * 128, row, 2 * (np & 3) + (mi >> 1)));
+          mma_bf16_16816(o[2 * np], pa, vf[0], vf[1]);
+          mma_bf16_16816(o[2 * np + 1], pa, vf[2], vf[3]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+
+  // ---- merge the four warps' (max, sum, O) into the slice's partial
+  lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+  lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+  lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+  lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+  named_bar_sync(1, kDecWarps * 32);  // every warp is done with the ring
+  float* ow = reinterpret_cast<float*>(ring);           // [warp][16][D]
+  float* mw = ow + kDecWarps * kDecMaxGroup * D;         // [warp][16]
+  float* lw = mw + kDecWarps * kDecMaxGroup;             // [warp][16]
+#pragma unroll
+  for (int t = 0; t < D / 8; ++t) {
+    const int d = 8 * t + 2 * cq;
+    *reinterpret_cast<float2*>(ow + (warp * kDecMaxGroup + hA) * D + d) = make_float2(o[t][0], o[t][1]);
+    *reinterpret_cast<float2*>(ow + (warp * kDecMaxGroup + hA + 8) * D + d) = make_float2(o[t][2], o[t][3]);
+  }
+  if (cq == 0) {
+    mw[warp * kDecMaxGroup + hA] = mA;
+    mw[warp * kDecMaxGroup + hA + 8] = mB;
+    lw[warp * kDecMaxGroup + hA] = lA;
+    lw[warp * kDecMaxGroup + hA + 8] = lB;
+  }
+  named_bar_sync(1, kDecWarps * 32);
+  const int64_t head0 = (int64_t)s * a.h_q + (int64_t)h * g;  // first query head of the group
+  for (int idx = tid; idx < g * D; idx += kDecWarps * 32) {
+    const int hh = idx / D, d = idx % D;
+    float m = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) m = fmaxf(m, mw[w * kDecMaxGroup + hh]);
+    float osum = 0.f, lsum = 0.f;
+    if (m != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kDecWarps; ++w) {
+        const float mx = mw[w * kDecMaxGroup + hh];
+        if (mx != -INFINITY) {
+          const float c = fast_exp2(mx - m);
+          osum += c * ow[(w * kDecMaxGroup + hh) * D + d];
+          lsum += c * lw[w * kDecMaxGroup + hh];
+        }
+      }
+    }
+    const int64_t slot = (head0 + hh) * a.n_split + split;
+    a.part_o[slot * D + d] = osum;
+    if (d == 0) a.part_ml[slot] = make_float2(m, lsum);
+  }
+  __threadfence();
+  named_bar_sync(1, kDecWarps * 32);
+  if (tid == 0) {
+    const uint32_t before = atomicAdd(&a.count[(int64_t)s * a.h_kv + h], 1u);
+    ctl[3] = before == (uint32_t)(a.n_split - 1);
+  }
+  named_bar_sync(1, kDecWarps * 32);
+  if (!ctl[3]) return;
+
+  // ---- last slice of this (sequence, KV head): merge the slices and the new row
+  __threadfence();
+  const bool ok = ctl[2] != 0;
+  const bool has_new = a.k_new != nullptr && ok;
+  for (int hh = warp; hh < g; hh += kDecWarps) {
+    float xn = -INFINITY;
+    if (has_new) {
+      float dot = 0.f;
+      const __nv_bfloat16* qh = qs + hh * C::kQPitch;
+      const __nv_bfloat16* kn = a.k_new + (int64_t)s * a.new_stride_seq + (int64_t)h * a.new_stride_head;
+      for (int d = lane; d < D; d += 32) dot += __bfloat162float(qh[d]) * __bfloat162float(kn[d]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      xn = dot * a.scale_log2;
+    }
+    float m = xn;
+    for (int x = lane; x < a.n_split; x += 32) m = fmaxf(m, __ldcg(&a.part_ml[(head0 + hh) * a.n_split + x]).x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float lsum = 0.f;
+    for (int x = lane; x < a.n_split; x += 32) {
+      const float2 ml = __ldcg(&a.part_ml[(head0 + hh) * a.n_split + x]);
+      const float c = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - m);
+      coef[hh * kDecMaxSplit + x] = c;
+      lsum += c * ml.y;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+    if (lane == 0) {
+      const float cn = has_new ? fast_exp2(xn - m) : 0.f;
+      xnew[hh] = cn;
+      lsum += cn;
+      rnorm[hh] = (ok && lsum > 0.f) ? 1.f / lsum : 0.f;
+    }
+  }
+  named_bar_sync(1, kDecWarps * 32);
+  for (int idx = tid; idx < g * D; idx += kDecWarps * 32) {
+    const int hh = idx / D, d = idx % D;
+    float acc = 0.f;
+    for (int x = 0; x < a.n_split; ++x) {
+      const float c = coef[hh * kDecMaxSplit + x];
+      if (c != 0.f) acc += c * __ldcg(&a.part_o[((head0 + hh) * a.n_split + x) * D + d]);
+    }
+    if (has_new) {
+      const __nv_bfloat16* vn = a.v_new + (int64_t)s * a.new_stride_seq + (int64_t)h * a.new_stride_head;
+      acc += xnew[hh] * __bfloat162float(vn[d]);
+    }
+    a.out[(head0 + hh) * D + d] = acc * rnorm[hh];
+  }
+}
+
+// ------------------------------------------------------------------ host
+
+struct DecPlan {
+  int d, g, n_split;
+  size_t zero_bytes, ml_off, o_off, total;
+};
+
+inline size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Validates `p` and sizes the launch; returns AIRCACHE_OK or an error code.
+int decode_plan(const aircache_decode_problem* p, DecPlan& pl) {
+  if (!p) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->num_seqs < 0 || p->num_seqs > 65535 || p->h_q <= 0 || p->h_kv <= 0 || p->h_q % p->h_kv != 0 ||
+      (p->head_dim != 64 && p->head_dim != 128) || p->reserved0 != 0 || p->kv_rows < 1 ||
+      p->kv_rows > 0x7fff0000LL || p->max_rows < 0)
+    return AIRCACHE_ERR_INVALID_ARG;
+  if (p->dtype != AIRCACHE_BF16 || p->h_q / p->h_kv > kDecMaxGroup) return AIRCACHE_ERR_UNSUPPORTED;
+  if (!p->q || !p->k || !p->v || !p->row_begin || !p->row_end || !p->out || (!p->k_new) != (!p->v_new))
+    return AIRCACHE_ERR_INVALID_ARG;
+  auto al16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
+  if (!al16(p->k) || !al16(p->v) || !al16(p->q) || p->kv_stride_row <= 0 || p->kv_stride_head <= 0 ||
+      p->kv_stride_row % 8 != 0 || p->kv_stride_head % 8 != 0 || p->q_stride_seq % 8 != 0 ||
+      p->q_stride_head % 8 != 0 || p->q_stride_seq < 0 || p->q_stride_head < 0)
+    return AIRCACHE_ERR_INVALID_ARG;
+  if (p->k_new && (p->new_stride_seq < 0 || p->new_stride_head < 0)) return AIRCACHE_ERR_INVALID_ARG;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  pl.d = p->head_dim;
+  pl.g = p->h_q / p->h_kv;
+  const long long pairs = (long long)p->num_seqs * p->h_kv;
+  const long long target = 2LL * sms;  // two CTAs resident per SM
+  long long want = pairs > 0 ? (target + pairs - 1) / pairs : 1;
+  const long long cap = (p->max_rows + kDecRows - 1) / kDecRows;
+  if (want > cap) want = cap;
+  if (want < 1) want = 1;
+  if (want > kDecMaxSplit) want = kDecMaxSplit;
+  pl.n_split = (int)want;
+  const size_t slots = (size_t)p->num_seqs * p->h_q * pl.n_split;
+  pl.zero_bytes = kDecZeroBlock + round256(sizeof(uint32_t) * (size_t)pairs);
+  pl.ml_off = pl.zero_bytes;
+  pl.o_off = pl.ml_off + round256(sizeof(float2) * slots);
+  pl.total = pl.o_off + round256(sizeof(float) * slots * pl.d);
+  return AIRCACHE_OK;
+}
+
+bool encode_arena(CUtensorMap* m, const void* base, const aircache_decode_problem* p) {
+  auto enc = tma_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)p->head_dim, (cuuint64_t)p->h_kv, (cuuint64_t)p->kv_rows};
+  cuuint64_t strides[2] = {(cuuint64_t)p->kv_stride_head * 2, (cuuint64_t)p->kv_stride_row * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kDecRows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+int launch_decode(const aircache_decode_problem* p, const DecPlan& pl, uint8_t* ws, cudaStream_t s) {
+  CUtensorMap km, vm;
+  if (!encode_arena(&km, p->k, p) || !encode_arena(&vm, p->v, p)) return AIRCACHE_ERR_UNSUPPORTED;
+  DecArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(p->q);
+  a.k_new = static_cast<const __nv_bfloat16*>(p->k_new);
+  a.v_new = static_cast<const __nv_bfloat16*>(p->v_new);
+  a.row_begin = p->row_begin;
+  a.row_end = p->row_end;
+  a.out = p->out;
+  a.error = reinterpret_cast<int32_t*>(ws);
+  a.count = reinterpret_cast<uint32_t*>(ws + kDecZeroBlock);
+  a.part_ml = reinterpret_cast<float2*>(ws + pl.ml_off);
+  a.part_o = reinterpret_cast<float*>(ws + pl.o_off);
+  a.kv_rows = p->kv_rows;
+  a.q_stride_seq = p->q_stride_seq;
+  a.q_stride_head = p->q_stride_head;
+  a.new_stride_seq = p->new_stride_seq;
+  a.new_stride_head = p->new_stride_head;
+  a.h_q = p->h_q;
+  a.h_kv = p->h_kv;
+  a.group = pl.g;
+  a.n_split = pl.n_split;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  const int smem = DecCfg<D>::kSmem;
+  if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D>), smem) != cudaSuccess) return AIRCACHE_ERR_CUDA;
+  decode_kernel<D><<<dim3(pl.n_split, p->h_kv, p->num_seqs), kDecThreads, smem, s>>>(km, vm, a);
+  return cudaGetLastError() == cudaSuccess ? AIRCACHE_OK : AIRCACHE_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace aircache
+
+using namespace aircache;
+
+extern "C" {
+
+size_t aircache_decode_workspace_size(const aircache_decode_problem* p) {
+  DecPlan pl;
+  return decode_plan(p, pl) == AIRCACHE_OK ? pl.total : 0;
+}
+
+int aircache_decode_splits(const aircache_decode_problem* p) {
+  DecPlan pl;
+  return decode_plan(p, pl) == AIRCACHE_OK ? pl.n_split : -1;
+}
+
+int aircache_decode(const aircache_decode_problem* p, void* ws, size_t ws_bytes, void* stream) {
+  DecPlan pl;
+  const int rc = decode_plan(p, pl);
+  if (rc != AIRCACHE_OK) return rc;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) != 0) return AIRCACHE_ERR_INVALID_ARG;
+  if (ws_bytes < pl.total) return AIRCACHE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  if (cudaMemsetAsync(w, 0, pl.zero_bytes, s) != cudaSuccess) return AIRCACHE_ERR_CUDA;
+  if (p->num_seqs == 0) return AIRCACHE_OK;
+  return pl.d == 128 ? launch_decode<128>(p, pl, w, s) : launch_decode<64>(p, pl, w, s);
+}
+
+}  // extern "C"

@@ -31,6 +31,12 @@ video_r01 / video_r10
 ragged      B=32, L=28, H_q=28, H_kv=4, D=128, N_v ~ U[576, 9000], N_t ~ U[32, 1024]
             (seeded integers), bf16 N(0,1), 10% heavy keys (7b rule); alpha=0.9,
             r=0.05.
+
+Decode steps (decode_inputs): S sequences of given lengths packed into one
+arena [rows, H_kv, D] (sequence s owns rows offsets[s]..offsets[s+1]-1), one
+query row [H_q, D] per sequence, bf16 N(0,1) entries (queries times q_scale),
+optional extra arena rows after the last sequence filled with NaN, and an
+optional new (k, v) row per sequence.
 """
 from __future__ import annotations
 
@@ -199,3 +205,36 @@ def host_bits(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.float32:
         return t.numpy()
     raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+@dataclasses.dataclass
+class DecodeInputs:
+    q: torch.Tensor        # [S, H_q, D]
+    k: torch.Tensor        # [rows, H_kv, D]
+    v: torch.Tensor
+    offsets: torch.Tensor  # int64 [S+1]
+    k_new: torch.Tensor | None = None  # [S, H_kv, D]
+    v_new: torch.Tensor | None = None
+
+
+def decode_inputs(lengths, h_q, h_kv, d, seed=0, device="cpu", q_scale=1.0, nan_tail=0, new_row=False,
+                  dtype=torch.bfloat16) -> DecodeInputs:
+    """Seeded inputs of one decode step over ragged cached rows (see the module docstring)."""
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    S = len(lengths)
+    offs = np.zeros(S + 1, np.int64)
+    offs[1:] = np.cumsum(np.asarray(lengths, np.int64))
+    rows = int(offs[-1]) + int(nan_tail)
+    q = (torch.randn((S, h_q, d), generator=gen, device=dev) * q_scale).to(dtype)
+    k = torch.randn((max(rows, 1), h_kv, d), generator=gen, device=dev).to(dtype)
+    v = torch.randn((max(rows, 1), h_kv, d), generator=gen, device=dev).to(dtype)
+    if nan_tail:
+        k[int(offs[-1]):] = float("nan")
+        v[int(offs[-1]):] = float("nan")
+    kn = vn = None
+    if new_row:
+        kn = torch.randn((S, h_kv, d), generator=gen, device=dev).to(dtype)
+        vn = torch.randn((S, h_kv, d), generator=gen, device=dev).to(dtype)
+    return DecodeInputs(q, k, v, torch.as_tensor(offs, device=dev), kn, vn)
