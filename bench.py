@@ -59,6 +59,12 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.5, help="untimed back-to-back load before timing")
     ap.add_argument("--cpu-sample-s", type=float, default=10.0)
+    ap.add_argument("--decode", action="store_true",
+                    help="measure the decode consumer instead: one decode step of attention over the full and "
+                         "the compressed cache, per decode configuration (one JSON line each)")
+    ap.add_argument("--decode-configs", default="8x2048,8x32768,16x16384",
+                    help="comma-separated BATCHxPROMPT list for --decode")
+    ap.add_argument("--decode-ratios", default="0.1,0.5", help="retention ratios r for --decode")
     return ap.parse_args()
 
 
@@ -235,6 +241,162 @@ def oracle_sample(wl, budget_s, device_for_copy=None, window_mode=0, budget_mode
     return tokens, elapsed, done
 
 
+# ------------------------------------------------------------------ decode consumer
+
+DECODE_METRIC = "decode attention step time (all 28 layers, one new token per request), full vs compressed cache"
+
+
+def decode_oracle_sample(q, ranges, budget_s):
+    """Time the oracle's decode on sequences (query row index, first row, end
+    row, K arena, V arena) until budget_s is spent; returns (rows, seconds,
+    sequences)."""
+    from oracle import oracle as O
+
+    rows, secs, n = 0, 0.0, 0
+    for (qi, r0, r1, kk, vv) in ranges:
+        qb = W_host(q[qi])
+        kb, vb = W_host(kk[r0:r1]), W_host(vv[r0:r1])
+        t = time.perf_counter()
+        O.decode(qb, kb, vb)
+        secs += time.perf_counter() - t
+        rows += r1 - r0
+        n += 1
+        if secs >= budget_s:
+            break
+    return rows, secs, n
+
+
+def W_host(t):
+    from lvlm_kv_cache_gb300 import workloads as W
+
+    return W.host_bits(t)
+
+
+def run_decode(args, local):
+    """One decode step = 28 per-layer aircache_decode calls (a CUDA graph of
+    them, as a decoder replays it), over (a) the full prefill cache and (b) the
+    cache aircache_compress left, for each BATCHxPROMPT and ratio r.  L2 is
+    flushed before every timed step (outside the events)."""
+    import dataclasses
+
+    import torch
+
+    from lvlm_kv_cache_gb300 import aircache as A
+    from lvlm_kv_cache_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peak, peak_kind = load_peaks()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        flush_buf.zero_()
+        torch.sum(flush_buf.view(torch.int64), dim=(0,), out=flush_sink)
+
+    ratios = [float(x) for x in args.decode_ratios.split(",") if x]
+    for cfg in [c for c in args.decode_configs.split(",") if c]:
+        B, P = (int(x) for x in cfg.lower().split("x"))
+        n_t = 128
+        base = W.spec("7b")
+        spec = dataclasses.replace(base, B=B, n_visual=[P - n_t] * B, n_text=[n_t] * B)
+        wl = W.generate(spec, seed=0, device=dev)
+        L, H_q, H_kv, D = spec.L, spec.H_q, spec.H_kv, spec.D
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1)
+        qdec = torch.randn((L, B, H_q, D), generator=gen, device=dev).to(torch.bfloat16)
+        cu64 = wl.cu_seqlens.to(torch.int64)
+
+        def timed(probs, ws):
+            for pr in probs:  # eager once: sets the kernel attributes before capture
+                A.aircache_decode(pr, ws)
+            torch.cuda.synchronize()
+            st = A.aircache_get_error(ws)
+            if st != 0:
+                raise RuntimeError(f"decode device error {st}")
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for pr in probs:
+                    A.aircache_decode(pr, ws)
+            for _ in range(max(args.warmup, 3)):
+                flush_l2()
+                g.replay()
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for s_, e_ in ev:
+                flush_l2()
+                s_.record()
+                g.replay()
+                e_.record()
+            torch.cuda.synchronize()
+            st = A.aircache_get_error(ws)
+            if st != 0:
+                raise RuntimeError(f"decode device error {st}")
+            return statistics.median(s_.elapsed_time(e_) for s_, e_ in ev)
+
+        full_probs = [A.DecodeProblem(qdec[l], wl.k[l], wl.v[l], offsets=cu64, max_rows=P) for l in range(L)]
+        ws = torch.zeros(max(p.workspace_size() for p in full_probs), dtype=torch.uint8, device=dev)
+        sampler = ClockSampler(local)
+        sampler.start()
+        full_ms = timed(full_probs, ws)
+        full_rows = L * B * P
+        kv_row_bytes = H_kv * D * 2 * 2
+        full_bytes = full_rows * kv_row_bytes + L * B * H_q * D * (2 + 4)
+        results = []
+        for r in ratios:
+            s_r = dataclasses.replace(spec, r=r)
+            prob = A.Problem(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.cu_visual, P - n_t, n_t, s_r.alpha, r,
+                             total_tokens=wl.total_tokens, total_visual=wl.total_visual)
+            out = A.compress(prob)
+            offs = out["out_offsets"]
+            rows_h = offs.cpu().numpy()
+            longest = int((rows_h[1:] - rows_h[:-1]).max())
+            comp_probs = [A.DecodeProblem(qdec[l], out["out_k"], out["out_v"], row_begin=offs[l * B:(l + 1) * B],
+                                          row_end=offs[l * B + 1:(l + 1) * B + 1], max_rows=longest)
+                          for l in range(L)]
+            need = max(p.workspace_size() for p in comp_probs)
+            ws_c = ws if ws.numel() >= need else torch.zeros(need, dtype=torch.uint8, device=dev)
+            comp_ms = timed(comp_probs, ws_c)
+            comp_rows = int(rows_h[-1])
+            comp_bytes = comp_rows * kv_row_bytes + L * B * H_q * D * (2 + 4)
+            results.append({"r": r, "ms": comp_ms, "rows": comp_rows, "algorithmic_bytes": comp_bytes,
+                            "gbs": comp_bytes / (comp_ms * 1e-3) / 1e9,
+                            "frac": comp_bytes / (comp_ms * 1e-3) / 1e9 / peak,
+                            "splits": comp_probs[0].splits(), "reduction": 1.0 - comp_ms / full_ms})
+            del out, prob
+        clocks = sampler.stop()
+        full_gbs = full_bytes / (full_ms * 1e-3) / 1e9
+        line = {
+            "metric": DECODE_METRIC, "value": results[0]["ms"] if results else full_ms, "unit": "ms",
+            "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"7B LVLM-shaped decode: batch {B}, prompt {P} ({P - n_t} visual + {n_t} text), "
+                                   f"L=28, H_q=28, H_kv=4, D=128, bf16; caches from aircache_compress",
+                       "batch": B, "prompt": P,
+                       "step": "28 aircache_decode calls (one per layer, num_seqs = batch) replayed as a CUDA graph",
+                       "l2": "flushed before every timed step outside the events"},
+            "full": {"ms": full_ms, "rows": full_rows, "algorithmic_bytes": full_bytes, "gbs": full_gbs,
+                     "frac": full_gbs / peak, "splits": full_probs[0].splits()},
+            "compressed": results,
+            "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": full_gbs, "peak": peak,
+                         "unit": "GB/s", "frac": full_gbs / peak, "peak_kind": peak_kind, "traffic": None},
+            "gpu_launches": L,
+            "clocks": clocks,
+        }
+        if not args.no_cpu_baseline:
+            ranges = [(b, int(cu64[b]), int(cu64[b + 1]), wl.k[0], wl.v[0]) for b in range(B)]
+            rows, secs, n = decode_oracle_sample(qdec[0], ranges, args.cpu_sample_s / 2)
+            ms_step = secs / rows * full_rows * 1e3
+            line["cpu_baseline"] = {"value": ms_step, "unit": "ms per full-cache step (extrapolated)", "cores": 1,
+                                    "kind": "oracle",
+                                    "sample": f"{n} (layer 0, request) sequence(s) of {P} rows in {secs:.2f} s, "
+                                              f"single thread, scaled by rows to the {L}x{B} sequences of a step"}
+        print(json.dumps(line), flush=True)
+        del wl, full_probs, ws
+        torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, rank, world):
@@ -278,6 +440,8 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.decode:
+        return run_decode(args, local)
 
     import torch
 

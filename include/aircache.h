@@ -320,10 +320,15 @@ typedef struct aircache_decode_problem {
  * device's SM count. */
 AIRCACHE_API size_t aircache_decode_workspace_size(const aircache_decode_problem* p);
 
-/* Enqueue the decode step on `stream` (one memset of the workspace's first
- * block, then one kernel).  ws is caller-owned device memory of at least
- * aircache_decode_workspace_size(p) bytes (256-byte aligned); its error word is
- * read by aircache_get_error. */
+/* Enqueue the decode step on `stream` (one kernel, nothing else).  ws is
+ * caller-owned device memory of at least aircache_decode_workspace_size(p)
+ * bytes (256-byte aligned), ZEROED ONCE by the caller before its first use;
+ * every call leaves it in that state again, so it can be reused call after
+ * call with no memset between them (a memset node between consecutive decode
+ * kernels costs several microseconds per layer).  Unlike the compression entry
+ * points, aircache_decode does not clear the error word: a device error stays
+ * recorded (aircache_get_error reports it) until the caller zeroes the
+ * workspace again. */
 AIRCACHE_API int aircache_decode(const aircache_decode_problem* p, void* ws, size_t ws_bytes, void* stream);
 
 /* Number of CTAs the decode kernel splits each (sequence, KV head) into for `p`

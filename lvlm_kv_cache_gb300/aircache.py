@@ -416,7 +416,9 @@ class DecodeProblem:
         return int(lib().aircache_decode_splits(self.ref))
 
     def new_workspace(self, device=None) -> torch.Tensor:
-        return torch.empty(self.workspace_size(), dtype=torch.uint8, device=device or self.out.device)
+        """A zeroed decode workspace (zeroed once; every call leaves it zeroed
+        again, apart from a recorded device error)."""
+        return torch.zeros(self.workspace_size(), dtype=torch.uint8, device=device or self.out.device)
 
 
 def aircache_decode(prob: DecodeProblem, ws, stream=None):

@@ -23,6 +23,8 @@
 // (2 * head_dim * 2 bytes per row and head), the queries, and the fp32 output.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "tmap.cuh"
@@ -35,6 +37,7 @@ constexpr int kDecWarps = 4;          // consumer warps, 16 rows each
 constexpr int kDecThreads = (kDecWarps + 1) * 32;
 constexpr int kDecMaxGroup = 16;      // query heads per KV head
 constexpr int kDecMaxSplit = 64;
+constexpr int kDecMaxCluster = 8;     // slices per (sequence, KV head) merged through a cluster
 constexpr int kDecZeroBlock = 256;    // error word, then the per-(s, h) counters
 
 template <int D>
@@ -49,8 +52,10 @@ struct DecCfg {
   static constexpr int kMain = kRing > kMerge ? kRing : kMerge;
   static constexpr int kQBytes = kDecMaxGroup * kQPitch * 2;
   // 1024-byte alignment slack for the swizzled ring
-  static constexpr int kSmem = 1024 + kMain + kQBytes + 2 * kStages * 8 + 64 + kDecMaxGroup * kDecMaxSplit * 4 +
-                               2 * kDecMaxGroup * 4;
+  static constexpr int kSmem = 1024 + kMain + kQBytes + 2 * kStages * 8 + 64 + 3 * kDecMaxGroup * 4;
+  static_assert(32768 + kDecMaxGroup * kDecMaxSplit * 12 <= 45056, "merge scratch below the cluster partial");
+  static_assert(kRing >= 45056 + kDecMaxGroup * D * 4 + kDecMaxGroup * 8, "merge scratch must fit in the ring");
+  static_assert(kSmem <= 113 * 1024, "two CTAs per SM");
 };
 
 struct DecArgs {
@@ -84,6 +89,15 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t r[4], uint32_t addr) {
                : "memory");
 }
 
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
@@ -92,7 +106,7 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-template <int D>
+template <int D, bool CL>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_constant__ CUtensorMap kmap,
                                                              const __grid_constant__ CUtensorMap vmap,
                                                              const __grid_constant__ DecArgs a) {
@@ -104,16 +118,25 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   uint64_t* full = reinterpret_cast<uint64_t*>(dsm + C::kMain + C::kQBytes);
   uint64_t* empty = full + C::kStages;
   int* ctl = reinterpret_cast<int*>(empty + C::kStages);                 // [16]
-  float* coef = reinterpret_cast<float*>(ctl + 16);                      // [16][kDecMaxSplit]
-  float* xnew = coef + kDecMaxGroup * kDecMaxSplit;                      // [16]
+  // the slices' (max, sum) and merge weights live in the ring once it is idle,
+  // above the 32 KB the per-warp merge and the final reduction use
+  float2* mlbuf = reinterpret_cast<float2*>(ring + 32768);               // [16][kDecMaxSplit]
+  float* coef = reinterpret_cast<float*>(mlbuf + kDecMaxGroup * kDecMaxSplit);  // [16][kDecMaxSplit]
+  float* pbuf = reinterpret_cast<float*>(ring + 45056);                  // [16][D] this slice's O (clusters)
+  float2* pml = reinterpret_cast<float2*>(ring + 45056 + kDecMaxGroup * D * 4);  // [16] its (max, sum)
+  float* xnew = reinterpret_cast<float*>(ctl + 16);                      // [16] new row's base-2 logit
   float* rnorm = xnew + kDecMaxGroup;                                    // [16]
+  float* cnew = rnorm + kDecMaxGroup;                                    // [16] new row's weight
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int split = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
   const int g = a.group;
 
-  // ---- this CTA's slice of the sequence's rows
-  if (tid == 0) {
+  if (warp == kDecWarps && lane == 0) {
+    // ---- producer lane: this CTA's slice of the sequence's rows, then the
+    // first tiles right away (the queries load meanwhile)
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
     const int64_t b = a.row_begin[s], e = a.row_end[s];
     const bool ok = b >= 0 && e >= b && e <= a.kv_rows;
     if (!ok && split == 0 && h == 0) set_error(a.error, AIRCACHE_ERR_DEVICE_BOUNDS);
@@ -122,14 +145,26 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
     per = (n >= (int64_t)kDecRows * a.n_split) ? (per + kDecRows - 1) / kDecRows * kDecRows : (per + 15) / 16 * 16;
     const int64_t lo = b + (int64_t)split * per;
     const int64_t hi = lo + per < e ? lo + per : e;
-    ctl[0] = (int)(lo & 0x7fffffff);
-    ctl[1] = ok && hi > lo ? (int)(hi - lo) : 0;
+    const int row0 = (int)(lo & 0x7fffffff);
+    const int nrows = ok && hi > lo ? (int)(hi - lo) : 0;
+    ctl[0] = row0;
+    ctl[1] = nrows;
     ctl[2] = ok ? 1 : 0;
     for (int i = 0; i < C::kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kDecWarps);
     }
     fence_mbar_init();
+    const int ntiles = (nrows + kDecRows - 1) / kDecRows;
+    for (int i = 0; i < ntiles && i < C::kStages; ++i) {
+      const uint32_t kb = smem_u32(ring + i * C::kStageBytes);
+      mbar_arrive_expect_tx(&full[i], C::kStageBytes);
+#pragma unroll
+      for (int sl = 0; sl < C::kSlabs; ++sl) {
+        tma_load_3d(kb + sl * kDecRows * 128, &kmap, sl * 64, h, row0 + i * kDecRows, &full[i]);
+        tma_load_3d(kb + C::kTileBytes + sl * kDecRows * 128, &vmap, sl * 64, h, row0 + i * kDecRows, &full[i]);
+      }
+    }
   }
   // ---- query rows of the group, zero-padded to 16 heads
   for (int c = tid; c < kDecMaxGroup * (D / 8); c += kDecThreads) {
@@ -143,32 +178,37 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   }
   __syncthreads();
   const int row0 = ctl[0], nrows = ctl[1];
+  const bool ok = ctl[2] != 0;
+  const bool has_new = a.k_new != nullptr && ok;
   const int ntiles = (nrows + kDecRows - 1) / kDecRows;
 
   if (warp == kDecWarps) {
-    // ---- producer: one elected lane streams the K/V tiles
+    // ---- producer: the remaining tiles, each into the stage its predecessor freed
     if (lane == 0) {
-      for (int i = 0; i < ntiles; ++i) {
+      for (int i = C::kStages; i < ntiles; ++i) {
         const int st = i % C::kStages;
-        if (i >= C::kStages && !mbar_wait(&empty[st], ((i / C::kStages) - 1) & 1)) {
+        if (!mbar_wait(&empty[st], ((i / C::kStages) - 1) & 1)) {
           set_error(a.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
           break;
         }
         fence_proxy_async_smem();  // the consumers' generic reads of this stage come first
         const uint32_t kb = smem_u32(ring + st * C::kStageBytes);
-        const uint32_t vb = kb + C::kTileBytes;
         mbar_arrive_expect_tx(&full[st], C::kStageBytes);
         const int r = row0 + i * kDecRows;
 #pragma unroll
         for (int sl = 0; sl < C::kSlabs; ++sl) {
           tma_load_3d(kb + sl * kDecRows * 128, &kmap, sl * 64, h, r, &full[st]);
-          tma_load_3d(vb + sl * kDecRows * 128, &vmap, sl * 64, h, r, &full[st]);
+          tma_load_3d(kb + C::kTileBytes + sl * kDecRows * 128, &vmap, sl * 64, h, r, &full[st]);
         }
       }
     }
+    __syncwarp();
+    if (CL) {  // the two cluster barriers of the slice merge below
+      cluster_sync_all();
+      cluster_sync_all();
+    }
     return;
   }
-
   // ---- consumers
   const int hA = lane >> 2;  // heads of this thread's accumulator rows: hA and hA + 8
   const int cq = lane & 3;
@@ -230,9 +270,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       for (int t = 0; t < 2; ++t) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const bool ok = 8 * t + 2 * cq + e < valid;
-          sc[t][e] = ok ? sc[t][e] * a.scale_log2 : -INFINITY;
-          sc[t][2 + e] = ok ? sc[t][2 + e] * a.scale_log2 : -INFINITY;
+          const bool in = 8 * t + 2 * cq + e < valid;
+          sc[t][e] = in ? sc[t][e] * a.scale_log2 : -INFINITY;
+          sc[t][2 + e] = in ? sc[t][2 + e] * a.scale_log2 : -INFINITY;
           tA = fmaxf(tA, sc[t][e]);
           tB = fmaxf(tB, sc[t][2 + e]);
         }
@@ -281,7 +321,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
     if (lane == 0) mbar_arrive(&empty[st]);
   }
 
-  // ---- merge the four warps' (max, sum, O) into the slice's partial
+  // ---- merge the four warps' (max, sum, O)
   lA += __shfl_xor_sync(0xffffffffu, lA, 1);
   lA += __shfl_xor_sync(0xffffffffu, lA, 2);
   lB += __shfl_xor_sync(0xffffffffu, lB, 1);
@@ -302,6 +342,20 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
     lw[warp * kDecMaxGroup + hA] = lA;
     lw[warp * kDecMaxGroup + hA + 8] = lB;
   }
+  const bool single = !CL && a.n_split == 1;
+  const int rank = blockIdx.x;  // rank in the cluster (CL): the cluster spans the slices
+  if (has_new && (single || CL)) {
+    // the new row's base-2 logit per query head (one warp per head)
+    for (int hh = warp; hh < g; hh += kDecWarps) {
+      float dot = 0.f;
+      const __nv_bfloat16* qh = qs + hh * C::kQPitch;
+      const __nv_bfloat16* kn = a.k_new + (int64_t)s * a.new_stride_seq + (int64_t)h * a.new_stride_head;
+      for (int d = lane; d < D; d += 32) dot += __bfloat162float(qh[d]) * __bfloat162float(kn[d]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+      if (lane == 0) xnew[hh] = dot * a.scale_log2;
+    }
+  }
   named_bar_sync(1, kDecWarps * 32);
   const int64_t head0 = (int64_t)s * a.h_q + (int64_t)h * g;  // first query head of the group
   for (int idx = tid; idx < g * D; idx += kDecWarps * 32) {
@@ -321,9 +375,100 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         }
       }
     }
-    const int64_t slot = (head0 + hh) * a.n_split + split;
-    a.part_o[slot * D + d] = osum;
-    if (d == 0) a.part_ml[slot] = make_float2(m, lsum);
+    if (single) {
+      // the whole sequence is this slice: finish here
+      float onum = osum, den = lsum;
+      if (has_new) {
+        const float xn = xnew[hh];
+        const float top = fmaxf(m, xn);
+        const float c = m == -INFINITY ? 0.f : fast_exp2(m - top);
+        const float cn = fast_exp2(xn - top);
+        const __nv_bfloat16* vn = a.v_new + (int64_t)s * a.new_stride_seq + (int64_t)h * a.new_stride_head;
+        onum = c * osum + cn * __bfloat162float(vn[d]);
+        den = c * lsum + cn;
+      }
+      a.out[(head0 + hh) * D + d] = (ok && den > 0.f) ? onum / den : 0.f;
+    } else if (CL) {
+      pbuf[hh * D + d] = osum;
+      if (d == 0) pml[hh] = make_float2(m, lsum);
+    } else {
+      const int64_t slot = (head0 + hh) * a.n_split + split;
+      a.part_o[slot * D + d] = osum;
+      if (d == 0) a.part_ml[slot] = make_float2(m, lsum);
+    }
+  }
+  if (single) return;
+  if (CL) {
+    // ---- slices of one cluster: every rank reads all ranks' (max, sum),
+    // then merges its share of the output columns straight from the ranks'
+    // shared memory
+    cluster_sync_all();
+    const int nsp = a.n_split;
+    for (int i = tid; i < g * nsp; i += kDecWarps * 32) {
+      const int hh = i / nsp, x = i % nsp;
+      const uint32_t ad = cluster_map(smem_u32(pml + hh), (uint32_t)x);
+      mlbuf[hh * kDecMaxSplit + x] = make_float2(ld_cluster_f32(ad), ld_cluster_f32(ad + 4));
+    }
+    named_bar_sync(1, kDecWarps * 32);
+    for (int hh = warp; hh < g; hh += kDecWarps) {
+      const float xn = has_new ? xnew[hh] : -INFINITY;
+      float m = xn;
+      for (int x = lane; x < nsp; x += 32) m = fmaxf(m, mlbuf[hh * kDecMaxSplit + x].x);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      float lsum = 0.f;
+      for (int x = lane; x < nsp; x += 32) {
+        const float2 ml = mlbuf[hh * kDecMaxSplit + x];
+        const float c = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - m);
+        coef[hh * kDecMaxSplit + x] = c;
+        lsum += c * ml.y;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
+      if (lane == 0) {
+        const float cn = has_new ? fast_exp2(xn - m) : 0.f;
+        cnew[hh] = cn;
+        lsum += cn;
+        rnorm[hh] = (ok && lsum > 0.f) ? 1.f / lsum : 0.f;
+      }
+    }
+    named_bar_sync(1, kDecWarps * 32);
+    constexpr int kC4 = D / 4;
+    for (int j = rank + nsp * tid; j < g * kC4; j += nsp * kDecWarps * 32) {
+      const int hh = j / kC4, c4 = j % kC4;
+      const uint32_t base = smem_u32(pbuf + hh * D + 4 * c4);
+      float4 v[kDecMaxCluster];
+#pragma unroll
+      for (int x = 0; x < kDecMaxCluster; ++x) {
+        v[x] = x < nsp ? ld_cluster_f32x4(cluster_map(base, (uint32_t)x)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int x = 0; x < kDecMaxCluster; ++x) {
+        const float c = x < nsp ? coef[hh * kDecMaxSplit + x] : 0.f;
+        acc.x += c * v[x].x;
+        acc.y += c * v[x].y;
+        acc.z += c * v[x].z;
+        acc.w += c * v[x].w;
+      }
+      if (has_new) {
+        const __nv_bfloat16* vn =
+            a.v_new + (int64_t)s * a.new_stride_seq + (int64_t)h * a.new_stride_head + 4 * c4;
+        const float cn = cnew[hh];
+        acc.x += cn * __bfloat162float(vn[0]);
+        acc.y += cn * __bfloat162float(vn[1]);
+        acc.z += cn * __bfloat162float(vn[2]);
+        acc.w += cn * __bfloat162float(vn[3]);
+      }
+      const float rn = rnorm[hh];
+      float* o4 = a.out + (head0 + hh) * D + 4 * c4;
+      o4[0] = acc.x * rn;
+      o4[1] = acc.y * rn;
+      o4[2] = acc.z * rn;
+      o4[3] = acc.w * rn;
+    }
+    cluster_sync_all();  // the partials stay readable until every rank is done
+    return;
   }
   __threadfence();
   named_bar_sync(1, kDecWarps * 32);
@@ -335,27 +480,31 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   if (!ctl[3]) return;
 
   // ---- last slice of this (sequence, KV head): merge the slices and the new row
+  if (tid == 0) a.count[(int64_t)s * a.h_kv + h] = 0;  // every call leaves the counters at zero
   __threadfence();
-  const bool ok = ctl[2] != 0;
-  const bool has_new = a.k_new != nullptr && ok;
-  for (int hh = warp; hh < g; hh += kDecWarps) {
-    float xn = -INFINITY;
-    if (has_new) {
-      float dot = 0.f;
-      const __nv_bfloat16* qh = qs + hh * C::kQPitch;
-      const __nv_bfloat16* kn = a.k_new + (int64_t)s * a.new_stride_seq + (int64_t)h * a.new_stride_head;
-      for (int d = lane; d < D; d += 32) dot += __bfloat162float(qh[d]) * __bfloat162float(kn[d]);
+  for (int i = tid; i < g * a.n_split; i += kDecWarps * 32) {
+    const int hh = i / a.n_split, x = i % a.n_split;
+    mlbuf[hh * kDecMaxSplit + x] = __ldcg(&a.part_ml[(head0 + hh) * a.n_split + x]);
+  }
+  for (int hh = warp; hh < g && has_new; hh += kDecWarps) {
+    float dot = 0.f;
+    const __nv_bfloat16* qh = qs + hh * C::kQPitch;
+    const __nv_bfloat16* kn = a.k_new + (int64_t)s * a.new_stride_seq + (int64_t)h * a.new_stride_head;
+    for (int d = lane; d < D; d += 32) dot += __bfloat162float(qh[d]) * __bfloat162float(kn[d]);
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-      xn = dot * a.scale_log2;
-    }
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (lane == 0) xnew[hh] = dot * a.scale_log2;
+  }
+  named_bar_sync(1, kDecWarps * 32);
+  for (int hh = warp; hh < g; hh += kDecWarps) {
+    const float xn = has_new ? xnew[hh] : -INFINITY;
     float m = xn;
-    for (int x = lane; x < a.n_split; x += 32) m = fmaxf(m, __ldcg(&a.part_ml[(head0 + hh) * a.n_split + x]).x);
+    for (int x = lane; x < a.n_split; x += 32) m = fmaxf(m, mlbuf[hh * kDecMaxSplit + x].x);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     float lsum = 0.f;
     for (int x = lane; x < a.n_split; x += 32) {
-      const float2 ml = __ldcg(&a.part_ml[(head0 + hh) * a.n_split + x]);
+      const float2 ml = mlbuf[hh * kDecMaxSplit + x];
       const float c = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - m);
       coef[hh * kDecMaxSplit + x] = c;
       lsum += c * ml.y;
@@ -364,22 +513,43 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
     for (int off = 16; off > 0; off >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, off);
     if (lane == 0) {
       const float cn = has_new ? fast_exp2(xn - m) : 0.f;
-      xnew[hh] = cn;
+      cnew[hh] = cn;
       lsum += cn;
       rnorm[hh] = (ok && lsum > 0.f) ? 1.f / lsum : 0.f;
     }
   }
   named_bar_sync(1, kDecWarps * 32);
+  // slices split across thread groups (float4 columns x slice groups): every
+  // slice's partial is finite (empty slices wrote zeros), so the loads need no
+  // condition and issue back to back
+  constexpr int kD4 = D / 4;
+  constexpr int kXG = kDecWarps * 32 / kD4;
+  const int d4 = tid % kD4, xg = tid / kD4;
+  float4* red = reinterpret_cast<float4*>(ring);  // [kXG][16][kD4]
+  for (int hh = 0; hh < g; ++hh) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4* src = reinterpret_cast<const float4*>(a.part_o + (head0 + hh) * a.n_split * D) + d4;
+#pragma unroll 4
+    for (int x = xg; x < a.n_split; x += kXG) {
+      const float c = coef[hh * kDecMaxSplit + x];
+      const float4 pv = __ldcg(src + (int64_t)x * kD4);
+      acc.x += c * pv.x;
+      acc.y += c * pv.y;
+      acc.z += c * pv.z;
+      acc.w += c * pv.w;
+    }
+    red[(xg * kDecMaxGroup + hh) * kD4 + d4] = acc;
+  }
+  named_bar_sync(1, kDecWarps * 32);
   for (int idx = tid; idx < g * D; idx += kDecWarps * 32) {
     const int hh = idx / D, d = idx % D;
+    const float* rf = reinterpret_cast<const float*>(red);
     float acc = 0.f;
-    for (int x = 0; x < a.n_split; ++x) {
-      const float c = coef[hh * kDecMaxSplit + x];
-      if (c != 0.f) acc += c * __ldcg(&a.part_o[((head0 + hh) * a.n_split + x) * D + d]);
-    }
+#pragma unroll
+    for (int x = 0; x < kXG; ++x) acc += rf[(x * kDecMaxGroup + hh) * D + d];
     if (has_new) {
       const __nv_bfloat16* vn = a.v_new + (int64_t)s * a.new_stride_seq + (int64_t)h * a.new_stride_head;
-      acc += xnew[hh] * __bfloat162float(vn[d]);
+      acc += cnew[hh] * __bfloat162float(vn[d]);
     }
     a.out[(head0 + hh) * D + d] = acc * rnorm[hh];
   }
@@ -388,6 +558,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
 // ------------------------------------------------------------------ host
 
 struct DecPlan {
+  bool cluster;  // slices merge inside a thread-block cluster
   int d, g, n_split;
   size_t zero_bytes, ml_off, o_off, total;
 };
@@ -415,12 +586,21 @@ int decode_plan(const aircache_decode_problem* p, DecPlan& pl) {
   pl.d = p->head_dim;
   pl.g = p->h_q / p->h_kv;
   const long long pairs = (long long)p->num_seqs * p->h_kv;
-  const long long target = 2LL * sms;  // two CTAs resident per SM
-  long long want = pairs > 0 ? (target + pairs - 1) / pairs : 1;
-  const long long cap = (p->max_rows + kDecRows - 1) / kDecRows;
-  if (want > cap) want = cap;
-  if (want < 1) want = 1;
-  if (want > kDecMaxSplit) want = kDecMaxSplit;
+  // At most one wave of two resident CTAs per SM.  Slices of one (sequence,
+  // KV head) form a thread-block cluster (up to 8) and merge through
+  // distributed shared memory, which costs about a microsecond, so slices may
+  // be as short as 128 rows.  Only long ranges over few (sequence, head) pairs
+  // go wider than 8 slices; those merge through global memory (a fence, an
+  // atomic, a reload: a few microseconds), with slices of at least 512 rows.
+  const long long per_pair = pairs > 0 ? 2LL * sms / pairs : 1;
+  auto clampll = [](long long x, long long lo, long long hi) { return x < lo ? lo : (x > hi ? hi : x); };
+  long long want = clampll(std::min<long long>(per_pair, (p->max_rows + 127) / 128), 1, kDecMaxCluster);
+  pl.cluster = want > 1;
+  const long long wide = std::min<long long>(per_pair, (p->max_rows + 511) / 512);
+  if (wide > kDecMaxCluster) {
+    want = std::min<long long>(wide, kDecMaxSplit);
+    pl.cluster = false;
+  }
   pl.n_split = (int)want;
   const size_t slots = (size_t)p->num_seqs * p->h_q * pl.n_split;
   pl.zero_bytes = kDecZeroBlock + round256(sizeof(uint32_t) * (size_t)pairs);
@@ -468,8 +648,28 @@ int launch_decode(const aircache_decode_problem* p, const DecPlan& pl, uint8_t* 
   a.n_split = pl.n_split;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   const int smem = DecCfg<D>::kSmem;
-  if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D>), smem) != cudaSuccess) return AIRCACHE_ERR_CUDA;
-  decode_kernel<D><<<dim3(pl.n_split, p->h_kv, p->num_seqs), kDecThreads, smem, s>>>(km, vm, a);
+  const dim3 grid(pl.n_split, p->h_kv, p->num_seqs);
+  if (pl.cluster) {
+    if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D, true>), smem) != cudaSuccess)
+      return AIRCACHE_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pl.n_split;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, decode_kernel<D, true>, km, vm, a) != cudaSuccess) return AIRCACHE_ERR_CUDA;
+  } else {
+    if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D, false>), smem) != cudaSuccess)
+      return AIRCACHE_ERR_CUDA;
+    decode_kernel<D, false><<<grid, kDecThreads, smem, s>>>(km, vm, a);
+  }
   return cudaGetLastError() == cudaSuccess ? AIRCACHE_OK : AIRCACHE_ERR_CUDA;
 }
 
@@ -498,7 +698,6 @@ int aircache_decode(const aircache_decode_problem* p, void* ws, size_t ws_bytes,
   if (ws_bytes < pl.total) return AIRCACHE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  if (cudaMemsetAsync(w, 0, pl.zero_bytes, s) != cudaSuccess) return AIRCACHE_ERR_CUDA;
   if (p->num_seqs == 0) return AIRCACHE_OK;
   return pl.d == 128 ? launch_decode<128>(p, pl, w, s) : launch_decode<64>(p, pl, w, s);
 }

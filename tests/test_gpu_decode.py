@@ -94,7 +94,7 @@ def test_decode_matches_oracle_ragged(A, oracle, h_q, h_kv, d):
     check_against_oracle(oracle, di, out)
 
 
-@pytest.mark.parametrize("max_rows", [0, 64, 5000, 10 ** 6])
+@pytest.mark.parametrize("max_rows", [0, 64, 300, 1000, 5000, 10 ** 6])
 def test_split_count_does_not_change_results_beyond_rounding(A, oracle, max_rows):
     # the hint only moves the split points
     di = W.decode_inputs([700, 33, 4100], 28, 4, 128, seed=2, device="cuda", q_scale=2.0)
@@ -184,10 +184,30 @@ def test_out_of_bounds_range_sets_the_error_word(A, oracle):
     out = prob.out.cpu().numpy().astype(np.float64)
     assert np.all(out[1] == 0.0)
     check_against_oracle(oracle, di, out, seqs=[0])
-    # the next call on the same workspace starts clean
+    # the error stays recorded until the caller zeroes the workspace
     prob2 = A.DecodeProblem(di.q, di.k, di.v, offsets=di.offsets, max_rows=20)
     A.aircache_decode(prob2, ws)
+    assert A.aircache_get_error(ws) == A.ERR_DEVICE_BOUNDS
+    ws.zero_()
+    A.aircache_decode(prob2, ws)
     assert A.aircache_get_error(ws) == A.OK
+    check_against_oracle(oracle, di, prob2.out.cpu().numpy().astype(np.float64))
+
+
+def test_workspace_reused_across_calls_and_split_modes(A, oracle):
+    # one zeroed workspace serves calls in every merge mode back to back (the
+    # global-merge counters reset themselves)
+    di = W.decode_inputs([3000, 50, 7000], 28, 4, 128, seed=14, device="cuda", q_scale=2.0)
+    probs = [A.DecodeProblem(di.q, di.k, di.v, offsets=di.offsets, max_rows=m) for m in (0, 1000, 10 ** 6)]
+    assert [p.splits() for p in probs][0] == 1 and probs[2].splits() > 8
+    ws = torch.zeros(max(p.workspace_size() for p in probs), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        for p in probs:
+            A.aircache_decode(p, ws)
+    assert A.aircache_get_error(ws) == A.OK
+    assert int(ws[256:512].view(torch.int32).abs().sum()) == 0
+    for p in probs:
+        check_against_oracle(oracle, di, p.out.cpu().numpy().astype(np.float64))
 
 
 def test_decode_over_the_compressed_arena(A, oracle):
