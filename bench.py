@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--decode-configs", default="8x2048,8x32768,16x16384",
                     help="comma-separated BATCHxPROMPT list for --decode")
     ap.add_argument("--decode-ratios", default="0.1,0.5", help="retention ratios r for --decode")
+    ap.add_argument("--decode-layers", type=int, default=28,
+                    help="layers of the decode workload (28 = the 7B shape; fewer only for small profiling runs)")
     return ap.parse_args()
 
 
@@ -79,25 +81,35 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_sources_hash():
+KERNEL_SOURCES = {"score_pass1": "stream.cu", "decode_kernel": "decode.cu"}
+
+
+def kernel_sources_hash(kernel):
+    """Hash of the translation unit that holds `kernel`, every shared header and
+    the C ABI header: what the kernel's DRAM traffic depends on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "lvlm_kv_cache_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+    files = [os.path.join(csrc, KERNEL_SOURCES.get(kernel, ""))]
+    files += [os.path.join(csrc, f) for f in sorted(os.listdir(csrc)) if f.endswith(".cuh")]
+    files.append(os.path.join(ROOT, "include", "aircache.h"))
+    for f in files:
+        if not os.path.isfile(f):
+            return None
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(config, kernel):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources."""
+    the current sources of that kernel."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     e = d.get(config, {}).get(kernel)
-    if not e or e.get("sources") != kernel_sources_hash():
+    if not e or e.get("sources") != kernel_sources_hash(kernel):
         return None
     return float(e["dram_bytes_per_launch_full"])
 
@@ -243,7 +255,7 @@ def oracle_sample(wl, budget_s, device_for_copy=None, window_mode=0, budget_mode
 
 # ------------------------------------------------------------------ decode consumer
 
-DECODE_METRIC = "decode attention step time (all 28 layers, one new token per request), full vs compressed cache"
+DECODE_METRIC = "decode attention step time (every layer, one new token per request), full vs compressed cache"
 
 
 def decode_oracle_sample(q, ranges, budget_s):
@@ -299,7 +311,7 @@ def run_decode(args, local):
         B, P = (int(x) for x in cfg.lower().split("x"))
         n_t = 128
         base = W.spec("7b")
-        spec = dataclasses.replace(base, B=B, n_visual=[P - n_t] * B, n_text=[n_t] * B)
+        spec = dataclasses.replace(base, B=B, L=args.decode_layers, n_visual=[P - n_t] * B, n_text=[n_t] * B)
         wl = W.generate(spec, seed=0, device=dev)
         L, H_q, H_kv, D = spec.L, spec.H_q, spec.H_kv, spec.D
         gen = torch.Generator(device=dev)
@@ -372,15 +384,17 @@ def run_decode(args, local):
             "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": max(args.warmup, 3),
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"7B LVLM-shaped decode: batch {B}, prompt {P} ({P - n_t} visual + {n_t} text), "
-                                   f"L=28, H_q=28, H_kv=4, D=128, bf16; caches from aircache_compress",
+                                   f"L={L}, H_q=28, H_kv=4, D=128, bf16; caches from aircache_compress",
                        "batch": B, "prompt": P,
-                       "step": "28 aircache_decode calls (one per layer, num_seqs = batch) replayed as a CUDA graph",
+                       "step": f"{L} aircache_decode calls (one per layer, num_seqs = batch) replayed as a CUDA graph",
                        "l2": "flushed before every timed step outside the events"},
             "full": {"ms": full_ms, "rows": full_rows, "algorithmic_bytes": full_bytes, "gbs": full_gbs,
                      "frac": full_gbs / peak, "splits": full_probs[0].splits()},
             "compressed": results,
             "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": full_gbs, "peak": peak,
-                         "unit": "GB/s", "frac": full_gbs / peak, "peak_kind": peak_kind, "traffic": None},
+                         "unit": "GB/s", "frac": full_gbs / peak, "peak_kind": peak_kind,
+                         "traffic": recorded_traffic(f"decode_{B}x{P}", "decode_kernel"),
+                         "note": "full-cache step: one decode_kernel launch per layer, bytes and time per launch"},
             "gpu_launches": L,
             "clocks": clocks,
         }
