@@ -47,6 +47,16 @@
  *   R16 a decode step (the consumer of the compacted cache) is plain softmax
  *       attention of the step's query over every cached row, per query head,
  *       with the head map of R1 and no mask.
+ *   R17 int8 storage of the kept cache (LLM KV-compression notes, section
+ *       "Quantization stacked on compression": quantise after the token
+ *       compression, one scale per head = the head's largest |value| over the
+ *       quantisation range; KV-cache tutorial page, section "Quantization":
+ *       symmetric q = clip(round(x/s), q_min, q_max), x_hat = s q).  Per
+ *       compacted unit (layer, request), per KV head, K and V separately:
+ *       s = max|x| / 127 over the unit's rows and the head's D values,
+ *       q = clip(round(x / s), -127, 127) with round half away from zero;
+ *       s and x / s are evaluated in fp32 (the precision that decides the
+ *       integer code on the device too); an all-zero head has s = 0, q = 0.
  *
  * Element access: tensors are token-major [tokens][heads][D] with explicit
  * element strides for the token and head axes and D contiguous; the element
@@ -484,5 +494,42 @@ int oracle_decode(const oracle_view* q, const oracle_view* k, const oracle_view*
         }
     }
     free(w);
+    return 0;
+}
+
+/* ------------------------------------------------------- int8 kept cache */
+
+/* The elementary symmetric step of R17 for one value: clip(round(x / s)),
+ * x / s in fp32, half away from zero; s == 0 gives 0. */
+int oracle_quant_code(float x, float s) {
+    if (s == 0.0f) return 0;
+    const float t = x / s;
+    float r = roundf(t);
+    if (r > 127.0f) r = 127.0f;
+    if (r < -127.0f) r = -127.0f;
+    return (int)r;
+}
+
+/*
+ * R17 over one compacted unit: rows 0..n_rows-1 of `src` ([rows][H_kv][D]).
+ * codes: [n_rows][h_kv][d] int8, dense; scales: [h_kv] fp32 (s of each head).
+ * returns 0, or -1 on bad arguments.
+ */
+int oracle_quantize_int8(const oracle_view* src, int64_t n_rows, int h_kv, int d, int8_t* codes,
+                         float* scales) {
+    if (n_rows < 0 || h_kv <= 0 || d <= 0) return -1;
+    for (int h = 0; h < h_kv; ++h) {
+        float big = 0.0f;
+        for (int64_t j = 0; j < n_rows; ++j)
+            for (int i = 0; i < d; ++i) {
+                const float a = fabsf((float)elem(src, j, h, i));
+                if (a > big) big = a;
+            }
+        const float s = big / 127.0f;
+        scales[h] = s;
+        for (int64_t j = 0; j < n_rows; ++j)
+            for (int i = 0; i < d; ++i)
+                codes[(j * h_kv + h) * d + i] = (int8_t)oracle_quant_code((float)elem(src, j, h, i), s);
+    }
     return 0;
 }

@@ -35,6 +35,9 @@ int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t
                        const int32_t* idx, int keep, void* dst);
 int oracle_decode(const oracle_view* q, const oracle_view* k, const oracle_view* v, int h_q, int h_kv,
                   int d, int64_t n_rows, double* out);
+int oracle_quant_code(float x, float s);
+int oracle_quantize_int8(const oracle_view* src, int64_t n_rows, int h_kv, int d, int8_t* codes,
+                         float* scales);
 int oracle_window(int n_t, int mode, int32_t* positions);
 int oracle_budget_variant(const double* s_t, const double* s_k, int n_layers, int n_v, double r,
                           int mode, double* r_l, int32_t* keep);

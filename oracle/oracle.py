@@ -78,6 +78,10 @@ def lib():
         L.oracle_request.restype = i32
         L.oracle_decode.argtypes = [V, V, V, i32, i32, i32, i64, vp]
         L.oracle_decode.restype = i32
+        L.oracle_quant_code.argtypes = [ctypes.c_float, ctypes.c_float]
+        L.oracle_quant_code.restype = i32
+        L.oracle_quantize_int8.argtypes = [V, i64, i32, i32, vp, vp]
+        L.oracle_quantize_int8.restype = i32
         L.oracle_window.argtypes = [i32, i32, vp]
         L.oracle_window.restype = i32
         L.oracle_budget_variant.argtypes = [vp, vp, i32, i32, f64, i32, vp, vp]
@@ -99,6 +103,8 @@ def _view(a: np.ndarray) -> _View:
     else:
         raise TypeError("oracle arrays are float32 or uint16 (bf16 bits)")
     es = a.itemsize
+    if a.size == 0:  # no element is read: any strides will do
+        return _View(a.ctypes.data, dt, 0, a.shape[1] * a.shape[2], a.shape[2])
     if a.strides[2] != es:
         raise ValueError("D must be contiguous")
     return _View(a.ctypes.data, dt, 0, a.strides[0] // es, a.strides[1] // es)
@@ -171,6 +177,23 @@ def decode(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle_decode rejected its arguments")
     return out
+
+
+def quant_code(x: float, s: float) -> int:
+    """The symmetric int8 step clip(round(x / s), -127, 127) in fp32 (reading R17)."""
+    return int(lib().oracle_quant_code(float(x), float(s)))
+
+
+def quantize_int8(src: np.ndarray):
+    """Per-head int8 codes of one compacted unit src [rows, H_kv, D] (fp32 or
+    bf16 bits).  Returns (codes int8 [rows, H_kv, D], scales fp32 [H_kv])."""
+    rows, h_kv, d = src.shape
+    codes = np.zeros((rows, h_kv, d), np.int8)
+    scales = np.zeros(h_kv, np.float32)
+    rc = lib().oracle_quantize_int8(ctypes.byref(_view(src)), rows, h_kv, d, _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise ValueError("oracle_quantize_int8 rejected its arguments")
+    return codes, scales
 
 
 def window(n_t: int, mode: int) -> np.ndarray:

@@ -43,8 +43,13 @@ MUTATIONS = {
                                   "for (int64_t j = 0; j + 1 < n_rows; ++j) acc +="),
     "decode logits unscaled": ("w[j] = scaled_dot(q, 0, h, k, j, kv_head, d);",
                                "w[j] = scaled_dot(q, 0, h, k, j, kv_head, d) * sqrt((double)d);"),
+    "quantization rounds half to even": ("float r = roundf(t);", "float r = rintf(t);"),
+    "quantization truncates": ("float r = roundf(t);", "float r = truncf(t);"),
+    "quantization range 128": ("const float s = big / 127.0f;", "const float s = big / 128.0f;"),
+    "one head's scale for every head": ("const float a = fabsf((float)elem(src, j, h, i));",
+                                        "const float a = fabsf((float)elem(src, j, 0, i));"),
 }
-PIN_FILES = ["test_oracle_pins.py", "test_oracle_variants.py", "test_oracle_decode.py"]
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_variants.py", "test_oracle_decode.py", "test_oracle_quant.py"]
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
