@@ -76,7 +76,7 @@ typedef enum {
     AIRCACHE_ERR_CAPACITY = -8         /* device: output arena smaller than the compacted rows */
 } aircache_status;
 
-typedef enum { AIRCACHE_F32 = 0, AIRCACHE_BF16 = 1 } aircache_dtype;
+typedef enum { AIRCACHE_F32 = 0, AIRCACHE_BF16 = 1, AIRCACHE_INT8 = 2 } aircache_dtype;
 
 /*
  * One compression problem: B requests, L layers.  All fields are read on the
@@ -278,12 +278,17 @@ AIRCACHE_API const char* aircache_kernel_name(const aircache_problem* p, int i);
  *   k_new, v_new [num_seqs][h_kv][head_dim]  new_stride_seq, new_stride_head
  *   out    [num_seqs][h_q][head_dim]    fp32, dense
  *   row_begin, row_end: device int64 [num_seqs].
+ * With kv_dtype AIRCACHE_INT8 the cached rows are int8 codes c with
+ * k_j = k_scale[s][h] * c_j (and likewise v); the kernel computes with the codes
+ * exactly and applies the scales to the logits and to the weighted sum, so the
+ * result is the attention over the dequantised rows (the new row stays bf16).
  * Requirements (else AIRCACHE_ERR_INVALID_ARG, or AIRCACHE_ERR_UNSUPPORTED
- * for the dtype / group limits): dtype AIRCACHE_BF16; head_dim 64 or 128;
+ * for the dtype / group limits): dtype AIRCACHE_BF16; kv_dtype AIRCACHE_BF16
+ * or AIRCACHE_INT8 (then k_scale and v_scale given); head_dim 64 or 128;
  * h_q % h_kv == 0 and h_q / h_kv <= 16; k and v 16-byte aligned with
- * kv_stride_row and kv_stride_head multiples of 8 elements (tensor-map rules);
+ * kv_stride_row and kv_stride_head multiples of 16 bytes (tensor-map rules);
  * 1 <= kv_rows <= 2^31 - 2^16; num_seqs <= 65535; q 16-byte aligned with
- * q_stride_seq and q_stride_head multiples of 8; max_rows >= 0; reserved0 == 0.
+ * q_stride_seq and q_stride_head multiples of 8; max_rows >= 0.
  * max_rows is a hint, not a limit: the expected longest range, which sizes the
  * split of each sequence across CTAs (and the workspace).  Device-side, a
  * range with row_begin < 0, row_end < row_begin or row_end > kv_rows sets
@@ -295,8 +300,9 @@ typedef struct aircache_decode_problem {
     int32_t h_q;
     int32_t h_kv;
     int32_t head_dim;
-    int32_t dtype;
-    int32_t reserved0;
+    int32_t dtype;     /* of q (and of k_new, v_new): AIRCACHE_BF16 */
+    int32_t kv_dtype;  /* of the cached rows k, v: AIRCACHE_BF16, or AIRCACHE_INT8 (codes of
+                          aircache_quantize_int8, with k_scale / v_scale) */
     int64_t kv_rows;
     int64_t max_rows;
     const void* q;
@@ -313,6 +319,9 @@ typedef struct aircache_decode_problem {
     int64_t new_stride_seq;
     int64_t new_stride_head;
     float* out;
+    const float* k_scale;  /* AIRCACHE_INT8 only: [num_seqs][h_kv] fp32 scales of the codes of */
+    const float* v_scale;  /* sequence s, KV head h (for the compacted arena of layer l: the
+                              aircache_quantize_int8 scales + l*B*h_kv) */
 } aircache_decode_problem;
 
 /* Workspace bytes aircache_decode needs for `p` on the current device, or 0 if
@@ -334,6 +343,53 @@ AIRCACHE_API int aircache_decode(const aircache_decode_problem* p, void* ws, siz
 /* Number of CTAs the decode kernel splits each (sequence, KV head) into for `p`
  * on the current device, or -1 if `p` is invalid (for measurement). */
 AIRCACHE_API int aircache_decode_splits(const aircache_decode_problem* p);
+
+/* ------------------------------------------------------------- int8 storage */
+
+/*
+ * int8 storage of a compacted cache, applied after the token compression (LLM
+ * KV-compression notes, section "Quantization stacked on compression":
+ * quantise after compressing, with one scale per head taken from the head's
+ * largest |value| over the quantisation range; KV-cache tutorial page, section
+ * "Quantization": symmetric q = clip(round(x / s), q_min, q_max), x_hat = s q).
+ * For every unit u (rows offsets[u] .. offsets[u+1]-1) and KV head h,
+ * separately for K and V:
+ *   s = max |x| / 127 in fp32 over the unit's rows and the head's head_dim values;
+ *   q = clip(round(x / s), -127, 127), x / s in fp32 (correctly rounded),
+ *       round half away from zero; a head whose values are all 0 has s = 0, q = 0.
+ * The units of aircache_compress's arena are its (layer, request) pairs:
+ * offsets = out_offsets, num_units = L*B.
+ *
+ * Layout: k, v bf16 [rows][h_kv][head_dim] (kv_stride_row, kv_stride_head
+ * element strides); k8, v8 int8 dense [rows][h_kv][head_dim] (same row
+ * numbering); k_scale, v_scale fp32 [num_units][h_kv]; offsets device int64
+ * [num_units + 1].  Requirements (else AIRCACHE_ERR_INVALID_ARG): head_dim 64
+ * or 128, dtype AIRCACHE_BF16, k and v 16-byte aligned with strides multiples
+ * of 8 elements, k8 and v8 16-byte aligned, 1 <= rows, 0 <= num_units <= 2^31/4,
+ * reserved0 == 0.  `status` (optional device int32) is cleared first, then
+ * receives AIRCACHE_ERR_DEVICE_BOUNDS if a unit's range lies outside [0, rows)
+ * (that unit is skipped).  One memset (when status is given) and one kernel.
+ */
+typedef struct aircache_quant_problem {
+    int32_t num_units;
+    int32_t h_kv;
+    int32_t head_dim;
+    int32_t dtype;
+    int32_t reserved0;
+    int32_t reserved1;
+    int64_t rows;
+    const void* k;
+    const void* v;
+    int64_t kv_stride_row;
+    int64_t kv_stride_head;
+    const int64_t* offsets;
+    int8_t* k8;
+    int8_t* v8;
+    float* k_scale;
+    float* v_scale;
+} aircache_quant_problem;
+
+AIRCACHE_API int aircache_quantize_int8(const aircache_quant_problem* p, int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -29,7 +29,7 @@ ERR_DEVICE_BOUNDS = -6
 ERR_ELITE_OVERFLOW = -7
 ERR_CAPACITY = -8
 
-F32, BF16 = 0, 1
+F32, BF16, INT8 = 0, 1, 2
 MAX_LAYERS = 256
 
 
@@ -73,7 +73,7 @@ _lib = None
 class DecodeProblemStruct(ctypes.Structure):
     _fields_ = [
         ("num_seqs", ctypes.c_int32), ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
-        ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32), ("dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
         ("kv_rows", ctypes.c_int64), ("max_rows", ctypes.c_int64),
         ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
         ("row_begin", ctypes.c_void_p), ("row_end", ctypes.c_void_p),
@@ -81,7 +81,18 @@ class DecodeProblemStruct(ctypes.Structure):
         ("q_stride_seq", ctypes.c_int64), ("q_stride_head", ctypes.c_int64),
         ("kv_stride_row", ctypes.c_int64), ("kv_stride_head", ctypes.c_int64),
         ("new_stride_seq", ctypes.c_int64), ("new_stride_head", ctypes.c_int64),
-        ("out", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+    ]
+
+
+class QuantProblemStruct(ctypes.Structure):
+    _fields_ = [
+        ("num_units", ctypes.c_int32), ("h_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("reserved0", ctypes.c_int32), ("reserved1", ctypes.c_int32),
+        ("rows", ctypes.c_int64), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("kv_stride_row", ctypes.c_int64), ("kv_stride_head", ctypes.c_int64),
+        ("offsets", ctypes.c_void_p), ("k8", ctypes.c_void_p), ("v8", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
     ]
 
 
@@ -122,6 +133,8 @@ def lib():
         L.aircache_compress_profile.restype = i32
         L.aircache_kernel_name.argtypes = [P, i32]
         L.aircache_kernel_name.restype = ctypes.c_char_p
+        L.aircache_quantize_int8.argtypes = [ctypes.POINTER(QuantProblemStruct), vp, vp]
+        L.aircache_quantize_int8.restype = i32
         DP = ctypes.POINTER(DecodeProblemStruct)
         L.aircache_decode_workspace_size.argtypes = [DP]
         L.aircache_decode_workspace_size.restype = sz
@@ -363,13 +376,14 @@ class DecodeProblem:
     """One decode step over cached rows (see aircache_decode in the header).
 
     q: [S, H_q, D] bf16 (one query row per sequence); k, v: arenas
-    [rows, H_kv, D] bf16; row_begin, row_end: int64 device tensors [S] (or one
-    offsets tensor [S+1] via ``offsets=``); k_new, v_new: optional [S, H_kv, D];
-    out: fp32 [S, H_q, D] (allocated when None).  max_rows: the expected
-    longest range (sizes the split; not a limit)."""
+    [rows, H_kv, D] bf16, or int8 codes with k_scale, v_scale [S, H_kv] fp32;
+    row_begin, row_end: int64 device tensors [S] (or one offsets tensor [S+1]
+    via ``offsets=``); k_new, v_new: optional [S, H_kv, D] bf16; out: fp32
+    [S, H_q, D] (allocated when None).  max_rows: the expected longest range
+    (sizes the split; not a limit)."""
 
     def __init__(self, q, k, v, row_begin=None, row_end=None, max_rows=0, k_new=None, v_new=None,
-                 out=None, offsets=None):
+                 out=None, offsets=None, k_scale=None, v_scale=None):
         if offsets is not None:
             row_begin, row_end = offsets[:-1], offsets[1:]
         S, h_q, d = (int(x) for x in q.shape)
@@ -385,11 +399,14 @@ class DecodeProblem:
             raise TypeError("row ranges are int64")
         if not out.is_contiguous() or tuple(out.shape) != (S, h_q, d) or out.dtype != torch.float32:
             raise ValueError("out must be a dense fp32 [S, H_q, D] tensor")
-        self.keep = (q, k, v, row_begin, row_end, k_new, v_new, out)
+        q8 = k.dtype == torch.int8
+        if q8 and (k_scale is None or v_scale is None or not k_scale.is_contiguous() or not v_scale.is_contiguous()):
+            raise ValueError("int8 caches need contiguous k_scale and v_scale [S, H_kv]")
+        self.keep = (q, k, v, row_begin, row_end, k_new, v_new, out, k_scale, v_scale)
         self.out = out
         self.c = DecodeProblemStruct(
             num_seqs=S, h_q=h_q, h_kv=h_kv, head_dim=d,
-            dtype=BF16 if q.dtype == torch.bfloat16 else F32, reserved0=0,
+            dtype=BF16 if q.dtype == torch.bfloat16 else F32, kv_dtype=INT8 if q8 else BF16,
             kv_rows=int(k.shape[0]), max_rows=int(max_rows),
             q=q.data_ptr(), k=k.data_ptr(), v=v.data_ptr(),
             row_begin=row_begin.data_ptr(), row_end=row_end.data_ptr(),
@@ -400,6 +417,7 @@ class DecodeProblem:
             new_stride_seq=k_new.stride(0) if k_new is not None else 0,
             new_stride_head=k_new.stride(1) if k_new is not None else 0,
             out=out.data_ptr(),
+            k_scale=k_scale.data_ptr() if q8 else None, v_scale=v_scale.data_ptr() if q8 else None,
         )
 
     @property
@@ -434,3 +452,33 @@ def decode(prob: DecodeProblem, ws=None, stream=None, check=True):
         if st != OK:
             raise AirCacheError(st, "aircache_decode (device)")
     return prob.out
+
+
+# ------------------------------------------------------------------ int8 storage
+
+def aircache_quantize_int8(k, v, offsets, k8, v8, k_scale, v_scale, status=None, stream=None):
+    """int8 codes and per-(unit, KV head) scales of the bf16 arenas k, v
+    ([rows, H_kv, D]); units are offsets[u] .. offsets[u+1]-1 (int64 device)."""
+    c = QuantProblemStruct(
+        num_units=offsets.numel() - 1, h_kv=int(k.shape[1]), head_dim=int(k.shape[2]),
+        dtype=BF16 if k.dtype == torch.bfloat16 else F32, reserved0=0, reserved1=0,
+        rows=int(k.shape[0]), k=k.data_ptr(), v=v.data_ptr(),
+        kv_stride_row=k.stride(0), kv_stride_head=k.stride(1), offsets=offsets.data_ptr(),
+        k8=k8.data_ptr(), v8=v8.data_ptr(), k_scale=k_scale.data_ptr(), v_scale=v_scale.data_ptr())
+    if k.stride() != v.stride() or k.stride(2) != 1:
+        raise ValueError("k and v must share strides, head_dim contiguous")
+    _check(lib().aircache_quantize_int8(ctypes.byref(c), _ptr(status), _stream(stream)), "aircache_quantize_int8")
+
+
+def quantize_int8(k, v, offsets, stream=None, check=True):
+    """Allocates and returns (k8, v8, k_scale, v_scale) for the arenas k, v."""
+    U = offsets.numel() - 1
+    k8 = torch.empty(k.shape, dtype=torch.int8, device=k.device)
+    v8 = torch.empty(v.shape, dtype=torch.int8, device=v.device)
+    ks = torch.empty((U, k.shape[1]), dtype=torch.float32, device=k.device)
+    vs = torch.empty((U, k.shape[1]), dtype=torch.float32, device=k.device)
+    st = torch.zeros(1, dtype=torch.int32, device=k.device) if check else None
+    aircache_quantize_int8(k, v, offsets, k8, v8, ks, vs, st, stream)
+    if check and int(st.item()) != OK:
+        raise AirCacheError(int(st.item()), "aircache_quantize_int8 (device)")
+    return k8, v8, ks, vs

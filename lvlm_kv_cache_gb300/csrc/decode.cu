@@ -40,21 +40,28 @@ constexpr int kDecMaxSplit = 64;
 constexpr int kDecMaxCluster = 8;     // slices per (sequence, KV head) merged through a cluster
 constexpr int kDecZeroBlock = 256;    // error word, then the per-(s, h) counters
 
-template <int D>
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
+
+// Q8: the cached rows are int8 codes (a plain row-major tile per stage, no
+// swizzle); each consumer warp widens its 16 rows to bf16 in a scratch of its
+// own, laid out like a swizzled bf16 tile, and runs the same MMA code on it.
+template <int D, bool Q8>
 struct DecCfg {
-  static constexpr int kSlabs = D / 64;                       // 128-byte column slabs per row
-  static constexpr int kTileBytes = kDecRows * D * 2;         // one K (or V) tile
-  static constexpr int kStages = D == 128 ? 3 : 5;
+  static constexpr int kSlabs = D / 64;                       // 128-byte bf16 column slabs per row
+  static constexpr int kTileBytes = kDecRows * D * (Q8 ? 1 : 2);  // one K (or V) tile
+  static constexpr int kStages = Q8 ? (D == 128 ? 4 : 6) : (D == 128 ? 3 : 5);
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kQPitch = D + 8;                       // bf16 elements per staged query row
   static constexpr int kRing = kStages * kStageBytes;
   static constexpr int kMerge = kDecWarps * (kDecMaxGroup * D + 2 * kDecMaxGroup) * 4;
-  static constexpr int kMain = kRing > kMerge ? kRing : kMerge;
+  static constexpr int kPartEnd = 45056 + kDecMaxGroup * D * 4 + kDecMaxGroup * 8;  // the cluster partial's end
+  static constexpr int kMain = (cmax(cmax(kRing, kMerge), kPartEnd) + 1023) / 1024 * 1024;
+  static constexpr int kWarpScratch = Q8 ? 2 * 16 * D * 2 : 0;  // K and V rows of one warp, bf16
+  static constexpr int kScratch = kDecWarps * kWarpScratch;
   static constexpr int kQBytes = kDecMaxGroup * kQPitch * 2;
   // 1024-byte alignment slack for the swizzled ring
-  static constexpr int kSmem = 1024 + kMain + kQBytes + 2 * kStages * 8 + 64 + 3 * kDecMaxGroup * 4;
+  static constexpr int kSmem = 1024 + kMain + kScratch + kQBytes + 2 * kStages * 8 + 64 + 3 * kDecMaxGroup * 4;
   static_assert(32768 + kDecMaxGroup * kDecMaxSplit * 12 <= 45056, "merge scratch below the cluster partial");
-  static_assert(kRing >= 45056 + kDecMaxGroup * D * 4 + kDecMaxGroup * 8, "merge scratch must fit in the ring");
   static_assert(kSmem <= 113 * 1024, "two CTAs per SM");
 };
 
@@ -72,6 +79,8 @@ struct DecArgs {
   int64_t kv_rows;
   int64_t q_stride_seq, q_stride_head, new_stride_seq, new_stride_head;
   int h_q, h_kv, group, n_split;
+  const float* k_scale;  // int8 caches: [S * h_kv]
+  const float* v_scale;
   float scale_log2;  // log2(e) / sqrt(D)
 };
 
@@ -87,6 +96,20 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t r[4], uint32_t addr) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr)
                : "memory");
+}
+
+__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// 8 int8 codes (lo: bytes 0-3, hi: bytes 4-7) -> 8 bf16 (exact: |code| <= 127)
+__device__ __forceinline__ uint32_t widen2(uint32_t w, int sh) {
+  const __nv_bfloat162 t = __floats2bfloat162_rn((float)(int8_t)(w >> sh), (float)(int8_t)(w >> (sh + 8)));
+  return *reinterpret_cast<const uint32_t*>(&t);
+}
+__device__ __forceinline__ uint4 widen8(uint32_t lo, uint32_t hi) {
+  return make_uint4(widen2(lo, 0), widen2(lo, 16), widen2(hi, 0), widen2(hi, 16));
 }
 
 __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
@@ -106,16 +129,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-template <int D, bool CL>
+template <int D, bool CL, bool Q8>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_constant__ CUtensorMap kmap,
                                                              const __grid_constant__ CUtensorMap vmap,
                                                              const __grid_constant__ DecArgs a) {
-  using C = DecCfg<D>;
+  using C = DecCfg<D, Q8>;
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = dsm;                                                   // [stages][K tile, V tile]
-  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(dsm + C::kMain);  // [16][kQPitch]
-  uint64_t* full = reinterpret_cast<uint64_t*>(dsm + C::kMain + C::kQBytes);
+  uint8_t* scratch = dsm + C::kMain;                                     // [warp][K, V][slab][16][128 B] (Q8)
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(dsm + C::kMain + C::kScratch);  // [16][kQPitch]
+  uint64_t* full = reinterpret_cast<uint64_t*>(dsm + C::kMain + C::kScratch + C::kQBytes);
   uint64_t* empty = full + C::kStages;
   int* ctl = reinterpret_cast<int*>(empty + C::kStages);                 // [16]
   // the slices' (max, sum) and merge weights live in the ring once it is idle,
@@ -159,10 +183,15 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
     for (int i = 0; i < ntiles && i < C::kStages; ++i) {
       const uint32_t kb = smem_u32(ring + i * C::kStageBytes);
       mbar_arrive_expect_tx(&full[i], C::kStageBytes);
+      if (Q8) {
+        tma_load_3d(kb, &kmap, 0, h, row0 + i * kDecRows, &full[i]);
+        tma_load_3d(kb + C::kTileBytes, &vmap, 0, h, row0 + i * kDecRows, &full[i]);
+      } else {
 #pragma unroll
-      for (int sl = 0; sl < C::kSlabs; ++sl) {
-        tma_load_3d(kb + sl * kDecRows * 128, &kmap, sl * 64, h, row0 + i * kDecRows, &full[i]);
-        tma_load_3d(kb + C::kTileBytes + sl * kDecRows * 128, &vmap, sl * 64, h, row0 + i * kDecRows, &full[i]);
+        for (int sl = 0; sl < C::kSlabs; ++sl) {
+          tma_load_3d(kb + sl * kDecRows * 128, &kmap, sl * 64, h, row0 + i * kDecRows, &full[i]);
+          tma_load_3d(kb + C::kTileBytes + sl * kDecRows * 128, &vmap, sl * 64, h, row0 + i * kDecRows, &full[i]);
+        }
       }
     }
   }
@@ -195,10 +224,15 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         const uint32_t kb = smem_u32(ring + st * C::kStageBytes);
         mbar_arrive_expect_tx(&full[st], C::kStageBytes);
         const int r = row0 + i * kDecRows;
+        if (Q8) {
+          tma_load_3d(kb, &kmap, 0, h, r, &full[st]);
+          tma_load_3d(kb + C::kTileBytes, &vmap, 0, h, r, &full[st]);
+        } else {
 #pragma unroll
-        for (int sl = 0; sl < C::kSlabs; ++sl) {
-          tma_load_3d(kb + sl * kDecRows * 128, &kmap, sl * 64, h, r, &full[st]);
-          tma_load_3d(kb + C::kTileBytes + sl * kDecRows * 128, &vmap, sl * 64, h, r, &full[st]);
+          for (int sl = 0; sl < C::kSlabs; ++sl) {
+            tma_load_3d(kb + sl * kDecRows * 128, &kmap, sl * 64, h, r, &full[st]);
+            tma_load_3d(kb + C::kTileBytes + sl * kDecRows * 128, &vmap, sl * 64, h, r, &full[st]);
+          }
         }
       }
     }
@@ -225,6 +259,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   for (int t = 0; t < D / 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
   float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
   const int r0 = 16 * warp;
+  // logits in base 2; an int8 cache folds its key scale in here (q . (s c) = s (q . c))
+  const float kmult = Q8 ? a.scale_log2 * a.k_scale[(int64_t)s * a.h_kv + h] : a.scale_log2;
   bool alive = true;
 
   for (int i = 0; i < ntiles && alive; ++i) {
@@ -235,9 +271,43 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       break;
     }
     const int valid = nrows - i * kDecRows - r0;  // rows of this warp's 16 that belong to the slice
+    bool released = false;
     if (valid > 0) {
-      const uint32_t kb = smem_u32(ring + st * C::kStageBytes);
-      const uint32_t vb = kb + C::kTileBytes;
+      uint32_t kb, vb;
+      int rb;                          // this warp's first row in the tile it reads
+      constexpr int kSlabStride = (Q8 ? 16 : kDecRows) * 128;
+      if constexpr (Q8) {
+        // widen the warp's 16 int8 rows of K and V to bf16 in its scratch
+        // (rows past the slice end become 0), then hand the stage back
+        const uint8_t* kt = ring + st * C::kStageBytes + r0 * D;
+        const uint8_t* vt = kt + C::kTileBytes;
+        uint8_t* wk = scratch + warp * C::kWarpScratch;
+        const uint32_t wks = smem_u32(wk), wvs = wks + C::kWarpScratch / 2;
+        __syncwarp();
+        for (int c = lane; c < 16 * (D / 16); c += 32) {
+          const int rr = c / (D / 16), ch = c % (D / 16);
+          uint4 kw = make_uint4(0, 0, 0, 0), vw = make_uint4(0, 0, 0, 0);
+          if (rr < valid) {
+            kw = *reinterpret_cast<const uint4*>(kt + rr * D + ch * 16);
+            vw = *reinterpret_cast<const uint4*>(vt + rr * D + ch * 16);
+          }
+          const uint32_t slab = (uint32_t)((ch * 16) / 64) * kSlabStride;
+          const int c8 = 2 * (ch & 3);
+          st_shared_u4(swz(wks + slab, rr, c8), widen8(kw.x, kw.y));
+          st_shared_u4(swz(wks + slab, rr, c8 + 1), widen8(kw.z, kw.w));
+          st_shared_u4(swz(wvs + slab, rr, c8), widen8(vw.x, vw.y));
+          st_shared_u4(swz(wvs + slab, rr, c8 + 1), widen8(vw.z, vw.w));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        released = true;
+        kb = wks;
+        vb = wvs;
+        rb = 0;
+      } else {
+      kb = smem_u32(ring + st * C::kStageBytes);
+      vb = kb + C::kTileBytes;
+      rb = r0;
       if (valid < 16) {
         // rows past the slice end may hold anything (another sequence, unused
         // arena rows): zero their V so that 0-weight rows add exactly 0
@@ -251,15 +321,16 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         }
       }
       __syncwarp();
+      }
       // S = Q K^T for 16 rows: two n-tiles of 8 rows
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       {
         const int mi = lane >> 3, ri = lane & 7;
-        const int row = r0 + ri + 8 * (mi >> 1);
+        const int row = rb + ri + 8 * (mi >> 1);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           uint32_t kf[4];
-          ldsm_x4(kf, swz(kb + (kk >> 2) * kDecRows * 128, row, 2 * (kk & 3) + (mi & 1)));
+          ldsm_x4(kf, swz(kb + (kk >> 2) * kSlabStride, row, 2 * (kk & 3) + (mi & 1)));
           mma_bf16_16816(sc[0], qa[kk], kf[0], kf[1]);
           mma_bf16_16816(sc[1], qa[kk], kf[2], kf[3]);
         }
@@ -271,8 +342,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const bool in = 8 * t + 2 * cq + e < valid;
-          sc[t][e] = in ? sc[t][e] * a.scale_log2 : -INFINITY;
-          sc[t][2 + e] = in ? sc[t][2 + e] * a.scale_log2 : -INFINITY;
+          sc[t][e] = in ? sc[t][e] * kmult : -INFINITY;
+          sc[t][2 + e] = in ? sc[t][2 + e] * kmult : -INFINITY;
           tA = fmaxf(tA, sc[t][e]);
           tB = fmaxf(tB, sc[t][2 + e]);
         }
@@ -307,18 +378,20 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       // O += P V: B = V rows via the transposing ldmatrix, two n-tiles of 8 d per load
       {
         const int mi = lane >> 3, ri = lane & 7;
-        const int row = r0 + ri + 8 * (mi & 1);
+        const int row = rb + ri + 8 * (mi & 1);
 #pragma unroll
         for (int np = 0; np < D / 16; ++np) {
           uint32_t vf[4];
-          ldsm_x4_trans(vf, swz(vb + (np >> 2) * kDecRows * 128, row, 2 * (np & 3) + (mi >> 1)));
+          ldsm_x4_trans(vf, swz(vb + (np >> 2) * kSlabStride, row, 2 * (np & 3) + (mi >> 1)));
           mma_bf16_16816(o[2 * np], pa, vf[0], vf[1]);
           mma_bf16_16816(o[2 * np + 1], pa, vf[2], vf[3]);
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
+    if (!released) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
   }
 
   // ---- merge the four warps' (max, sum, O)
@@ -358,6 +431,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   }
   named_bar_sync(1, kDecWarps * 32);
   const int64_t head0 = (int64_t)s * a.h_q + (int64_t)h * g;  // first query head of the group
+  // an int8 cache's value scale multiplies the cached rows' weighted sum
+  const float vmult = Q8 ? a.v_scale[(int64_t)s * a.h_kv + h] : 1.f;
   for (int idx = tid; idx < g * D; idx += kDecWarps * 32) {
     const int hh = idx / D, d = idx % D;
     float m = -INFINITY;
@@ -377,14 +452,14 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
     }
     if (single) {
       // the whole sequence is this slice: finish here
-      float onum = osum, den = lsum;
+      float onum = osum * vmult, den = lsum;
       if (has_new) {
         const float xn = xnew[hh];
         const float top = fmaxf(m, xn);
         const float c = m == -INFINITY ? 0.f : fast_exp2(m - top);
         const float cn = fast_exp2(xn - top);
         const __nv_bfloat16* vn = a.v_new + (int64_t)s * a.new_stride_seq + (int64_t)h * a.new_stride_head;
-        onum = c * osum + cn * __bfloat162float(vn[d]);
+        onum = c * osum * vmult + cn * __bfloat162float(vn[d]);
         den = c * lsum + cn;
       }
       a.out[(head0 + hh) * D + d] = (ok && den > 0.f) ? onum / den : 0.f;
@@ -451,6 +526,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         acc.z += c * v[x].z;
         acc.w += c * v[x].w;
       }
+      acc.x *= vmult;
+      acc.y *= vmult;
+      acc.z *= vmult;
+      acc.w *= vmult;
       if (has_new) {
         const __nv_bfloat16* vn =
             a.v_new + (int64_t)s * a.new_stride_seq + (int64_t)h * a.new_stride_head + 4 * c4;
@@ -547,6 +626,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
     float acc = 0.f;
 #pragma unroll
     for (int x = 0; x < kXG; ++x) acc += rf[(x * kDecMaxGroup + hh) * D + d];
+    acc *= vmult;
     if (has_new) {
       const __nv_bfloat16* vn = a.v_new + (int64_t)s * a.new_stride_seq + (int64_t)h * a.new_stride_head;
       acc += cnew[hh] * __bfloat162float(vn[d]);
@@ -559,6 +639,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
 
 struct DecPlan {
   bool cluster;  // slices merge inside a thread-block cluster
+  bool q8;       // the cached rows are int8 codes
   int d, g, n_split;
   size_t zero_bytes, ml_off, o_off, total;
 };
@@ -569,10 +650,16 @@ inline size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 int decode_plan(const aircache_decode_problem* p, DecPlan& pl) {
   if (!p) return AIRCACHE_ERR_INVALID_ARG;
   if (p->num_seqs < 0 || p->num_seqs > 65535 || p->h_q <= 0 || p->h_kv <= 0 || p->h_q % p->h_kv != 0 ||
-      (p->head_dim != 64 && p->head_dim != 128) || p->reserved0 != 0 || p->kv_rows < 1 ||
+      (p->head_dim != 64 && p->head_dim != 128) || p->kv_rows < 1 ||
       p->kv_rows > 0x7fff0000LL || p->max_rows < 0)
     return AIRCACHE_ERR_INVALID_ARG;
+  if (p->kv_dtype != AIRCACHE_BF16 && p->kv_dtype != AIRCACHE_INT8) return AIRCACHE_ERR_INVALID_ARG;
   if (p->dtype != AIRCACHE_BF16 || p->h_q / p->h_kv > kDecMaxGroup) return AIRCACHE_ERR_UNSUPPORTED;
+  pl.q8 = p->kv_dtype == AIRCACHE_INT8;
+  // tensor-map strides are multiples of 16 bytes: 8 bf16 or 16 int8 elements
+  const int64_t sm = pl.q8 ? 16 : 8;
+  if (pl.q8 && (!p->k_scale || !p->v_scale || p->kv_stride_row % sm != 0 || p->kv_stride_head % sm != 0))
+    return AIRCACHE_ERR_INVALID_ARG;
   if (!p->q || !p->k || !p->v || !p->row_begin || !p->row_end || !p->out || (!p->k_new) != (!p->v_new))
     return AIRCACHE_ERR_INVALID_ARG;
   auto al16 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15) == 0; };
@@ -614,6 +701,15 @@ bool encode_arena(CUtensorMap* m, const void* base, const aircache_decode_proble
   auto enc = tma_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)p->head_dim, (cuuint64_t)p->h_kv, (cuuint64_t)p->kv_rows};
+  if (p->kv_dtype == AIRCACHE_INT8) {
+    // int8 codes: whole rows of one head per box, row-major, no swizzle
+    cuuint64_t strides8[2] = {(cuuint64_t)p->kv_stride_head, (cuuint64_t)p->kv_stride_row};
+    cuuint32_t box8[3] = {(cuuint32_t)p->head_dim, 1, (cuuint32_t)kDecRows};
+    cuuint32_t es8[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides8, box8, es8,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   cuuint64_t strides[2] = {(cuuint64_t)p->kv_stride_head * 2, (cuuint64_t)p->kv_stride_row * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)kDecRows};
   cuuint32_t es[3] = {1, 1, 1};
@@ -622,7 +718,7 @@ bool encode_arena(CUtensorMap* m, const void* base, const aircache_decode_proble
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, bool Q8>
 int launch_decode(const aircache_decode_problem* p, const DecPlan& pl, uint8_t* ws, cudaStream_t s) {
   CUtensorMap km, vm;
   if (!encode_arena(&km, p->k, p) || !encode_arena(&vm, p->v, p)) return AIRCACHE_ERR_UNSUPPORTED;
@@ -647,10 +743,12 @@ int launch_decode(const aircache_decode_problem* p, const DecPlan& pl, uint8_t* 
   a.group = pl.g;
   a.n_split = pl.n_split;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-  const int smem = DecCfg<D>::kSmem;
+  a.k_scale = p->k_scale;
+  a.v_scale = p->v_scale;
+  const int smem = DecCfg<D, Q8>::kSmem;
   const dim3 grid(pl.n_split, p->h_kv, p->num_seqs);
   if (pl.cluster) {
-    if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D, true>), smem) != cudaSuccess)
+    if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D, true, Q8>), smem) != cudaSuccess)
       return AIRCACHE_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -664,11 +762,11 @@ int launch_decode(const aircache_decode_problem* p, const DecPlan& pl, uint8_t* 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, decode_kernel<D, true>, km, vm, a) != cudaSuccess) return AIRCACHE_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, decode_kernel<D, true, Q8>, km, vm, a) != cudaSuccess) return AIRCACHE_ERR_CUDA;
   } else {
-    if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D, false>), smem) != cudaSuccess)
+    if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D, false, Q8>), smem) != cudaSuccess)
       return AIRCACHE_ERR_CUDA;
-    decode_kernel<D, false><<<grid, kDecThreads, smem, s>>>(km, vm, a);
+    decode_kernel<D, false, Q8><<<grid, kDecThreads, smem, s>>>(km, vm, a);
   }
   return cudaGetLastError() == cudaSuccess ? AIRCACHE_OK : AIRCACHE_ERR_CUDA;
 }
@@ -699,7 +797,8 @@ int aircache_decode(const aircache_decode_problem* p, void* ws, size_t ws_bytes,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   if (p->num_seqs == 0) return AIRCACHE_OK;
-  return pl.d == 128 ? launch_decode<128>(p, pl, w, s) : launch_decode<64>(p, pl, w, s);
+  if (pl.q8) return pl.d == 128 ? launch_decode<128, true>(p, pl, w, s) : launch_decode<64, true>(p, pl, w, s);
+  return pl.d == 128 ? launch_decode<128, false>(p, pl, w, s) : launch_decode<64, false>(p, pl, w, s);
 }
 
 }  // extern "C"

@@ -18,7 +18,7 @@ def A():
 
 def fake(A, **over):
     p = A.DecodeProblemStruct(
-        num_seqs=8, h_q=28, h_kv=4, head_dim=128, dtype=A.BF16, reserved0=0,
+        num_seqs=8, h_q=28, h_kv=4, head_dim=128, dtype=A.BF16, kv_dtype=A.BF16,
         kv_rows=100000, max_rows=2048,
         q=0x100000, k=0x200000, v=0x300000, row_begin=0x400000, row_end=0x400008,
         k_new=None, v_new=None,
@@ -46,7 +46,8 @@ def test_sizes_and_splits(A):
 
 @pytest.mark.parametrize("field,value,code", [
     ("num_seqs", -1, -1), ("num_seqs", 65536, -1), ("h_q", 27, -1), ("h_kv", 0, -1),
-    ("head_dim", 96, -1), ("dtype", 0, -2), ("h_q", 68, -2), ("reserved0", 1, -1),
+    ("head_dim", 96, -1), ("dtype", 0, -2), ("h_q", 68, -2), ("kv_dtype", 0, -1), ("kv_dtype", 3, -1),
+    ("kv_dtype", 2, -1),
     ("kv_rows", 0, -1), ("kv_rows", 1 << 31, -1), ("max_rows", -1, -1),
     ("q", None, -1), ("k", None, -1), ("out", None, -1), ("row_begin", None, -1),
     ("k", 0x200008, -1), ("q", 0x100004, -1), ("kv_stride_row", 4 * 128 + 4, -1),
@@ -67,3 +68,22 @@ def test_decode_workspace_checks(A):
     assert lib.aircache_decode(ctypes.byref(p), ctypes.c_void_p(0x700000), need - 1, None) == -3
     assert lib.aircache_decode(ctypes.byref(p), ctypes.c_void_p(0x700010), need, None) == -1
     assert lib.aircache_decode(ctypes.byref(p), None, need, None) == -1
+
+
+def fake_quant(A, **over):
+    p = A.QuantProblemStruct(num_units=28, h_kv=4, head_dim=128, dtype=A.BF16, reserved0=0, reserved1=0,
+                             rows=30000, k=0x100000, v=0x200000, kv_stride_row=512, kv_stride_head=128,
+                             offsets=0x300000, k8=0x400000, v8=0x500000, k_scale=0x600000, v_scale=0x700000)
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("field,value", [
+    ("num_units", -1), ("h_kv", 0), ("head_dim", 96), ("dtype", 0), ("reserved0", 1), ("rows", 0),
+    ("k", None), ("v8", None), ("k_scale", None), ("offsets", None), ("k", 0x100008), ("k8", 0x400004),
+    ("kv_stride_row", 510), ("kv_stride_head", 0),
+])
+def test_invalid_quantize_rejected_on_host(A, field, value):
+    p = fake_quant(A, **{field: value})
+    assert A.lib().aircache_quantize_int8(ctypes.byref(p), None, None) == -1
