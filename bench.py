@@ -372,11 +372,38 @@ def run_decode(args, local):
             comp_ms = timed(comp_probs, ws_c)
             comp_rows = int(rows_h[-1])
             comp_bytes = comp_rows * kv_row_bytes + L * B * H_q * D * (2 + 4)
+            # int8 storage of the compressed cache (one aircache_quantize_int8 call, timed on its own)
+            kc, vc = out["out_k"][:comp_rows], out["out_v"][:comp_rows]
+            k8 = torch.empty(kc.shape, dtype=torch.int8, device=dev)
+            v8 = torch.empty(vc.shape, dtype=torch.int8, device=dev)
+            ks = torch.empty((L * B, H_kv), dtype=torch.float32, device=dev)
+            vs = torch.empty((L * B, H_kv), dtype=torch.float32, device=dev)
+            qt = []
+            for it in range(max(args.warmup, 3) + 5):
+                flush_l2()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                A.aircache_quantize_int8(kc, vc, offs, k8, v8, ks, vs)
+                e1.record()
+                torch.cuda.synchronize()
+                if it >= max(args.warmup, 3):
+                    qt.append(e0.elapsed_time(e1))
+            q_ms = statistics.median(qt)
+            q_bytes = comp_rows * kv_row_bytes * 3 // 2 + 2 * L * B * H_kv * 4  # bf16 read + int8 written
+            q8_probs = [A.DecodeProblem(qdec[l], k8, v8, row_begin=offs[l * B:(l + 1) * B],
+                                        row_end=offs[l * B + 1:(l + 1) * B + 1], max_rows=longest,
+                                        k_scale=ks[l * B:(l + 1) * B], v_scale=vs[l * B:(l + 1) * B])
+                        for l in range(L)]
+            q8_ms = timed(q8_probs, ws_c)
+            q8_bytes = comp_rows * kv_row_bytes // 2 + L * B * H_q * D * (2 + 4) + 2 * L * B * H_kv * 4
             results.append({"r": r, "ms": comp_ms, "rows": comp_rows, "algorithmic_bytes": comp_bytes,
                             "gbs": comp_bytes / (comp_ms * 1e-3) / 1e9,
                             "frac": comp_bytes / (comp_ms * 1e-3) / 1e9 / peak,
-                            "splits": comp_probs[0].splits(), "reduction": 1.0 - comp_ms / full_ms})
-            del out, prob
+                            "splits": comp_probs[0].splits(), "reduction": 1.0 - comp_ms / full_ms,
+                            "int8": {"ms": q8_ms, "algorithmic_bytes": q8_bytes,
+                                     "gbs": q8_bytes / (q8_ms * 1e-3) / 1e9, "reduction": 1.0 - q8_ms / full_ms,
+                                     "quantize_ms": q_ms, "quantize_gbs": q_bytes / (q_ms * 1e-3) / 1e9}})
+            del out, prob, k8, v8
         clocks = sampler.stop()
         full_gbs = full_bytes / (full_ms * 1e-3) / 1e9
         line = {

@@ -365,10 +365,11 @@ AIRCACHE_API int aircache_decode_splits(const aircache_decode_problem* p);
  * numbering); k_scale, v_scale fp32 [num_units][h_kv]; offsets device int64
  * [num_units + 1].  Requirements (else AIRCACHE_ERR_INVALID_ARG): head_dim 64
  * or 128, dtype AIRCACHE_BF16, k and v 16-byte aligned with strides multiples
- * of 8 elements, k8 and v8 16-byte aligned, 1 <= rows, 0 <= num_units <= 2^31/4,
+ * of 8 elements, k8 and v8 16-byte aligned, 1 <= rows, 0 <= num_units <= 2^27,
  * reserved0 == 0.  `status` (optional device int32) is cleared first, then
  * receives AIRCACHE_ERR_DEVICE_BOUNDS if a unit's range lies outside [0, rows)
- * (that unit is skipped).  One memset (when status is given) and one kernel.
+ * (that unit's codes are not written).  One memset (when status is given)
+ * and one kernel (a cluster of 8 CTAs per unit, KV head and K or V).
  */
 typedef struct aircache_quant_problem {
     int32_t num_units;

@@ -180,3 +180,18 @@ def test_decode_from_the_quantised_compressed_arena(A, oracle):
             kd, vd = dequant(c_k[r0:r1], s_k[u]), dequant(c_v[r0:r1], s_v[u])
             ref = oracle.decode(qb[b], kd, vd)
             assert np.all(np.abs(out[b] - ref) <= tolerance(qb[b], kd, vd, ref)), f"layer {l} request {b}"
+
+
+def test_quantize_many_values_and_exact_halves(A, oracle):
+    # a million values over units of varied scale, plus exact half-integer
+    # quotients (max 254 -> s = 2, x = 5 -> 2.5 -> 3): bit-exact everywhere
+    g = torch.Generator(device="cuda").manual_seed(28)
+    rows, h_kv, d = 4000, 2, 128
+    k = (torch.randn((rows, h_kv, d), generator=g, device="cuda") *
+         torch.exp(torch.randn((rows, 1, 1), generator=g, device="cuda") * 2)).to(torch.bfloat16)
+    k[:10] = 0.0
+    k[0, 0, 0], k[1, 0, 1], k[2, 0, 2], k[3, 1, 3] = 254.0, 5.0, -5.0, 3.0
+    offs = torch.tensor([0, 10, 333, 1000, 2500, 4000], dtype=torch.int64, device="cuda")
+    k8, v8, ks, vs = A.quantize_int8(k, k, offs)
+    check_units(oracle, k, k8, ks, offs)
+    assert int(k8[1, 0, 1]) == 3 and int(k8[2, 0, 2]) == -3
