@@ -322,7 +322,22 @@ typedef struct aircache_decode_problem {
     const float* k_scale;  /* AIRCACHE_INT8 only: [num_seqs][h_kv] fp32 scales of the codes of */
     const float* v_scale;  /* sequence s, KV head h (for the compacted arena of layer l: the
                               aircache_quantize_int8 scales + l*B*h_kv) */
+    int32_t flags;         /* 0, or AIRCACHE_DECODE_EARLY_CACHE */
+    int32_t reserved1;     /* 0 */
 } aircache_decode_problem;
+
+/*
+ * AIRCACHE_DECODE_EARLY_CACHE: launch with programmatic dependent launch.  The
+ * kernel may start while the kernel before it on the stream is finishing, and
+ * reads row_begin, row_end and the cached rows right away; it waits for that
+ * kernel (griddepcontrol.wait) before it reads q, k_new, v_new or the scales and
+ * before it writes anything else than the error word.  Valid only when the
+ * kernel launched just before on the stream writes neither the row ranges nor
+ * the cached rows (in a decoder: the cache append of this step goes to k_new /
+ * v_new, or happened earlier).  Consecutive layers of a decode step (one call
+ * per layer) then overlap each kernel's start with the previous one's end.
+ */
+#define AIRCACHE_DECODE_EARLY_CACHE 1
 
 /* Workspace bytes aircache_decode needs for `p` on the current device, or 0 if
  * `p` is invalid.  Depends on num_seqs, h_q, h_kv, head_dim, max_rows and the

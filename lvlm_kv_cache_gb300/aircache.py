@@ -20,6 +20,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libaircache.so")
 
 OK = 0
+DECODE_EARLY_CACHE = 1
 ERR_INVALID_ARG = -1
 ERR_UNSUPPORTED = -2
 ERR_WORKSPACE = -3
@@ -82,6 +83,7 @@ class DecodeProblemStruct(ctypes.Structure):
         ("kv_stride_row", ctypes.c_int64), ("kv_stride_head", ctypes.c_int64),
         ("new_stride_seq", ctypes.c_int64), ("new_stride_head", ctypes.c_int64),
         ("out", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+        ("flags", ctypes.c_int32), ("reserved1", ctypes.c_int32),
     ]
 
 
@@ -380,10 +382,12 @@ class DecodeProblem:
     row_begin, row_end: int64 device tensors [S] (or one offsets tensor [S+1]
     via ``offsets=``); k_new, v_new: optional [S, H_kv, D] bf16; out: fp32
     [S, H_q, D] (allocated when None).  max_rows: the expected longest range
-    (sizes the split; not a limit)."""
+    (sizes the split; not a limit).  early_cache: AIRCACHE_DECODE_EARLY_CACHE
+    (programmatic dependent launch; the kernel launched just before on the
+    stream must not write the ranges or the cached rows)."""
 
     def __init__(self, q, k, v, row_begin=None, row_end=None, max_rows=0, k_new=None, v_new=None,
-                 out=None, offsets=None, k_scale=None, v_scale=None):
+                 out=None, offsets=None, k_scale=None, v_scale=None, early_cache=False):
         if offsets is not None:
             row_begin, row_end = offsets[:-1], offsets[1:]
         S, h_q, d = (int(x) for x in q.shape)
@@ -418,6 +422,7 @@ class DecodeProblem:
             new_stride_head=k_new.stride(1) if k_new is not None else 0,
             out=out.data_ptr(),
             k_scale=k_scale.data_ptr() if q8 else None, v_scale=v_scale.data_ptr() if q8 else None,
+            flags=DECODE_EARLY_CACHE if early_cache else 0, reserved1=0,
         )
 
     @property

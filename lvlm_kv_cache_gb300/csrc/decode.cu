@@ -82,6 +82,7 @@ struct DecArgs {
   const float* k_scale;  // int8 caches: [S * h_kv]
   const float* v_scale;
   float scale_log2;  // log2(e) / sqrt(D)
+  int early;         // AIRCACHE_DECODE_EARLY_CACHE: ranges and rows read before the dependency wait
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& lo_r, float& hi_r) {
@@ -156,11 +157,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   const int split = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
   const int g = a.group;
 
+  pdl_trigger();  // the next kernel on the stream may launch; it waits for this one before using its output
   if (warp == kDecWarps && lane == 0) {
     // ---- producer lane: this CTA's slice of the sequence's rows, then the
     // first tiles right away (the queries load meanwhile)
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
+    if (!a.early) pdl_wait();  // the ranges and rows may come from the previous kernel
     const int64_t b = a.row_begin[s], e = a.row_end[s];
     const bool ok = b >= 0 && e >= b && e <= a.kv_rows;
     if (!ok && split == 0 && h == 0) set_error(a.error, AIRCACHE_ERR_DEVICE_BOUNDS);
@@ -195,7 +198,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       }
     }
   }
-  // ---- query rows of the group, zero-padded to 16 heads
+  // ---- query rows of the group, zero-padded to 16 heads (after the previous
+  // kernel on the stream is done: it may have written q; everything below
+  // comes after this wait in every thread but the producer's early reads)
+  pdl_wait();
   for (int c = tid; c < kDecMaxGroup * (D / 8); c += kDecThreads) {
     const int hh = c / (D / 8), ch = c % (D / 8);
     uint4 val = make_uint4(0, 0, 0, 0);
@@ -650,7 +656,8 @@ inline size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 int decode_plan(const aircache_decode_problem* p, DecPlan& pl) {
   if (!p) return AIRCACHE_ERR_INVALID_ARG;
   if (p->num_seqs < 0 || p->num_seqs > 65535 || p->h_q <= 0 || p->h_kv <= 0 || p->h_q % p->h_kv != 0 ||
-      (p->head_dim != 64 && p->head_dim != 128) || p->kv_rows < 1 ||
+      (p->head_dim != 64 && p->head_dim != 128) || p->kv_rows < 1 || (p->flags & ~AIRCACHE_DECODE_EARLY_CACHE) != 0 ||
+      p->reserved1 != 0 ||
       p->kv_rows > 0x7fff0000LL || p->max_rows < 0)
     return AIRCACHE_ERR_INVALID_ARG;
   if (p->kv_dtype != AIRCACHE_BF16 && p->kv_dtype != AIRCACHE_INT8) return AIRCACHE_ERR_INVALID_ARG;
@@ -720,6 +727,20 @@ bool encode_arena(CUtensorMap* m, const void* base, const aircache_decode_proble
 
 template <int D, bool Q8>
 int launch_decode(const aircache_decode_problem* p, const DecPlan& pl, uint8_t* ws, cudaStream_t s) {
+  auto launch_pdl3 = [](void (*k)(CUtensorMap, CUtensorMap, DecArgs), dim3 grid, dim3 block, size_t smem,
+                        cudaStream_t st, const CUtensorMap& km, const CUtensorMap& vm, const DecArgs& a) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, km, vm, a);
+  };
   CUtensorMap km, vm;
   if (!encode_arena(&km, p->k, p) || !encode_arena(&vm, p->v, p)) return AIRCACHE_ERR_UNSUPPORTED;
   DecArgs a;
@@ -745,6 +766,7 @@ int launch_decode(const aircache_decode_problem* p, const DecPlan& pl, uint8_t* 
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   a.k_scale = p->k_scale;
   a.v_scale = p->v_scale;
+  a.early = (p->flags & AIRCACHE_DECODE_EARLY_CACHE) != 0;
   const int smem = DecCfg<D, Q8>::kSmem;
   const dim3 grid(pl.n_split, p->h_kv, p->num_seqs);
   if (pl.cluster) {
@@ -755,18 +777,25 @@ int launch_decode(const aircache_decode_problem* p, const DecPlan& pl, uint8_t* 
     cfg.blockDim = dim3(kDecThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = pl.n_split;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = a.early ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, decode_kernel<D, true, Q8>, km, vm, a) != cudaSuccess) return AIRCACHE_ERR_CUDA;
   } else {
     if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D, false, Q8>), smem) != cudaSuccess)
       return AIRCACHE_ERR_CUDA;
-    decode_kernel<D, false, Q8><<<grid, kDecThreads, smem, s>>>(km, vm, a);
+    if (a.early) {
+      if (launch_pdl3(decode_kernel<D, false, Q8>, grid, dim3(kDecThreads), smem, s, km, vm, a) != cudaSuccess)
+        return AIRCACHE_ERR_CUDA;
+    } else {
+      decode_kernel<D, false, Q8><<<grid, kDecThreads, smem, s>>>(km, vm, a);
+    }
   }
   return cudaGetLastError() == cudaSuccess ? AIRCACHE_OK : AIRCACHE_ERR_CUDA;
 }

@@ -47,7 +47,7 @@ def test_sizes_and_splits(A):
 @pytest.mark.parametrize("field,value,code", [
     ("num_seqs", -1, -1), ("num_seqs", 65536, -1), ("h_q", 27, -1), ("h_kv", 0, -1),
     ("head_dim", 96, -1), ("dtype", 0, -2), ("h_q", 68, -2), ("kv_dtype", 0, -1), ("kv_dtype", 3, -1),
-    ("kv_dtype", 2, -1),
+    ("kv_dtype", 2, -1), ("flags", 2, -1), ("reserved1", 1, -1),
     ("kv_rows", 0, -1), ("kv_rows", 1 << 31, -1), ("max_rows", -1, -1),
     ("q", None, -1), ("k", None, -1), ("out", None, -1), ("row_begin", None, -1),
     ("k", 0x200008, -1), ("q", 0x100004, -1), ("kv_stride_row", 4 * 128 + 4, -1),

@@ -248,3 +248,26 @@ def test_full_size_cache_sampled(A, oracle, batch, prompt):
     di = W.decode_inputs([prompt] * batch, 28, 4, 128, seed=13, device="cuda", q_scale=2.0)
     out, _ = run(A, di, max_rows=prompt)
     check_against_oracle(oracle, di, out, seqs=[0, batch - 1])
+
+
+def test_early_cache_launches_match_plain_launches(A, oracle):
+    # consecutive calls with programmatic dependent launch (the cache is not
+    # written by the kernel before each call) give the same bits as plain ones,
+    # also when each call's queries come from the kernel just before it
+    di = W.decode_inputs([700, 33, 4100, 5], 28, 4, 128, seed=15, device="cuda", q_scale=2.0, new_row=True)
+    outs = {}
+    for early in (False, True):
+        ws = torch.zeros(1 << 22, dtype=torch.uint8, device="cuda")
+        res = []
+        for m in (0, 1000, 10 ** 6):
+            q = torch.empty_like(di.q)
+            q.copy_(di.q)  # written by the kernel right before the decode kernel
+            p = A.DecodeProblem(q, di.k, di.v, offsets=di.offsets, max_rows=m, k_new=di.k_new, v_new=di.v_new,
+                                early_cache=early)
+            A.aircache_decode(p, ws)
+            res.append(p.out)
+        assert A.aircache_get_error(ws) == A.OK
+        outs[early] = [r.clone() for r in res]
+    for a, b in zip(outs[False], outs[True]):
+        assert torch.equal(a, b)
+    check_against_oracle(oracle, di, outs[True][1].cpu().numpy().astype(np.float64))
