@@ -47,6 +47,15 @@
  *   R16 a decode step (the consumer of the compacted cache) is plain softmax
  *       attention of the step's query over every cached row, per query head,
  *       with the head map of R1 and no mask.
+ *   R18 a visual span at an offset (the multimodal-layout page, section on
+ *       the correct sequence layout: system text, then the visual tokens, then
+ *       the question): request b's prompt is [n_p prefix text][n_v visual]
+ *       [suffix text]; "text" is every non-visual token, prefix then suffix,
+ *       and text index j is prompt row j (j < n_p) or n_v + j (j >= n_p);
+ *       visual index i is prompt row n_p + i.  Every step above runs in those
+ *       indices unchanged (the last text query is the prompt's last token);
+ *       compaction writes the kept visual rows, then the text rows in text
+ *       order.  n_p = 0 is the layout X = Concat(X_v, X_t).
  *   R17 int8 storage of the kept cache (LLM KV-compression notes, section
  *       "Quantization stacked on compression": quantise after the token
  *       compression, one scale per head = the head's largest |value| over the
@@ -82,6 +91,10 @@ static double elem(const oracle_view* t, int64_t tok, int64_t head, int64_t i) {
     return (double)f;
 }
 
+/* Prompt rows of visual index i and text index j (R18). */
+static int64_t vis_row(int n_p, int i) { return (int64_t)n_p + i; }
+static int64_t text_row(int n_p, int n_v, int j) { return j < n_p ? (int64_t)j : (int64_t)n_v + j; }
+
 /* q_row . k_row / sqrt(D), both rows read in fp64 (R2: D = head dimension). */
 static double scaled_dot(const oracle_view* q, int64_t q_tok, int64_t q_head,
                          const oracle_view* k, int64_t k_tok, int64_t k_head, int d) {
@@ -109,8 +122,8 @@ static double scaled_dot(const oracle_view* q, int64_t q_tok, int64_t q_head,
  * returns N_tk, or -1 on bad arguments.
  */
 int oracle_elite(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, int d,
-                 int n_v, int n_t, double alpha, double* p_out, int32_t* elite) {
-    if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || n_t <= 0 || d <= 0) return -1;
+                 int n_v, int n_t, int n_p, double alpha, double* p_out, int32_t* elite) {
+    if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || n_t <= 0 || d <= 0 || n_p < 0 || n_p > n_t) return -1;
     const int g = h_q / h_kv;
     double* logit = (double*)malloc(sizeof(double) * (size_t)n_t);
     double* P = (double*)calloc((size_t)n_t, sizeof(double));
@@ -120,7 +133,7 @@ int oracle_elite(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, 
         const int kvh = h / g;
         double m = -INFINITY;
         for (int j = 0; j < n_t; ++j) {
-            logit[j] = scaled_dot(q, n_t - 1, h, k, (int64_t)n_v + j, kvh, d);
+            logit[j] = scaled_dot(q, n_t - 1, h, k, text_row(n_p, n_v, j), kvh, d);
             if (logit[j] > m) m = logit[j];
         }
         double z = 0.0;
@@ -156,9 +169,9 @@ int oracle_elite(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, 
  * returns 0, or -1 on bad arguments.
  */
 int oracle_score(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, int d,
-                 int n_v, int n_t, const int32_t* elite, int n_tk,
+                 int n_v, int n_t, int n_p, const int32_t* elite, int n_tk,
                  double* iv, double* elite_mass) {
-    if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || n_v <= 0 || n_tk <= 0) return -1;
+    if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || n_v <= 0 || n_tk <= 0 || n_p < 0 || n_p > n_t) return -1;
     for (int e = 0; e < n_tk; ++e) {
         if (elite[e] < 0 || elite[e] >= n_t) return -1;
     }
@@ -174,11 +187,11 @@ int oracle_score(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, 
             const int64_t q_tok = elite[e];
             double m = -INFINITY;
             for (int c = 0; c < n_v; ++c) {
-                logit[c] = scaled_dot(q, q_tok, h, k, c, kvh, d);
+                logit[c] = scaled_dot(q, q_tok, h, k, vis_row(n_p, c), kvh, d);
                 if (logit[c] > m) m = logit[c];
             }
             for (int e2 = 0; e2 < n_tk; ++e2) {
-                logit[n_v + e2] = scaled_dot(q, q_tok, h, k, (int64_t)n_v + elite[e2], kvh, d);
+                logit[n_v + e2] = scaled_dot(q, q_tok, h, k, text_row(n_p, n_v, elite[e2]), kvh, d);
                 if (logit[n_v + e2] > m) m = logit[n_v + e2];
             }
             double z = 0.0;
@@ -384,13 +397,14 @@ int oracle_select(const double* iv, int n_v, int keep, int32_t* idx) {
  * Rows are copied element by element (bit-exact, in the source type) into a
  * dense [rows][h_kv][d] destination.  Returns the number of rows written.
  */
-int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t,
+int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t, int n_p,
                        const int32_t* idx, int keep, void* dst) {
+    if (n_p < 0 || n_p > n_t) return -1;
     const size_t esize = (src->dtype == ORACLE_F32) ? 4 : 2;
     unsigned char* out = (unsigned char*)dst;
     int64_t row = 0;
     for (int j = 0; j < keep + n_t; ++j) {
-        const int64_t tok = (j < keep) ? idx[j] : (int64_t)n_v + (j - keep);
+        const int64_t tok = (j < keep) ? vis_row(n_p, idx[j]) : text_row(n_p, n_v, j - keep);
         for (int h = 0; h < h_kv; ++h) {
             const unsigned char* from = (const unsigned char*)src->base +
                 (size_t)(tok * src->stride_tok + h * src->stride_head) * esize;
@@ -414,7 +428,7 @@ int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t
  * stats      : [n_layers * 4]; keep: [n_layers]; idx: [n_layers * n_v].
  */
 int oracle_request_variant(const oracle_view* q, const oracle_view* k, int n_layers, int h_q,
-                           int h_kv, int d, int n_v, int n_t, double alpha, double r, int window_mode,
+                           int h_kv, int d, int n_v, int n_t, int n_p, double alpha, double r, int window_mode,
                            int budget_mode, double* iv, int32_t* elite, int32_t* n_tk, double* stats,
                            int32_t* keep, int32_t* idx) {
     double* s_t = (double*)malloc(sizeof(double) * (size_t)n_layers);
@@ -423,12 +437,12 @@ int oracle_request_variant(const oracle_view* q, const oracle_view* k, int n_lay
     int rc = 0;
     for (int l = 0; l < n_layers && rc == 0; ++l) {
         int32_t* el = elite + (int64_t)l * n_t;
-        const int ntk = window_mode == 0 ? oracle_elite(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, alpha, NULL, el)
+        const int ntk = window_mode == 0 ? oracle_elite(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, n_p, alpha, NULL, el)
                                          : oracle_window(n_t, window_mode, el);
         if (ntk <= 0) { rc = -1; break; }
         n_tk[l] = ntk;
         double* ivl = iv + (int64_t)l * n_v;
-        rc = oracle_score(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, el, ntk, ivl, NULL);
+        rc = oracle_score(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, n_p, el, ntk, ivl, NULL);
         if (rc == 0) rc = oracle_stats(ivl, n_v, stats + (int64_t)l * 4);
         if (rc == 0) { s_t[l] = stats[l * 4 + 0]; s_k[l] = stats[l * 4 + 1]; }
     }
@@ -446,7 +460,7 @@ int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int
                    int d, int n_v, int n_t, double alpha, double r,
                    double* iv, int32_t* elite, int32_t* n_tk, double* stats,
                    int32_t* keep, int32_t* idx) {
-    return oracle_request_variant(q, k, n_layers, h_q, h_kv, d, n_v, n_t, alpha, r, 0, 0, iv, elite,
+    return oracle_request_variant(q, k, n_layers, h_q, h_kv, d, n_v, n_t, 0, alpha, r, 0, 0, iv, elite,
                                   n_tk, stats, keep, idx);
 }
 

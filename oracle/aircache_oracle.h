@@ -23,15 +23,15 @@ typedef struct {
 } oracle_view;
 
 int oracle_elite(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, int d,
-                 int n_v, int n_t, double alpha, double* p_out, int32_t* elite);
+                 int n_v, int n_t, int n_p, double alpha, double* p_out, int32_t* elite);
 int oracle_score(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, int d,
-                 int n_v, int n_t, const int32_t* elite, int n_tk,
+                 int n_v, int n_t, int n_p, const int32_t* elite, int n_tk,
                  double* iv, double* elite_mass);
 int oracle_stats(const double* iv, int n_v, double* out);
 int oracle_budget(const double* s_t, const double* s_k, int n_layers, int n_v, double r,
                   double* r_l, int32_t* keep);
 int oracle_select(const double* iv, int n_v, int keep, int32_t* idx);
-int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t,
+int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t, int n_p,
                        const int32_t* idx, int keep, void* dst);
 int oracle_decode(const oracle_view* q, const oracle_view* k, const oracle_view* v, int h_q, int h_kv,
                   int d, int64_t n_rows, double* out);
@@ -42,7 +42,7 @@ int oracle_window(int n_t, int mode, int32_t* positions);
 int oracle_budget_variant(const double* s_t, const double* s_k, int n_layers, int n_v, double r,
                           int mode, double* r_l, int32_t* keep);
 int oracle_request_variant(const oracle_view* q, const oracle_view* k, int n_layers, int h_q,
-                           int h_kv, int d, int n_v, int n_t, double alpha, double r, int window_mode,
+                           int h_kv, int d, int n_v, int n_t, int n_p, double alpha, double r, int window_mode,
                            int budget_mode, double* iv, int32_t* elite, int32_t* n_tk, double* stats,
                            int32_t* keep, int32_t* idx);
 int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int h_q, int h_kv,

@@ -61,9 +61,9 @@ def lib():
         L = ctypes.CDLL(path)
         vp, i32, i64, f64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
         V = ctypes.POINTER(_View)
-        L.oracle_elite.argtypes = [V, V, i32, i32, i32, i32, i32, f64, vp, vp]
+        L.oracle_elite.argtypes = [V, V, i32, i32, i32, i32, i32, i32, f64, vp, vp]
         L.oracle_elite.restype = i32
-        L.oracle_score.argtypes = [V, V, i32, i32, i32, i32, i32, vp, i32, vp, vp]
+        L.oracle_score.argtypes = [V, V, i32, i32, i32, i32, i32, i32, vp, i32, vp, vp]
         L.oracle_score.restype = i32
         L.oracle_stats.argtypes = [vp, i32, vp]
         L.oracle_stats.restype = i32
@@ -71,7 +71,7 @@ def lib():
         L.oracle_budget.restype = i32
         L.oracle_select.argtypes = [vp, i32, i32, vp]
         L.oracle_select.restype = i32
-        L.oracle_compact.argtypes = [V, i32, i32, i32, i32, vp, i32, vp]
+        L.oracle_compact.argtypes = [V, i32, i32, i32, i32, i32, vp, i32, vp]
         L.oracle_compact.restype = i64
         L.oracle_request.argtypes = [V, V, i32, i32, i32, i32, i32, i32, f64, f64,
                                      vp, vp, vp, vp, vp, vp]
@@ -86,7 +86,7 @@ def lib():
         L.oracle_window.restype = i32
         L.oracle_budget_variant.argtypes = [vp, vp, i32, i32, f64, i32, vp, vp]
         L.oracle_budget_variant.restype = i32
-        L.oracle_request_variant.argtypes = [V, V, i32, i32, i32, i32, i32, i32, f64, f64, i32, i32,
+        L.oracle_request_variant.argtypes = [V, V, i32, i32, i32, i32, i32, i32, i32, f64, f64, i32, i32,
                                              vp, vp, vp, vp, vp, vp]
         L.oracle_request_variant.restype = i32
         _lib = L
@@ -114,22 +114,23 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-def elite(q: np.ndarray, k: np.ndarray, n_v: int, alpha: float):
+def elite(q: np.ndarray, k: np.ndarray, n_v: int, alpha: float, n_p: int = 0):
     """Elite window of one (request, layer): q = this request's text queries
-    [N_t, H_q, D]; k = this request's keys [N_v+N_t, H_kv, D].
+    [N_t, H_q, D]; k = this request's keys [N_v+N_t, H_kv, D] in prompt order
+    (n_p prefix text rows, the visual rows, the other text rows; reading R18).
     Returns (elite positions (text-relative, ascending), head-mean row P)."""
     n_t, h_q, d = q.shape
     h_kv = k.shape[1]
     P = np.zeros(n_t, np.float64)
     el = np.zeros(n_t, np.int32)
     n = lib().oracle_elite(ctypes.byref(_view(q)), ctypes.byref(_view(k)), h_q, h_kv, d,
-                           n_v, n_t, float(alpha), _ptr(P), _ptr(el))
+                           n_v, n_t, int(n_p), float(alpha), _ptr(P), _ptr(el))
     if n < 0:
         raise ValueError("oracle_elite rejected its arguments")
     return el[:n].copy(), P
 
 
-def score(q: np.ndarray, k: np.ndarray, n_v: int, elite_idx: np.ndarray):
+def score(q: np.ndarray, k: np.ndarray, n_v: int, elite_idx: np.ndarray, n_p: int = 0):
     """I_v of one (request, layer) for a given elite set.
     Returns (I_v [N_v] fp64, elite-key mass [H_q, N_tk])."""
     n_t, h_q, d = q.shape
@@ -138,7 +139,7 @@ def score(q: np.ndarray, k: np.ndarray, n_v: int, elite_idx: np.ndarray):
     iv = np.zeros(n_v, np.float64)
     mass = np.zeros(h_q * len(el), np.float64)
     rc = lib().oracle_score(ctypes.byref(_view(q)), ctypes.byref(_view(k)), h_q, h_kv, d,
-                            n_v, n_t, _ptr(el), len(el), _ptr(iv), _ptr(mass))
+                            n_v, n_t, int(n_p), _ptr(el), len(el), _ptr(iv), _ptr(mass))
     if rc != 0:
         raise ValueError("oracle_score rejected its arguments")
     return iv, mass.reshape(h_q, len(el))
@@ -229,20 +230,21 @@ def select(iv: np.ndarray, keep: int) -> np.ndarray:
     return idx[: int(keep)].copy()
 
 
-def compact(src: np.ndarray, n_v: int, n_t: int, idx: np.ndarray) -> np.ndarray:
-    """Rows [src[idx]; src[N_v:N_v+N_t]] of one (request, layer), dense
-    [keep+N_t, H_kv, D] in the source element type."""
+def compact(src: np.ndarray, n_v: int, n_t: int, idx: np.ndarray, n_p: int = 0) -> np.ndarray:
+    """The kept visual rows (visual indices idx), then every text row in text
+    order, of one (request, layer) whose rows are in prompt order with n_p
+    prefix text rows; dense [keep+N_t, H_kv, D] in the source element type."""
     h_kv, d = src.shape[1], src.shape[2]
     el = np.ascontiguousarray(idx, dtype=np.int32)
     out = np.zeros((len(el) + n_t, h_kv, d), src.dtype)
-    n = lib().oracle_compact(ctypes.byref(_view(src)), h_kv, d, n_v, n_t, _ptr(el),
+    n = lib().oracle_compact(ctypes.byref(_view(src)), h_kv, d, n_v, n_t, int(n_p), _ptr(el),
                              len(el), _ptr(out))
     assert n == len(el) + n_t
     return out
 
 
 def request(q_layers, k_layers, n_v: int, alpha: float, r: float, window_mode: int = 0,
-            budget_mode: int = 0):
+            budget_mode: int = 0, n_p: int = 0):
     """The whole one-shot pass for one request over its layers (optionally
     with an ablation window / budget variant).
 
@@ -259,7 +261,7 @@ def request(q_layers, k_layers, n_v: int, alpha: float, r: float, window_mode: i
     st = np.zeros((L, 4), np.float64)
     keep = np.zeros(L, np.int32)
     idx = np.zeros((L, n_v), np.int32)
-    rc = lib().oracle_request_variant(qv, kv, L, h_q, h_kv, d, n_v, n_t, float(alpha), float(r),
+    rc = lib().oracle_request_variant(qv, kv, L, h_q, h_kv, d, n_v, n_t, int(n_p), float(alpha), float(r),
                                       int(window_mode), int(budget_mode), _ptr(iv), _ptr(el),
                                       _ptr(ntk), _ptr(st), _ptr(keep), _ptr(idx))
     if rc != 0:

@@ -21,7 +21,7 @@ MUTATIONS = {
     "scale by D instead of sqrt(D)": ("return s / sqrt((double)d);", "return s / (double)d;"),
     "softmax drops the elite text keys": ("for (int c = 0; c < n_keys; ++c) z +=",
                                           "for (int c = 0; c < n_v; ++c) z +="),
-    "elite text key index not mapped": ("(int64_t)n_v + elite[e2], kvh, d);", "(int64_t)n_v + e2, kvh, d);"),
+    "elite text key index not mapped": ("text_row(n_p, n_v, elite[e2]), kvh, d);", "text_row(n_p, n_v, e2), kvh, d);"),
     "score query row not mapped": ("const int64_t q_tok = elite[e];", "const int64_t q_tok = e;"),
     "I_v not averaged over heads": ("const double norm = (double)h_q * (double)n_tk;",
                                     "const double norm = (double)n_tk;"),
@@ -33,7 +33,9 @@ MUTATIONS = {
     "budget drops the 1/2": ("const double rl = 0.5 * (st_n[l] + sk_n[l]) * r;", "const double rl = (st_n[l] + sk_n[l]) * r;"),
     "ties go to the higher index": ("return (x->i > y->i) - (x->i < y->i);", "return (x->i < y->i) - (x->i > y->i);"),
     "selection left in score order": ("    qsort(idx, (size_t)keep, sizeof(int32_t), ascending_int);\n", ""),
-    "text rows shifted by one": ("(int64_t)n_v + (j - keep);", "(int64_t)n_v + (j - keep) - (j > keep);"),
+    "text rows shifted by one": ("text_row(n_p, n_v, j - keep);", "text_row(n_p, n_v, j - keep) - (j > keep);"),
+    "visual rows ignore the prefix": ("return (int64_t)n_p + i;", "return (int64_t)i;"),
+    "text rows ignore the prefix": ("return j < n_p ? (int64_t)j : (int64_t)n_v + j;", "return (int64_t)n_v + j;"),
     "decode head map h mod h_kv": ("const int kv_head = h / group;", "const int kv_head = h % h_kv;"),
     "decode weights not normalised": ("acc += w[j] / total * elem(v, j, kv_head, i);",
                                       "acc += w[j] * elem(v, j, kv_head, i);"),
@@ -49,7 +51,8 @@ MUTATIONS = {
     "one head's scale for every head": ("const float a = fabsf((float)elem(src, j, h, i));",
                                         "const float a = fabsf((float)elem(src, j, 0, i));"),
 }
-PIN_FILES = ["test_oracle_pins.py", "test_oracle_variants.py", "test_oracle_decode.py", "test_oracle_quant.py"]
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_variants.py", "test_oracle_decode.py", "test_oracle_quant.py",
+             "test_oracle_prefix.py"]
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
