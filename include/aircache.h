@@ -35,7 +35,8 @@
  * - Layout (varlen, token-major, like FlashAttention's varlen convention):
  *   request b owns prompt positions cu_seqlens[b] .. cu_seqlens[b+1]-1 of every
  *   layer's K and V; its first N_v[b] = cu_visual[b+1]-cu_visual[b] positions
- *   are visual, the remaining N_t[b] are text (visual first, X = Concat(X_v, X_t)).
+ *   are visual, the remaining N_t[b] are text (visual first, X = Concat(X_v, X_t)),
+ *   unless n_prefix puts some text before the visual span.
  *   Its text queries are rows cu_seqlens[b]-cu_visual[b] .. +N_t[b]-1 of the
  *   layer's Q_text.  K/V rows are [h_kv][head_dim], Q rows [h_q][head_dim], with
  *   element strides per token and per head; head_dim is contiguous.
@@ -113,6 +114,16 @@ typedef struct aircache_problem {
     int64_t kv_stride_head; /* elements between consecutive KV heads */
     double alpha;           /* elite threshold, [0, 1] (the notes use 0.9) */
     double r;               /* mean visual retention ratio, (0, 1] */
+    const int32_t* n_prefix;  /* optional device [B] (NULL: all 0): text tokens of request b
+                                 BEFORE its visual span (a system prompt; the multimodal-
+                                 layout page puts it there).  Request b's prompt is then
+                                 [n_prefix[b] text][N_v[b] visual][the other text]; its
+                                 text rows in q_text are all of its text tokens in prompt
+                                 order; 0 <= n_prefix[b] <= N_t[b], else a device error
+                                 AIRCACHE_ERR_DEVICE_BOUNDS.  Text is every non-visual
+                                 token: the elite window and the scoring run over text
+                                 indices as before, and compaction writes the kept visual
+                                 rows, then every text row in text order. */
 } aircache_problem;
 
 /*

@@ -65,6 +65,7 @@ class ProblemStruct(ctypes.Structure):
         ("kv_stride_head", ctypes.c_int64),
         ("alpha", ctypes.c_double),
         ("r", ctypes.c_double),
+        ("n_prefix", ctypes.c_void_p),
     ]
 
 
@@ -180,7 +181,8 @@ class Problem:
     """
 
     def __init__(self, q, k, v, cu_seqlens, cu_visual, max_visual, max_text, alpha=0.9, r=0.1,
-                 max_elite=0, total_tokens=None, total_visual=None, window_mode=0, budget_mode=0):
+                 max_elite=0, total_tokens=None, total_visual=None, window_mode=0, budget_mode=0,
+                 n_prefix=None):
         qs = list(q.unbind(0)) if torch.is_tensor(q) else list(q)
         ks = list(k.unbind(0)) if torch.is_tensor(k) else list(k)
         vs = list(v.unbind(0)) if torch.is_tensor(v) else list(v)
@@ -218,7 +220,9 @@ class Problem:
             q_stride_tok=qs[0].stride(0), q_stride_head=qs[0].stride(1),
             kv_stride_tok=ks[0].stride(0), kv_stride_head=ks[0].stride(1),
             alpha=float(alpha), r=float(r),
+            n_prefix=n_prefix.data_ptr() if n_prefix is not None else None,
         )
+        self.n_prefix = n_prefix  # keep alive
         for t in ks + vs + qs:
             if t.stride(2) != 1:
                 raise ValueError("head_dim must be contiguous")

@@ -114,6 +114,7 @@ Dev make_dev(const aircache_problem* p) {
   d.total_text = p->total_tokens - p->total_visual;
   d.cu_seqlens = p->cu_seqlens;
   d.cu_visual = p->cu_visual;
+  d.n_prefix = p->n_prefix;
   d.q_stride_tok = p->q_stride_tok;
   d.q_stride_head = p->q_stride_head;
   d.kv_stride_tok = p->kv_stride_tok;

@@ -68,21 +68,20 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_cons
     Req R;
     const bool ok = load_req(p, b, R);
     const int kp = w.keep[u];
-    int64_t pos;
+    // kept visual rows first, then every text row in text order
+    int64_t tok = -1;
     if (j < kp) {
-      pos = w.idx[(size_t)l * p.total_visual + R.vis0 + j];
-      if (pos < 0 || pos >= R.n_v) pos = -1;
-    } else {
-      pos = (int64_t)R.n_v + (j - kp);
-      if (pos >= (int64_t)R.n_v + R.n_t) pos = -1;
+      const int64_t pos = w.idx[(size_t)l * p.total_visual + R.vis0 + j];
+      if (pos >= 0 && pos < R.n_v) tok = vis_tok(R, pos);
+    } else if (j - kp < R.n_t) {
+      tok = text_tok(R, j - kp);
     }
-    if (!ok || pos < 0) {
+    if (!ok || tok < 0) {
       if (lane == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
       continue;
     }
     const char* kb = reinterpret_cast<const char*>(a.lp.k[l]);
     const char* vb = reinterpret_cast<const char*>(a.lp.v[l]);
-    const int64_t tok = R.seq0 + pos;
     uint4 kbuf[4], vbuf[4];
     for (int v0 = 0; v0 < vec_per_row; v0 += 4 * 32) {
 #pragma unroll

@@ -50,7 +50,7 @@ __device__ __forceinline__ void load_item(const Dev& p, const Req& R, const char
     const char* src = kbase;
     int bytes = 0;
     if (key < R.n_t) {
-      src = kbase + ((R.seq0 + R.n_v + key) * p.kv_stride_tok + (int64_t)kvh * p.kv_stride_head) * sizeof(T) + 16 * v;
+      src = kbase + (text_tok(R, key) * p.kv_stride_tok + (int64_t)kvh * p.kv_stride_head) * sizeof(T) + 16 * v;
       bytes = 16;
     }
     cp_async16(stage + row * G::kRowPitch + 16 * v, src, bytes);
@@ -271,7 +271,7 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
           const int kvh = kvb + r / n_tk, e = r % n_tk;
           const int pos = min(max(pos_s[e], 0), n_t - 1);
           v[q] = __ldg(reinterpret_cast<const uint4*>(
-                           kbase + ((R.seq0 + R.n_v + pos) * p.kv_stride_tok + (int64_t)kvh * p.kv_stride_head) *
+                           kbase + (text_tok(R, pos) * p.kv_stride_tok + (int64_t)kvh * p.kv_stride_head) *
                                        sizeof(T)) +
                        c);
         }
@@ -290,8 +290,10 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
   }
   if (rank == 0 && tid == 0) {
     a.w.n_tk[u] = base;
-    // the unit's layout, so that the scoring kernel resolves a work item with one load
-    a.w.uinfo[2 * u] = make_int4((int)R.seq0, (int)R.vis0, (int)R.txt0, R.n_v);
+    // the unit's layout, so that the scoring kernel resolves a work item with one
+    // load; .x is the first VISUAL prompt position (the scoring kernels read
+    // visual keys only: the elite text keys are gathered here)
+    a.w.uinfo[2 * u] = make_int4((int)vis_tok(R, 0), (int)R.vis0, (int)R.txt0, R.n_v);
     a.w.uinfo[2 * u + 1] = make_int4(R.n_t, base, 1, 0);
     if (base > p.max_elite) {
       set_error(a.w.error, AIRCACHE_ERR_ELITE_OVERFLOW);
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
         const int slot = p.g * base > kRowChunk ? atomicAdd(&a.w.list_n[2], 1)
                                                 : p.L * p.B - 1 - atomicAdd(&a.w.list_n[3], 1);
         a.w.stream_list[slot] = u;
-        a.w.stream_info[2 * slot] = make_int4((int)R.seq0, (int)R.vis0, (int)R.txt0, R.n_v);
+        a.w.stream_info[2 * slot] = make_int4((int)vis_tok(R, 0), (int)R.vis0, (int)R.txt0, R.n_v);
         a.w.stream_info[2 * slot + 1] = make_int4(R.n_t, base, 1, u);
       } else {
         a.w.wide_list[atomicAdd(&a.w.list_n[1], 1)] = u;

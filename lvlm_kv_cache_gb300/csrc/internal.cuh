@@ -22,6 +22,7 @@ struct Dev {
   int64_t total_tokens, total_visual, total_text;
   const int32_t* cu_seqlens;
   const int32_t* cu_visual;
+  const int32_t* n_prefix;  // optional [B]: text tokens before the visual span
   int64_t q_stride_tok, q_stride_head, kv_stride_tok, kv_stride_head;
   double alpha, r;
   float scale_log2;      // log2(e) / sqrt(D): logits are kept in base 2
@@ -87,6 +88,7 @@ struct Req {
   int64_t vis0;   // first I_v slot
   int64_t txt0;   // first Q_text row
   int n_v, n_t;
+  int n_p;        // text tokens before the visual span
 };
 
 __device__ __forceinline__ void set_error(int32_t* err, int code) {
@@ -102,12 +104,22 @@ __device__ __forceinline__ bool load_req(const Dev& p, int b, Req& r) {
             (s0 - v0) >= 0 && (s0 - v0) + n_t <= p.total_text;
   if (b == 0) ok = ok && s0 == 0 && v0 == 0;
   if (b == p.B - 1) ok = ok && s1 == p.total_tokens && v1 == p.total_visual;
+  const int64_t n_p = p.n_prefix ? p.n_prefix[b] : 0;
+  ok = ok && n_p >= 0 && n_p <= n_t;
   r.seq0 = s0;
   r.vis0 = v0;
   r.txt0 = s0 - v0;
   r.n_v = (int)n_v;
   r.n_t = (int)n_t;
+  r.n_p = ok ? (int)n_p : 0;
   return ok;
+}
+
+// Prompt positions (rows of K and V) of visual index i and text index j: the
+// prompt is [n_p text][n_v visual][n_t - n_p text].
+__device__ __forceinline__ int64_t vis_tok(const Req& r, int64_t i) { return r.seq0 + r.n_p + i; }
+__device__ __forceinline__ int64_t text_tok(const Req& r, int64_t j) {
+  return r.seq0 + j + (j >= r.n_p ? r.n_v : 0);
 }
 
 // Launch plan of the persistent scoring kernel.

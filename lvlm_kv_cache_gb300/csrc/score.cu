@@ -257,7 +257,7 @@ __device__ __forceinline__ bool unit_valid(const Dev& p, const int4& i0, const i
   const long long seq0 = i0.x, vis0 = i0.y, txt0 = i0.z;
   const int n_v = i0.w, n_t = i1.x, n_tk = i1.y;
   return i1.z == 1 && n_tk >= 1 && n_tk <= p.max_elite && n_tk <= n_t && n_v >= 3 && n_v <= p.max_visual &&
-         seq0 >= 0 && seq0 + n_v + n_t <= p.total_tokens && txt0 >= 0 && txt0 + n_t <= p.total_text &&
+         seq0 >= 0 && seq0 + n_v <= p.total_tokens && txt0 >= 0 && txt0 + n_t <= p.total_text &&
          vis0 >= 0 && vis0 + n_v <= p.total_visual;
 }
 

@@ -110,7 +110,7 @@ __device__ __forceinline__ float2 merge_ms(float2 a, float2 b) {
 __device__ __forceinline__ bool stream_unit(const Dev& p, int u, const int4& i0, const int4& i1) {
   const int n_v = i0.w, n_t = i1.x, n_tk = i1.y;
   return u >= 0 && u < p.L * p.B && i1.z == 1 && n_tk >= 1 && n_tk <= n_t && n_tk <= p.max_elite &&
-         n_v >= 3 && n_v <= p.max_visual && i0.x >= 0 && (long long)i0.x + n_v + n_t <= p.total_tokens &&
+         n_v >= 3 && n_v <= p.max_visual && i0.x >= 0 && (long long)i0.x + n_v <= p.total_tokens &&
          i0.y >= 0 && (long long)i0.y + n_v <= p.total_visual;
 }
 

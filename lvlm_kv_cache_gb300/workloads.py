@@ -207,6 +207,27 @@ def host_bits(t: torch.Tensor) -> np.ndarray:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
+def with_prefix(wl: Workload, n_prefix) -> tuple:
+    """The same tokens with the first n_prefix[b] text tokens of request b moved
+    before its visual span (prompt order [prefix text][visual][other text]).
+    Returns (k, v, n_prefix int32 tensor on the workload's device); q (text rows
+    in text order), cu_seqlens and cu_visual are unchanged."""
+    s = wl.spec
+    cu_s, cu_v, _ = offsets(s)
+    perm = np.arange(cu_s[-1])
+    for b in range(s.B):
+        s0, nv, nt, npf = cu_s[b], s.n_visual[b], s.n_text[b], int(n_prefix[b])
+        if not 0 <= npf <= nt:
+            raise ValueError("0 <= n_prefix <= N_t")
+        # new row r of the request takes old (visual-first) row perm[r]
+        old = np.concatenate([np.arange(nv, nv + npf), np.arange(nv), np.arange(nv + npf, nv + nt)])
+        perm[s0:s0 + nv + nt] = s0 + old
+    idx = torch.as_tensor(perm, device=wl.k.device)
+    k = wl.k[:, idx].contiguous()
+    v = wl.v[:, idx].contiguous()
+    return k, v, torch.tensor([int(x) for x in n_prefix], dtype=torch.int32, device=wl.k.device)
+
+
 @dataclasses.dataclass
 class DecodeInputs:
     q: torch.Tensor        # [S, H_q, D]
