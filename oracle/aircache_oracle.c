@@ -56,6 +56,13 @@
  *       indices unchanged (the last text query is the prompt's last token);
  *       compaction writes the kept visual rows, then the text rows in text
  *       order.  n_p = 0 is the layout X = Concat(X_v, X_t).
+ *   R19 one index set per KV head (the edge-device compression page: group-wise
+ *       top-k, one decision per KV group): I_v^(h) averages the visual columns
+ *       over the g query heads of KV group h and the elite rows, so that
+ *       mean_h I_v^(h) = I_v; the layer's budget keep_l stays the one of I_v;
+ *       KV head h keeps the keep_l visual positions with the largest I_v^(h)
+ *       (R8's tie and order rules), and its compacted rows are those
+ *       positions, then every text row.
  *   R17 int8 storage of the kept cache (LLM KV-compression notes, section
  *       "Quantization stacked on compression": quantise after the token
  *       compression, one scale per head = the head's largest |value| over the
@@ -170,7 +177,7 @@ int oracle_elite(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, 
  */
 int oracle_score(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, int d,
                  int n_v, int n_t, int n_p, const int32_t* elite, int n_tk,
-                 double* iv, double* elite_mass) {
+                 double* iv, double* elite_mass, double* iv_heads) {
     if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || n_v <= 0 || n_tk <= 0 || n_p < 0 || n_p > n_t) return -1;
     for (int e = 0; e < n_tk; ++e) {
         if (elite[e] < 0 || elite[e] >= n_t) return -1;
@@ -180,6 +187,7 @@ int oracle_score(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, 
     double* logit = (double*)malloc(sizeof(double) * (size_t)n_keys);
     if (!logit) return -1;
     for (int i = 0; i < n_v; ++i) iv[i] = 0.0;
+    if (iv_heads) for (int64_t i = 0; i < (int64_t)h_kv * n_v; ++i) iv_heads[i] = 0.0;
 
     for (int h = 0; h < h_q; ++h) {
         const int kvh = h / g;
@@ -197,6 +205,8 @@ int oracle_score(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, 
             double z = 0.0;
             for (int c = 0; c < n_keys; ++c) z += exp(logit[c] - m);
             for (int c = 0; c < n_v; ++c) iv[c] += exp(logit[c] - m) / z;
+            if (iv_heads)
+                for (int c = 0; c < n_v; ++c) iv_heads[(int64_t)kvh * n_v + c] += exp(logit[c] - m) / z;
             if (elite_mass) {
                 double mass = 0.0;
                 for (int e2 = 0; e2 < n_tk; ++e2) mass += exp(logit[n_v + e2] - m) / z;
@@ -206,6 +216,10 @@ int oracle_score(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, 
     }
     const double norm = (double)h_q * (double)n_tk;
     for (int i = 0; i < n_v; ++i) iv[i] /= norm;
+    if (iv_heads) {
+        const double norm_h = (double)g * (double)n_tk;  /* R19: a group's g query heads */
+        for (int64_t i = 0; i < (int64_t)h_kv * n_v; ++i) iv_heads[i] /= norm_h;
+    }
     free(logit);
     return 0;
 }
@@ -430,7 +444,7 @@ int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t
 int oracle_request_variant(const oracle_view* q, const oracle_view* k, int n_layers, int h_q,
                            int h_kv, int d, int n_v, int n_t, int n_p, double alpha, double r, int window_mode,
                            int budget_mode, double* iv, int32_t* elite, int32_t* n_tk, double* stats,
-                           int32_t* keep, int32_t* idx) {
+                           int32_t* keep, int32_t* idx, double* iv_heads, int32_t* idx_heads) {
     double* s_t = (double*)malloc(sizeof(double) * (size_t)n_layers);
     double* s_k = (double*)malloc(sizeof(double) * (size_t)n_layers);
     if (!s_t || !s_k) { free(s_t); free(s_k); return -1; }
@@ -442,13 +456,19 @@ int oracle_request_variant(const oracle_view* q, const oracle_view* k, int n_lay
         if (ntk <= 0) { rc = -1; break; }
         n_tk[l] = ntk;
         double* ivl = iv + (int64_t)l * n_v;
-        rc = oracle_score(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, n_p, el, ntk, ivl, NULL);
+        rc = oracle_score(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, n_p, el, ntk, ivl, NULL,
+                          iv_heads ? iv_heads + (int64_t)l * h_kv * n_v : NULL);
         if (rc == 0) rc = oracle_stats(ivl, n_v, stats + (int64_t)l * 4);
         if (rc == 0) { s_t[l] = stats[l * 4 + 0]; s_k[l] = stats[l * 4 + 1]; }
     }
     if (rc == 0) rc = oracle_budget_variant(s_t, s_k, n_layers, n_v, r, budget_mode, NULL, keep);
     for (int l = 0; l < n_layers && rc == 0; ++l) {
         rc = oracle_select(iv + (int64_t)l * n_v, n_v, keep[l], idx + (int64_t)l * n_v);
+        /* R19: each KV head's own set, with the layer's keep count */
+        for (int h = 0; h < h_kv && rc == 0 && iv_heads && idx_heads; ++h) {
+            const int64_t o = ((int64_t)l * h_kv + h) * n_v;
+            rc = oracle_select(iv_heads + o, n_v, keep[l], idx_heads + o);
+        }
     }
     free(s_t);
     free(s_k);
@@ -461,7 +481,7 @@ int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int
                    double* iv, int32_t* elite, int32_t* n_tk, double* stats,
                    int32_t* keep, int32_t* idx) {
     return oracle_request_variant(q, k, n_layers, h_q, h_kv, d, n_v, n_t, 0, alpha, r, 0, 0, iv, elite,
-                                  n_tk, stats, keep, idx);
+                                  n_tk, stats, keep, idx, NULL, NULL);
 }
 
 /* ------------------------------------------------------- decode consumer */
@@ -546,4 +566,25 @@ int oracle_quantize_int8(const oracle_view* src, int64_t n_rows, int h_kv, int d
                 codes[(j * h_kv + h) * d + i] = (int8_t)oracle_quant_code((float)elem(src, j, h, i), s);
     }
     return 0;
+}
+
+/*
+ * R19 compaction with one index set per KV head: row j of head h is visual
+ * position idx_heads[h * n_v + j] (j < keep) or text index j - keep, in the
+ * prompt layout of R18.  dst: dense [keep + n_t][h_kv][d].  Returns the rows.
+ */
+int64_t oracle_compact_heads(const oracle_view* src, int h_kv, int d, int n_v, int n_t, int n_p,
+                             const int32_t* idx_heads, int keep, void* dst) {
+    if (n_p < 0 || n_p > n_t) return -1;
+    const size_t esize = (src->dtype == ORACLE_F32) ? 4 : 2;
+    unsigned char* out = (unsigned char*)dst;
+    for (int j = 0; j < keep + n_t; ++j) {
+        for (int h = 0; h < h_kv; ++h) {
+            const int64_t tok = (j < keep) ? vis_row(n_p, idx_heads[(int64_t)h * n_v + j]) : text_row(n_p, n_v, j - keep);
+            const unsigned char* from = (const unsigned char*)src->base +
+                (size_t)(tok * src->stride_tok + h * src->stride_head) * esize;
+            memcpy(out + ((size_t)j * h_kv + h) * d * esize, from, (size_t)d * esize);
+        }
+    }
+    return (int64_t)keep + n_t;
 }

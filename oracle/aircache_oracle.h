@@ -26,7 +26,7 @@ int oracle_elite(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, 
                  int n_v, int n_t, int n_p, double alpha, double* p_out, int32_t* elite);
 int oracle_score(const oracle_view* q, const oracle_view* k, int h_q, int h_kv, int d,
                  int n_v, int n_t, int n_p, const int32_t* elite, int n_tk,
-                 double* iv, double* elite_mass);
+                 double* iv, double* elite_mass, double* iv_heads);
 int oracle_stats(const double* iv, int n_v, double* out);
 int oracle_budget(const double* s_t, const double* s_k, int n_layers, int n_v, double r,
                   double* r_l, int32_t* keep);
@@ -44,7 +44,9 @@ int oracle_budget_variant(const double* s_t, const double* s_k, int n_layers, in
 int oracle_request_variant(const oracle_view* q, const oracle_view* k, int n_layers, int h_q,
                            int h_kv, int d, int n_v, int n_t, int n_p, double alpha, double r, int window_mode,
                            int budget_mode, double* iv, int32_t* elite, int32_t* n_tk, double* stats,
-                           int32_t* keep, int32_t* idx);
+                           int32_t* keep, int32_t* idx, double* iv_heads, int32_t* idx_heads);
+int64_t oracle_compact_heads(const oracle_view* src, int h_kv, int d, int n_v, int n_t, int n_p,
+                             const int32_t* idx_heads, int keep, void* dst);
 int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int h_q, int h_kv,
                    int d, int n_v, int n_t, double alpha, double r,
                    double* iv, int32_t* elite, int32_t* n_tk, double* stats,

@@ -63,7 +63,7 @@ def lib():
         V = ctypes.POINTER(_View)
         L.oracle_elite.argtypes = [V, V, i32, i32, i32, i32, i32, i32, f64, vp, vp]
         L.oracle_elite.restype = i32
-        L.oracle_score.argtypes = [V, V, i32, i32, i32, i32, i32, i32, vp, i32, vp, vp]
+        L.oracle_score.argtypes = [V, V, i32, i32, i32, i32, i32, i32, vp, i32, vp, vp, vp]
         L.oracle_score.restype = i32
         L.oracle_stats.argtypes = [vp, i32, vp]
         L.oracle_stats.restype = i32
@@ -87,7 +87,9 @@ def lib():
         L.oracle_budget_variant.argtypes = [vp, vp, i32, i32, f64, i32, vp, vp]
         L.oracle_budget_variant.restype = i32
         L.oracle_request_variant.argtypes = [V, V, i32, i32, i32, i32, i32, i32, i32, f64, f64, i32, i32,
-                                             vp, vp, vp, vp, vp, vp]
+                                             vp, vp, vp, vp, vp, vp, vp, vp]
+        L.oracle_compact_heads.argtypes = [V, i32, i32, i32, i32, i32, vp, i32, vp]
+        L.oracle_compact_heads.restype = i64
         L.oracle_request_variant.restype = i32
         _lib = L
     return _lib
@@ -139,10 +141,40 @@ def score(q: np.ndarray, k: np.ndarray, n_v: int, elite_idx: np.ndarray, n_p: in
     iv = np.zeros(n_v, np.float64)
     mass = np.zeros(h_q * len(el), np.float64)
     rc = lib().oracle_score(ctypes.byref(_view(q)), ctypes.byref(_view(k)), h_q, h_kv, d,
-                            n_v, n_t, int(n_p), _ptr(el), len(el), _ptr(iv), _ptr(mass))
+                            n_v, n_t, int(n_p), _ptr(el), len(el), _ptr(iv), _ptr(mass), None)
     if rc != 0:
         raise ValueError("oracle_score rejected its arguments")
     return iv, mass.reshape(h_q, len(el))
+
+
+def score_heads(q: np.ndarray, k: np.ndarray, n_v: int, elite_idx: np.ndarray, n_p: int = 0):
+    """I_v and the per-KV-head I_v^(h) [H_kv, N_v] of one (request, layer) for a
+    given elite set (reading R19)."""
+    n_t, h_q, d = q.shape
+    h_kv = k.shape[1]
+    el = np.ascontiguousarray(elite_idx, dtype=np.int32)
+    iv = np.zeros(n_v, np.float64)
+    ivh = np.zeros((h_kv, n_v), np.float64)
+    rc = lib().oracle_score(ctypes.byref(_view(q)), ctypes.byref(_view(k)), h_q, h_kv, d,
+                            n_v, n_t, int(n_p), _ptr(el), len(el), _ptr(iv), None, _ptr(ivh))
+    if rc != 0:
+        raise ValueError("oracle_score rejected its arguments")
+    return iv, ivh
+
+
+def compact_heads(src: np.ndarray, n_v: int, n_t: int, idx_heads, n_p: int = 0) -> np.ndarray:
+    """Compaction with one visual index set per KV head (reading R19): idx_heads
+    [H_kv, keep]; dense [keep+N_t, H_kv, D]."""
+    h_kv, d = src.shape[1], src.shape[2]
+    ih = np.asarray(idx_heads, dtype=np.int32)
+    keep = ih.shape[1]
+    full = np.zeros((h_kv, n_v), np.int32)
+    full[:, :keep] = ih
+    out = np.zeros((keep + n_t, h_kv, d), src.dtype)
+    n = lib().oracle_compact_heads(ctypes.byref(_view(src)), h_kv, d, n_v, n_t, int(n_p), _ptr(full), keep,
+                                   _ptr(out))
+    assert n == keep + n_t
+    return out
 
 
 def stats(iv: np.ndarray):
@@ -244,7 +276,7 @@ def compact(src: np.ndarray, n_v: int, n_t: int, idx: np.ndarray, n_p: int = 0) 
 
 
 def request(q_layers, k_layers, n_v: int, alpha: float, r: float, window_mode: int = 0,
-            budget_mode: int = 0, n_p: int = 0):
+            budget_mode: int = 0, n_p: int = 0, per_head: bool = False):
     """The whole one-shot pass for one request over its layers (optionally
     with an ablation window / budget variant).
 
@@ -261,9 +293,12 @@ def request(q_layers, k_layers, n_v: int, alpha: float, r: float, window_mode: i
     st = np.zeros((L, 4), np.float64)
     keep = np.zeros(L, np.int32)
     idx = np.zeros((L, n_v), np.int32)
+    ivh = np.zeros((L, h_kv, n_v), np.float64) if per_head else None
+    idxh = np.zeros((L, h_kv, n_v), np.int32) if per_head else None
     rc = lib().oracle_request_variant(qv, kv, L, h_q, h_kv, d, n_v, n_t, int(n_p), float(alpha), float(r),
                                       int(window_mode), int(budget_mode), _ptr(iv), _ptr(el),
-                                      _ptr(ntk), _ptr(st), _ptr(keep), _ptr(idx))
+                                      _ptr(ntk), _ptr(st), _ptr(keep), _ptr(idx),
+                                      _ptr(ivh) if per_head else None, _ptr(idxh) if per_head else None)
     if rc != 0:
         raise ValueError("oracle_request rejected its arguments")
     return {
@@ -273,4 +308,5 @@ def request(q_layers, k_layers, n_v: int, alpha: float, r: float, window_mode: i
         "stats": st,
         "keep": keep,
         "idx": [idx[l, : keep[l]].copy() for l in range(L)],
+        **({"iv_heads": ivh, "idx_heads": [idxh[l, :, : keep[l]].copy() for l in range(L)]} if per_head else {}),
     }

@@ -33,7 +33,13 @@ MUTATIONS = {
     "budget drops the 1/2": ("const double rl = 0.5 * (st_n[l] + sk_n[l]) * r;", "const double rl = (st_n[l] + sk_n[l]) * r;"),
     "ties go to the higher index": ("return (x->i > y->i) - (x->i < y->i);", "return (x->i < y->i) - (x->i > y->i);"),
     "selection left in score order": ("    qsort(idx, (size_t)keep, sizeof(int32_t), ascending_int);\n", ""),
-    "text rows shifted by one": ("text_row(n_p, n_v, j - keep);", "text_row(n_p, n_v, j - keep) - (j > keep);"),
+    "text rows shifted by one": ("? vis_row(n_p, idx[j]) : text_row(n_p, n_v, j - keep);",
+                                 "? vis_row(n_p, idx[j]) : text_row(n_p, n_v, j - keep) - (j > keep);"),
+    "per-head I_v normalised over all heads": ("const double norm_h = (double)g * (double)n_tk;",
+                                               "const double norm_h = (double)h_q * (double)n_tk;"),
+    "per-head I_v all into head 0": ("iv_heads[(int64_t)kvh * n_v + c] +=", "iv_heads[(int64_t)0 * n_v + c] +="),
+    "per-head compaction reads head 0's set": ("vis_row(n_p, idx_heads[(int64_t)h * n_v + j])",
+                                               "vis_row(n_p, idx_heads[j])"),
     "visual rows ignore the prefix": ("return (int64_t)n_p + i;", "return (int64_t)i;"),
     "text rows ignore the prefix": ("return j < n_p ? (int64_t)j : (int64_t)n_v + j;", "return (int64_t)n_v + j;"),
     "decode head map h mod h_kv": ("const int kv_head = h / group;", "const int kv_head = h % h_kv;"),
@@ -52,7 +58,7 @@ MUTATIONS = {
                                         "const float a = fabsf((float)elem(src, j, 0, i));"),
 }
 PIN_FILES = ["test_oracle_pins.py", "test_oracle_variants.py", "test_oracle_decode.py", "test_oracle_quant.py",
-             "test_oracle_prefix.py"]
+             "test_oracle_prefix.py", "test_oracle_heads.py"]
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
