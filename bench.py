@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--budget-mode", type=int, default=0,
                     help="ablation budget: 0 strength + skewness (the method), 1 uniform, 2 PyramidKV-style, "
                          "3 strength only, 4 skewness only")
+    ap.add_argument("--head-sets", action="store_true",
+                    help="one visual index set per KV head (group-wise top-k) instead of one per layer")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.5, help="untimed back-to-back load before timing")
@@ -507,7 +509,7 @@ def main():
     esize = 2 if spec.dtype == torch.bfloat16 else 4
     prob = A.Problem(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.cu_visual, max(spec.n_visual), max(spec.n_text),
                      spec.alpha, spec.r, total_tokens=wl.total_tokens, total_visual=wl.total_visual,
-                     window_mode=args.window_mode, budget_mode=args.budget_mode)
+                     window_mode=args.window_mode, budget_mode=args.budget_mode, head_sets=args.head_sets)
     ws = prob.new_workspace()
     out = A.alloc_outputs(prob)
     L, B, TV = prob.L, prob.B, prob.total_visual
@@ -615,7 +617,8 @@ def main():
         "data": "synthetic",
         "config": {"workload": DESCRIPTIONS.get(args.config, args.config), "name": args.config,
                    "requests_per_rank": spec.B, "layers": spec.L, "seed": "rank",
-                   "variant": {"window_mode": args.window_mode, "budget_mode": args.budget_mode},
+                   "variant": {"window_mode": args.window_mode, "budget_mode": args.budget_mode,
+                               "head_sets": bool(args.head_sets)},
                    "l2": "flushed before every timed step outside the events: 256 MB written, then read back "
                          "(so the flush's own dirty lines are not written back inside the step)"},
         "requests_per_s": world * spec.B * args.steps / (total_ms / 1e3),

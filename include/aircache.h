@@ -100,7 +100,15 @@ typedef struct aircache_problem {
                             * bits 8-15 the layer budget -- 0 strength + skewness, 1
                             * uniform (r_l = r), 2 PyramidKV-style (linear in depth from
                             * (2 - 1/20) r to r/20), 3 strength only (s'_t r), 4
-                            * skewness only (s'_k r); other bits 0. */
+                            * skewness only (s'_k r); bits 16-23 the index sets -- 0
+                            * one per layer, shared by the KV heads, 1 one per KV head
+                            * (the edge-device compression page's group-wise top-k:
+                            * KV head h keeps the keep_l visual positions with the
+                            * largest I_v of its own g query heads; the budget stays
+                            * the layer's; aircache_compress on the streaming path only
+                            * -- else AIRCACHE_ERR_UNSUPPORTED, as from the staged
+                            * calls -- and idx is then [L][h_kv][total_visual]);
+                            * other bits 0. */
     int64_t total_tokens;  /* == cu_seqlens[B] */
     int64_t total_visual;  /* == cu_visual[B] */
     const int32_t* cu_seqlens;  /* device [B+1], non-decreasing, cu_seqlens[0] == 0 */
@@ -221,7 +229,7 @@ AIRCACHE_API int aircache_compact(const aircache_problem* p, const int32_t* idx,
 /*
  * Steps 1-4 in one call on one stream (the one-shot schedule: every layer is
  * scored, then every budget is set, then every layer is compacted).
- * keep [L][B] is required; iv [L][total_visual] and idx [L][total_visual] are
+ * keep [L][B] is required; iv [L][total_visual] and idx [L][total_visual] ([L][h_kv][total_visual] with one index set per KV head) are
  * optional (NULL keeps them inside the workspace).  Outputs as above.
  */
 AIRCACHE_API int aircache_compress(const aircache_problem* p, void* ws, size_t ws_bytes,

@@ -182,7 +182,7 @@ class Problem:
 
     def __init__(self, q, k, v, cu_seqlens, cu_visual, max_visual, max_text, alpha=0.9, r=0.1,
                  max_elite=0, total_tokens=None, total_visual=None, window_mode=0, budget_mode=0,
-                 n_prefix=None):
+                 n_prefix=None, head_sets=False):
         qs = list(q.unbind(0)) if torch.is_tensor(q) else list(q)
         ks = list(k.unbind(0)) if torch.is_tensor(k) else list(k)
         vs = list(v.unbind(0)) if torch.is_tensor(v) else list(v)
@@ -200,6 +200,7 @@ class Problem:
         if TV is None:
             TV = int(cu_visual[-1].item())
         self.B, self.L = B, L
+        self.head_sets = bool(head_sets)
         self.h_q, self.h_kv, self.d = int(qs[0].shape[1]), int(ks[0].shape[1]), int(ks[0].shape[2])
         self.total_tokens, self.total_visual = T, TV
         self.cu_seqlens, self.cu_visual = cu_seqlens, cu_visual
@@ -211,7 +212,7 @@ class Problem:
             num_layers=L, num_requests=B, h_q=self.h_q, h_kv=self.h_kv, head_dim=self.d,
             dtype=BF16 if dt == torch.bfloat16 else F32,
             max_visual=int(max_visual), max_text=int(max_text), max_elite=int(max_elite),
-            variant=int(window_mode) | (int(budget_mode) << 8),
+            variant=int(window_mode) | (int(budget_mode) << 8) | ((1 << 16) if head_sets else 0),
             total_tokens=T, total_visual=TV,
             cu_seqlens=cu_seqlens.data_ptr(), cu_visual=cu_visual.data_ptr(),
             q_text=ctypes.cast(self._q, ctypes.POINTER(ctypes.c_void_p)),
@@ -334,7 +335,8 @@ def alloc_outputs(prob: Problem, device=None):
         "out_v": torch.empty((rows, prob.h_kv, prob.d), dtype=prob.dtype, device=dev),
         "out_offsets": torch.empty(L * B + 1, dtype=torch.int64, device=dev),
         "keep": torch.empty(L * B, dtype=torch.int32, device=dev),
-        "idx": torch.empty((L, prob.total_visual), dtype=torch.int32, device=dev),
+        "idx": torch.empty((L, prob.h_kv, prob.total_visual) if prob.head_sets else (L, prob.total_visual),
+                           dtype=torch.int32, device=dev),
         "iv": torch.empty((L, prob.total_visual), dtype=torch.float32, device=dev),
     }
 

@@ -62,7 +62,8 @@ int validate(const aircache_problem* p) {
   if (p->max_visual < 3 || p->max_text < 1) return AIRCACHE_ERR_INVALID_ARG;
   if (p->max_text > AIRCACHE_MAX_TEXT) return AIRCACHE_ERR_UNSUPPORTED;
   if (p->max_elite < 0 || p->max_elite > p->max_text) return AIRCACHE_ERR_INVALID_ARG;
-  if ((p->variant & ~0xffff) != 0 || (p->variant & 0xff) > 3 || ((p->variant >> 8) & 0xff) > 4) {
+  if ((p->variant & ~0xffffff) != 0 || (p->variant & 0xff) > 3 || ((p->variant >> 8) & 0xff) > 4 ||
+      ((p->variant >> 16) & 0xff) > 1) {
     return AIRCACHE_ERR_INVALID_ARG;
   }
   const int64_t B = p->num_requests;
@@ -123,6 +124,7 @@ Dev make_dev(const aircache_problem* p) {
   d.r = p->r;
   d.window_mode = p->variant & 0xff;
   d.budget_mode = (p->variant >> 8) & 0xff;
+  d.head_sets = (p->variant >> 16) & 0xff;
   d.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->head_dim));
   const int tv = (d.max_visual + 127) / 128;
   d.chn = (tv + kStreamTiles - 1) / kStreamTiles + 1;
@@ -194,7 +196,10 @@ size_t carve(const Dev& d, char* base, Ws* w) {
   t.iv = reinterpret_cast<float*>(take(sizeof(float) * (size_t)d.L * d.total_visual));
   t.stats = reinterpret_cast<double*>(take(sizeof(double) * 2 * LB));
   t.keep = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
-  t.idx = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * (size_t)d.L * d.total_visual));
+  // one index set per (layer, request), or per (layer, KV head, request)
+  const size_t sets = d.head_sets ? (size_t)d.h_kv : 1;
+  t.idx = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * sets * (size_t)d.L * d.total_visual));
+  t.ivh = d.head_sets ? reinterpret_cast<float*>(take(sizeof(float) * sets * (size_t)d.L * d.total_visual)) : nullptr;
   t.out_offsets = reinterpret_cast<int64_t*>(take(sizeof(int64_t) * (LB + 1)));
   if (w) *w = t;
   return off;
@@ -251,6 +256,7 @@ int aircache_score(const aircache_problem* p, void* ws, size_t ws_bytes, float* 
   if (rc != AIRCACHE_OK) return rc;
   if ((rc = check_ws(p, ws, ws_bytes)) != AIRCACHE_OK) return rc;
   if (!iv || !elite || !n_tk) return AIRCACHE_ERR_INVALID_ARG;
+  if (((p->variant >> 16) & 0xff) != 0) return AIRCACHE_ERR_UNSUPPORTED;  // per-head sets: aircache_compress only
   const Dev d = make_dev(p);
   const LayerPtrs lp = make_ptrs(p);
   Ws w;
@@ -308,6 +314,7 @@ int aircache_select(const aircache_problem* p, const float* iv, const int32_t* k
   if (rc != AIRCACHE_OK) return rc;
   if ((rc = check_ws(p, ws, ws_bytes)) != AIRCACHE_OK) return rc;
   if (!iv || !keep || !idx) return AIRCACHE_ERR_INVALID_ARG;
+  if (((p->variant >> 16) & 0xff) != 0) return AIRCACHE_ERR_UNSUPPORTED;
   const Dev d = make_dev(p);
   Ws w;
   carve(d, static_cast<char*>(ws), &w);
@@ -328,6 +335,7 @@ int aircache_compact(const aircache_problem* p, const int32_t* idx, const int32_
   if ((rc = check_ws(p, ws, ws_bytes)) != AIRCACHE_OK) return rc;
   if (!idx || !keep || !out_k || !out_v || !out_offsets || out_rows_capacity < 0) return AIRCACHE_ERR_INVALID_ARG;
   if (!aligned16(out_k) || !aligned16(out_v)) return AIRCACHE_ERR_INVALID_ARG;
+  if (((p->variant >> 16) & 0xff) != 0) return AIRCACHE_ERR_UNSUPPORTED;
   const Dev d = make_dev(p);
   const LayerPtrs lp = make_ptrs(p);
   Ws w;
@@ -354,6 +362,7 @@ static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, v
   const LayerPtrs lp = make_ptrs(p);
   Dev dn = d;
   dn.stream_ok = stream_eligible(d, lp) ? 1 : 0;
+  if (d.head_sets && !dn.stream_ok) return AIRCACHE_ERR_UNSUPPORTED;  // per-head sets: the streaming path only
   if (events && n_events != (dn.stream_ok ? kStreamCount : kWideCount) + 1) return AIRCACHE_ERR_INVALID_ARG;
   Ws w;
   carve(d, static_cast<char*>(ws), &w);

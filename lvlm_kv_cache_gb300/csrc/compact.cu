@@ -68,10 +68,12 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_cons
     Req R;
     const bool ok = load_req(p, b, R);
     const int kp = w.keep[u];
-    // kept visual rows first, then every text row in text order
+    // kept visual rows first, then every text row in text order; with one set
+    // per KV head the visual row differs per head (resolved per vector below)
+    const size_t set0 = p.head_sets ? (size_t)l * p.h_kv : (size_t)l;
     int64_t tok = -1;
     if (j < kp) {
-      const int64_t pos = w.idx[(size_t)l * p.total_visual + R.vis0 + j];
+      const int64_t pos = w.idx[set0 * p.total_visual + R.vis0 + j];
       if (pos >= 0 && pos < R.n_v) tok = vis_tok(R, pos);
     } else if (j - kp < R.n_t) {
       tok = text_tok(R, j - kp);
@@ -89,7 +91,13 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_cons
         const int vec = v0 + i * 32 + lane;
         if (vec < vec_per_row) {
           const int head = vec / vec_per_head, part = vec % vec_per_head;
-          const int64_t eo = tok * p.kv_stride_tok + head * p.kv_stride_head + part * elems_per_vec;
+          int64_t t = tok;
+          if (p.head_sets && j < kp && head > 0) {
+            const int64_t pos = w.idx[(set0 + head) * p.total_visual + R.vis0 + j];
+            t = (pos >= 0 && pos < R.n_v) ? vis_tok(R, pos) : tok;
+            if (pos < 0 || pos >= R.n_v) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+          }
+          const int64_t eo = t * p.kv_stride_tok + head * p.kv_stride_head + part * elems_per_vec;
           kbuf[i] = __ldg(reinterpret_cast<const uint4*>(kb + eo * esize));
           vbuf[i] = __ldg(reinterpret_cast<const uint4*>(vb + eo * esize));
         }

@@ -30,6 +30,7 @@ struct Dev {
   int mom_slots;         // ceil(max_visual / 128): moment records per unit
   int window_mode;       // 0 elite window; 1 / 2 / 3: last 16 / last 32 / every text token
   int budget_mode;       // 0 strength + skewness; 1 uniform; 2 PyramidKV-style; 3 strength; 4 skewness
+  int head_sets;         // 1: one visual index set per KV head (I_v of each KV group)
   int chn;               // streaming pass-1 chunks per (unit, KV head): visual chunks + 1 text chunk
 };
 
@@ -75,9 +76,10 @@ struct Ws {
   float* lse;            // [L*B][h_kv][rc_max][32] row log-sum-exp, base 2
   float* ivp;            // [G][L*total_visual] per-KV-group I_v partials (G > 1 only)
   float* iv;             // [L*total_visual]
+  float* ivh;            // [L][h_kv][total_visual] I_v of each KV group (head_sets only)
   double* stats;         // [L*B*2]
   int32_t* keep;         // [L*B]
-  int32_t* idx;          // [L*total_visual]
+  int32_t* idx;          // [L*total_visual]; head_sets: [L][h_kv][total_visual]
   int64_t* out_offsets;  // [L*B+1]
   size_t zero_bytes;     // bytes of the zeroed block
 };

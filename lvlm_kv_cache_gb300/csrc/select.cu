@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   const Dev& p = a.p;
   const Ws& w = a.w;
   const int b = blockIdx.x, l = blockIdx.y, u = l * p.B + b;
+  const int hs = blockIdx.z;  // KV head of the set (one set per layer unless head_sets)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   extern __shared__ uint32_t keys_s[];  // [smem_keys] keys, then [smem_keys] candidates
   __shared__ unsigned hist[kMaxBins];
@@ -94,8 +95,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
     if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
     return;
   }
-  const float* x = w.iv + (size_t)l * p.total_visual + R.vis0;
-  int32_t* out = w.idx + (size_t)l * p.total_visual + R.vis0;
+  // one set per layer from I_v, or one per KV head from that KV group's I_v
+  const size_t set = p.head_sets ? (size_t)l * p.h_kv + hs : (size_t)l;
+  const float* x = (p.head_sets ? w.ivh : w.iv) + set * p.total_visual + R.vis0;
+  int32_t* out = w.idx + set * p.total_visual + R.vis0;
   if (k == n) {
     for (int i = tid; i < n; i += kSelThreads) out[i] = i;
     return;
@@ -276,7 +279,7 @@ cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s) {
   const int smem = 2 * (int)sizeof(uint32_t) * a.smem_keys;  // keys + candidates
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(select_kernel), smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(select_kernel, dim3(p.B, p.L), dim3(kSelThreads), smem, s, a);
+  return launch_pdl(select_kernel, dim3(p.B, p.L, p.head_sets ? p.h_kv : 1), dim3(kSelThreads), smem, s, a);
 }
 
 }  // namespace aircache

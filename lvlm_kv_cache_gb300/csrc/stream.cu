@@ -758,14 +758,22 @@ __device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, long 
     }
     const float* x = slices + (size_t)slot * (kRC * kKeysP2) + tid;
     const float* ls = S.lse_s + it.kvh * kRC;
+    float acc_h = 0.f;  // this KV head's rows
     int r = 0;
     for (; r + 8 <= it.rows; r += 8) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc += fast_exp2(fmaf(x[(r + q) * kKeysP2], scale, -ls[r + q]));
+      for (int q = 0; q < 8; ++q) acc_h += fast_exp2(fmaf(x[(r + q) * kKeysP2], scale, -ls[r + q]));
     }
-    for (; r < it.rows; ++r) acc += fast_exp2(fmaf(x[r * kKeysP2], scale, -ls[r]));
+    for (; r < it.rows; ++r) acc_h += fast_exp2(fmaf(x[r * kKeysP2], scale, -ls[r]));
+    acc += acc_h;
     __syncwarp();
     if (lane == 0) mbar_arrive(&c->empty[slot]);  // this warp is done with the slot and its record
+    if (p.head_sets) {
+      // the KV group's own I_v: its g query heads and the elite rows
+      const int key = it.kb * kKeysP2 + tid;
+      if (key < it.n_v)
+        w.ivh[((size_t)it.l * p.h_kv + it.kvh) * p.total_visual + it.vis0 + key] = acc_h / (float)(p.g * it.n_tk);
+    }
     if (it.kvh == p.h_kv - 1) {
       const int key = it.kb * kKeysP2 + tid;
       const float v = acc / (float)(p.h_q * it.n_tk);
@@ -943,6 +951,7 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
     float accK[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
     int step = 0;
     for (int kvh = 0; kvh < p.h_kv; ++kvh) {
+      float accH[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // this KV head's rows
       if (!mbar_wait(&c->kfull, kph, 4 * kWaitCycles)) {
         if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
         return;
@@ -998,12 +1007,28 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
 #pragma unroll
               for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) accK[nt][e] += fast_exp2(fmaf(acc[mt][nt][2 * hh + e], scale, -lse));
+                for (int e = 0; e < 2; ++e) accH[nt][e] += fast_exp2(fmaf(acc[mt][nt][2 * hh + e], scale, -lse));
             }
           }
         __syncthreads();  // every thread is done with the slot
         if (tid == 0 && step + kNQ < steps) issue_q(step + kNQ, qn + kNQ);
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          accK[nt][e] += accH[nt][e];
+          if (p.head_sets) {
+            // the KV group's own I_v (lanes with the same c4 hold the same keys)
+            float v = accH[nt][e];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            const int key = 16 * warp + 8 * nt + 2 * c4 + e;
+            if (g4 == 0 && key < klim)
+              w.ivh[((size_t)l * p.h_kv + kvh) * TV + i0.y + (long long)tile * kTK + key] = v / (float)(p.g * n_tk);
+          }
+        }
     }
     // per key: the sum over every row (lanes with the same c4 hold the same keys)
     float* iv = w.iv + (size_t)l * TV + i0.y;

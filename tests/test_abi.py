@@ -76,7 +76,7 @@ def test_sizes_of_a_valid_problem(A):
     ("num_layers", 0, -1), ("num_layers", 257, -1), ("num_requests", 0, -1),
     ("h_q", 7, -1), ("h_kv", 0, -1), ("head_dim", 96, -2), ("head_dim", 0, -1),
     ("dtype", 7, -2), ("max_visual", 2, -1), ("max_text", 0, -1), ("max_text", 9000, -2),
-    ("max_elite", 65, -1), ("max_elite", -1, -1), ("variant", 1 << 16, -1), ("variant", 4, -1), ("variant", 5 << 8, -1),
+    ("max_elite", 65, -1), ("max_elite", -1, -1), ("variant", 2 << 16, -1), ("variant", 1 << 24, -1), ("variant", 4, -1), ("variant", 5 << 8, -1),
     ("total_visual", 5, -1), ("total_tokens", 1901, -1), ("total_visual", 2001, -1),
     ("cu_seqlens", None, -1), ("cu_visual", None, -1),
     ("kv_stride_tok", 0, -1), ("kv_stride_tok", 3, -1), ("q_stride_head", 4, -1),
@@ -131,3 +131,17 @@ def test_workspace_grows_with_max_elite(A):
     b = A.lib().aircache_workspace_size(ctypes.byref(fake_problem(A, max_elite=64)))
     c = A.lib().aircache_workspace_size(ctypes.byref(fake_problem(A)))
     assert 0 < a < b == c
+
+
+def test_per_head_sets_only_through_the_fused_call(A):
+    # one index set per KV head (variant bits 16-23 = 1): the staged calls refuse it on the host
+    p = fake_problem(A, variant=1 << 16)
+    lib = A.lib()
+    need = lib.aircache_workspace_size(ctypes.byref(p))
+    assert need > lib.aircache_workspace_size(ctypes.byref(fake_problem(A)))  # per-head I_v and index sets
+    ws = ctypes.c_void_p(0x400000)
+    bufs = (ctypes.c_void_p(0x500000), ctypes.c_void_p(0x600000), ctypes.c_void_p(0x700000))
+    assert lib.aircache_score(ctypes.byref(p), ws, need, *bufs, None) == -2
+    assert lib.aircache_select(ctypes.byref(p), bufs[0], bufs[1], ws, need, bufs[2], None) == -2
+    assert lib.aircache_compact(ctypes.byref(p), bufs[0], bufs[1], ws, need, ctypes.c_void_p(0x800000),
+                                ctypes.c_void_p(0x900000), ctypes.c_void_p(0xa00000), 100, None) == -2
