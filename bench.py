@@ -517,7 +517,12 @@ def main():
     iv_s = torch.empty((L, TV), dtype=torch.float32, device=dev)
     el_s = torch.empty((L * B, prob.max_text), dtype=torch.int32, device=dev)
     ntk_s = torch.empty(L * B, dtype=torch.int32, device=dev)
-    A.aircache_score(prob, ws, iv_s, el_s, ntk_s)
+    # (the staged scorer takes one index set per layer; the elite sizes do not depend on it)
+    prob_s = prob if not args.head_sets else A.Problem(
+        wl.q, wl.k, wl.v, wl.cu_seqlens, wl.cu_visual, max(spec.n_visual), max(spec.n_text), spec.alpha, spec.r,
+        total_tokens=wl.total_tokens, total_visual=wl.total_visual, window_mode=args.window_mode,
+        budget_mode=args.budget_mode)
+    A.aircache_score(prob_s, ws, iv_s, el_s, ntk_s)
     assert A.aircache_get_error(ws) == 0
 
     def step():
