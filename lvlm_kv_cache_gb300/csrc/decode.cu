@@ -6,21 +6,30 @@
 //
 // Split-K over the rows.  CTA (x, h, s) takes the x-th slice of sequence s's
 // row range for KV head h and every query head of h's group (g <= 16, padded
-// to the 16 rows of an mma.sync A operand).  A producer warp streams 64-row
-// K and V tiles of that head with TMA (128-byte swizzle) through a ring of
-// stages; four consumer warps each take 16 rows of a tile:
+// to the 16 rows of an mma.sync A operand).  A producer warp reads the range
+// and streams 64-row K and V tiles of that head with TMA through a ring of
+// stages (bf16: 128-byte swizzle; int8 codes: plain rows, which each consumer
+// warp widens to bf16 in a scratch laid out like a swizzled tile); four
+// consumer warps each take 16 rows of a tile:
 //   S = Q K^T      A = Q (16 heads x 16 d, in registers), B = K (ldmatrix),
 //   online softmax in base 2 per head, P rounded to bf16 (the normaliser sums
 //                  the rounded weights, so the output is an exact convex
 //                  combination with relatively perturbed weights),
 //   O += P V       A = P (the S accumulators repacked), B = V (ldmatrix.trans).
-// The warps' (max, sum, O) merge in shared memory into the slice's partial;
-// the last CTA of a (sequence, KV head) to finish (an atomic count, no
-// waiting) merges the slices, adds the step's own (k_new, v_new) row when
-// given, and writes out = O / sum in fp32.
+// The warps' (max, sum, O) merge in shared memory.  The slices of one
+// (sequence, KV head) then merge in one of three ways: a single slice writes
+// the output; up to 8 slices form a thread-block cluster and every rank merges
+// its share of the output columns from all ranks' shared memory; more slices
+// write partials and the last CTA to finish (an atomic count, no waiting)
+// merges them.  The step's own (k_new, v_new) row joins the final merge.  An
+// int8 cache's scales fold into the logit multiplier and the weighted sum.
+// With AIRCACHE_DECODE_EARLY_CACHE the kernel is launched with programmatic
+// dependent launch and reads the ranges and rows before waiting for the kernel
+// before it.
 //
 // Traffic per launch: every cached row's K and V of each KV head once
-// (2 * head_dim * 2 bytes per row and head), the queries, and the fp32 output.
+// (2 * head_dim * element bytes per row and head), the queries, and the fp32
+// output.
 #include <cuda_bf16.h>
 
 #include <algorithm>
