@@ -343,6 +343,14 @@ typedef struct aircache_decode_problem {
                               aircache_quantize_int8 scales + l*B*h_kv) */
     int32_t flags;         /* 0, or AIRCACHE_DECODE_EARLY_CACHE */
     int32_t reserved1;     /* 0 */
+    const int32_t* row_index;  /* optional (NULL: ranges are arena rows): device [index_len]
+                                  arena rows; row_begin[s] .. row_end[s]-1 then index this
+                                  array, and sequence s attends over the rows it lists
+                                  (gather-fused decode: the full cache with the row list of
+                                  aircache_row_index, no compaction).  bf16 rows only.  A
+                                  listed row outside [0, kv_rows) sets
+                                  AIRCACHE_ERR_DEVICE_BOUNDS and reads row 0 instead. */
+    int64_t index_len;         /* entries of row_index (the ranges' bound), >= 1 when given */
 } aircache_decode_problem;
 
 /*
@@ -357,6 +365,22 @@ typedef struct aircache_decode_problem {
  * per layer) then overlap each kernel's start with the previous one's end.
  */
 #define AIRCACHE_DECODE_EARLY_CACHE 1
+
+/*
+ * The row list of a compression without the copy: for every (l, b) of `p`, in
+ * aircache_compact's row order (rows out_offsets[l*B+b] .. out_offsets[l*B+b+1]-1),
+ * row_index[row] = the prompt position in layer l's K / V of that compacted
+ * row (the kept visual positions, then every text position; n_prefix
+ * respected).  keep, idx and out_offsets are aircache_compress's outputs
+ * (one index set per layer: with one per KV head, AIRCACHE_ERR_UNSUPPORTED);
+ * capacity is the length of row_index (too small: AIRCACHE_ERR_CAPACITY in
+ * the workspace error word).  Decoding layer l over wl.k[l] with these rows
+ * (aircache_decode with row_index) attends over the same rows as decoding the
+ * compacted arena.  One memset and one kernel.
+ */
+AIRCACHE_API int aircache_row_index(const aircache_problem* p, const int32_t* keep, const int32_t* idx,
+                                    const int64_t* out_offsets, void* ws, size_t ws_bytes, int32_t* row_index,
+                                    int64_t capacity, void* stream);
 
 /* Workspace bytes aircache_decode needs for `p` on the current device, or 0 if
  * `p` is invalid.  Depends on num_seqs, h_q, h_kv, head_dim, max_rows and the

@@ -85,6 +85,7 @@ class DecodeProblemStruct(ctypes.Structure):
         ("new_stride_seq", ctypes.c_int64), ("new_stride_head", ctypes.c_int64),
         ("out", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
         ("flags", ctypes.c_int32), ("reserved1", ctypes.c_int32),
+        ("row_index", ctypes.c_void_p), ("index_len", ctypes.c_int64),
     ]
 
 
@@ -136,6 +137,8 @@ def lib():
         L.aircache_compress_profile.restype = i32
         L.aircache_kernel_name.argtypes = [P, i32]
         L.aircache_kernel_name.restype = ctypes.c_char_p
+        L.aircache_row_index.argtypes = [P, vp, vp, vp, vp, sz, vp, i64, vp]
+        L.aircache_row_index.restype = i32
         L.aircache_quantize_int8.argtypes = [ctypes.POINTER(QuantProblemStruct), vp, vp]
         L.aircache_quantize_int8.restype = i32
         DP = ctypes.POINTER(DecodeProblemStruct)
@@ -393,7 +396,7 @@ class DecodeProblem:
     stream must not write the ranges or the cached rows)."""
 
     def __init__(self, q, k, v, row_begin=None, row_end=None, max_rows=0, k_new=None, v_new=None,
-                 out=None, offsets=None, k_scale=None, v_scale=None, early_cache=False):
+                 out=None, offsets=None, k_scale=None, v_scale=None, early_cache=False, row_index=None):
         if offsets is not None:
             row_begin, row_end = offsets[:-1], offsets[1:]
         S, h_q, d = (int(x) for x in q.shape)
@@ -412,7 +415,9 @@ class DecodeProblem:
         q8 = k.dtype == torch.int8
         if q8 and (k_scale is None or v_scale is None or not k_scale.is_contiguous() or not v_scale.is_contiguous()):
             raise ValueError("int8 caches need contiguous k_scale and v_scale [S, H_kv]")
-        self.keep = (q, k, v, row_begin, row_end, k_new, v_new, out, k_scale, v_scale)
+        if row_index is not None and (row_index.dtype != torch.int32 or not row_index.is_contiguous()):
+            raise TypeError("row_index is a contiguous int32 tensor")
+        self.keep = (q, k, v, row_begin, row_end, k_new, v_new, out, k_scale, v_scale, row_index)
         self.out = out
         self.c = DecodeProblemStruct(
             num_seqs=S, h_q=h_q, h_kv=h_kv, head_dim=d,
@@ -429,6 +434,8 @@ class DecodeProblem:
             out=out.data_ptr(),
             k_scale=k_scale.data_ptr() if q8 else None, v_scale=v_scale.data_ptr() if q8 else None,
             flags=DECODE_EARLY_CACHE if early_cache else 0, reserved1=0,
+            row_index=row_index.data_ptr() if row_index is not None else None,
+            index_len=row_index.numel() if row_index is not None else 0,
         )
 
     @property
@@ -493,3 +500,22 @@ def quantize_int8(k, v, offsets, stream=None, check=True):
     if check and int(st.item()) != OK:
         raise AirCacheError(int(st.item()), "aircache_quantize_int8 (device)")
     return k8, v8, ks, vs
+
+
+def aircache_row_index(prob: Problem, keep, idx, out_offsets, ws, row_index, stream=None):
+    _check(lib().aircache_row_index(prob.ref, _ptr(keep), _ptr(idx), _ptr(out_offsets), _ptr(ws), ws.numel(),
+                                    _ptr(row_index), row_index.numel(), _stream(stream)), "aircache_row_index")
+
+
+def row_index(prob: Problem, out, ws=None, stream=None, check=True):
+    """The compacted rows' prompt positions (int32 [rows]) for a gather-fused
+    decode from the full cache; `out` is aircache_compress's output dict."""
+    ws = prob.new_workspace() if ws is None else ws
+    rows = int(out["out_offsets"][-1])
+    ri = torch.empty(max(rows, 1), dtype=torch.int32, device=out["keep"].device)
+    aircache_row_index(prob, out["keep"], out["idx"], out["out_offsets"], ws, ri, stream)
+    if check:
+        st = aircache_get_error(ws, stream)
+        if st != OK:
+            raise AirCacheError(st, "aircache_row_index (device)")
+    return ri

@@ -350,6 +350,27 @@ int aircache_compact(const aircache_problem* p, const int32_t* idx, const int32_
   return AIRCACHE_OK;
 }
 
+int aircache_row_index(const aircache_problem* p, const int32_t* keep, const int32_t* idx,
+                       const int64_t* out_offsets, void* ws, size_t ws_bytes, int32_t* row_index, int64_t capacity,
+                       void* stream) {
+  int rc = validate(p);
+  if (rc != AIRCACHE_OK) return rc;
+  if ((rc = check_ws(p, ws, ws_bytes)) != AIRCACHE_OK) return rc;
+  if (!keep || !idx || !out_offsets || !row_index || capacity < 0) return AIRCACHE_ERR_INVALID_ARG;
+  if (((p->variant >> 16) & 0xff) != 0) return AIRCACHE_ERR_UNSUPPORTED;  // one row list: one set per layer
+  const Dev d = make_dev(p);
+  const LayerPtrs lp = make_ptrs(p);
+  Ws w;
+  carve(d, static_cast<char*>(ws), &w);
+  w.keep = const_cast<int32_t*>(keep);
+  w.idx = const_cast<int32_t*>(idx);
+  w.out_offsets = const_cast<int64_t*>(out_offsets);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
+  AC_TRY(launch_row_index(d, lp, w, row_index, capacity, s));
+  return AIRCACHE_OK;
+}
+
 static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, void* out_k, void* out_v,
                          int64_t* out_offsets, int64_t out_rows_capacity, int32_t* keep, int32_t* idx,
                          float* iv, void* const* events, int n_events, void* stream) {

@@ -24,7 +24,8 @@ struct CompactArgs {
   Ws w;
   void* out_k;
   void* out_v;
-  int64_t capacity;  // rows out_k / out_v hold
+  int64_t capacity;  // rows out_k / out_v hold (or entries of row_index)
+  int32_t* row_index;  // non-null: write each row's prompt position instead of copying it
 };
 
 __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_constant__ CompactArgs a) {
@@ -82,6 +83,10 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_cons
       if (lane == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
       continue;
     }
+    if (a.row_index) {  // the row list of a gather-fused decode: no copy
+      if (lane == 0) a.row_index[row] = (int32_t)tok;
+      continue;
+    }
     const char* kb = reinterpret_cast<const char*>(a.lp.k[l]);
     const char* vb = reinterpret_cast<const char*>(a.lp.v[l]);
     uint4 kbuf[4], vbuf[4];
@@ -125,10 +130,31 @@ cudaError_t launch_compact(const Dev& p, const LayerPtrs& lp, const Ws& w, void*
   a.out_k = out_k;
   a.out_v = out_v;
   a.capacity = capacity;
+  a.row_index = nullptr;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   return launch_pdl(compact_kernel, dim3(sms * 4), dim3(kCopyThreads), 0, s, a);
+}
+
+}  // namespace aircache
+
+namespace aircache {
+
+cudaError_t launch_row_index(const Dev& p, const LayerPtrs& lp, const Ws& w, int32_t* row_index, int64_t capacity,
+                             cudaStream_t s) {
+  CompactArgs a;
+  a.p = p;
+  a.lp = lp;
+  a.w = w;
+  a.out_k = nullptr;
+  a.out_v = nullptr;
+  a.capacity = capacity;
+  a.row_index = row_index;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return launch_pdl(compact_kernel, dim3(sms), dim3(kCopyThreads), 0, s, a);
 }
 
 }  // namespace aircache

@@ -92,6 +92,9 @@ struct DecArgs {
   const float* v_scale;
   float scale_log2;  // log2(e) / sqrt(D)
   int early;         // AIRCACHE_DECODE_EARLY_CACHE: ranges and rows read before the dependency wait
+  const int32_t* row_index;  // gather mode: arena rows listed per range position
+  int64_t range_len;         // bound of the ranges: kv_rows, or the row list's length
+  int64_t col_stride_head;   // gather mode: elements between KV heads in a row
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& lo_r, float& hi_r) {
@@ -131,6 +134,17 @@ __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
   return v;
 }
 
+// Four rows (r0..r3) of a 2-D tensor map whose box is one row high, landing as
+// four consecutive box rows at dst (the Blackwell tile::gather4 form).
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0, int r1, int r2,
+                                            int r3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5, %6}], [%7];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
@@ -139,7 +153,7 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-template <int D, bool CL, bool Q8>
+template <int D, bool CL, bool Q8, bool GA>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_constant__ CUtensorMap kmap,
                                                              const __grid_constant__ CUtensorMap vmap,
                                                              const __grid_constant__ DecArgs a) {
@@ -174,7 +188,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
     if (!a.early) pdl_wait();  // the ranges and rows may come from the previous kernel
     const int64_t b = a.row_begin[s], e = a.row_end[s];
-    const bool ok = b >= 0 && e >= b && e <= a.kv_rows;
+    const bool ok = b >= 0 && e >= b && e <= a.range_len;
     if (!ok && split == 0 && h == 0) set_error(a.error, AIRCACHE_ERR_DEVICE_BOUNDS);
     const int64_t n = ok ? e - b : 0;
     int64_t per = (n + a.n_split - 1) / a.n_split;
@@ -191,7 +205,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       mbar_init(&empty[i], kDecWarps);
     }
     fence_mbar_init();
-    const int ntiles = (nrows + kDecRows - 1) / kDecRows;
+    const int ntiles = GA ? 0 : (nrows + kDecRows - 1) / kDecRows;  // gather mode: the warp issues every tile
     for (int i = 0; i < ntiles && i < C::kStages; ++i) {
       const uint32_t kb = smem_u32(ring + i * C::kStageBytes);
       mbar_arrive_expect_tx(&full[i], C::kStageBytes);
@@ -226,6 +240,59 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   const bool has_new = a.k_new != nullptr && ok;
   const int ntiles = (nrows + kDecRows - 1) / kDecRows;
 
+  if (warp == kDecWarps && GA) {
+    // ---- gather producer: the warp reads each tile's 64 listed rows (rows past
+    // the slice end repeat its first row; they are masked), lane 0 issues 16
+    // four-row gathers per 128-byte column slab of K and of V
+    for (int i = 0; i < ntiles; ++i) {
+      const int st = i % C::kStages;
+      if (i >= C::kStages) {  // one lane waits for the stage, the warp follows its verdict
+        bool freed = true;
+        if (lane == 0) freed = mbar_wait(&empty[st], ((i / C::kStages) - 1) & 1);
+        if (!__shfl_sync(0xffffffffu, freed ? 1 : 0, 0)) {
+          if (lane == 0) set_error(a.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+          break;
+        }
+      }
+      int rr[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int j = i * kDecRows + lane + 32 * q;
+        int v = __ldg(a.row_index + row0 + (j < nrows ? j : 0));
+        if (v < 0 || v >= a.kv_rows) {
+          set_error(a.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+          v = 0;
+        }
+        rr[q] = v;
+      }
+      const uint32_t kb = smem_u32(ring + st * C::kStageBytes);
+      if (lane == 0) {
+        fence_proxy_async_smem();  // the consumers' generic reads of this stage come first
+        mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+      }
+#pragma unroll
+      for (int g4 = 0; g4 < kDecRows / 4; ++g4) {
+        const int src = (4 * g4) & 31, q = (4 * g4) >> 5;
+        const int v0 = __shfl_sync(0xffffffffu, rr[q], src), v1 = __shfl_sync(0xffffffffu, rr[q], src + 1);
+        const int v2 = __shfl_sync(0xffffffffu, rr[q], src + 2), v3 = __shfl_sync(0xffffffffu, rr[q], src + 3);
+        if (lane == 0) {
+#pragma unroll
+          for (int sl = 0; sl < C::kSlabs; ++sl) {
+            const int col = (int)(h * a.col_stride_head) + sl * 64;
+            tma_gather4(kb + sl * kDecRows * 128 + g4 * 512, &kmap, col, v0, v1, v2, v3, &full[st]);
+            tma_gather4(kb + C::kTileBytes + sl * kDecRows * 128 + g4 * 512, &vmap, col, v0, v1, v2, v3, &full[st]);
+          }
+        }
+      }
+      __syncwarp();
+    }
+    __syncwarp();
+    if (CL) {  // the two cluster barriers of the slice merge below
+      cluster_sync_all();
+      cluster_sync_all();
+    }
+    return;
+  }
   if (warp == kDecWarps) {
     // ---- producer: the remaining tiles, each into the stage its predecessor freed
     if (lane == 0) {
@@ -684,6 +751,8 @@ int decode_plan(const aircache_decode_problem* p, DecPlan& pl) {
       p->q_stride_head % 8 != 0 || p->q_stride_seq < 0 || p->q_stride_head < 0)
     return AIRCACHE_ERR_INVALID_ARG;
   if (p->k_new && (p->new_stride_seq < 0 || p->new_stride_head < 0)) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->row_index && (p->index_len < 1 || p->index_len > 0x7fff0000LL)) return AIRCACHE_ERR_INVALID_ARG;
+  if (p->row_index && pl.q8) return AIRCACHE_ERR_UNSUPPORTED;  // gathered rows: bf16 only
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   pl.d = p->head_dim;
@@ -734,7 +803,21 @@ bool encode_arena(CUtensorMap* m, const void* base, const aircache_decode_proble
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool Q8>
+// The arena as a 2-D tensor [kv_rows][heads' columns] whose box is one row of
+// 64 elements: the form of the four-row gathers.
+bool encode_gather(CUtensorMap* m, const void* base, const aircache_decode_problem* p) {
+  auto enc = tma_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)((p->h_kv - 1) * p->kv_stride_head + p->head_dim), (cuuint64_t)p->kv_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)p->kv_stride_row * 2};
+  cuuint32_t box[2] = {64, 1};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, bool Q8, bool GA>
 int launch_decode(const aircache_decode_problem* p, const DecPlan& pl, uint8_t* ws, cudaStream_t s) {
   auto launch_pdl3 = [](void (*k)(CUtensorMap, CUtensorMap, DecArgs), dim3 grid, dim3 block, size_t smem,
                         cudaStream_t st, const CUtensorMap& km, const CUtensorMap& vm, const DecArgs& a) {
@@ -751,7 +834,11 @@ int launch_decode(const aircache_decode_problem* p, const DecPlan& pl, uint8_t* 
     return cudaLaunchKernelEx(&cfg, k, km, vm, a);
   };
   CUtensorMap km, vm;
-  if (!encode_arena(&km, p->k, p) || !encode_arena(&vm, p->v, p)) return AIRCACHE_ERR_UNSUPPORTED;
+  if (GA) {
+    if (!encode_gather(&km, p->k, p) || !encode_gather(&vm, p->v, p)) return AIRCACHE_ERR_UNSUPPORTED;
+  } else if (!encode_arena(&km, p->k, p) || !encode_arena(&vm, p->v, p)) {
+    return AIRCACHE_ERR_UNSUPPORTED;
+  }
   DecArgs a;
   a.q = static_cast<const __nv_bfloat16*>(p->q);
   a.k_new = static_cast<const __nv_bfloat16*>(p->k_new);
@@ -776,10 +863,13 @@ int launch_decode(const aircache_decode_problem* p, const DecPlan& pl, uint8_t* 
   a.k_scale = p->k_scale;
   a.v_scale = p->v_scale;
   a.early = (p->flags & AIRCACHE_DECODE_EARLY_CACHE) != 0;
+  a.row_index = p->row_index;
+  a.range_len = GA ? p->index_len : p->kv_rows;
+  a.col_stride_head = p->kv_stride_head;
   const int smem = DecCfg<D, Q8>::kSmem;
   const dim3 grid(pl.n_split, p->h_kv, p->num_seqs);
   if (pl.cluster) {
-    if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D, true, Q8>), smem) != cudaSuccess)
+    if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D, true, Q8, GA>), smem) != cudaSuccess)
       return AIRCACHE_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -795,15 +885,15 @@ int launch_decode(const aircache_decode_problem* p, const DecPlan& pl, uint8_t* 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = a.early ? 2 : 1;
-    if (cudaLaunchKernelEx(&cfg, decode_kernel<D, true, Q8>, km, vm, a) != cudaSuccess) return AIRCACHE_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, decode_kernel<D, true, Q8, GA>, km, vm, a) != cudaSuccess) return AIRCACHE_ERR_CUDA;
   } else {
-    if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D, false, Q8>), smem) != cudaSuccess)
+    if (allow_smem(reinterpret_cast<const void*>(&decode_kernel<D, false, Q8, GA>), smem) != cudaSuccess)
       return AIRCACHE_ERR_CUDA;
     if (a.early) {
-      if (launch_pdl3(decode_kernel<D, false, Q8>, grid, dim3(kDecThreads), smem, s, km, vm, a) != cudaSuccess)
+      if (launch_pdl3(decode_kernel<D, false, Q8, GA>, grid, dim3(kDecThreads), smem, s, km, vm, a) != cudaSuccess)
         return AIRCACHE_ERR_CUDA;
     } else {
-      decode_kernel<D, false, Q8><<<grid, kDecThreads, smem, s>>>(km, vm, a);
+      decode_kernel<D, false, Q8, GA><<<grid, kDecThreads, smem, s>>>(km, vm, a);
     }
   }
   return cudaGetLastError() == cudaSuccess ? AIRCACHE_OK : AIRCACHE_ERR_CUDA;
@@ -835,8 +925,10 @@ int aircache_decode(const aircache_decode_problem* p, void* ws, size_t ws_bytes,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   if (p->num_seqs == 0) return AIRCACHE_OK;
-  if (pl.q8) return pl.d == 128 ? launch_decode<128, true>(p, pl, w, s) : launch_decode<64, true>(p, pl, w, s);
-  return pl.d == 128 ? launch_decode<128, false>(p, pl, w, s) : launch_decode<64, false>(p, pl, w, s);
+  if (pl.q8) return pl.d == 128 ? launch_decode<128, true, false>(p, pl, w, s) : launch_decode<64, true, false>(p, pl, w, s);
+  if (p->row_index)
+    return pl.d == 128 ? launch_decode<128, false, true>(p, pl, w, s) : launch_decode<64, false, true>(p, pl, w, s);
+  return pl.d == 128 ? launch_decode<128, false, false>(p, pl, w, s) : launch_decode<64, false, false>(p, pl, w, s);
 }
 
 }  // extern "C"

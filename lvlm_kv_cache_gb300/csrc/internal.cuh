@@ -139,6 +139,9 @@ ScoreLaunch plan_score(const Dev& p, int sms, bool tail, int64_t out_capacity);
 
 // Launchers (each returns cudaGetLastError() of its launches).
 cudaError_t launch_elite(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_t s);
+// compact_kernel in row-list mode: row_index[row] = the prompt position of each compacted row.
+cudaError_t launch_row_index(const Dev& p, const LayerPtrs& lp, const Ws& w, int32_t* row_index, int64_t capacity,
+                             cudaStream_t s);
 cudaError_t launch_score(const Dev& p, const LayerPtrs& lp, const Ws& w, const ScoreLaunch& L,
                          cudaStream_t s);
 // Stats and keep counts from I_v, one CTA per (layer, request); with

@@ -47,7 +47,7 @@ def test_sizes_and_splits(A):
 @pytest.mark.parametrize("field,value,code", [
     ("num_seqs", -1, -1), ("num_seqs", 65536, -1), ("h_q", 27, -1), ("h_kv", 0, -1),
     ("head_dim", 96, -1), ("dtype", 0, -2), ("h_q", 68, -2), ("kv_dtype", 0, -1), ("kv_dtype", 3, -1),
-    ("kv_dtype", 2, -1), ("flags", 2, -1), ("reserved1", 1, -1),
+    ("kv_dtype", 2, -1), ("flags", 2, -1), ("reserved1", 1, -1), ("row_index", 0x800000, -1),
     ("kv_rows", 0, -1), ("kv_rows", 1 << 31, -1), ("max_rows", -1, -1),
     ("q", None, -1), ("k", None, -1), ("out", None, -1), ("row_begin", None, -1),
     ("k", 0x200008, -1), ("q", 0x100004, -1), ("kv_stride_row", 4 * 128 + 4, -1),
@@ -87,3 +87,10 @@ def fake_quant(A, **over):
 def test_invalid_quantize_rejected_on_host(A, field, value):
     p = fake_quant(A, **{field: value})
     assert A.lib().aircache_quantize_int8(ctypes.byref(p), None, None) == -1
+
+
+def test_gather_rows_need_bf16(A):
+    p = fake(A, row_index=0x800000, index_len=100, kv_dtype=A.INT8, k_scale=0x900000, v_scale=0x910000,
+             kv_stride_row=512, kv_stride_head=128)
+    assert A.lib().aircache_decode_workspace_size(ctypes.byref(p)) == 0
+    assert A.lib().aircache_decode(ctypes.byref(p), ctypes.c_void_p(0x700000), 1 << 40, None) == -2

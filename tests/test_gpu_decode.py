@@ -271,3 +271,82 @@ def test_early_cache_launches_match_plain_launches(A, oracle):
     for a, b in zip(outs[False], outs[True]):
         assert torch.equal(a, b)
     check_against_oracle(oracle, di, outs[True][1].cpu().numpy().astype(np.float64))
+
+
+def test_gather_fused_decode_equals_decoding_the_compacted_arena(A):
+    # decoding layer l's full cache through aircache_row_index's list attends
+    # over the same rows, in the same order, as decoding the compacted arena:
+    # the same bits
+    for with_prefix in (False, True):
+        wl = W.make("ragged", seed=16, device="cuda", layers=3, requests=4)
+        s = wl.spec
+        npf = [min(x, t) for x, t in zip([3, 0, 60, 11], s.n_text)]
+        k, v, npt = W.with_prefix(wl, npf) if with_prefix else (wl.k, wl.v, None)
+        prob = A.Problem(wl.q, k, v, wl.cu_seqlens, wl.cu_visual, max(s.n_visual), max(s.n_text),
+                         alpha=s.alpha, r=s.r, total_tokens=wl.total_tokens, total_visual=wl.total_visual,
+                         n_prefix=npt)
+        res = A.compress(prob)
+        ri = A.row_index(prob, res)
+        offs = res["out_offsets"]
+        rows = offs.cpu().numpy()
+        B = s.B
+        g = torch.Generator(device="cuda").manual_seed(17)
+        qs = torch.randn((s.L, B, s.H_q, s.D), generator=g, device="cuda").to(torch.bfloat16)
+        longest = int(np.diff(rows).max())
+        for l in range(s.L):
+            rb, re = offs[l * B:(l + 1) * B], offs[l * B + 1:(l + 1) * B + 1]
+            a = A.decode(A.DecodeProblem(qs[l], res["out_k"], res["out_v"], row_begin=rb, row_end=re,
+                                         max_rows=longest))
+            b = A.decode(A.DecodeProblem(qs[l], k[l], v[l], row_begin=rb, row_end=re, max_rows=longest,
+                                         row_index=ri))
+            assert torch.equal(a, b), f"layer {l}"
+
+
+@pytest.mark.parametrize("max_rows", [0, 1000, 10 ** 6])
+def test_gather_decode_of_listed_rows_matches_oracle(A, oracle, max_rows):
+    # arbitrary row lists (repeats allowed) over an arena, in every merge mode
+    di = W.decode_inputs([3000], 28, 4, 128, seed=18, device="cuda", q_scale=2.0)
+    rng = np.random.default_rng(19)
+    lens = [1, 70, 129, 1500]
+    lists = [rng.integers(0, 3000, n) for n in lens]
+    ri = torch.tensor(np.concatenate(lists), dtype=torch.int32, device="cuda")
+    offs = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int64, device="cuda")
+    q = torch.randn((len(lens), 28, 128), generator=torch.Generator(device="cuda").manual_seed(20),
+                    device="cuda").to(torch.bfloat16)
+    out = A.decode(A.DecodeProblem(q, di.k, di.v, offsets=offs, max_rows=max_rows, row_index=ri))
+    out = out.cpu().numpy().astype(np.float64)
+    kb, vb, qb = W.host_bits(di.k), W.host_bits(di.v), W.host_bits(q)
+    for s_, rows in enumerate(lists):
+        ref = oracle.decode(qb[s_], kb[rows], vb[rows])
+        assert np.all(np.abs(out[s_] - ref) <= tolerance(qb[s_], kb[rows], vb[rows], ref)), f"sequence {s_}"
+
+
+def test_gather_row_outside_the_arena_is_a_device_error(A):
+    di = W.decode_inputs([100], 8, 2, 64, seed=21, device="cuda")
+    ri = torch.tensor([0, 5, 100, 7], dtype=torch.int32, device="cuda")  # 100 is past the arena
+    offs = torch.tensor([0, 4], dtype=torch.int64, device="cuda")
+    prob = A.DecodeProblem(di.q[:1], di.k, di.v, offsets=offs, max_rows=4, row_index=ri)
+    ws = prob.new_workspace()
+    A.aircache_decode(prob, ws)
+    assert A.aircache_get_error(ws) == A.ERR_DEVICE_BOUNDS
+    assert np.isfinite(prob.out.cpu().numpy()).all()
+
+
+def test_row_index_lists_the_compacted_positions(A):
+    wl = W.make("ragged", seed=22, device="cuda", layers=2, requests=3)
+    s = wl.spec
+    npf = [0, 9, s.n_text[2]]
+    k, v, npt = W.with_prefix(wl, npf)
+    prob = A.Problem(wl.q, k, v, wl.cu_seqlens, wl.cu_visual, max(s.n_visual), max(s.n_text), alpha=s.alpha,
+                     r=s.r, total_tokens=wl.total_tokens, total_visual=wl.total_visual, n_prefix=npt)
+    res = A.compress(prob)
+    ri = A.row_index(prob, res).cpu().numpy()
+    cu_s, cu_v, _ = W.offsets(s)
+    keep, idx, offs = res["keep"].cpu().numpy(), res["idx"].cpu().numpy(), res["out_offsets"].cpu().numpy()
+    for l in range(s.L):
+        for b in range(s.B):
+            u = l * s.B + b
+            kk, nv, nt, p_ = int(keep[u]), s.n_visual[b], s.n_text[b], npf[b]
+            vis = cu_s[b] + p_ + idx[l, cu_v[b]:cu_v[b] + kk]
+            txt = cu_s[b] + np.array([j if j < p_ else nv + j for j in range(nt)])
+            assert np.array_equal(ri[offs[u]:offs[u + 1]], np.concatenate([vis, txt]))
