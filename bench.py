@@ -402,7 +402,16 @@ def run_decode(args, local):
                         for l in range(L)]  # plain launches: the early start measured slower for int8 rows
             q8_ms = timed(q8_probs, ws_c)
             q8_bytes = comp_rows * kv_row_bytes // 2 + L * B * H_q * D * (2 + 4) + 2 * L * B * H_kv * 4
+            # gather-fused: the same rows read from the full cache through the row list
+            ri = A.row_index(prob, out)
+            ga_probs = [A.DecodeProblem(qdec[l], wl.k[l], wl.v[l], row_begin=offs[l * B:(l + 1) * B],
+                                        row_end=offs[l * B + 1:(l + 1) * B + 1], max_rows=longest,
+                                        early_cache=True, row_index=ri)
+                        for l in range(L)]
+            ga_ms = timed(ga_probs, ws_c)
             results.append({"r": r, "ms": comp_ms, "rows": comp_rows, "algorithmic_bytes": comp_bytes,
+                            "gather_fused": {"ms": ga_ms, "gbs": comp_bytes / (ga_ms * 1e-3) / 1e9,
+                                             "reduction": 1.0 - ga_ms / full_ms},
                             "gbs": comp_bytes / (comp_ms * 1e-3) / 1e9,
                             "frac": comp_bytes / (comp_ms * 1e-3) / 1e9 / peak,
                             "splits": comp_probs[0].splits(), "reduction": 1.0 - comp_ms / full_ms,

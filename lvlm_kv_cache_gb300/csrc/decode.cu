@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
 
   if (warp == kDecWarps && GA) {
     // ---- gather producer: the warp reads each tile's 64 listed rows (rows past
-    // the slice end repeat its first row; they are masked), lane 0 issues 16
-    // four-row gathers per 128-byte column slab of K and of V
+    // the slice end repeat its first row; they are masked) and issues the
+    // four-row gathers, one group of K or V per lane
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % C::kStages;
       if (i >= C::kStages) {  // one lane waits for the stage, the warp follows its verdict
@@ -266,23 +266,25 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         rr[q] = v;
       }
       const uint32_t kb = smem_u32(ring + st * C::kStageBytes);
-      if (lane == 0) {
-        fence_proxy_async_smem();  // the consumers' generic reads of this stage come first
-        mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+      // lane L issues four-row group L % 16 of K (L < 16) or of V (L >= 16),
+      // every column slab: the rows of its group come by shuffles
+      const int gg = lane & 15;
+      int rv[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int pos = 4 * gg + t;
+        const int a0 = __shfl_sync(0xffffffffu, rr[0], pos & 31), a1 = __shfl_sync(0xffffffffu, rr[1], pos & 31);
+        rv[t] = pos < 32 ? a0 : a1;
       }
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], C::kStageBytes);
+      __syncwarp();
+      fence_proxy_async_smem();  // the consumers' generic reads of this stage come first
+      const uint32_t base = kb + (lane >= 16 ? C::kTileBytes : 0) + gg * 512;
 #pragma unroll
-      for (int g4 = 0; g4 < kDecRows / 4; ++g4) {
-        const int src = (4 * g4) & 31, q = (4 * g4) >> 5;
-        const int v0 = __shfl_sync(0xffffffffu, rr[q], src), v1 = __shfl_sync(0xffffffffu, rr[q], src + 1);
-        const int v2 = __shfl_sync(0xffffffffu, rr[q], src + 2), v3 = __shfl_sync(0xffffffffu, rr[q], src + 3);
-        if (lane == 0) {
-#pragma unroll
-          for (int sl = 0; sl < C::kSlabs; ++sl) {
-            const int col = (int)(h * a.col_stride_head) + sl * 64;
-            tma_gather4(kb + sl * kDecRows * 128 + g4 * 512, &kmap, col, v0, v1, v2, v3, &full[st]);
-            tma_gather4(kb + C::kTileBytes + sl * kDecRows * 128 + g4 * 512, &vmap, col, v0, v1, v2, v3, &full[st]);
-          }
-        }
+      for (int sl = 0; sl < C::kSlabs; ++sl) {
+        const int col = (int)(h * a.col_stride_head) + sl * 64;
+        tma_gather4(base + sl * kDecRows * 128, lane >= 16 ? &vmap : &kmap, col, rv[0], rv[1], rv[2], rv[3],
+                    &full[st]);
       }
       __syncwarp();
     }
