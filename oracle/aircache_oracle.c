@@ -37,8 +37,11 @@
  *       observation-window table): a continuous window of w = 16 or 32 is the
  *       last w text tokens, "all text tokens" is every text token; either set
  *       takes the elite set's place (its queries score, its keys join the
- *       softmax).  The visual window needs visual-token queries and is not
- *       restated.
+ *       softmax).  The visual window of 32 is the last 32 visual tokens (all of
+ *       them if fewer): their queries attend over the visual keys only (the
+ *       window's own keys are visual keys already), and the visual columns
+ *       averaged over the window rows and the query heads give I_v; it reads
+ *       the visual tokens' queries.
  *   R15 the ablation budgets (same section, layer-budget table): uniform
  *       r_l = r; PyramidKV-style, linear in depth from (2 - 1/beta) r at layer
  *       0 to r / beta at the last layer (mean r; beta = 20, PyramidKV's
@@ -331,6 +334,45 @@ int oracle_window(int n_t, int mode, int32_t* positions) {
     return w;
 }
 
+/* R14's visual window: the last min(32, n_v) visual indices, ascending. */
+int oracle_window_visual(int n_v, int32_t* positions) {
+    if (n_v < 1) return -1;
+    const int w = n_v < 32 ? n_v : 32;
+    for (int e = 0; e < w; ++e) positions[e] = n_v - w + e;
+    return w;
+}
+
+/*
+ * I_v of one (request, layer) for R14's visual window: qv holds the request's
+ * visual-token queries (row i = visual index i), k its keys in prompt order
+ * (R18); window rows pos[0..n_w), softmax over the n_v visual keys only.
+ */
+int oracle_score_visual_window(const oracle_view* qv, const oracle_view* k, int h_q, int h_kv, int d, int n_v,
+                               int n_p, const int32_t* pos, int n_w, double* iv) {
+    if (h_q <= 0 || h_kv <= 0 || h_q % h_kv != 0 || n_v <= 0 || n_w <= 0 || n_p < 0) return -1;
+    for (int e = 0; e < n_w; ++e) if (pos[e] < 0 || pos[e] >= n_v) return -1;
+    const int g = h_q / h_kv;
+    double* logit = (double*)malloc(sizeof(double) * (size_t)n_v);
+    if (!logit) return -1;
+    for (int i = 0; i < n_v; ++i) iv[i] = 0.0;
+    for (int h = 0; h < h_q; ++h) {
+        const int kvh = h / g;
+        for (int e = 0; e < n_w; ++e) {
+            double m = -INFINITY;
+            for (int c = 0; c < n_v; ++c) {
+                logit[c] = scaled_dot(qv, pos[e], h, k, vis_row(n_p, c), kvh, d);
+                if (logit[c] > m) m = logit[c];
+            }
+            double z = 0.0;
+            for (int c = 0; c < n_v; ++c) z += exp(logit[c] - m);
+            for (int c = 0; c < n_v; ++c) iv[c] += exp(logit[c] - m) / z;
+        }
+    }
+    for (int i = 0; i < n_v; ++i) iv[i] /= (double)h_q * (double)n_w;
+    free(logit);
+    return 0;
+}
+
 /*
  * "Ablation studies", layer-budget table (R15): budget mode 0 is the method's
  * own (oracle_budget); 1 uniform; 2 PyramidKV-style (beta = 20); 3 strength
@@ -438,26 +480,32 @@ int64_t oracle_compact(const oracle_view* src, int h_kv, int d, int n_v, int n_t
  * oracle_compact so that callers choose where rows go.
  *
  * q[l], k[l] : views of layer l restricted to this request.
- * iv         : [n_layers * n_v] output; elite: [n_layers * n_t]; n_tk: [n_layers];
+ * iv         : [n_layers * n_v] output; elite: [n_layers * max(n_t, 32)]; n_tk: [n_layers];
  * stats      : [n_layers * 4]; keep: [n_layers]; idx: [n_layers * n_v].
  */
 int oracle_request_variant(const oracle_view* q, const oracle_view* k, int n_layers, int h_q,
                            int h_kv, int d, int n_v, int n_t, int n_p, double alpha, double r, int window_mode,
                            int budget_mode, double* iv, int32_t* elite, int32_t* n_tk, double* stats,
-                           int32_t* keep, int32_t* idx, double* iv_heads, int32_t* idx_heads) {
+                           int32_t* keep, int32_t* idx, double* iv_heads, int32_t* idx_heads,
+                           const oracle_view* qv) {
+    if (window_mode == 4 && (!qv || iv_heads)) return -1;  /* the visual window reads qv; one set per layer */
     double* s_t = (double*)malloc(sizeof(double) * (size_t)n_layers);
     double* s_k = (double*)malloc(sizeof(double) * (size_t)n_layers);
     if (!s_t || !s_k) { free(s_t); free(s_k); return -1; }
     int rc = 0;
     for (int l = 0; l < n_layers && rc == 0; ++l) {
-        int32_t* el = elite + (int64_t)l * n_t;
-        const int ntk = window_mode == 0 ? oracle_elite(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, n_p, alpha, NULL, el)
-                                         : oracle_window(n_t, window_mode, el);
+        int32_t* el = elite + (int64_t)l * (n_t > 32 ? n_t : 32);
+        const int ntk = window_mode == 0   ? oracle_elite(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, n_p, alpha, NULL, el)
+                        : window_mode == 4 ? oracle_window_visual(n_v, el)
+                                           : oracle_window(n_t, window_mode, el);
         if (ntk <= 0) { rc = -1; break; }
         n_tk[l] = ntk;
         double* ivl = iv + (int64_t)l * n_v;
-        rc = oracle_score(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, n_p, el, ntk, ivl, NULL,
-                          iv_heads ? iv_heads + (int64_t)l * h_kv * n_v : NULL);
+        if (window_mode == 4)
+            rc = oracle_score_visual_window(&qv[l], &k[l], h_q, h_kv, d, n_v, n_p, el, ntk, ivl);
+        else
+            rc = oracle_score(&q[l], &k[l], h_q, h_kv, d, n_v, n_t, n_p, el, ntk, ivl, NULL,
+                              iv_heads ? iv_heads + (int64_t)l * h_kv * n_v : NULL);
         if (rc == 0) rc = oracle_stats(ivl, n_v, stats + (int64_t)l * 4);
         if (rc == 0) { s_t[l] = stats[l * 4 + 0]; s_k[l] = stats[l * 4 + 1]; }
     }
@@ -481,7 +529,7 @@ int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int
                    double* iv, int32_t* elite, int32_t* n_tk, double* stats,
                    int32_t* keep, int32_t* idx) {
     return oracle_request_variant(q, k, n_layers, h_q, h_kv, d, n_v, n_t, 0, alpha, r, 0, 0, iv, elite,
-                                  n_tk, stats, keep, idx, NULL, NULL);
+                                  n_tk, stats, keep, idx, NULL, NULL, NULL);
 }
 
 /* ------------------------------------------------------- decode consumer */

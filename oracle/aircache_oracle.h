@@ -44,7 +44,11 @@ int oracle_budget_variant(const double* s_t, const double* s_k, int n_layers, in
 int oracle_request_variant(const oracle_view* q, const oracle_view* k, int n_layers, int h_q,
                            int h_kv, int d, int n_v, int n_t, int n_p, double alpha, double r, int window_mode,
                            int budget_mode, double* iv, int32_t* elite, int32_t* n_tk, double* stats,
-                           int32_t* keep, int32_t* idx, double* iv_heads, int32_t* idx_heads);
+                           int32_t* keep, int32_t* idx, double* iv_heads, int32_t* idx_heads,
+                           const oracle_view* qv);
+int oracle_window_visual(int n_v, int32_t* positions);
+int oracle_score_visual_window(const oracle_view* qv, const oracle_view* k, int h_q, int h_kv, int d, int n_v,
+                               int n_p, const int32_t* pos, int n_w, double* iv);
 int64_t oracle_compact_heads(const oracle_view* src, int h_kv, int d, int n_v, int n_t, int n_p,
                              const int32_t* idx_heads, int keep, void* dst);
 int oracle_request(const oracle_view* q, const oracle_view* k, int n_layers, int h_q, int h_kv,

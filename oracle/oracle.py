@@ -87,7 +87,11 @@ def lib():
         L.oracle_budget_variant.argtypes = [vp, vp, i32, i32, f64, i32, vp, vp]
         L.oracle_budget_variant.restype = i32
         L.oracle_request_variant.argtypes = [V, V, i32, i32, i32, i32, i32, i32, i32, f64, f64, i32, i32,
-                                             vp, vp, vp, vp, vp, vp, vp, vp]
+                                             vp, vp, vp, vp, vp, vp, vp, vp, V]
+        L.oracle_window_visual.argtypes = [i32, vp]
+        L.oracle_window_visual.restype = i32
+        L.oracle_score_visual_window.argtypes = [V, V, i32, i32, i32, i32, i32, vp, i32, vp]
+        L.oracle_score_visual_window.restype = i32
         L.oracle_compact_heads.argtypes = [V, i32, i32, i32, i32, i32, vp, i32, vp]
         L.oracle_compact_heads.restype = i64
         L.oracle_request_variant.restype = i32
@@ -275,8 +279,31 @@ def compact(src: np.ndarray, n_v: int, n_t: int, idx: np.ndarray, n_p: int = 0) 
     return out
 
 
+def window_visual(n_v: int) -> np.ndarray:
+    """R14's visual window: the last min(32, N_v) visual indices."""
+    out = np.zeros(32, np.int32)
+    n = lib().oracle_window_visual(int(n_v), _ptr(out))
+    if n < 0:
+        raise ValueError("oracle_window_visual rejected its arguments")
+    return out[:n].copy()
+
+
+def score_visual_window(qv: np.ndarray, k: np.ndarray, n_v: int, pos, n_p: int = 0) -> np.ndarray:
+    """I_v of one (request, layer) for the visual window: qv [N_v, H_q, D] the
+    visual tokens' queries, k [N_v+N_t, H_kv, D] in prompt order."""
+    _, h_q, d = qv.shape
+    h_kv = k.shape[1]
+    ps = np.ascontiguousarray(pos, dtype=np.int32)
+    iv = np.zeros(n_v, np.float64)
+    rc = lib().oracle_score_visual_window(ctypes.byref(_view(qv)), ctypes.byref(_view(k)), h_q, h_kv, d, n_v,
+                                          int(n_p), _ptr(ps), len(ps), _ptr(iv))
+    if rc != 0:
+        raise ValueError("oracle_score_visual_window rejected its arguments")
+    return iv
+
+
 def request(q_layers, k_layers, n_v: int, alpha: float, r: float, window_mode: int = 0,
-            budget_mode: int = 0, n_p: int = 0, per_head: bool = False):
+            budget_mode: int = 0, n_p: int = 0, per_head: bool = False, qv_layers=None):
     """The whole one-shot pass for one request over its layers (optionally
     with an ablation window / budget variant).
 
@@ -287,8 +314,9 @@ def request(q_layers, k_layers, n_v: int, alpha: float, r: float, window_mode: i
     h_kv = k_layers[0].shape[1]
     qv = (_View * L)(*[_view(a) for a in q_layers])
     kv = (_View * L)(*[_view(a) for a in k_layers])
+    qvis = (_View * L)(*[_view(a) for a in qv_layers]) if qv_layers is not None else None
     iv = np.zeros((L, n_v), np.float64)
-    el = np.zeros((L, n_t), np.int32)
+    el = np.zeros((L, max(n_t, 32)), np.int32)
     ntk = np.zeros(L, np.int32)
     st = np.zeros((L, 4), np.float64)
     keep = np.zeros(L, np.int32)
@@ -298,7 +326,7 @@ def request(q_layers, k_layers, n_v: int, alpha: float, r: float, window_mode: i
     rc = lib().oracle_request_variant(qv, kv, L, h_q, h_kv, d, n_v, n_t, int(n_p), float(alpha), float(r),
                                       int(window_mode), int(budget_mode), _ptr(iv), _ptr(el),
                                       _ptr(ntk), _ptr(st), _ptr(keep), _ptr(idx),
-                                      _ptr(ivh) if per_head else None, _ptr(idxh) if per_head else None)
+                                      _ptr(ivh) if per_head else None, _ptr(idxh) if per_head else None, qvis)
     if rc != 0:
         raise ValueError("oracle_request rejected its arguments")
     return {

@@ -40,6 +40,10 @@ MUTATIONS = {
     "per-head I_v all into head 0": ("iv_heads[(int64_t)kvh * n_v + c] +=", "iv_heads[(int64_t)0 * n_v + c] +="),
     "per-head compaction reads head 0's set": ("vis_row(n_p, idx_heads[(int64_t)h * n_v + j])",
                                                "vis_row(n_p, idx_heads[j])"),
+    "visual window scores the text keys too": ("for (int c = 0; c < n_v; ++c) z += exp(logit[c] - m);\n            for (int c = 0; c < n_v; ++c) iv[c] +=",
+                                               "for (int c = 0; c < n_v; ++c) z += exp(logit[c] - m);\n            z += 1.0;\n            for (int c = 0; c < n_v; ++c) iv[c] +="),
+    "visual window reads the first visual tokens": ("for (int e = 0; e < w; ++e) positions[e] = n_v - w + e;",
+                                                    "for (int e = 0; e < w; ++e) positions[e] = e;"),
     "visual rows ignore the prefix": ("return (int64_t)n_p + i;", "return (int64_t)i;"),
     "text rows ignore the prefix": ("return j < n_p ? (int64_t)j : (int64_t)n_v + j;", "return (int64_t)n_v + j;"),
     "decode head map h mod h_kv": ("const int kv_head = h / group;", "const int kv_head = h % h_kv;"),
@@ -58,7 +62,7 @@ MUTATIONS = {
                                         "const float a = fabsf((float)elem(src, j, 0, i));"),
 }
 PIN_FILES = ["test_oracle_pins.py", "test_oracle_variants.py", "test_oracle_decode.py", "test_oracle_quant.py",
-             "test_oracle_prefix.py", "test_oracle_heads.py"]
+             "test_oracle_prefix.py", "test_oracle_heads.py", "test_oracle_visual_window.py"]
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
