@@ -518,7 +518,8 @@ def main():
     esize = 2 if spec.dtype == torch.bfloat16 else 4
     prob = A.Problem(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.cu_visual, max(spec.n_visual), max(spec.n_text),
                      spec.alpha, spec.r, total_tokens=wl.total_tokens, total_visual=wl.total_visual,
-                     window_mode=args.window_mode, budget_mode=args.budget_mode, head_sets=args.head_sets)
+                     window_mode=args.window_mode, budget_mode=args.budget_mode, head_sets=args.head_sets,
+                     q_visual=W.visual_queries(wl, seed=rank + 1) if args.window_mode == 4 else None)
     ws = prob.new_workspace()
     out = A.alloc_outputs(prob)
     L, B, TV = prob.L, prob.B, prob.total_visual
@@ -527,10 +528,10 @@ def main():
     el_s = torch.empty((L * B, prob.max_text), dtype=torch.int32, device=dev)
     ntk_s = torch.empty(L * B, dtype=torch.int32, device=dev)
     # (the staged scorer takes one index set per layer; the elite sizes do not depend on it)
-    prob_s = prob if not args.head_sets else A.Problem(
+    prob_s = prob if not (args.head_sets or args.window_mode == 4) else A.Problem(
         wl.q, wl.k, wl.v, wl.cu_seqlens, wl.cu_visual, max(spec.n_visual), max(spec.n_text), spec.alpha, spec.r,
-        total_tokens=wl.total_tokens, total_visual=wl.total_visual, window_mode=args.window_mode,
-        budget_mode=args.budget_mode)
+        total_tokens=wl.total_tokens, total_visual=wl.total_visual,
+        window_mode=args.window_mode if args.window_mode != 4 else 0, budget_mode=args.budget_mode)
     A.aircache_score(prob_s, ws, iv_s, el_s, ntk_s)
     assert A.aircache_get_error(ws) == 0
 

@@ -96,7 +96,10 @@ typedef struct aircache_problem {
     int32_t variant;       /* 0: the method.  Ablation variants (AirCache notes, "Ablation
                             * studies"): bits 0-7 the observation window -- 0 the elite
                             * window, 1 the last 16 text tokens, 2 the last 32, 3 every
-                            * text token (a fixed window takes the elite set's place);
+                            * text token (a fixed window takes the elite set's place),
+                            * 4 the last 32 visual tokens (their queries, from q_visual,
+                            * over the visual keys only; aircache_compress on the
+                            * streaming path only);
                             * bits 8-15 the layer budget -- 0 strength + skewness, 1
                             * uniform (r_l = r), 2 PyramidKV-style (linear in depth from
                             * (2 - 1/20) r to r/20), 3 strength only (s'_t r), 4
@@ -132,6 +135,10 @@ typedef struct aircache_problem {
                                  token: the elite window and the scoring run over text
                                  indices as before, and compaction writes the kept visual
                                  rows, then every text row in text order. */
+    const void* const* q_visual;  /* window 4 only (else NULL): HOST array [L] of device
+                                     pointers to the visual tokens' post-RoPE queries,
+                                     [total_visual] rows (request b's at cu_visual[b]..),
+                                     with q_stride_tok / q_stride_head */
 } aircache_problem;
 
 /*

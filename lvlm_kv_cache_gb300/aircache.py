@@ -66,6 +66,7 @@ class ProblemStruct(ctypes.Structure):
         ("alpha", ctypes.c_double),
         ("r", ctypes.c_double),
         ("n_prefix", ctypes.c_void_p),
+        ("q_visual", ctypes.POINTER(ctypes.c_void_p)),
     ]
 
 
@@ -185,7 +186,7 @@ class Problem:
 
     def __init__(self, q, k, v, cu_seqlens, cu_visual, max_visual, max_text, alpha=0.9, r=0.1,
                  max_elite=0, total_tokens=None, total_visual=None, window_mode=0, budget_mode=0,
-                 n_prefix=None, head_sets=False):
+                 n_prefix=None, head_sets=False, q_visual=None):
         qs = list(q.unbind(0)) if torch.is_tensor(q) else list(q)
         ks = list(k.unbind(0)) if torch.is_tensor(k) else list(k)
         vs = list(v.unbind(0)) if torch.is_tensor(v) else list(v)
@@ -226,6 +227,13 @@ class Problem:
             alpha=float(alpha), r=float(r),
             n_prefix=n_prefix.data_ptr() if n_prefix is not None else None,
         )
+        if q_visual is not None:  # window 4: the visual tokens' queries, per layer [total_visual, H_q, D]
+            qvs = list(q_visual.unbind(0)) if torch.is_tensor(q_visual) else list(q_visual)
+            if len(qvs) != L or any(t.stride() != qs[0].stride() for t in qvs):
+                raise ValueError("q_visual: one tensor per layer with q's strides")
+            self._qv = arr(*[t.data_ptr() for t in qvs])
+            self.c.q_visual = ctypes.cast(self._qv, ctypes.POINTER(ctypes.c_void_p))
+            self.q_visual = qvs  # keep alive
         self.n_prefix = n_prefix  # keep alive
         for t in ks + vs + qs:
             if t.stride(2) != 1:

@@ -62,7 +62,7 @@ int validate(const aircache_problem* p) {
   if (p->max_visual < 3 || p->max_text < 1) return AIRCACHE_ERR_INVALID_ARG;
   if (p->max_text > AIRCACHE_MAX_TEXT) return AIRCACHE_ERR_UNSUPPORTED;
   if (p->max_elite < 0 || p->max_elite > p->max_text) return AIRCACHE_ERR_INVALID_ARG;
-  if ((p->variant & ~0xffffff) != 0 || (p->variant & 0xff) > 3 || ((p->variant >> 8) & 0xff) > 4 ||
+  if ((p->variant & ~0xffffff) != 0 || (p->variant & 0xff) > 4 || ((p->variant >> 8) & 0xff) > 4 ||
       ((p->variant >> 16) & 0xff) > 1) {
     return AIRCACHE_ERR_INVALID_ARG;
   }
@@ -76,6 +76,11 @@ int validate(const aircache_problem* p) {
   for (int l = 0; l < p->num_layers; ++l) {
     if (!p->q_text[l] || !p->k[l] || !p->v[l]) return AIRCACHE_ERR_INVALID_ARG;
     if (!aligned16(p->q_text[l]) || !aligned16(p->k[l]) || !aligned16(p->v[l])) return AIRCACHE_ERR_INVALID_ARG;
+  }
+  if ((p->variant & 0xff) == 4) {  // the visual window reads the visual tokens' queries
+    if (!p->q_visual) return AIRCACHE_ERR_INVALID_ARG;
+    for (int l = 0; l < p->num_layers; ++l)
+      if (!p->q_visual[l] || !aligned16(p->q_visual[l])) return AIRCACHE_ERR_INVALID_ARG;
   }
   const int64_t strides[4] = {p->q_stride_tok, p->q_stride_head, p->kv_stride_tok, p->kv_stride_head};
   for (int64_t st : strides) {
@@ -107,6 +112,8 @@ Dev make_dev(const aircache_problem* p) {
   d.max_visual = p->max_visual;
   d.max_text = p->max_text;
   d.max_elite = p->max_elite ? p->max_elite : p->max_text;
+  if ((p->variant & 0xff) == 4) d.max_elite = p->max_visual < 32 ? p->max_visual : 32;  // the visual window's rows
+  d.elite_stride = d.max_text > d.max_elite ? d.max_text : d.max_elite;
   d.rows_max = d.h_q * d.max_elite;
   d.rc_max = (d.g * d.max_elite + 31) / 32;
   d.lse_stride = d.h_kv * d.rc_max * 32;
@@ -138,6 +145,7 @@ LayerPtrs make_ptrs(const aircache_problem* p) {
   std::memset(&lp, 0, sizeof lp);
   for (int l = 0; l < p->num_layers; ++l) {
     lp.q[l] = p->q_text[l];
+    lp.qv[l] = p->q_visual ? p->q_visual[l] : nullptr;
     lp.k[l] = p->k[l];
     lp.v[l] = p->v[l];
   }
@@ -172,7 +180,7 @@ size_t carve(const Dev& d, char* base, Ws* w) {
   t.zero_bytes = zbytes;
   const size_t T1 = (size_t)(d.max_visual + 127) / 128 + (size_t)(d.max_elite + 127) / 128;  // score tile slots
   const size_t G = (size_t)(d.h_kv + 3) / 4;
-  t.elite = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB * d.max_text));
+  t.elite = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB * d.elite_stride));
   t.n_tk = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
   t.stream_list = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
   t.stream_info = reinterpret_cast<int4*>(take(sizeof(int4) * 2 * LB));
@@ -257,6 +265,7 @@ int aircache_score(const aircache_problem* p, void* ws, size_t ws_bytes, float* 
   if ((rc = check_ws(p, ws, ws_bytes)) != AIRCACHE_OK) return rc;
   if (!iv || !elite || !n_tk) return AIRCACHE_ERR_INVALID_ARG;
   if (((p->variant >> 16) & 0xff) != 0) return AIRCACHE_ERR_UNSUPPORTED;  // per-head sets: aircache_compress only
+  if ((p->variant & 0xff) == 4) return AIRCACHE_ERR_UNSUPPORTED;          // the visual window: aircache_compress only
   const Dev d = make_dev(p);
   const LayerPtrs lp = make_ptrs(p);
   Ws w;
@@ -384,6 +393,7 @@ static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, v
   Dev dn = d;
   dn.stream_ok = stream_eligible(d, lp) ? 1 : 0;
   if (d.head_sets && !dn.stream_ok) return AIRCACHE_ERR_UNSUPPORTED;  // per-head sets: the streaming path only
+  if (d.window_mode == 4 && !dn.stream_ok) return AIRCACHE_ERR_UNSUPPORTED;  // the visual window: likewise
   if (events && n_events != (dn.stream_ok ? kStreamCount : kWideCount) + 1) return AIRCACHE_ERR_INVALID_ARG;
   Ws w;
   carve(d, static_cast<char*>(ws), &w);

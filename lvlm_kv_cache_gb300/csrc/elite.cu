@@ -103,9 +103,18 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
 
   const char* kbase = reinterpret_cast<const char*>(a.lp.k[l]);
   const char* qbase = reinterpret_cast<const char*>(a.lp.q[l]);
+  const char* qvbase = reinterpret_cast<const char*>(a.lp.qv[l]);
   int base = 0;
-  int32_t* out = a.w.elite + (size_t)u * p.max_text;
-  if (p.window_mode != 0) {
+  int32_t* out = a.w.elite + (size_t)u * p.elite_stride;
+  if (p.window_mode == 4) {
+    // the visual window: the last min(32, N_v) visual tokens (their queries
+    // score; they add no keys: theirs are visual keys already)
+    base = min(32, R.n_v);
+    for (int e = tid; e < base; e += kEliteThreads) {
+      pos_s[e] = R.n_v - base + e;
+      if (rank == 0) out[e] = R.n_v - base + e;
+    }
+  } else if (p.window_mode != 0) {
     // an ablation window takes the elite set's place: the last 16 / 32 text
     // tokens or every one (the same in every CTA of the cluster)
     const int wsz = p.window_mode == 1 ? 16 : (p.window_mode == 2 ? 32 : n_t);
@@ -247,10 +256,13 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
         if (i < q_n) {
           const int r = q_r0 + i / kVec, c = i % kVec;
           const int kvh = r / rows_g, rr = r % rows_g, hh = rr / n_tk, e = rr % n_tk;
-          const int pos = min(max(pos_s[e], 0), n_t - 1);
+          // window 4: a visual token's query row (visual slot vis0 + pos), else a text row
+          const bool vq = p.window_mode == 4;
+          const int pos = min(max(pos_s[e], 0), (vq ? R.n_v : n_t) - 1);
           v[q] = __ldg(reinterpret_cast<const uint4*>(
-                           qbase + ((R.txt0 + pos) * p.q_stride_tok + (int64_t)(kvh * p.g + hh) * p.q_stride_head) *
-                                       sizeof(T)) +
+                           (vq ? qvbase : qbase) + (((vq ? R.vis0 : R.txt0) + pos) * p.q_stride_tok +
+                                                    (int64_t)(kvh * p.g + hh) * p.q_stride_head) *
+                                                       sizeof(T)) +
                        c);
         }
       }
@@ -260,7 +272,7 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
         if (i < q_n) qdst[i] = v[q];
       }
     }
-    const int k_n = (kve - kvb) * n_tk * kVec;
+    const int k_n = p.window_mode == 4 ? 0 : (kve - kvb) * n_tk * kVec;  // the visual window adds no keys
     for (int i0 = tid; i0 < k_n; i0 += kGatherBatch * kEliteThreads) {
       uint4 v[kGatherBatch];
 #pragma unroll

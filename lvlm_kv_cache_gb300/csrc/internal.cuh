@@ -16,6 +16,7 @@ namespace aircache {
 struct Dev {
   int L, B, h_q, h_kv, d, g, dtype;
   int max_visual, max_text, max_elite;
+  int elite_stride;      // entries per (layer, request) of the elite list: max(max_text, max_elite)
   int rows_max;          // h_q * max_elite: query rows per (layer, request)
   int rc_max;            // ceil(g * max_elite / 32): 32-row chunks per KV head
   int lse_stride;        // h_kv * rc_max * 32: floats of row LSEs per (layer, request)
@@ -42,6 +43,7 @@ constexpr int kStreamTiles = 4;
 
 struct LayerPtrs {
   const void* q[AIRCACHE_MAX_LAYERS];
+  const void* qv[AIRCACHE_MAX_LAYERS];  // visual-token queries (window 4 only)
   const void* k[AIRCACHE_MAX_LAYERS];
   const void* v[AIRCACHE_MAX_LAYERS];
 };

@@ -109,7 +109,8 @@ __device__ __forceinline__ float2 merge_ms(float2 a, float2 b) {
 
 __device__ __forceinline__ bool stream_unit(const Dev& p, int u, const int4& i0, const int4& i1) {
   const int n_v = i0.w, n_t = i1.x, n_tk = i1.y;
-  return u >= 0 && u < p.L * p.B && i1.z == 1 && n_tk >= 1 && n_tk <= n_t && n_tk <= p.max_elite &&
+  return u >= 0 && u < p.L * p.B && i1.z == 1 && n_tk >= 1 && (n_tk <= n_t || p.window_mode == 4) &&
+         n_tk <= p.max_elite &&
          n_v >= 3 && n_v <= p.max_visual && i0.x >= 0 && (long long)i0.x + n_v <= p.total_tokens &&
          i0.y >= 0 && (long long)i0.y + n_v <= p.total_visual;
 }
@@ -237,10 +238,10 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
       } else {
         kind = kTxt;  // elite text keys: at most max_elite <= 8192, 128 per stage
         key0 = 0;
-        nkeys = n_tk;
+        nkeys = p.window_mode == 4 ? 0 : n_tk;  // the visual window adds no keys: one empty stage
         stage_keys = kTK;
       }
-      const int nst = (nkeys + stage_keys - 1) / stage_keys;
+      const int nst = max(1, (nkeys + stage_keys - 1) / stage_keys);
       const uint32_t kbytes = kind == kVis ? (uint32_t)Gm::kSBytes : (uint32_t)(Gm::kNH * kTK * 128);
       const int l = u / p.B;
       for (int rc = 0; ok && rc < n_rc; ++rc, ++sub) {
@@ -263,7 +264,7 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
           h.l = l;
           h.kvh = kvh;
           h.key0 = k0;
-          h.klim = min(stage_keys, (kind == kVis ? n_v : n_tk) - k0);
+          h.klim = min(stage_keys, (kind == kVis ? n_v : nkeys) - k0);
           h.rows = min(kRC, rows - rc * kRC);
           h.r0 = rc * kRC;
           h.first = (j == 0);

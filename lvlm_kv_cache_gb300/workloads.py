@@ -207,6 +207,16 @@ def host_bits(t: torch.Tensor) -> np.ndarray:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
+def visual_queries(wl: Workload, seed: int = 0) -> torch.Tensor:
+    """Seeded post-RoPE queries of the visual tokens, [L, total_visual, H_q, D]
+    (the entries' distribution of the text queries), for the visual window."""
+    s = wl.spec
+    gen = torch.Generator(device=wl.q.device)
+    gen.manual_seed(seed)
+    q = torch.randn((s.L, wl.total_visual, s.H_q, s.D), generator=gen, device=wl.q.device) * s.entry_std
+    return q.to(s.dtype)
+
+
 def with_prefix(wl: Workload, n_prefix) -> tuple:
     """The same tokens with the first n_prefix[b] text tokens of request b moved
     before its visual span (prompt order [prefix text][visual][other text]).
