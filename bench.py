@@ -51,7 +51,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="7b")
     ap.add_argument("--window-mode", type=int, default=0,
-                    help="ablation observation window: 0 elite (the method), 1 last 16, 2 last 32, 3 all text")
+                    help="ablation observation window: 0 elite (the method), 1 last 16, 2 last 32, 3 all text, "
+                         "4 the last 32 visual tokens (seeded visual queries)")
     ap.add_argument("--budget-mode", type=int, default=0,
                     help="ablation budget: 0 strength + skewness (the method), 1 uniform, 2 PyramidKV-style, "
                          "3 strength only, 4 skewness only")
@@ -555,6 +556,8 @@ def main():
     if st != 0:
         raise RuntimeError(f"device error {st}: {A.status_string(st)}")
     n_tk = ntk_s.cpu().numpy()
+    if args.window_mode == 4:  # 32 window rows per unit (their keys are visual keys: a slight overcount)
+        n_tk = np.minimum(32, np.tile(np.asarray(spec.n_visual), spec.L))
     keep = out["keep"].cpu().numpy()
     kbytes, path_bytes = algorithmic_bytes(spec, n_tk, keep, esize)
 
