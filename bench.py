@@ -557,6 +557,8 @@ def main():
         raise RuntimeError(f"device error {st}: {A.status_string(st)}")
     n_tk = ntk_s.cpu().numpy()
     if args.window_mode == 4:  # 32 window rows per unit (their keys are visual keys: a slight overcount)
+        import numpy as np
+
         n_tk = np.minimum(32, np.tile(np.asarray(spec.n_visual), spec.L))
     keep = out["keep"].cpu().numpy()
     kbytes, path_bytes = algorithmic_bytes(spec, n_tk, keep, esize)
