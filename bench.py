@@ -533,8 +533,9 @@ def main():
         wl.q, wl.k, wl.v, wl.cu_seqlens, wl.cu_visual, max(spec.n_visual), max(spec.n_text), spec.alpha, spec.r,
         total_tokens=wl.total_tokens, total_visual=wl.total_visual,
         window_mode=args.window_mode if args.window_mode != 4 else 0, budget_mode=args.budget_mode)
-    A.aircache_score(prob_s, ws, iv_s, el_s, ntk_s)
-    assert A.aircache_get_error(ws) == 0
+    ws_s = ws if prob_s is prob else prob_s.new_workspace()
+    A.aircache_score(prob_s, ws_s, iv_s, el_s, ntk_s)
+    assert A.aircache_get_error(ws_s) == 0
 
     def step():
         A.aircache_compress(prob, ws, out["out_k"], out["out_v"], out["out_offsets"], out["keep"],
