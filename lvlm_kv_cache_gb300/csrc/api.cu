@@ -426,7 +426,7 @@ static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, v
     AC_TRY(launch_score(dn, lp, w, plan_score(dn, sms, true, out_rows_capacity), s));
     AC_TRY(mark(k++));
   }
-  AC_TRY(launch_select(dn, w, s));
+  AC_TRY(launch_select(dn, w, s, dn.stream_ok != 0));
   AC_TRY(mark(k++));
   AC_TRY(launch_compact(dn, lp, w, out_k, out_v, out_rows_capacity, s));
   AC_TRY(mark(k++));

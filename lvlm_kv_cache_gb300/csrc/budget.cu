@@ -94,8 +94,8 @@ __global__ void __launch_bounds__(kTailThreads) stream_stats_kernel(const __grid
   __shared__ ff st_s[AIRCACHE_MAX_LAYERS], sk_s[AIRCACHE_MAX_LAYERS];
   __shared__ long long seg[kTailThreads / 32 + 1];
   __shared__ int flag;
-  pdl_trigger();
-  pdl_wait();  // the moment records
+  pdl_wait();     // the moment records
+  pdl_trigger();  // only now: the selection kernel reads I_v as soon as it starts
   if (*(volatile int32_t*)w.error != 0) return;
   Req R;
   if (!load_req(p, b, R)) {

@@ -152,7 +152,9 @@ cudaError_t launch_score(const Dev& p, const LayerPtrs& lp, const Ws& w, const S
 // records that passes 2 and 2k wrote instead of a pass over I_v.
 cudaError_t launch_stats_budget(const Dev& p, const Ws& w, double* stats_out,
                                 int64_t out_capacity, bool offsets, cudaStream_t s, bool parts = false);
-cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s);
+// early_iv: I_v is complete when the select grid launches (it follows the
+// streaming statistics kernel, which triggers its dependents only after its wait).
+cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s, bool early_iv = false);
 // Streaming scoring path (stream.cu).  stream_eligible: the problem's dtype,
 // sizes and key layout allow it (bf16, per-layer key pointers evenly strided);
 // it depends on the problem alone, so the kernel sequence of a call is known on

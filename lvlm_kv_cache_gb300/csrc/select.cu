@@ -31,6 +31,9 @@ struct SelectArgs {
   Dev p;
   Ws w;
   int smem_keys;  // capacity of the dynamic shared-memory key buffer
+  int early_iv;   // 1: I_v is complete when this grid launches (the kernel before triggers only after
+                  // pass 2k is done), so the keys are staged and the first digit counted before the
+                  // wait for the keep counts
 };
 
 // Larger float <=> larger key (handles -0.0 and negatives, which I_v never has).
@@ -82,28 +85,14 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   __shared__ unsigned sel_digit, sel_above, sel_count, n_cand_s;
   __shared__ uint32_t wmin[kSelWarps], wmax[kSelWarps];
   pdl_trigger();
-  pdl_wait();  // I_v and the keep counts
-  if (*(volatile int32_t*)w.error != 0) return;
+  if (!a.early_iv) pdl_wait();  // I_v and the keep counts
   Req R;
-  if (!load_req(p, b, R)) {
-    if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
-    return;
-  }
-  const int n = R.n_v;
-  const int k = w.keep[u];
-  if (k < 0 || k > n) {
-    if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
-    return;
-  }
+  const bool ok_req = load_req(p, b, R);
+  const int n = ok_req ? R.n_v : 0;
   // one set per layer from I_v, or one per KV head from that KV group's I_v
   const size_t set = p.head_sets ? (size_t)l * p.h_kv + hs : (size_t)l;
   const float* x = (p.head_sets ? w.ivh : w.iv) + set * p.total_visual + R.vis0;
   int32_t* out = w.idx + set * p.total_visual + R.vis0;
-  if (k == n) {
-    for (int i = tid; i < n; i += kSelThreads) out[i] = i;
-    return;
-  }
-  if (k == 0) return;
   const bool staged = n <= a.smem_keys;
   // stage the keys (when they fit) and find the smallest and largest
   uint32_t kmin = 0xffffffffu, kmax = 0u;
@@ -139,6 +128,33 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   uint32_t mask = top >= 31 ? 0u : ~((2u << top) - 1u);
   if (top < 0) mask = 0xffffffffu;
   uint32_t prefix = kmin & mask;
+  // the first digit's histogram needs the keys only
+  if (top >= 0) {
+    const int bits = min(11, top + 1), shift = top - bits + 1;
+    const uint32_t dmask = (1u << bits) - 1u;
+    for (int i = tid; i < (1 << bits); i += kSelThreads) hist[i] = 0;
+    __syncthreads();  // also: the staged keys are in shared memory
+    for (int i = tid; i < n; i += kSelThreads) {
+      const uint32_t key = key_at(i);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
+    }
+  }
+  if (a.early_iv) pdl_wait();  // the keep counts
+  if (*(volatile int32_t*)w.error != 0) return;
+  if (!ok_req) {
+    if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int k = __ldcg(&w.keep[u]);
+  if (k < 0 || k > n) {
+    if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  if (k == n) {
+    for (int i = tid; i < n; i += kSelThreads) out[i] = i;
+    return;
+  }
+  if (k == 0) return;
   unsigned want = (unsigned)k;  // keys >= T still to account for
   bool all_taken = false;       // every key of the selected bucket is taken: T = prefix, no ties to break
   if (tid == 0) sel_count = (unsigned)n;  // all keys equal: every one is == T
@@ -148,13 +164,15 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
     top = shift - 1;
     const int nb = 1 << bits;
     const uint32_t dmask = (uint32_t)nb - 1u;
-    for (int i = tid; i < nb; i += kSelThreads) hist[i] = 0;
-    __syncthreads();  // also: the staged keys are in shared memory
-    const bool from_cand = staged && pass > 0;
-    const int m = from_cand ? n_cand : n;
-    for (int i = tid; i < m; i += kSelThreads) {
-      const uint32_t key = from_cand ? cand[i] : key_at(i);
-      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
+    if (pass > 0) {  // pass 0's histogram was counted above
+      for (int i = tid; i < nb; i += kSelThreads) hist[i] = 0;
+      __syncthreads();
+      const bool from_cand = staged;
+      const int m = from_cand ? n_cand : n;
+      for (int i = tid; i < m; i += kSelThreads) {
+        const uint32_t key = from_cand ? cand[i] : key_at(i);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
+      }
     }
     __syncthreads();
     // bins in descending digit order: thread t owns positions t*bpt .. t*bpt+bpt-1
@@ -271,10 +289,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
 
 }  // namespace
 
-cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s) {
+cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s, bool early_iv) {
   SelectArgs a;
   a.p = p;
   a.w = w;
+  a.early_iv = early_iv ? 1 : 0;
   a.smem_keys = p.max_visual < kSmemKeys ? p.max_visual : kSmemKeys;
   const int smem = 2 * (int)sizeof(uint32_t) * a.smem_keys;  // keys + candidates
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(select_kernel), smem);
