@@ -9,12 +9,13 @@
 // to the 16 rows of an mma.sync A operand).  A producer warp reads the range
 // and streams 64-row K and V tiles of that head with TMA through a ring of
 // stages (bf16: 128-byte swizzle; int8 codes: plain rows, which each consumer
-// warp widens to bf16 in a scratch laid out like a swizzled tile); four
+// warp widens to f16 in a scratch laid out like a swizzled tile); four
 // consumer warps each take 16 rows of a tile:
 //   S = Q K^T      A = Q (16 heads x 16 d, in registers), B = K (ldmatrix),
-//   online softmax in base 2 per head, P rounded to bf16 (the normaliser sums
-//                  the rounded weights, so the output is an exact convex
-//                  combination with relatively perturbed weights),
+//   online softmax in base 2 per head, P rounded to bf16 (int8 cache: to f16,
+//                  scaled by 2^14; the normaliser sums the rounded weights, so
+//                  the output is an exact convex combination with relatively
+//                  perturbed weights),
 //   O += P V       A = P (the S accumulators repacked), B = V (ldmatrix.trans).
 // The warps' (max, sum, O) merge in shared memory.  The slices of one
 // (sequence, KV head) then merge in one of three ways: a single slice writes
@@ -31,6 +32,7 @@
 // (2 * head_dim * element bytes per row and head), the queries, and the fp32
 // output.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <algorithm>
 
@@ -52,8 +54,9 @@ constexpr int kDecZeroBlock = 256;    // error word, then the per-(s, h) counter
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 // Q8: the cached rows are int8 codes (a plain row-major tile per stage, no
-// swizzle); each consumer warp widens its 16 rows to bf16 in a scratch of its
-// own, laid out like a swizzled bf16 tile, and runs the same MMA code on it.
+// swizzle); each consumer warp widens its 16 rows to f16 (exact integers) in a
+// scratch of its own, laid out like a swizzled 16-bit tile, and runs the same
+// MMA code on it with f16 operands (Q converted once, P packed to f16).
 template <int D, bool Q8>
 struct DecCfg {
   static constexpr int kSlabs = D / 64;                       // 128-byte bf16 column slabs per row
@@ -65,7 +68,7 @@ struct DecCfg {
   static constexpr int kMerge = kDecWarps * (kDecMaxGroup * D + 2 * kDecMaxGroup) * 4;
   static constexpr int kPartEnd = 45056 + kDecMaxGroup * D * 4 + kDecMaxGroup * 8;  // the cluster partial's end
   static constexpr int kMain = (cmax(cmax(kRing, kMerge), kPartEnd) + 1023) / 1024 * 1024;
-  static constexpr int kWarpScratch = Q8 ? 2 * 16 * D * 2 : 0;  // K and V rows of one warp, bf16
+  static constexpr int kWarpScratch = Q8 ? 2 * 16 * D * 2 : 0;  // K and V rows of one warp, f16
   static constexpr int kScratch = kDecWarps * kWarpScratch;
   static constexpr int kQBytes = kDecMaxGroup * kQPitch * 2;
   // 1024-byte alignment slack for the swizzled ring
@@ -103,6 +106,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi, float& lo_r, f
   hi_r = __high2float(t);
   return *reinterpret_cast<uint32_t*>(&t);
 }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi, float& lo_r, float& hi_r) {
+  __half2 t = __floats2half2_rn(lo, hi);
+  lo_r = __low2float(t);
+  hi_r = __high2float(t);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+// D(16x8, fp32) += A(16x16, f16, row) * B(16x8, f16, col)
+__device__ __forceinline__ void mma_f16_16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// The int8 path multiplies in f16 (codes are exact there), the bf16 path in bf16.
+template <bool F16>
+__device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  if constexpr (F16) {
+    mma_f16_16816(c, a, b0, b1);
+  } else {
+    mma_bf16_16816(c, a, b0, b1);
+  }
+}
+// P leaves the int8 path's softmax scaled by 2^14 (its largest weight, 1,
+// becomes 16384 < 65504): weights down to 2^-28 stay normal f16 numbers.
+constexpr float kP16 = 16384.f;
 
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t r[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -116,13 +145,21 @@ __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-// 8 int8 codes (lo: bytes 0-3, hi: bytes 4-7) -> 8 bf16 (exact: |code| <= 127)
-__device__ __forceinline__ uint32_t widen2(uint32_t w, int sh) {
-  const __nv_bfloat162 t = __floats2bfloat162_rn((float)(int8_t)(w >> sh), (float)(int8_t)(w >> (sh + 8)));
-  return *reinterpret_cast<const uint32_t*>(&t);
+// 8 int8 codes (lo: bytes 0-3, hi: bytes 4-7) -> 8 f16, exactly, without a
+// conversion instruction: code c becomes the unsigned byte u = c + 128 (flip
+// the top bit), the byte permute places u in the low mantissa bits of the f16
+// 0x6400 (= 1024), so the half is 1024 + u, and one packed subtraction of 1152
+// leaves c (every integer below 2048 is an f16).
+__device__ __forceinline__ uint32_t widen2_f16(uint32_t u4, uint32_t sel) {
+  uint32_t t = __byte_perm(u4, 0x64646464u, sel);
+  const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&t), __float2half2_rn(1152.f));
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 __device__ __forceinline__ uint4 widen8(uint32_t lo, uint32_t hi) {
-  return make_uint4(widen2(lo, 0), widen2(lo, 16), widen2(hi, 0), widen2(hi, 16));
+  lo ^= 0x80808080u;
+  hi ^= 0x80808080u;
+  return make_uint4(widen2_f16(lo, 0x4140u), widen2_f16(lo, 0x4342u), widen2_f16(hi, 0x4140u),
+                    widen2_f16(hi, 0x4342u));
 }
 
 __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
@@ -338,13 +375,42 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       ldmatrix_x4(qa[kk], qs + (ri + 8 * (mi & 1)) * C::kQPitch + 16 * kk + 8 * (mi >> 1));
     }
   }
+  // int8 cache: Q enters the f16 MMA as Q * 2^e, with e chosen so that the
+  // group's largest |q| lands in [2^14, 2^15) (no f16 overflow; scaling by a
+  // power of two is exact, and a bf16 value fits an f16 mantissa)
+  float qscale = 1.f;
+  if constexpr (Q8) {
+    float mx = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qa[kk][j]));
+        mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (mx > 0.f && mx < INFINITY) {
+      int ex;
+      (void)frexpf(mx, &ex);  // mx = f * 2^ex, f in [0.5, 1)
+      qscale = ldexpf(1.f, min(15 - ex, 120));  // (a subnormal maximum: no overflow)
+    }
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qa[kk][j]));
+        const __half2 hq = __floats2half2_rn(f.x * qscale, f.y * qscale);
+        qa[kk][j] = *reinterpret_cast<const uint32_t*>(&hq);
+      }
+  }
   float o[D / 8][4];
 #pragma unroll
   for (int t = 0; t < D / 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
   float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
   const int r0 = 16 * warp;
   // logits in base 2; an int8 cache folds its key scale in here (q . (s c) = s (q . c))
-  const float kmult = Q8 ? a.scale_log2 * a.k_scale[(int64_t)s * a.h_kv + h] : a.scale_log2;
+  const float kmult = Q8 ? a.scale_log2 * a.k_scale[(int64_t)s * a.h_kv + h] / qscale : a.scale_log2;
   bool alive = true;
 
   for (int i = 0; i < ntiles && alive; ++i) {
@@ -361,7 +427,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       int rb;                          // this warp's first row in the tile it reads
       constexpr int kSlabStride = (Q8 ? 16 : kDecRows) * 128;
       if constexpr (Q8) {
-        // widen the warp's 16 int8 rows of K and V to bf16 in its scratch
+        // widen the warp's 16 int8 rows of K and V to f16 in its scratch
         // (rows past the slice end become 0), then hand the stage back
         const uint8_t* kt = ring + st * C::kStageBytes + r0 * D;
         const uint8_t* vt = kt + C::kTileBytes;
@@ -415,8 +481,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         for (int kk = 0; kk < D / 16; ++kk) {
           uint32_t kf[4];
           ldsm_x4(kf, swz(kb + (kk >> 2) * kSlabStride, row, 2 * (kk & 3) + (mi & 1)));
-          mma_bf16_16816(sc[0], qa[kk], kf[0], kf[1]);
-          mma_bf16_16816(sc[1], qa[kk], kf[2], kf[3]);
+          mma16816<Q8>(sc[0], qa[kk], kf[0], kf[1]);
+          mma16816<Q8>(sc[1], qa[kk], kf[2], kf[3]);
         }
       }
       // online softmax, base 2; rows at or past `valid` get weight 0
@@ -445,10 +511,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         float x0, x1;
-        pa[2 * t] = pack_bf16(fast_exp2(sc[t][0] - nA), fast_exp2(sc[t][1] - nA), x0, x1);
-        sA += x0 + x1;
-        pa[2 * t + 1] = pack_bf16(fast_exp2(sc[t][2] - nB), fast_exp2(sc[t][3] - nB), x0, x1);
-        sB += x0 + x1;
+        if constexpr (Q8) {
+          pa[2 * t] = pack_f16(kP16 * fast_exp2(sc[t][0] - nA), kP16 * fast_exp2(sc[t][1] - nA), x0, x1);
+          sA += (x0 + x1) * (1.f / kP16);
+          pa[2 * t + 1] = pack_f16(kP16 * fast_exp2(sc[t][2] - nB), kP16 * fast_exp2(sc[t][3] - nB), x0, x1);
+          sB += (x0 + x1) * (1.f / kP16);
+        } else {
+          pa[2 * t] = pack_bf16(fast_exp2(sc[t][0] - nA), fast_exp2(sc[t][1] - nA), x0, x1);
+          sA += x0 + x1;
+          pa[2 * t + 1] = pack_bf16(fast_exp2(sc[t][2] - nB), fast_exp2(sc[t][3] - nB), x0, x1);
+          sB += x0 + x1;
+        }
       }
       lA = lA * fA + sA;
       lB = lB * fB + sB;
@@ -467,8 +540,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         for (int np = 0; np < D / 16; ++np) {
           uint32_t vf[4];
           ldsm_x4_trans(vf, swz(vb + (np >> 2) * kSlabStride, row, 2 * (np & 3) + (mi >> 1)));
-          mma_bf16_16816(o[2 * np], pa, vf[0], vf[1]);
-          mma_bf16_16816(o[2 * np + 1], pa, vf[2], vf[3]);
+          mma16816<Q8>(o[2 * np], pa, vf[0], vf[1]);
+          mma16816<Q8>(o[2 * np + 1], pa, vf[2], vf[3]);
         }
       }
     }
@@ -515,8 +588,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   }
   named_bar_sync(1, kDecWarps * 32);
   const int64_t head0 = (int64_t)s * a.h_q + (int64_t)h * g;  // first query head of the group
-  // an int8 cache's value scale multiplies the cached rows' weighted sum
-  const float vmult = Q8 ? a.v_scale[(int64_t)s * a.h_kv + h] : 1.f;
+  // an int8 cache's value scale multiplies the cached rows' weighted sum (and
+  // undoes the 2^14 its f16 weights carry; the sums of weights do not carry it)
+  const float vmult = Q8 ? a.v_scale[(int64_t)s * a.h_kv + h] * (1.f / kP16) : 1.f;
   for (int idx = tid; idx < g * D; idx += kDecWarps * 32) {
     const int hh = idx / D, d = idx % D;
     float m = -INFINITY;
