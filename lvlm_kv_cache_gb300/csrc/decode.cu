@@ -68,7 +68,7 @@ struct DecCfg {
   static constexpr int kMerge = kDecWarps * (kDecMaxGroup * D + 2 * kDecMaxGroup) * 4;
   static constexpr int kPartEnd = 45056 + kDecMaxGroup * D * 4 + kDecMaxGroup * 8;  // the cluster partial's end
   static constexpr int kMain = (cmax(cmax(kRing, kMerge), kPartEnd) + 1023) / 1024 * 1024;
-  static constexpr int kWarpScratch = Q8 ? 2 * 16 * D * 2 : 0;  // K and V rows of one warp, f16
+  static constexpr int kWarpScratch = Q8 ? 16 * D * 2 : 0;  // V rows of one warp, f16
   static constexpr int kScratch = kDecWarps * kWarpScratch;
   static constexpr int kQBytes = kDecMaxGroup * kQPitch * 2;
   // 1024-byte alignment slack for the swizzled ring
@@ -368,7 +368,23 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   const int hA = lane >> 2;  // heads of this thread's accumulator rows: hA and hA + 8
   const int cq = lane & 3;
   uint32_t qa[D / 16][4];
-  {
+  if constexpr (Q8) {
+    // int8 cache: the head dimension is permuted so that each thread takes its
+    // key codes as whole words (k-step kk of quad lane cq covers
+    // d = cq*D/4 + 4kk + 0..3: k = 2cq, 2cq+1 -> +0, +1; k = 2cq+8, 2cq+9 ->
+    // +2, +3); Q's A fragments are read from the staged rows the same way
+    const __nv_bfloat16* q0 = qs + hA * C::kQPitch + cq * (D / 4);
+    const __nv_bfloat16* q1 = q0 + 8 * C::kQPitch;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint2 x = *reinterpret_cast<const uint2*>(q0 + 4 * kk);
+      const uint2 y = *reinterpret_cast<const uint2*>(q1 + 4 * kk);
+      qa[kk][0] = x.x;
+      qa[kk][1] = y.x;
+      qa[kk][2] = x.y;
+      qa[kk][3] = y.y;
+    }
+  } else {
     const int mi = lane >> 3, ri = lane & 7;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
@@ -426,32 +442,41 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       uint32_t kb, vb;
       int rb;                          // this warp's first row in the tile it reads
       constexpr int kSlabStride = (Q8 ? 16 : kDecRows) * 128;
+      uint32_t kq[2][Q8 ? D / 16 : 1];  // int8: this thread's key codes of rows hA and hA + 8
       if constexpr (Q8) {
-        // widen the warp's 16 int8 rows of K and V to f16 in its scratch
-        // (rows past the slice end become 0), then hand the stage back
+        // keys: the thread's D/4 codes of each of its two rows, as words (rows
+        // past the slice end read as 0); values: widened to f16 in the warp's
+        // scratch for the transposing ldmatrix; then hand the stage back
         const uint8_t* kt = ring + st * C::kStageBytes + r0 * D;
         const uint8_t* vt = kt + C::kTileBytes;
-        uint8_t* wk = scratch + warp * C::kWarpScratch;
-        const uint32_t wks = smem_u32(wk), wvs = wks + C::kWarpScratch / 2;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int rr = 8 * t + hA;
+          const uint4* src = reinterpret_cast<const uint4*>(kt + rr * D + cq * (D / 4));
+#pragma unroll
+          for (int v = 0; v < D / 64; ++v) {
+            const uint4 x = rr < valid ? src[v] : make_uint4(0, 0, 0, 0);
+            kq[t][4 * v] = x.x;
+            kq[t][4 * v + 1] = x.y;
+            kq[t][4 * v + 2] = x.z;
+            kq[t][4 * v + 3] = x.w;
+          }
+        }
+        const uint32_t wvs = smem_u32(scratch + warp * C::kWarpScratch);
         __syncwarp();
         for (int c = lane; c < 16 * (D / 16); c += 32) {
           const int rr = c / (D / 16), ch = c % (D / 16);
-          uint4 kw = make_uint4(0, 0, 0, 0), vw = make_uint4(0, 0, 0, 0);
-          if (rr < valid) {
-            kw = *reinterpret_cast<const uint4*>(kt + rr * D + ch * 16);
-            vw = *reinterpret_cast<const uint4*>(vt + rr * D + ch * 16);
-          }
+          uint4 vw = make_uint4(0, 0, 0, 0);
+          if (rr < valid) vw = *reinterpret_cast<const uint4*>(vt + rr * D + ch * 16);
           const uint32_t slab = (uint32_t)((ch * 16) / 64) * kSlabStride;
           const int c8 = 2 * (ch & 3);
-          st_shared_u4(swz(wks + slab, rr, c8), widen8(kw.x, kw.y));
-          st_shared_u4(swz(wks + slab, rr, c8 + 1), widen8(kw.z, kw.w));
           st_shared_u4(swz(wvs + slab, rr, c8), widen8(vw.x, vw.y));
           st_shared_u4(swz(wvs + slab, rr, c8 + 1), widen8(vw.z, vw.w));
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
         released = true;
-        kb = wks;
+        kb = 0;
         vb = wvs;
         rb = 0;
       } else {
@@ -474,7 +499,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       }
       // S = Q K^T for 16 rows: two n-tiles of 8 rows
       float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-      {
+      if constexpr (Q8) {
+        // B fragments from the codes: bytes 0, 1 of a word -> b0, bytes 2, 3 -> b1
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t x = kq[t][kk] ^ 0x80808080u;
+            mma16816<true>(sc[t], qa[kk], widen2_f16(x, 0x4140u), widen2_f16(x, 0x4342u));
+          }
+        }
+      } else {
         const int mi = lane >> 3, ri = lane & 7;
         const int row = rb + ri + 8 * (mi >> 1);
 #pragma unroll
