@@ -141,6 +141,17 @@ def test_decode_from_int8_with_new_row_and_empty(A, oracle):
     decode_int8_check(A, oracle, di, 900)
 
 
+@pytest.mark.parametrize("q_scale", [1e20, 1e-20, 1e-37])
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_from_int8_extreme_query_magnitudes(A, oracle, q_scale, d):
+    # the int8 path feeds Q to its f16 MMAs times a power of two chosen from
+    # the group's largest |q|: no overflow for huge queries (one-hot weights),
+    # no loss for tiny ones (near-uniform weights), and the exponent clamp for
+    # a maximum near the bottom of the bf16 range
+    di = W.decode_inputs([3, 64, 1000], 28, 4, d, seed=27, device="cuda", q_scale=q_scale)
+    decode_int8_check(A, oracle, di, 1000)
+
+
 def test_decode_from_int8_rows_past_a_range(A, oracle):
     # the codes after the last range are garbage for this call: never mixed in
     di = W.decode_inputs([40, 77], 8, 2, 128, seed=25, device="cuda")
