@@ -194,9 +194,13 @@ AIRCACHE_API int aircache_budget(const aircache_problem* p, const float* iv, voi
  * Limit: num_layers * num_requests <= AIRCACHE_NOALLOC_MAX_UNITS (2048); a
  * larger problem returns AIRCACHE_ERR_UNSUPPORTED before anything is enqueued
  * (use aircache_budget with a workspace instead).
- * First call on a device: looks up the scratch address (cudaGetSymbolAddress,
- * which may load the module) with that device current and caches it; make
- * that first call before capturing any stream.  Later calls reuse the address.
+ * First call in a context: looks up the scratch address (cudaGetSymbolAddress,
+ * which may load the module) with that context current and caches it under
+ * the context's unique id; make that first call before capturing any stream.
+ * Later calls in the same context reuse the address; a call made in another
+ * context (a new one after cudaDeviceReset, or a second context of a
+ * driver-API caller) looks it up again, since the address is only valid in
+ * the context that was current when it was looked up.
  * Concurrency: the scratch is shared by every call on the device in the
  * process, so calls whose executions overlap (other streams, other host
  * threads) race on it and give wrong results; order them on one stream or
@@ -204,7 +208,9 @@ AIRCACHE_API int aircache_budget(const aircache_problem* p, const float* iv, voi
  *   iv, stats, keep: as in aircache_budget (stats may be NULL).
  *   device_status: NULL, or a device int32 that receives the device-side
  *     status (AIRCACHE_OK or an AIRCACHE_ERR_DEVICE_* code) by a 4-byte
- *     device-to-device copy enqueued after the kernel.
+ *     device-to-device copy enqueued after the kernel.  keep and stats are
+ *     only meaningful when that status is AIRCACHE_OK; after an inconsistent
+ *     request layout the keep counts of the affected request are written as 0.
  * Host-detected errors are returned as by aircache_budget.
  */
 AIRCACHE_API int aircache_budget_noalloc(const aircache_problem* p, const float* iv, double* stats,

@@ -15,6 +15,7 @@
 // keep counts, and the CTA finishing the last request writes the offsets.
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "internal.cuh"
 #include "ptx.cuh"
@@ -23,7 +24,7 @@
 namespace aircache {
 namespace {
 
-constexpr int kStatsThreads = 256;   // stand-alone offsets kernel, allocation-free budget
+constexpr int kStatsThreads = 256;   // stand-alone offsets kernel
 constexpr int kTailThreads = 1024;   // one (layer, request) per CTA: one load round per moment pass
 constexpr int kBarAll = 1;
 
@@ -50,25 +51,35 @@ __global__ void __launch_bounds__(NT) stats_budget_kernel(const __grid_constant_
   pdl_wait();  // I_v
   if (*(volatile int32_t*)w.error != 0) return;
   Req R;
-  if (!load_req(p, b, R)) {
-    if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
-    return;
-  }
-  const float* x = w.iv + (size_t)l * p.total_visual + R.vis0;
-  const double2 m = unit_moments<NT>(x, R.n_v, tid, redff, kBarAll);
-  if (tid == 0) {
-    w.stats[2 * u] = m.x;
-    w.stats[2 * u + 1] = m.y;
-    if (a.stats_out) {
-      a.stats_out[2 * u] = m.x;
-      a.stats_out[2 * u + 1] = m.y;
+  const bool ok = load_req(p, b, R);
+  if (ok) {
+    const float* x = w.iv + (size_t)l * p.total_visual + R.vis0;
+    const double2 m = unit_moments<NT>(x, R.n_v, tid, redff, kBarAll);
+    if (tid == 0) {
+      w.stats[2 * u] = m.x;
+      w.stats[2 * u + 1] = m.y;
+      if (a.stats_out) {
+        a.stats_out[2 * u] = m.x;
+        a.stats_out[2 * u + 1] = m.y;
+      }
     }
+  } else if (tid == 0) {
+    set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+  }
+  // every CTA arrives, also after an error, so that the request's last CTA
+  // always runs and its keep counts are always written
+  if (tid == 0) {
     __threadfence();
     flag = (atomicAdd(&w.cnt_req[b], 1u) == (unsigned)(p.L - 1)) ? 1 : 0;
   }
   __syncthreads();
   if (!flag) return;
   __threadfence();
+  if (!ok || *(volatile int32_t*)w.error != 0) {
+    // an inconsistent layout: the request's keep counts are 0 (the error word says why)
+    for (int ll = tid; ll < p.L; ll += NT) w.keep[ll * p.B + b] = 0;
+    return;
+  }
   if (tid < 32) request_budget(p, b, R.n_v, w.stats, w.keep, tid);
   if constexpr (OFFSETS) {
     __threadfence();
@@ -184,23 +195,63 @@ static_assert(kNaStatsOff % 256 == 0, "stats block alignment");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNaBytes];
 
-constexpr int kNaMaxDevices = 64;
+// The scratch address belongs to the context in which the module was loaded:
+// the cache is keyed on the driver's unique id of the current context, so a new
+// context (after cudaDeviceReset, or a second context that a driver-API caller
+// made current) looks the address up again instead of using a stale one.
+struct NaEntry {
+  unsigned long long ctx_id;
+  char* addr;
+};
 std::mutex g_na_mutex;
-char* g_na_addr[kNaMaxDevices] = {};
+std::vector<NaEntry> g_na_cache;
 
-// Device address of the scratch on the current device; looked up once per
-// device (the lookup may load the module), then cached.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Id of the current context (0 with none current, or where the driver lacks the call).
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the scratch in the current context; looked up once per
+// context (the lookup may load the module and make the device's primary
+// context current), then cached under that context's id.
 int noalloc_scratch(char** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return AIRCACHE_ERR_CUDA;
-  if (dev < 0 || dev >= kNaMaxDevices) return AIRCACHE_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_na_mutex);
-  if (!g_na_addr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return AIRCACHE_ERR_CUDA;
-    g_na_addr[dev] = static_cast<char*>(ptr);
+  unsigned long long id = current_ctx_id();
+  if (id != 0) {
+    for (const NaEntry& e : g_na_cache) {
+      if (e.ctx_id == id) {
+        *out = e.addr;
+        return AIRCACHE_OK;
+      }
+    }
   }
-  *out = g_na_addr[dev];
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return AIRCACHE_ERR_CUDA;
+  if (id == 0) id = current_ctx_id();  // the lookup made a context current
+  if (id != 0) g_na_cache.push_back(NaEntry{id, static_cast<char*>(ptr)});
+  *out = static_cast<char*>(ptr);
   return AIRCACHE_OK;
 }
 
@@ -223,7 +274,8 @@ int budget_noalloc(const Dev& p, const float* iv, double* stats_out, int32_t* ke
   a.w.keep = keep;
   a.stats_out = stats_out;
   a.out_capacity = 0;
-  stats_budget_kernel<kStatsThreads, false><<<dim3(p.B, p.L), kStatsThreads, 0, s>>>(a);
+  // the same kernel and block size as aircache_budget: the same reduction order
+  stats_budget_kernel<kTailThreads, false><<<dim3(p.B, p.L), kTailThreads, 0, s>>>(a);
   if (cudaGetLastError() != cudaSuccess) return AIRCACHE_ERR_CUDA;
   if (device_status &&
       cudaMemcpyAsync(device_status, base, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess) {

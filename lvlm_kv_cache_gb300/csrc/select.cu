@@ -86,8 +86,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   __shared__ uint32_t wmin[kSelWarps], wmax[kSelWarps];
   pdl_trigger();
   if (!a.early_iv) pdl_wait();  // I_v and the keep counts
-  Req R;
+  Req R{};
   const bool ok_req = load_req(p, b, R);
+  if (!ok_req) R.vis0 = 0;
   const int n = ok_req ? R.n_v : 0;
   // one set per layer from I_v, or one per KV head from that KV group's I_v
   const size_t set = p.head_sets ? (size_t)l * p.h_kv + hs : (size_t)l;

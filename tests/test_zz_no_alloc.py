@@ -5,6 +5,8 @@ The GPU test runs the workspace entry point aircache_budget and then the
 no-allocation entry point twice in a row on the same I_v (the second call
 relies on the first having left its scratch reusable) and requires the same
 statistics, the same keep counts and a clean device status each time.  The
+keep counts are also checked directly against the oracle's budget of the same
+I_v, so the test does not rest on the workspace path alone.  The
 file is named to be collected last, so the scratch is also exercised after
 every other GPU test of a session; it passes on its own in a fresh process
 too.  The host-side limit check needs no GPU."""
@@ -63,9 +65,28 @@ def test_noalloc_budget_matches_workspace_budget(A, name, layers, requests):
         A.aircache_budget_noalloc(prob, iv, stats, keep, device_status=status)
         torch.cuda.synchronize()
         assert int(status.item()) == 0, f"call {call}: device status {int(status.item())}"
-        # same kernel, same reduction order: the tolerance only guards the comparison itself
-        np.testing.assert_allclose(stats.cpu().numpy(), ref_s, rtol=1e-12, atol=0.0)
+        # both entry points launch the same kernel with the same block size, so
+        # the reduction order is the same and the results agree bit for bit
+        np.testing.assert_array_equal(stats.cpu().numpy(), ref_s)
         assert np.array_equal(keep.cpu().numpy(), ref_k), f"call {call}: keep counts differ"
+
+    # against the oracle: (s_t, s_k) of the same I_v in fp64 to the float-float
+    # precision of the device reduction, and the oracle's keep counts exactly
+    from oracle import oracle as O
+
+    iv_h = iv.cpu().numpy().astype(np.float64)
+    cu_v = wl.cu_visual.cpu().numpy()
+    for b in range(B):
+        n_v = int(cu_v[b + 1] - cu_v[b])
+        st, sk = [], []
+        for l in range(L):
+            s_t, s_k, _, _ = O.stats(iv_h[l, cu_v[b]:cu_v[b + 1]])
+            st.append(s_t)
+            sk.append(s_k)
+            np.testing.assert_allclose(ref_s[l * B + b], [s_t, s_k], rtol=1e-9, atol=1e-12)
+        _, keep_o = O.budget(st, sk, n_v, wl.spec.r)
+        keep_g = ref_k[[l * B + b for l in range(L)]]
+        assert np.array_equal(keep_g, keep_o), f"request {b}: keep differs from the oracle"
 
     # stats may be omitted
     keep = torch.full((L * B,), -1, dtype=torch.int32, device="cuda")
