@@ -447,6 +447,7 @@ def run_decode(args, local):
             rows, secs, n = decode_oracle_sample(qdec[0], ranges, args.cpu_sample_s / 2)
             ms_step = secs / rows * full_rows * 1e3
             line["cpu_baseline"] = {"value": ms_step, "unit": "ms per full-cache step (extrapolated)", "cores": 1,
+                                    "host_cores": os.cpu_count(),
                                     "kind": "oracle",
                                     "sample": f"{n} (layer 0, request) sequence(s) of {P} rows in {secs:.2f} s, "
                                               f"single thread, scaled by rows to the {L}x{B} sequences of a step"}
@@ -480,9 +481,11 @@ def run_reference(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": DESCRIPTIONS.get(args.config, args.config), "name": args.config,
                    "sample": "one request (all layers) per step",
+                   "inputs": "the same recipe and shapes drawn by the CPU generator (same seed, other values "
+                             "than the GPU arm's device generator draws)",
                    "variant": {"window_mode": args.window_mode, "budget_mode": args.budget_mode}},
         "impl": "reference",
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
                          "sample": "request 0 of the workload, all layers, per step"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -700,7 +703,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tok, secs, nreq = oracle_sample(wl, args.cpu_sample_s, window_mode=args.window_mode,
                                         budget_mode=args.budget_mode)
-        line["cpu_baseline"] = {"value": tok / secs, "unit": UNIT, "cores": 1, "kind": "oracle",
+        line["cpu_baseline"] = {"value": tok / secs, "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(),
+                                "kind": "oracle",
                                 "sample": f"{nreq} whole request(s) x {spec.L} layers "
                                           f"({tok} visual KV rows) in {secs:.2f} s, single thread"}
     if rank == 0:

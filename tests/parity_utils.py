@@ -108,9 +108,15 @@ def check_request(oracle, wl, b, cu_s, cu_v, gpu, report, oracle_iv_by_layer=Non
             np.testing.assert_allclose(gpu["stats"][u], [s_t, s_k], rtol=1e-9, atol=1e-12)
     rl, keep_o = oracle.budget_variant(st, sk, n_v, spec.r, budget_mode)
     keep_g = np.array([gpu["keep"][l * spec.B + b] for l in range(spec.L)])
+    # distance of r_l * N_v from the nearest half-integer (where rounding turns)
+    margin = [abs(rl[l] * n_v - np.floor(rl[l] * n_v) - 0.5) for l in range(spec.L)]
+    report["half_margin"] = min(report.get("half_margin", np.inf), min(margin))
     boundary = [l for l in range(spec.L) if near_half(rl[l] * n_v, 1e-9)]
     mism = [l for l in range(spec.L) if keep_g[l] != keep_o[l] and l not in boundary]
     assert not mism, f"keep counts differ at layers {mism}: gpu {keep_g[mism]} oracle {keep_o[mism]}"
+    # a mismatch inside the 1e-9 band is counted; strict callers fail on it
+    report["near_half_exempt"] = report.get("near_half_exempt", 0) + sum(
+        1 for l in boundary if keep_g[l] != keep_o[l])
     for l in range(spec.L):
         iv_g = gpu["iv"][l, cu_v[b]:cu_v[b + 1]].astype(np.float64)
         sel_o = oracle.select(iv_g, int(keep_g[l]))
@@ -122,6 +128,8 @@ def check_request(oracle, wl, b, cu_s, cu_v, gpu, report, oracle_iv_by_layer=Non
     if oracle_iv_by_layer is not None and len(oracle_iv_by_layer) == spec.L:
         st_o, sk_o = zip(*[oracle.stats(oracle_iv_by_layer[l])[:2] for l in range(spec.L)])
         rl_o, keep_oo = oracle.budget_variant(st_o, sk_o, n_v, spec.r, budget_mode)
+        report["half_margin_oracle"] = min(report.get("half_margin_oracle", np.inf),
+                                           min(abs(x * n_v - np.floor(x * n_v) - 0.5) for x in rl_o))
         for l in range(spec.L):
             if keep_oo[l] != keep_g[l]:
                 assert abs(int(keep_oo[l]) - int(keep_g[l])) <= 1 and near_half(rl_o[l] * n_v), \

@@ -80,7 +80,7 @@ def assert_same(staged, fused, prob):
     assert np.array_equal(staged["out_v"], fused["out_v"])
 
 
-def full_check(A, oracle, wl, units="all", compact_units="all", score_requests=None, **kw):
+def full_check(A, oracle, wl, units="all", compact_units="all", score_requests=None, strict=True, **kw):
     window_mode, budget_mode = kw.get("window_mode", 0), kw.get("budget_mode", 0)
     prob = make_problem(A, wl, **kw)
     staged = run_staged(A, prob)
@@ -102,6 +102,11 @@ def full_check(A, oracle, wl, units="all", compact_units="all", score_requests=N
     cu = all_units if compact_units == "all" else compact_units
     for (l, b) in cu:
         PU.check_compaction(oracle, wl, l, b, cu_s, cu_v, staged)
+    if strict:
+        # no keep count may rest on a rounding exemption: every one equals the
+        # oracle's budget on the GPU's I_v and on the oracle's own I_v
+        assert report.get("near_half_exempt", 0) == 0, report
+        assert report.get("keep_boundary", 0) == 0, report
     return staged, report
 
 
