@@ -196,12 +196,13 @@ def algorithmic_bytes(spec, n_tk, keep, esize):
     layer) formula 2*H_kv*D*(N_v+N_t) + 2*H_q*D*(1+N_tk) + 8*H_kv*D*(keep+N_t)
     (bf16; esize-scaled) + the I_v workspace.  bf16 units take the streaming
     path (pass 1 reads the unit's keys and elite query rows; pass 2, or pass 2k
-    when g * N_tk > 32, writes I_v); other units the wide kernel."""
+    when g * N_tk > 64, writes I_v; the selection kernel reads the moment records
+    back for the budget); other units the wide kernel."""
     row = spec.H_kv * spec.D * esize
     qrow = spec.H_q * spec.D * esize
     g = spec.H_q // spec.H_kv
     k = {"elite_window": 0, "score_pass1": 0, "score_pass2": 0, "score_pass2k": 0, "score_wide": 0,
-         "stats_budget": 0, "select_topk": 0, "gather_compact": 0}
+         "budget_select": 0, "select_topk": 0, "gather_compact": 0}
     path = 0
     for l in range(spec.L):
         for b, (nv, nt) in enumerate(unit_lengths(spec)):
@@ -211,15 +212,15 @@ def algorithmic_bytes(spec, n_tk, keep, esize):
             if esize == 2:
                 k["score_pass1"] += (nv + t) * row + t * qrow
                 # I_v written, plus one 48-byte moment record per key block
-                # (256 keys in pass 2, 128 in pass 2k), read back by the stats kernel
-                recs = -(-nv // (256 if g * t <= 32 else 128))
-                k["score_pass2" if g * t <= 32 else "score_pass2k"] += 4 * nv + 48 * recs
-                k["stats_budget"] += 48 * recs
+                # (256 keys in pass 2, 128 in pass 2k), read back by the selection
+                recs = -(-nv // (256 if g * t <= 64 else 128))
+                k["score_pass2" if g * t <= 64 else "score_pass2k"] += 4 * nv + 48 * recs
+                k["budget_select"] += 48 * recs + 4 * nv + 4 * kp
                 iv_passes = 2  # written, read by the selection
             else:
                 k["score_wide"] += (nv + t) * row + t * qrow + 4 * nv
                 recs, iv_passes = 0, 3  # written, read for the moments and by the selection
-            k["select_topk"] += 4 * nv + 4 * kp
+                k["select_topk"] += 4 * nv + 4 * kp
             k["gather_compact"] += 2 * 2 * (kp + nt) * row + 4 * kp
             path += ((nv + nt) * row + (1 + t) * qrow + 2 * 2 * (kp + nt) * row + 4 * nv * iv_passes
                      + 96 * recs + 8 * kp)

@@ -39,10 +39,10 @@ namespace {
 
 constexpr size_t kAlign = 256;
 // Kernels of one aircache_compress call, by scoring path.
-const char* const kStreamKernels[] = {"elite_window", "score_pass1", "score_pass2",   "score_pass2k",
-                                      "stats_budget", "select_topk", "gather_compact"};
+const char* const kStreamKernels[] = {"elite_window", "score_pass1",   "score_pass2",
+                                      "score_pass2k", "budget_select", "gather_compact"};
 const char* const kWideKernels[] = {"elite_window", "score_wide", "select_topk", "gather_compact"};
-constexpr int kStreamCount = 7, kWideCount = 4;
+constexpr int kStreamCount = 6, kWideCount = 4;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -163,16 +163,17 @@ size_t carve(const Dev& d, char* base, Ws* w) {
   };
   Ws t;
   std::memset(&t, 0, sizeof t);
-  // zeroed block: error, cnt_all, ticket, ticket_n, list_n[4], cnt_req[B],
+  // zeroed block: error, cnt_all, ticket, ticket_n, list_n[4], p2pack, cnt_req[B],
   // cnt_p1/cnt_p2/lse_ready/p2claim[L*B]
-  const size_t zbytes = 40 + sizeof(uint32_t) * (d.B + 4 * LB);
+  const size_t zbytes = 48 + sizeof(uint32_t) * (d.B + 4 * LB);
   char* zero = take(zbytes);
   t.error = reinterpret_cast<int32_t*>(zero);
   t.cnt_all = reinterpret_cast<uint32_t*>(zero ? zero + 4 : nullptr);
   t.ticket = reinterpret_cast<unsigned long long*>(zero ? zero + 8 : nullptr);
   t.ticket_n = reinterpret_cast<unsigned long long*>(zero ? zero + 16 : nullptr);
   t.list_n = reinterpret_cast<int32_t*>(zero ? zero + 24 : nullptr);
-  t.cnt_req = reinterpret_cast<uint32_t*>(zero ? zero + 40 : nullptr);
+  t.p2pack = reinterpret_cast<unsigned long long*>(zero ? zero + 40 : nullptr);
+  t.cnt_req = reinterpret_cast<uint32_t*>(zero ? zero + 48 : nullptr);
   t.cnt_p1 = t.cnt_req ? t.cnt_req + d.B : nullptr;
   t.cnt_p2 = t.cnt_p1 ? t.cnt_p1 + LB : nullptr;
   t.lse_ready = t.cnt_p2 ? t.cnt_p2 + LB : nullptr;
@@ -184,13 +185,14 @@ size_t carve(const Dev& d, char* base, Ws* w) {
   t.n_tk = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
   t.stream_list = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
   t.stream_info = reinterpret_cast<int4*>(take(sizeof(int4) * 2 * LB));
+  t.p2wpre = reinterpret_cast<uint32_t*>(take(sizeof(uint32_t) * LB));
   t.wide_list = reinterpret_cast<int32_t*>(take(sizeof(int32_t) * LB));
   if (d.dtype == AIRCACHE_BF16) {  // the streaming path exists for bf16 only
     const size_t kvrows = (size_t)d.L * d.h_kv;
     // rows of the streaming path's logit buffer: every request's keys, each
     // request starting at a multiple of 4 columns (4 columns of padding per request)
     const size_t stride = (size_t)(d.total_visual + 4 * (int64_t)d.B + 7) / 4 * 4;
-    t.lg = reinterpret_cast<float*>(take(sizeof(float) * kvrows * kRowChunk * stride));
+    t.lg = reinterpret_cast<float*>(take(sizeof(float) * kvrows * kLgRows * stride));
     t.mom = reinterpret_cast<float4*>(take(sizeof(float4) * 3 * LB * (size_t)d.mom_slots));
     t.part_s = reinterpret_cast<float2*>(take(sizeof(float2) * LB * d.h_kv * d.rc_max * kRowChunk * d.chn));
   }
@@ -420,13 +422,11 @@ static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, v
     AC_TRY(mark(k++));
     AC_TRY(launch_stream_p2k(dn, maps, w, sms, s));
     AC_TRY(mark(k++));
-    AC_TRY(launch_stats_budget(dn, w, nullptr, out_rows_capacity, true, s, true));
-    AC_TRY(mark(k++));
   } else {
     AC_TRY(launch_score(dn, lp, w, plan_score(dn, sms, true, out_rows_capacity), s));
     AC_TRY(mark(k++));
   }
-  AC_TRY(launch_select(dn, w, s, dn.stream_ok != 0));
+  AC_TRY(launch_select(dn, w, s, dn.stream_ok != 0, out_rows_capacity));
   AC_TRY(mark(k++));
   AC_TRY(launch_compact(dn, lp, w, out_k, out_v, out_rows_capacity, s));
   AC_TRY(mark(k++));

@@ -7,12 +7,9 @@
 // compression the CTA finishing the last request writes the compacted-cache
 // row offsets.  The wide scoring kernel computes the same quantities at its
 // tail with the same device functions.  A separate one-CTA kernel writes the
-// offsets for the staged compaction.
-//
-// On the streaming scoring path the moments are already reduced per key block
-// (passes 2 and 2k write one record per block), so one CTA per request merges
-// them: warp w takes layers w, w+32, ..., warp 0 then computes the request's
-// keep counts, and the CTA finishing the last request writes the offsets.
+// offsets for the staged compaction.  (On the streaming scoring path of the
+// fused call the selection kernel derives the budgets itself, from the key-block
+// moment records of passes 2 and 2k: select.cu.)
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -89,71 +86,6 @@ __global__ void __launch_bounds__(NT) stats_budget_kernel(const __grid_constant_
     if (!flag) return;
     __threadfence();
     write_offsets<NT>(p, w.keep, w.out_offsets, w.error, a.out_capacity, seg, tid, kBarAll);
-  }
-}
-
-// Streaming path: (s_t, s_k) of every layer of request b from the key-block
-// moment records, then its keep counts; with OFFSETS the CTA finishing the
-// last request writes the row offsets.
-template <bool OFFSETS>
-__global__ void __launch_bounds__(kTailThreads) stream_stats_kernel(const __grid_constant__ StatsArgs a) {
-  constexpr int kWarps = kTailThreads / 32;
-  const Dev& p = a.p;
-  const Ws& w = a.w;
-  const int b = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  __shared__ ff st_s[AIRCACHE_MAX_LAYERS], sk_s[AIRCACHE_MAX_LAYERS];
-  __shared__ long long seg[kTailThreads / 32 + 1];
-  __shared__ int flag;
-  pdl_wait();     // the moment records
-  pdl_trigger();  // only now: the selection kernel reads I_v as soon as it starts
-  if (*(volatile int32_t*)w.error != 0) return;
-  Req R;
-  if (!load_req(p, b, R)) {
-    if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
-    return;
-  }
-  for (int l = warp; l < p.L; l += kWarps) {
-    const int u = l * p.B + b;
-    // pass 2 wrote one record per 256 keys of a one-chunk unit, pass 2k one per
-    // 128-key tile of a multi-chunk unit
-    const int blk = p.g * __ldcg(&w.n_tk[u]) <= kRowChunk ? 256 : 128;
-    ff s_t, s_k;
-    layer_stats_warp(w.mom + (size_t)u * p.mom_slots * kMomWords, (R.n_v + blk - 1) / blk, lane, s_t, s_k);
-    if (lane == 0) {
-      st_s[l] = s_t;
-      sk_s[l] = s_k;
-      const double dt = ff_to_double(s_t), dk = ff_to_double(s_k);
-      w.stats[2 * u] = dt;
-      w.stats[2 * u + 1] = dk;
-      if (a.stats_out) {
-        a.stats_out[2 * u] = dt;
-        a.stats_out[2 * u + 1] = dk;
-      }
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    request_budget_warp(
-        p, b, R.n_v,
-        [&](int l, ff& st, ff& sk) {
-          st = st_s[l];
-          sk = sk_s[l];
-        },
-        w.keep, lane);
-  }
-  if constexpr (OFFSETS) {
-    if (p.B > 1) {
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) flag = (atomicAdd(w.cnt_all, 1u) == (unsigned)(p.B - 1)) ? 1 : 0;
-      __syncthreads();
-      if (!flag) return;
-      __threadfence();
-    } else {
-      __syncthreads();  // one request: this CTA wrote every keep count
-    }
-    write_offsets<kTailThreads>(p, w.keep, w.out_offsets, w.error, a.out_capacity, seg, tid, kBarAll);
   }
 }
 
@@ -285,16 +217,12 @@ int budget_noalloc(const Dev& p, const float* iv, double* stats_out, int32_t* ke
 }
 
 cudaError_t launch_stats_budget(const Dev& p, const Ws& w, double* stats_out, int64_t out_capacity,
-                                bool offsets, cudaStream_t s, bool parts) {
+                                bool offsets, cudaStream_t s) {
   StatsArgs a;
   a.p = p;
   a.w = w;
   a.stats_out = stats_out;
   a.out_capacity = out_capacity;
-  if (parts) {
-    return offsets ? launch_pdl(stream_stats_kernel<true>, dim3(p.B), dim3(kTailThreads), 0, s, a)
-                   : launch_pdl(stream_stats_kernel<false>, dim3(p.B), dim3(kTailThreads), 0, s, a);
-  }
   return offsets ? launch_pdl(stats_budget_kernel<kTailThreads, true>, dim3(p.B, p.L), dim3(kTailThreads), 0, s, a)
                  : launch_pdl(stats_budget_kernel<kTailThreads, false>, dim3(p.B, p.L), dim3(kTailThreads), 0, s, a);
 }

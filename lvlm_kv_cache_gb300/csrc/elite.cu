@@ -312,11 +312,22 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
     } else {
       // route the unit to its scoring path
       if (p.stream_ok) {
-        // units with several row chunks (the heavier work) fill the list from the
-        // front, the others from the back: the streaming pass claims the heavy ones first
+        // units whose logits are recomputed in pass 2k (more than kLgRows query
+        // rows per KV head: the heavier work) fill the list from the front, the
+        // others from the back: the streaming pass claims the heavy ones first
         atomicAdd(&a.w.list_n[0], 1);
-        const int slot = p.g * base > kRowChunk ? atomicAdd(&a.w.list_n[2], 1)
-                                                : p.L * p.B - 1 - atomicAdd(&a.w.list_n[3], 1);
+        int slot;
+        if (p.g * base > kLgRows) {
+          slot = atomicAdd(&a.w.list_n[2], 1);
+        } else {
+          // the pass-2 units also carry their weight (256-key blocks x 32-row
+          // chunks per KV head) and the weight routed before them, for pass 2's
+          // balanced partition: one 64-bit atomic assigns both
+          const unsigned wgt = (unsigned)(((R.n_v + 255) / 256) * ((p.g * base + kRowChunk - 1) / kRowChunk));
+          const unsigned long long old = atomicAdd(a.w.p2pack, (1ULL << 32) | wgt);
+          slot = p.L * p.B - 1 - (int)(old >> 32);
+          a.w.p2wpre[slot] = (uint32_t)old;
+        }
         a.w.stream_list[slot] = u;
         a.w.stream_info[2 * slot] = make_int4((int)vis_tok(R, 0), (int)R.vis0, (int)R.txt0, R.n_v);
         a.w.stream_info[2 * slot + 1] = make_int4(R.n_t, base, 1, u);

@@ -40,6 +40,10 @@ struct Dev {
 // covers this many 128-key visual tiles.
 constexpr int kRowChunk = 32;
 constexpr int kStreamTiles = 4;
+// Rows per (layer, KV head) of the stored-logit buffer: units with at most
+// this many query rows per KV head (two row chunks) keep their pass-1 logits
+// and take pass 2; the others recompute them from the keys in pass 2k.
+constexpr int kLgRows = 2 * kRowChunk;
 
 struct LayerPtrs {
   const void* q[AIRCACHE_MAX_LAYERS];
@@ -56,7 +60,8 @@ struct Ws {
   unsigned long long* ticket;  // [1] next pass-1 work item of the wide scoring kernel
   unsigned long long* ticket_n;  // [1] next pass-1 work item of the streaming path
   int32_t* list_n;       // [4]   units on the streaming path, on the wide path, streaming units
-                         //       with more than one row chunk per KV head, the other streaming units
+                         //       without stored logits (pass 2k), the other streaming units
+  unsigned long long* p2pack;  // [1] routing of the pass-2 units: (count << 32) + their total weight
   uint32_t* cnt_req;     // [B]   layers of a request whose stats are done
   uint32_t* p2claim;     // [L*B] claimed pass-2 work items per (layer, request)
   uint32_t* cnt_p1;      // [L*B] finished pass-1 items per (layer, request)
@@ -64,11 +69,14 @@ struct Ws {
   uint32_t* lse_ready;   // [L*B] row log-sum-exps published
   int32_t* elite;        // [L*B*max_text]
   int32_t* n_tk;         // [L*B]
-  int32_t* stream_list;  // [L*B] streaming units: multi-chunk ones in slots [0, list_n[2]), the
-                         //       others in [L*B - list_n[3], L*B) (any order within each)
+  int32_t* stream_list;  // [L*B] streaming units: those with more than kLgRows rows per KV head
+                         //       (pass 2k) in slots [0, list_n[2]), the others (pass 2) in
+                         //       [L*B - list_n[3], L*B) (any order within each)
   int4* stream_info;     // [L*B][2] the layout record of stream_list[i] (as uinfo, with .w of the second = u)
+  uint32_t* p2wpre;      // [L*B] pass-2 units: the weight of the pass-2 units routed before the one in
+                         //       this slot (weight = 256-key blocks x 32-row chunks per KV head)
   int32_t* wide_list;    // [L*B] units on the wide path (list_n[1] of them, any order)
-  float* lg;             // [L][h_kv][32][lg stride] streaming path: logits of row r of KV head h
+  float* lg;             // [L][h_kv][kLgRows][lg stride] streaming path: logits of row r of KV head h
   float4* mom;           // [L*B][mom_slots][3] streaming path: moments of each key block / tile of I_v
   float2* part_s;        // [L*B][h_kv][rc_max*32][chn] streaming pass 1: (max, sum of exp2) per (row, chunk)
   int4* uinfo;           // [L*B][2] {seq0, vis0, txt0, N_v}, {N_t, N_tk, 1, 0} per (layer, request)
@@ -148,13 +156,13 @@ cudaError_t launch_score(const Dev& p, const LayerPtrs& lp, const Ws& w, const S
                          cudaStream_t s);
 // Stats and keep counts from I_v, one CTA per (layer, request); with
 // `offsets` also the compacted-cache row offsets (checked against out_capacity).
-// With `parts` (streaming path), the statistics come from the per-block moment
-// records that passes 2 and 2k wrote instead of a pass over I_v.
 cudaError_t launch_stats_budget(const Dev& p, const Ws& w, double* stats_out,
-                                int64_t out_capacity, bool offsets, cudaStream_t s, bool parts = false);
-// early_iv: I_v is complete when the select grid launches (it follows the
-// streaming statistics kernel, which triggers its dependents only after its wait).
-cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s, bool early_iv = false);
+                                int64_t out_capacity, bool offsets, cudaStream_t s);
+// budget (streaming path): the select kernel first derives the keep counts of
+// its request from passes 2 / 2k's moment records, writes the statistics and
+// keep counts, and its last CTA the row offsets (checked against out_capacity).
+cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s, bool budget = false,
+                          int64_t out_capacity = 0);
 // Streaming scoring path (stream.cu).  stream_eligible: the problem's dtype,
 // sizes and key layout allow it (bf16, per-layer key pointers evenly strided);
 // it depends on the problem alone, so the kernel sequence of a call is known on

@@ -400,9 +400,8 @@ __device__ __forceinline__ void layer_stats_warp(const float4* rec, int nslots, 
 // against an fp64 evaluation r_l N_v moves by ~1e-10 at most, which matters only
 // within that distance of a half-integer); the layer sums are fixed-order
 // butterflies, so the result is the same run to run.
-template <typename Get>
-__device__ __forceinline__ void request_budget_warp(const Dev& p, int b, int n_v, Get get, int32_t* keep,
-                                                    int lane) {
+template <typename Get, typename Put>
+__device__ __forceinline__ void request_budget_warp_put(const Dev& p, int n_v, Get get, Put put, int lane) {
   // The loops over a lane's layers stay rolled (re-reading the pairs through
   // `get`): this runs once per request, so its code is usually cold in the
   // instruction cache and its size, not its arithmetic, sets the time.
@@ -464,8 +463,16 @@ __device__ __forceinline__ void request_budget_warp(const Dev& p, int b, int n_v
       kf = ff_floor(ff_add(ff_mul(rl, ff{(float)n_v, 0.f}), ff{0.5f, 0.f}));
     }
     kf = fminf(fmaxf(kf, 1.f), (float)n_v);
-    keep[l * p.B + b] = (int32_t)kf;
+    put(l, (int32_t)kf);
   }
+}
+
+// The same, writing keep[l * B + b].
+template <typename Get>
+__device__ __forceinline__ void request_budget_warp(const Dev& p, int b, int n_v, Get get, int32_t* keep,
+                                                    int lane) {
+  request_budget_warp_put(
+      p, n_v, get, [&](int l, int32_t k) { keep[l * p.B + b] = k; }, lane);
 }
 
 // request_budget_warp over (s_t, s_k) pairs stored as doubles (stats[2u],

@@ -16,8 +16,17 @@
 // lowest-position keys == T with ballots and one scan of the warp totals, so
 // the output is in ascending position order.
 // Integer work only: the result is exact and deterministic.
+//
+// On the streaming path of the fused call the kernel also takes the layer
+// budget ("Key design 2") off the critical path of a kernel of its own: while
+// its keys are staged, warp w merges the key-block moment records of layers w,
+// w + 32, ... of its request into (s_t, s_k) (float-float, the same arithmetic
+// in every CTA of the request), warp 0 turns them into the request's keep
+// counts, and the CTA keeps its own layer's count.  The last CTA to arrive
+// writes the compacted-cache row offsets.
 #include "internal.cuh"
 #include "ptx.cuh"
+#include "reduce.cuh"
 
 namespace aircache {
 namespace {
@@ -30,10 +39,11 @@ constexpr int kMaxBins = 2048;        // widest digit: 11 bits
 struct SelectArgs {
   Dev p;
   Ws w;
-  int smem_keys;  // capacity of the dynamic shared-memory key buffer
-  int early_iv;   // 1: I_v is complete when this grid launches (the kernel before triggers only after
-                  // pass 2k is done), so the keys are staged and the first digit counted before the
-                  // wait for the keep counts
+  int smem_keys;          // capacity of the dynamic shared-memory key buffer
+  int budget;             // 1 (streaming path): the CTA first computes its request's layer budgets
+                          // from the moment records of passes 2 / 2k, writes its own layer's keep
+                          // count and statistics, and the last CTA writes the row offsets
+  int64_t out_capacity;   // rows of the output arena (budget mode)
 };
 
 // Larger float <=> larger key (handles -0.0 and negatives, which I_v never has).
@@ -84,11 +94,32 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   __shared__ int wgt[kSelWarps + 1], weq[kSelWarps + 1];
   __shared__ unsigned sel_digit, sel_above, sel_count, n_cand_s;
   __shared__ uint32_t wmin[kSelWarps], wmax[kSelWarps];
+  __shared__ ff st_s[AIRCACHE_MAX_LAYERS], sk_s[AIRCACHE_MAX_LAYERS];
+  __shared__ int32_t keep_s[AIRCACHE_MAX_LAYERS];
+  __shared__ long long off_seg[kSelWarps + 1];
+  __shared__ int last_s;
   pdl_trigger();
-  if (!a.early_iv) pdl_wait();  // I_v and the keep counts
+  pdl_wait();  // I_v, and the keep counts or (budget mode) the moment records
   Req R{};
   const bool ok_req = load_req(p, b, R);
   if (!ok_req) R.vis0 = 0;
+  if (a.budget && ok_req) {
+    // (s_t, s_k) of every layer of the request: warp w merges the key-block
+    // records of layers w, w + 32, ... (the same arithmetic in every CTA of the
+    // request, so all of them derive the same budgets)
+    for (int ll = warp; ll < p.L; ll += kSelWarps) {
+      const int uu = ll * p.B + b;
+      // pass 2 wrote one record per 256 keys of a unit with stored logits,
+      // pass 2k one per 128-key tile of the others
+      const int blk = p.g * __ldcg(&w.n_tk[uu]) <= kLgRows ? 256 : 128;
+      ff s_t, s_k;
+      layer_stats_warp(w.mom + (size_t)uu * p.mom_slots * kMomWords, (R.n_v + blk - 1) / blk, lane, s_t, s_k);
+      if (lane == 0) {
+        st_s[ll] = s_t;
+        sk_s[ll] = s_k;
+      }
+    }
+  }
   const int n = ok_req ? R.n_v : 0;
   // one set per layer from I_v, or one per KV head from that KV group's I_v
   const size_t set = p.head_sets ? (size_t)l * p.h_kv + hs : (size_t)l;
@@ -140,13 +171,44 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
       if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
     }
   }
-  if (a.early_iv) pdl_wait();  // the keep counts
   if (*(volatile int32_t*)w.error != 0) return;
   if (!ok_req) {
     if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
     return;
   }
-  const int k = __ldcg(&w.keep[u]);
+  int k;
+  if (a.budget) {
+    __syncthreads();  // every layer's statistics are in shared memory
+    if (warp == 0) {
+      request_budget_warp_put(
+          p, R.n_v,
+          [&](int ll, ff& st, ff& sk) {
+            st = st_s[ll];
+            sk = sk_s[ll];
+          },
+          [&](int ll, int32_t kk) { keep_s[ll] = kk; }, lane);
+    }
+    __syncthreads();
+    k = keep_s[l];
+    if (hs == 0) {
+      // this layer's keep count and statistics; the last CTA to get here
+      // writes the compacted-cache row offsets from every keep count
+      if (tid == 0) {
+        w.keep[u] = k;
+        w.stats[2 * u] = ff_to_double(st_s[l]);
+        w.stats[2 * u + 1] = ff_to_double(sk_s[l]);
+        __threadfence();
+        last_s = atomicAdd(w.cnt_all, 1u) == (unsigned)(p.L * p.B - 1) ? 1 : 0;
+      }
+      __syncthreads();
+      if (last_s) {
+        __threadfence();
+        write_offsets<kSelThreads>(p, w.keep, w.out_offsets, w.error, a.out_capacity, off_seg, tid, 1);
+      }
+    }
+  } else {
+    k = __ldcg(&w.keep[u]);
+  }
   if (k < 0 || k > n) {
     if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
     return;
@@ -290,11 +352,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
 
 }  // namespace
 
-cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s, bool early_iv) {
+cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s, bool budget, int64_t out_capacity) {
   SelectArgs a;
   a.p = p;
   a.w = w;
-  a.early_iv = early_iv ? 1 : 0;
+  a.budget = budget ? 1 : 0;
+  a.out_capacity = out_capacity;
   a.smem_keys = p.max_visual < kSmemKeys ? p.max_visual : kSmemKeys;
   const int smem = 2 * (int)sizeof(uint32_t) * a.smem_keys;  // keys + candidates
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(select_kernel), smem);

@@ -8,30 +8,34 @@
 // probability of visual key i.  With an elite threshold near the notes'
 // alpha = 0.9 the window holds a few text tokens, so a unit has few rows and
 // many keys, and scoring is a stream over the keys.  Rows are taken in chunks
-// of 32 (one mma.sync M extent of two 16-row tiles).
+// of 32 (the N extent of one tensor-core logit tile).
 //
 // Pass 1 (score_pass1, persistent, one CTA per SM).  A work item is (unit, KV
 // head, chunk of four 128-key visual tiles) or (unit, KV head, the elite text
 // keys); it runs once per row chunk of the unit.  A producer thread claims
 // items from an atomic counter and moves each key tile into a shared-memory
 // ring with one TMA tensor copy per 128-byte column slab; the row chunk's
-// queries come with its first tile.  Eight consumer warps (16 keys each) hold
-// the chunk's queries in registers as mma.sync A fragments, compute the 32 x 128
-// logit tile (bf16 x bf16 -> fp32, base-2 logits), and keep a running (max, sum
-// of exp2) per row and thread; at the item's end the pairs are merged across
-// lanes and warps in a fixed order into one partial per (row, item).  A unit
-// with a single row chunk per KV head also writes its visual logits to a
-// row-major buffer (4 bytes per row and key: cheaper than reading the keys
-// again while rows <= 32; its keys are read once, with an L2 evict-first
-// policy).
+// queries come with its first tile.  One thread issues the logit tiles on the
+// tensor cores (tcgen05: D[key][row] = K[key] . Q[row], M = 128 keys, N = 32
+// rows, fp32 accumulators in tensor memory, four accumulator buffers), and eight
+// epilogue warps read them back one key per thread (32 rows in registers),
+// store them (below) and keep per-row sums of exp2 of the base-2 logits against
+// a per-warp reference; at the item's end the sums are reduce-scattered over
+// the lanes and the warps' pairs merged in a fixed order into one partial
+// (max, sum of exp2) per (row, item).  A unit with at most two row chunks per
+// KV head (64 rows) also writes its visual logits to a row-major buffer (4
+// bytes per row and key: cheaper than reading a 256-byte key row again; the
+// logits of the units in flight stay in L2).  The keys of a unit with a single
+// row chunk are read once, with an L2 evict-first policy.
 //
-// Pass 2 (score_pass2, one CTA per (unit, 256 keys)).  Single-chunk units:
-// each CTA merges the unit's row partials (chunk order) into row
-// log-sum-exps, then sums exp2(logit - lse) over every row of every KV head
-// for each of its keys.  Multi-chunk units: the first CTA of the unit merges
-// the row LSEs into the workspace for pass 2k.
+// Pass 2 (score_pass2, persistent).  Units with stored logits: each CTA takes a
+// contiguous range of (unit, 256 keys) items, merges a unit's row partials
+// (chunk order) into row log-sum-exps when it enters the unit, then sums
+// exp2(logit - lse) over every row of every KV head for each key.  Units
+// without stored logits (more than 64 rows per KV head): the CTAs first merge
+// their row LSEs into the workspace for pass 2k.
 //
-// Pass 2k (score_pass2k, persistent).  Multi-chunk units: a work item is (unit,
+// Pass 2k (score_pass2k, persistent).  Units without stored logits: a work item is (unit,
 // key tile); for each KV head the tile is loaded once and its B fragments stay
 // in registers while that head's row chunks (queries + LSEs) stream through a
 // small TMA ring; per-key sums of exp2(logit - lse) over every row give the
@@ -45,6 +49,7 @@
 #include "ptx.cuh"
 #include "reduce.cuh"
 #include "tmap.cuh"
+#include "umma.cuh"
 
 namespace aircache {
 namespace {
@@ -54,7 +59,11 @@ constexpr int kRC = kRowChunk;            // query rows per chunk
 constexpr int kCK = kStreamTiles;         // visual tiles per pass-1 item
 constexpr int kCW = 8;                    // consumer warps
 constexpr int kCT = kCW * 32;             // consumer threads
-constexpr int kThreads1 = kCT + 32;       // + the producer warp
+constexpr int kThreads1 = kCT + 64;       // + the producer warp and the MMA warp
+constexpr int kMmaWarp = kCW + 1;         // issues the pass-1 MMAs; allocates the TMEM
+constexpr int kNB = 4;                    // pass-1 TMEM accumulator buffers
+constexpr int kTmemStage = 2 * kRowChunk; // TMEM columns of one buffer: two 128-key tiles x 32 rows
+constexpr int kTmemCols = kNB * kTmemStage;
 constexpr int kBarC = 1;                  // named barrier of the consumer threads
 constexpr int kT2 = 256;                  // pass-2 / pass-2k threads
 constexpr int kBarT2 = 1;                 // named barrier over all kT2 threads
@@ -118,7 +127,7 @@ __device__ __forceinline__ bool stream_unit(const Dev& p, int u, const int4& i0,
 __device__ __forceinline__ int rows_per_kv(const Dev& p) { return p.rc_max * kRC; }
 
 // Slot in stream_list / stream_info of position li of the streaming units in
-// claim order (multi-chunk units first; n_multi of n_total).
+// claim order (units without stored logits first; n_multi of n_total).
 __device__ __forceinline__ int stream_slot(const Dev& p, int li, int n_multi, int n_total) {
   return li < n_multi ? li : p.L * p.B - (n_total - li);
 }
@@ -177,8 +186,11 @@ struct Hdr {
 
 struct Ctl1 {
   uint64_t full[kMaxStages], empty[kMaxStages], qempty[2];
+  uint64_t tfull[kNB], tempty[kNB];  // TMEM accumulator buffers: MMA done / read by every epilogue warp
   Hdr hdr[kMaxStages];
-  float2 red[2][kCW][kRC];
+  Hdr thdr[kNB];                     // the stage header of what TMEM buffer b holds
+  float2 red[2][2][4][kRC];          // [warpgroup][parity][warp][row] per-warp stage partials
+  uint32_t tmem;                     // TMEM base address
 };
 
 // One thread.  Items (unit, KV head, chunk of four visual tiles or the elite
@@ -246,7 +258,7 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
       const int l = u / p.B;
       for (int rc = 0; ok && rc < n_rc; ++rc, ++sub) {
         const int qb = sub & 1;
-        // the query buffer is free once every consumer warp has loaded the pass that used it before
+        // the query buffer is free once the MMAs of the pass that used it before have completed
         if (!mbar_wait(&c->qempty[qb], (uint32_t)(((sub >> 1) & 1) ^ 1))) {
           ok = false;
           break;
@@ -271,7 +283,7 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
           h.last = (j == nst - 1);
           h.chunk = ch;
           h.qbuf = qb;
-          h.store = (kind == kVis && n_rc == 1) ? 1 : 0;
+          h.store = (kind == kVis && n_rc * kRC <= kLgRows) ? 1 : 0;
           h.b = u % p.B;
           h.vis0 = i0.y;
           fence_proxy_async_smem();  // the stage (and query buffer) were last read by generic loads
@@ -320,178 +332,253 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
   mbar_arrive(&c->full[s]);
 }
 
-// Eight warps; warp w owns keys 32w .. 32w+31 of a stage (four 8-key mma N
-// tiles).  The key rows are fed to the B fragments permuted, so that thread
-// (g4 = lane/4, c4 = lane%4) holds, for query rows g4 and g4+8 of each 16-row M
-// tile, the four contiguous keys 32w + 16j + 4c4 + {0..3} in N tiles 2j and
-// 2j+1 (j = 0, 1): its logits of a row leave as two 16-byte stores.
+// One thread.  For every stage the producer filled: wait for the TMA bytes and
+// for a free TMEM buffer of the warpgroup that owns the stage's row-chunk pass
+// (passes alternate between the two epilogue warpgroups, like the query
+// buffers: warpgroup g takes the passes with query buffer g and owns TMEM
+// buffers 2g and 2g + 1), hand the stage header to that buffer, and issue the
+// logit tile(s) D[key][row] = K[key] . Q[row] (M = 128 keys per tile, N = 32
+// query rows, K = D in steps of 16) on the tensor cores.  The stage is released
+// to the producer, the query buffer after the last stage of a pass, and the
+// accumulators to the warpgroup, each when those MMAs complete.
 template <int D>
-__device__ void p1_consumers(const SArgs& a, Ctl1* c, unsigned char* sm) {
+__device__ void p1_mma(const SArgs& a, Ctl1* c, unsigned char* sm, uint32_t tmem) {
   using Gm = SGeo<D>;
   constexpr int NS = Gm::kStages;
   constexpr int KS = Gm::kKS;
-  const Dev& p = a.p;
-  const Ws& w = a.w;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g4 = lane >> 2, c4 = lane & 3;
   const uint32_t sbase = smem_u32(sm);
-  // ldmatrix lane roles: key rows as the B operand, query rows as the A operand
-  // row j of N tile t (lanes 8m..8m+7 address matrix m: t = m >> 1, k half m & 1)
-  // is key 4(j >> 1) + (j & 1) + 2t of the 16-key group
-  const int kr = 32 * warp + 4 * ((lane & 7) >> 1) + (lane & 1) + 2 * (lane >> 4);
-  const int kc = (lane >> 3) & 1;
-  const int qr = lane & 15, qc = lane >> 4;
-  const float scale = p.scale_log2;
-  const long long LS = lg_stride(p);
-  uint32_t qf[2][KS][4];
-  float m_run[2][2], s_run[2][2];
-  int mts = 1, par = 0;
+  constexpr uint32_t idesc = umma_idesc_bf16(kTK, kRC);
+  long long ng[2] = {0, 0};  // stages handed to each warpgroup
+  // the next TMEM buffer of warpgroup g, once its previous use is read
+  auto take = [&](int g, int& b) -> bool {
+    b = 2 * g + (int)(ng[g] & 1);
+    const bool ok = mbar_wait(&c->tempty[b], (uint32_t)(((ng[g] >> 1) & 1) ^ 1), 8 * kWaitCycles);
+    ++ng[g];
+    return ok;
+  };
   for (long long it = 0;; ++it) {
     const int s = (int)(it % NS);
     if (!mbar_wait(&c->full[s], (uint32_t)((it / NS) & 1), 8 * kWaitCycles)) {
-      if (lane == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+      set_error(a.w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
       return;
     }
     const Hdr h = c->hdr[s];
+    if (h.kind == kEnd) {
+      for (int g = 0; g < 2; ++g) {  // both warpgroups learn of the end
+        int b;
+        if (!take(g, b)) {
+          set_error(a.w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+          return;
+        }
+        c->thdr[b] = h;
+        mbar_arrive(&c->tfull[b]);
+        mbar_arrive(&c->tfull[b]);
+      }
+      return;
+    }
+    int b;
+    if (!take(h.qbuf, b)) {
+      set_error(a.w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    c->thdr[b] = h;
+    tc_fence_after();
+    const int ntiles = h.klim > kTK ? 2 : (h.klim > 0 ? 1 : 0);
+    const uint32_t kst = sbase + (uint32_t)(s * Gm::kSBytes);
+    const uint32_t qst = sbase + (uint32_t)(Gm::kQOff + h.qbuf * Gm::kQBytes);
+    for (int t = 0; t < ntiles; ++t) {
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        const uint32_t ka = kst + (uint32_t)((kk >> 2) * Gm::kSSlab + t * kTK * 128 + (kk & 3) * 32);
+        const uint32_t qb = qst + (uint32_t)((kk >> 2) * Gm::kQSlab + (kk & 3) * 32);
+        umma_bf16(tmem + (uint32_t)(b * kTmemStage + t * kRC), umma_desc_sw128(ka), umma_desc_sw128(qb), idesc,
+                  kk > 0 ? 1u : 0u);
+      }
+    }
+    umma_commit(&c->empty[s]);                   // the stage may be refilled once these MMAs have read it
+    if (h.last) umma_commit(&c->qempty[h.qbuf]);  // and the query buffer after the pass's last stage
+    umma_commit(&c->tfull[b]);                   // the accumulators are written
+    mbar_arrive(&c->tfull[b]);                   // the header copy is visible
+  }
+}
+
+// Reduce-scatter of 32 per-row values over the lanes of a warp (31 shuffles):
+// afterwards lane t returns the sum over all lanes of row t.  `v` is consumed.
+__device__ __forceinline__ float warp_rows_sum(float (&v)[kRC], int lane) {
+#pragma unroll
+  for (int o = kRC / 2; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < o; ++j) {
+      const float send = up ? v[j] : v[j + o];
+      const float keep = up ? v[j + o] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0];
+}
+
+// The same for (max, sum of exp2) pairs with different maxima; the lower
+// lanes' partial is always the first operand, so every lane merges in one order.
+__device__ __forceinline__ float2 warp_rows_merge(float (&m)[kRC], float (&s)[kRC], int lane) {
+#pragma unroll
+  for (int o = kRC / 2; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < o; ++j) {
+      const float2 send = up ? make_float2(m[j], s[j]) : make_float2(m[j + o], s[j + o]);
+      const float2 keep = up ? make_float2(m[j + o], s[j + o]) : make_float2(m[j], s[j]);
+      const float2 other =
+          make_float2(__shfl_xor_sync(0xffffffffu, send.x, o), __shfl_xor_sync(0xffffffffu, send.y, o));
+      const float2 r = up ? merge_ms(other, keep) : merge_ms(keep, other);
+      m[j] = r.x;
+      s[j] = r.y;
+    }
+  }
+  return make_float2(m[0], s[0]);
+}
+
+// v[lane] without dynamic register indexing: the reduce-scatter's selection
+// pattern without the exchange (31 selects, depth 5).  `v` is consumed.
+__device__ __forceinline__ float pick_lane(float (&v)[kRC], int lane) {
+#pragma unroll
+  for (int o = kRC / 2; o >= 1; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int j = 0; j < o; ++j) v[j] = up ? v[j + o] : v[j];
+  }
+  return v[0];
+}
+
+// Two warpgroups of four warps; warpgroup g takes the row-chunk passes of query
+// buffer g (every other pass), so the two work on consecutive items at once.
+// Warp w reads TMEM lane quarter w % 4 of both key tiles of a stage: thread
+// (w, lane) holds the 32 row logits of keys 32(w%4) + lane and 128 + 32(w%4) +
+// lane.  It stores them (units with stored logits: row-major logit buffer, coalesced
+// across the warp) and keeps, per row, a sum of exp2(scaled logit - m) against
+// a reference m shared by the warp: the scaled logit of the warp's first key in
+// the item.  A logit more than 2^6 above the reference (never seen on the
+// workloads here) moves that thread's reference up and rescales its sum.  At
+// the item's end the warp's sums are reduce-scattered (lane t: row t) and the
+// warpgroup's four pairs are merged in order into the item's row partial.
+template <int D>
+__device__ void p1_epilogue(const SArgs& a, Ctl1* c, uint32_t tmem) {
+  const Dev& p = a.p;
+  const Ws& w = a.w;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = warp >> 2, q = warp & 3;
+  const float scale = p.scale_log2;
+  const long long LS = lg_stride(p);
+  const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+  const int k0 = 32 * q, k1 = kTK + 32 * q;  // this warp's first key in each tile of a stage
+  float m[kRC], s[kRC];
+#pragma unroll
+  for (int r = 0; r < kRC; ++r) {
+    m[r] = 0.f;
+    s[r] = 0.f;
+  }
+  bool has_ref = false, resc = false;
+  int par = 0;
+  for (long long k = 0;; ++k) {
+    const int b = 2 * g + (int)(k & 1);
+    if (!mbar_wait(&c->tfull[b], (uint32_t)((k >> 1) & 1), 16 * kWaitCycles)) {
+      if (lane == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    __syncwarp();  // tcgen05.ld is warp-collective: the whole warp, converged
+    tc_fence_after();
+    const Hdr h = c->thdr[b];
     if (h.kind == kEnd) return;
     if (h.first) {
-      mts = h.rows > 16 ? 2 : 1;
-      const uint32_t qs = sbase + (uint32_t)(Gm::kQOff + h.qbuf * Gm::kQBytes);
-      __syncwarp();  // ldmatrix / mma are warp-collective: the whole warp, converged
+      has_ref = false;
+      resc = false;
 #pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        const int slab = kk >> 2, c0 = (kk & 3) * 2;
-        ldsm_x4(qf[0][kk], swz(qs + slab * Gm::kQSlab, qr, c0 + qc));
-        if (mts > 1) ldsm_x4(qf[1][kk], swz(qs + slab * Gm::kQSlab, 16 + qr, c0 + qc));
-      }
+      for (int r = 0; r < kRC; ++r) s[r] = 0.f;
+    }
+    const bool busy0 = k0 < h.klim, busy1 = k1 < h.klim;  // warp-uniform
+    // tile 0 first; the buffer is released after the last TMEM load of the stage
+    float v[kRC];
+    if (busy0) {
+      tmem_ld32(tl + (uint32_t)(b * kTmemStage), v);
+      tmem_wait_ld();
+    }
+    auto release = [&]() {
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&c->qempty[h.qbuf]);
+      if (lane == 0) mbar_arrive(&c->tempty[b]);  // this warp is done with the buffer
+    };
+    if (!busy1) release();
+    if (busy0) {
+      if (!has_ref) {
+        // lane 0's key exists whenever the warp is busy
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          m_run[mt][hh] = -INFINITY;
-          s_run[mt][hh] = 0.f;
-        }
-    }
-    float acc[2][4][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[mt][nt][i] = 0.f;
-    const bool busy = 32 * warp < h.klim;  // a warp whose keys are all masked skips the tile
-    if (busy) {
-      const uint32_t ks = sbase + (uint32_t)(s * Gm::kSBytes);
-      __syncwarp();  // ldmatrix / mma are warp-collective: the whole warp, converged
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        const int slab = kk >> 2, c0 = (kk & 3) * 2;
-        uint32_t b0[4], b1[4];
-        ldsm_x4(b0, swz(ks + slab * Gm::kSSlab, kr, c0 + kc));
-        ldsm_x4(b1, swz(ks + slab * Gm::kSSlab, kr + 16, c0 + kc));
-        mma_bf16_16816(acc[0][0], qf[0][kk], b0[0], b0[1]);
-        mma_bf16_16816(acc[0][1], qf[0][kk], b0[2], b0[3]);
-        mma_bf16_16816(acc[0][2], qf[0][kk], b1[0], b1[1]);
-        mma_bf16_16816(acc[0][3], qf[0][kk], b1[2], b1[3]);
-        if (mts > 1) {
-          mma_bf16_16816(acc[1][0], qf[1][kk], b0[0], b0[1]);
-          mma_bf16_16816(acc[1][1], qf[1][kk], b0[2], b0[3]);
-          mma_bf16_16816(acc[1][2], qf[1][kk], b1[0], b1[1]);
-          mma_bf16_16816(acc[1][3], qf[1][kk], b1[2], b1[3]);
-        }
+        for (int r = 0; r < kRC; ++r) m[r] = __shfl_sync(0xffffffffu, v[r], 0) * scale;
+        has_ref = true;
       }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&c->empty[s]);  // the stage is read: the producer may refill it
-
-    if (busy) {
-      // epilogue: store the raw logits (single-chunk units; the scale is applied
-      // where they are read), update the running pairs in base-2 units
-      float* lbase = nullptr;
-      if (h.store) {
-        lbase = w.lg + ((size_t)h.l * p.h_kv + h.kvh) * kRC * LS + lg_col0(h.vis0, h.b) + h.key0 +
-                32 * warp + 4 * c4;
-      }
-      const bool full = h.klim >= Gm::kSK;
+      float* dst = nullptr;
+      if (h.store)
+        dst = w.lg + (((size_t)h.l * p.h_kv + h.kvh) * kLgRows + h.r0) * LS + lg_col0(h.vis0, h.b) + h.key0;
+#pragma unroll 1
+      for (int t = 0; t < 2; ++t) {
+        if (t == 1) {
+          if (!busy1) break;
+          __syncwarp();
+          tmem_ld32(tl + (uint32_t)(b * kTmemStage + kRC), v);
+          tmem_wait_ld();
+          release();
+        }
+        const int key = (t ? k1 : k0) + lane;
+        if (key < h.klim) {
+          // blocks of 8 rows: the block's exponents are computed first and
+          // checked against the reference once, so the block's exponentials
+          // and sums carry no branch between them
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        if (mt < mts) {
+          for (int g8 = 0; g8 < kRC / 8; ++g8) {
+            if (8 * g8 < h.rows) {
+              float d[8];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int row = 16 * mt + g4 + 8 * hh;
-            if (row < h.rows) {
-              float v[8];
-              float mx = -INFINITY;
-              float* dst = lbase ? lbase + (size_t)row * LS : nullptr;
+              for (int j = 0; j < 8; ++j) d[j] = fmaf(v[8 * g8 + j], scale, -m[8 * g8 + j]);
+              const float dmax = fmaxf(fmaxf(fmaxf(d[0], d[1]), fmaxf(d[2], d[3])),
+                                       fmaxf(fmaxf(d[4], d[5]), fmaxf(d[6], d[7])));
+              if (dst) {
 #pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                // keys 32w + 16j + 4c4 + {0..3}: N tiles 2j, 2j+1
-                const int key = 32 * warp + 16 * j + 4 * c4;
-                const float4 x = make_float4(acc[mt][2 * j][2 * hh], acc[mt][2 * j][2 * hh + 1],
-                                             acc[mt][2 * j + 1][2 * hh], acc[mt][2 * j + 1][2 * hh + 1]);
-                if (full) {
-                  v[4 * j] = x.x;
-                  v[4 * j + 1] = x.y;
-                  v[4 * j + 2] = x.z;
-                  v[4 * j + 3] = x.w;
-                  if (dst) *reinterpret_cast<float4*>(dst + 16 * j) = x;
-                } else {
-                  v[4 * j] = key < h.klim ? x.x : -INFINITY;
-                  v[4 * j + 1] = key + 1 < h.klim ? x.y : -INFINITY;
-                  v[4 * j + 2] = key + 2 < h.klim ? x.z : -INFINITY;
-                  v[4 * j + 3] = key + 3 < h.klim ? x.w : -INFINITY;
-                  if (dst) {
-                    if (key + 3 < h.klim) {
-                      *reinterpret_cast<float4*>(dst + 16 * j) = x;
-                    } else {
-                      if (key < h.klim) dst[16 * j] = x.x;
-                      if (key + 1 < h.klim) dst[16 * j + 1] = x.y;
-                      if (key + 2 < h.klim) dst[16 * j + 2] = x.z;
-                    }
+                for (int j = 0; j < 8; ++j)
+                  if (8 * g8 + j < h.rows) dst[(size_t)(8 * g8 + j) * LS + key] = v[8 * g8 + j];
+              }
+              if (dmax > 64.f) {  // a logit far above the reference: move it (rare)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  if (d[j] > 64.f) {
+                    s[8 * g8 + j] *= fast_exp2(-d[j]);
+                    m[8 * g8 + j] = v[8 * g8 + j] * scale;
+                    d[j] = 0.f;
                   }
                 }
-                mx = fmaxf(mx, fmaxf(fmaxf(v[4 * j], v[4 * j + 1]), fmaxf(v[4 * j + 2], v[4 * j + 3])));
+                resc = true;
               }
-              // running (max, sum of exp2) of the scaled logits: rescale only when the maximum grows
-              if (mx != -INFINITY) {
-                const float ms = mx * scale;
-                if (ms > m_run[mt][hh]) {
-                  s_run[mt][hh] *= fast_exp2(m_run[mt][hh] - ms);
-                  m_run[mt][hh] = ms;
-                }
-                const float neg = -m_run[mt][hh];
-                float sum = 0.f;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) sum += fast_exp2(fmaf(v[q], scale, neg));
-                s_run[mt][hh] += sum;
-              }
+              for (int j = 0; j < 8; ++j) s[8 * g8 + j] += fast_exp2(d[j]);
             }
           }
         }
       }
     }
     if (h.last) {
-      // merge the item's running pairs: the four lanes of a row, then the warps in order
+      float2 pr;
+      if (!has_ref) {
+        pr = make_float2(-INFINITY, 0.f);
+      } else if (!__any_sync(0xffffffffu, resc)) {
+        const float S = warp_rows_sum(s, lane);
+        pr = make_float2(pick_lane(m, lane), S);
+      } else {
+        pr = warp_rows_merge(m, s, lane);
+      }
+      c->red[g][par][q][lane] = pr;
+      named_bar_sync(kBarC + g, 4 * 32);
+      if (q == 0 && lane < h.rows) {
+        float2 ms = c->red[g][par][0][lane];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          float2 ms = make_float2(m_run[mt][hh], s_run[mt][hh]);
-#pragma unroll
-          for (int o = 1; o <= 2; o <<= 1) {
-            const float2 other =
-                make_float2(__shfl_xor_sync(0xffffffffu, ms.x, o), __shfl_xor_sync(0xffffffffu, ms.y, o));
-            ms = merge_ms(ms, other);
-          }
-          if (c4 == 0) c->red[par][warp][16 * mt + g4 + 8 * hh] = ms;
-        }
-      named_bar_sync(kBarC, kCT);
-      if (warp == 0 && lane < h.rows) {
-        float2 ms = c->red[par][0][lane];
-#pragma unroll
-        for (int ww = 1; ww < kCW; ++ww) ms = merge_ms(ms, c->red[par][ww][lane]);
+        for (int ww = 1; ww < 4; ++ww) ms = merge_ms(ms, c->red[g][par][ww][lane]);
         w.part_s[part_index(p, h.u, h.kvh, h.r0 + lane, h.chunk)] = ms;
       }
       par ^= 1;
@@ -506,23 +593,46 @@ __global__ void __launch_bounds__(kThreads1, 1) stream_p1_kernel(const __grid_co
   // tiles need 1024-byte alignment (the 128-byte swizzle repeats every 8 rows)
   unsigned char* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   Ctl1* c = reinterpret_cast<Ctl1*>(sm + Gm::kCtlOff);
+  const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int s = 0; s < Gm::kStages; ++s) {
       mbar_init(&c->full[s], 1);
-      mbar_init(&c->empty[s], kCW);
+      mbar_init(&c->empty[s], 1);
     }
-    mbar_init(&c->qempty[0], kCW);
-    mbar_init(&c->qempty[1], kCW);
+    for (int b = 0; b < kNB; ++b) {
+      mbar_init(&c->tfull[b], 2);  // the MMA completion and the header hand-off
+      mbar_init(&c->tempty[b], 4);  // the four warps of the warpgroup that reads it
+    }
+    mbar_init(&c->qempty[0], 1);
+    mbar_init(&c->qempty[1], 1);
     fence_mbar_init();
   }
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tmem_alloc(&c->tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c->tmem;
   pdl_trigger();
   pdl_wait();  // the elite kernel's lists, query rows and elite keys
-  if (*(volatile int32_t*)a.w.error != 0) return;  // an earlier kernel reported an error
-  if (threadIdx.x < kCT) {
-    p1_consumers<D>(a, c, sm);
-  } else if (threadIdx.x == kCT) {
-    p1_producer<D>(a, c, sm);
+  if (*(volatile int32_t*)a.w.error == 0) {  // else an earlier kernel reported an error
+    if (threadIdx.x < kCT) {
+      p1_epilogue<D>(a, c, tmem);
+    } else if (threadIdx.x == kCT) {
+      p1_producer<D>(a, c, sm);
+    } else if (threadIdx.x == kCT + 32) {
+      p1_mma<D>(a, c, sm, tmem);
+    }
+  }
+  __syncwarp();  // the role threads rejoin their warps
+  tc_fence_before();
+  __syncthreads();  // every TMEM read and every MMA of this CTA is done
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -543,7 +653,7 @@ constexpr int kP2CtlOff = kP2Stages * kP2Slice;
 // block kb), or the end of the CTA's walk (state 1), or a unit record that
 // failed validation (state 2).
 struct P2Rec {
-  int state, u, l, b, kb, n_v, n_tk, rows, kvh;
+  int state, u, l, b, kb, n_v, n_tk, rows, kvh, rc;
   long long vis0;
 };
 
@@ -560,32 +670,39 @@ struct Ctl2p {
   float hx[2][kKeysP2];
 };
 
-// The unit record (seq0, vis0, txt0, n_v), (n_t, n_tk, 1, u) of single unit
-// si, loaded once per unit.
-// The walk of a CTA's items: item index, its (single unit si, key block kb),
-// and the record (seq0, vis0, txt0, n_v), (n_t, n_tk, 1, u) of unit si, loaded
-// once per unit.
+// The walk of a CTA's items over the pass-2 units (unit si in slot L*B - 1 - si,
+// in routing order) and their 256-key blocks kb.  Item (si, kb) starts at
+// weight wpre(si) + kb * nrc (nrc = 32-row chunks per KV head); the CTA takes
+// the items that start in its share [lo, hi) of the total weight.  The unit's
+// layout record (seq0, vis0, txt0, n_v), (n_t, n_tk, 1, u) and weight prefix
+// are loaded once per unit.
 struct P2Cursor {
-  long long item, end;
-  int si, kb, KB, slot0;
+  int si, kb, n;
+  unsigned long long hi;
   int loaded = -1;
   int4 r0, r1;
+  unsigned long long wpre;
+  int nrc, nkb;
 };
 
-// Advance the cursor to the first item at or after its position whose key
-// block lies inside its unit; items run over (si, kb), si-major, KB blocks per
-// unit.  Returns 0 past the end, 1 with the item in `r` (the cursor stays on
-// it), 2 for a unit record that fails validation.
+// Move the cursor to the first item at or after it (the cursor stays on it).
+// Returns 0 past the CTA's share, 1 with the item in `r`, 2 for a unit record
+// that fails validation.
 __device__ __forceinline__ int p2_item(const Dev& p, const Ws& w, P2Cursor& cu, P2Rec& r) {
-  for (; cu.item < cu.end; ++cu.item) {
+  while (cu.si < cu.n) {
     if (cu.si != cu.loaded) {
       cu.loaded = cu.si;
-      cu.r0 = __ldcg(&w.stream_info[2 * (cu.slot0 + cu.si)]);
-      cu.r1 = __ldcg(&w.stream_info[2 * (cu.slot0 + cu.si) + 1]);
+      const int slot = p.L * p.B - 1 - cu.si;
+      cu.r0 = __ldcg(&w.stream_info[2 * slot]);
+      cu.r1 = __ldcg(&w.stream_info[2 * slot + 1]);
+      cu.wpre = __ldcg(&w.p2wpre[slot]);
+      if (!stream_unit(p, cu.r1.w, cu.r0, cu.r1) || p.g * cu.r1.y > kLgRows) return 2;
+      cu.nrc = (p.g * cu.r1.y + kRC - 1) / kRC;
+      cu.nkb = (cu.r0.w + kKeysP2 - 1) / kKeysP2;
     }
-    const int4 r0 = cu.r0, r1 = cu.r1;
-    if (!stream_unit(p, r1.w, r0, r1) || p.g * r1.y > kRC) return 2;
-    if (cu.kb * kKeysP2 < r0.w) {
+    if (cu.wpre + (unsigned long long)cu.kb * cu.nrc >= cu.hi) return 0;
+    if (cu.kb < cu.nkb) {
+      const int4 r0 = cu.r0, r1 = cu.r1;
       r.state = 0;
       r.u = r1.w;
       r.l = r1.w / p.B;
@@ -595,43 +712,53 @@ __device__ __forceinline__ int p2_item(const Dev& p, const Ws& w, P2Cursor& cu, 
       r.n_tk = r1.y;
       r.rows = p.g * r1.y;
       r.kvh = 0;
+      r.rc = 0;
       r.vis0 = r0.y;
       return 1;
     }
-    if (++cu.kb == cu.KB) {
-      cu.kb = 0;
-      ++cu.si;
-    }
+    ++cu.si;
+    cu.kb = 0;
   }
   return 0;
 }
 
 // Step past the current item.
-__device__ __forceinline__ void p2_next(P2Cursor& cu) {
-  ++cu.item;
-  if (++cu.kb == cu.KB) {
-    cu.kb = 0;
-    ++cu.si;
+__device__ __forceinline__ void p2_next(P2Cursor& cu) { ++cu.kb; }
+
+// The pass-2 unit that holds weight position `lo` (the largest si with
+// wpre(si) <= lo), by the 32 lanes of a warp: each round probes 32 evenly
+// spaced units and keeps the span after the last one at or below `lo`.
+__device__ __forceinline__ int p2_find(const Dev& p, const Ws& w, int n, unsigned long long lo, int lane) {
+  int a = 0, b = n;  // answer in [a, b); wpre(a) <= lo
+  while (b - a > 1) {
+    const int step = (b - a + 31) / 32;
+    const int k = a + lane * step;
+    const bool le = k < b && (unsigned long long)__ldcg(&w.p2wpre[p.L * p.B - 1 - k]) <= lo;
+    const unsigned bal = __ballot_sync(0xffffffffu, le);
+    const int last = 31 - __clz((int)bal);  // lane 0 always qualifies
+    a += last * step;
+    b = min(b, a + step);
   }
+  return a;
 }
 
-// Pass 2 for one-chunk units (g * N_tk <= 32), persistent: CTA c takes a
-// contiguous range of the (unit, 256-key block) items.  A producer warp walks
-// the range and loads, for each item and KV head, that head's logits (rows <
-// 32, 256 keys) by TMA into a ring of 32 KB shared-memory stages, with a record
-// of what the stage holds.  Streaming thread t owns key k0 + t and sums
+// Pass 2 for units with stored logits (g * N_tk <= 64), persistent: CTA c takes
+// a contiguous range of the (unit, 256-key block) items.  A producer warp walks
+// the range and loads, for each item, KV head and 32-row chunk, those logits
+// (256 keys) by TMA into a ring of 32 KB shared-memory stages, with a record of
+// what the stage holds.  Streaming thread t owns key k0 + t and sums
 // exp2(logit - lse) over the rows of every KV head, writes I_v and hands the
 // item's values to the moment warps (double-buffered), which reduce them to the
 // item's moment record while the streamers go on.  The row LSEs of a unit are
 // merged from pass 1's partials (quads of lanes) when the walk enters the unit.
-// Multi-chunk units: every thread first helps publish their row LSEs for pass
-// 2k.
+// Units without stored logits: every thread first helps publish their row LSEs
+// for pass 2k.
 
 // Shared state of a pass-2 CTA.
 struct P2Smem {
   unsigned char* sm;  // stage area
   Ctl2p* c;           // ring and the moment hand-off
-  float* lse_s;       // [h_kv][32] row LSEs of the current unit
+  float* lse_s;       // [h_kv][kLgRows] row LSEs of the current unit
   ff* red;
   float* redf;
 };
@@ -674,27 +801,34 @@ __device__ __forceinline__ void p2_moments(const Dev& p, const Ws& w, const P2Sm
   }
 }
 
-// One-chunk role: the producer warp (warp kP2Prod, lane 0) and the 256
-// streamers over items [i_beg, i_end) of the one-chunk units.
-__device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, long long i_beg, long long i_end, int KB,
-                                          int slot0) {
+// Stored-logit role: the producer warp (warp kP2Prod) and the 256 streamers
+// over the items of the units with stored logits that start in weight [lo, hi).
+__device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, unsigned long long lo,
+                                          unsigned long long hi, int n) {
   const Dev& p = a.p;
   const Ws& w = a.w;
   Ctl2p* c = S.c;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float* slices = reinterpret_cast<const float*>(S.sm);  // [kP2Stages][32][256]
   if (warp == kP2Prod) {
-    // producer: one thread fills the ring, then sends the end record
+    // producer: the warp finds the first unit of the share, then one thread
+    // fills the ring and sends the end record
+    const int si0 = lo < hi ? p2_find(p, w, n, lo, lane) : n;
     if (lane != 0) return;
     fence_proxy_async_global();  // the logits were written by the previous kernel's generic stores
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&a.lgmap)) : "memory");
     P2Cursor cu;
-    cu.item = i_beg;
-    cu.end = i_end;
-    cu.KB = KB;
-    cu.slot0 = slot0;
-    cu.si = (int)(i_beg / KB);
-    cu.kb = (int)(i_beg % KB);
+    cu.si = si0;
+    cu.n = n;
+    cu.hi = hi;
+    cu.kb = 0;
+    if (si0 < n) {
+      // the first block of unit si0 that starts at or after lo
+      const int slot = p.L * p.B - 1 - si0;
+      const unsigned long long wp = __ldcg(&w.p2wpre[slot]);
+      const int nrc = (p.g * __ldcg(&w.stream_info[2 * slot + 1]).y + kRC - 1) / kRC;
+      if (nrc > 0 && lo > wp) cu.kb = (int)((lo - wp + nrc - 1) / nrc);
+    }
     P2Rec pr = {};
     int pstate = p2_item(p, w, cu, pr);
     for (long long st = 0;; ++st) {
@@ -709,18 +843,23 @@ __device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, long 
         return;
       }
       c->rec[slot] = pr;
-      const int nb = (pr.rows + kP2Box - 1) / kP2Box;
+      const int rows_c = min(kRC, pr.rows - pr.rc * kRC);
+      const int nb = (rows_c + kP2Box - 1) / kP2Box;
       fence_proxy_async_smem();  // the slot was last read by generic loads
       mbar_arrive_expect_tx(&c->full[slot], (uint32_t)(nb * kP2Box * kKeysP2 * 4));
       const int x = (int)(lg_col0(pr.vis0, pr.b) + (long long)pr.kb * kKeysP2);
-      const int y = (pr.l * p.h_kv + pr.kvh) * kRC;
+      const int y = (pr.l * p.h_kv + pr.kvh) * kLgRows + pr.rc * kRC;
       for (int j = 0; j < nb; ++j) {
         tma_load_2d(smem_u32(S.sm + slot * kP2Slice + j * kP2Box * kKeysP2 * 4), &a.lgmap, x, y + j * kP2Box,
                     &c->full[slot]);
       }
-      if (++pr.kvh == p.h_kv) {
-        p2_next(cu);
-        pstate = p2_item(p, w, cu, pr);
+      // stages run over (KV head, row chunk), head-major
+      if (++pr.rc * kRC >= pr.rows) {
+        pr.rc = 0;
+        if (++pr.kvh == p.h_kv) {
+          p2_next(cu);
+          pstate = p2_item(p, w, cu, pr);
+        }
       }
     }
   }
@@ -728,7 +867,7 @@ __device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, long 
   // streamers
   const float scale = p.scale_log2;  // stored logits are raw q.k
   int cur_u = -1, n_hand = 0;
-  float acc = 0.f;
+  float acc = 0.f, acc_h = 0.f;
   for (long long stage = 0;; ++stage) {
     const int slot = (int)(stage % kP2Stages);
     if (!mbar_wait(&c->full[slot], (uint32_t)((stage / kP2Stages) & 1), 4 * kWaitCycles)) {
@@ -740,7 +879,7 @@ __device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, long 
       if (it.state == 2 && tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
       break;
     }
-    if (it.kvh == 0) {
+    if (it.kvh == 0 && it.rc == 0) {
       if (it.u != cur_u) {
         // the unit's row LSEs, four lanes per row (whole quads iterate together)
         named_bar_sync(kBarP2S, kT2);  // every streamer is done with the previous unit's LSEs
@@ -750,7 +889,7 @@ __device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, long 
           const int qq = min(q4, nr - 1);
           const int kvh = qq / it.rows, r = qq % it.rows;
           const float lse = row_lse4(p, w, it.u, kvh, r, chv, tid & 3);
-          if (q4 < nr && (tid & 3) == 0) S.lse_s[kvh * kRC + r] = lse;
+          if (q4 < nr && (tid & 3) == 0) S.lse_s[kvh * kLgRows + r] = lse;
         }
         named_bar_sync(kBarP2S, kT2);
         cur_u = it.u;
@@ -758,17 +897,19 @@ __device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, long 
       acc = 0.f;
     }
     const float* x = slices + (size_t)slot * (kRC * kKeysP2) + tid;
-    const float* ls = S.lse_s + it.kvh * kRC;
-    float acc_h = 0.f;  // this KV head's rows
+    const float* ls = S.lse_s + it.kvh * kLgRows + it.rc * kRC;
+    const int rows_c = min(kRC, it.rows - it.rc * kRC);
+    if (it.rc == 0) acc_h = 0.f;  // this KV head's rows
     int r = 0;
-    for (; r + 8 <= it.rows; r += 8) {
+    for (; r + 8 <= rows_c; r += 8) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc_h += fast_exp2(fmaf(x[(r + q) * kKeysP2], scale, -ls[r + q]));
     }
-    for (; r < it.rows; ++r) acc_h += fast_exp2(fmaf(x[r * kKeysP2], scale, -ls[r]));
-    acc += acc_h;
+    for (; r < rows_c; ++r) acc_h += fast_exp2(fmaf(x[r * kKeysP2], scale, -ls[r]));
     __syncwarp();
     if (lane == 0) mbar_arrive(&c->empty[slot]);  // this warp is done with the slot and its record
+    if ((it.rc + 1) * kRC < it.rows) continue;  // the head's next row chunk follows
+    acc += acc_h;
     if (p.head_sets) {
       // the KV group's own I_v: its g query heads and the elite rows
       const int key = it.kb * kKeysP2 + tid;
@@ -829,11 +970,15 @@ __global__ void __launch_bounds__(kT2p, 1) stream_p2_kernel(const __grid_constan
   if (*(volatile int32_t*)w.error != 0) return;
   const int n_total = __ldcg(&w.list_n[0]), n_multi = __ldcg(&w.list_n[2]);
   const int LB = p.L * p.B;
-  if (n_total < 0 || n_total > LB || n_multi < 0 || n_multi > n_total) {
+  // units with stored logits, partitioned by weight (blocks x row chunks)
+  const unsigned long long pack = __ldcg(w.p2pack);
+  const int n_single = (int)(pack >> 32);
+  const unsigned long long W = pack & 0xffffffffULL;
+  if (n_total < 0 || n_total > LB || n_multi < 0 || n_multi > n_total || n_single != n_total - n_multi) {
     if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
     return;
   }
-  // multi-chunk units: row LSEs for pass 2k
+  // units without stored logits: row LSEs for pass 2k
   for (int m = blockIdx.x; m < n_multi; m += gridDim.x) {
     const int u = __ldcg(&w.stream_list[m]);
     const int4 i0 = (u >= 0 && u < LB) ? __ldcg(&w.uinfo[2 * u]) : make_int4(0, 0, 0, 0);
@@ -854,11 +999,8 @@ __global__ void __launch_bounds__(kT2p, 1) stream_p2_kernel(const __grid_constan
     p2_moments(p, w, S, tid - kT2 - 32);
     return;
   }
-  const int n_single = n_total - n_multi;
-  const int KB = (p.max_visual + kKeysP2 - 1) / kKeysP2;
-  const long long N_s = (long long)n_single * KB;
-  const long long i_beg = N_s * blockIdx.x / gridDim.x, i_end = N_s * (blockIdx.x + 1) / gridDim.x;
-  p2_single(a, S, i_beg, i_end, KB, LB - n_single);
+  const unsigned long long lo = W * blockIdx.x / gridDim.x, hi = W * (blockIdx.x + 1) / gridDim.x;
+  p2_single(a, S, lo, hi, n_single);
 }
 
 // ------------------------------------------------------------------ pass 2k
@@ -867,7 +1009,7 @@ struct Ctl2 {
   uint64_t kfull, qfull[kNQ];
 };
 
-// Multi-chunk units.  Item = (unit, key tile): for each KV head in turn the
+// Units without stored logits.  Item = (unit, key tile): for each KV head in turn the
 // key tile's B fragments are loaded into registers (the buffer is refilled
 // with the next head's tile at once), and the head's row chunks stream through
 // a ring of query chunks with their LSEs.  Each thread sums exp2(logit - lse)
@@ -909,7 +1051,7 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
   if (tid == 0) fence_proxy_async_global();  // LSEs were written by the previous kernel's generic stores
   for (long long item = blockIdx.x; item < total; item += gridDim.x) {
     const int li = (int)(item / TVmax), tile = (int)(item % TVmax);
-    const int u = __ldcg(&w.stream_list[li]);  // slots [0, list_n[2]): the multi-chunk units
+    const int u = __ldcg(&w.stream_list[li]);  // slots [0, list_n[2]): the units without stored logits
     const int4 i0 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u]) : make_int4(0, 0, 0, 0);
     const int4 i1 = (u >= 0 && u < p.L * p.B) ? __ldcg(&w.uinfo[2 * u + 1]) : make_int4(0, 0, 0, 0);
     if (!stream_unit(p, u, i0, i1)) {
@@ -1097,7 +1239,7 @@ cudaError_t launch_p2k_t(const Dev& p, const StreamMaps& m, const Ws& w, int sms
 
 bool stream_eligible(const Dev& p, const LayerPtrs& lp) {
   if (p.dtype != AIRCACHE_BF16 || (p.d != 64 && p.d != 128)) return false;
-  if ((p.max_visual + kKeysP2 - 1) / kKeysP2 > 65535 || p.h_kv * kRC * (int)sizeof(float) > 16 * 1024) return false;
+  if ((p.max_visual + kKeysP2 - 1) / kKeysP2 > 65535 || p.h_kv * kLgRows * (int)sizeof(float) > 16 * 1024) return false;
   const long long U = (long long)p.L * p.B;
   if (U * p.rows_max + kRC > INT32_MAX || U * p.h_kv * p.max_elite + kTK > INT32_MAX) {
     return false;  // TMA row coordinates are 32-bit
@@ -1112,7 +1254,7 @@ bool encode_stream_maps(const Dev& p, const LayerPtrs& lp, const Ws& w, StreamMa
          encode_keys<__nv_bfloat16>(&m->kmap2, p, lp, 2 * kTK) &&
          encode_rows<__nv_bfloat16>(&m->qmap, w.qel, p.d, U * p.rows_max, kRC) &&
          encode_rows<__nv_bfloat16>(&m->kelmap, w.kel, p.d, U * p.h_kv * p.max_elite, kTK) &&
-         encode_logits(&m->lgmap, w.lg, (p.total_visual + 4LL * p.B + 7) / 4 * 4, (long long)p.L * p.h_kv * kRC,
+         encode_logits(&m->lgmap, w.lg, (p.total_visual + 4LL * p.B + 7) / 4 * 4, (long long)p.L * p.h_kv * kLgRows,
                        kKeysP2, kP2Box);
 }
 
@@ -1126,7 +1268,7 @@ cudaError_t launch_stream_p2(const Dev& p, const StreamMaps& m, const Ws& w, int
   a.lgmap = m.lgmap;
   a.p = p;
   a.w = w;
-  const int smem = kP2CtlOff + (int)sizeof(Ctl2p) + (int)sizeof(float) * p.h_kv * kRC + 128;
+  const int smem = kP2CtlOff + (int)sizeof(Ctl2p) + (int)sizeof(float) * p.h_kv * kLgRows + 128;
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(stream_p2_kernel), smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(stream_p2_kernel, dim3(sms), dim3(kT2p), smem, s, a);

@@ -1,0 +1,117 @@
+// Fifth-generation tensor-core building blocks for sm_103a (inline PTX):
+// tensor-memory (TMEM) allocation, shared-memory matrix descriptors, the
+// instruction descriptor of a bf16 x bf16 -> fp32 MMA, the single-thread MMA
+// issue, its completion signal on an mbarrier, and TMEM -> register loads.
+//
+// Conventions used by this library: both operands are K-major tiles that a TMA
+// copy with the 128-byte swizzle placed in shared memory as 128-byte column
+// slabs (slab j holds elements 64j .. 64j+63 of every row, rows 128 bytes
+// apart, 8-row groups 1024 bytes apart).  One MMA consumes K = 16 elements
+// (32 bytes of every row); the k-th step of a slab starts 32k bytes into it.
+// The accumulator of an M = 128 MMA occupies TMEM lanes 0..127 (lane = row of
+// A) and N consecutive 32-bit columns (column = row of B).
+#pragma once
+
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace aircache {
+
+// Shared-memory matrix descriptor of a K-major operand with the 128-byte
+// swizzle: start address, stride between 8-row groups (1024 bytes), the
+// descriptor version of this architecture (bit 46) and the swizzle mode (2).
+// The leading-dimension offset is not used by swizzled K-major operands.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);         // bits 0-13: start address >> 4
+  d |= (uint64_t)1 << 16;                               // bits 16-29: leading byte offset (unused) = 16 B
+  d |= (uint64_t)(1024u >> 4) << 32;                    // bits 32-45: stride byte offset >> 4
+  d |= (uint64_t)1 << 46;                               // bits 46-47: descriptor version
+  d |= (uint64_t)2 << 61;                               // bits 61-63: 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulation,
+// both operands K-major, shape M x N (M in {64, 128}; N a multiple of 8 for
+// M = 64, of 16 for M = 128, up to 256).
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+  return (1u << 4)                       // D format: f32
+         | (1u << 7)                     // A format: bf16
+         | (1u << 10)                    // B format: bf16
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.  accumulate = 0
+// overwrites D.
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every MMA this thread issued before has completed
+// (its shared-memory operands are read and its accumulator is written).
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// Order tensor-core operations across a thread synchronisation (an mbarrier
+// wait or arrive, a named barrier): `before` ahead of the signal, `after`
+// behind the wait.
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// TMEM allocation by one whole warp: `ncols` (a power of two, 32..512) columns;
+// the base address is written to `slot` in shared memory.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(base), "r"(ncols) : "memory");
+}
+
+// 32 consecutive 32-bit columns of this warp's 32 TMEM lanes: thread t gets
+// lane (addr.lane + t), columns addr.col .. addr.col + 31.  The warp may only
+// address the lanes of its quarter (32 * (warp % 4) .. +31).  Complete after
+// tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float v[32]) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// The same for 16 columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+  uint32_t* r = reinterpret_cast<uint32_t*>(v);
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+
+}  // namespace aircache
