@@ -62,6 +62,7 @@ extern "C" {
 #endif
 
 #define AIRCACHE_MAX_LAYERS 256
+#define AIRCACHE_VARIANT_WAIT_TEST (1 << 24)
 #define AIRCACHE_MAX_TEXT 8192
 #define AIRCACHE_NOALLOC_MAX_UNITS 2048  /* L * B limit of aircache_budget_noalloc */
 
@@ -111,6 +112,13 @@ typedef struct aircache_problem {
                             * the layer's; aircache_compress on the streaming path only
                             * -- else AIRCACHE_ERR_UNSUPPORTED, as from the staged
                             * calls -- and idx is then [L][h_kv][total_visual]);
+                            * bit 24 (AIRCACHE_VARIANT_WAIT_TEST) a test hook for the
+                            * device's bounded waits, not a variant of the method:
+                            * the call's first kernel waits on a workspace flag that
+                            * nothing sets, gives up after about 2^20 SM cycles, and
+                            * records AIRCACHE_ERR_DEVICE_TIMEOUT; every later kernel
+                            * of the call then returns without work.  The workspace
+                            * stays usable (the next call clears the error word);
                             * other bits 0. */
     int64_t total_tokens;  /* == cu_seqlens[B] */
     int64_t total_visual;  /* == cu_visual[B] */

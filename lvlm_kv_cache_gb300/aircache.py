@@ -32,6 +32,8 @@ ERR_CAPACITY = -8
 
 F32, BF16, INT8 = 0, 1, 2
 MAX_LAYERS = 256
+# test hook of the variant word: the first kernel's bounded wait runs out (see aircache.h)
+VARIANT_WAIT_TEST = 1 << 24
 
 
 class AirCacheError(RuntimeError):
@@ -186,7 +188,7 @@ class Problem:
 
     def __init__(self, q, k, v, cu_seqlens, cu_visual, max_visual, max_text, alpha=0.9, r=0.1,
                  max_elite=0, total_tokens=None, total_visual=None, window_mode=0, budget_mode=0,
-                 n_prefix=None, head_sets=False, q_visual=None):
+                 n_prefix=None, head_sets=False, q_visual=None, wait_test=False):
         qs = list(q.unbind(0)) if torch.is_tensor(q) else list(q)
         ks = list(k.unbind(0)) if torch.is_tensor(k) else list(k)
         vs = list(v.unbind(0)) if torch.is_tensor(v) else list(v)
@@ -216,7 +218,8 @@ class Problem:
             num_layers=L, num_requests=B, h_q=self.h_q, h_kv=self.h_kv, head_dim=self.d,
             dtype=BF16 if dt == torch.bfloat16 else F32,
             max_visual=int(max_visual), max_text=int(max_text), max_elite=int(max_elite),
-            variant=int(window_mode) | (int(budget_mode) << 8) | ((1 << 16) if head_sets else 0),
+            variant=int(window_mode) | (int(budget_mode) << 8) | ((1 << 16) if head_sets else 0)
+            | (VARIANT_WAIT_TEST if wait_test else 0),
             total_tokens=T, total_visual=TV,
             cu_seqlens=cu_seqlens.data_ptr(), cu_visual=cu_visual.data_ptr(),
             q_text=ctypes.cast(self._q, ctypes.POINTER(ctypes.c_void_p)),

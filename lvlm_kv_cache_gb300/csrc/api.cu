@@ -62,7 +62,8 @@ int validate(const aircache_problem* p) {
   if (p->max_visual < 3 || p->max_text < 1) return AIRCACHE_ERR_INVALID_ARG;
   if (p->max_text > AIRCACHE_MAX_TEXT) return AIRCACHE_ERR_UNSUPPORTED;
   if (p->max_elite < 0 || p->max_elite > p->max_text) return AIRCACHE_ERR_INVALID_ARG;
-  if ((p->variant & ~0xffffff) != 0 || (p->variant & 0xff) > 4 || ((p->variant >> 8) & 0xff) > 4 ||
+  if ((p->variant & ~(0xffffff | AIRCACHE_VARIANT_WAIT_TEST)) != 0 || (p->variant & 0xff) > 4 ||
+      ((p->variant >> 8) & 0xff) > 4 ||
       ((p->variant >> 16) & 0xff) > 1) {
     return AIRCACHE_ERR_INVALID_ARG;
   }
@@ -132,6 +133,7 @@ Dev make_dev(const aircache_problem* p) {
   d.window_mode = p->variant & 0xff;
   d.budget_mode = (p->variant >> 8) & 0xff;
   d.head_sets = (p->variant >> 16) & 0xff;
+  d.wait_test = (p->variant & AIRCACHE_VARIANT_WAIT_TEST) ? 1 : 0;
   d.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->head_dim));
   const int tv = (d.max_visual + 127) / 128;
   d.chn = (tv + kStreamTiles - 1) / kStreamTiles + 1;

@@ -81,6 +81,15 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g4 = lane >> 2, c4 = lane & 3;
 
+  if (p.wait_test) {
+    // test hook: a bounded wait on a flag of the zeroed workspace block that no
+    // kernel of this call sets (the wide path's LSE-ready flag of unit 0; this
+    // call does no scoring), so it runs out and reports a timeout; the kernels
+    // after this one see the error and return
+    if (rank == 0 && b == 0 && l == 0 && threadIdx.x == 0 && !wait_flag(a.w.lse_ready, 1LL << 20))
+      set_error(a.w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+    return;
+  }
   Req R;
   if (!load_req(p, b, R)) {  // the same verdict in every CTA of the cluster
     if (rank == 0 && tid == 0) set_error(a.w.error, AIRCACHE_ERR_DEVICE_BOUNDS);

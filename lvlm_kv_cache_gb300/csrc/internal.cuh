@@ -33,6 +33,7 @@ struct Dev {
   int budget_mode;       // 0 strength + skewness; 1 uniform; 2 PyramidKV-style; 3 strength; 4 skewness
   int head_sets;         // 1: one visual index set per KV head (I_v of each KV group)
   int chn;               // streaming pass-1 chunks per (unit, KV head): visual chunks + 1 text chunk
+  int wait_test;         // 1: the first kernel's bounded wait on a flag nothing sets (a test hook)
 };
 
 // Streaming scoring path: query rows are taken in chunks of this many (a unit

@@ -123,12 +123,12 @@ __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
 }
 
-// Spin until *flag != 0; false if kWaitCycles elapse first.
-__device__ __forceinline__ bool wait_flag(const uint32_t* flag) {
+// Spin until *flag != 0; false if `limit` cycles elapse first.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, long long limit = kWaitCycles) {
   if (ld_acquire(flag) != 0) return true;
   const long long t0 = clock64();
   while (ld_acquire(flag) == 0) {
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
     __nanosleep(64);
   }
   return true;

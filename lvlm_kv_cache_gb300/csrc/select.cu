@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   __shared__ int last_s;
   pdl_trigger();
   pdl_wait();  // I_v, and the keep counts or (budget mode) the moment records
+  if (*(volatile int32_t*)w.error != 0) return;  // an earlier kernel reported an error
   Req R{};
   const bool ok_req = load_req(p, b, R);
   if (!ok_req) R.vis0 = 0;

@@ -76,7 +76,7 @@ def test_sizes_of_a_valid_problem(A):
     ("num_layers", 0, -1), ("num_layers", 257, -1), ("num_requests", 0, -1),
     ("h_q", 7, -1), ("h_kv", 0, -1), ("head_dim", 96, -2), ("head_dim", 0, -1),
     ("dtype", 7, -2), ("max_visual", 2, -1), ("max_text", 0, -1), ("max_text", 9000, -2),
-    ("max_elite", 65, -1), ("max_elite", -1, -1), ("variant", 2 << 16, -1), ("variant", 1 << 24, -1), ("variant", 4, -1), ("variant", 5 << 8, -1),
+    ("max_elite", 65, -1), ("max_elite", -1, -1), ("variant", 2 << 16, -1), ("variant", 1 << 25, -1), ("variant", 4, -1), ("variant", 5 << 8, -1),
     ("total_visual", 5, -1), ("total_tokens", 1901, -1), ("total_visual", 2001, -1),
     ("cu_seqlens", None, -1), ("cu_visual", None, -1),
     ("kv_stride_tok", 0, -1), ("kv_stride_tok", 3, -1), ("q_stride_head", 4, -1),
@@ -93,6 +93,14 @@ def test_invalid_problem_rejected_on_host(A, field, value, code):
                                ctypes.c_void_p(0x700000), 10 ** 6, ctypes.c_void_p(0x800000),
                                None, None, None)
     assert rc == code
+
+
+def test_wait_test_hook_is_accepted(A):
+    # bit 24 of the variant word is the bounded-wait test hook (the workspace is unchanged)
+    p = fake_problem(A)
+    q = fake_problem(A, variant=A.VARIANT_WAIT_TEST)
+    assert A.VARIANT_WAIT_TEST == 1 << 24
+    assert A.lib().aircache_workspace_size(ctypes.byref(q)) == A.lib().aircache_workspace_size(ctypes.byref(p)) > 0
 
 
 def test_unaligned_layer_pointer_rejected(A):
