@@ -62,6 +62,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.5, help="untimed back-to-back load before timing")
     ap.add_argument("--cpu-sample-s", type=float, default=10.0)
+    ap.add_argument("--prefill", action="store_true",
+                    help="time the causal prefill attention of every layer alone, with the AirCache scoring "
+                         "fused in (aircache_prefill_compress), and followed by aircache_compress")
     ap.add_argument("--decode", action="store_true",
                     help="measure the decode consumer instead: one decode step of attention over the full and "
                          "the compressed cache, per decode configuration (one JSON line each)")
@@ -457,6 +460,105 @@ def run_decode(args, local):
         torch.cuda.empty_cache()
 
 
+def run_prefill(args, local):
+    """The scoring fused into prefill: (a) aircache_prefill (causal attention of
+    every layer), (b) aircache_prefill_compress (the same attention, and the
+    whole compression from its logits), (c) aircache_prefill then
+    aircache_compress (the scoring streams the keys again).  L2 is flushed before
+    every timed call (outside the events); medians of the timed calls."""
+    import torch
+
+    from lvlm_kv_cache_gb300 import aircache as A
+    from lvlm_kv_cache_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        flush_buf.zero_()
+        torch.sum(flush_buf.view(torch.int64), dim=(0,), out=flush_sink)
+
+    wl = W.make(args.config, device=dev)
+    spec = wl.spec
+    qv = W.visual_queries(wl, 1)
+    cu_s, cu_v, cu_t = W.offsets(spec)
+    q = torch.empty((spec.L, wl.total_tokens, spec.H_q, spec.D), dtype=spec.dtype, device=dev)
+    for b in range(spec.B):
+        nv = cu_v[b + 1] - cu_v[b]
+        q[:, cu_s[b]:cu_s[b] + nv] = qv[:, cu_v[b]:cu_v[b + 1]]
+        q[:, cu_s[b] + nv:cu_s[b + 1]] = wl.q[:, cu_t[b]:cu_t[b + 1]]
+    del qv
+    prob = A.Problem(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.cu_visual, max(spec.n_visual), max(spec.n_text),
+                     spec.alpha, spec.r)
+    attn = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    ws = prob.new_workspace()
+    out = A.alloc_outputs(prob)
+
+    def plain():
+        A.aircache_prefill(prob, q, attn, ws)
+
+    def fused():
+        A.aircache_prefill_compress(prob, q, attn, ws, out["out_k"], out["out_v"], out["out_offsets"],
+                                    out["keep"], out["idx"], out["iv"])
+
+    def separate():
+        plain()
+        A.aircache_compress(prob, ws, out["out_k"], out["out_v"], out["out_offsets"], out["keep"], out["idx"],
+                            out["iv"])
+
+    def compress_only():
+        A.aircache_compress(prob, ws, out["out_k"], out["out_v"], out["out_offsets"], out["keep"], out["idx"],
+                            out["iv"])
+
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for it in range(max(args.warmup, 3) + args.steps):
+            flush_l2()
+            torch.cuda.synchronize()
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if it >= max(args.warmup, 3):
+                ts.append(e0.elapsed_time(e1))
+        assert A.aircache_get_error(ws) == 0
+        return statistics.median(ts)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_plain = timed(plain)
+    t_fused = timed(fused)
+    t_sep = timed(separate)
+    t_comp = timed(compress_only)
+    clocks = sampler.stop()
+    flops = sum((n := cu_s[b + 1] - cu_s[b]) * (n + 1) // 2 for b in range(spec.B)) * spec.H_q * spec.L * spec.D * 4
+    tflops = flops / (t_plain * 1e-3) / 1e12
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peak, peak_kind = 1900.0, "fallback"
+    if os.path.exists(peaks_path):
+        with open(peaks_path) as f:
+            peak, peak_kind = float(json.load(f)["bf16_tflops"]), "measured (burst)"
+    line = {
+        "metric": "prefill with the AirCache scoring fused in: time over the plain prefill", "unit": "ms",
+        "value": t_fused, "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS.get(args.config, args.config) + "; queries of every prompt row "
+                               "(seeded visual-token queries, then the text queries)",
+                   "name": args.config, "l2": "flushed before every timed call outside the events"},
+        "prefill_ms": t_plain, "prefill_compress_ms": t_fused, "prefill_then_compress_ms": t_sep,
+        "compress_ms": t_comp,
+        "fused_overhead": (t_fused - t_plain) / t_plain, "separate_overhead": (t_sep - t_plain) / t_plain,
+        "causal_flops": flops,
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": tflops, "peak": peak,
+                     "unit": "TFLOP/s", "frac": tflops / peak, "peak_kind": peak_kind, "traffic": None},
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, rank, world):
@@ -502,6 +604,8 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.prefill:
+        return run_prefill(args, local)
     if args.decode:
         return run_decode(args, local)
 

@@ -274,6 +274,44 @@ AIRCACHE_API const char* aircache_status_string(int status);
  */
 AIRCACHE_API int aircache_compress_launches(const aircache_problem* p);
 
+/* Scoring fused into prefill (AirCache notes, "Limitations and outlook": the
+ * method's scoring costs the prefill 5-12 %; here it reads the prefill's own
+ * logits instead of streaming the keys again).
+ *
+ * aircache_prefill: causal prefill attention of every layer of `p`,
+ *   O_h = softmax_j(q_h . k_j / sqrt(D), j <= i within the request) V, for every
+ *   prompt row i of every request and query head h (KV head h / (h_q / h_kv)).
+ * aircache_prefill_compress: the same attention, and from it the whole one-shot
+ *   compression of aircache_compress: the elite window on the prompt's own text
+ *   queries, then each elite row's logits against every visual key and their
+ *   log-sum-exp taken inside the prefill (no second pass over the keys), then
+ *   I_v, the layer budgets, the selection and the compacted cache as
+ *   aircache_compress produces them (the same arguments and outputs; I_v agrees
+ *   with aircache_compress's within fp32 summation order).
+ *
+ * q_all: HOST array [L] of device pointers, evenly strided across layers, to the
+ *   queries of EVERY prompt row, [total_tokens] rows in the order of k and v,
+ *   element strides qa_stride_tok / qa_stride_head (D contiguous, 16-byte
+ *   aligned); p->q_text and its strides are not read.
+ * attn_out: HOST array [L] of device pointers, 16-byte aligned, the bf16 output
+ *   [total_tokens] rows of h_q heads x D with element strides o_stride_tok /
+ *   o_stride_head, written by both calls.
+ * Supported: bf16, head_dim 128, visual-first prompts (n_prefix NULL), variant 0,
+ *   k, v and q_all evenly strided across layers; else AIRCACHE_ERR_UNSUPPORTED
+ *   (before any launch).  ws as for aircache_compress (aircache_workspace_size of
+ *   p).  Errors as for aircache_compress; enqueued on `stream`, no allocation,
+ *   no synchronisation.
+ */
+AIRCACHE_API int aircache_prefill(const aircache_problem* p, const void* const* q_all, int64_t qa_stride_tok,
+                                  int64_t qa_stride_head, void* const* attn_out, int64_t o_stride_tok,
+                                  int64_t o_stride_head, void* ws, size_t ws_bytes, void* stream);
+AIRCACHE_API int aircache_prefill_compress(const aircache_problem* p, const void* const* q_all,
+                                           int64_t qa_stride_tok, int64_t qa_stride_head, void* const* attn_out,
+                                           int64_t o_stride_tok, int64_t o_stride_head, void* ws, size_t ws_bytes,
+                                           void* out_k, void* out_v, int64_t* out_offsets,
+                                           int64_t out_rows_capacity, int32_t* keep, int32_t* idx, float* iv,
+                                           void* stream);
+
 /*
  * aircache_compress with timing marks, for measurement: `events` is a host
  * array of n_events == aircache_compress_launches(p) + 1 cudaEvent_t handles

@@ -138,6 +138,12 @@ def lib():
         L.aircache_compress_profile.argtypes = [P, vp, sz, vp, vp, vp, i64, vp, vp, vp,
                                                 ctypes.POINTER(ctypes.c_void_p), i32, vp]
         L.aircache_compress_profile.restype = i32
+        pv = ctypes.POINTER(ctypes.c_void_p)
+        L.aircache_prefill.argtypes = [P, pv, i64, i64, pv, i64, i64, vp, sz, vp]
+        L.aircache_prefill.restype = i32
+        L.aircache_prefill_compress.argtypes = [P, pv, i64, i64, pv, i64, i64, vp, sz, vp, vp, vp, i64, vp, vp,
+                                                vp, vp]
+        L.aircache_prefill_compress.restype = i32
         L.aircache_kernel_name.argtypes = [P, i32]
         L.aircache_kernel_name.restype = ctypes.c_char_p
         L.aircache_row_index.argtypes = [P, vp, vp, vp, vp, sz, vp, i64, vp]
@@ -310,6 +316,51 @@ def aircache_compress(prob: Problem, ws, out_k, out_v, out_offsets, keep, idx=No
     _check(lib().aircache_compress(prob.ref, _ptr(ws), ws.numel(), _ptr(out_k), _ptr(out_v),
                                    _ptr(out_offsets), cap, _ptr(keep), _ptr(idx), _ptr(iv),
                                    _stream(stream)), "aircache_compress")
+
+
+def _layer_array(ts):
+    arr = (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+    return arr, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+
+
+def aircache_prefill(prob: Problem, q_all, attn_out, ws, stream=None):
+    """Causal prefill attention of every layer: q_all [L][T][H_q][D] (every
+    prompt row), attn_out [L][T][H_q][D] bf16 (written)."""
+    qs = list(q_all.unbind(0)) if torch.is_tensor(q_all) else list(q_all)
+    os_ = list(attn_out.unbind(0)) if torch.is_tensor(attn_out) else list(attn_out)
+    qa, qp = _layer_array(qs)
+    oa, op = _layer_array(os_)
+    _check(lib().aircache_prefill(prob.ref, qp, qs[0].stride(0), qs[0].stride(1), op, os_[0].stride(0),
+                                  os_[0].stride(1), _ptr(ws), ws.numel(), _stream(stream)), "aircache_prefill")
+
+
+def aircache_prefill_compress(prob: Problem, q_all, attn_out, ws, out_k, out_v, out_offsets, keep, idx=None,
+                              iv=None, stream=None):
+    """The prefill attention and, from its own logits, the whole compression."""
+    qs = list(q_all.unbind(0)) if torch.is_tensor(q_all) else list(q_all)
+    os_ = list(attn_out.unbind(0)) if torch.is_tensor(attn_out) else list(attn_out)
+    qa, qp = _layer_array(qs)
+    oa, op = _layer_array(os_)
+    cap = out_k.shape[0]
+    _check(lib().aircache_prefill_compress(prob.ref, qp, qs[0].stride(0), qs[0].stride(1), op, os_[0].stride(0),
+                                           os_[0].stride(1), _ptr(ws), ws.numel(), _ptr(out_k), _ptr(out_v),
+                                           _ptr(out_offsets), cap, _ptr(keep), _ptr(idx), _ptr(iv),
+                                           _stream(stream)), "aircache_prefill_compress")
+
+
+def prefill_compress(prob: Problem, q_all, attn_out=None, ws=None, out=None, stream=None, check=True):
+    """aircache_prefill_compress with allocated outputs; returns (attn_out, out dict)."""
+    ws = prob.new_workspace() if ws is None else ws
+    out = alloc_outputs(prob) if out is None else out
+    if attn_out is None:
+        attn_out = torch.empty(q_all.shape, dtype=torch.bfloat16, device=q_all.device)
+    aircache_prefill_compress(prob, q_all, attn_out, ws, out["out_k"], out["out_v"], out["out_offsets"],
+                              out["keep"], out["idx"], out["iv"], stream)
+    if check:
+        st = aircache_get_error(ws, stream)
+        if st != OK:
+            raise AirCacheError(st, "aircache_prefill_compress (device)")
+    return attn_out, out
 
 
 def aircache_compress_profile(prob: Problem, ws, out_k, out_v, out_offsets, keep, events, idx=None,

@@ -451,6 +451,90 @@ int aircache_compress_profile(const aircache_problem* p, void* ws, size_t ws_byt
                        events, n_events, stream);
 }
 
+// The problem with its query pointers and strides replaced by the full-prompt
+// queries of the fused prefill.
+static aircache_problem with_q_all(const aircache_problem* p, const void* const* q_all, int64_t qa_stride_tok,
+                                   int64_t qa_stride_head) {
+  aircache_problem pp = *p;
+  pp.q_text = q_all;
+  pp.q_stride_tok = qa_stride_tok;
+  pp.q_stride_head = qa_stride_head;
+  return pp;
+}
+
+static int prefill_checks(const aircache_problem* pp, const void* const* attn_out, int64_t o_stride_tok,
+                          int64_t o_stride_head, void* ws, size_t ws_bytes) {
+  int rc = validate(pp);
+  if (rc != AIRCACHE_OK) return rc;
+  if ((rc = check_ws(pp, ws, ws_bytes)) != AIRCACHE_OK) return rc;
+  if (!attn_out) return AIRCACHE_ERR_INVALID_ARG;
+  for (int l = 0; l < pp->num_layers; ++l)
+    if (!attn_out[l] || !aligned16(attn_out[l])) return AIRCACHE_ERR_INVALID_ARG;
+  if (o_stride_tok <= 0 || o_stride_head <= 0 || (o_stride_head < pp->head_dim && pp->h_q > 1))
+    return AIRCACHE_ERR_INVALID_ARG;
+  if (pp->variant != 0 || pp->n_prefix) return AIRCACHE_ERR_UNSUPPORTED;  // the method's own path only
+  const Dev d = make_dev(pp);
+  if (!prefill_eligible(d, make_ptrs(pp), pp->q_stride_tok, pp->q_stride_head, o_stride_tok, o_stride_head))
+    return AIRCACHE_ERR_UNSUPPORTED;
+  return AIRCACHE_OK;
+}
+
+int aircache_prefill(const aircache_problem* p, const void* const* q_all, int64_t qa_stride_tok,
+                     int64_t qa_stride_head, void* const* attn_out, int64_t o_stride_tok, int64_t o_stride_head,
+                     void* ws, size_t ws_bytes, void* stream) {
+  if (!p || !q_all) return AIRCACHE_ERR_INVALID_ARG;
+  const aircache_problem pp = with_q_all(p, q_all, qa_stride_tok, qa_stride_head);
+  int rc = prefill_checks(&pp, attn_out, o_stride_tok, o_stride_head, ws, ws_bytes);
+  if (rc != AIRCACHE_OK) return rc;
+  Dev d = make_dev(&pp);
+  d.q_all = 1;
+  const LayerPtrs lp = make_ptrs(&pp);
+  Ws w;
+  carve(d, static_cast<char*>(ws), &w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
+  AC_TRY(launch_prefill(d, lp, w, qa_stride_tok, qa_stride_head, attn_out, o_stride_tok, o_stride_head,
+                        pp.max_visual + pp.max_text, false, sm_count(), s));
+  return AIRCACHE_OK;
+}
+
+int aircache_prefill_compress(const aircache_problem* p, const void* const* q_all, int64_t qa_stride_tok,
+                              int64_t qa_stride_head, void* const* attn_out, int64_t o_stride_tok,
+                              int64_t o_stride_head, void* ws, size_t ws_bytes, void* out_k, void* out_v,
+                              int64_t* out_offsets, int64_t out_rows_capacity, int32_t* keep, int32_t* idx,
+                              float* iv, void* stream) {
+  if (!p || !q_all) return AIRCACHE_ERR_INVALID_ARG;
+  const aircache_problem pp = with_q_all(p, q_all, qa_stride_tok, qa_stride_head);
+  int rc = prefill_checks(&pp, attn_out, o_stride_tok, o_stride_head, ws, ws_bytes);
+  if (rc != AIRCACHE_OK) return rc;
+  if (!out_k || !out_v || !out_offsets || !keep || out_rows_capacity < 0) return AIRCACHE_ERR_INVALID_ARG;
+  if (!aligned16(out_k) || !aligned16(out_v)) return AIRCACHE_ERR_INVALID_ARG;
+  Dev dn = make_dev(&pp);
+  dn.q_all = 1;
+  const LayerPtrs lp = make_ptrs(&pp);
+  if (!stream_eligible(dn, lp)) return AIRCACHE_ERR_UNSUPPORTED;
+  dn.stream_ok = 1;
+  Ws w;
+  carve(dn, static_cast<char*>(ws), &w);
+  w.keep = keep;
+  w.out_offsets = out_offsets;
+  if (idx) w.idx = idx;
+  if (iv) w.iv = iv;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int sms = sm_count();
+  StreamMaps maps;
+  if (!encode_stream_maps(dn, lp, w, &maps)) return AIRCACHE_ERR_CUDA;
+  if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
+  AC_TRY(launch_elite(dn, lp, w, s));
+  AC_TRY(launch_prefill(dn, lp, w, qa_stride_tok, qa_stride_head, attn_out, o_stride_tok, o_stride_head,
+                        pp.max_visual + pp.max_text, true, sms, s));
+  AC_TRY(launch_stream_p2(dn, maps, w, sms, s));
+  AC_TRY(launch_stream_p2k(dn, maps, w, sms, s));
+  AC_TRY(launch_select(dn, w, s, true, out_rows_capacity));
+  AC_TRY(launch_compact(dn, lp, w, out_k, out_v, out_rows_capacity, s));
+  return AIRCACHE_OK;
+}
+
 const char* aircache_kernel_name(const aircache_problem* p, int i) {
   if (validate(p) != AIRCACHE_OK) return nullptr;
   if (stream_path(p)) return (i >= 0 && i < kStreamCount) ? kStreamKernels[i] : nullptr;

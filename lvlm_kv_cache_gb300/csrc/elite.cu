@@ -62,7 +62,8 @@ __device__ __forceinline__ void load_item(const Dev& p, const Req& R, const char
     int bytes = 0;
     if (hh < p.g) {
       const int h = kvh * p.g + hh;
-      src = qbase + ((R.txt0 + R.n_t - 1) * p.q_stride_tok + (int64_t)h * p.q_stride_head) * sizeof(T) + 16 * v;
+      src = qbase + (text_q_row(p, R, R.n_t - 1) * p.q_stride_tok + (int64_t)h * p.q_stride_head) * sizeof(T) +
+            16 * v;
       bytes = 16;
     }
     cp_async16(stage + G::kKBytes + n * G::kRowPitch + 16 * v, src, bytes);
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
           const bool vq = p.window_mode == 4;
           const int pos = min(max(pos_s[e], 0), (vq ? R.n_v : n_t) - 1);
           v[q] = __ldg(reinterpret_cast<const uint4*>(
-                           (vq ? qvbase : qbase) + (((vq ? R.vis0 : R.txt0) + pos) * p.q_stride_tok +
+                           (vq ? qvbase : qbase) + ((vq ? R.vis0 + pos : text_q_row(p, R, pos)) * p.q_stride_tok +
                                                     (int64_t)(kvh * p.g + hh) * p.q_stride_head) *
                                                        sizeof(T)) +
                        c);

@@ -34,6 +34,8 @@ struct Dev {
   int head_sets;         // 1: one visual index set per KV head (I_v of each KV group)
   int chn;               // streaming pass-1 chunks per (unit, KV head): visual chunks + 1 text chunk
   int wait_test;         // 1: the first kernel's bounded wait on a flag nothing sets (a test hook)
+  int q_all;             // 1: the query pointers cover every prompt row (fused prefill), so text
+                         //    query j of a request is row text_tok(R, j), not R.txt0 + j
 };
 
 // Streaming scoring path: query rows are taken in chunks of this many (a unit
@@ -135,6 +137,12 @@ __device__ __forceinline__ int64_t text_tok(const Req& r, int64_t j) {
   return r.seq0 + j + (j >= r.n_p ? r.n_v : 0);
 }
 
+// Row of text query j of request R in the query tensor: packed text rows, or
+// (fused prefill) the prompt row of that text token.
+__device__ __forceinline__ int64_t text_q_row(const Dev& p, const Req& r, int64_t j) {
+  return p.q_all ? text_tok(r, j) : r.txt0 + j;
+}
+
 // Launch plan of the persistent scoring kernel.
 struct ScoreLaunch {
   int TV, TT;      // visual / elite-text tile slots per unit
@@ -180,6 +188,15 @@ bool encode_stream_maps(const Dev& p, const LayerPtrs& lp, const Ws& w, StreamMa
 cudaError_t launch_stream_p1(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s);
 cudaError_t launch_stream_p2(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s);
 cudaError_t launch_stream_p2k(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s);
+
+// Fused prefill (prefill.cu): causal attention of every layer (bf16, D = 128,
+// visual-first prompts); with `score`, also each elite row's visual logits
+// (stored-logit buffer) and row partials, and the elite rows' text-key partials.
+bool prefill_eligible(const Dev& p, const LayerPtrs& lp, int64_t qa_stride_tok, int64_t qa_stride_head,
+                      int64_t o_stride_tok, int64_t o_stride_head);
+cudaError_t launch_prefill(const Dev& p, const LayerPtrs& lp, const Ws& w, int64_t qa_stride_tok,
+                           int64_t qa_stride_head, void* const* out, int64_t o_stride_tok, int64_t o_stride_head,
+                           int max_tokens, bool score, int sms, cudaStream_t s);
 
 // Launch `kernel` on `s` with programmatic stream serialization, so that its
 // CTAs may start (and run up to pdl_wait()) while the previous kernel on the
