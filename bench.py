@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.5, help="untimed back-to-back load before timing")
     ap.add_argument("--cpu-sample-s", type=float, default=10.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="--prefill only: use the workload's first N layers (a small case for profiling)")
     ap.add_argument("--prefill", action="store_true",
                     help="time the causal prefill attention of every layer alone, with the AirCache scoring "
                          "fused in (aircache_prefill_compress), and followed by aircache_compress")
@@ -480,7 +482,7 @@ def run_prefill(args, local):
         flush_buf.zero_()
         torch.sum(flush_buf.view(torch.int64), dim=(0,), out=flush_sink)
 
-    wl = W.make(args.config, device=dev)
+    wl = W.make(args.config, device=dev, layers=args.layers or None)
     spec = wl.spec
     qv = W.visual_queries(wl, 1)
     cu_s, cu_v, cu_t = W.offsets(spec)
@@ -547,7 +549,8 @@ def run_prefill(args, local):
         "warmup": max(args.warmup, 3), "dtype": "bf16", "data": "synthetic",
         "config": {"workload": DESCRIPTIONS.get(args.config, args.config) + "; queries of every prompt row "
                                "(seeded visual-token queries, then the text queries)",
-                   "name": args.config, "l2": "flushed before every timed call outside the events"},
+                   "name": args.config, "layers": spec.L,
+                   "l2": "flushed before every timed call outside the events"},
         "prefill_ms": t_plain, "prefill_compress_ms": t_fused, "prefill_then_compress_ms": t_sep,
         "compress_ms": t_comp,
         "fused_overhead": (t_fused - t_plain) / t_plain, "separate_overhead": (t_sep - t_plain) / t_plain,

@@ -28,7 +28,7 @@
 // logits of the units in flight stay in L2).  The keys of a unit with a single
 // row chunk are read once, with an L2 evict-first policy.
 //
-// Pass 2 (score_pass2, persistent).  Units with stored logits: each CTA takes a
+// Pass 2 (score_pass2, persistent, two CTAs per SM).  Units with stored logits: each CTA takes a
 // contiguous range of (unit, 256 keys) items, merges a unit's row partials
 // (chunk order) into row log-sum-exps when it enters the unit, then sums
 // exp2(logit - lse) over every row of every KV head for each key.  Units
@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(kThreads1, 1) stream_p1_kernel(const __grid_co
 constexpr int kKeysP2 = kT2;                  // keys per pass-2 item (one per thread)
 constexpr int kP2Box = 8;                     // logit rows per TMA box
 constexpr int kP2Slice = kRC * kKeysP2 * 4;   // one KV head's logits of an item (32 KB)
-constexpr int kP2Stages = 6;                  // slices in flight
+constexpr int kP2Stages = 3;                  // slices in flight (two CTAs per SM)
 constexpr int kMomT = 128;                    // pass-2 moment threads (two values each)
 constexpr int kT2p = kT2 + 32 + kMomT;        // pass-2 threads: streamers, the producer warp, moment warps
 constexpr int kP2Prod = kT2 / 32;             // the producer warp
@@ -940,7 +940,7 @@ __device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, unsig
   if (!p2_hand_off(c, n_hand, h, 1, &zero, &tid, &no) && tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
 }
 
-__global__ void __launch_bounds__(kT2p, 1) stream_p2_kernel(const __grid_constant__ SArgs a) {
+__global__ void __launch_bounds__(kT2p, 2) stream_p2_kernel(const __grid_constant__ SArgs a) {
   const Dev& p = a.p;
   const Ws& w = a.w;
   extern __shared__ unsigned char smem_raw[];
@@ -1271,7 +1271,7 @@ cudaError_t launch_stream_p2(const Dev& p, const StreamMaps& m, const Ws& w, int
   const int smem = kP2CtlOff + (int)sizeof(Ctl2p) + (int)sizeof(float) * p.h_kv * kLgRows + 128;
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(stream_p2_kernel), smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(stream_p2_kernel, dim3(sms), dim3(kT2p), smem, s, a);
+  return launch_pdl(stream_p2_kernel, dim3(2 * sms), dim3(kT2p), smem, s, a);
 }
 
 cudaError_t launch_stream_p2k(const Dev& p, const StreamMaps& m, const Ws& w, int sms, cudaStream_t s) {
