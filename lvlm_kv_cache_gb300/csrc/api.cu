@@ -430,7 +430,7 @@ static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, v
   }
   AC_TRY(launch_select(dn, w, s, dn.stream_ok != 0, out_rows_capacity));
   AC_TRY(mark(k++));
-  AC_TRY(launch_compact(dn, lp, w, out_k, out_v, out_rows_capacity, s));
+  AC_TRY(launch_compact(dn, lp, w, out_k, out_v, out_rows_capacity, s, dn.stream_ok != 0));
   AC_TRY(mark(k++));
   return AIRCACHE_OK;
 }
@@ -531,7 +531,7 @@ int aircache_prefill_compress(const aircache_problem* p, const void* const* q_al
   AC_TRY(launch_stream_p2(dn, maps, w, sms, s));
   AC_TRY(launch_stream_p2k(dn, maps, w, sms, s));
   AC_TRY(launch_select(dn, w, s, true, out_rows_capacity));
-  AC_TRY(launch_compact(dn, lp, w, out_k, out_v, out_rows_capacity, s));
+  AC_TRY(launch_compact(dn, lp, w, out_k, out_v, out_rows_capacity, s, true));
   return AIRCACHE_OK;
 }
 

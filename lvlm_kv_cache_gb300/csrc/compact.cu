@@ -5,11 +5,14 @@
 // The output arena holds, for each layer l and request b in that order, the
 // rows [K_v[idx]; K_t] (and the same rows of V) as dense [h_kv][head_dim] rows.
 // A persistent grid of warps walks the output rows; each warp finds its row's
-// (l, b) by binary search over the row offsets (staged in shared memory),
+// (l, b) by binary search over the row offsets (staged in shared memory; after
+// the budget-mode selection every CTA forms them itself from the keep counts,
+// and CTA 0 writes them out),
 // resolves the source position and copies the K and V rows with 16-byte loads
 // and stores.  Bit-exact: no arithmetic touches the data.
 #include "internal.cuh"
 #include "ptx.cuh"
+#include "reduce.cuh"
 
 namespace aircache {
 namespace {
@@ -26,6 +29,7 @@ struct CompactArgs {
   void* out_v;
   int64_t capacity;  // rows out_k / out_v hold (or entries of row_index)
   int32_t* row_index;  // non-null: write each row's prompt position instead of copying it
+  int make_offsets;    // 1: form the row offsets from the keep counts (at most kMaxSmemOffsets units)
 };
 
 __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_constant__ CompactArgs a) {
@@ -33,12 +37,21 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_cons
   const Ws& w = a.w;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ long long offs[kMaxSmemOffsets + 1];
+  __shared__ long long seg[kCopyWarps + 1];
   pdl_trigger();
   pdl_wait();  // selections, keep counts and row offsets
   if (*(volatile int32_t*)w.error != 0) return;
   const int units = p.L * p.B;
   const bool in_smem = units <= kMaxSmemOffsets;
-  if (in_smem) {
+  if (a.make_offsets && in_smem) {
+    // exclusive prefix of keep + N_t over the units, in shared memory; CTA 0
+    // also writes it to the caller's offsets (and flags a capacity overflow)
+    write_offsets<kCopyThreads>(p, w.keep, reinterpret_cast<int64_t*>(offs), blockIdx.x == 0 ? w.error : nullptr,
+                                a.capacity, seg, tid, 1);
+    __syncthreads();
+    if (blockIdx.x == 0)
+      for (int i = tid; i <= units; i += kCopyThreads) w.out_offsets[i] = offs[i];
+  } else if (in_smem) {
     for (int i = tid; i <= units; i += kCopyThreads) offs[i] = w.out_offsets[i];
   }
   __syncthreads();
@@ -121,9 +134,12 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_cons
 
 }  // namespace
 
+bool compact_makes_offsets(const Dev& p) { return (long long)p.L * p.B <= kMaxSmemOffsets; }
+
 cudaError_t launch_compact(const Dev& p, const LayerPtrs& lp, const Ws& w, void* out_k, void* out_v,
-                           int64_t capacity, cudaStream_t s) {
+                           int64_t capacity, cudaStream_t s, bool make_offsets) {
   CompactArgs a;
+  a.make_offsets = make_offsets && compact_makes_offsets(p) ? 1 : 0;
   a.p = p;
   a.lp = lp;
   a.w = w;
@@ -151,6 +167,7 @@ cudaError_t launch_row_index(const Dev& p, const LayerPtrs& lp, const Ws& w, int
   a.out_v = nullptr;
   a.capacity = capacity;
   a.row_index = row_index;
+  a.make_offsets = 0;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -168,8 +168,9 @@ cudaError_t launch_score(const Dev& p, const LayerPtrs& lp, const Ws& w, const S
 cudaError_t launch_stats_budget(const Dev& p, const Ws& w, double* stats_out,
                                 int64_t out_capacity, bool offsets, cudaStream_t s);
 // budget (streaming path): the select kernel first derives the keep counts of
-// its request from passes 2 / 2k's moment records, writes the statistics and
-// keep counts, and its last CTA the row offsets (checked against out_capacity).
+// its request from passes 2 / 2k's moment records and writes the statistics
+// and keep counts; the row offsets (checked against out_capacity) come from the
+// compaction, or from the selection's last CTA when !compact_makes_offsets(p).
 cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s, bool budget = false,
                           int64_t out_capacity = 0);
 // Streaming scoring path (stream.cu).  stream_eligible: the problem's dtype,
@@ -224,7 +225,11 @@ cudaError_t launch_offsets(const Dev& p, const Ws& w, int64_t out_capacity, cuda
 // optional device status copy, with the module's fixed scratch.
 int budget_noalloc(const Dev& p, const float* iv, double* stats_out, int32_t* keep, int32_t* device_status,
                    cudaStream_t s);
+// make_offsets (after the budget-mode selection): the compaction forms the row
+// offsets from the keep counts itself when compact_makes_offsets(p); otherwise
+// the selection's last CTA writes them.
+bool compact_makes_offsets(const Dev& p);
 cudaError_t launch_compact(const Dev& p, const LayerPtrs& lp, const Ws& w, void* out_k,
-                           void* out_v, int64_t capacity, cudaStream_t s);
+                           void* out_v, int64_t capacity, cudaStream_t s, bool make_offsets = false);
 
 }  // namespace aircache

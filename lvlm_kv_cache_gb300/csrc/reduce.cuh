@@ -359,15 +359,31 @@ __device__ __forceinline__ ff skew_ff(float n, ff m2, ff m3, bool all_equal) {
 // (the block's own deviations sum to zero).  Lane j takes records j, j+32, ...;
 // the lane totals are summed in a fixed butterfly order.
 __device__ __forceinline__ void layer_stats_warp(const float4* rec, int nslots, int lane, ff& s_t, ff& s_k) {
+  // records lane and lane + 32 are loaded once (all three words, up front) and
+  // kept in registers for the second pass; any further ones are read twice
+  float4 h0[2], h1[2], h2[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int j = lane + 32 * q;
+    const bool ok = j < nslots;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    h0[q] = ok ? __ldcg(rec + (size_t)j * kMomWords) : z;
+    h1[q] = ok ? __ldcg(rec + (size_t)j * kMomWords + 1) : z;
+    h2[q] = ok ? __ldcg(rec + (size_t)j * kMomWords + 2) : z;
+  }
   float n = 0.f, mn = INFINITY, mx = -INFINITY;
   ff s{0.f, 0.f};
-  for (int j = lane; j < nslots; j += 32) {
-    const float4 w0 = __ldcg(rec + (size_t)j * kMomWords), w2 = __ldcg(rec + (size_t)j * kMomWords + 2);
+  auto first = [&](const float4& w0, const float4& w2) {
     n += w0.x;  // integers below 2^24: exact
     s = ff_add(s, ff{w0.y, w0.z});
     mn = fminf(mn, w0.w);
     mx = fmaxf(mx, w2.x);
-  }
+  };
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    if (lane + 32 * q < nslots) first(h0[q], h2[q]);
+  for (int j = lane + 64; j < nslots; j += 32)
+    first(__ldcg(rec + (size_t)j * kMomWords), __ldcg(rec + (size_t)j * kMomWords + 2));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     n += __shfl_xor_sync(0xffffffffu, n, o);
@@ -377,15 +393,19 @@ __device__ __forceinline__ void layer_stats_warp(const float4* rec, int nslots, 
   s = warp_sum_ff(s);
   const ff mu = ff_div_f(s, n);
   ff m2{0.f, 0.f}, m3{0.f, 0.f};
-  for (int j = lane; j < nslots; j += 32) {
-    const float4 w0 = __ldcg(rec + (size_t)j * kMomWords), w1 = __ldcg(rec + (size_t)j * kMomWords + 1),
-                 w2 = __ldcg(rec + (size_t)j * kMomWords + 2);
+  auto second = [&](const float4& w0, const float4& w1, const float4& w2) {
     const ff nj{w0.x, 0.f}, m2j{w1.x, w1.y}, m3j{w1.z, w1.w};
     const ff d = ff_add(ff{w2.y, w2.z}, ff_neg(mu));
     const ff nd2 = ff_mul(nj, ff_mul(d, d));
     m2 = ff_add(m2, ff_add(m2j, nd2));
     m3 = ff_add(m3, ff_add(m3j, ff_add(ff_mul(ff_mul(ff{3.f, 0.f}, d), m2j), ff_mul(nd2, d))));
-  }
+  };
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    if (lane + 32 * q < nslots) second(h0[q], h1[q], h2[q]);
+  for (int j = lane + 64; j < nslots; j += 32)
+    second(__ldcg(rec + (size_t)j * kMomWords), __ldcg(rec + (size_t)j * kMomWords + 1),
+           __ldcg(rec + (size_t)j * kMomWords + 2));
   m2 = warp_sum_ff(m2);
   m3 = warp_sum_ff(m3);
   s_t = s;
@@ -490,7 +510,7 @@ __device__ __forceinline__ void request_budget(const Dev& p, int b, int n_v, con
 
 // out_offsets[u] (u = l*B + b): exclusive prefix over u of keep[u] + N_t[b];
 // out_offsets[L*B] is the total.  Sets AIRCACHE_ERR_CAPACITY if the total
-// exceeds `capacity`.  NT threads (a multiple of 32, at most 1024); thread tix
+// exceeds `capacity` (unless err is null).  NT threads (a multiple of 32, at most 1024); thread tix
 // owns a contiguous run of units; the per-thread totals are scanned with warp
 // shuffles.  `seg` is shared scratch of NT/32 + 1 entries.
 template <int NT>
@@ -538,7 +558,7 @@ __device__ __forceinline__ void write_offsets(const Dev& p, const int32_t* keep,
   if (tix == 0) {
     const long long total = seg[NW];
     out_offsets[units] = total;
-    if (total > capacity) set_error(err, AIRCACHE_ERR_CAPACITY);
+    if (total > capacity && err) set_error(err, AIRCACHE_ERR_CAPACITY);
   }
 }
 

@@ -44,6 +44,7 @@ struct SelectArgs {
                           // from the moment records of passes 2 / 2k, writes its own layer's keep
                           // count and statistics, and the last CTA writes the row offsets
   int64_t out_capacity;   // rows of the output arena (budget mode)
+  int offsets;            // budget mode: the last CTA writes the row offsets (else the compaction does)
 };
 
 // Larger float <=> larger key (handles -0.0 and negatives, which I_v never has).
@@ -101,9 +102,17 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   pdl_trigger();
   pdl_wait();  // I_v, and the keep counts or (budget mode) the moment records
   if (*(volatile int32_t*)w.error != 0) return;  // an earlier kernel reported an error
+  // (budget mode) this warp's first layer's elite count, fetched beside the request record
+  const int ntk0 = (a.budget && warp < p.L) ? __ldcg(&w.n_tk[warp * p.B + b]) : 0;
   Req R{};
   const bool ok_req = load_req(p, b, R);
   if (!ok_req) R.vis0 = 0;
+  const int n = ok_req ? R.n_v : 0;
+  // one set per layer from I_v, or one per KV head from that KV group's I_v
+  const size_t set = p.head_sets ? (size_t)l * p.h_kv + hs : (size_t)l;
+  const float* x = (p.head_sets ? w.ivh : w.iv) + set * p.total_visual + R.vis0;
+  int32_t* out = w.idx + set * p.total_visual + R.vis0;
+  const bool staged = n <= a.smem_keys;
   if (a.budget && ok_req) {
     // (s_t, s_k) of every layer of the request: warp w merges the key-block
     // records of layers w, w + 32, ... (the same arithmetic in every CTA of the
@@ -112,7 +121,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
       const int uu = ll * p.B + b;
       // pass 2 wrote one record per 256 keys of a unit with stored logits,
       // pass 2k one per 128-key tile of the others
-      const int blk = p.g * __ldcg(&w.n_tk[uu]) <= kLgRows ? 256 : 128;
+      const int ntk = ll == warp ? ntk0 : __ldcg(&w.n_tk[uu]);
+      const int blk = p.g * ntk <= kLgRows ? 256 : 128;
       ff s_t, s_k;
       layer_stats_warp(w.mom + (size_t)uu * p.mom_slots * kMomWords, (R.n_v + blk - 1) / blk, lane, s_t, s_k);
       if (lane == 0) {
@@ -121,12 +131,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
       }
     }
   }
-  const int n = ok_req ? R.n_v : 0;
-  // one set per layer from I_v, or one per KV head from that KV group's I_v
-  const size_t set = p.head_sets ? (size_t)l * p.h_kv + hs : (size_t)l;
-  const float* x = (p.head_sets ? w.ivh : w.iv) + set * p.total_visual + R.vis0;
-  int32_t* out = w.idx + set * p.total_visual + R.vis0;
-  const bool staged = n <= a.smem_keys;
   // stage the keys (when they fit) and find the smallest and largest
   uint32_t kmin = 0xffffffffu, kmax = 0u;
   for (int i0 = tid; i0 < n; i0 += 8 * kSelThreads) {
@@ -192,19 +196,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
     __syncthreads();
     k = keep_s[l];
     if (hs == 0) {
-      // this layer's keep count and statistics; the last CTA to get here
-      // writes the compacted-cache row offsets from every keep count
+      // this layer's keep count and statistics; unless the compaction forms
+      // the row offsets, the last CTA to get here writes them from every keep count
       if (tid == 0) {
         w.keep[u] = k;
         w.stats[2 * u] = ff_to_double(st_s[l]);
         w.stats[2 * u + 1] = ff_to_double(sk_s[l]);
-        __threadfence();
-        last_s = atomicAdd(w.cnt_all, 1u) == (unsigned)(p.L * p.B - 1) ? 1 : 0;
       }
-      __syncthreads();
-      if (last_s) {
-        __threadfence();
-        write_offsets<kSelThreads>(p, w.keep, w.out_offsets, w.error, a.out_capacity, off_seg, tid, 1);
+      if (a.offsets) {
+        if (tid == 0) {
+          __threadfence();
+          last_s = atomicAdd(w.cnt_all, 1u) == (unsigned)(p.L * p.B - 1) ? 1 : 0;
+        }
+        __syncthreads();
+        if (last_s) {
+          __threadfence();
+          write_offsets<kSelThreads>(p, w.keep, w.out_offsets, w.error, a.out_capacity, off_seg, tid, 1);
+        }
       }
     }
   } else {
@@ -359,6 +367,7 @@ cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s, bool budget
   a.w = w;
   a.budget = budget ? 1 : 0;
   a.out_capacity = out_capacity;
+  a.offsets = budget && !compact_makes_offsets(p) ? 1 : 0;
   a.smem_keys = p.max_visual < kSmemKeys ? p.max_visual : kSmemKeys;
   const int smem = 2 * (int)sizeof(uint32_t) * a.smem_keys;  // keys + candidates
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(select_kernel), smem);

@@ -138,41 +138,20 @@ __device__ __forceinline__ size_t part_index(const Dev& p, int u, int kvh, int r
 }
 
 // Merge row `row`'s partials in chunk order (visual chunks, then the text chunk)
-// into its base-2 log-sum-exp (one thread).
-// (Loads are issued eight chunks at a time.)
+// into its base-2 log-sum-exp (one thread).  Loads are issued sixteen chunks
+// (and the text chunk) at a time; a padding partial (-inf, 0) leaves the merge
+// unchanged, so the batch size does not change the result.
 __device__ __forceinline__ float row_lse(const Dev& p, const Ws& w, int u, int kvh, int row, int chv) {
   const float2* pr = w.part_s + part_index(p, u, kvh, row, 0);
-  float2 ms = make_float2(-INFINITY, 0.f);
-  for (int c0 = 0; c0 < chv; c0 += 8) {
-    float2 v[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = (c0 + q < chv) ? __ldcg(pr + c0 + q) : make_float2(-INFINITY, 0.f);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) ms = merge_ms(ms, v[q]);
-  }
-  ms = merge_ms(ms, __ldcg(pr + p.chn - 1));
-  return ms.x + log2f(ms.y);
-}
-
-// The same merge by the four lanes q = lane & 3 of a quad (all four call it):
-// lane q merges chunks q, q+4, ... in order, then the quad combines its four
-// partials (0+1, 2+3, then the two) and the text chunk.  Fixed order: the
-// result is the same run to run (it may differ from row_lse in the last bits).
-__device__ __forceinline__ float row_lse4(const Dev& p, const Ws& w, int u, int kvh, int row, int chv, int q) {
-  const float2* pr = w.part_s + part_index(p, u, kvh, row, 0);
-  float2 v[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int c = q + 4 * j;
-    v[j] = c < chv ? __ldcg(pr + c) : make_float2(-INFINITY, 0.f);
-  }
   const float2 txt = __ldcg(pr + p.chn - 1);
-  float2 ms = merge_ms(merge_ms(v[0], v[1]), merge_ms(v[2], v[3]));
-  for (int c = q + 16; c < chv; c += 4) ms = merge_ms(ms, __ldcg(pr + c));
-  float2 o = make_float2(__shfl_xor_sync(0xffffffffu, ms.x, 1), __shfl_xor_sync(0xffffffffu, ms.y, 1));
-  ms = (q & 1) ? merge_ms(o, ms) : merge_ms(ms, o);
-  o = make_float2(__shfl_xor_sync(0xffffffffu, ms.x, 2), __shfl_xor_sync(0xffffffffu, ms.y, 2));
-  ms = (q & 2) ? merge_ms(o, ms) : merge_ms(ms, o);
+  float2 ms = make_float2(-INFINITY, 0.f);
+  for (int c0 = 0; c0 < chv; c0 += 16) {
+    float2 v[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) v[q] = (c0 + q < chv) ? __ldcg(pr + c0 + q) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) ms = merge_ms(ms, v[q]);
+  }
   ms = merge_ms(ms, txt);
   return ms.x + log2f(ms.y);
 }
@@ -750,7 +729,7 @@ __device__ __forceinline__ int p2_find(const Dev& p, const Ws& w, int n, unsigne
 // exp2(logit - lse) over the rows of every KV head, writes I_v and hands the
 // item's values to the moment warps (double-buffered), which reduce them to the
 // item's moment record while the streamers go on.  The row LSEs of a unit are
-// merged from pass 1's partials (quads of lanes) when the walk enters the unit.
+// merged from pass 1's partials (one row per thread) when the walk enters the unit.
 // Units without stored logits: every thread first helps publish their row LSEs
 // for pass 2k.
 
@@ -881,15 +860,13 @@ __device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, unsig
     }
     if (it.kvh == 0 && it.rc == 0) {
       if (it.u != cur_u) {
-        // the unit's row LSEs, four lanes per row (whole quads iterate together)
+        // the unit's row LSEs, one row per thread (each row's partials loaded at once)
         named_bar_sync(kBarP2S, kT2);  // every streamer is done with the previous unit's LSEs
         const int chv = ((it.n_v + kTK - 1) / kTK + kCK - 1) / kCK;
         const int nr = p.h_kv * it.rows;
-        for (int q4 = tid >> 2; q4 < (nr + kT2 / 4 - 1) / (kT2 / 4) * (kT2 / 4); q4 += kT2 / 4) {
-          const int qq = min(q4, nr - 1);
-          const int kvh = qq / it.rows, r = qq % it.rows;
-          const float lse = row_lse4(p, w, it.u, kvh, r, chv, tid & 3);
-          if (q4 < nr && (tid & 3) == 0) S.lse_s[kvh * kLgRows + r] = lse;
+        for (int q = tid; q < nr; q += kT2) {
+          const int kvh = q / it.rows, r = q % it.rows;
+          S.lse_s[kvh * kLgRows + r] = row_lse(p, w, it.u, kvh, r, chv);
         }
         named_bar_sync(kBarP2S, kT2);
         cur_u = it.u;
