@@ -10,6 +10,14 @@
 // and CTA 0 writes them out),
 // resolves the source position and copies the K and V rows with 16-byte loads
 // and stores.  Bit-exact: no arithmetic touches the data.
+//
+// Bulk form (compact_bulk_kernel; every KV head of a token in one contiguous
+// row, one index set per layer): each CTA takes chunks of R consecutive output
+// rows.  R threads resolve the chunk's source tokens, one thread moves each
+// token's K and V rows into shared memory with bulk copies (one mbarrier per
+// buffer counts the bytes), and writes the chunk back with two bulk stores
+// (the chunk's output rows are contiguous).  Two buffers: the next chunk's
+// rows are resolved and loaded while the current one is stored.
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "reduce.cuh"
@@ -132,7 +140,145 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_cons
   }
 }
 
+// Bulk copies: global -> shared (counted on an mbarrier), shared -> global
+// (bulk group), and the waits on the bulk groups.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(smem_u32(src)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+
+constexpr int kBulkThreads = 128;
+constexpr int kBulkBuf = 48 * 1024;  // one buffer: R rows of K, then R rows of V
+constexpr int kBulkMaxRows = 64;
+
+__global__ void __launch_bounds__(kBulkThreads) compact_bulk_kernel(const __grid_constant__ CompactArgs a) {
+  const Dev& p = a.p;
+  const Ws& w = a.w;
+  const int tid = threadIdx.x;
+  extern __shared__ __align__(128) unsigned char bsm[];  // [2][kBulkBuf], then the row offsets [L*B + 1]
+  long long* offs = reinterpret_cast<long long*>(bsm + 2 * kBulkBuf);
+  __shared__ long long seg[kBulkThreads / 32 + 1];
+  __shared__ long long tok_s[2][kBulkMaxRows];
+  __shared__ __align__(8) uint64_t full[2];
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    fence_mbar_init();
+  }
+  pdl_trigger();
+  pdl_wait();  // selections, keep counts (and row offsets)
+  if (*(volatile int32_t*)w.error != 0) return;
+  const int units = p.L * p.B;  // at most kMaxSmemOffsets on this path
+  if (a.make_offsets) {
+    write_offsets<kBulkThreads>(p, w.keep, reinterpret_cast<int64_t*>(offs), blockIdx.x == 0 ? w.error : nullptr,
+                                a.capacity, seg, tid, 1);
+    __syncthreads();
+    if (blockIdx.x == 0)
+      for (int i = tid; i <= units; i += kBulkThreads) w.out_offsets[i] = offs[i];
+  } else {
+    for (int i = tid; i <= units; i += kBulkThreads) offs[i] = w.out_offsets[i];
+  }
+  __syncthreads();
+  const long long total = offs[units];
+  if (total > a.capacity || total < 0) {
+    if (tid == 0) set_error(w.error, AIRCACHE_ERR_CAPACITY);
+    return;
+  }
+  const int esize = (p.dtype == AIRCACHE_BF16) ? 2 : 4;
+  const uint32_t row_bytes = (uint32_t)(p.h_kv * p.d * esize);
+  const int R = min(kBulkMaxRows, (int)(kBulkBuf / 2 / row_bytes));
+  const long long chunks = (total + R - 1) / R;
+  // thread r < R: the source token of row r of chunk c (-1: past the end or invalid)
+  auto resolve = [&](long long c, int buf) {
+    if (tid >= R) return;
+    const long long row = c * R + tid;
+    long long tok = -1;
+    if (c < chunks && row < total) {
+      int lo = 0, hi = units - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (offs[mid] <= row) lo = mid; else hi = mid - 1;
+      }
+      const int u = lo, l = u / p.B, b = u % p.B;
+      const long long j = row - offs[u];
+      Req Rq;
+      const bool ok = load_req(p, b, Rq);
+      const int kp = w.keep[u];
+      if (j < kp) {
+        const int64_t pos = w.idx[(size_t)l * p.total_visual + Rq.vis0 + j];
+        if (pos >= 0 && pos < Rq.n_v) tok = vis_tok(Rq, pos);
+      } else if (j - kp < Rq.n_t) {
+        tok = text_tok(Rq, j - kp);
+      }
+      if (!ok || tok < 0) {
+        set_error(w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
+        tok = -1;
+      }
+      tok = tok >= 0 ? ((long long)l << 40) | tok : -1;  // the layer rides in the high bits
+    }
+    tok_s[buf][tid] = tok;
+  };
+  // one thread: the bulk loads of chunk c's rows into buffer buf
+  auto load = [&](long long c, int buf) {
+    unsigned char* kd = bsm + buf * kBulkBuf;
+    unsigned char* vd = kd + R * row_bytes;
+    uint32_t bytes = 0;
+    for (int r = 0; r < R; ++r)
+      if (tok_s[buf][r] >= 0) bytes += 2 * row_bytes;
+    mbar_arrive_expect_tx(&full[buf], bytes);
+    for (int r = 0; r < R; ++r) {
+      const long long t = tok_s[buf][r];
+      if (t < 0) continue;
+      const int l = (int)(t >> 40);
+      const long long tok = t & ((1LL << 40) - 1);
+      const size_t off = (size_t)tok * p.kv_stride_tok * esize;
+      bulk_g2s(kd + r * row_bytes, reinterpret_cast<const char*>(a.lp.k[l]) + off, row_bytes, &full[buf]);
+      bulk_g2s(vd + r * row_bytes, reinterpret_cast<const char*>(a.lp.v[l]) + off, row_bytes, &full[buf]);
+    }
+  };
+  long long c = blockIdx.x;
+  resolve(c, 0);
+  __syncthreads();
+  if (tid == 0 && c < chunks) load(c, 0);
+  for (int k = 0; c < chunks; ++k, c += gridDim.x) {
+    const int buf = k & 1;
+    const long long cn = c + gridDim.x;
+    resolve(cn, buf ^ 1);  // overlaps the loads in flight
+    __syncthreads();
+    if (tid == 0) {
+      if (cn < chunks) {
+        bulk_wait_read_all();  // the stores of the chunk before have read buffer buf ^ 1
+        load(cn, buf ^ 1);
+      }
+      if (!mbar_wait(&full[buf], (uint32_t)((k >> 1) & 1))) {
+        set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
+      } else {
+        const int nr = (int)min((long long)R, total - c * R);
+        const unsigned char* kd = bsm + buf * kBulkBuf;
+        bulk_s2g(reinterpret_cast<char*>(a.out_k) + (size_t)c * R * row_bytes, kd, nr * row_bytes);
+        bulk_s2g(reinterpret_cast<char*>(a.out_v) + (size_t)c * R * row_bytes, kd + R * row_bytes, nr * row_bytes);
+        bulk_commit();
+      }
+    }
+    __syncthreads();  // tok_s[buf] is rewritten by the next iteration's resolve
+  }
+  if (tid == 0) bulk_wait_all();  // the stores are complete before the buffers go away
+}
+
 }  // namespace
+
+bool compact_bulk_ok(const Dev& p) {
+  const int esize = (p.dtype == AIRCACHE_BF16) ? 2 : 4;
+  const long long row_bytes = (long long)p.h_kv * p.d * esize;
+  return !p.head_sets && (p.h_kv == 1 || p.kv_stride_head == p.d) && row_bytes <= kBulkBuf / 2 &&
+         (long long)p.L * p.B <= kMaxSmemOffsets;
+}
 
 bool compact_makes_offsets(const Dev& p) { return (long long)p.L * p.B <= kMaxSmemOffsets; }
 
@@ -150,6 +296,12 @@ cudaError_t launch_compact(const Dev& p, const LayerPtrs& lp, const Ws& w, void*
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (compact_bulk_ok(p)) {
+    const int smem = 2 * kBulkBuf + (int)sizeof(long long) * (p.L * p.B + 1);
+    cudaError_t e = allow_smem(reinterpret_cast<const void*>(compact_bulk_kernel), smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(compact_bulk_kernel, dim3(sms * 2), dim3(kBulkThreads), smem, s, a);
+  }
   return launch_pdl(compact_kernel, dim3(sms * 4), dim3(kCopyThreads), 0, s, a);
 }
 

@@ -757,26 +757,40 @@ __device__ __forceinline__ bool p2_hand_off(Ctl2p* c, int& n_hand, const P2Hand&
   return true;
 }
 
-// Moment warps: one record per handed-off item, until the end record.
+// Moment warps: one record per handed-off item, until the end record.  They
+// are idle until the first item arrives, and the first pass through the
+// float-float code costs several microseconds of instruction fetches; so the
+// loop starts with one pass over zeros (n = -1) whose record is discarded,
+// through the same code, while the streamers are still on the first item.
 __device__ __forceinline__ void p2_moments(const Dev& p, const Ws& w, const P2Smem& S, int mt) {
   Ctl2p* c = S.c;
-  for (int n = 0;; ++n) {
+  for (int n = -1;; ++n) {
     const int hb = n & 1;
-    if (!mbar_wait(&c->hfull[hb], (uint32_t)((n >> 1) & 1), 4 * kWaitCycles)) {
+    const bool warm = n < 0;
+    if (!warm && !mbar_wait(&c->hfull[hb], (uint32_t)((n >> 1) & 1), 4 * kWaitCycles)) {
       if (mt == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
       return;
     }
-    const P2Hand h = c->hand[hb];
-    const float* hx = c->hx[hb];
-    float xv[2] = {(!h.end && mt < h.n) ? hx[mt] : 0.f, (!h.end && mt + kMomT < h.n) ? hx[mt + kMomT] : 0.f};
-    // shift: the mean of four of the item's values (the same in every thread)
-    const float sh = h.end ? 0.f
-                           : 0.25f * ((hx[0] + hx[min(64, h.n - 1)]) + (hx[min(128, h.n - 1)] + hx[min(192, h.n - 1)]));
-    mbar_arrive(&c->hempty[hb]);
+    P2Hand h;
+    float xv[2] = {0.f, 0.f};
+    float sh = 0.f;
+    if (warm) {
+      h.u = h.kb = h.end = 0;
+      h.n = 2 * kMomT;
+    } else {
+      h = c->hand[hb];
+      const float* hx = c->hx[hb];
+      xv[0] = (!h.end && mt < h.n) ? hx[mt] : 0.f;
+      xv[1] = (!h.end && mt + kMomT < h.n) ? hx[mt + kMomT] : 0.f;
+      // shift: the mean of four of the item's values (the same in every thread)
+      sh = h.end ? 0.f
+                 : 0.25f * ((hx[0] + hx[min(64, h.n - 1)]) + (hx[min(128, h.n - 1)] + hx[min(192, h.n - 1)]));
+      mbar_arrive(&c->hempty[hb]);
+    }
     if (h.end) return;
     bool okv[2] = {mt < h.n, mt + kMomT < h.n};
     const Mom mb = block_moments<kMomT, 2>(xv, okv, (float)h.n, sh, S.red, S.redf, mt, kBarP2M);
-    if (mt == 0) mom_store(w.mom + ((size_t)h.u * p.mom_slots + h.kb) * kMomWords, mb);
+    if (mt == 0 && !warm) mom_store(w.mom + ((size_t)h.u * p.mom_slots + h.kb) * kMomWords, mb);
   }
 }
 
