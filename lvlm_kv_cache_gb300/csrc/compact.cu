@@ -140,19 +140,6 @@ __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_cons
   }
 }
 
-// Bulk copies: global -> shared (counted on an mbarrier), shared -> global
-// (bulk group), and the waits on the bulk groups.
-__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(smem_u32(src)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
-
 constexpr int kBulkThreads = 128;
 constexpr int kBulkBuf = 48 * 1024;  // one buffer: R rows of K, then R rows of V
 constexpr int kBulkMaxRows = 64;

@@ -251,55 +251,57 @@ __global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_const
   }
   // Gather this CTA's elite query rows (row kvh*g*N_tk + hh*N_tk + e) and elite
   // text keys into dense buffers: the scoring kernel then addresses them by
-  // arithmetic alone.  One index space covers both (query rows first), so that
-  // each thread keeps up to kGatherBatch loads of either kind in flight.
+  // arithmetic alone.  Each row's source and destination are worked out once,
+  // by one thread, into a table in the (now free) stage buffers; the copy loop
+  // then moves 16-byte pieces with kGatherBatch loads in flight per thread.
   if (base <= p.max_elite) {
-    __syncthreads();  // the elite positions are in shared memory
+    __syncthreads();  // the elite positions are in shared memory; the stages are free
     const int n_tk = base;
     const int rows_g = p.g * n_tk;
     const bool vq = p.window_mode == 4;  // window 4: visual tokens' query rows; no keys added
-    const int q_r0 = kvb * rows_g, q_n = (kve - kvb) * rows_g * kVec;
-    const int k_n = vq ? 0 : (kve - kvb) * n_tk * kVec;
-    uint4* qdst = reinterpret_cast<uint4*>(a.w.qel) + ((size_t)u * p.rows_max + q_r0) * kVec;
+    const int nq = (kve - kvb) * rows_g, nk = vq ? 0 : (kve - kvb) * n_tk;
+    const int tab = NS * G::kStageBytes / (2 * (int)sizeof(void*));  // rows per table
+    const uint4** srcp = reinterpret_cast<const uint4**>(stages);
+    uint4** dstp = reinterpret_cast<uint4**>(stages) + tab;
+    uint4* qdst = reinterpret_cast<uint4*>(a.w.qel) + ((size_t)u * p.rows_max + (size_t)kvb * rows_g) * kVec;
     uint4* kdst = reinterpret_cast<uint4*>(a.w.kel) + (size_t)u * p.h_kv * p.max_elite * kVec;
-    // element i: its source, and its destination
-    auto src = [&](int i) -> const uint4* {
-      if (i < q_n) {
-        const int r = q_r0 + i / kVec, c = i % kVec;
-        const int kvh = r / rows_g, rr = r % rows_g, hh = rr / n_tk, e = rr % n_tk;
-        const int pos = min(max(pos_s[e], 0), (vq ? R.n_v : n_t) - 1);
-        return reinterpret_cast<const uint4*>((vq ? qvbase : qbase) +
-                                              ((vq ? R.vis0 + pos : text_q_row(p, R, pos)) * p.q_stride_tok +
-                                               (int64_t)(kvh * p.g + hh) * p.q_stride_head) *
-                                                  sizeof(T)) +
-               c;
+    for (int r0 = 0; r0 < nq + nk; r0 += tab) {
+      const int n = min(tab, nq + nk - r0);
+      for (int r = r0 + tid; r < r0 + n; r += kEliteThreads) {
+        const char* src;
+        uint4* dst;
+        if (r < nq) {
+          const int kvh = kvb + r / rows_g, rr = r % rows_g, hh = rr / n_tk, e = rr % n_tk;
+          const int pos = min(max(pos_s[e], 0), (vq ? R.n_v : n_t) - 1);
+          src = (vq ? qvbase : qbase) + ((vq ? R.vis0 + pos : text_q_row(p, R, pos)) * p.q_stride_tok +
+                                         (int64_t)(kvh * p.g + hh) * p.q_stride_head) *
+                                            sizeof(T);
+          dst = qdst + (size_t)r * kVec;
+        } else {
+          const int j = r - nq, kvh = kvb + j / n_tk, e = j % n_tk;
+          const int pos = min(max(pos_s[e], 0), n_t - 1);
+          src = kbase + (text_tok(R, pos) * p.kv_stride_tok + (int64_t)kvh * p.kv_stride_head) * sizeof(T);
+          dst = kdst + ((size_t)kvh * p.max_elite + e) * kVec;
+        }
+        srcp[r - r0] = reinterpret_cast<const uint4*>(src);
+        dstp[r - r0] = dst;
       }
-      const int j = i - q_n, r = j / kVec, c = j % kVec;
-      const int kvh = kvb + r / n_tk, e = r % n_tk;
-      const int pos = min(max(pos_s[e], 0), n_t - 1);
-      return reinterpret_cast<const uint4*>(
-                 kbase + (text_tok(R, pos) * p.kv_stride_tok + (int64_t)kvh * p.kv_stride_head) * sizeof(T)) +
-             c;
-    };
-    auto dst = [&](int i) -> uint4* {
-      if (i < q_n) return qdst + i;
-      const int j = i - q_n, r = j / kVec, c = j % kVec;
-      const int kvh = kvb + r / n_tk, e = r % n_tk;
-      return kdst + ((size_t)kvh * p.max_elite + e) * kVec + c;
-    };
-    const int n_all = q_n + k_n;
-    for (int i0 = tid; i0 < n_all; i0 += kGatherBatch * kEliteThreads) {
-      uint4 v[kGatherBatch];
+      __syncthreads();
+      const int nel = n * kVec;
+      for (int i0 = tid; i0 < nel; i0 += kGatherBatch * kEliteThreads) {
+        uint4 v[kGatherBatch];
 #pragma unroll
-      for (int q = 0; q < kGatherBatch; ++q) {
-        const int i = i0 + q * kEliteThreads;
-        if (i < n_all) v[q] = __ldg(src(i));
-      }
+        for (int q = 0; q < kGatherBatch; ++q) {
+          const int i = i0 + q * kEliteThreads;
+          if (i < nel) v[q] = __ldg(srcp[i / kVec] + i % kVec);
+        }
 #pragma unroll
-      for (int q = 0; q < kGatherBatch; ++q) {
-        const int i = i0 + q * kEliteThreads;
-        if (i < n_all) *dst(i) = v[q];
+        for (int q = 0; q < kGatherBatch; ++q) {
+          const int i = i0 + q * kEliteThreads;
+          if (i < nel) dstp[i / kVec][i % kVec] = v[q];
+        }
       }
+      __syncthreads();  // the table is reused by the next chunk
     }
   }
   if (rank == 0 && tid == 0) {
