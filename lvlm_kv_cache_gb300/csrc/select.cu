@@ -35,6 +35,7 @@ constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSmemKeys = 24 * 1024;  // units up to this many keys are staged in shared memory
 constexpr int kMaxBins = 2048;        // widest digit: 11 bits
+constexpr int kEmitStep = 2;          // 32-key groups per step of the emission sweeps (short code: it runs once)
 
 struct SelectArgs {
   Dev p;
@@ -298,15 +299,15 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   const unsigned lt = (1u << lane) - 1u;
   __syncthreads();  // sel_count of the last pass is read above by every thread
   int gt = 0, eq = 0;
-  for (int i0 = s0; i0 < s1; i0 += 8 * 32) {
-    uint32_t kk[8];
+  for (int i0 = s0; i0 < s1; i0 += kEmitStep * 32) {
+    uint32_t kk[kEmitStep];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < kEmitStep; ++q) {
       const int i = i0 + 32 * q + lane;
       kk[q] = i < s1 ? key_at(i) : 0u;
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < kEmitStep; ++q) {
       const int i = i0 + 32 * q + lane;
       const bool g = i < s1 && (all_taken ? kk[q] >= thr : kk[q] > thr);
       const bool e = i < s1 && !all_taken && kk[q] == thr;
@@ -336,15 +337,15 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   }
   __syncthreads();
   int gt_run = wgt[warp], eq_run = weq[warp];
-  for (int i0 = s0; i0 < s1; i0 += 8 * 32) {
-    uint32_t kk[8];
+  for (int i0 = s0; i0 < s1; i0 += kEmitStep * 32) {
+    uint32_t kk[kEmitStep];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < kEmitStep; ++q) {
       const int i = i0 + 32 * q + lane;
       kk[q] = i < s1 ? key_at(i) : 0u;
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < kEmitStep; ++q) {
       const int i = i0 + 32 * q + lane;
       const bool g = i < s1 && (all_taken ? kk[q] >= thr : kk[q] > thr);
       const bool e = i < s1 && !all_taken && kk[q] == thr;
