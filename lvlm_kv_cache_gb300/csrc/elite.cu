@@ -24,6 +24,7 @@ namespace {
 constexpr int kEliteThreads = 256;
 constexpr int kEliteWarps = kEliteThreads / 32;
 constexpr int kSmemBudget = 220 * 1024;
+constexpr int kSmemBudget2 = 110 * 1024;  // two CTAs per SM
 constexpr int kMaxCluster = 8;  // portable cluster size
 constexpr int kGatherBatch = 8; // 16-byte loads in flight per thread in the gathers
 
@@ -71,7 +72,7 @@ __device__ __forceinline__ void load_item(const Dev& p, const Req& R, const char
 }
 
 template <typename T, int D, int NS>
-__global__ void __launch_bounds__(kEliteThreads) elite_kernel(const __grid_constant__ EliteArgs a) {
+__global__ void __launch_bounds__(kEliteThreads, 2) elite_kernel(const __grid_constant__ EliteArgs a) {
   pdl_trigger();  // the next kernel may set up while this one runs
   using G = TileGeom<T, D>;
   constexpr int kVec = G::kRowBytes / 16;
@@ -381,9 +382,26 @@ cudaError_t launch_t(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStream_
   if (bytes(4, a.kv_per_cta) > (size_t)kSmemBudget) ns = 2;
   int kvc = a.kv_per_cta;
   while (kvc > 1 && bytes(ns, kvc) > (size_t)kSmemBudget) --kvc;
+  // more CTAs than SMs: the CTAs are short and latency-bound, so two per SM
+  // (two stages, fewer heads' logits at once) beat one with a deeper ring
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if ((long long)C * p.B * p.L > sms) {
+    for (int ns2 = 2; ns2 >= 1; --ns2) {  // one stage: the two CTAs of an SM overlap each other's loads
+      int kvc2 = a.kv_per_cta;
+      while (kvc2 > 1 && bytes(ns2, kvc2) > (size_t)kSmemBudget2) --kvc2;
+      if (bytes(ns2, kvc2) <= (size_t)kSmemBudget2) {
+        ns = ns2;
+        kvc = kvc2;
+        break;
+      }
+    }
+  }
   a.kv_chunk = kvc;
   const size_t smem = bytes(ns, kvc);
-  return ns == 4 ? launch_ns<T, D, 4>(a, C, smem, s) : launch_ns<T, D, 2>(a, C, smem, s);
+  if (ns == 4) return launch_ns<T, D, 4>(a, C, smem, s);
+  return ns == 2 ? launch_ns<T, D, 2>(a, C, smem, s) : launch_ns<T, D, 1>(a, C, smem, s);
 }
 
 }  // namespace
