@@ -75,6 +75,9 @@ def parse():
     ap.add_argument("--decode-ratios", default="0.1,0.5", help="retention ratios r for --decode")
     ap.add_argument("--decode-layers", type=int, default=28,
                     help="layers of the decode workload (28 = the 7B shape; fewer only for small profiling runs)")
+    ap.add_argument("--timeline", action="store_true",
+                    help="device timeline of aircache_compress on the measurement build of the library (each "
+                         "kernel's CTAs stamp their entry and exit): per kernel, when its CTAs start and end")
     return ap.parse_args()
 
 
@@ -462,6 +465,95 @@ def run_decode(args, local):
         torch.cuda.empty_cache()
 
 
+TIMELINE_UNITS = ("elite", "stream", "select", "compact")
+TIMELINE_KERNELS = {0: "elite_window", 1: "score_pass1", 2: "score_pass2", 3: "score_pass2k",
+                    5: "budget_select", 6: "gather_compact"}
+
+
+def run_timeline(args, local):
+    """Device timeline of aircache_compress on the measurement build of the
+    library (libaircache_timeline.so, compiled with -DAIRCACHE_TIMELINE: every
+    CTA of each compression kernel records its first thread's entry time and
+    its warps' latest exit time with globaltimer).  L2 flushed before every
+    call (outside it).  Per kernel: CTAs, first and last CTA entry, median and
+    last CTA exit, in microseconds from the call's first entry, each the median
+    over --steps calls.  The exit stamps add an atomic per warp, so spans read a
+    few percent longer than the product build's."""
+    os.environ["AIRCACHE_TIMELINE"] = "1"  # before the binding loads its library
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    from lvlm_kv_cache_gb300 import build
+
+    build.build(timeline=True)
+    from lvlm_kv_cache_gb300 import aircache as A
+    from lvlm_kv_cache_gb300 import workloads as W
+
+    if not A.LIB_PATH.endswith("libaircache_timeline.so"):
+        raise RuntimeError("the binding was loaded before --timeline selected the measurement build")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = A.lib()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_sink = torch.empty((), dtype=torch.int64, device=dev)
+    wl = W.make(args.config, device=dev)
+    spec = wl.spec
+    prob = A.Problem(wl.q, wl.k, wl.v, wl.cu_seqlens, wl.cu_visual, max(spec.n_visual), max(spec.n_text),
+                     spec.alpha, spec.r, total_tokens=wl.total_tokens, total_visual=wl.total_visual)
+    ws = prob.new_workspace()
+    out = A.alloc_outputs(prob)
+    for _ in range(max(3, args.warmup)):
+        A.compress(prob, ws=ws, out=out)
+    torch.cuda.synchronize()
+    shape = (8, 4096, 2)
+    rows = {k: [] for k in TIMELINE_KERNELS}
+    spans = []
+    for _ in range(args.steps):
+        for u in TIMELINE_UNITS:
+            if getattr(lib, "aircache_timeline_clear_" + u)() != 0:
+                raise RuntimeError("timeline table clear failed")
+        flush_buf.zero_()
+        torch.sum(flush_buf.view(torch.int64), dim=(0,), out=flush_sink)
+        torch.cuda.synchronize()
+        A.compress(prob, ws=ws, out=out)
+        torch.cuda.synchronize()
+        tab = np.zeros(shape, np.uint64)
+        for u in TIMELINE_UNITS:
+            buf = np.zeros(shape, np.uint64)
+            if getattr(lib, "aircache_timeline_read_" + u)(buf.ctypes.data_as(ctypes.c_void_p)) != 0:
+                raise RuntimeError("timeline table read failed")
+            tab = np.maximum(tab, buf)
+        starts = tab[:, :, 0].astype(np.int64)
+        t0 = starts[starts > 0].min()
+        last = 0.0
+        for k in TIMELINE_KERNELS:
+            ok = starts[k] > 0
+            if not ok.any():
+                continue
+            st = (starts[k][ok] - t0) / 1000.0
+            en = (tab[k, :, 1].astype(np.int64)[ok] - t0) / 1000.0
+            rows[k].append((int(ok.sum()), st.min(), st.max(), float(np.median(en)), en.max()))
+            last = max(last, en.max())
+        spans.append(last)
+    kernels = []
+    for k, name in TIMELINE_KERNELS.items():
+        if not rows[k]:
+            continue
+        r = np.array(rows[k])
+        kernels.append({"name": name, "ctas": int(r[0, 0]), "start_first_us": round(float(np.median(r[:, 1])), 2),
+                        "start_last_us": round(float(np.median(r[:, 2])), 2),
+                        "end_median_us": round(float(np.median(r[:, 3])), 2),
+                        "end_last_us": round(float(np.median(r[:, 4])), 2)})
+    print(json.dumps({"metric": "device timeline of one aircache_compress call (measurement build)",
+                      "unit": "us", "value": round(float(np.median(spans)), 2), "higher_is_better": False,
+                      "steps": args.steps, "data": "synthetic",
+                      "config": {"workload": DESCRIPTIONS.get(args.config, args.config), "name": args.config,
+                                 "l2": "flushed before every call outside it"},
+                      "kernels": kernels}), flush=True)
+
+
 def run_prefill(args, local):
     """The scoring fused into prefill: (a) aircache_prefill (causal attention of
     every layer), (b) aircache_prefill_compress (the same attention, and the
@@ -607,6 +699,8 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.timeline:
+        return run_timeline(args, local)
     if args.prefill:
         return run_prefill(args, local)
     if args.decode:

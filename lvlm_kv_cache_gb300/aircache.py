@@ -17,7 +17,10 @@ import os
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libaircache.so")
+# AIRCACHE_TIMELINE=1 selects the measurement build whose kernels record their
+# entry and exit times (build.build(timeline=True)); the default is the product build
+LIB_PATH = os.path.join(HERE, "libaircache_timeline.so" if os.environ.get("AIRCACHE_TIMELINE") == "1"
+                        else "libaircache.so")
 
 OK = 0
 DECODE_EARLY_CACHE = 1

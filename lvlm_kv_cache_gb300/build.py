@@ -3,6 +3,10 @@
 Plain nvcc, one translation unit per kernel file compiled in parallel, linked
 into one shared library with the CUDA runtime linked statically.  Usage:
 ``python -m lvlm_kv_cache_gb300.build`` (or ``build()`` from Python).
+``build(timeline=True)`` makes the separate measurement build
+``libaircache_timeline.so`` (kernels compiled with -DAIRCACHE_TIMELINE: each
+compression kernel's CTAs record their entry and exit times; see
+csrc/timeline.cuh and ``bench.py --timeline``).
 """
 from __future__ import annotations
 
@@ -16,6 +20,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libaircache.so")
+OBJ_TIMELINE = os.path.join(HERE, "_build_timeline")
+LIB_TIMELINE = os.path.join(HERE, "libaircache_timeline.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -37,11 +43,11 @@ def _headers_mtime() -> float:
     return max(os.path.getmtime(h) for h in hs)
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, verbose: bool, timeline: bool = False) -> str:
+    obj = os.path.join(OBJ_TIMELINE if timeline else OBJ, os.path.basename(src)[:-3] + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), _headers_mtime()):
         return obj
-    cmd = [_nvcc(), *ARCH, *FLAGS, "-c", src, "-o", obj + ".tmp"]
+    cmd = [_nvcc(), *ARCH, *FLAGS, *(["-DAIRCACHE_TIMELINE"] if timeline else []), "-c", src, "-o", obj + ".tmp"]
     if verbose:
         print(" ".join(cmd), flush=True)
     res = subprocess.run(cmd, capture_output=True, text=True)
@@ -53,21 +59,22 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False) -> str:
-    os.makedirs(OBJ, exist_ok=True)
+def build(verbose: bool = False, timeline: bool = False) -> str:
+    obj_dir, lib = (OBJ_TIMELINE, LIB_TIMELINE) if timeline else (OBJ, LIB)
+    os.makedirs(obj_dir, exist_ok=True)
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
-    if os.path.exists(LIB) and os.path.getmtime(LIB) >= max(os.path.getmtime(o) for o in objs):
-        return LIB
-    cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", LIB + ".tmp", *objs]
+        objs = list(ex.map(lambda s: _compile(s, verbose, timeline), srcs))
+    if os.path.exists(lib) and os.path.getmtime(lib) >= max(os.path.getmtime(o) for o in objs):
+        return lib
+    cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", lib + ".tmp", *objs]
     if verbose:
         print(" ".join(cmd), flush=True)
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(LIB + ".tmp", LIB)
-    return LIB
+    os.replace(lib + ".tmp", lib)
+    return lib
 
 
 if __name__ == "__main__":

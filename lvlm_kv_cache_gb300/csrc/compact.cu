@@ -21,6 +21,7 @@
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "reduce.cuh"
+#include "timeline.cuh"
 
 namespace aircache {
 namespace {
@@ -41,6 +42,7 @@ struct CompactArgs {
 };
 
 __global__ void __launch_bounds__(kCopyThreads) compact_kernel(const __grid_constant__ CompactArgs a) {
+  AIRCACHE_KT(6);
   const Dev& p = a.p;
   const Ws& w = a.w;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -145,6 +147,7 @@ constexpr int kBulkBuf = 48 * 1024;  // one buffer: R rows of K, then R rows of 
 constexpr int kBulkMaxRows = 64;
 
 __global__ void __launch_bounds__(kBulkThreads) compact_bulk_kernel(const __grid_constant__ CompactArgs a) {
+  AIRCACHE_KT(6);
   const Dev& p = a.p;
   const Ws& w = a.w;
   const int tid = threadIdx.x;
@@ -314,3 +317,5 @@ cudaError_t launch_row_index(const Dev& p, const LayerPtrs& lp, const Ws& w, int
 }
 
 }  // namespace aircache
+
+AIRCACHE_TIMELINE_EXPORT(compact)

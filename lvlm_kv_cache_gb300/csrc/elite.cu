@@ -17,6 +17,7 @@
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "tile.cuh"
+#include "timeline.cuh"
 
 namespace aircache {
 namespace {
@@ -73,6 +74,7 @@ __device__ __forceinline__ void load_item(const Dev& p, const Req& R, const char
 
 template <typename T, int D, int NS>
 __global__ void __launch_bounds__(kEliteThreads, 2) elite_kernel(const __grid_constant__ EliteArgs a) {
+  AIRCACHE_KT(0);
   pdl_trigger();  // the next kernel may set up while this one runs
   using G = TileGeom<T, D>;
   constexpr int kVec = G::kRowBytes / 16;
@@ -414,3 +416,5 @@ cudaError_t launch_elite(const Dev& p, const LayerPtrs& lp, const Ws& w, cudaStr
 }
 
 }  // namespace aircache
+
+AIRCACHE_TIMELINE_EXPORT(elite)

@@ -27,6 +27,7 @@
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "reduce.cuh"
+#include "timeline.cuh"
 
 namespace aircache {
 namespace {
@@ -84,6 +85,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
 }
 
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_constant__ SelectArgs a) {
+  AIRCACHE_KT(5);
   static_assert(kSelWarps == 32, "the warp-total scans assume 32 warps");
   const Dev& p = a.p;
   const Ws& w = a.w;
@@ -377,3 +379,5 @@ cudaError_t launch_select(const Dev& p, const Ws& w, cudaStream_t s, bool budget
 }
 
 }  // namespace aircache
+
+AIRCACHE_TIMELINE_EXPORT(select)

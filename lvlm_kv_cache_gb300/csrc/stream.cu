@@ -50,6 +50,7 @@
 #include "reduce.cuh"
 #include "tmap.cuh"
 #include "umma.cuh"
+#include "timeline.cuh"
 
 namespace aircache {
 namespace {
@@ -567,6 +568,7 @@ __device__ void p1_epilogue(const SArgs& a, Ctl1* c, uint32_t tmem) {
 
 template <int D>
 __global__ void __launch_bounds__(kThreads1, 1) stream_p1_kernel(const __grid_constant__ SArgs a) {
+  AIRCACHE_KT(1);
   using Gm = SGeo<D>;
   extern __shared__ unsigned char smem_raw[];
   // tiles need 1024-byte alignment (the 128-byte swizzle repeats every 8 rows)
@@ -932,6 +934,7 @@ __device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, unsig
 }
 
 __global__ void __launch_bounds__(kT2p, 2) stream_p2_kernel(const __grid_constant__ SArgs a) {
+  AIRCACHE_KT(2);
   const Dev& p = a.p;
   const Ws& w = a.w;
   extern __shared__ unsigned char smem_raw[];
@@ -1008,6 +1011,7 @@ struct Ctl2 {
 // share those keys gives the tile's final I_v.
 template <int D>
 __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constant__ SArgs a) {
+  AIRCACHE_KT(3);
   using Gm = SGeo<D>;
   constexpr int KS = Gm::kKS;
   const Dev& p = a.p;
@@ -1270,3 +1274,5 @@ cudaError_t launch_stream_p2k(const Dev& p, const StreamMaps& m, const Ws& w, in
 }
 
 }  // namespace aircache
+
+AIRCACHE_TIMELINE_EXPORT(stream)
