@@ -8,15 +8,18 @@
 // row range for KV head h and every query head of h's group (g <= 16, padded
 // to the 16 rows of an mma.sync A operand).  A producer warp reads the range
 // and streams 64-row K and V tiles of that head with TMA through a ring of
-// stages (bf16: 128-byte swizzle; int8 codes: plain rows, which each consumer
-// warp widens to f16 in a scratch laid out like a swizzled tile); four
-// consumer warps each take 16 rows of a tile:
-//   S = Q K^T      A = Q (16 heads x 16 d, in registers), B = K (ldmatrix),
+// stages (bf16: 128-byte swizzle; int8 codes: the swizzle of the row's width,
+// widened to f16 on their way into the fragments); four consumer warps each
+// take 16 rows of a tile:
+//   S = Q K^T      A = Q (16 heads x 16 d, in registers), B = K (ldmatrix;
+//                  int8: the lane's codes read as words),
 //   online softmax in base 2 per head, P rounded to bf16 (int8 cache: to f16,
 //                  scaled by 2^14; the normaliser sums the rounded weights, so
 //                  the output is an exact convex combination with relatively
 //                  perturbed weights),
-//   O += P V       A = P (the S accumulators repacked), B = V (ldmatrix.trans).
+//   O += P V       A = P (the S accumulators repacked), B = V (ldmatrix.trans;
+//                  int8: byte pairs of two rows from one 16- or 8-byte read
+//                  per row, with permuted value columns).
 // The warps' (max, sum, O) merge in shared memory.  The slices of one
 // (sequence, KV head) then merge in one of three ways: a single slice writes
 // the output; up to 8 slices form a thread-block cluster and every rank merges
@@ -53,10 +56,14 @@ constexpr int kDecZeroBlock = 256;    // error word, then the per-(s, h) counter
 
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
-// Q8: the cached rows are int8 codes (a plain row-major tile per stage, no
-// swizzle); each consumer warp widens its 16 rows to f16 (exact integers) in a
-// scratch of its own, laid out like a swizzled 16-bit tile, and runs the same
-// MMA code on it with f16 operands (Q converted once, P packed to f16).
+// Q8: the cached rows are int8 codes (one row-major tile per stage, in the
+// 128-byte swizzle, 64-byte for D = 64), widened to f16 (exact integers) on
+// their way into the MMA fragments, which then run with f16 operands (Q
+// converted once, P packed to f16).  Keys: the head dimension is permuted
+// alike for Q and K so that a lane's key codes are contiguous.  Values: n-tile
+// t's column n is the value column n*(D/8) + t, so a lane's codes of a row are
+// one contiguous piece; the output columns are put back in order when the
+// warps merge.
 template <int D, bool Q8>
 struct DecCfg {
   static constexpr int kSlabs = D / 64;                       // 128-byte bf16 column slabs per row
@@ -68,11 +75,9 @@ struct DecCfg {
   static constexpr int kMerge = kDecWarps * (kDecMaxGroup * D + 2 * kDecMaxGroup) * 4;
   static constexpr int kPartEnd = 45056 + kDecMaxGroup * D * 4 + kDecMaxGroup * 8;  // the cluster partial's end
   static constexpr int kMain = (cmax(cmax(kRing, kMerge), kPartEnd) + 1023) / 1024 * 1024;
-  static constexpr int kWarpScratch = Q8 ? 16 * D * 2 : 0;  // V rows of one warp, f16
-  static constexpr int kScratch = kDecWarps * kWarpScratch;
   static constexpr int kQBytes = kDecMaxGroup * kQPitch * 2;
   // 1024-byte alignment slack for the swizzled ring
-  static constexpr int kSmem = 1024 + kMain + kScratch + kQBytes + 2 * kStages * 8 + 64 + 3 * kDecMaxGroup * 4;
+  static constexpr int kSmem = 1024 + kMain + kQBytes + 2 * kStages * 8 + 64 + 3 * kDecMaxGroup * 4;
   static_assert(32768 + kDecMaxGroup * kDecMaxSplit * 12 <= 45056, "merge scratch below the cluster partial");
   static_assert(kSmem <= 113 * 1024, "two CTAs per SM");
 };
@@ -140,13 +145,9 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t r[4], uint32_t addr) {
                : "memory");
 }
 
-__device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
-// 8 int8 codes (lo: bytes 0-3, hi: bytes 4-7) -> 8 f16, exactly, without a
-// conversion instruction: code c becomes the unsigned byte u = c + 128 (flip
+// Two int8 codes (the bytes `sel` picks of u4, whose top bits the caller has
+// flipped) -> two f16, exactly, without a conversion instruction: code c
+// becomes the unsigned byte u = c + 128 (flip
 // the top bit), the byte permute places u in the low mantissa bits of the f16
 // 0x6400 (= 1024), so the half is 1024 + u, and one packed subtraction of 1152
 // leaves c (every integer below 2048 is an f16).
@@ -155,11 +156,14 @@ __device__ __forceinline__ uint32_t widen2_f16(uint32_t u4, uint32_t sel) {
   const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&t), __float2half2_rn(1152.f));
   return *reinterpret_cast<const uint32_t*>(&h);
 }
-__device__ __forceinline__ uint4 widen8(uint32_t lo, uint32_t hi) {
-  lo ^= 0x80808080u;
-  hi ^= 0x80808080u;
-  return make_uint4(widen2_f16(lo, 0x4140u), widen2_f16(lo, 0x4342u), widen2_f16(hi, 0x4140u),
-                    widen2_f16(hi, 0x4342u));
+
+// Byte offset within an int8 tile of the 128-byte swizzle (D = 128: rows of
+// 128 bytes, 16-byte pieces XORed with the row mod 8) or the 64-byte swizzle
+// (D = 64: pieces XORed with bits 7-8 of the offset), as the TMA copy places
+// them (each tile starts on a 1024-byte boundary).
+template <int D>
+__device__ __forceinline__ int swz8(int off) {
+  return off ^ (((off >> 7) & (D == 128 ? 7 : 3)) << 4);
 }
 
 __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
@@ -198,9 +202,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = dsm;                                                   // [stages][K tile, V tile]
-  uint8_t* scratch = dsm + C::kMain;                                     // [warp][K, V][slab][16][128 B] (Q8)
-  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(dsm + C::kMain + C::kScratch);  // [16][kQPitch]
-  uint64_t* full = reinterpret_cast<uint64_t*>(dsm + C::kMain + C::kScratch + C::kQBytes);
+  __nv_bfloat16* qs = reinterpret_cast<__nv_bfloat16*>(dsm + C::kMain);  // [16][kQPitch]
+  uint64_t* full = reinterpret_cast<uint64_t*>(dsm + C::kMain + C::kQBytes);
   uint64_t* empty = full + C::kStages;
   int* ctl = reinterpret_cast<int*>(empty + C::kStages);                 // [16]
   // the slices' (max, sum) and merge weights live in the ring once it is idle,
@@ -437,7 +440,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       break;
     }
     const int valid = nrows - i * kDecRows - r0;  // rows of this warp's 16 that belong to the slice
-    bool released = false;
     if (valid > 0) {
       uint32_t kb, vb;
       int rb;                          // this warp's first row in the tile it reads
@@ -445,39 +447,23 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       uint32_t kq[2][Q8 ? D / 16 : 1];  // int8: this thread's key codes of rows hA and hA + 8
       if constexpr (Q8) {
         // keys: the thread's D/4 codes of each of its two rows, as words (rows
-        // past the slice end read as 0); values: widened to f16 in the warp's
-        // scratch for the transposing ldmatrix; then hand the stage back
-        const uint8_t* kt = ring + st * C::kStageBytes + r0 * D;
-        const uint8_t* vt = kt + C::kTileBytes;
+        // past the slice end read as 0); the tile is in the int8 swizzle
+        const uint8_t* kt = ring + st * C::kStageBytes;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int rr = 8 * t + hA;
-          const uint4* src = reinterpret_cast<const uint4*>(kt + rr * D + cq * (D / 4));
 #pragma unroll
           for (int v = 0; v < D / 64; ++v) {
-            const uint4 x = rr < valid ? src[v] : make_uint4(0, 0, 0, 0);
+            const uint4 x = rr < valid ? *reinterpret_cast<const uint4*>(
+                                             kt + swz8<D>((r0 + rr) * D + cq * (D / 4) + 16 * v))
+                                       : make_uint4(0, 0, 0, 0);
             kq[t][4 * v] = x.x;
             kq[t][4 * v + 1] = x.y;
             kq[t][4 * v + 2] = x.z;
             kq[t][4 * v + 3] = x.w;
           }
         }
-        const uint32_t wvs = smem_u32(scratch + warp * C::kWarpScratch);
-        __syncwarp();
-        for (int c = lane; c < 16 * (D / 16); c += 32) {
-          const int rr = c / (D / 16), ch = c % (D / 16);
-          uint4 vw = make_uint4(0, 0, 0, 0);
-          if (rr < valid) vw = *reinterpret_cast<const uint4*>(vt + rr * D + ch * 16);
-          const uint32_t slab = (uint32_t)((ch * 16) / 64) * kSlabStride;
-          const int c8 = 2 * (ch & 3);
-          st_shared_u4(swz(wvs + slab, rr, c8), widen8(vw.x, vw.y));
-          st_shared_u4(swz(wvs + slab, rr, c8 + 1), widen8(vw.z, vw.w));
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-        released = true;
-        kb = 0;
-        vb = wvs;
+        kb = vb = 0;
         rb = 0;
       } else {
       kb = smem_u32(ring + st * C::kStageBytes);
@@ -567,8 +553,39 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         o[t][2] *= fB;
         o[t][3] *= fB;
       }
-      // O += P V: B = V rows via the transposing ldmatrix, two n-tiles of 8 d per load
-      {
+      // O += P V
+      if constexpr (Q8) {
+        // B fragments straight from the value tile: lane (n, c) takes rows 2c,
+        // 2c+1, 2c+8, 2c+9 of the warp's 16, value columns n*(D/8) .. +D/8-1
+        // (one piece per row); n-tile t pairs byte t of two rows (rows past
+        // the slice end hold finite codes and get weight 0)
+        const uint8_t* vt = ring + st * C::kStageBytes + C::kTileBytes;
+        uint32_t vw[4][D / 32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int rr = r0 + 2 * cq + (j & 1) + 8 * (j >> 1);
+          const int off = swz8<D>(rr * D + hA * (D / 8));
+          if constexpr (D == 128) {
+            const uint4 x = *reinterpret_cast<const uint4*>(vt + off);
+            vw[j][0] = x.x ^ 0x80808080u;
+            vw[j][1] = x.y ^ 0x80808080u;
+            vw[j][2] = x.z ^ 0x80808080u;
+            vw[j][3] = x.w ^ 0x80808080u;
+          } else {
+            const uint2 x = *reinterpret_cast<const uint2*>(vt + off);
+            vw[j][0] = x.x ^ 0x80808080u;
+            vw[j][1] = x.y ^ 0x80808080u;
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < D / 8; ++t) {
+          const uint32_t sel = (uint32_t)(t & 3) | ((uint32_t)((t & 3) + 4) << 4);
+          const uint32_t b0 = widen2_f16(__byte_perm(vw[0][t >> 2], vw[1][t >> 2], sel), 0x4140u);
+          const uint32_t b1 = widen2_f16(__byte_perm(vw[2][t >> 2], vw[3][t >> 2], sel), 0x4140u);
+          mma16816<true>(o[t], pa, b0, b1);
+        }
+      } else {
+        // B = V rows via the transposing ldmatrix, two n-tiles of 8 d per load
         const int mi = lane >> 3, ri = lane & 7;
         const int row = rb + ri + 8 * (mi & 1);
 #pragma unroll
@@ -580,10 +597,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         }
       }
     }
-    if (!released) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
   }
 
   // ---- merge the four warps' (max, sum, O)
@@ -628,6 +643,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   const float vmult = Q8 ? a.v_scale[(int64_t)s * a.h_kv + h] * (1.f / kP16) : 1.f;
   for (int idx = tid; idx < g * D; idx += kDecWarps * 32) {
     const int hh = idx / D, d = idx % D;
+    // int8 values: column d sits where n-tile d % (D/8) keeps its column d / (D/8)
+    const int dsrc = Q8 ? 8 * (d % (D / 8)) + d / (D / 8) : d;
     float m = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kDecWarps; ++w) m = fmaxf(m, mw[w * kDecMaxGroup + hh]);
@@ -638,7 +655,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         const float mx = mw[w * kDecMaxGroup + hh];
         if (mx != -INFINITY) {
           const float c = fast_exp2(mx - m);
-          osum += c * ow[(w * kDecMaxGroup + hh) * D + d];
+          osum += c * ow[(w * kDecMaxGroup + hh) * D + dsrc];
           lsum += c * lw[w * kDecMaxGroup + hh];
         }
       }
@@ -898,13 +915,15 @@ bool encode_arena(CUtensorMap* m, const void* base, const aircache_decode_proble
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)p->head_dim, (cuuint64_t)p->h_kv, (cuuint64_t)p->kv_rows};
   if (p->kv_dtype == AIRCACHE_INT8) {
-    // int8 codes: whole rows of one head per box, row-major, no swizzle
+    // int8 codes: whole rows of one head per box (128 or 64 bytes), in the
+    // swizzle of that width (the consumers undo it with swz8)
     cuuint64_t strides8[2] = {(cuuint64_t)p->kv_stride_head, (cuuint64_t)p->kv_stride_row};
     cuuint32_t box8[3] = {(cuuint32_t)p->head_dim, 1, (cuuint32_t)kDecRows};
     cuuint32_t es8[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides8, box8, es8,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE,
+               p->head_dim == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   }
   cuuint64_t strides[2] = {(cuuint64_t)p->kv_stride_head * 2, (cuuint64_t)p->kv_stride_row * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)kDecRows};
