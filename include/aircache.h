@@ -126,7 +126,15 @@ typedef struct aircache_problem {
     const int32_t* cu_visual;   /* device [B+1], non-decreasing, cu_visual[0] == 0 */
     const void* const* q_text;  /* HOST array [L] of device pointers: [total_tokens - total_visual] text rows */
     const void* const* k;       /* HOST array [L] of device pointers: [total_tokens] rows */
-    const void* const* v;       /* HOST array [L] of device pointers: [total_tokens] rows */
+    const void* const* v;       /* HOST array [L] of device pointers: [total_tokens] rows.
+                                   In aircache_compress and aircache_compact the values are
+                                   read only by the compaction (the kept visual rows and
+                                   every text row), so there v may also point to page-locked
+                                   host memory that the device can address (cudaHostAlloc /
+                                   cudaHostRegister, unified addressing): the compaction
+                                   then reads those rows in place over the host link and
+                                   the other rows never move.  The prefill entry points
+                                   read every value and need them in device memory. */
     int64_t q_stride_tok;   /* elements between consecutive Q_text rows */
     int64_t q_stride_head;  /* elements between consecutive query heads */
     int64_t kv_stride_tok;  /* elements between consecutive K/V rows (same for K and V) */

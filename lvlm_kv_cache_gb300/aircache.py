@@ -425,12 +425,14 @@ def compress(prob: Problem, ws=None, out=None, stream=None, check=True):
 
 def compress_host(q, k, v, cu_seqlens, cu_visual, max_visual, max_text, alpha=0.9, r=0.1,
                   device="cuda", stream=None):
-    """End-to-end from HOST tensors: copies q/k/v and the offsets to the device,
-    compresses, and copies the compacted cache and its offsets back.
+    """End-to-end from HOST tensors: copies q, k and the offsets to the device,
+    compresses, and copies the compacted cache and its offsets back.  Values in
+    page-locked memory (v.is_pinned()) stay on the host: only the compaction
+    reads them, and only the rows it keeps; other values are copied first.
     Returns (out_k, out_v, out_offsets) as host tensors trimmed to the rows used."""
     dq = q.to(device, non_blocking=True)
     dk = k.to(device, non_blocking=True)
-    dv = v.to(device, non_blocking=True)
+    dv = v if v.is_pinned() else v.to(device, non_blocking=True)
     dcs = cu_seqlens.to(device, non_blocking=True)
     dcv = cu_visual.to(device, non_blocking=True)
     prob = Problem(dq, dk, dv, dcs, dcv, max_visual, max_text, alpha, r,

@@ -476,6 +476,14 @@ static int prefill_checks(const aircache_problem* pp, const void* const* attn_ou
   const Dev d = make_dev(pp);
   if (!prefill_eligible(d, make_ptrs(pp), pp->q_stride_tok, pp->q_stride_head, o_stride_tok, o_stride_head))
     return AIRCACHE_ERR_UNSUPPORTED;
+  for (int l = 0; l < pp->num_layers; ++l) {  // the attention reads every value: device memory only
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, pp->v[l]) != cudaSuccess) {
+      cudaGetLastError();
+      return AIRCACHE_ERR_UNSUPPORTED;
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return AIRCACHE_ERR_UNSUPPORTED;
+  }
   return AIRCACHE_OK;
 }
 

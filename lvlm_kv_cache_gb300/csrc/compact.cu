@@ -263,11 +263,19 @@ __global__ void __launch_bounds__(kBulkThreads) compact_bulk_kernel(const __grid
 
 }  // namespace
 
-bool compact_bulk_ok(const Dev& p) {
+bool compact_bulk_ok(const Dev& p, const LayerPtrs& lp) {
   const int esize = (p.dtype == AIRCACHE_BF16) ? 2 : 4;
   const long long row_bytes = (long long)p.h_kv * p.d * esize;
-  return !p.head_sets && (p.h_kv == 1 || p.kv_stride_head == p.d) && row_bytes <= kBulkBuf / 2 &&
-         (long long)p.L * p.B <= kMaxSmemOffsets;
+  if (p.head_sets || (p.h_kv > 1 && p.kv_stride_head != p.d) || row_bytes > kBulkBuf / 2 ||
+      (long long)p.L * p.B > kMaxSmemOffsets)
+    return false;
+  // values in page-locked host memory (read in place): the warp copies
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, lp.v[0]) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
 }
 
 bool compact_makes_offsets(const Dev& p) { return (long long)p.L * p.B <= kMaxSmemOffsets; }
@@ -286,7 +294,7 @@ cudaError_t launch_compact(const Dev& p, const LayerPtrs& lp, const Ws& w, void*
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (compact_bulk_ok(p)) {
+  if (compact_bulk_ok(p, lp)) {
     const int smem = 2 * kBulkBuf + (int)sizeof(long long) * (p.L * p.B + 1);
     cudaError_t e = allow_smem(reinterpret_cast<const void*>(compact_bulk_kernel), smem);
     if (e != cudaSuccess) return e;

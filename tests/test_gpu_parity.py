@@ -155,6 +155,40 @@ def test_deterministic(A):
         assert np.array_equal(a[key], b[key], equal_nan=True), key
 
 
+def test_values_in_pinned_host_memory(A):
+    """Values left in page-locked host memory (read in place by the compaction,
+    the kept rows only): the same compressed cache, bit for bit, as with every
+    value in device memory; also through the host-tensor API."""
+    wl = W.make("7b", device="cuda", layers=3)
+    dev_out = run_fused(A, make_problem(A, wl))
+    hv = wl.v.cpu().pin_memory()
+    s = wl.spec
+    prob_h = A.Problem(wl.q, wl.k, hv, wl.cu_seqlens, wl.cu_visual, max(s.n_visual), max(s.n_text),
+                       s.alpha, s.r, total_tokens=wl.total_tokens, total_visual=wl.total_visual)
+    host_out = run_fused(A, prob_h)
+    for key in ("iv", "keep", "idx", "out_offsets", "out_k", "out_v"):
+        assert np.array_equal(dev_out[key], host_out[key], equal_nan=True), key
+    ok_, ov_, of_ = A.compress_host(wl.q.cpu(), wl.k.cpu(), hv, wl.cu_seqlens.cpu(), wl.cu_visual.cpu(),
+                                    max(s.n_visual), max(s.n_text), s.alpha, s.r)
+    rows = int(of_[-1])
+    assert np.array_equal(W.host_bits(ok_[:rows]), dev_out["out_k"][:rows])
+    assert np.array_equal(W.host_bits(ov_[:rows]), dev_out["out_v"][:rows])
+
+
+def test_prefill_rejects_values_in_host_memory(A):
+    """The prefill attention reads every value: host-resident values are refused."""
+    wl = W.make("7b", device="cuda", layers=1)
+    s = wl.spec
+    hv = wl.v.cpu().pin_memory()
+    prob_h = A.Problem(wl.q, wl.k, hv, wl.cu_seqlens, wl.cu_visual, max(s.n_visual), max(s.n_text),
+                       s.alpha, s.r, total_tokens=wl.total_tokens, total_visual=wl.total_visual)
+    q_all = torch.zeros((s.L, wl.total_tokens, s.H_q, s.D), dtype=s.dtype, device="cuda")
+    attn = torch.empty_like(q_all)
+    with pytest.raises(A.AirCacheError) as e:
+        A.aircache_prefill(prob_h, q_all, attn, prob_h.new_workspace())
+    assert e.value.status == A.ERR_UNSUPPORTED
+
+
 # ------------------------------------------------------------------ edge cases
 
 def custom_workload(n_visual, n_text, L=2, H_q=8, H_kv=2, D=128, dtype=torch.bfloat16, seed=0,
