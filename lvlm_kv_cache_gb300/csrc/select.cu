@@ -22,8 +22,9 @@
 // its keys are staged, warp w merges the key-block moment records of layers w,
 // w + 32, ... of its request into (s_t, s_k) (float-float, the same arithmetic
 // in every CTA of the request), warp 0 turns them into the request's keep
-// counts, and the CTA keeps its own layer's count.  The last CTA to arrive
-// writes the compacted-cache row offsets.
+// counts, and the CTA keeps its own layer's count.  The compacted-cache row
+// offsets then come from the compaction kernel (or, for more units than it
+// stages, from the last CTA of this one to arrive).
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "reduce.cuh"
@@ -43,8 +44,8 @@ struct SelectArgs {
   Ws w;
   int smem_keys;          // capacity of the dynamic shared-memory key buffer
   int budget;             // 1 (streaming path): the CTA first computes its request's layer budgets
-                          // from the moment records of passes 2 / 2k, writes its own layer's keep
-                          // count and statistics, and the last CTA writes the row offsets
+                          // from the moment records of passes 2 / 2k and writes its own layer's
+                          // keep count and statistics
   int64_t out_capacity;   // rows of the output arena (budget mode)
   int offsets;            // budget mode: the last CTA writes the row offsets (else the compaction does)
 };
