@@ -870,28 +870,60 @@ def main():
         ov_h = torch.empty_like(ok_h).pin_memory()
         of_h = torch.empty(out["out_offsets"].shape, dtype=torch.int64).pin_memory()
         # the values stay in pinned host memory: only the compaction reads them,
-        # the kept visual rows and the text rows, in place over the host link
-        prob_h = A.Problem(wl.q, wl.k, hv, wl.cu_seqlens, wl.cu_visual, max(spec.n_visual), max(spec.n_text),
-                           spec.alpha, spec.r, total_tokens=wl.total_tokens, total_visual=wl.total_visual,
+        # the kept visual rows and the text rows, in place over the host link.
+        # Two buffer sets, double-buffered across steps: step i+1's inputs
+        # cross the link while step i computes and its compacted rows come
+        # back (three streams; every step's copies and compute are inside the
+        # timed region, which ends when the last step's rows are on the host)
+        sets = []
+        for j in range(2):
+            dq = wl.q if j == 0 else torch.empty_like(wl.q)
+            dk = wl.k if j == 0 else torch.empty_like(wl.k)
+            dcs = wl.cu_seqlens if j == 0 else torch.empty_like(wl.cu_seqlens)
+            dcv = wl.cu_visual if j == 0 else torch.empty_like(wl.cu_visual)
+            pj = A.Problem(dq, dk, hv, dcs, dcv, max(spec.n_visual), max(spec.n_text), spec.alpha, spec.r,
+                           total_tokens=wl.total_tokens, total_visual=wl.total_visual,
                            window_mode=args.window_mode, budget_mode=args.budget_mode, head_sets=args.head_sets,
                            q_visual=prob.q_visual if args.window_mode == 4 else None)
+            oj = out if j == 0 else A.alloc_outputs(pj)
+            hj = (ok_h, ov_h, of_h) if j == 0 else (torch.empty_like(ok_h).pin_memory(),
+                                                   torch.empty_like(ov_h).pin_memory(),
+                                                   torch.empty_like(of_h).pin_memory())
+            sets.append({"q": dq, "k": dk, "cs": dcs, "cv": dcv, "prob": pj, "out": oj, "host": hj,
+                         "in_done": torch.cuda.Event(), "comp_done": torch.cuda.Event(),
+                         "out_done": torch.cuda.Event()})
+        s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
         v_read = int(out["out_offsets"][-1]) * spec.H_kv * spec.D * esize  # value rows the compaction reads
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hcs, hcv)) + v_read
         d2h = sum(t.numel() * t.element_size() for t in (ok_h, ov_h, of_h))
+        for st in sets:  # every event starts recorded, so the first waits are no-ops
+            for e in ("in_done", "comp_done", "out_done"):
+                st[e].record()
 
-        def e2e_step():
-            wl.q.copy_(hq, non_blocking=True)
-            wl.k.copy_(hk, non_blocking=True)
-            wl.cu_seqlens.copy_(hcs, non_blocking=True)
-            wl.cu_visual.copy_(hcv, non_blocking=True)
-            A.aircache_compress(prob_h, ws, out["out_k"], out["out_v"], out["out_offsets"], out["keep"],
-                                out["idx"], out["iv"])
-            ok_h.copy_(out["out_k"], non_blocking=True)
-            ov_h.copy_(out["out_v"], non_blocking=True)
-            of_h.copy_(out["out_offsets"], non_blocking=True)
+        def e2e_step(i):
+            st = sets[i % 2]
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(st["comp_done"])  # the step before on this set has read its inputs
+                st["q"].copy_(hq, non_blocking=True)
+                st["k"].copy_(hk, non_blocking=True)
+                st["cs"].copy_(hcs, non_blocking=True)
+                st["cv"].copy_(hcv, non_blocking=True)
+                st["in_done"].record()
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(st["in_done"])
+                s_comp.wait_event(st["out_done"])  # the step before on this set has its rows back
+                o = st["out"]
+                A.aircache_compress(st["prob"], ws, o["out_k"], o["out_v"], o["out_offsets"], o["keep"],
+                                    o["idx"], o["iv"])
+                st["comp_done"].record()
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(st["comp_done"])
+                for hb, db in zip(st["host"], (st["out"]["out_k"], st["out"]["out_v"], st["out"]["out_offsets"])):
+                    hb.copy_(db, non_blocking=True)
+                st["out_done"].record()
 
-        for _ in range(3):
-            e2e_step()
+        for i in range(4):
+            e2e_step(i)
         torch.cuda.synchronize()
         n_e2e = max(3, min(args.steps, 20))
         s_ev = torch.cuda.Event(enable_timing=True)
@@ -899,26 +931,31 @@ def main():
         if dist:
             dist.barrier()
         torch.cuda.synchronize()
-        s_ev.record()
-        for _ in range(n_e2e):
-            e2e_step()
-        e_ev.record()
+        s_ev.record(s_in)
+        for i in range(n_e2e):
+            e2e_step(i)
+        s_out.wait_stream(s_in)
+        s_out.wait_stream(s_comp)
+        e_ev.record(s_out)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(s_ev.elapsed_time(e_ev), dist, dev)
-        assert int(of_h[-1]) == int(out["out_offsets"][-1])
-        # the same rows, bit for bit, as the call with every value in device memory
-        rows_e = int(of_h[-1])
+        # every set's rows equal, bit for bit, those of the call with every value in device memory
         step()
         torch.cuda.synchronize()
-        if not (torch.equal(ok_h[:rows_e], out["out_k"][:rows_e].cpu())
-                and torch.equal(ov_h[:rows_e], out["out_v"][:rows_e].cpu())):
-            raise RuntimeError("values read in place from host memory gave other rows than device-resident values")
+        rows_e = int(out["out_offsets"][-1])
+        for st in sets:
+            hk_, hv_, ho_ = st["host"]
+            if not (int(ho_[-1]) == rows_e and torch.equal(hk_[:rows_e], out["out_k"][:rows_e].cpu())
+                    and torch.equal(hv_[:rows_e], out["out_v"][:rows_e].cpu())):
+                raise RuntimeError("the end-to-end steps (values read in place from host memory) gave other "
+                                   "rows than the device-resident call")
         line["e2e"] = {"value": whole_job_rate(world, units, n_e2e, e2e_ms), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                        "ms_per_step": e2e_ms / n_e2e,
                        "inputs": "q, k and the offsets copied from pinned host memory; the values stay "
                                  "there and the compaction reads the rows it keeps in place "
-                                 "(counted in h2d_bytes_per_step)"}
+                                 "(counted in h2d_bytes_per_step); two buffer sets, so one step's "
+                                 "inputs cross the link while the step before computes and copies back"}
 
     # ---- CPU baseline: the oracle on the host cores, rank 0 at N=1 only
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
