@@ -3,12 +3,14 @@
 // entry point validates on the host, then enqueues its kernels on the caller's
 // stream; nothing here allocates, frees or synchronises except
 // aircache_get_error.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
 #include <vector>
 
 #include "internal.cuh"
+#include "ptx.cuh"
 
 namespace aircache {
 
@@ -239,8 +241,25 @@ int sm_count() {
 // The scoring path of a validated problem (known on the host: see stream_eligible).
 bool stream_path(const aircache_problem* p) { return stream_eligible(make_dev(p), make_ptrs(p)); }
 
+// Clears the call's zeroed block (error word, counters, flags).  A kernel, not a
+// memset: the call's next kernel is launched with programmatic serialization and
+// sets up while this one runs; every kernel so launched waits for its
+// predecessor (griddepcontrol.wait) before it touches the block.  Launched
+// without that attribute itself, so it starts after everything queued before it.
+__global__ void __launch_bounds__(256) zero_kernel(uint32_t* z, int n) {
+  pdl_trigger();
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < n; i += gridDim.x * 256) z[i] = 0u;
+}
+
 int begin(const Ws& w, cudaStream_t s) {
-  return cudaMemsetAsync(w.error, 0, w.zero_bytes, s) == cudaSuccess ? AIRCACHE_OK : AIRCACHE_ERR_CUDA;
+  const int n = (int)(w.zero_bytes / sizeof(uint32_t));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::min(64, (n + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, zero_kernel, reinterpret_cast<uint32_t*>(w.error), n) == cudaSuccess
+             ? AIRCACHE_OK
+             : AIRCACHE_ERR_CUDA;
 }
 
 }  // namespace

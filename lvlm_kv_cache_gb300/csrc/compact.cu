@@ -182,7 +182,12 @@ __global__ void __launch_bounds__(kBulkThreads) compact_bulk_kernel(const __grid
   }
   const int esize = (p.dtype == AIRCACHE_BF16) ? 2 : 4;
   const uint32_t row_bytes = (uint32_t)(p.h_kv * p.d * esize);
-  const int R = min(kBulkMaxRows, (int)(kBulkBuf / 2 / row_bytes));
+  // rows per chunk: as many as a buffer holds, then evened out so that every
+  // CTA gets the same number of chunks (to one) and no CTA is left with a
+  // whole chunk more than most
+  const int Rmax = min(kBulkMaxRows, (int)(kBulkBuf / 2 / row_bytes));
+  const long long per_cta = (total + (long long)gridDim.x * Rmax - 1) / ((long long)gridDim.x * Rmax);
+  const int R = per_cta > 0 ? (int)((total + gridDim.x * per_cta - 1) / (gridDim.x * per_cta)) : Rmax;
   const long long chunks = (total + R - 1) / R;
   // thread r < R: the source token of row r of chunk c (-1: past the end or invalid)
   auto resolve = [&](long long c, int buf) {

@@ -90,12 +90,14 @@ __global__ void __launch_bounds__(kEliteThreads, 2) elite_kernel(const __grid_co
     // kernel of this call sets (the wide path's LSE-ready flag of unit 0; this
     // call does no scoring), so it runs out and reports a timeout; the kernels
     // after this one see the error and return
+    pdl_wait();  // the zeroed block
     if (rank == 0 && b == 0 && l == 0 && threadIdx.x == 0 && !wait_flag(a.w.lse_ready, 1LL << 20))
       set_error(a.w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
     return;
   }
   Req R;
   if (!load_req(p, b, R)) {  // the same verdict in every CTA of the cluster
+    pdl_wait();
     if (rank == 0 && tid == 0) set_error(a.w.error, AIRCACHE_ERR_DEVICE_BOUNDS);
     return;
   }
@@ -307,6 +309,10 @@ __global__ void __launch_bounds__(kEliteThreads, 2) elite_kernel(const __grid_co
       __syncthreads();  // the table is reused by the next chunk
     }
   }
+  // the call's zeroed block (error word, routing counters) is cleared by the
+  // kernel before this one: every thread waits for it here, so that this grid
+  // completes after it
+  pdl_wait();
   if (rank == 0 && tid == 0) {
     a.w.n_tk[u] = base;
     // the unit's layout, so that the scoring kernel resolves a work item with one
@@ -354,13 +360,15 @@ cudaError_t launch_ns(const EliteArgs& a, int C, size_t smem, cudaStream_t s) {
   cfg.blockDim = dim3(kEliteThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, elite_kernel<T, D, NS>, a);
 }
 
