@@ -167,9 +167,9 @@ size_t carve(const Dev& d, char* base, Ws* w) {
   };
   Ws t;
   std::memset(&t, 0, sizeof t);
-  // zeroed block: error, cnt_all, ticket, ticket_n, list_n[4], p2pack, cnt_req[B],
-  // cnt_p1/cnt_p2/lse_ready/p2claim[L*B]
-  const size_t zbytes = 48 + sizeof(uint32_t) * (d.B + 4 * LB);
+  // zeroed block: error, cnt_all, ticket, ticket_n, list_n[4], p2pack, cnt_cmp,
+  // cnt_req[B], cnt_p1/cnt_p2/lse_ready/p2claim[L*B]
+  const size_t zbytes = 52 + sizeof(uint32_t) * (d.B + 4 * LB);
   char* zero = take(zbytes);
   t.error = reinterpret_cast<int32_t*>(zero);
   t.cnt_all = reinterpret_cast<uint32_t*>(zero ? zero + 4 : nullptr);
@@ -177,7 +177,8 @@ size_t carve(const Dev& d, char* base, Ws* w) {
   t.ticket_n = reinterpret_cast<unsigned long long*>(zero ? zero + 16 : nullptr);
   t.list_n = reinterpret_cast<int32_t*>(zero ? zero + 24 : nullptr);
   t.p2pack = reinterpret_cast<unsigned long long*>(zero ? zero + 40 : nullptr);
-  t.cnt_req = reinterpret_cast<uint32_t*>(zero ? zero + 48 : nullptr);
+  t.cnt_cmp = reinterpret_cast<uint32_t*>(zero ? zero + 48 : nullptr);
+  t.cnt_req = reinterpret_cast<uint32_t*>(zero ? zero + 52 : nullptr);
   t.cnt_p1 = t.cnt_req ? t.cnt_req + d.B : nullptr;
   t.cnt_p2 = t.cnt_p1 ? t.cnt_p1 + LB : nullptr;
   t.lse_ready = t.cnt_p2 ? t.cnt_p2 + LB : nullptr;

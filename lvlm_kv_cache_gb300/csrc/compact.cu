@@ -13,11 +13,13 @@
 //
 // Bulk form (compact_bulk_kernel; every KV head of a token in one contiguous
 // row, one index set per layer): each CTA takes chunks of R consecutive output
-// rows.  R threads resolve the chunk's source tokens, one thread moves each
-// token's K and V rows into shared memory with bulk copies (one mbarrier per
-// buffer counts the bytes), and writes the chunk back with two bulk stores
-// (the chunk's output rows are contiguous).  Two buffers: the next chunk's
-// rows are resolved and loaded while the current one is stored.
+// rows (its first two by index, the rest claimed from a counter).  R threads
+// resolve the chunk's source tokens; each thread then moves its row's K and V
+// rows into shared memory with bulk copies (a run of consecutive tokens as one
+// copy; one mbarrier per buffer counts the bytes), and one thread writes the
+// chunk back with two bulk stores (the chunk's output rows are contiguous).
+// A chunk is resolved two iterations before it is stored and loaded one
+// before, so the index lookups and the loads overlap the stores.
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "reduce.cuh"
@@ -154,7 +156,8 @@ __global__ void __launch_bounds__(kBulkThreads) compact_bulk_kernel(const __grid
   extern __shared__ __align__(128) unsigned char bsm[];  // [2][kBulkBuf], then the row offsets [L*B + 1]
   long long* offs = reinterpret_cast<long long*>(bsm + 2 * kBulkBuf);
   __shared__ long long seg[kBulkThreads / 32 + 1];
-  __shared__ long long tok_s[2][kBulkMaxRows];
+  __shared__ long long tok_s[3][kBulkMaxRows];  // three resolved chunks: stored, loading, next
+  __shared__ long long claim_s[4];              // claimed chunk ids, by iteration
   __shared__ __align__(8) uint64_t full[2];
   if (tid == 0) {
     mbar_init(&full[0], 1);
@@ -189,8 +192,8 @@ __global__ void __launch_bounds__(kBulkThreads) compact_bulk_kernel(const __grid
   const long long per_cta = (total + (long long)gridDim.x * Rmax - 1) / ((long long)gridDim.x * Rmax);
   const int R = per_cta > 0 ? (int)((total + gridDim.x * per_cta - 1) / (gridDim.x * per_cta)) : Rmax;
   const long long chunks = (total + R - 1) / R;
-  // thread r < R: the source token of row r of chunk c (-1: past the end or invalid)
-  auto resolve = [&](long long c, int buf) {
+  // thread r < R: the source token of row r of chunk c into slot sl (-1: past the end or invalid)
+  auto resolve = [&](long long c, int sl) {
     if (tid >= R) return;
     const long long row = c * R + tid;
     long long tok = -1;
@@ -217,40 +220,70 @@ __global__ void __launch_bounds__(kBulkThreads) compact_bulk_kernel(const __grid
       }
       tok = tok >= 0 ? ((long long)l << 40) | tok : -1;  // the layer rides in the high bits
     }
-    tok_s[buf][tid] = tok;
+    tok_s[sl][tid] = tok;
   };
-  // one thread: the bulk loads of chunk c's rows into buffer buf
-  auto load = [&](long long c, int buf) {
-    unsigned char* kd = bsm + buf * kBulkBuf;
-    unsigned char* vd = kd + R * row_bytes;
+  // bytes of the rows of slot sl (thread 0, for the buffer's expected-transaction count)
+  auto chunk_bytes = [&](int sl) {
     uint32_t bytes = 0;
     for (int r = 0; r < R; ++r)
-      if (tok_s[buf][r] >= 0) bytes += 2 * row_bytes;
-    mbar_arrive_expect_tx(&full[buf], bytes);
-    for (int r = 0; r < R; ++r) {
-      const long long t = tok_s[buf][r];
-      if (t < 0) continue;
-      const int l = (int)(t >> 40);
-      const long long tok = t & ((1LL << 40) - 1);
-      const size_t off = (size_t)tok * p.kv_stride_tok * esize;
-      bulk_g2s(kd + r * row_bytes, reinterpret_cast<const char*>(a.lp.k[l]) + off, row_bytes, &full[buf]);
-      bulk_g2s(vd + r * row_bytes, reinterpret_cast<const char*>(a.lp.v[l]) + off, row_bytes, &full[buf]);
-    }
+      if (tok_s[sl][r] >= 0) bytes += 2 * row_bytes;
+    return bytes;
   };
+  // rows of consecutive tokens are adjacent in K and V (dense token stride)
+  const bool dense = (size_t)p.kv_stride_tok * esize == row_bytes;
+  // thread r < R: the bulk loads of slot sl's rows into buffer buf, issued in
+  // parallel by the threads (one thread issuing a chunk's 2R copies back to back
+  // set the pace of a chunk); a run of consecutive tokens (the text rows, and
+  // neighbouring kept visual rows) is one copy, issued by the run's first row
+  auto load_row = [&](int sl, int buf) {
+    if (tid >= R) return;
+    const long long t = tok_s[sl][tid];
+    if (t < 0) return;
+    if (dense && tid > 0 && tok_s[sl][tid - 1] >= 0 && tok_s[sl][tid - 1] == t - 1) return;  // inside a run
+    int n = 1;
+    if (dense)
+      while (tid + n < R && tok_s[sl][tid + n] == t + n) ++n;
+    unsigned char* kd = bsm + buf * kBulkBuf;
+    unsigned char* vd = kd + R * row_bytes;
+    const int l = (int)(t >> 40);
+    const long long tok = t & ((1LL << 40) - 1);
+    const size_t off = (size_t)tok * p.kv_stride_tok * esize;
+    bulk_g2s(kd + tid * row_bytes, reinterpret_cast<const char*>(a.lp.k[l]) + off, n * row_bytes, &full[buf]);
+    bulk_g2s(vd + tid * row_bytes, reinterpret_cast<const char*>(a.lp.v[l]) + off, n * row_bytes, &full[buf]);
+  };
+  // Chunks are claimed: the first two of a CTA are blockIdx.x and
+  // blockIdx.x + grid, the later ones come from a counter (from 2 * grid on),
+  // so that CTAs on SMs that copy faster take more of them.  Chunk k of the CTA
+  // is claimed three iterations ahead (by the last thread, which resolves no
+  // row) into claim_s[k % 4], resolved two ahead into slot k % 3, loaded one
+  // ahead into buffer k % 2 and stored in iteration k.
+  const long long G = gridDim.x;
+  auto claim = [&]() { return 2 * G + (long long)atomicAdd(w.cnt_cmp, 1u); };
+  if (tid == kBulkThreads - 1) claim_s[2] = claim();
+  if (tid == 0) {
+    claim_s[0] = blockIdx.x;
+    claim_s[1] = blockIdx.x + G;
+  }
   long long c = blockIdx.x;
   resolve(c, 0);
+  resolve(c + G, 1);
   __syncthreads();
-  if (tid == 0 && c < chunks) load(c, 0);
-  for (int k = 0; c < chunks; ++k, c += gridDim.x) {
+  if (tid == 0 && c < chunks) mbar_arrive_expect_tx(&full[0], chunk_bytes(0));
+  __syncthreads();
+  if (c < chunks) load_row(0, 0);
+  for (int k = 0; c < chunks; ++k) {
     const int buf = k & 1;
-    const long long cn = c + gridDim.x;
-    resolve(cn, buf ^ 1);  // overlaps the loads in flight
+    const long long cn = claim_s[(k + 1) & 3];
+    if (tid == kBulkThreads - 1) claim_s[(k + 3) & 3] = cn < chunks ? claim() : chunks;
+    resolve(claim_s[(k + 2) & 3], (k + 2) % 3);  // overlaps the loads and stores in flight
     __syncthreads();
+    if (tid == 0 && cn < chunks) {
+      bulk_wait_read_all();  // the stores of chunk k - 1 have read buffer buf ^ 1
+      mbar_arrive_expect_tx(&full[buf ^ 1], chunk_bytes((k + 1) % 3));
+    }
+    __syncthreads();
+    if (cn < chunks) load_row((k + 1) % 3, buf ^ 1);
     if (tid == 0) {
-      if (cn < chunks) {
-        bulk_wait_read_all();  // the stores of the chunk before have read buffer buf ^ 1
-        load(cn, buf ^ 1);
-      }
       if (!mbar_wait(&full[buf], (uint32_t)((k >> 1) & 1))) {
         set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
       } else {
@@ -261,7 +294,8 @@ __global__ void __launch_bounds__(kBulkThreads) compact_bulk_kernel(const __grid
         bulk_commit();
       }
     }
-    __syncthreads();  // tok_s[buf] is rewritten by the next iteration's resolve
+    __syncthreads();  // slot k % 3 and claim k are rewritten by the next iterations
+    c = cn;
   }
   if (tid == 0) bulk_wait_all();  // the stores are complete before the buffers go away
 }

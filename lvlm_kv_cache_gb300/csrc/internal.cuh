@@ -65,6 +65,7 @@ struct Ws {
   int32_t* list_n;       // [4]   units on the streaming path, on the wide path, streaming units
                          //       without stored logits (pass 2k), the other streaming units
   unsigned long long* p2pack;  // [1] routing of the pass-2 units: (count << 32) + their total weight
+  uint32_t* cnt_cmp;     // [1]   compaction chunks claimed after each CTA's first two
   uint32_t* cnt_req;     // [B]   layers of a request whose stats are done
   uint32_t* p2claim;     // [L*B] claimed pass-2 work items per (layer, request)
   uint32_t* cnt_p1;      // [L*B] finished pass-1 items per (layer, request)
