@@ -266,8 +266,11 @@ __device__ __forceinline__ void block_sum_ff3(ff& a, ff& b, ff& c, ff* red, int 
     ff ta = lane < NW ? red[lane] : ff{0.f, 0.f};
     ff tb = lane < NW ? red[NW + lane] : ff{0.f, 0.f};
     ff tc = lane < NW ? red[2 * NW + lane] : ff{0.f, 0.f};
+    // lanes >= NW hold zeros, and adding a zero float-float leaves a value
+    // unchanged, so the butterfly starts at the highest level that pairs two
+    // of the first NW lanes (lane 0 ends with the same sum)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
+    for (int o = NW / 2; o > 0; o >>= 1) {
       ta = ff_add(ta, ff_shfl_xor(ta, o));
       tb = ff_add(tb, ff_shfl_xor(tb, o));
       tc = ff_add(tc, ff_shfl_xor(tc, o));

@@ -200,14 +200,17 @@ __device__ void p1_producer(const SArgs& a, Ctl1* c, unsigned char* sm) {
   long long st = 0;  // stages issued
   int sub = 0;       // row-chunk passes issued (selects the query buffer)
   bool ok = true;
-  long long claim = (long long)atomicAdd(w.ticket_n, 1ULL);
-  long long next = (long long)atomicAdd(w.ticket_n, 1ULL);
+  // the CTA's first item is its index, the later ones come from the counter
+  // (after the first grid-size items): no atomic round trip before the first stage
+  const long long G = gridDim.x;
+  long long claim = blockIdx.x;
+  long long next = G + (long long)atomicAdd(w.ticket_n, 1ULL);
   int4 i0 = make_int4(0, 0, 0, 0), i1 = make_int4(0, 0, 0, 0);
   record(claim, i0, i1);
   while (ok && claim < total) {
     int4 n0 = make_int4(0, 0, 0, 0), n1 = make_int4(0, 0, 0, 0);
-    record(next, n0, n1);                                               // used by the next item
-    const long long next2 = (long long)atomicAdd(w.ticket_n, 1ULL);  // the claim after that
+    record(next, n0, n1);                                                   // used by the next item
+    const long long next2 = G + (long long)atomicAdd(w.ticket_n, 1ULL);  // the claim after that
     const int rem = (int)(claim % per_unit);
     const int kvh = rem / p.chn, ch = rem % p.chn;
     const int u = i1.w;
@@ -598,6 +601,11 @@ __global__ void __launch_bounds__(kThreads1, 1) stream_p1_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem = c->tmem;
   pdl_trigger();
+  if (threadIdx.x == kCT) {  // the producer's tensor maps, fetched while the elite kernel runs
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&a.kmap2)) : "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&a.qmap)) : "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&a.kelmap)) : "memory");
+  }
   pdl_wait();  // the elite kernel's lists, query rows and elite keys
   if (*(volatile int32_t*)a.w.error == 0) {  // else an earlier kernel reported an error
     if (threadIdx.x < kCT) {
