@@ -199,6 +199,7 @@ size_t carve(const Dev& d, char* base, Ws* w) {
     const size_t stride = (size_t)(d.total_visual + 4 * (int64_t)d.B + 7) / 4 * 4;
     t.lg = reinterpret_cast<float*>(take(sizeof(float) * kvrows * kLgRows * stride));
     t.mom = reinterpret_cast<float4*>(take(sizeof(float4) * 3 * LB * (size_t)d.mom_slots));
+    t.lstat = reinterpret_cast<float4*>(take(sizeof(float4) * LB));
     t.part_s = reinterpret_cast<float2*>(take(sizeof(float2) * LB * d.h_kv * d.rc_max * kRowChunk * d.chn));
   }
   t.uinfo = reinterpret_cast<int4*>(take(sizeof(int4) * 2 * LB));

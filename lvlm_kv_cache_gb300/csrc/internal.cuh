@@ -82,6 +82,7 @@ struct Ws {
   int32_t* wide_list;    // [L*B] units on the wide path (list_n[1] of them, any order)
   float* lg;             // [L][h_kv][kLgRows][lg stride] streaming path: logits of row r of KV head h
   float4* mom;           // [L*B][mom_slots][3] streaming path: moments of each key block / tile of I_v
+  float4* lstat;         // [L*B] streaming path: the unit's (s_t, s_k) as float-float pairs
   float2* part_s;        // [L*B][h_kv][rc_max*32][chn] streaming pass 1: (max, sum of exp2) per (row, chunk)
   int4* uinfo;           // [L*B][2] {seq0, vis0, txt0, N_v}, {N_t, N_tk, 1, 0} per (layer, request)
   void* qel;             // [L*B][rows_max][D] elite query rows, row kvh*g*N_tk + hh*N_tk + e

@@ -106,8 +106,6 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   pdl_trigger();
   pdl_wait();  // I_v, and the keep counts or (budget mode) the moment records
   if (*(volatile int32_t*)w.error != 0) return;  // an earlier kernel reported an error
-  // (budget mode) this warp's first layer's elite count, fetched beside the request record
-  const int ntk0 = (a.budget && warp < p.L) ? __ldcg(&w.n_tk[warp * p.B + b]) : 0;
   Req R{};
   const bool ok_req = load_req(p, b, R);
   if (!ok_req) R.vis0 = 0;
@@ -118,21 +116,12 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   int32_t* out = w.idx + set * p.total_visual + R.vis0;
   const bool staged = n <= a.smem_keys;
   if (a.budget && ok_req) {
-    // (s_t, s_k) of every layer of the request: warp w merges the key-block
-    // records of layers w, w + 32, ... (the same arithmetic in every CTA of the
-    // request, so all of them derive the same budgets)
-    for (int ll = warp; ll < p.L; ll += kSelWarps) {
-      const int uu = ll * p.B + b;
-      // pass 2 wrote one record per 256 keys of a unit with stored logits,
-      // pass 2k one per 128-key tile of the others
-      const int ntk = ll == warp ? ntk0 : __ldcg(&w.n_tk[uu]);
-      const int blk = p.g * ntk <= kLgRows ? 256 : 128;
-      ff s_t, s_k;
-      layer_stats_warp(w.mom + (size_t)uu * p.mom_slots * kMomWords, (R.n_v + blk - 1) / blk, lane, s_t, s_k);
-      if (lane == 0) {
-        st_s[ll] = s_t;
-        sk_s[ll] = s_k;
-      }
+    // (s_t, s_k) of every layer of the request, merged from the unit's moment
+    // records by the pass-2 (or pass-2k) CTA that wrote its last one
+    for (int ll = tid; ll < p.L; ll += kSelThreads) {
+      const float4 v = __ldcg(&w.lstat[ll * p.B + b]);
+      st_s[ll] = ff{v.x, v.y};
+      sk_s[ll] = ff{v.z, v.w};
     }
   }
   // stage the keys (when they fit) and find the smallest and largest

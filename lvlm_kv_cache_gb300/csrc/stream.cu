@@ -649,6 +649,7 @@ struct P2Rec {
 // Hand-off of one item's I_v from the streaming warps to the moment warps.
 struct P2Hand {
   int u, kb, n, end;
+  int nb;  // the unit's 256-key blocks (its moment records)
 };
 
 struct Ctl2p {
@@ -744,6 +745,26 @@ __device__ __forceinline__ int p2_find(const Dev& p, const Ws& w, int n, unsigne
 // for pass 2k.
 
 // Shared state of a pass-2 CTA.
+// After a moment record of unit u is stored by lane 0 of the calling warp: count
+// it in cnt_p2 and, if it completes the unit (nb records), merge the unit's
+// records into its layer statistics (s_t, s_k).  The selection kernel then
+// reads one record per layer instead of merging them in every CTA of the
+// request.  The merge is the function the selection used, on the same records
+// in the same order: the keep counts do not change.  One warp.
+__device__ __forceinline__ void unit_record_done(const Dev& p, const Ws& w, int u, int nb, int lane) {
+  int last = 0;
+  if (lane == 0) {
+    __threadfence();  // the record before its count
+    last = atomicAdd(w.cnt_p2 + u, 1u) == (unsigned)(nb - 1) ? 1 : 0;
+  }
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();  // (acquire) the unit's other records, counted by other CTAs
+  ff s_t, s_k;
+  layer_stats_warp(w.mom + (size_t)u * p.mom_slots * kMomWords, nb, lane, s_t, s_k);
+  if (lane == 0) w.lstat[u] = make_float4(s_t.hi, s_t.lo, s_k.hi, s_k.lo);
+}
+
 struct P2Smem {
   unsigned char* sm;  // stage area
   Ctl2p* c;           // ring and the moment hand-off
@@ -800,7 +821,9 @@ __device__ __forceinline__ void p2_moments(const Dev& p, const Ws& w, const P2Sm
     if (h.end) return;
     bool okv[2] = {mt < h.n, mt + kMomT < h.n};
     const Mom mb = block_moments<kMomT, 2>(xv, okv, (float)h.n, sh, S.red, S.redf, mt, kBarP2M);
-    if (mt == 0 && !warm) mom_store(w.mom + ((size_t)h.u * p.mom_slots + h.kb) * kMomWords, mb);
+    if (warm || mt >= 32) continue;
+    if (mt == 0) mom_store(w.mom + ((size_t)h.u * p.mom_slots + h.kb) * kMomWords, mb);
+    unit_record_done(p, w, h.u, h.nb, mt);
   }
 }
 
@@ -927,6 +950,7 @@ __device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, unsig
       h.kb = it.kb;
       h.n = min(kKeysP2, it.n_v - it.kb * kKeysP2);
       h.end = 0;
+      h.nb = (it.n_v + kKeysP2 - 1) / kKeysP2;
       if (!p2_hand_off(c, n_hand, h, 1, &v, &tid, &ok)) {
         if (tid == 0) set_error(w.error, AIRCACHE_ERR_DEVICE_TIMEOUT);
         return;
@@ -934,7 +958,7 @@ __device__ __forceinline__ void p2_single(const SArgs& a, const P2Smem& S, unsig
     }
   }
   P2Hand h;
-  h.u = h.kb = h.n = 0;
+  h.u = h.kb = h.n = h.nb = 0;
   h.end = 1;
   const bool no = false;
   const float zero = 0.f;
@@ -1203,7 +1227,10 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
     for (int i = 1; i < nsh; ++i) sh += shs[i];
     sh /= (float)nsh;
     const Mom mb = block_moments<kT2, 4>(xv, okv, (float)klim, sh, red, redf, tid, kBarT2);
-    if (tid == 0) mom_store(w.mom + ((size_t)u * p.mom_slots + tile) * kMomWords, mb);
+    if (warp == 0) {
+      if (tid == 0) mom_store(w.mom + ((size_t)u * p.mom_slots + tile) * kMomWords, mb);
+      unit_record_done(p, w, u, tv, lane);
+    }
   }
 }
 
