@@ -754,8 +754,9 @@ __device__ __forceinline__ int p2_find(const Dev& p, const Ws& w, int n, unsigne
 __device__ __forceinline__ void unit_record_done(const Dev& p, const Ws& w, int u, int nb, int lane) {
   int last = 0;
   if (lane == 0) {
-    __threadfence();  // the record before its count
-    last = atomicAdd(w.cnt_p2 + u, 1u) == (unsigned)(nb - 1) ? 1 : 0;
+    unsigned old;  // release: the record before its count
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;\n" : "=r"(old) : "l"(w.cnt_p2 + u) : "memory");
+    last = old == (unsigned)(nb - 1) ? 1 : 0;
   }
   last = __shfl_sync(0xffffffffu, last, 0);
   if (!last) return;
