@@ -204,14 +204,19 @@ def algorithmic_bytes(spec, n_tk, keep, esize):
     layer) formula 2*H_kv*D*(N_v+N_t) + 2*H_q*D*(1+N_tk) + 8*H_kv*D*(keep+N_t)
     (bf16; esize-scaled) + the I_v workspace.  bf16 units take the streaming
     path (pass 1 reads the unit's keys and elite query rows; pass 2, or pass 2k
-    when g * N_tk > 64, writes I_v; the selection kernel reads the moment records
-    back for the budget); other units the wide kernel."""
+    when g * N_tk > 64, writes I_v and the moment records, and the CTA that
+    completes a unit reads its records back and writes its layer statistics;
+    each selection CTA reads its request's layer statistics for the budget);
+    other units the wide kernel.  The first kernel zeroes the call's block of
+    counters."""
     row = spec.H_kv * spec.D * esize
     qrow = spec.H_q * spec.D * esize
     g = spec.H_q // spec.H_kv
-    k = {"elite_window": 0, "score_pass1": 0, "score_pass2": 0, "score_pass2k": 0, "score_wide": 0,
-         "budget_select": 0, "select_topk": 0, "gather_compact": 0}
-    path = 0
+    units = spec.L * spec.B
+    zero = 52 + 4 * (spec.B + 4 * units)  # the call's zeroed block
+    k = {"zero_block": zero, "elite_window": 0, "score_pass1": 0, "score_pass2": 0, "score_pass2k": 0,
+         "score_wide": 0, "budget_select": 0, "select_topk": 0, "gather_compact": 0}
+    path = zero
     for l in range(spec.L):
         for b, (nv, nt) in enumerate(unit_lengths(spec)):
             u = l * spec.B + b
@@ -220,10 +225,11 @@ def algorithmic_bytes(spec, n_tk, keep, esize):
             if esize == 2:
                 k["score_pass1"] += (nv + t) * row + t * qrow
                 # I_v written, plus one 48-byte moment record per key block
-                # (256 keys in pass 2, 128 in pass 2k), read back by the selection
+                # (256 keys in pass 2, 128 in pass 2k), written and read back
+                # once by the merge, and the unit's 16-byte layer statistics
                 recs = -(-nv // (256 if g * t <= 64 else 128))
-                k["score_pass2" if g * t <= 64 else "score_pass2k"] += 4 * nv + 48 * recs
-                k["budget_select"] += 48 * recs + 4 * nv + 4 * kp
+                k["score_pass2" if g * t <= 64 else "score_pass2k"] += 4 * nv + 96 * recs + 16
+                k["budget_select"] += 16 * spec.L + 4 * nv + 4 * kp
                 iv_passes = 2  # written, read by the selection
             else:
                 k["score_wide"] += (nv + t) * row + t * qrow + 4 * nv
@@ -231,7 +237,7 @@ def algorithmic_bytes(spec, n_tk, keep, esize):
                 k["select_topk"] += 4 * nv + 4 * kp
             k["gather_compact"] += 2 * 2 * (kp + nt) * row + 4 * kp
             path += ((nv + nt) * row + (1 + t) * qrow + 2 * 2 * (kp + nt) * row + 4 * nv * iv_passes
-                     + 96 * recs + 8 * kp)
+                     + 96 * recs + (16 + 16 * spec.L if recs else 0) + 8 * kp)
     return k, path
 
 

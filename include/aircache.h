@@ -278,7 +278,8 @@ AIRCACHE_API const char* aircache_status_string(int status);
  * Number of kernels one aircache_compress call on `p` launches (for launch
  * accounting), or -1 if `p` is invalid.  It depends on the scoring path, which
  * the problem alone decides: bf16 inputs whose per-layer key pointers are
- * evenly strided take the streaming path (7 kernels), others the wide path (4).
+ * evenly strided take the streaming path (7 kernels), others the wide path (5).
+ * The first kernel clears the call's block of counters and its error word.
  */
 AIRCACHE_API int aircache_compress_launches(const aircache_problem* p);
 
@@ -443,7 +444,8 @@ typedef struct aircache_decode_problem {
  * capacity is the length of row_index (too small: AIRCACHE_ERR_CAPACITY in
  * the workspace error word).  Decoding layer l over wl.k[l] with these rows
  * (aircache_decode with row_index) attends over the same rows as decoding the
- * compacted arena.  One memset and one kernel.
+ * compacted arena.  Two kernels: one clears the workspace's counters, one
+ * writes the rows.
  */
 AIRCACHE_API int aircache_row_index(const aircache_problem* p, const int32_t* keep, const int32_t* idx,
                                     const int64_t* out_offsets, void* ws, size_t ws_bytes, int32_t* row_index,

@@ -40,11 +40,12 @@ using namespace aircache;
 namespace {
 
 constexpr size_t kAlign = 256;
-// Kernels of one aircache_compress call, by scoring path.
-const char* const kStreamKernels[] = {"elite_window", "score_pass1",   "score_pass2",
+// Kernels of one aircache_compress call, by scoring path (the first clears the
+// call's zeroed block).
+const char* const kStreamKernels[] = {"zero_block",   "elite_window",  "score_pass1",   "score_pass2",
                                       "score_pass2k", "budget_select", "gather_compact"};
-const char* const kWideKernels[] = {"elite_window", "score_wide", "select_topk", "gather_compact"};
-constexpr int kStreamCount = 6, kWideCount = 4;
+const char* const kWideKernels[] = {"zero_block", "elite_window", "score_wide", "select_topk", "gather_compact"};
+constexpr int kStreamCount = 7, kWideCount = 5;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -433,8 +434,9 @@ static int compress_impl(const aircache_problem* p, void* ws, size_t ws_bytes, v
   const int sms = sm_count();
   StreamMaps maps;
   if (dn.stream_ok && !encode_stream_maps(dn, lp, w, &maps)) return AIRCACHE_ERR_CUDA;
-  if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
   int k = 0;
+  AC_TRY(mark(k++));
+  if ((rc = begin(w, s)) != AIRCACHE_OK) return rc;
   AC_TRY(mark(k++));
   AC_TRY(launch_elite(dn, lp, w, s));
   AC_TRY(mark(k++));

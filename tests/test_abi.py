@@ -72,6 +72,28 @@ def test_sizes_of_a_valid_problem(A):
     assert A.lib().aircache_compress_launches(ctypes.byref(p)) > 0
 
 
+def test_launch_count_and_kernel_names(A):
+    """The kernels one aircache_compress call launches, by scoring path: the
+    first clears the call's counters and error word (so aircache_compress_profile
+    times it too), then the elite step, the scoring, the selection and the
+    compaction."""
+    lib = A.lib()
+    stream = ["zero_block", "elite_window", "score_pass1", "score_pass2", "score_pass2k", "budget_select",
+              "gather_compact"]
+    wide = ["zero_block", "elite_window", "score_wide", "select_topk", "gather_compact"]
+    q = fake_problem(A, dtype=A.F32)  # fp32: the wide path
+    assert lib.aircache_compress_launches(ctypes.byref(q)) == len(wide)
+    assert [lib.aircache_kernel_name(ctypes.byref(q), i).decode() for i in range(len(wide))] == wide
+    assert lib.aircache_kernel_name(ctypes.byref(q), len(wide)) is None
+    # bf16 with evenly strided layers takes the streaming path where the driver
+    # can encode its key tensor map (a GPU host); here the wide path is allowed
+    p = fake_problem(A)
+    n = lib.aircache_compress_launches(ctypes.byref(p))
+    names = stream if n == len(stream) else wide
+    assert n == len(names)
+    assert [lib.aircache_kernel_name(ctypes.byref(p), i).decode() for i in range(n)] == names
+
+
 @pytest.mark.parametrize("field,value,code", [
     ("num_layers", 0, -1), ("num_layers", 257, -1), ("num_requests", 0, -1),
     ("h_q", 7, -1), ("h_kv", 0, -1), ("head_dim", 96, -2), ("head_dim", 0, -1),

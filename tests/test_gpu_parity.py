@@ -146,6 +146,16 @@ def test_full_size_sampled(A, oracle, name):
     print(name, "report", rep)
 
 
+def test_streaming_path_kernels(A):
+    """The 7b-shaped problem (bf16, evenly strided layers) takes the streaming
+    path: the zeroing kernel, the elite step, the three scoring passes, the
+    selection and the compaction."""
+    wl = W.make("7b", device="cuda", layers=2)
+    prob = make_problem(A, wl)
+    assert A.kernel_names(prob) == ["zero_block", "elite_window", "score_pass1", "score_pass2", "score_pass2k",
+                                    "budget_select", "gather_compact"]
+
+
 def test_deterministic(A):
     wl = W.make("7b", device="cuda", layers=4)
     prob = make_problem(A, wl)
