@@ -8,8 +8,9 @@
 // row offsets.  The wide scoring kernel computes the same quantities at its
 // tail with the same device functions.  A separate one-CTA kernel writes the
 // offsets for the staged compaction.  (On the streaming scoring path of the
-// fused call the selection kernel derives the budgets itself, from the key-block
-// moment records of passes 2 and 2k: select.cu.)
+// fused call passes 2 and 2k merge each unit's key-block moment records into
+// its statistics, and the selection kernel derives the budgets from them:
+// stream.cu, select.cu.)
 #include <cstring>
 #include <mutex>
 #include <vector>

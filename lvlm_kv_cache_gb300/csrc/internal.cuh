@@ -69,7 +69,8 @@ struct Ws {
   uint32_t* cnt_req;     // [B]   layers of a request whose stats are done
   uint32_t* p2claim;     // [L*B] claimed pass-2 work items per (layer, request)
   uint32_t* cnt_p1;      // [L*B] finished pass-1 items per (layer, request)
-  uint32_t* cnt_p2;      // [L*B] finished pass-2 items per (layer, request)
+  uint32_t* cnt_p2;      // [L*B] finished pass-2 items per (layer, request) (wide path); moment
+                         //       records stored per unit (streaming path)
   uint32_t* lse_ready;   // [L*B] row log-sum-exps published
   int32_t* elite;        // [L*B*max_text]
   int32_t* n_tk;         // [L*B]

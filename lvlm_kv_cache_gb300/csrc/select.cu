@@ -18,13 +18,14 @@
 // Integer work only: the result is exact and deterministic.
 //
 // On the streaming path of the fused call the kernel also takes the layer
-// budget ("Key design 2") off the critical path of a kernel of its own: while
-// its keys are staged, warp w merges the key-block moment records of layers w,
-// w + 32, ... of its request into (s_t, s_k) (float-float, the same arithmetic
-// in every CTA of the request), warp 0 turns them into the request's keep
-// counts, and the CTA keeps its own layer's count.  The compacted-cache row
-// offsets then come from the compaction kernel (or, for more units than it
-// stages, from the last CTA of this one to arrive).
+// budget ("Key design 2") off the critical path of a kernel of its own.
+// Passes 2 and 2k have already merged each unit's key-block moment records
+// into its layer statistics (s_t, s_k) (float-float).  While its keys are
+// staged, the CTA reads the statistics of every layer of its request, warp 0
+// turns them into the request's keep counts (the same arithmetic in every CTA
+// of the request), and the CTA keeps its own layer's count.  The
+// compacted-cache row offsets then come from the compaction kernel (or, for
+// more units than it stages, from the last CTA of this one to arrive).
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "reduce.cuh"
@@ -44,8 +45,8 @@ struct SelectArgs {
   Ws w;
   int smem_keys;          // capacity of the dynamic shared-memory key buffer
   int budget;             // 1 (streaming path): the CTA first computes its request's layer budgets
-                          // from the moment records of passes 2 / 2k and writes its own layer's
-                          // keep count and statistics
+                          // from the layer statistics that passes 2 / 2k merged, and writes its own
+                          // layer's keep count and statistics
   int64_t out_capacity;   // rows of the output arena (budget mode)
   int offsets;            // budget mode: the last CTA writes the row offsets (else the compaction does)
 };

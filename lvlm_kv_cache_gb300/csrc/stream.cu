@@ -12,8 +12,9 @@
 //
 // Pass 1 (score_pass1, persistent, one CTA per SM).  A work item is (unit, KV
 // head, chunk of four 128-key visual tiles) or (unit, KV head, the elite text
-// keys); it runs once per row chunk of the unit.  A producer thread claims
-// items from an atomic counter and moves each key tile into a shared-memory
+// keys); it runs once per row chunk of the unit.  A producer thread takes the
+// CTA's index as its first item, claims the rest from an atomic counter, and
+// moves each key tile into a shared-memory
 // ring with one TMA tensor copy per 128-byte column slab; the row chunk's
 // queries come with its first tile.  One thread issues the logit tiles on the
 // tensor cores (tcgen05: D[key][row] = K[key] . Q[row], M = 128 keys, N = 32
@@ -41,8 +42,11 @@
 // small TMA ring; per-key sums of exp2(logit - lse) over every row give the
 // tile's I_v directly.
 //
-// The per-layer statistics, budgets and offsets follow in a kernel of their own
-// (budget.cu), one CTA per unit.
+// Passes 2 and 2k also reduce each key block's I_v to a moment record (256
+// keys in pass 2, a 128-key tile in pass 2k) and count the records per unit.
+// The CTA whose record completes a unit merges the unit's records into its
+// layer statistics (s_t, s_k).  The budgets and the selection follow in the
+// selection kernel (select.cu), the row offsets in the compaction.
 #include <cstring>
 
 #include "internal.cuh"
@@ -1219,7 +1223,7 @@ __global__ void __launch_bounds__(kT2, 1) stream_p2k_kernel(const __grid_constan
         okv[2 * nt + e] = g4 == 0 && key < klim;
         if (okv[2 * nt + e]) iv[(long long)tile * kTK + key] = xv[2 * nt + e];
       }
-    // this tile's moments, for the statistics kernel; shift: the mean of the
+    // this tile's moments, for the unit's layer statistics; shift: the mean of the
     // tile's values at keys 0, 32, 64, 96 that exist (warps 0, 2, 4, 6, lane 0)
     if ((warp & 1) == 0 && lane == 0) shs[warp >> 1] = okv[0] ? xv[0] : 0.f;
     named_bar_sync(kBarT2, kT2);
