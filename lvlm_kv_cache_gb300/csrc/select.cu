@@ -116,26 +116,38 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   const float* x = (p.head_sets ? w.ivh : w.iv) + set * p.total_visual + R.vis0;
   int32_t* out = w.idx + set * p.total_visual + R.vis0;
   const bool staged = n <= a.smem_keys;
-  if (a.budget && ok_req) {
-    // (s_t, s_k) of every layer of the request, merged from the unit's moment
-    // records by the pass-2 (or pass-2k) CTA that wrote its last one
-    for (int ll = tid; ll < p.L; ll += kSelThreads) {
+  if (a.budget && ok_req && warp == 0) {
+    // warp 0: the request's keep counts, while the other warps stage the keys.
+    // (s_t, s_k) of every layer of the request were merged from the unit's
+    // moment records by the pass-2 (or pass-2k) CTA that wrote its last one.
+    for (int ll = lane; ll < p.L; ll += 32) {
       const float4 v = __ldcg(&w.lstat[ll * p.B + b]);
       st_s[ll] = ff{v.x, v.y};
       sk_s[ll] = ff{v.z, v.w};
     }
+    __syncwarp();
+    request_budget_warp_put(
+        p, R.n_v,
+        [&](int ll, ff& st, ff& sk) {
+          st = st_s[ll];
+          sk = sk_s[ll];
+        },
+        [&](int ll, int32_t kk) { keep_s[ll] = kk; }, lane);
   }
-  // stage the keys (when they fit) and find the smallest and largest
+  // stage the keys (when they fit) and find the smallest and largest (in
+  // budget mode warp 0 takes no part)
+  const int sw = a.budget ? 1 : 0;                  // warps left out of the staging
+  const int st0 = tid - 32 * sw, nst = kSelThreads - 32 * sw;
   uint32_t kmin = 0xffffffffu, kmax = 0u;
-  for (int i0 = tid; i0 < n; i0 += 8 * kSelThreads) {
+  for (int i0 = st0; st0 >= 0 && i0 < n; i0 += 8 * nst) {
     float v[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = (i0 + q * kSelThreads < n) ? __ldcg(x + i0 + q * kSelThreads) : 0.f;
+    for (int q = 0; q < 8; ++q) v[q] = (i0 + q * nst < n) ? __ldcg(x + i0 + q * nst) : 0.f;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      if (i0 + q * kSelThreads < n) {
+      if (i0 + q * nst < n) {
         const uint32_t key = order_key(v[q]);
-        if (staged) keys_s[i0 + q * kSelThreads] = key;
+        if (staged) keys_s[i0 + q * nst] = key;
         kmin = min(kmin, key);
         kmax = max(kmax, key);
       }
@@ -177,17 +189,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   }
   int k;
   if (a.budget) {
-    __syncthreads();  // every layer's statistics are in shared memory
-    if (warp == 0) {
-      request_budget_warp_put(
-          p, R.n_v,
-          [&](int ll, ff& st, ff& sk) {
-            st = st_s[ll];
-            sk = sk_s[ll];
-          },
-          [&](int ll, int32_t kk) { keep_s[ll] = kk; }, lane);
-    }
-    __syncthreads();
+    // warp 0's keep counts: published by the barriers of the key staging above
     k = keep_s[l];
     if (hs == 0) {
       // this layer's keep count and statistics; unless the compaction forms
