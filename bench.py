@@ -414,8 +414,9 @@ def run_decode(args, local):
             q_bytes = comp_rows * kv_row_bytes * 3 // 2 + 2 * L * B * H_kv * 4  # bf16 read + int8 written
             q8_probs = [A.DecodeProblem(qdec[l], k8, v8, row_begin=offs[l * B:(l + 1) * B],
                                         row_end=offs[l * B + 1:(l + 1) * B + 1], max_rows=longest,
-                                        k_scale=ks[l * B:(l + 1) * B], v_scale=vs[l * B:(l + 1) * B])
-                        for l in range(L)]  # plain launches: the early start measured slower for int8 rows
+                                        k_scale=ks[l * B:(l + 1) * B], v_scale=vs[l * B:(l + 1) * B],
+                                        early_cache=True)
+                        for l in range(L)]
             need8 = max(p.workspace_size() for p in q8_probs)  # the int8 launch plan may split differently
             ws_8 = ws_c if ws_c.numel() >= need8 else torch.zeros(need8, dtype=torch.uint8, device=dev)
             q8_ms = timed(q8_probs, ws_8)

@@ -152,6 +152,29 @@ def test_decode_from_int8_extreme_query_magnitudes(A, oracle, q_scale, d):
     decode_int8_check(A, oracle, di, 1000)
 
 
+def test_decode_from_int8_early_cache_matches_plain_launches(A, oracle):
+    # int8 rows with programmatic dependent launch (the codes are not written by
+    # the kernel before each call; the queries are): the same bits as plain
+    # launches
+    di = W.decode_inputs([700, 33, 4100, 5], 28, 4, 128, seed=28, device="cuda", q_scale=2.0, new_row=True)
+    k8, v8, ks, vs = A.quantize_int8(di.k, di.v, di.offsets)
+    outs = {}
+    for early in (False, True):
+        ws = torch.zeros(1 << 22, dtype=torch.uint8, device="cuda")
+        res = []
+        for m in (0, 1000, 10 ** 6):
+            q = torch.empty_like(di.q)
+            q.copy_(di.q)  # written by the kernel right before the decode kernel
+            p = A.DecodeProblem(q, k8, v8, offsets=di.offsets, max_rows=m, k_new=di.k_new, v_new=di.v_new,
+                                k_scale=ks, v_scale=vs, early_cache=early)
+            A.aircache_decode(p, ws)
+            res.append(p.out)
+        assert A.aircache_get_error(ws) == A.OK
+        outs[early] = [r.clone() for r in res]
+    for a, b in zip(outs[False], outs[True]):
+        assert torch.equal(a, b)
+
+
 def test_decode_from_int8_rows_past_a_range(A, oracle):
     # the codes after the last range are garbage for this call: never mixed in
     di = W.decode_inputs([40, 77], 8, 2, 128, seed=25, device="cuda")
