@@ -185,9 +185,9 @@ __global__ void __launch_bounds__(kBulkThreads) compact_bulk_kernel(const __grid
   }
   const int esize = (p.dtype == AIRCACHE_BF16) ? 2 : 4;
   const uint32_t row_bytes = (uint32_t)(p.h_kv * p.d * esize);
-  // rows per chunk: as many as a buffer holds, then evened out so that every
-  // CTA gets the same number of chunks (to one) and no CTA is left with a
-  // whole chunk more than most
+  // rows per chunk: at most what a buffer holds, evened out so that the rows
+  // split into a whole number of equal rounds of chunks over the grid (the
+  // last chunks are then as long as the others)
   const int Rmax = min(kBulkMaxRows, (int)(kBulkBuf / 2 / row_bytes));
   const long long per_cta = (total + (long long)gridDim.x * Rmax - 1) / ((long long)gridDim.x * Rmax);
   const int R = per_cta > 0 ? (int)((total + gridDim.x * per_cta - 1) / (gridDim.x * per_cta)) : Rmax;
